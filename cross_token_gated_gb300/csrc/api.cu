@@ -1,0 +1,273 @@
+// C ABI of the gate-aggregation library: argument validation, workspace layout,
+// dispatch to the kernels, and the per-device error word.  See include/tango.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "tango.h"
+#include "tg_kernels.h"
+#include "tg_common.cuh"
+#include "tg_tc.h"
+
+namespace tg {
+
+__device__ unsigned g_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+
+// Device address of this device's error word (looked up once per device).
+cudaError_t error_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+size_t elem_size(tg_dtype dt) { return dt == TG_F32 ? 4 : 2; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tg_status validate_agg(const tg_agg_params* p, bool wango) {
+  if (!p) return TG_ERR_INVALID_ARG;
+  if (p->B < 1 || p->T < 1 || p->H < 1 || p->H > TG_MAX_HEADS || p->d_qk < 1 || p->m < 1)
+    return TG_ERR_INVALID_ARG;
+  if (p->d_qk % p->H != 0 || p->m % p->H != 0) return TG_ERR_INVALID_ARG;
+  if (p->dtype != TG_F32 && p->dtype != TG_BF16) return TG_ERR_INVALID_ARG;
+  if (!p->tau && !(p->s >= 0.f && p->s <= 20.f)) return TG_ERR_INVALID_ARG;
+  if (wango && p->window < 1) return TG_ERR_INVALID_ARG;
+  if (wango && p->phi_mode != 0 && p->phi_mode != 1) return TG_ERR_INVALID_ARG;
+  if (p->flags & ~(TG_FLAG_QK_NORMALIZED | TG_FLAG_DEBUG_TIMEOUT)) return TG_ERR_INVALID_ARG;
+  const int d_h = p->d_qk / p->H;
+  if (d_h > 128) return TG_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->T > (1LL << 31) - 1) return TG_ERR_UNSUPPORTED;
+  if (p->dtype == TG_BF16) {
+    if (d_h != 16 && d_h != 32 && d_h != 64) return TG_ERR_UNSUPPORTED;
+    if ((p->m / p->H) % 8 != 0) return TG_ERR_UNSUPPORTED;
+  }
+  return TG_OK;
+}
+
+size_t agg_ws_bytes(const tg_agg_params* p) {
+  if (p->flags & TG_FLAG_QK_NORMALIZED) return 0;
+  const size_t qk = (size_t)p->B * p->T * p->d_qk * elem_size(p->dtype);
+  return 2 * align256(qk);
+}
+
+struct BlockWs {
+  size_t x, q, k, g, v, total;
+};
+
+BlockWs block_ws_layout(const tg_block_params* p) {
+  const tg_agg_params& a = p->agg;
+  const size_t es = elem_size(a.dtype), BT = (size_t)a.B * a.T;
+  BlockWs w;
+  w.x = 0;
+  w.q = w.x + align256(BT * p->d * es);
+  w.k = w.q + align256(BT * a.d_qk * es);
+  w.g = w.k + align256(BT * a.d_qk * es);
+  w.v = w.g + align256(BT * a.m * es);
+  w.total = w.v + align256(BT * a.m * es);
+  return w;
+}
+
+tg_status validate_block(const tg_block_params* p) {
+  if (!p) return TG_ERR_INVALID_ARG;
+  tg_status st = validate_agg(&p->agg, p->mode == TG_MODE_WANGO);
+  if (st != TG_OK) return st;
+  if (p->agg.flags != 0) return TG_ERR_INVALID_ARG;
+  if (p->d < 1 || !(p->rms_eps > 0.f) || !(p->rope_base >= 0.f)) return TG_ERR_INVALID_ARG;
+  if (p->mode != TG_MODE_TANGO && p->mode != TG_MODE_WANGO) return TG_ERR_INVALID_ARG;
+  if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
+  if (p->agg.dtype == TG_BF16 && p->d % 64 != 0) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+tg_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return TG_OK;
+  if (!ws || ws_bytes < need) return TG_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return TG_ERR_WORKSPACE;
+  return TG_OK;
+}
+
+tg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TG_OK : TG_ERR_CUDA; }
+
+// Shared body of tango_aggregate / wango_aggregate.
+tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
+                    const void* v, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  tg_status st = validate_agg(p, wango);
+  if (st != TG_OK) return st;
+  if (!q || !k || !g || !out) return TG_ERR_INVALID_ARG;
+  if (p->dtype == TG_BF16 && !(aligned16(q) && aligned16(k) && aligned16(g) && aligned16(out) &&
+                               (!v || aligned16(v))))
+    return TG_ERR_UNSUPPORTED;
+  const size_t need = agg_ws_bytes(p);
+  st = check_ws(ws, ws_bytes, need);
+  if (st != TG_OK) return st;
+
+  AggArgs a;
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = p->m;
+  a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
+  a.window = p->window; a.phi_mode = p->phi_mode; a.flags = p->flags; a.dtype = p->dtype;
+  a.g = g; a.v = v; a.out = out;
+  cudaError_t e = error_word(&a.err);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  if (p->flags & TG_FLAG_QK_NORMALIZED) {
+    a.q = q;
+    a.k = k;
+  } else {
+    const long long rows = (long long)p->B * p->T;
+    char* base = static_cast<char*>(ws);
+    void* qn = base;
+    void* kn = base + need / 2;
+    e = launch_qk_prep(p->dtype, q, qn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
+    if (e == cudaSuccess) e = launch_qk_prep(p->dtype, k, kn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    a.q = qn;
+    a.k = kn;
+  }
+  if (p->dtype == TG_F32) return cuda_status(wango ? launch_wango_simt(a, stream) : launch_tango_simt(a, stream));
+  return cuda_status(wango ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream));
+}
+
+}  // namespace
+}  // namespace tg
+
+using namespace tg;
+
+extern "C" {
+
+tg_status tango_aggregate(const tg_agg_params* p, const void* q, const void* k, const void* g, const void* v,
+                          void* out, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  return aggregate(false, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status wango_aggregate(const tg_agg_params* p, const void* q, const void* k, const void* g, const void* v,
+                          void* out, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  return aggregate(true, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* w, const void* h, void* h_out,
+                              void* ws, size_t ws_bytes, tg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  tg_status st = validate_block(p);
+  if (st != TG_OK) return st;
+  if (!w || !w->rms_gamma || !w->Wq || !w->Wk || !w->Wg || !w->Wv || !w->Wo || !h || !h_out)
+    return TG_ERR_INVALID_ARG;
+  const tg_agg_params& ap = p->agg;
+  if (ap.dtype == TG_BF16) {
+    const void* ptrs[] = {w->rms_gamma, w->Wq, w->Wk, w->Wg, w->Wv, w->Wo, h, h_out};
+    for (const void* x : ptrs)
+      if (!aligned16(x)) return TG_ERR_UNSUPPORTED;
+  }
+  const BlockWs L = block_ws_layout(p);
+  st = check_ws(ws, ws_bytes, L.total);
+  if (st != TG_OK) return st;
+  char* base = static_cast<char*>(ws);
+  void *x = base + L.x, *qb = base + L.q, *kb = base + L.k, *gb = base + L.g, *vb = base + L.v;
+  const long long BT = (long long)ap.B * ap.T;
+  const int M = (int)BT, d = p->d;
+
+  AggArgs a;
+  a.B = ap.B; a.T = ap.T; a.H = ap.H; a.dqk = ap.d_qk; a.m = ap.m;
+  a.s = ap.s; a.tau = ap.tau; a.null_bias = ap.null_bias;
+  a.window = ap.window; a.phi_mode = ap.phi_mode; a.flags = 0; a.dtype = ap.dtype;
+  a.q = qb; a.k = kb; a.g = gb; a.v = vb; a.out = vb;  // gbar * v overwrites v in place
+  cudaError_t e = error_word(&a.err);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+
+  // eq. 2 and sec. 2.1: x = RMSNorm(h); q, k, g = SiLU(.), v.
+  e = launch_rmsnorm(ap.dtype, h, w->rms_gamma, x, BT, d, p->rms_eps, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  if (ap.dtype == TG_F32) {
+    e = launch_gemm_simt(ap.dtype, x, w->Wq, qb, nullptr, M, ap.d_qk, d, ap.d_qk, kEpiStore, stream);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt(ap.dtype, x, w->Wk, kb, nullptr, M, ap.d_qk, d, ap.d_qk, kEpiStore, stream);
+    if (e == cudaSuccess)
+      e = launch_qk_prep(ap.dtype, qb, qb, BT, ap.T, ap.H, ap.d_qk, p->rope_base, true, stream);
+    if (e == cudaSuccess)
+      e = launch_qk_prep(ap.dtype, kb, kb, BT, ap.T, ap.H, ap.d_qk, p->rope_base, true, stream);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt(ap.dtype, x, w->Wg, gb, nullptr, M, ap.m, d, ap.m, kEpiSilu, stream);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt(ap.dtype, x, w->Wv, vb, nullptr, M, ap.m, d, ap.m, kEpiStore, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    // eqs. 5-10
+    e = p->mode == TG_MODE_WANGO ? launch_wango_simt(a, stream) : launch_tango_simt(a, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    // eq. 3: h_out = h + W_o u
+    e = launch_gemm_simt(ap.dtype, vb, w->Wo, h_out, h, M, d, ap.m, d, kEpiResidual, stream);
+    return cuda_status(e);
+  }
+  ProjArgs pa;
+  pa.x = x; pa.Wq = w->Wq; pa.Wk = w->Wk; pa.Wg = w->Wg; pa.Wv = w->Wv;
+  pa.q = qb; pa.k = kb; pa.g = gb; pa.v = vb;
+  pa.M = M; pa.d = d; pa.T = ap.T; pa.H = ap.H; pa.dqk = ap.d_qk; pa.m = ap.m;
+  pa.rope_base = p->rope_base; pa.err = a.err;
+  e = launch_proj_tc(pa, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  e = p->mode == TG_MODE_WANGO ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  e = launch_out_tc(vb, w->Wo, h, h_out, M, d, ap.m, a.err, stream);
+  return cuda_status(e);
+}
+
+size_t tg_workspace_size(int which, const void* params) {
+  if (!params) return 0;
+  if (which == TG_WS_TANGO || which == TG_WS_WANGO) {
+    const tg_agg_params* p = static_cast<const tg_agg_params*>(params);
+    if (validate_agg(p, which == TG_WS_WANGO) != TG_OK) return 0;
+    return agg_ws_bytes(p);
+  }
+  if (which == TG_WS_BLOCK) {
+    const tg_block_params* p = static_cast<const tg_block_params*>(params);
+    if (validate_block(p) != TG_OK) return 0;
+    return block_ws_layout(p).total;
+  }
+  return 0;
+}
+
+const char* tg_status_string(tg_status s) {
+  switch (s) {
+    case TG_OK: return "ok";
+    case TG_ERR_INVALID_ARG: return "invalid argument";
+    case TG_ERR_UNSUPPORTED: return "unsupported shape, alignment or dtype";
+    case TG_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case TG_ERR_CUDA: return "CUDA call failed";
+    case TG_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case TG_ERR_DEVICE: return "out-of-range value in device memory";
+  }
+  return "unknown status";
+}
+
+tg_status tg_check_device_error(tg_stream_t stream, unsigned* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TG_ERR_CUDA;
+  unsigned* dev = nullptr;
+  if (error_word(&dev) != cudaSuccess) return TG_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return TG_ERR_CUDA;
+  if (word != 0 && cudaMemset(dev, 0, sizeof word) != cudaSuccess) return TG_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word & kErrTimeout) return TG_ERR_TIMEOUT;
+  if (word & kErrValue) return TG_ERR_DEVICE;
+  return TG_OK;
+}
+
+int tg_version(void) { return 100; }
+
+}  // extern "C"

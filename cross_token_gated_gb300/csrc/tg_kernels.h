@@ -1,0 +1,45 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tango.h"
+
+namespace tg {
+
+// Arguments of one aggregation launch.  q/k are unit-normalised per head.
+struct AggArgs {
+  int B, T, H, dqk, m;
+  float s;
+  const float* tau;
+  const float* null_bias;
+  int window;  // WANGO only
+  int phi_mode;
+  unsigned flags;
+  tg_dtype dtype;
+  const void* q;
+  const void* k;
+  const void* g;
+  const void* v;  // may be NULL
+  void* out;
+  unsigned* err;  // device error word
+};
+
+enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
+
+// ---- CUDA-core kernels (simt.cu) -------------------------------------------
+// Per (row, head): optional RoPE at position row % T, then optional unit
+// normalisation.  in may equal out.
+cudaError_t launch_qk_prep(tg_dtype dt, const void* in, void* out, long long rows, int T, int H, int dqk,
+                           float rope_base, bool normalize, cudaStream_t s);
+// x = gamma * h / sqrt(mean(h^2) + eps), per row of width d.
+cudaError_t launch_rmsnorm(tg_dtype dt, const void* h, const void* gamma, void* x, long long rows, int d,
+                           float eps, cudaStream_t s);
+// C[M, N] (row pitch ldc) = epi(A[M, K] * B[N, K]^T), fp32 accumulation.
+cudaError_t launch_gemm_simt(tg_dtype dt, const void* A, const void* B, void* C, const void* R, int M, int N,
+                             int K, int ldc, int epi, cudaStream_t s);
+cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
+cudaError_t launch_wango_simt(const AggArgs& a, cudaStream_t s);
+
+}  // namespace tg

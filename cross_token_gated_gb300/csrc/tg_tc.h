@@ -1,0 +1,26 @@
+// Internal launchers of the tensor-core (tcgen05) kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "tg_kernels.h"
+
+namespace tg {
+
+// Projection GEMM of one block: x [M, d] against W_q, W_k [dqk, d] and W_g, W_v
+// [m, d]; epilogues: RoPE + unit norm per head (q, k), SiLU (g), identity (v).
+struct ProjArgs {
+  const void *x, *Wq, *Wk, *Wg, *Wv;
+  void *q, *k, *g, *v;
+  int M, d, T, H, dqk, m;
+  float rope_base;
+  unsigned* err;
+};
+
+cudaError_t launch_proj_tc(const ProjArgs& a, cudaStream_t s);
+// h_out [M, d] = h + u [M, m] * Wo [d, m]^T
+cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_out, int M, int d, int m,
+                          unsigned* err, cudaStream_t s);
+cudaError_t launch_tango_tc(const AggArgs& a, cudaStream_t s);
+cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
+
+}  // namespace tg

@@ -1,0 +1,184 @@
+/*
+ * tango.h -- C ABI of the GB300 (sm_103a) cross-token gate aggregation library.
+ *
+ * Operations defined by "TANGO: Token-Aggregated Nonlinear Gating Operators for
+ * Natural and Formal Language Modeling" (arXiv 2608.22117):
+ *   - tango_aggregate      sec. 2.1 eq. 5 with the full-prefix weights of sec. 2.2 eq. 6
+ *   - wango_aggregate      sec. 2.1 eq. 5 with the windowed weights of sec. 2.2 eqs. 7-10
+ *   - tango_block_forward  one block application, sec. 2.1 eqs. 2-3 around either of the above
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument named as "device" is a CUDA device pointer owned by the
+ *     caller.  The library never allocates, frees or synchronises; scratch memory is
+ *     passed in as a workspace whose size tg_workspace_size() reports.
+ *   - Tensors are row-major and contiguous.  q, k: [B, T, d_qk]; g, v, out: [B, T, m];
+ *     h: [B, T, d]; weights are [out_features, in_features].  Head a owns columns
+ *     [a*d_qk/H, (a+1)*d_qk/H) of q/k and [a*m/H, (a+1)*m/H) of g/v/out.
+ *   - All tensors of one call share one storage type (tg_dtype).  Accumulation is
+ *     always fp32.  TG_BF16 runs on the tensor cores (tcgen05); TG_F32 runs on the
+ *     CUDA cores in full fp32 (no TF32).
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns an error status and launches nothing.  A failed launch
+ *     returns TG_ERR_CUDA.  Errors found on the device (a bounded wait that ran out,
+ *     a temperature outside [0, 20]) are recorded in a per-device error word that
+ *     tg_check_device_error() reads and clears.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Calls are thread-safe with respect to each other; concurrent calls that share
+ *     a workspace race.
+ */
+#ifndef TANGO_GB300_H
+#define TANGO_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tg_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, inconsistent shape */
+    TG_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. bf16 head width not in {16,32,64}) */
+    TG_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or smaller than required */
+    TG_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+    TG_ERR_TIMEOUT = 5,     /* (device) a bounded wait inside a kernel ran out */
+    TG_ERR_DEVICE = 6       /* (device) an out-of-range value was seen in device memory */
+} tg_status;
+
+typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
+
+/* tg_agg_params.flags */
+#define TG_FLAG_QK_NORMALIZED 0x1u  /* q and k are already unit vectors per head */
+#define TG_FLAG_DEBUG_TIMEOUT 0x100u /* test hook: bf16 kernels wait on a barrier that is
+                                        never signalled, with a ~1 ms limit, and return
+                                        TG_ERR_TIMEOUT through tg_check_device_error() */
+
+/* tango_block_forward mode */
+#define TG_MODE_TANGO 0
+#define TG_MODE_WANGO 1
+
+/* tg_workspace_size() selector */
+#define TG_WS_TANGO 0 /* params: const tg_agg_params*   */
+#define TG_WS_WANGO 1 /* params: const tg_agg_params*   */
+#define TG_WS_BLOCK 2 /* params: const tg_block_params* */
+
+#define TG_MAX_HEADS 64
+
+/*
+ * Parameters of one aggregation (eq. 5).
+ *   B, T       batch and sequence length (>= 1)
+ *   H          heads (1..TG_MAX_HEADS); d_qk % H == 0 and m % H == 0
+ *   d_qk       total query/key width (d_h = d_qk / H per head)
+ *   m          total gate width F (m_h = m / H per head)
+ *   s          temperature tau used for every head when tau == NULL; 0 <= s <= 20
+ *              (eq. 4 caps tau at 20)
+ *   tau        device float[H] of per-head temperatures, or NULL.  Values outside
+ *              [0, 20] are clamped and flagged as TG_ERR_DEVICE.
+ *   null_bias  device float[H] of null-gate biases b_a, or NULL for no null gate
+ *              (eq. 5: weight n_i exp(b_a), n_i = i + 1, in the denominator only)
+ *   window     WANGO window W >= 1, counting the destination itself (eq. 7);
+ *              ignored by tango_aggregate
+ *   phi_mode   WANGO feature map: 0 = eq. 8 (max(ELU(u)+1+1e-4, 1e-4)/sqrt(d_h)),
+ *              1 = plain ELU(u) + 1
+ *   flags      TG_FLAG_*
+ *   dtype      storage type of q, k, g, v, out
+ * bf16 requirements: d_h in {16, 32, 64}, m_h % 8 == 0, all tensor base
+ * addresses 16-byte aligned (else TG_ERR_UNSUPPORTED).
+ */
+typedef struct {
+    int B, T, H, d_qk, m;
+    float s;
+    const float *tau;
+    const float *null_bias;
+    int window;
+    int phi_mode;
+    unsigned flags;
+    tg_dtype dtype;
+} tg_agg_params;
+
+/*
+ * Full-prefix aggregation (sec. 2.2 eq. 6 in sec. 2.1 eq. 5):
+ *   out[b,i,a-cols] = gbar_ia * v[b,i,a-cols],
+ *   gbar_ia = sum_{j<=i} e^{l_ija} g_ja / (sum_{j<=i} e^{l_ija} + (i+1) e^{b_a}),
+ *   l_ija = tau_a qhat_ia . khat_ja (unit-normalised unless TG_FLAG_QK_NORMALIZED).
+ * q, k, g: device, read only.  v: device, or NULL (then out = gbar).  out: device,
+ * written; may alias v, must not overlap q, k or g.  ws: device scratch of at least
+ * tg_workspace_size(TG_WS_TANGO, p) bytes (256-byte aligned; may be NULL if 0).
+ */
+tg_status tango_aggregate(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                          const void *v, void *out, void *ws, size_t ws_bytes,
+                          tg_stream_t stream);
+
+/*
+ * Windowed aggregation (sec. 2.2 eqs. 7-10): sources i-W < j <= i get e^{l_ija};
+ * older sources j <= i-W get phi(sqrt(tau_a) qhat_ia) . phi(sqrt(tau_a) khat_ja),
+ * evaluated through the running sums S = sum phi(k~) g^T, z = sum phi(k~); one joint
+ * numerator and denominator (with the null term) per destination.  Arguments as for
+ * tango_aggregate; the workspace is sized by tg_workspace_size(TG_WS_WANGO, p).
+ */
+tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                          const void *v, void *out, void *ws, size_t ws_bytes,
+                          tg_stream_t stream);
+
+/* Weights of one block, all of the block's dtype, row-major [out, in]. */
+typedef struct {
+    const void *rms_gamma; /* [d]      RMSNorm gain                           */
+    const void *Wq;        /* [d_qk, d]                                        */
+    const void *Wk;        /* [d_qk, d]                                        */
+    const void *Wg;        /* [m, d]   gate projection (SiLU applied, eq. 2)   */
+    const void *Wv;        /* [m, d]   feature projection (eq. 2)              */
+    const void *Wo;        /* [d, m]   output projection (eq. 3)               */
+} tg_block_weights;
+
+/*
+ * Block parameters: agg gives B, T, H, d_qk, m, s/tau, null_bias, window, phi_mode,
+ * dtype (agg.flags must be 0).  d: residual width.  mode: TG_MODE_TANGO or
+ * TG_MODE_WANGO.  rms_eps: RMSNorm epsilon (> 0).  rope_base: RoPE base (0 = no
+ * RoPE); rotate-half pairing (c, c + d_h/2), positions 0..T-1 per sequence.
+ */
+typedef struct {
+    tg_agg_params agg;
+    int d;
+    int mode;
+    float rms_eps;
+    float rope_base;
+} tg_block_params;
+
+/*
+ * One block application (sec. 2.1 eqs. 2-3):
+ *   x = RMSNorm(h); q, k = RoPE(W_q x), RoPE(W_k x), unit-normalised per head;
+ *   g = SiLU(W_g x); v = W_v x; gbar by TANGO or WANGO; h_out = h + W_o (gbar * v).
+ * h: device [B, T, d], read.  h_out: device [B, T, d], written; may alias h.
+ * ws: device scratch of at least tg_workspace_size(TG_WS_BLOCK, p) bytes, 256-byte
+ * aligned; it holds x, q, k, g and v (v is overwritten by gbar * v).
+ */
+tg_status tango_block_forward(const tg_block_params *p, const tg_block_weights *w,
+                              const void *h, void *h_out, void *ws, size_t ws_bytes,
+                              tg_stream_t stream);
+
+/* Workspace bytes needed by the call `which` (TG_WS_*) with `params`; 0 for invalid
+ * parameters (validate with the call itself to get the reason). */
+size_t tg_workspace_size(int which, const void *params);
+
+/* Static, NUL-terminated description of a status. */
+const char *tg_status_string(tg_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns TG_OK, TG_ERR_TIMEOUT or TG_ERR_DEVICE (the first kind recorded), or
+ * TG_ERR_CUDA if the synchronisation itself failed.  If `detail` is not NULL it
+ * receives the raw word (bit 0: timeout, bit 1: value out of range; bits 8..15:
+ * the kernel that recorded it, 1 = TANGO, 2 = WANGO, 3 = GEMM).
+ */
+tg_status tg_check_device_error(tg_stream_t stream, unsigned *detail);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TANGO_GB300_H */

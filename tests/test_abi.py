@@ -1,0 +1,113 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+function include/tango.h declares, and rejects bad arguments before launching."""
+import ctypes
+
+import pytest
+
+import cross_token_gated_gb300 as tg
+
+
+def test_exports_every_declared_function(lib):
+    names = tg.declared_functions()
+    assert {"tango_aggregate", "wango_aggregate", "tango_block_forward", "tg_workspace_size",
+            "tg_status_string", "tg_check_device_error", "tg_version"} <= set(names)
+    raw = tg.load()
+    for n in names:
+        assert hasattr(raw, n), f"library does not export {n}"
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert tg.status_string(st)
+    assert tg.status_string(99) == "unknown status"
+    assert tg.tg_version() >= 100
+
+
+def _agg(**kw):
+    base = dict(B=2, T=64, H=2, d_qk=128, m=256, dtype=tg.TG_BF16, s=10.0, window=16)
+    base.update(kw)
+    B, T, H, d_qk, m = (base.pop(x) for x in ("B", "T", "H", "d_qk", "m"))
+    return tg.agg_params(B, T, H, d_qk, m, **base)
+
+
+def test_workspace_sizes(lib):
+    p = _agg()
+    # two normalised copies of q and k, each 256-byte aligned
+    assert tg.tg_workspace_size(tg.TG_WS_TANGO, p) == 2 * 2 * 64 * 128 * 2
+    p = _agg(flags=tg.TG_FLAG_QK_NORMALIZED)
+    assert tg.tg_workspace_size(tg.TG_WS_TANGO, p) == 0
+    bp = tg.block_params(8, 2048, 512, 2, 128, 28480, dtype=tg.TG_BF16)
+    need = tg.tg_workspace_size(tg.TG_WS_BLOCK, bp)
+    BT = 8 * 2048
+    assert need == BT * 2 * (512 + 2 * 128 + 2 * 28480)
+    assert tg.tg_workspace_size(tg.TG_WS_TANGO, _agg(H=3)) == 0        # invalid -> 0
+    assert tg.tg_workspace_size(7, p) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), tg.TG_ERR_INVALID_ARG),
+    (dict(T=0), tg.TG_ERR_INVALID_ARG),
+    (dict(H=3), tg.TG_ERR_INVALID_ARG),             # d_qk % H != 0
+    (dict(m=255), tg.TG_ERR_INVALID_ARG),           # m % H != 0
+    (dict(s=25.0), tg.TG_ERR_INVALID_ARG),          # tau cap of eq. 4
+    (dict(s=-1.0), tg.TG_ERR_INVALID_ARG),
+    (dict(window=0), tg.TG_ERR_INVALID_ARG),
+    (dict(phi_mode=2), tg.TG_ERR_INVALID_ARG),
+    (dict(flags=0x80), tg.TG_ERR_INVALID_ARG),
+    (dict(dtype=5), tg.TG_ERR_INVALID_ARG),
+    (dict(d_qk=96, H=2), tg.TG_ERR_UNSUPPORTED),    # bf16 head width 48
+    (dict(m=2 * 4747), tg.TG_ERR_UNSUPPORTED),      # bf16 head gate width not a multiple of 8
+])
+def test_invalid_arguments_rejected_on_host(lib, kw, status):
+    p = _agg(**kw)
+    raw = tg.load()
+    dummy = 256  # never dereferenced: validation fails first
+    st = raw.wango_aggregate(ctypes.byref(p), dummy, dummy, dummy, dummy, dummy, None, 0, None)
+    assert st == status
+
+
+def test_null_pointers_and_workspace(lib):
+    raw = tg.load()
+    p = _agg()
+    assert raw.tango_aggregate(None, 256, 256, 256, 256, 256, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert raw.tango_aggregate(ctypes.byref(p), None, 256, 256, 256, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    # misaligned bf16 tensor
+    assert raw.tango_aggregate(ctypes.byref(p), 258, 256, 256, 256, 256, None, 0, None) == \
+        tg.TG_ERR_UNSUPPORTED
+    # workspace required but missing / too small / misaligned
+    need = tg.tg_workspace_size(tg.TG_WS_TANGO, p)
+    assert raw.tango_aggregate(ctypes.byref(p), 256, 256, 256, 256, 256, None, 0, None) == tg.TG_ERR_WORKSPACE
+    assert raw.tango_aggregate(ctypes.byref(p), 256, 256, 256, 256, 256, 4096, need - 1, None) == \
+        tg.TG_ERR_WORKSPACE
+    assert raw.tango_aggregate(ctypes.byref(p), 256, 256, 256, 256, 256, 4096 + 16, need, None) == \
+        tg.TG_ERR_WORKSPACE
+
+
+def test_block_validation(lib):
+    raw = tg.load()
+    w = tg.tg_block_weights(*([256] * 6))
+    bp = tg.block_params(1, 8, 64, 2, 32, 256, dtype=tg.TG_BF16, rms_eps=0.0)
+    assert raw.tango_block_forward(ctypes.byref(bp), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    bp = tg.block_params(1, 8, 64, 2, 32, 256, dtype=tg.TG_BF16, mode=5)
+    assert raw.tango_block_forward(ctypes.byref(bp), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    bp = tg.block_params(1, 8, 60, 2, 32, 256, dtype=tg.TG_BF16)   # bf16 needs d % 64 == 0
+    assert raw.tango_block_forward(ctypes.byref(bp), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_UNSUPPORTED
+    bp = tg.block_params(1, 8, 64, 2, 32, 256, dtype=tg.TG_BF16)
+    w0 = tg.tg_block_weights(256, 256, None, 256, 256, 256)
+    assert raw.tango_block_forward(ctypes.byref(bp), ctypes.byref(w0), 256, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    assert raw.tango_block_forward(ctypes.byref(bp), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_WORKSPACE
+
+
+def test_binding_has_no_fallback(monkeypatch, tmp_path):
+    """Without the library the binding raises instead of computing anything itself."""
+    monkeypatch.setattr(tg, "_lib", None)
+    monkeypatch.setattr(tg._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        tg.load(build_if_missing=False)
+    monkeypatch.undo()

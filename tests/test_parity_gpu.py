@@ -1,0 +1,172 @@
+"""Parity of the CUDA path with the fp64 oracle, element by element, on seeded inputs.
+
+Tolerances (stated for the path): max |gpu - oracle| / max |oracle| per output tensor
+must be <= 1e-4 for fp32 storage (CUDA-core fp32 arithmetic) and <= 2e-2 for bf16
+storage (bf16 tensor-core operands, fp32 accumulation).  The oracle reads exactly the
+values the GPU reads (bf16 inputs are widened, not re-rounded).
+"""
+import numpy as np
+import pytest
+import torch
+
+import cross_token_gated_gb300 as tg
+import oracle
+from cross_token_gated_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def rel_err(gpu: torch.Tensor, ref: np.ndarray) -> float:
+    g = gpu.detach().double().cpu().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(g)), "non-finite values in the GPU output"
+    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def run_agg(kind, q, k, g, v, H, W=16, **kw):
+    qd, kd, gd = q.cuda(), k.cuda(), g.cuda()
+    vd = v.cuda() if v is not None else None
+    out = torch.empty_like(gd)
+    if kind == "tango":
+        tg.tango_aggregate(qd, kd, gd, vd, out, H=H, **kw)
+    else:
+        tg.wango_aggregate(qd, kd, gd, vd, out, H=H, window=W, **kw)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    return out
+
+
+def ref_agg(kind, q, k, g, v, H, W=16, s=10.0, rows=None, **kw):
+    args = [synth.oracle_view(t) if t is not None else None for t in (q, k, g, v)]
+    if kind == "tango":
+        return oracle.tango(*args, H=H, tau=s, rows=rows, **kw)
+    return oracle.wango_direct(*args, H=H, tau=s, window=W, rows=rows, **kw)
+
+
+# (B, T, H, d_qk, m, W): tiny oracle config, ragged T, ragged gate tiles, several W
+SMALL = [
+    (1, 64, 2, 32, 256, 16),      # the tiny oracle configuration
+    (1, 1, 2, 32, 256, 16),       # T = 1
+    (2, 63, 2, 128, 144, 1),      # W = 1: every earlier source is older
+    (3, 65, 2, 64, 272, 64),      # W = T - 1
+    (1, 200, 2, 128, 1040, 200),  # W = T: no older prefix
+    (2, 130, 4, 128, 528, 300),   # W > T, four heads of d_h = 32
+    (1, 300, 2, 128, 2096, 129),  # ragged window boundary
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+@pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}T{c[1]}H{c[2]}dqk{c[3]}m{c[4]}W{c[5]}" for c in SMALL])
+def test_agg_parity_small(kind, dtype, case):
+    B, T, H, dqk, m, W = case
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=T + m, dtype=dtype)
+    out = run_agg(kind, q, k, g, v, H, W)
+    ref = ref_agg(kind, q, k, g, v, H, W)
+    assert rel_err(out, ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_agg_null_gate_tau_array_and_gbar_output(kind, dtype):
+    """Per-head tau from device memory, the null gate on, v = NULL (out = gbar), and
+    pre-normalised q/k passed with TG_FLAG_QK_NORMALIZED."""
+    B, T, H, dqk, m, W = 2, 150, 2, 128, 512, 40
+    q, k, g, _ = synth.agg_inputs(B, T, dqk, m, seed=7, dtype=dtype)
+    tau = torch.tensor([10.0, 4.0], device="cuda")
+    nb = torch.tensor([-1.0, 0.5], device="cuda")
+    out = run_agg(kind, q, k, g, None, H, W, tau=tau, null_bias=nb)
+    ref = ref_agg(kind, q, k, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5])
+    assert rel_err(out, ref) <= TOL[dtype]
+    # unit vectors in, no normalisation inside
+    qn = q.double().reshape(B, T, H, -1)
+    qn = (qn / qn.norm(dim=-1, keepdim=True)).reshape(B, T, dqk).to(q.dtype)
+    kn = k.double().reshape(B, T, H, -1)
+    kn = (kn / kn.norm(dim=-1, keepdim=True)).reshape(B, T, dqk).to(k.dtype)
+    out2 = run_agg(kind, qn, kn, g, None, H, W, tau=tau, null_bias=nb, flags=tg.TG_FLAG_QK_NORMALIZED)
+    ref2 = ref_agg(kind, qn, kn, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5], qk_normalized=True)
+    assert rel_err(out2, ref2) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_agg_weights_sum_to_one_on_gpu(kind, dtype):
+    """g == 1 gives gbar == 1 on the GPU path too (the denominator is the sum of the
+    very weights applied to g)."""
+    B, T, H, dqk, m, W = 1, 333, 2, 128, 256, 70
+    q, k, _, _ = synth.agg_inputs(B, T, dqk, m, seed=11, dtype=dtype)
+    g = torch.ones(B, T, m, dtype=q.dtype)
+    out = run_agg(kind, q, k, g, None, H, W)
+    tol = 1e-5 if dtype == "f32" else 8e-3
+    assert (out.float() - 1).abs().max().item() <= tol
+
+
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_agg_parity_70m_shape_sampled(kind):
+    """bf16 at the 70M-tier aggregation shape (B=8, T=2048, m=28480, q/k width 128,
+    W=256): oracle rows sampled at the sequence ends, the window and tile boundaries,
+    plus random rows."""
+    B, T, H, dqk, m, W = 8, 2048, 2, 128, 28480, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=0, dtype="bf16")
+    out = run_agg(kind, q, k, g, v, H, W)
+    extra = [0, 1, 127, 128, 255, 256, 257, 383, 384, 2047, 7 * T + 2047, 3 * T + 1000]
+    rows = synth.random_rows(B, T, 40, seed=1, extra=extra)
+    ref = ref_agg(kind, q, k, g, v, H, W, rows=rows)
+    got = out.reshape(B * T, m)[torch.from_numpy(rows).cuda()]
+    assert rel_err(got, ref) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ block forward
+
+def run_block(h, w, H, mode, W, **kw):
+    hd = h.cuda()
+    wd = {n: t.cuda() for n, t in w.items()}
+    out = torch.empty_like(hd)
+    tg.tango_block_forward(hd, wd, out, H=H, mode=mode, window=W, **kw)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    return out
+
+
+def ref_block(h, w, H, mode, W, batches=None, s=10.0):
+    wv = {n: synth.oracle_view(t) for n, t in w.items()}
+    return oracle.block_forward(synth.oracle_view(h), wv, H=H, tau=s, mode=mode, window=W,
+                                batches=batches, rope_base=10000.0, rms_eps=1e-6)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_block_tiny_fp32(mode):
+    """The tiny oracle configuration: B=1, T=64, d=64, m=256, q/k width 32, W=16, fp32."""
+    B, T, d, dqk, m, H, W = 1, 64, 64, 32, 256, 2, 16
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=0, dtype="f32")
+    out = run_block(h, w, H, mode, W)
+    ref = ref_block(h, w, H, mode, W)
+    h64 = h.double().numpy()
+    assert rel_err(out, ref) <= 1e-4
+    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= 1e-4
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape", [(2, 100, 128, 64, 512, 2, 32), (1, 257, 128, 128, 1040, 2, 100)])
+def test_block_bf16_small(mode, shape):
+    B, T, d, dqk, m, H, W = shape
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=5, dtype="bf16")
+    out = run_block(h, w, H, mode, W)
+    ref = ref_block(h, w, H, mode, W)
+    h64 = h.double().numpy()
+    assert rel_err(out, ref) <= TOL["bf16"]
+    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+
+
+def test_block_70m_shape_sampled_sequences():
+    """The benchmarked configuration (B=8, T=2048, d=512, m=28480, q/k width 128, TANGO,
+    bf16): sequences 0 and 7 compared in full against the oracle."""
+    B, T, d, dqk, m, H = 8, 2048, 512, 128, 28480, 2
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=0, dtype="bf16")
+    out = run_block(h, w, H, 0, 1)
+    ref = ref_block(h, w, H, 0, 1, batches=[0, 7])
+    got = out[[0, 7]]
+    h64 = h[[0, 7]].double().numpy()
+    assert rel_err(got, ref) <= TOL["bf16"]
+    assert rel_err(got.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
