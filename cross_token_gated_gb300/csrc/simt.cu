@@ -18,9 +18,6 @@
 namespace tg {
 namespace {
 
-template <typename T> struct dtype_of;
-template <> struct dtype_of<float> { static constexpr tg_dtype v = TG_F32; };
-template <> struct dtype_of<__nv_bfloat16> { static constexpr tg_dtype v = TG_BF16; };
 
 // ---------------------------------------------------------------- row kernels
 

@@ -51,7 +51,7 @@ SMALL = [
     (2, 63, 2, 128, 144, 1),      # W = 1: every earlier source is older
     (3, 65, 2, 64, 272, 64),      # W = T - 1
     (1, 200, 2, 128, 1040, 200),  # W = T: no older prefix
-    (2, 130, 4, 128, 528, 300),   # W > T, four heads of d_h = 32
+    (2, 130, 4, 128, 544, 300),   # W > T, four heads of d_h = 32
     (1, 300, 2, 128, 2096, 129),  # ragged window boundary
 ]
 
