@@ -170,3 +170,20 @@ def test_block_70m_shape_sampled_sequences():
     h64 = h[[0, 7]].double().numpy()
     assert rel_err(got, ref) <= TOL["bf16"]
     assert rel_err(got.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+
+
+def test_bounded_wait_timeout_reports_status():
+    """TG_FLAG_DEBUG_TIMEOUT makes the TANGO kernel wait on a barrier that nothing
+    signals; the bounded wait runs out, the kernel records a timeout and returns, and
+    the context stays usable for the next call."""
+    B, T, H, dqk, m = 1, 256, 2, 128, 512
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=3, dtype="bf16")
+    qd, kd, gd, vd = q.cuda(), k.cuda(), g.cuda(), v.cuda()
+    out = torch.empty_like(gd)
+    tg.tango_aggregate(qd, kd, gd, vd, out, H=H, flags=tg.TG_FLAG_DEBUG_TIMEOUT)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_ERR_TIMEOUT
+    assert word & 1 and (word >> 8) & 0xFF == 1
+    assert tg.tg_check_device_error() == (tg.TG_OK, 0)      # the word was cleared
+    out = run_agg("tango", q, k, g, v, H)
+    assert rel_err(out, ref_agg("tango", q, k, g, v, H)) <= TOL["bf16"]
