@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the cross-token gate aggregation path on GB300.
+
+One step = one TANGO block forward (RMSNorm -> projection GEMM with RoPE/norm/SiLU
+epilogues -> TANGO aggregation -> W_o GEMM + residual) at the 70M-tier shape
+B=8, T=2048, d=512, m=28480, q/k width 128 (2 heads of 64), bf16 storage, fp32
+accumulation, through the C ABI (tango_block_forward).
+
+Printed: ONE JSON line (rank 0).  `value` = tokens/s of the whole job with inputs
+resident in HBM; `e2e` = the same through the C ABI with pinned host buffers and the
+host<->device copies inside the timed region; `roofline` = the TANGO aggregation
+kernel's algorithmic TFLOP/s against the measured bf16 peak; `cpu_baseline` = the
+fp64 oracle on the host cores on a bounded sample.  `also` carries the WANGO and
+long-context aggregation measurements.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "aggregation tokens/s and TFLOP/s at T=2k/8k on 1 GB300; % of BF16 tensor-core roofline"
+B, T, D, DQK, M, H = 8, 2048, 512, 128, 28480, 2
+WORKLOAD = f"TANGO block forward (RMSNorm, q/k/g/v projections, full-prefix aggregation, W_o + residual), " \
+           f"B={B} T={T} d={D} m={M} q/k width {DQK} (H={H}, d_h=64), s=10, bf16"
+KERNELS_PER_STEP = 4  # rmsnorm, projection GEMM, TANGO aggregation, output GEMM
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true")
+    ap.add_argument("--agg-only", choices=["tango", "wango"],
+                    help="only run one aggregation kernel (for profiler captures)")
+    ap.add_argument("--agg-B", type=int, default=2)
+    ap.add_argument("--agg-T", type=int, default=2048)
+    ap.add_argument("--agg-iters", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return p["bf16_tflops"], p["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_cpu_baseline(max_seconds: float = 30.0):
+    """The fp64 oracle on the host cores: one block forward over the first Tc positions of
+    sequence 0 (causality makes those outputs depend on those positions only).  Tc grows
+    from 128 while the sample stays within the budget."""
+    import oracle
+    from cross_token_gated_gb300 import synth
+    h, w = synth.block_inputs(1, T, D, DQK, M, seed=0, dtype="bf16")
+    wv = {n: synth.oracle_view(t) for n, t in w.items()}
+    hv = synth.oracle_view(h)
+    Tc, spent, result = 128, 0.0, None
+    while True:
+        t0 = time.perf_counter()
+        oracle.block_forward(hv[:, :Tc], wv, H=H, tau=10.0, mode=0, window=1)
+        dt = time.perf_counter() - t0
+        spent += dt
+        result = (Tc, dt)
+        # the next size costs ~2.5x (linear projections plus the quadratic pair term)
+        if Tc * 2 > T or spent + 2.5 * dt > max_seconds:
+            break
+        Tc *= 2
+    Tc, dt = result
+    return {"value": Tc / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"block forward of sequence 0, positions 0..{Tc - 1} (T={Tc} of {T}), "
+                      f"{dt:.2f} s, fp64"}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as it stands on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from cross_token_gated_gb300 import synth
+    h, w = synth.block_inputs(1, T, D, DQK, M, seed=0, dtype="bf16")
+    wv = {n: synth.oracle_view(t) for n, t in w.items()}
+    hv = synth.oracle_view(h)
+    Tc = 256
+    for _ in range(args.warmup):
+        oracle.block_forward(hv[:, :Tc], wv, H=H, tau=10.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.block_forward(hv[:, :Tc], wv, H=H, tau=10.0)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = Tc / dt
+    sample = f"each step: block forward of sequence 0, positions 0..{Tc - 1}, fp64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_T": Tc},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.agg_only:
+        run_agg_only(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import cross_token_gated_gb300 as tg
+    from cross_token_gated_gb300 import accounting as acc
+    from cross_token_gated_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    tg.load()
+    peak_tf, peak_gbs, peak_src = peaks()
+
+    # ---------------------------------------------------------------- inputs
+    h, w = synth.block_inputs(B, T, D, DQK, M, seed=rank, dtype="bf16")
+    hd = h.to(dev)
+    wd = {n: t.to(dev) for n, t in w.items()}
+    out = torch.empty_like(hd)
+    ws = tg.block_workspace(B, T, D, H, DQK, M, dtype=tg.TG_BF16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tg.tango_block_forward(hd, wd, out, H=H, ws=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st, word = tg.tg_check_device_error(stream)
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error after warm-up: {tg.status_string(st)} ({word:#x})")
+
+    # ------------------------------------------------------------- timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clocks = clk.summary()
+    t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * B * T / (ms_max * 1e-3)
+    st, word = tg.tg_check_device_error(stream)
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error in timed region: {tg.status_string(st)} ({word:#x})")
+
+    # ------------------------------------------ dominant kernel: TANGO aggregation
+    # The aggregation kernel re-run on the step's own projected q/k/g and u (the
+    # workspace regions x, q, k, g, v in that order, each 256-byte aligned, as
+    # tango.h documents), timed with events on the same stream.
+    L = {"q": 0, "k": 0, "g": 0, "v": 0}
+    es = 2
+    off = 0
+    sz = {"x": B * T * D, "q": B * T * DQK, "k": B * T * DQK, "g": B * T * M, "v": B * T * M}
+    base = (ws.data_ptr() + 255) & ~255
+    for name in ("x", "q", "k", "g", "v"):
+        L[name] = base + off
+        off += (sz[name] * es + 255) & ~255
+    agg_out = torch.empty(B, T, M, dtype=torch.bfloat16, device=dev)
+
+    def agg_once():
+        p = tg.agg_params(B, T, H, DQK, M, dtype=tg.TG_BF16, s=10.0, flags=tg.TG_FLAG_QK_NORMALIZED)
+        r = tg.load().tango_aggregate(ctypes.byref(p), L["q"], L["k"], L["g"], L["v"],
+                                      agg_out.data_ptr(), None, 0, stream.cuda_stream)
+        if r != tg.TG_OK:
+            raise tg.TgError(r, "tango_aggregate")
+
+    step()  # refresh the workspace (v was overwritten by gbar * v)
+    for _ in range(3):
+        agg_once()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(5, args.steps // 2)
+    k0.record(stream)
+    for _ in range(reps):
+        agg_once()
+    k1.record(stream)
+    torch.cuda.synchronize(dev)
+    agg_ms = k0.elapsed_time(k1) / reps
+    agg_flops = acc.tango_agg_flops(B, T, DQK, M)
+    achieved = agg_flops / (agg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": None,
+                "kernel": "tango_tc_kernel", "kernel_ms": agg_ms,
+                "algorithmic_flops_per_launch": agg_flops,
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+
+    # ------------------------------------------------------------------ e2e
+    h_host = h.pin_memory()
+    o_host = torch.empty_like(h_host).pin_memory()
+    for _ in range(2):
+        hd.copy_(h_host, non_blocking=True)
+        step()
+        o_host.copy_(out, non_blocking=True)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        hd.copy_(h_host, non_blocking=True)
+        step()
+        o_host.copy_(out, non_blocking=True)
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    t = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e = {"value": world * B * T / (float(t.item()) * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h_host.numel() * 2, "d2h_bytes_per_step": o_host.numel() * 2}
+
+    # -------------------------------------------- other configurations (context)
+    also = {}
+    if rank == 0 and not args.no_also:
+        also = other_configs(tg, acc, dev, stream, peak_tf, peak_gbs)
+
+    step_flops = acc.block_flops(B, T, D, DQK, M)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T, "d": D, "m": M,
+                       "qk_width": DQK, "heads": H, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (g, v are 0.93 GB each)"},
+            "step_tflops": step_flops / (ms_max * 1e-3) / 1e12,
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+            "also": also,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_cpu_baseline()
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
+    """Aggregation-only timings: TANGO at B=8/T=2048 and B=1/T=8192, WANGO (W=256) at
+    both; unit-normalised q/k and N(0,1) g, v generated on the device."""
+    import torch
+    res = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    for (b, t_len) in ((8, 2048), (1, 8192)):
+        q = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+        q = (q / q.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+        k = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+        k = (k / k.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+        g = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
+        v = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
+        o = torch.empty_like(g)
+        for kind in ("tango", "wango"):
+            if kind == "tango":
+                f = lambda: tg.tango_aggregate(q, k, g, v, o, H=H, flags=tg.TG_FLAG_QK_NORMALIZED, stream=stream)
+                fl = acc.tango_agg_flops(b, t_len, DQK, M)
+            else:
+                f = lambda: tg.wango_aggregate(q, k, g, v, o, H=H, window=256, flags=tg.TG_FLAG_QK_NORMALIZED,
+                                               stream=stream)
+                fl = acc.wango_agg_flops(b, t_len, DQK, M, H, 256)
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            e0.record(stream)
+            for _ in range(reps):
+                f()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            by = acc.agg_bytes(b, t_len, DQK, M)
+            res[f"{kind}_B{b}_T{t_len}"] = {
+                "ms": ms, "tokens_per_s": b * t_len / (ms * 1e-3),
+                "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf,
+                "gbs": by / (ms * 1e-3) / 1e9, "frac_hbm_peak": by / (ms * 1e-3) / 1e9 / peak_gbs}
+        del q, k, g, v, o
+        torch.cuda.empty_cache()
+    st, word = tg.tg_check_device_error(stream)
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error in aggregation timings ({word:#x})")
+    return res
+
+
+def run_agg_only(args):
+    """A few launches of one aggregation kernel on a small case (B, T given), inputs
+    larger than L2.  Used for profiler captures; prints one timing line."""
+    import torch
+
+    import cross_token_gated_gb300 as tg
+    from cross_token_gated_gb300 import accounting as acc
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    b, t_len = args.agg_B, args.agg_T
+    q = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+    q = (q / q.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+    k = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+    k = (k / k.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+    g = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
+    v = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
+    o = torch.empty_like(g)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.agg_iters):
+        if args.agg_only == "tango":
+            tg.tango_aggregate(q, k, g, v, o, H=H, flags=tg.TG_FLAG_QK_NORMALIZED)
+        else:
+            tg.wango_aggregate(q, k, g, v, o, H=H, window=256, flags=tg.TG_FLAG_QK_NORMALIZED)
+    st, word = tg.tg_check_device_error()
+    dt = (time.perf_counter() - t0) / args.agg_iters
+    print(json.dumps({"agg_only": args.agg_only, "B": b, "T": t_len, "status": st, "word": word,
+                      "wall_ms_per_launch": dt * 1e3}))
+    if st != tg.TG_OK:
+        sys.exit(1)
+
+
+if __name__ == "__main__":
+    main()

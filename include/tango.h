@@ -152,7 +152,9 @@ typedef struct {
  *   g = SiLU(W_g x); v = W_v x; gbar by TANGO or WANGO; h_out = h + W_o (gbar * v).
  * h: device [B, T, d], read.  h_out: device [B, T, d], written; may alias h.
  * ws: device scratch of at least tg_workspace_size(TG_WS_BLOCK, p) bytes, 256-byte
- * aligned; it holds x, q, k, g and v (v is overwritten by gbar * v).
+ * aligned.  On return it holds, in this order, each region starting on a 256-byte
+ * boundary: x [B*T, d], unit q [B*T, d_qk], unit k [B*T, d_qk], g [B*T, m] and
+ * u = gbar * v [B*T, m] (v is overwritten in place).
  */
 tg_status tango_block_forward(const tg_block_params *p, const tg_block_weights *w,
                               const void *h, void *h_out, void *ws, size_t ws_bytes,
