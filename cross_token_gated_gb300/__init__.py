@@ -6,7 +6,7 @@ kernels.  PyTorch supplies device memory and streams.  There is no fallback: if
 the library cannot be loaded, every call raises.
 
 Functions (same names as the C ABI):
-  tango_aggregate, wango_aggregate, tango_block_forward,
+  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_block_forward,
   tg_workspace_size, tg_status_string, tg_check_device_error, tg_version
 """
 from __future__ import annotations
@@ -82,6 +82,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, sz, vp]
             f.restype = ctypes.c_int
+        lib.tango_aggregate_noalloc.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp]
+        lib.tango_aggregate_noalloc.restype = ctypes.c_int
         lib.tango_block_forward.argtypes = [P(tg_block_params), P(tg_block_weights), vp, vp, vp, sz, vp]
         lib.tango_block_forward.restype = ctypes.c_int
         lib.tg_workspace_size.argtypes = [ctypes.c_int, vp]
@@ -195,6 +197,24 @@ def wango_aggregate(q, k, g, v, out, *, H, window, s=10.0, tau=None, null_bias=N
     """Windowed aggregation (eqs. 7-10); arguments as for tango_aggregate."""
     return _aggregate("wango_aggregate", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias,
                       window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream)
+
+
+def tango_aggregate_noalloc(q, k, g, v, out, *, H, s=10.0, tau=None, null_bias=None, flags=0,
+                            stream=None):
+    """tango_aggregate without a workspace: the library's fixed device scratch array is
+    used instead (for callers that cannot allocate device memory).  Raises TgError with
+    TG_ERR_WORKSPACE when the problem needs more scratch than TG_NOALLOC_SCRATCH_BYTES."""
+    B, T, d_qk = q.shape
+    m = g.shape[-1]
+    p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias, flags=flags)
+    st = load().tango_aggregate_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(out),
+                                        _stream(stream))
+    if st != TG_OK:
+        raise TgError(st, "tango_aggregate_noalloc")
+    return out
+
+
+TG_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def block_params(B, T, d, H, d_qk, m, *, dtype, mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None,

@@ -160,6 +160,33 @@ tg_status tango_block_forward(const tg_block_params *p, const tg_block_weights *
                               const void *h, void *h_out, void *ws, size_t ws_bytes,
                               tg_stream_t stream);
 
+/*
+ * tango_aggregate for callers that cannot allocate device memory: runtimes that
+ * forbid cudaMalloc once they are running, code confined to a memory pool it does not
+ * own, or drivers that must not meet an out-of-memory failure mid-work.  The paper has
+ * no counterpart; this is a deployment variant of tango_aggregate with no workspace
+ * argument.
+ *   - Scratch: one fixed array of TG_NOALLOC_SCRATCH_BYTES in device memory, declared
+ *     by the library; every GPU that loads the library holds it until the process
+ *     exits.  The call itself allocates nothing (no cudaMalloc, cudaFree or allocating
+ *     library routine).
+ *   - Limit: the call needs tg_workspace_size(TG_WS_TANGO, p) bytes of that array
+ *     (two 256-byte-aligned copies of B*T*d_qk elements; none with
+ *     TG_FLAG_QK_NORMALIZED).  Larger problems return TG_ERR_WORKSPACE and launch
+ *     nothing; for bf16 that is B*T*d_qk > 4,194,304.
+ *   - The first call on each device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and keeps the last call's contents;
+ *     each call overwrites the part it reads before reading it, so nothing has to be
+ *     cleared between calls.  Calls whose kernels overlap on the GPU (different
+ *     streams, or concurrent host threads) race on the array.
+ * Other arguments, results and errors are those of tango_aggregate.
+ */
+#define TG_NOALLOC_SCRATCH_BYTES (16u << 20)
+tg_status tango_aggregate_noalloc(const tg_agg_params *p, const void *q, const void *k,
+                                  const void *g, const void *v, void *out, tg_stream_t stream);
+
 /* Workspace bytes needed by the call `which` (TG_WS_*) with `params`; 0 for invalid
  * parameters (validate with the call itself to get the reason). */
 size_t tg_workspace_size(int which, const void *params);
