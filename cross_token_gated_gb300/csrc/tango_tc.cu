@@ -5,20 +5,30 @@
 // per head.  The shift by e^-tau cancels in the ratio; since |cos| <= 1 and
 // tau <= 20 every weight lies in [e^-40, 1], so no running maximum is kept.
 //
-// One CTA computes a 128-destination x 256-gate-column tile of one (batch, head)
-// and walks the 128-source blocks j = 0..i-block:
-//   warp 0        TMA: qhat tile once; per source block khat (128 x d_h) and the
-//                 gate tile G_j (128 x 256, four 64-column boxes), 2-stage ring
-//   warp 1        TMEM allocation; MMA issue:
-//                   S_j = Qhat Khat_j^T  (M=128, N=128, K=d_h)      -> TMEM S[j % 2]
-//                   O  += P_j G_j        (M=128, N=256, K=128)      A = P_j from TMEM
-//                 S_{j+1} is issued before O += P_j G_j, so the exponentials of one
-//                 block overlap the MMA of the previous one.
-//   warps 2-5     softmax warpgroup 0 (even j), warps 6-9 warpgroup 1 (odd j): read a
-//                 row of S from TMEM, weights exp2(tau log2e (s - 1)) with the causal
-//                 mask on the diagonal block, round to bf16, add the ROUNDED weights
-//                 to the row's denominator, write P (bf16) back over S.
-//   epilogue      both warpgroups: O / denominator * v, bf16 stores.
+// A tile is 128 destinations x 256 gate columns of one (batch, head); it walks the
+// 128-source blocks j = 0..ib (ib = its destination block).  Persistent CTAs, one
+// per SM, take "units" round-robin: a unit is the pair of tiles (nI-1-p, p) of one
+// (batch, head, gate tile), so every unit costs nI+1 source blocks and the units
+// of one gate tile, which share G and khat, run side by side out of L2.
+//
+//   warp 0     TMA: qhat tiles (2 buffers), khat blocks (2-stage ring), G in half
+//              blocks of 64 sources x 256 columns (5-stage ring, four 64-column boxes
+//              each); prefetches the tile's v into L2.
+//   warp 1     TMEM allocation; MMA issue from one thread:
+//                S_j = Qhat Khat_j^T   (M=128, N=128, K=d_h)     -> TMEM S[J % 2]
+//                O  += P_j G_j         (M=128, N=256, K=64 x 2)  A = P_j from TMEM
+//              J counts source blocks over all tiles of the CTA.  S_{j+1} is issued
+//              before O += P_j G_j.  The issue path keeps descriptors in registers
+//              and avoids compiler memory barriers: one thread issues 12 MMAs per
+//              block, so its per-instruction cost bounds the whole kernel.
+//   warps 2-9  softmax: warpgroup w (warps 2-5, 6-9) takes columns [64w, 64w+64) of
+//              every score block; one row per thread from TMEM, exp2(tau log2e
+//              (s - 1)) with the causal mask on the diagonal block, rounded to bf16;
+//              the ROUNDED weights are summed into the row's denominator; P (bf16) is
+//              written back over S once both warpgroups have read their scores.
+//   epilogue   the same warps after a tile's last block: O / den * v from TMEM,
+//              bf16 stores; the accumulator is released to the next tile as soon as
+//              it has been read.
 // TMEM: O in columns [0, 256), S[0] in [256, 384), S[1] in [384, 512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -30,28 +40,36 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBlk = 128;     // destinations per tile and sources per block
-constexpr int kNg = 256;      // gate columns per tile
-constexpr int kStages = 2;
+constexpr int kBlk = 128;      // destinations per tile; sources per score block
+constexpr int kHalf = 64;      // sources per G stage
+constexpr int kNg = 256;       // gate columns per tile
+constexpr int kQBufs = 2;
+constexpr int kKStages = 2;
+constexpr int kGStages = 5;
 constexpr int kThreads = 320;  // 10 warps
-constexpr uint32_t kGBytes = kBlk * kNg * 2;  // 64 KB
-constexpr uint32_t kGBox = kBlk * 64 * 2;     // 16 KB: one 64-column box
-constexpr uint32_t kQKMax = kBlk * 64 * 2;    // 16 KB at d_h = 64
+constexpr uint32_t kQKMax = kBlk * 64 * 2;     // 16 KB at d_h = 64
+constexpr uint32_t kGBox = kHalf * 64 * 2;     // 8 KB: 64 sources x 64 columns
+constexpr uint32_t kGStage = 4 * kGBox;        // 32 KB
 constexpr uint32_t kColO = 0, kColS0 = 256;
 
 struct __align__(8) Bars {
-  uint64_t q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_full, drain, never;
+  uint64_t q_full[kQBufs], q_empty[kQBufs];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t g_full[kGStages], g_empty[kGStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_full, o_empty;
+  uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
   float rowsum[2][kBlk];
 };
 
-// smem: Q | K[2] | G[2] | Bars, all tiles 1024-byte aligned
-constexpr size_t kSmemBytes = 1024 + kQKMax * (1 + kStages) + kGBytes * kStages + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kQKMax * (kQBufs + kKStages) + kGStage * kGStages + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
   int B, T, H, dqk, m, d_h, m_h;
-  int n_iblk, n_ntile;
+  int n_iblk, n_ntile, n_pair, n_units;
   float s;
   const float* tau;
   const float* null_bias;
@@ -62,54 +80,134 @@ struct Args {
   int debug_timeout;
 };
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+struct Tile {
+  int b, head, ib, n0;
+};
+
+// Walks this CTA's tiles: units u = blockIdx.x, blockIdx.x + gridDim.x, ...; a unit
+// is the pair of destination blocks (nI-1-p, p) of one (batch, head, gate tile), the
+// long one first, so every unit costs nI+1 source blocks.
+struct TileSeq {
+  int u, k;
+  Tile t;
+  __device__ __forceinline__ bool load(const Args& a) {
+    for (; u < a.n_units; u += gridDim.x, k = 0) {
+      const int g = u / a.n_pair, p = u % a.n_pair;
+      const int lo = p, hi = a.n_iblk - 1 - p;
+      if (k == 1 && lo == hi) continue;
+      t.ib = k == 0 ? hi : lo;
+      t.n0 = (g % a.n_ntile) * kNg;
+      t.head = (g / a.n_ntile) % a.H;
+      t.b = g / (a.n_ntile * a.H);
+      return true;
+    }
+    return false;
+  }
+  __device__ __forceinline__ bool first(const Args& a) {
+    u = blockIdx.x;
+    k = 0;
+    return load(a);
+  }
+  __device__ __forceinline__ bool next(const Args& a) {
+    if (++k == 2) {
+      k = 0;
+      u += gridDim.x;
+    }
+    return load(a);
+  }
+};
+
+// Bounded wait with a cheap fast path: one try_wait; only when that fails, the
+// abort flag and the wall-clock limit are consulted.
+__device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
   if (*(volatile int*)&b.abort) return false;
   if (mbar_wait(bar, parity, a.timeout_ns)) return true;
   *(volatile int*)&b.abort = 1;
   record_error(a.err, kErrTimeout | kKernTango);
   return false;
 }
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+  if (mbar_try_wait_nc(smem_u32(bar), parity)) return true;
+  return wait_slow(bar, parity, b, a);
+}
 
 __device__ __forceinline__ uint32_t qk_layout(int d_h) {
   return d_h == 64 ? kSwizzle128B : d_h == 32 ? kSwizzle64B : kSwizzle32B;
 }
 
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+               "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// 64 scores of one row (columns [64w, 64w+64) of a block): weights exp2(c (s - 1)),
+// with sources after the destination zeroed on the diagonal block, rounded to bf16
+// and written as P at TMEM columns [32w, 32w+32) of the score buffer; the rounded
+// weights are added to four partial denominators.
+template <bool kDiag>
+__device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p_tm, float c, int row,
+                                          int src0, float (&dsum)[4]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t p[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float w0 = ex2_approx(fmaf(c, __uint_as_float(r[q][e]), -c));
+      float w1 = ex2_approx(fmaf(c, __uint_as_float(r[q][e + 1]), -c));
+      if (kDiag) {
+        if (src0 + q * 32 + e > row) w0 = 0.f;
+        if (src0 + q * 32 + e + 1 > row) w1 = 0.f;
+      }
+      const uint32_t pk = pack_bf16x2(w0, w1);
+      dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
+      p[e / 2] = pk;
+    }
+    tmem_st16(p_tm + q * 16, p);
+  }
+}
+
+// Ring position: stage index and the parity of its current phase.
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++stage == n) { stage = 0; phase ^= 1; }
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     tango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmG, const Args a) {
+                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                    const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
-  uint8_t* sK = sQ + kQKMax;
-  uint8_t* sG = sK + kStages * kQKMax;
-  Bars& b = *reinterpret_cast<Bars*>(sG + kStages * kGBytes);
+  uint8_t* sK = sQ + kQBufs * kQKMax;
+  uint8_t* sG = sK + kKStages * kQKMax;
+  Bars& b = *reinterpret_cast<Bars*>(sG + kGStages * kGStage);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // tile -> (batch, head, gate tile, destination block); destination blocks of
-  // one (batch, head, gate tile) are adjacent, longest first, so that the CTAs
-  // that share G_j and Khat_j run together and the causal imbalance evens out.
-  int t = blockIdx.x;
-  const int ib = a.n_iblk - 1 - t % a.n_iblk;
-  t /= a.n_iblk;
-  const int nt = t % a.n_ntile;
-  t /= a.n_ntile;
-  const int head = t % a.H;
-  const int bb = t / a.H;
-  const int i0 = ib * kBlk, n0 = nt * kNg;
-  const int nj = ib + 1;
   const uint32_t qk_bytes = kBlk * a.d_h * 2;
 
   if (threadIdx.x == 0) {
-    mbar_init(&b.q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&b.full[s], 1);
-      mbar_init(&b.empty[s], 1);
+    for (int s = 0; s < kQBufs; ++s) {
+      mbar_init(&b.q_full[s], 1);
+      mbar_init(&b.q_empty[s], 1);
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&b.k_full[s], 1);
+      mbar_init(&b.k_empty[s], 1);
+    }
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&b.g_full[s], 1);
+      mbar_init(&b.g_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], 4);
+      mbar_init(&b.p_full[i], 8);
     }
     mbar_init(&b.o_full, 1);
+    mbar_init(&b.o_empty, 8);
     mbar_init(&b.drain, 1);
     mbar_init(&b.never, 1);
     b.abort = 0;
@@ -126,142 +224,207 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
-    mbar_arrive_expect_tx(&b.q_full, qk_bytes);
-    tma_load_3d(sQ, &tmQ, &b.q_full, head * a.d_h, i0, bb);
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued_mask = 0;
-    uint32_t issued_phase[kStages] = {0, 0};
-    for (int j = 0; j < nj; ++j) {
-      if (!wait_bar(&b.empty[stage], phase ^ 1, b, a)) break;
-      mbar_arrive_expect_tx(&b.full[stage], qk_bytes + kGBytes);
-      tma_load_3d(sK + stage * kQKMax, &tmK, &b.full[stage], head * a.d_h, j * kBlk, bb);
-      uint8_t* g = sG + stage * kGBytes;
-      const int gx = head * a.m_h + n0;
+    Ring kr, gr;
+    bool ok = true;
+    uint32_t qmask = 0, kmask = 0, gmask = 0, qph[kQBufs] = {}, kph[kKStages] = {}, gph[kGStages] = {};
+    TileSeq seq;
+    int tc = 0;
+    for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
+      const Tile& t = seq.t;
+      const int i0 = t.ib * kBlk, qb = tc & 1;
+      const uint32_t qp = (tc >> 1) & 1;
+      if (!(ok = wait_bar(&b.q_empty[qb], qp ^ 1, b, a))) break;
+      mbar_arrive_expect_tx(&b.q_full[qb], qk_bytes);
+      tma_load_3d(sQ + qb * kQKMax, &tmQ, &b.q_full[qb], t.head * a.d_h, i0, t.b);
+      qmask |= 1u << qb;
+      qph[qb] = qp;
+      if (a.v)
+        for (int c = 0; c < kNg; c += 64) tma_prefetch_l2_3d(&tmV, t.head * a.m_h + t.n0 + c, i0, t.b);
+      const int gx = t.head * a.m_h + t.n0;
+      for (int j = 0; ok && j <= t.ib; ++j) {
+        if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
+        mbar_arrive_expect_tx(&b.k_full[kr.stage], qk_bytes);
+        tma_load_3d(sK + kr.stage * kQKMax, &tmK, &b.k_full[kr.stage], t.head * a.d_h, j * kBlk, t.b);
+        kmask |= 1u << kr.stage;
+        kph[kr.stage] = kr.phase;
+        kr.next(kKStages);
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a))) break;
+          uint8_t* dst = sG + gr.stage * kGStage;
+          mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) tma_load_3d(g + u * kGBox, &tmG, &b.full[stage], gx + 64 * u, j * kBlk, bb);
-      issued_mask |= 1 << stage;
-      issued_phase[stage] = phase;
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
+          for (int c = 0; c < 4; ++c)
+            tma_load_3d(dst + c * kGBox, &tmG, &b.g_full[gr.stage], gx + 64 * c, j * kBlk + h * kHalf, t.b);
+          gmask |= 1u << gr.stage;
+          gph[gr.stage] = gr.phase;
+          gr.next(kGStages);
+        }
+      }
     }
-    mbar_wait(&b.q_full, 0, a.timeout_ns);
-    for (int s = 0; s < kStages; ++s)
-      if (issued_mask & (1 << s)) mbar_wait(&b.full[s], issued_phase[s], a.timeout_ns);
+    // Copies still in flight land before the CTA exits.
+    for (int s = 0; s < kQBufs; ++s)
+      if (qmask & (1u << s)) mbar_wait(&b.q_full[s], qph[s], a.timeout_ns);
+    for (int s = 0; s < kKStages; ++s)
+      if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
+    for (int s = 0; s < kGStages; ++s)
+      if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);
     const uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);
     const uint32_t lay = qk_layout(a.d_h);
-    const uint32_t sbo = 8u * a.d_h * 2u;  // 8 rows of one swizzle atom
+    const uint32_t sbo = 8u * a.d_h * 2u;
+    const int ksteps = a.d_h / 16;
+    // Descriptors of stage 0; other stages differ only in the start-address field
+    // ((byte offset) >> 4 added to the low bits, which never carry: smem < 256 KB).
+    const uint64_t qdesc0 = smem_desc(smem_u32(sQ), 16, sbo, lay);
+    const uint64_t kdesc0 = smem_desc(smem_u32(sK), 16, sbo, lay);
+    const uint64_t gdesc0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
-    if (ok) ok = wait_bar(&b.q_full, 0, b, a);
-    const uint32_t qaddr = smem_u32(sQ);
-    int stage = 0;
-    uint32_t phase = 0;
-    auto issue_pg = [&](int jj) -> bool {
-      const int buf = jj & 1;
+    Ring kr, gr;
+    uint32_t ophase = 0;
+    uint32_t J = 0;  // source blocks issued by this CTA
+    // O += P_jj G_jj (two half blocks); the tile's first block overwrites O once the
+    // previous tile's epilogue has read the accumulator out of TMEM.
+    auto issue_pg = [&](uint32_t jj, bool first) -> bool {
+      const uint32_t buf = jj & 1;
       if (!wait_bar(&b.p_full[buf], (jj >> 1) & 1, b, a)) return false;
-      tc_fence_after();
-      const int st = jj % kStages;
-      const uint32_t gaddr = smem_u32(sG + st * kGBytes);
+      if (first) {
+        if (!wait_bar(&b.o_empty, ophase ^ 1, b, a)) return false;
+        ophase ^= 1;
+      }
       const uint32_t ptm = tmem + kColS0 + buf * 128;
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk) {
-        const uint64_t bd = smem_desc(gaddr + kk * 2048, kGBox, 1024, kSwizzle128B);
-        mma_bf16_ts(tmem + kColO, ptm + kk * 8, bd, idesc_o, (jj | kk) != 0);
+      for (int h = 0; h < 2; ++h) {
+        if (!wait_bar(&b.g_full[gr.stage], gr.phase, b, a)) return false;
+        tc_fence_after_nc();
+        const uint64_t gd = gdesc0 + (uint64_t)((gr.stage * kGStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kHalf / 16; ++kk)
+          mma_bf16_ts_nc(tmem + kColO, ptm + h * 32 + kk * 8, gd + (uint64_t)(kk * (2048 >> 4)), idesc_o,
+                         (first && h == 0 && kk == 0) ? 0u : 1u);
+        mma_commit_nc(&b.g_empty[gr.stage]);
+        gr.next(kGStages);
       }
-      mma_commit(&b.empty[st]);
       return true;
     };
-    for (int j = 0; ok && j < nj; ++j) {
-      if (!wait_bar(&b.full[stage], phase, b, a)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t kaddr = smem_u32(sK + stage * kQKMax);
-      const uint32_t stm = tmem + kColS0 + (j & 1) * 128;
-      for (int kk = 0; kk < a.d_h / 16; ++kk) {
-        const uint64_t ad = smem_desc(qaddr + kk * 32, 16, sbo, lay);
-        const uint64_t bd = smem_desc(kaddr + kk * 32, 16, sbo, lay);
-        mma_bf16_ss(stm, ad, bd, idesc_s, kk != 0);
+    TileSeq seq;
+    int tc = 0;
+    for (bool have = ok && seq.first(a); ok && have; have = seq.next(a), ++tc) {
+      const int qb = tc & 1;
+      if (!(ok = wait_bar(&b.q_full[qb], (tc >> 1) & 1, b, a))) break;
+      const uint64_t qd = qdesc0 + (uint64_t)((qb * kQKMax) >> 4);
+      const int nj = seq.t.ib + 1;
+      for (int j = 0; j < nj; ++j, ++J) {
+        if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
+        tc_fence_after_nc();
+        const uint64_t kd = kdesc0 + (uint64_t)((kr.stage * kQKMax) >> 4);
+        const uint32_t stm = tmem + kColS0 + (J & 1) * 128;
+        for (int kk = 0; kk < ksteps; ++kk)
+          mma_bf16_ss_nc(stm, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+        mma_commit_nc(&b.k_empty[kr.stage]);
+        mma_commit_nc(&b.s_full[J & 1]);
+        kr.next(kKStages);
+        if (j == nj - 1) mma_commit_nc(&b.q_empty[qb]);
+        if (j >= 1 && !(ok = issue_pg(J - 1, j == 1))) break;
       }
-      mma_commit(&b.s_full[j & 1]);
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
-      if (j >= 1 && !issue_pg(j - 1)) { ok = false; break; }
+      if (!ok) break;
+      if (!(ok = issue_pg(J - 1, nj == 1))) break;
+      mma_commit_nc(&b.o_full);
     }
-    if (ok && issue_pg(nj - 1)) mma_commit(&b.o_full);
     mma_commit(&b.drain);
     mbar_wait(&b.drain, 0, a.timeout_ns);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 2) / 4;          // 0: even source blocks, 1: odd
-    const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+    const int wg = (warp - 2) / 4;   // columns [64 wg, 64 wg + 64) of every score block
+    const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
-    const int i = i0 + row;
-    const float tau = head_tau(a.tau, a.s, head, a.err, kKernTango);
-    const float c = tau * kLog2e;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t stm = tmem + kColS0 + wg * 128 + lane_off;
-    float den = 0.f;
+    const uint32_t otm = tmem + kColO + lane_off;
     bool ok = true;
-    for (int j = wg, use = 0; j < nj; j += 2, ++use) {
-      if (!wait_bar(&b.s_full[wg], use & 1, b, a)) { ok = false; break; }
-      tc_fence_after();
-      const bool diag = (j == ib);
-#pragma unroll
-      for (int c0 = 0; c0 < kBlk; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(stm + c0, r);
-        tmem_ld_wait();
-        uint32_t p[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float w0 = ex2_approx(fmaf(c, __uint_as_float(r[e]), -c));
-          float w1 = ex2_approx(fmaf(c, __uint_as_float(r[e + 1]), -c));
-          if (diag) {
-            if (c0 + e > row) w0 = 0.f;
-            if (c0 + e + 1 > row) w1 = 0.f;
-          }
-          const uint32_t pk = pack_bf16x2(w0, w1);
-          den += bf16lo(pk) + bf16hi(pk);
-          p[e / 2] = pk;
+    uint32_t J = 0, ophase = 0;
+    TileSeq seq;
+    for (bool have = seq.first(a); ok && have; have = seq.next(a)) {
+      const Tile t = seq.t;
+      const int i = t.ib * kBlk + row;
+      const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
+      const float c = tau * kLog2e;
+      float dsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      const int nj = t.ib + 1;
+      for (int j = 0; j < nj; ++j, ++J) {
+        const uint32_t buf = J & 1;
+        const uint32_t stm = tmem + kColS0 + buf * 128 + lane_off;
+        uint32_t r[2][32];
+        if (ok) ok = wait_bar(&b.s_full[buf], (J >> 1) & 1, b, a);
+        if (ok) {
+          tc_fence_after();
+          tmem_ld32(stm + wg * 64, r[0]);
+          tmem_ld32(stm + wg * 64 + 32, r[1]);
+          tmem_ld_wait();
         }
-        tmem_st16(stm + c0 / 2, p);
+        // P overwrites the first half of the buffer: both warpgroups must have read
+        // their scores first.  The barrier also ANDs their status.
+        ok = named_bar_and(1, 256, ok);
+        if (!ok) break;
+        const int src0 = (j - t.ib) * kBlk + wg * 64;  // relative to the destination block
+        if (src0 + 63 > 0) softmax64<true>(r, stm + wg * 32, c, row, src0, dsum);
+        else softmax64<false>(r, stm + wg * 32, c, row, src0, dsum);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.p_full[buf]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&b.p_full[wg]);
-    }
-    b.rowsum[wg][row] = den;
-    named_bar_sync(1, 256);
-    den = b.rowsum[0][row] + b.rowsum[1][row];
-    if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[head] - tau) * kLog2e);
-    const float inv = 1.f / den;
-    if (ok && wait_bar(&b.o_full, 0, b, a)) {
+      // Both warpgroups hold half of each row's denominator.
+      ok = named_bar_and(1, 256, ok);
+      b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
+      named_bar_sync(1, 256);
+      float den = b.rowsum[0][row] + b.rowsum[1][row];
+      if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
+      const float inv = 1.f / den;
+      if (ok) ok = wait_bar(&b.o_full, ophase, b, a);
+      ok = named_bar_and(1, 256, ok);
+      if (!ok) break;
+      ophase ^= 1;
       tc_fence_after();
+      // This warpgroup's 128 columns, 64 at a time: O / den * v, bf16 stores.  The
+      // accumulator is released to the next tile after the last TMEM read.
       const bool row_ok = i < a.T;
-      const size_t rowoff = ((size_t)bb * a.T + (row_ok ? i : 0)) * a.m + (size_t)head * a.m_h;
-      const uint32_t otm = tmem + kColO + lane_off;
+      const size_t rowoff = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_h;
 #pragma unroll 1
-      for (int c0 = wg * 128; c0 < wg * 128 + 128; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(otm + c0, r);
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t o[2][32];
+        tmem_ld32(otm + wg * 128 + hq * 64, o[0]);
+        tmem_ld32(otm + wg * 128 + hq * 64 + 32, o[1]);
         tmem_ld_wait();
-        const int col = n0 + c0;
-        if (!row_ok || col >= a.m_h) continue;  // after the collective load
+        if (hq == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b.o_empty);
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (col + 8 * u >= a.m_h) break;
-          float y[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = __uint_as_float(r[8 * u + e]) * inv;
+        for (int q = 0; q < 2; ++q) {
+          const int col = t.n0 + wg * 128 + hq * 64 + q * 32;
+          if (!row_ok || col >= a.m_h) continue;
+          uint4 vv[4];
           if (a.v) {
-            const uint4 vv = ld_global_v4(a.v + rowoff + col + 8 * u);
-            y[0] *= bf16lo(vv.x); y[1] *= bf16hi(vv.x); y[2] *= bf16lo(vv.y); y[3] *= bf16hi(vv.y);
-            y[4] *= bf16lo(vv.z); y[5] *= bf16hi(vv.z); y[6] *= bf16lo(vv.w); y[7] *= bf16hi(vv.w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (col + 8 * e < a.m_h) vv[e] = ld_global_v4(a.v + rowoff + col + 8 * e);
           }
-          st_global_v4(a.out + rowoff + col + 8 * u, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                       pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (col + 8 * e >= a.m_h) break;
+            float y[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) y[z] = __uint_as_float(o[q][8 * e + z]) * inv;
+            if (a.v) {
+              y[0] *= bf16lo(vv[e].x); y[1] *= bf16hi(vv[e].x); y[2] *= bf16lo(vv[e].y); y[3] *= bf16hi(vv[e].y);
+              y[4] *= bf16lo(vv[e].z); y[5] *= bf16hi(vv[e].z); y[6] *= bf16lo(vv[e].w); y[7] *= bf16hi(vv[e].w);
+            }
+            st_global_v4(a.out + rowoff + col + 8 * e, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                         pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+          }
         }
       }
     }
@@ -274,6 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
 }  // namespace
 
 cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
@@ -282,22 +452,26 @@ cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
   a.d_h = p.dqk / p.H; a.m_h = p.m / p.H;
   a.n_iblk = ceil_div(p.T, kBlk);
   a.n_ntile = ceil_div(a.m_h, kNg);
+  a.n_pair = (a.n_iblk + 1) / 2;
+  const long long units = (long long)p.B * p.H * a.n_ntile * a.n_pair;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_units = (int)units;
   a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
   a.v = static_cast<const __nv_bfloat16*>(p.v);
   a.out = static_cast<__nv_bfloat16*>(p.out);
   a.err = p.err;
   a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
   a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
-  CUtensorMap mq, mk, mg;
+  CUtensorMap mq, mk, mg, mv;
   cudaError_t e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, a.d_h);
-  if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, kBlk, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, kHalf, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, kBlk, 64);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tango_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long tiles = (long long)p.B * p.H * a.n_ntile * a.n_iblk;
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  tango_tc_kernel<<<(unsigned)tiles, kThreads, kSmemBytes, s>>>(mq, mk, mg, a);
+  const int grid = a.n_units < num_sms() ? a.n_units : num_sms();
+  tango_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mg, mv, a);
   return cudaGetLastError();
 }
 
