@@ -11,24 +11,24 @@
 // (batch, head, gate tile), so every unit costs nI+1 source blocks and the units
 // of one gate tile, which share G and khat, run side by side out of L2.
 //
-//   warp 0     TMA: qhat tiles (2 buffers), khat blocks (2-stage ring), G in half
-//              blocks of 64 sources x 256 columns (5-stage ring, four 64-column boxes
-//              each); prefetches the tile's v into L2.
-//   warp 1     TMEM allocation; MMA issue from one thread:
-//                S_j = Qhat Khat_j^T   (M=128, N=128, K=d_h)     -> TMEM S[J % 2]
-//                O  += P_j G_j         (M=128, N=256, K=64 x 2)  A = P_j from TMEM
-//              J counts source blocks over all tiles of the CTA.  S_{j+1} is issued
-//              before O += P_j G_j.  The issue path keeps descriptors in registers
-//              and avoids compiler memory barriers: one thread issues 12 MMAs per
-//              block, so its per-instruction cost bounds the whole kernel.
-//   warps 2-9  softmax: warpgroup w (warps 2-5, 6-9) takes columns [64w, 64w+64) of
-//              every score block; one row per thread from TMEM, exp2(tau log2e
-//              (s - 1)) with the causal mask on the diagonal block, rounded to bf16;
-//              the ROUNDED weights are summed into the row's denominator; P (bf16) is
-//              written back over S once both warpgroups have read their scores.
-//   epilogue   the same warps after a tile's last block: O / den * v from TMEM,
-//              bf16 stores; the accumulator is released to the next tile as soon as
-//              it has been read.
+//   warp 0       TMA: qhat tiles (2 buffers), khat blocks (2-stage ring), and one ring
+//                of 32 KB stages (5 of them) that carries, per tile, G in half blocks
+//                of 64 sources x 256 columns and then the tile's v (2 stages).
+//   warp 1       TMEM allocation; MMA issue from one thread:
+//                  S_j = Qhat Khat_j^T   (M=128, N=128, K=d_h)     -> TMEM S[J % 2]
+//                  O  += P_j G_j         (M=128, N=256, K=64 x 2)  A = P_j from TMEM
+//                J counts source blocks over all tiles of the CTA.  S_{j+1} is issued
+//                before O += P_j G_j.  The issue path keeps descriptors in registers
+//                and avoids compiler memory barriers.
+//   warps 4-11   softmax: warpgroup w takes columns [64w, 64w+64) of every score block;
+//                one row per thread from TMEM, exp2(tau log2e (s - 1)) with the causal
+//                mask on the diagonal block, rounded to bf16; the ROUNDED weights are
+//                summed into the row's denominator; P (bf16) is written back over S
+//                once both warpgroups have read their scores.
+//   warps 12-15  epilogue: O / den from TMEM times v from shared memory; u is written
+//                over v in shared memory and stored by TMA, while the softmax warps
+//                already work on the next tile.  (A 64-column box that straddles the
+//                end of a head's gate columns is written directly instead.)
 // TMEM: O in columns [0, 256), S[0] in [256, 384), S[1] in [384, 512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -41,14 +41,15 @@ namespace {
 using namespace ptx;
 
 constexpr int kBlk = 128;      // destinations per tile; sources per score block
-constexpr int kHalf = 64;      // sources per G stage
+constexpr int kHalf = 64;      // rows per ring stage
 constexpr int kNg = 256;       // gate columns per tile
 constexpr int kQBufs = 2;
 constexpr int kKStages = 2;
 constexpr int kGStages = 5;
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 512;  // 16 warps
+constexpr int kSoftWarp0 = 4, kEpiWarp0 = 12;
 constexpr uint32_t kQKMax = kBlk * 64 * 2;     // 16 KB at d_h = 64
-constexpr uint32_t kGBox = kHalf * 64 * 2;     // 8 KB: 64 sources x 64 columns
+constexpr uint32_t kGBox = kHalf * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;        // 32 KB
 constexpr uint32_t kColO = 0, kColS0 = 256;
 
@@ -57,7 +58,7 @@ struct __align__(8) Bars {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t g_full[kGStages], g_empty[kGStages];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_full, o_empty;
+  uint64_t o_full, o_empty, den_full, den_empty;
   uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
@@ -73,7 +74,7 @@ struct Args {
   float s;
   const float* tau;
   const float* null_bias;
-  const __nv_bfloat16* v;
+  int has_v;
   __nv_bfloat16* out;
   unsigned* err;
   uint64_t timeout_ns;
@@ -135,12 +136,6 @@ __device__ __forceinline__ uint32_t qk_layout(int d_h) {
   return d_h == 64 ? kSwizzle128B : d_h == 32 ? kSwizzle64B : kSwizzle32B;
 }
 
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
-               "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // 64 scores of one row (columns [64w, 64w+64) of a block): weights exp2(c (s - 1)),
 // with sources after the destination zeroed on the diagonal block, rounded to bf16
 // and written as P at TMEM columns [32w, 32w+32) of the score buffer; the rounded
@@ -167,6 +162,15 @@ __device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p
   }
 }
 
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t o_lo, uint32_t o_hi, uint32_t v, float inv, bool has_v) {
+  float y0 = __uint_as_float(o_lo) * inv, y1 = __uint_as_float(o_hi) * inv;
+  if (has_v) {
+    y0 *= bf16lo(v);
+    y1 *= bf16hi(v);
+  }
+  return pack_bf16x2(y0, y1);
+}
+
 // Ring position: stage index and the parity of its current phase.
 struct Ring {
   int stage = 0;
@@ -179,7 +183,7 @@ struct Ring {
 __global__ void __launch_bounds__(kThreads, 1)
     tango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
-                    const Args a) {
+                    const __grid_constant__ CUtensorMap tmU, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
@@ -207,7 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b.p_full[i], 8);
     }
     mbar_init(&b.o_full, 1);
-    mbar_init(&b.o_empty, 8);
+    mbar_init(&b.o_empty, 4);
+    mbar_init(&b.den_full, 8);
+    mbar_init(&b.den_empty, 4);
     mbar_init(&b.drain, 1);
     mbar_init(&b.never, 1);
     b.abort = 0;
@@ -229,6 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qmask = 0, kmask = 0, gmask = 0, qph[kQBufs] = {}, kph[kKStages] = {}, gph[kGStages] = {};
     TileSeq seq;
     int tc = 0;
+    auto ring_load = [&](const CUtensorMap* map, int x, int y, int bb) -> bool {
+      if (!wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a)) return false;
+      uint8_t* dst = sG + gr.stage * kGStage;
+      if (map) {
+        mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_load_3d(dst + c * kGBox, map, &b.g_full[gr.stage], x + 64 * c, y, bb);
+        gmask |= 1u << gr.stage;
+        gph[gr.stage] = gr.phase;
+      } else {
+        mbar_arrive(&b.g_full[gr.stage]);
+      }
+      gr.next(kGStages);
+      return true;
+    };
     for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
       const Tile& t = seq.t;
       const int i0 = t.ib * kBlk, qb = tc & 1;
@@ -238,8 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sQ + qb * kQKMax, &tmQ, &b.q_full[qb], t.head * a.d_h, i0, t.b);
       qmask |= 1u << qb;
       qph[qb] = qp;
-      if (a.v)
-        for (int c = 0; c < kNg; c += 64) tma_prefetch_l2_3d(&tmV, t.head * a.m_h + t.n0 + c, i0, t.b);
       const int gx = t.head * a.m_h + t.n0;
       for (int j = 0; ok && j <= t.ib; ++j) {
         if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
@@ -248,18 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         kmask |= 1u << kr.stage;
         kph[kr.stage] = kr.phase;
         kr.next(kKStages);
-        for (int h = 0; h < 2; ++h) {
-          if (!(ok = wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a))) break;
-          uint8_t* dst = sG + gr.stage * kGStage;
-          mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(dst + c * kGBox, &tmG, &b.g_full[gr.stage], gx + 64 * c, j * kBlk + h * kHalf, t.b);
-          gmask |= 1u << gr.stage;
-          gph[gr.stage] = gr.phase;
-          gr.next(kGStages);
-        }
+        for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, j * kBlk + h * kHalf, t.b);
       }
+      // the tile's v, rows [i0, i0+64) and [i0+64, i0+128), for the epilogue
+      for (int h = 0; ok && h < 2; ++h) ok = ring_load(a.has_v ? &tmV : nullptr, gx, i0 + h * kHalf, t.b);
     }
     // Copies still in flight land before the CTA exits.
     for (int s = 0; s < kQBufs; ++s)
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ophase = 0;
     uint32_t J = 0;  // source blocks issued by this CTA
     // O += P_jj G_jj (two half blocks); the tile's first block overwrites O once the
-    // previous tile's epilogue has read the accumulator out of TMEM.
+    // epilogue has read the previous tile's accumulator out of TMEM.
     auto issue_pg = [&](uint32_t jj, bool first) -> bool {
       const uint32_t buf = jj & 1;
       if (!wait_bar(&b.p_full[buf], (jj >> 1) & 1, b, a)) return false;
@@ -332,22 +343,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!(ok = issue_pg(J - 1, nj == 1))) break;
       mma_commit_nc(&b.o_full);
+      gr.next(kGStages);  // the tile's two v stages belong to the epilogue
+      gr.next(kGStages);
     }
     mma_commit(&b.drain);
     mbar_wait(&b.drain, 0, a.timeout_ns);
-  } else if (warp >= 2) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 2) / 4;   // columns [64 wg, 64 wg + 64) of every score block
-    const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
+  } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int wg = (warp - kSoftWarp0) / 4;  // columns [64 wg, 64 wg + 64) of every block
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t otm = tmem + kColO + lane_off;
     bool ok = true;
-    uint32_t J = 0, ophase = 0;
+    uint32_t J = 0;
+    int tc = 0;
     TileSeq seq;
-    for (bool have = seq.first(a); ok && have; have = seq.next(a)) {
+    for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
       const Tile t = seq.t;
-      const int i = t.ib * kBlk + row;
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       const float c = tau * kLog2e;
       float dsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
@@ -375,57 +387,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&b.p_full[buf]);
       }
-      // Both warpgroups hold half of each row's denominator.
-      ok = named_bar_and(1, 256, ok);
+      if (!ok) break;
+      // Hand this warpgroup's half of the row denominators to the epilogue.
+      if (!(ok = wait_bar(&b.den_empty, ((tc & 1) ^ 1), b, a))) break;
       b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
-      named_bar_sync(1, 256);
-      float den = b.rowsum[0][row] + b.rowsum[1][row];
-      if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
-      const float inv = 1.f / den;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.den_full);
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t otm = tmem + kColO + ((uint32_t)(quarter * 32) << 16);
+    const bool issuer = (warp == kEpiWarp0 && lane == 0);
+    bool ok = true;
+    uint32_t ophase = 0;
+    int gpos = 0;  // ring stages consumed so far (G and v)
+    int tc = 0;
+    TileSeq seq;
+    for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
+      const Tile t = seq.t;
+      const int i = t.ib * kBlk + row;
+      gpos += 2 * (t.ib + 1);
+      const int sa = gpos % kGStages, sb = (gpos + 1) % kGStages;
+      const uint32_t pa = (gpos / kGStages) & 1, pb = ((gpos + 1) / kGStages) & 1;
+      gpos += 2;
+      float den = 0.f;
+      if (ok) ok = wait_bar(&b.den_full, tc & 1, b, a);
+      if (ok) {
+        den = b.rowsum[0][row] + b.rowsum[1][row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.den_empty);
+      }
       if (ok) ok = wait_bar(&b.o_full, ophase, b, a);
-      ok = named_bar_and(1, 256, ok);
+      if (ok) ok = wait_bar(&b.g_full[sa], pa, b, a);
+      if (ok) ok = wait_bar(&b.g_full[sb], pb, b, a);
+      ok = named_bar_and(2, 128, ok);
       if (!ok) break;
       ophase ^= 1;
+      const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
+      if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
+      const float inv = 1.f / den;
       tc_fence_after();
-      // This warpgroup's 128 columns, 64 at a time: O / den * v, bf16 stores.  The
-      // accumulator is released to the next tile after the last TMEM read.
       const bool row_ok = i < a.T;
-      const size_t rowoff = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_h;
+      const int rr = row & 63;
+      const uint32_t vrow = smem_u32(sG + (row < 64 ? sa : sb) * kGStage) + rr * 128;
+      const size_t grow = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_h;
 #pragma unroll 1
-      for (int hq = 0; hq < 2; ++hq) {
+      for (int cq = 0; cq < 4; ++cq) {
         uint32_t o[2][32];
-        tmem_ld32(otm + wg * 128 + hq * 64, o[0]);
-        tmem_ld32(otm + wg * 128 + hq * 64 + 32, o[1]);
+        tmem_ld32(otm + cq * 64, o[0]);
+        tmem_ld32(otm + cq * 64 + 32, o[1]);
         tmem_ld_wait();
-        if (hq == 1) {
+        if (cq == 3) {  // the accumulator is free for the next tile
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&b.o_empty);
         }
+        const int col0 = t.n0 + cq * 64;
+        const bool straddle = col0 < a.m_h && col0 + 64 > a.m_h;
+        const uint32_t box = vrow + cq * kGBox;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int col = t.n0 + wg * 128 + hq * 64 + q * 32;
-          if (!row_ok || col >= a.m_h) continue;
-          uint4 vv[4];
-          if (a.v) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (col + 8 * e < a.m_h) vv[e] = ld_global_v4(a.v + rowoff + col + 8 * e);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (col + 8 * e >= a.m_h) break;
-            float y[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z) y[z] = __uint_as_float(o[q][8 * e + z]) * inv;
-            if (a.v) {
-              y[0] *= bf16lo(vv[e].x); y[1] *= bf16hi(vv[e].x); y[2] *= bf16lo(vv[e].y); y[3] *= bf16hi(vv[e].y);
-              y[4] *= bf16lo(vv[e].z); y[5] *= bf16hi(vv[e].z); y[6] *= bf16lo(vv[e].w); y[7] *= bf16hi(vv[e].w);
-            }
-            st_global_v4(a.out + rowoff + col + 8 * e, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                         pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
+          const uint4 vv = a.has_v ? ld_shared_v4(addr) : make_uint4(0, 0, 0, 0);
+          const uint32_t* ok8 = &o[k >> 2][(k & 3) * 8];
+          uint4 uu;
+          uu.x = mul_bf16x2(ok8[0], ok8[1], vv.x, inv, a.has_v);
+          uu.y = mul_bf16x2(ok8[2], ok8[3], vv.y, inv, a.has_v);
+          uu.z = mul_bf16x2(ok8[4], ok8[5], vv.z, inv, a.has_v);
+          uu.w = mul_bf16x2(ok8[6], ok8[7], vv.w, inv, a.has_v);
+          if (!straddle) {
+            st_shared_v4(addr, uu);
+          } else if (row_ok && col0 + 8 * k < a.m_h) {
+            st_global_v4(a.out + grow + col0 + 8 * k, uu.x, uu.y, uu.z, uu.w);
           }
         }
+      }
+      // u is in shared memory; one thread stores the whole 64-column boxes.
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      if (issuer) {
+        for (int h = 0; h < 2; ++h) {
+          const int y = t.ib * kBlk + h * kHalf;
+          if (y >= a.T) continue;
+          for (int cq = 0; cq < 4; ++cq) {
+            const int col0 = t.n0 + cq * 64;
+            if (col0 + 64 > a.m_h) continue;
+            tma_store_3d(&tmU, sG + (h == 0 ? sa : sb) * kGStage + cq * kGBox, t.head * a.m_h + col0, y, t.b);
+          }
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&b.g_empty[sa]);
+        mbar_arrive(&b.g_empty[sb]);
       }
     }
   }
@@ -457,21 +512,22 @@ cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.n_units = (int)units;
   a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
-  a.v = static_cast<const __nv_bfloat16*>(p.v);
+  a.has_v = p.v != nullptr;
   a.out = static_cast<__nv_bfloat16*>(p.out);
   a.err = p.err;
   a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
   a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
-  CUtensorMap mq, mk, mg, mv;
+  CUtensorMap mq, mk, mg, mv, mu;
   cudaError_t e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, a.d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, kHalf, 64);
-  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, kBlk, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, kHalf, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, kHalf, 64);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tango_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < num_sms() ? a.n_units : num_sms();
-  tango_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mg, mv, a);
+  tango_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mg, mv, mu, a);
   return cudaGetLastError();
 }
 
