@@ -388,8 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&b.p_full[buf]);
       }
       if (!ok) break;
-      // Hand this warpgroup's half of the row denominators to the epilogue.
-      if (!(ok = wait_bar(&b.den_empty, ((tc & 1) ^ 1), b, a))) break;
+      // Hand this warpgroup's half of the row denominators to the epilogue.  Both
+      // warpgroups agree on the status before either goes on.
+      if (ok) ok = wait_bar(&b.den_empty, ((tc & 1) ^ 1), b, a);
+      ok = named_bar_and(1, 256, ok);
+      if (!ok) break;
       b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.den_full);

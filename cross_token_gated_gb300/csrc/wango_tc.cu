@@ -1,0 +1,738 @@
+// WANGO windowed gate aggregation on the tensor cores (tcgen05), "TANGO:
+// Token-Aggregated Nonlinear Gating Operators ...", sec. 2.2 eqs. 7-10 in sec. 2.1
+// eq. 5.  For destination i and head a (all weights carry the common factor e^-tau,
+// which cancels in the ratio):
+//   window  i-W < j <= i :  w_ij = exp(tau (qhat_i.khat_j - 1))                (eq. 6)
+//   older   j <= i-W     :  w_ij = e^-tau phi(sqrt(tau) qhat_i).phi(sqrt(tau) khat_j) (eq. 9)
+//   u_i = [sum_j w_ij g_j] / [sum_j w_ij + (i+1) e^{b-tau}] * v_i
+// The older sources enter through the running sums of eq. 10,
+//   S = sum phi(k~_j) g_j^T (d_h x gate columns),   z = sum phi(k~_j),
+// with read-outs  e^-tau phi(q~_i)^T S  and  e^-tau phi(q~_i)^T z.
+//
+// One CTA walks, in order, the 128-row destination blocks ib of one (batch, head,
+// 128-column gate tile) -- a "strip"; persistent CTAs take strips round-robin.  For
+// destination block ib the per-pair sources are the 128-source blocks
+//   jb = jlo(ib) .. ib,   jlo(ib) = floor(max(0, 128 ib - W + 1) / 128),
+// and the state holds every source j < 128 jlo(ib), which is older than the window
+// for every destination of the block.  A block jb is "mixed" when it also holds
+// older pairs (128 jb <= 128 ib + 127 - W): its weights need both scores.  A block
+// "leaves" when jb < jlo(ib + 1): after its P.G MMA the same G tile updates the state.
+//
+// Roles (16 warps, 512 threads):
+//   warp 0       TMA: qhat (1 buffer), khat (2-stage ring), and a 3-stage ring of
+//                32 KB stages carrying G blocks (128 sources x 128 columns) and, after a
+//                destination block's sources, its v tile for the epilogue.
+//   warp 1       MMA issue (one thread), per destination block:
+//                  O  = e^-tau Phi(Q~) S_bf16           (M=128, N=128, K=d_h), read-out
+//                  for each source block: Sc = Qhat Khat^T (f32 -> slot), mixed blocks
+//                  also Sf = e^-tau Phi(Q~) Phi(K~)^T (-> second slot); O += P G;
+//                  leaving blocks: S^T += G^T Phi(K~)  (M=128, N=d_h, K=128) in TMEM.
+//   warps 2-3    feature maps on the CUDA cores: Phi(Q~) (scaled by e^-tau) and the
+//                older-prefix denominator e^-tau phi(q~).z per row; Phi(K~) of mixed and
+//                leaving blocks, and z += sum phi(k~) over leaving blocks.
+//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of each block; the
+//                row's weight per pair is exp (window), the feature-map score (older),
+//                or 0 (after i); rounded to bf16, summed into the row's denominator,
+//                written as P over the score slot.
+//   warps 12-15  the state copy S^T (TMEM, f32) -> S (shared memory, bf16) for the next
+//                read-out; the epilogue O / den * v with u stored by TMA.
+// TMEM: O [0,128), S^T [128, 128+d_h), score slots [256,384) and [384,512).
+#include "tg_common.cuh"
+#include "tg_ptx.cuh"
+#include "tg_tc.h"
+#include "tg_tma.h"
+
+namespace tg {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBlk = 128;
+constexpr int kNg = 128;       // gate columns per strip
+constexpr int kKStages = 2;
+constexpr int kGStages = 3;
+constexpr int kThreads = 512;
+constexpr int kPhiWarp0 = 2, kSoftWarp0 = 4, kEpiWarp0 = 12;
+constexpr uint32_t kTile = kBlk * 64 * 2;   // 16 KB: a 128 x d_h bf16 tile at d_h = 64
+constexpr uint32_t kGBox = 64 * 64 * 2;     // 8 KB: 64 rows x 64 columns
+constexpr uint32_t kGStage = 4 * kGBox;     // 32 KB: 128 rows x 128 columns
+constexpr uint32_t kColO = 0, kColSt = 128, kColSlot0 = 256;
+
+struct __align__(8) Bars {
+  uint64_t q_full, q_empty;                     // qhat tile: MMA + phi warps consume
+  uint64_t fq_full, fq_empty;                   // Phi(Q~) tile
+  uint64_t k_full[kKStages], k_empty[kKStages]; // khat tiles: MMA + phi warps consume
+  uint64_t fk_full[2], fk_empty[2];             // Phi(K~) tiles (mixed / leaving blocks)
+  uint64_t g_full[kGStages], g_empty[kGStages];
+  uint64_t s_full[2], p_full[2];                // score slots; P of source blocks
+  uint64_t o_full, o_empty;
+  uint64_t st_full;                             // S^T updates of a destination block done
+  uint64_t sb_full, sb_empty;                   // bf16 state copy for the read-out
+  uint64_t den_full, den_empty;                 // P row sums -> epilogue
+  uint64_t dold_full[2], dold_empty[2];         // older-prefix denominators -> epilogue
+  uint64_t drain, never;
+  uint32_t tmem_base;
+  int abort;
+  float rowsum[2][kBlk];
+  float dold[2][kBlk];
+  float z[2][64];
+};
+
+// smem: Q | PhiQ | K[2] | PhiK[2] | S_bf16 | G ring | Bars
+constexpr size_t kSmemBytes = 1024 + kTile * 7 + kGStage * kGStages + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Args {
+  int B, T, H, dqk, m, d_h, m_h, W, phi_mode;
+  int n_iblk, n_ntile, n_strips;
+  float s;
+  const float* tau;
+  const float* null_bias;
+  int has_v;
+  __nv_bfloat16* out;
+  unsigned* err;
+  uint64_t timeout_ns;
+  int debug_timeout;
+};
+
+__device__ __forceinline__ int jlo_of(int ib, int W) {
+  const int lo = ib * kBlk - W + 1;
+  return lo > 0 ? lo / kBlk : 0;
+}
+__device__ __forceinline__ bool is_mixed(int jb, int ib, int W) { return jb * kBlk <= ib * kBlk + kBlk - 1 - W; }
+__device__ __forceinline__ bool is_leaving(int jb, int ib, int W) { return jb < jlo_of(ib + 1, W); }
+
+struct Strip {
+  int b, head, n0;
+};
+__device__ __forceinline__ Strip strip_of(const Args& a, int s) {
+  Strip r;
+  r.n0 = (s % a.n_ntile) * kNg;
+  r.head = (s / a.n_ntile) % a.H;
+  r.b = s / (a.n_ntile * a.H);
+  return r;
+}
+
+__device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+  if (*(volatile int*)&b.abort) return false;
+  if (mbar_wait(bar, parity, a.timeout_ns)) return true;
+  *(volatile int*)&b.abort = 1;
+  record_error(a.err, kErrTimeout | kKernWango);
+  return false;
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+  if (mbar_try_wait_nc(smem_u32(bar), parity)) return true;
+  return wait_slow(bar, parity, b, a);
+}
+
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++stage == n) { stage = 0; phase ^= 1; }
+  }
+};
+
+// Byte offset of element column c (16-bit elements) of row r in a tile whose rows
+// are RB bytes wide, stored with the matching TMA/UMMA swizzle (RB = 32, 64, 128).
+template <int RB>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  const uint32_t off = (uint32_t)(r * RB + c * 2);
+  constexpr uint32_t mask = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
+  return off ^ (((off >> 7) & mask) << 4);
+}
+
+// Feature map of eq. 8 (mode 0) or plain ELU + 1 (mode 1).
+__device__ __forceinline__ float phi_map(float u, float inv_sqrt_dh, int mode) {
+  const float elu = u > 0.f ? u : expm1f(u);
+  if (mode == 1) return elu + 1.f;
+  return fmaxf(elu + 1.f + 1e-4f, 1e-4f) * inv_sqrt_dh;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kThreads, 1)
+    wango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmU, const Args a) {
+  constexpr int RB = DH * 2;  // bytes per row of the q/k/feature tiles
+  constexpr uint32_t lay = DH == 64 ? kSwizzle128B : DH == 32 ? kSwizzle64B : kSwizzle32B;
+  constexpr uint32_t sbo = 8u * RB;
+  constexpr uint32_t tile_bytes = kBlk * RB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sFQ = sQ + kTile;
+  uint8_t* sK = sFQ + kTile;           // 2 stages
+  uint8_t* sFK = sK + 2 * kTile;       // 2 stages
+  uint8_t* sSB = sFK + 2 * kTile;      // bf16 state, [128 gate rows x d_h]
+  uint8_t* sG = sSB + kTile;
+  Bars& b = *reinterpret_cast<Bars*>(sG + kGStages * kGStage);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&b.q_full, 1);
+    mbar_init(&b.q_empty, 3);   // MMA commit + both feature-map warps
+    mbar_init(&b.fq_full, 2);
+    mbar_init(&b.fq_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&b.k_full[s], 1);
+      mbar_init(&b.k_empty[s], 3);  // MMA commit + both feature-map warps
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&b.fk_full[s], 2);
+      mbar_init(&b.fk_empty[s], 1);
+      mbar_init(&b.s_full[s], 1);
+      mbar_init(&b.p_full[s], 8);
+      mbar_init(&b.dold_full[s], 2);
+      mbar_init(&b.dold_empty[s], 4);
+    }
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&b.g_full[s], 1);
+      mbar_init(&b.g_empty[s], 1);
+    }
+    mbar_init(&b.o_full, 1);
+    mbar_init(&b.o_empty, 4);
+    mbar_init(&b.st_full, 1);
+    mbar_init(&b.sb_full, 4);
+    mbar_init(&b.sb_empty, 1);
+    mbar_init(&b.den_full, 8);
+    mbar_init(&b.den_empty, 4);
+    mbar_init(&b.drain, 1);
+    mbar_init(&b.never, 1);
+    b.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&b.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b.tmem_base;
+  const int W = a.W;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    Ring kr, gr;
+    bool ok = true;
+    uint32_t qph = 0, kmask = 0, gmask = 0, kph[kKStages] = {}, gph[kGStages] = {};
+    bool q_issued = false;
+    auto ring_load = [&](const CUtensorMap* map, int x, int y, int bb) -> bool {
+      if (!wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a)) return false;
+      uint8_t* dst = sG + gr.stage * kGStage;
+      if (map) {
+        mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(dst + h * 2 * kGBox + c * kGBox, map, &b.g_full[gr.stage], x + 64 * c, y + 64 * h, bb);
+        gmask |= 1u << gr.stage;
+        gph[gr.stage] = gr.phase;
+      } else {
+        mbar_arrive(&b.g_full[gr.stage]);
+      }
+      gr.next(kGStages);
+      return true;
+    };
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      const Strip sp = strip_of(a, st);
+      const int gx = sp.head * a.m_h + sp.n0;
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
+        if (!(ok = wait_bar(&b.q_empty, qph ^ 1, b, a))) break;
+        mbar_arrive_expect_tx(&b.q_full, tile_bytes);
+        tma_load_3d(sQ, &tmQ, &b.q_full, sp.head * DH, ib * kBlk, sp.b);
+        q_issued = true;
+        qph ^= 1;
+        for (int jb = jlo_of(ib, W); ok && jb <= ib; ++jb) {
+          if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
+          mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
+          tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
+          kmask |= 1u << kr.stage;
+          kph[kr.stage] = kr.phase;
+          kr.next(kKStages);
+          ok = ring_load(&tmG, gx, jb * kBlk, sp.b);
+        }
+        if (ok) ok = ring_load(a.has_v ? &tmV : nullptr, gx, ib * kBlk, sp.b);
+      }
+    }
+    if (q_issued) mbar_wait(&b.q_full, qph ^ 1, a.timeout_ns);
+    for (int s = 0; s < kKStages; ++s)
+      if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
+    for (int s = 0; s < kGStages; ++s)
+      if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);   // scores
+    constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);     // O += P G
+    constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);    // O = Phi(Q) S
+    constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);       // S^T += G^T Phi(K)
+    const uint64_t qd = smem_desc(smem_u32(sQ), 16, sbo, lay);
+    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
+    const uint64_t kd0 = smem_desc(smem_u32(sK), 16, sbo, lay);
+    const uint64_t fkd0 = smem_desc(smem_u32(sFK), 16, sbo, lay);
+    const uint64_t fkd_mn0 = smem_desc(smem_u32(sFK), tile_bytes, sbo, lay);  // Phi(K~) as MN-major B
+    const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
+    const uint64_t gd0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
+    bool ok = true;
+    if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
+    Ring kr, gr;
+    int fkstage = 0;
+    uint32_t fkphase = 0, qph = 0, oph = 0, sbph = 0;
+    uint32_t slot = 0;       // score slots used so far (ring of 2)
+    uint32_t blk = 0;        // source blocks processed so far (p_full ring of 2)
+    bool first_update = true;
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      first_update = true;
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
+        if (!(ok = wait_bar(&b.q_full, qph, b, a))) break;
+        if (!(ok = wait_bar(&b.fq_full, qph, b, a))) break;
+        qph ^= 1;
+        // the previous destination block's accumulator has been read; the bf16 state
+        // copy for this block is in place
+        if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
+        if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+        oph ^= 1;
+        sbph ^= 1;
+        tc_fence_after_nc();
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_bf16_ss_nc(tmem + kColO, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, kk != 0);
+        mma_commit_nc(&b.sb_empty);
+        const int jlo = jlo_of(ib, W);
+        bool updated = false;
+        for (int jb = jlo; ok && jb <= ib; ++jb) {
+          const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
+          const bool need_fk = mixed || leaving;
+          if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
+          tc_fence_after_nc();
+          const uint64_t kd = kd0 + (uint64_t)((kr.stage * kTile) >> 4);
+          const uint32_t sc = tmem + kColSlot0 + (slot & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk)
+            mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+          mma_commit_nc(&b.k_empty[kr.stage]);
+          mma_commit_nc(&b.s_full[slot & 1]);
+          kr.next(kKStages);
+          const uint32_t pslot = slot;
+          ++slot;
+          if (need_fk) {
+            if (!(ok = wait_bar(&b.fk_full[fkstage], fkphase, b, a))) break;
+            tc_fence_after_nc();
+          }
+          if (mixed) {
+            const uint32_t sf = tmem + kColSlot0 + (slot & 1) * 128;
+            const uint64_t fkd = fkd0 + (uint64_t)((fkstage * kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk)
+              mma_bf16_ss_nc(sf, fqd + (uint64_t)(kk * 2), fkd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+            mma_commit_nc(&b.s_full[slot & 1]);
+            ++slot;
+          }
+          // O += P G  (P in the block's cos slot)
+          if (!(ok = wait_bar(&b.p_full[blk & 1], (blk >> 1) & 1, b, a))) break;
+          ++blk;
+          if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
+          tc_fence_after_nc();
+          const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
+          const uint32_t ptm = tmem + kColSlot0 + (pslot & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
+            mma_bf16_ts_nc(tmem + kColO, ptm + kk * 8, gd + (uint64_t)(goff >> 4), idesc_o, 1u);
+          }
+          if (leaving) {
+            // S^T += G^T Phi(K~): A = G (MN-major), B = Phi(K~) (MN-major)
+            const uint64_t fkmn = fkd_mn0 + (uint64_t)((fkstage * kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBlk / 16; ++kk) {
+              const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
+              mma_bf16_ss_nc(tmem + kColSt, gd + (uint64_t)(goff >> 4), fkmn + (uint64_t)((kk * 16 * RB) >> 4),
+                             idesc_u, (first_update && kk == 0) ? 0u : 1u);
+            }
+            first_update = false;
+            updated = true;
+          }
+          mma_commit_nc(&b.g_empty[gr.stage]);
+          gr.next(kGStages);
+          if (need_fk) {
+            mma_commit_nc(&b.fk_empty[fkstage]);
+            if (++fkstage == 2) { fkstage = 0; fkphase ^= 1; }
+          }
+        }
+        if (!ok) break;
+        (void)updated;
+        mma_commit_nc(&b.st_full);   // the state now holds every source leaving at ib
+        mma_commit_nc(&b.q_empty);
+        mma_commit_nc(&b.fq_empty);
+        mma_commit_nc(&b.o_full);
+        gr.next(kGStages);           // the v stage belongs to the epilogue
+      }
+    }
+    mma_commit(&b.drain);
+    mbar_wait(&b.drain, 0, a.timeout_ns);
+  } else if (warp >= kPhiWarp0 && warp < kSoftWarp0) {
+    // ------------------------------------------------------------ feature maps
+    const int pt = threadIdx.x - kPhiWarp0 * 32;  // 0..63: rows pt and pt + 64; z dim pt
+    const float inv_sqrt_dh = rsqrtf((float)DH);
+    bool ok = true;
+    uint32_t qph = 0;
+    Ring kr;
+    int fkstage = 0;
+    uint32_t fkphase = 0;
+    int gib = 0;  // destination blocks done by this CTA
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      const Strip sp = strip_of(a, st);
+      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
+      const float sq = sqrtf(tau), shift = exp2f(-tau * kLog2e);
+      // the state of a new strip is empty
+      if (pt < DH) b.z[0][pt] = 0.f;
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
+        const int zc = ib & 1;
+        if (ok) ok = wait_bar(&b.q_full, qph, b, a);
+        if (ok) ok = wait_bar(&b.fq_empty, qph ^ 1, b, a);
+        if (ok) ok = wait_bar(&b.dold_empty[gib & 1], ((gib >> 1) & 1) ^ 1, b, a);
+        // both warps agree on the status; the barrier also completes z of this block
+        ok = named_bar_and(3, 64, ok);
+        if (!ok) break;
+        qph ^= 1;
+        for (int h = 0; h < 2; ++h) {
+          const int r = pt + 64 * h;
+          float dot = 0.f;
+#pragma unroll
+          for (int c = 0; c < DH; c += 8) {
+            const uint32_t off = swz<RB>(r, c);
+            const uint4 qv = ld_shared_v4(smem_u32(sQ) + off);
+            const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float f0 = shift * phi_map(sq * bf16lo(w[e]), inv_sqrt_dh, a.phi_mode);
+              const float f1 = shift * phi_map(sq * bf16hi(w[e]), inv_sqrt_dh, a.phi_mode);
+              o[e] = pack_bf16x2(f0, f1);
+              dot = fmaf(bf16lo(o[e]), b.z[zc][c + 2 * e], dot);
+              dot = fmaf(bf16hi(o[e]), b.z[zc][c + 2 * e + 1], dot);
+            }
+            st_shared_v4(smem_u32(sFQ) + off, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+          b.dold[gib & 1][r] = dot;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&b.fq_full);
+          mbar_arrive(&b.q_empty);
+          mbar_arrive(&b.dold_full[gib & 1]);
+        }
+        // the next block's z starts from this one's
+        if (pt < DH) b.z[zc ^ 1][pt] = b.z[zc][pt];
+        const int jlo = jlo_of(ib, W);
+        for (int jb = jlo; ok && jb <= ib; ++jb) {
+          const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
+          if (ok) ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a);
+          if (ok && (mixed || leaving)) ok = wait_bar(&b.fk_empty[fkstage], fkphase ^ 1, b, a);
+          ok = named_bar_and(3, 64, ok);
+          if (!ok) break;
+          if (mixed || leaving) {
+            uint8_t* fk = sFK + fkstage * kTile;
+            const uint8_t* kt = sK + kr.stage * kTile;
+            for (int h = 0; h < 2; ++h) {
+              const int r = pt + 64 * h;
+#pragma unroll
+              for (int c = 0; c < DH; c += 8) {
+                const uint32_t off = swz<RB>(r, c);
+                const uint4 kv = ld_shared_v4(smem_u32(kt) + off);
+                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  o[e] = pack_bf16x2(phi_map(sq * bf16lo(w[e]), inv_sqrt_dh, a.phi_mode),
+                                     phi_map(sq * bf16hi(w[e]), inv_sqrt_dh, a.phi_mode));
+                st_shared_v4(smem_u32(fk) + off, make_uint4(o[0], o[1], o[2], o[3]));
+              }
+            }
+            if (leaving) {
+              // z += sum over the block's valid sources of phi(k~) (the bf16 values the
+              // state update multiplies, so numerator and denominator agree)
+              named_bar_sync(3, 64);
+              if (pt < DH) {
+                float zs = 0.f;
+                const int nrows = min(kBlk, a.T - jb * kBlk);
+                for (int r = 0; r < nrows; ++r) {
+                  const uint32_t v2 = *reinterpret_cast<const uint32_t*>(fk + (swz<RB>(r, pt & ~1)));
+                  zs += (pt & 1) ? bf16hi(v2) : bf16lo(v2);
+                }
+                b.z[zc ^ 1][pt] += zs;
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b.fk_full[fkstage]);
+            if (++fkstage == 2) { fkstage = 0; fkphase ^= 1; }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b.k_empty[kr.stage]);
+          kr.next(kKStages);
+        }
+      }
+    }
+  } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
+    // ------------------------------------------------------------ weights
+    const int wg = (warp - kSoftWarp0) / 4;  // sources [64 wg, 64 wg + 64) of each block
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    uint32_t slot = 0, blk = 0;
+    int gib = 0;
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      const Strip sp = strip_of(a, st);
+      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
+      const float c = tau * kLog2e;
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
+        const int i = ib * kBlk + row;
+        float dsum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int jb = jlo_of(ib, W); jb <= ib; ++jb) {
+          const bool mixed = is_mixed(jb, ib, W);
+          const uint32_t cs = slot;
+          const uint32_t sc = tmem + kColSlot0 + (cs & 1) * 128 + lane_off + wg * 64;
+          uint32_t r[2][32], f[2][32];
+          if (ok) ok = wait_bar(&b.s_full[cs & 1], (cs >> 1) & 1, b, a);
+          if (ok && mixed) ok = wait_bar(&b.s_full[(cs + 1) & 1], ((cs + 1) >> 1) & 1, b, a);
+          if (ok) {
+            tc_fence_after();
+            tmem_ld32(sc, r[0]);
+            tmem_ld32(sc + 32, r[1]);
+            if (mixed) {
+              const uint32_t sf = tmem + kColSlot0 + ((cs + 1) & 1) * 128 + lane_off + wg * 64;
+              tmem_ld32(sf, f[0]);
+              tmem_ld32(sf + 32, f[1]);
+            }
+            tmem_ld_wait();
+          }
+          slot += mixed ? 2 : 1;
+          // P overwrites the first half of the cos slot: both warpgroups must have
+          // read their scores first.  The barrier also ANDs their status.
+          ok = named_bar_and(1, 256, ok);
+          if (!ok) break;
+          const int j0 = jb * kBlk + wg * 64;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t p[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float w[2];
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const int j = j0 + q * 32 + e + z;
+                float x = 0.f;
+                if (j <= i) {
+                  if (j >= i - W + 1) x = ex2_approx(fmaf(c, __uint_as_float(r[q][e + z]), -c));
+                  else x = __uint_as_float(f[q][e + z]);
+                }
+                w[z] = x;
+              }
+              const uint32_t pk = pack_bf16x2(w[0], w[1]);
+              dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
+              p[e / 2] = pk;
+            }
+            tmem_st16(sc - wg * 64 + wg * 32 + q * 16, p);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b.p_full[blk & 1]);
+          ++blk;
+        }
+        if (!ok) break;
+        if (ok) ok = wait_bar(&b.den_empty, ((gib & 1) ^ 1), b, a);
+        ok = named_bar_and(1, 256, ok);
+        if (!ok) break;
+        b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.den_full);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ state copy + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // destination row; also the gate column of S^T
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool issuer = (warp == kEpiWarp0 && lane == 0);
+    bool ok = true;
+    uint32_t oph = 0, stph = 0, sbph = 0;
+    int gpos = 0, gib = 0;
+    // bf16 copy of the state for the read-out of destination block ib (zero until the
+    // first source has left the window)
+    auto copy_state = [&](bool empty) -> bool {
+      if (!wait_bar(&b.sb_empty, sbph ^ 1, b, a)) return false;
+      sbph ^= 1;
+      uint32_t s[DH];
+      if (!empty) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DH; c += 16) {
+          uint32_t t16[16];
+          tmem_ld16(tmem + kColSt + lane_off + c, t16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) s[c + e] = t16[e];
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < DH; c += 8) {
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (!empty) {
+          o.x = pack_bf16x2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          o.y = pack_bf16x2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+          o.z = pack_bf16x2(__uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+          o.w = pack_bf16x2(__uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+        }
+        st_shared_v4(smem_u32(sSB) + swz<RB>(row, c), o);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b.sb_full);
+      return true;
+    };
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      const Strip sp = strip_of(a, st);
+      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
+      if (ok) ok = copy_state(true);  // read-out of block 0: empty state
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
+        const int i = ib * kBlk + row;
+        gpos += ib - jlo_of(ib, W) + 1;      // the block's G stages
+        const int sv = gpos % kGStages;
+        const uint32_t pv = (gpos / kGStages) & 1;
+        ++gpos;                               // its v stage
+        // state copy for the next destination block, once this block's updates are in
+        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
+        stph ^= 1;
+        if (ok && ib + 1 < a.n_iblk) ok = copy_state(jlo_of(ib + 1, W) == 0);
+        float den = 0.f;
+        if (ok) ok = wait_bar(&b.den_full, gib & 1, b, a);
+        if (ok) ok = wait_bar(&b.dold_full[gib & 1], (gib >> 1) & 1, b, a);
+        if (ok) {
+          den = b.rowsum[0][row] + b.rowsum[1][row] + b.dold[gib & 1][row];
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&b.den_empty);
+            mbar_arrive(&b.dold_empty[gib & 1]);
+          }
+        }
+        if (ok) ok = wait_bar(&b.o_full, oph, b, a);
+        if (ok) ok = wait_bar(&b.g_full[sv], pv, b, a);
+        ok = named_bar_and(2, 128, ok);
+        if (!ok) break;
+        oph ^= 1;
+        if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[sp.head] - tau) * kLog2e);
+        const float inv = 1.f / den;
+        tc_fence_after();
+        const bool row_ok = i < a.T;
+        const uint32_t vst = smem_u32(sG + sv * kGStage);
+        const int rh = row >> 6, rr = row & 63;
+        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
+#pragma unroll 1
+        for (int cq = 0; cq < 2; ++cq) {
+          uint32_t o[2][32];
+          tmem_ld32(tmem + kColO + lane_off + cq * 64, o[0]);
+          tmem_ld32(tmem + kColO + lane_off + cq * 64 + 32, o[1]);
+          tmem_ld_wait();
+          if (cq == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b.o_empty);
+          }
+          const int col0 = sp.n0 + cq * 64;
+          const bool straddle = col0 < a.m_h && col0 + 64 > a.m_h;
+          const uint32_t box = vst + rh * 2 * kGBox + cq * kGBox + rr * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
+            const uint4 vv = a.has_v ? ld_shared_v4(addr) : make_uint4(0, 0, 0, 0);
+            const uint32_t* o8 = &o[k >> 2][(k & 3) * 8];
+            uint32_t u[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float y0 = __uint_as_float(o8[2 * e]) * inv, y1 = __uint_as_float(o8[2 * e + 1]) * inv;
+              if (a.has_v) {
+                const uint32_t vw = e == 0 ? vv.x : e == 1 ? vv.y : e == 2 ? vv.z : vv.w;
+                y0 *= bf16lo(vw);
+                y1 *= bf16hi(vw);
+              }
+              u[e] = pack_bf16x2(y0, y1);
+            }
+            if (!straddle) st_shared_v4(addr, make_uint4(u[0], u[1], u[2], u[3]));
+            else if (row_ok && col0 + 8 * k < a.m_h) st_global_v4(a.out + grow + col0 + 8 * k, u[0], u[1], u[2], u[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (issuer) {
+          for (int h = 0; h < 2; ++h) {
+            const int y = ib * kBlk + 64 * h;
+            if (y >= a.T) continue;
+            for (int cq = 0; cq < 2; ++cq) {
+              const int col0 = sp.n0 + cq * 64;
+              if (col0 + 64 > a.m_h) continue;
+              tma_store_3d(&tmU, sG + sv * kGStage + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
+            }
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&b.g_empty[sv]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
+  Args a = {};
+  a.B = p.B; a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
+  a.d_h = p.dqk / p.H; a.m_h = p.m / p.H;
+  a.W = p.window; a.phi_mode = p.phi_mode;
+  a.n_iblk = ceil_div(p.T, kBlk);
+  a.n_ntile = ceil_div(a.m_h, kNg);
+  const long long strips = (long long)p.B * p.H * a.n_ntile;
+  if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_strips = (int)strips;
+  a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
+  a.has_v = p.v != nullptr;
+  a.out = static_cast<__nv_bfloat16*>(p.out);
+  a.err = p.err;
+  a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
+  a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
+  CUtensorMap mq, mk, mg, mv, mu;
+  cudaError_t e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, a.d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
+  if (e != cudaSuccess) return e;
+  auto kern = a.d_h == 64 ? wango_tc_kernel<64> : a.d_h == 32 ? wango_tc_kernel<32> : wango_tc_kernel<16>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = a.n_strips < num_sms() ? a.n_strips : num_sms();
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mg, mv, mu, a);
+  return cudaGetLastError();
+}
+
+}  // namespace tg
