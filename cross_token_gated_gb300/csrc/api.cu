@@ -62,14 +62,20 @@ tg_status validate_agg(const tg_agg_params* p, bool wango) {
   return TG_OK;
 }
 
-size_t agg_ws_bytes(const tg_agg_params* p) {
+// Normalised q/k copies (unless the caller passes unit vectors).
+size_t agg_qk_bytes(const tg_agg_params* p) {
   if (p->flags & TG_FLAG_QK_NORMALIZED) return 0;
   const size_t qk = (size_t)p->B * p->T * p->d_qk * elem_size(p->dtype);
   return 2 * align256(qk);
 }
+// Feature-map scratch of the tensor-core WANGO path.
+size_t agg_aux_bytes(const tg_agg_params* p, bool wango) {
+  return (wango && p->dtype == TG_BF16) ? wango_aux_bytes(p->B, p->T, p->H, p->d_qk) : 0;
+}
+size_t agg_ws_bytes(const tg_agg_params* p, bool wango) { return agg_qk_bytes(p) + agg_aux_bytes(p, wango); }
 
 struct BlockWs {
-  size_t x, q, k, g, v, total;
+  size_t x, q, k, g, v, aux, total;
 };
 
 BlockWs block_ws_layout(const tg_block_params* p) {
@@ -81,7 +87,8 @@ BlockWs block_ws_layout(const tg_block_params* p) {
   w.k = w.q + align256(BT * a.d_qk * es);
   w.g = w.k + align256(BT * a.d_qk * es);
   w.v = w.g + align256(BT * a.m * es);
-  w.total = w.v + align256(BT * a.m * es);
+  w.aux = w.v + align256(BT * a.m * es);
+  w.total = w.aux + agg_aux_bytes(&a, p->mode == TG_MODE_WANGO);
   return w;
 }
 
@@ -115,7 +122,7 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
   if (p->dtype == TG_BF16 && !(aligned16(q) && aligned16(k) && aligned16(g) && aligned16(out) &&
                                (!v || aligned16(v))))
     return TG_ERR_UNSUPPORTED;
-  const size_t need = agg_ws_bytes(p);
+  const size_t need = agg_ws_bytes(p, wango), qk_bytes = agg_qk_bytes(p);
   st = check_ws(ws, ws_bytes, need);
   if (st != TG_OK) return st;
 
@@ -124,6 +131,7 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
   a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
   a.window = p->window; a.phi_mode = p->phi_mode; a.flags = p->flags; a.dtype = p->dtype;
   a.g = g; a.v = v; a.out = out;
+  a.aux = static_cast<char*>(ws) + qk_bytes;
   cudaError_t e = error_word(&a.err);
   if (e != cudaSuccess) return TG_ERR_CUDA;
   if (p->flags & TG_FLAG_QK_NORMALIZED) {
@@ -133,7 +141,7 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
     const long long rows = (long long)p->B * p->T;
     char* base = static_cast<char*>(ws);
     void* qn = base;
-    void* kn = base + need / 2;
+    void* kn = base + qk_bytes / 2;
     e = launch_qk_prep(p->dtype, q, qn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
     if (e == cudaSuccess) e = launch_qk_prep(p->dtype, k, kn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
     if (e != cudaSuccess) return TG_ERR_CUDA;
@@ -187,6 +195,7 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
   a.s = ap.s; a.tau = ap.tau; a.null_bias = ap.null_bias;
   a.window = ap.window; a.phi_mode = ap.phi_mode; a.flags = 0; a.dtype = ap.dtype;
   a.q = qb; a.k = kb; a.g = gb; a.v = vb; a.out = vb;  // gbar * v overwrites v in place
+  a.aux = base + L.aux;
   cudaError_t e = error_word(&a.err);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
@@ -231,7 +240,7 @@ size_t tg_workspace_size(int which, const void* params) {
   if (which == TG_WS_TANGO || which == TG_WS_WANGO) {
     const tg_agg_params* p = static_cast<const tg_agg_params*>(params);
     if (validate_agg(p, which == TG_WS_WANGO) != TG_OK) return 0;
-    return agg_ws_bytes(p);
+    return agg_ws_bytes(p, which == TG_WS_WANGO);
   }
   if (which == TG_WS_BLOCK) {
     const tg_block_params* p = static_cast<const tg_block_params*>(params);

@@ -24,6 +24,7 @@ struct AggArgs {
   const void* v;  // may be NULL
   void* out;
   unsigned* err;  // device error word
+  void* aux;      // WANGO, tensor-core path: feature-map scratch (wango_aux_bytes)
 };
 
 enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };

@@ -2,40 +2,41 @@
 // Token-Aggregated Nonlinear Gating Operators ...", sec. 2.2 eqs. 7-10 in sec. 2.1
 // eq. 5.  For destination i and head a (all weights carry the common factor e^-tau,
 // which cancels in the ratio):
-//   window  i-W < j <= i :  w_ij = exp(tau (qhat_i.khat_j - 1))                (eq. 6)
-//   older   j <= i-W     :  w_ij = e^-tau phi(sqrt(tau) qhat_i).phi(sqrt(tau) khat_j) (eq. 9)
+//   window  i-W < j <= i :  w_ij = exp(tau (qhat_i.khat_j - 1))                 (eq. 6)
+//   older   j <= i-W     :  w_ij = e^-tau phi(sqrt(tau) qhat_i).phi(sqrt(tau) khat_j)  (eq. 9)
 //   u_i = [sum_j w_ij g_j] / [sum_j w_ij + (i+1) e^{b-tau}] * v_i
 // The older sources enter through the running sums of eq. 10,
 //   S = sum phi(k~_j) g_j^T (d_h x gate columns),   z = sum phi(k~_j),
-// with read-outs  e^-tau phi(q~_i)^T S  and  e^-tau phi(q~_i)^T z.
+// read out as  e^-tau phi(q~_i)^T S  and  e^-tau phi(q~_i)^T z.
 //
-// One CTA walks, in order, the 128-row destination blocks ib of one (batch, head,
-// 128-column gate tile) -- a "strip"; persistent CTAs take strips round-robin.  For
-// destination block ib the per-pair sources are the 128-source blocks
-//   jb = jlo(ib) .. ib,   jlo(ib) = floor(max(0, 128 ib - W + 1) / 128),
-// and the state holds every source j < 128 jlo(ib), which is older than the window
-// for every destination of the block.  A block jb is "mixed" when it also holds
-// older pairs (128 jb <= 128 ib + 127 - W): its weights need both scores.  A block
-// "leaves" when jb < jlo(ib + 1): after its P.G MMA the same G tile updates the state.
+// Two stages:
+//  1. wango_prep (CUDA cores): Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat)
+//     in bf16; per 128-source block the column sums of Fk; and per destination the
+//     older-prefix denominator Fq_i . z, z summed over the blocks older than the
+//     destination block's window (the same blocks the state holds below).
+//  2. wango_tc_kernel: one CTA walks, in order, the 128-row destination blocks ib of one
+//     (batch, head, 128-column gate tile) -- a "strip"; persistent CTAs take strips
+//     round-robin.  For destination block ib the per-pair sources are the blocks
+//        jb = jlo(ib) .. ib,   jlo(ib) = floor(max(0, 128 ib - W + 1) / 128),
+//     and the state holds every source j < 128 jlo(ib), older than the window for every
+//     destination of the block.  A block is "mixed" when it also holds older pairs
+//     (128 jb <= 128 ib + 127 - W): its weights need both scores.  A block "leaves" when
+//     jb < jlo(ib + 1): after its P.G MMA the same G tile updates the state.
 //
-// Roles (16 warps, 512 threads):
-//   warp 0       TMA: qhat (1 buffer), khat (2-stage ring), and a 3-stage ring of
-//                32 KB stages carrying G blocks (128 sources x 128 columns) and, after a
-//                destination block's sources, its v tile for the epilogue.
+// Roles of the main kernel (16 warps; warps 2-3 idle):
+//   warp 0       TMA: qhat + Fq (one 32 KB buffer), khat + Fk (2-stage ring), and a
+//                3-stage ring of 32 KB stages carrying G blocks (128 sources x 128
+//                columns) and, after a destination block's sources, its v tile.
 //   warp 1       MMA issue (one thread), per destination block:
-//                  O  = e^-tau Phi(Q~) S_bf16           (M=128, N=128, K=d_h), read-out
-//                  for each source block: Sc = Qhat Khat^T (f32 -> slot), mixed blocks
-//                  also Sf = e^-tau Phi(Q~) Phi(K~)^T (-> second slot); O += P G;
-//                  leaving blocks: S^T += G^T Phi(K~)  (M=128, N=d_h, K=128) in TMEM.
-//   warps 2-3    feature maps on the CUDA cores: Phi(Q~) (scaled by e^-tau) and the
-//                older-prefix denominator e^-tau phi(q~).z per row; Phi(K~) of mixed and
-//                leaving blocks, and z += sum phi(k~) over leaving blocks.
-//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of each block; the
-//                row's weight per pair is exp (window), the feature-map score (older),
-//                or 0 (after i); rounded to bf16, summed into the row's denominator,
-//                written as P over the score slot.
-//   warps 12-15  the state copy S^T (TMEM, f32) -> S (shared memory, bf16) for the next
-//                read-out; the epilogue O / den * v with u stored by TMA.
+//                  per source block: Sc = Qhat Khat^T (f32 slot); mixed: Sf = Fq Fk^T
+//                  (second slot); O (+)= P G; leaving: S^T += G^T Fk (M=128, N=d_h) in
+//                  TMEM; the next block's scores are issued early when slots allow;
+//                  last: O += Fq S_bf16 (read-out of the state before this block).
+//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of each block: exp
+//                (window), the feature-map score (older) or 0 (after i), rounded to bf16,
+//                summed into the row's denominator, written as P over the score slot.
+//   warps 12-15  epilogue O / den * v, u stored by TMA; then the copy S^T (TMEM, f32)
+//                -> S (shared memory, bf16) for the next destination block's read-out.
 // TMEM: O [0,128), S^T [128, 128+d_h), score slots [256,384) and [384,512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -52,42 +53,38 @@ constexpr int kNg = 128;       // gate columns per strip
 constexpr int kKStages = 2;
 constexpr int kGStages = 3;
 constexpr int kThreads = 512;
-constexpr int kPhiWarp0 = 2, kSoftWarp0 = 4, kEpiWarp0 = 12;
+constexpr int kSoftWarp0 = 4, kEpiWarp0 = 12;
 constexpr uint32_t kTile = kBlk * 64 * 2;   // 16 KB: a 128 x d_h bf16 tile at d_h = 64
 constexpr uint32_t kGBox = 64 * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;     // 32 KB: 128 rows x 128 columns
 constexpr uint32_t kColO = 0, kColSt = 128, kColSlot0 = 256;
 
 struct __align__(8) Bars {
-  uint64_t q_full, q_empty;                     // qhat tile: MMA + phi warps consume
-  uint64_t fq_full, fq_empty;                   // Phi(Q~) tile
-  uint64_t k_full[kKStages], k_empty[kKStages]; // khat tiles: MMA + phi warps consume
-  uint64_t fk_full[2], fk_empty[2];             // Phi(K~) tiles (mixed / leaving blocks)
+  uint64_t q_full, q_empty;                     // qhat + Fq of a destination block
+  uint64_t k_full[kKStages], k_empty[kKStages]; // khat (+ Fk) of a source block
   uint64_t g_full[kGStages], g_empty[kGStages];
   uint64_t s_full[2], p_full[2];                // score slots; P of source blocks
   uint64_t o_full, o_empty;
-  uint64_t st_full;                             // S^T updates of a destination block done
-  uint64_t sb_full, sb_empty;                   // bf16 state copy for the read-out
+  uint64_t st_full;                             // a destination block's MMAs are done
+  uint64_t sb_full;                             // bf16 state copy in place
   uint64_t den_full, den_empty;                 // P row sums -> epilogue
-  uint64_t dold_full[2], dold_empty[2];         // older-prefix denominators -> epilogue
   uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
   float rowsum[2][kBlk];
-  float dold[2][kBlk];
-  float z[2][64];
 };
 
-// smem: Q | PhiQ | K[2] | PhiK[2] | S_bf16 | G ring | Bars
+// smem: Q | Fq | (K | Fk) x 2 | S_bf16 | G ring | Bars
 constexpr size_t kSmemBytes = 1024 + kTile * 7 + kGStage * kGStages + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
-  int B, T, H, dqk, m, d_h, m_h, W, phi_mode;
+  int B, T, H, dqk, m, d_h, m_h, W;
   int n_iblk, n_ntile, n_strips;
   float s;
   const float* tau;
   const float* null_bias;
+  const float* den_old;  // [B, H, T]
   int has_v;
   __nv_bfloat16* out;
   unsigned* err;
@@ -95,7 +92,7 @@ struct Args {
   int debug_timeout;
 };
 
-__device__ __forceinline__ int jlo_of(int ib, int W) {
+__host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
   const int lo = ib * kBlk - W + 1;
   return lo > 0 ? lo / kBlk : 0;
 }
@@ -142,16 +139,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return off ^ (((off >> 7) & mask) << 4);
 }
 
-// Feature map of eq. 8 (mode 0) or plain ELU + 1 (mode 1).
-__device__ __forceinline__ float phi_map(float u, float inv_sqrt_dh, int mode) {
-  const float elu = u > 0.f ? u : expm1f(u);
-  if (mode == 1) return elu + 1.f;
-  return fmaxf(elu + 1.f + 1e-4f, 1e-4f) * inv_sqrt_dh;
-}
-
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     wango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
                     const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmU, const Args a) {
   constexpr int RB = DH * 2;  // bytes per row of the q/k/feature tiles
@@ -160,31 +151,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t tile_bytes = kBlk * RB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sFQ = sQ + kTile;
-  uint8_t* sK = sFQ + kTile;           // 2 stages
-  uint8_t* sFK = sK + 2 * kTile;       // 2 stages
-  uint8_t* sSB = sFK + 2 * kTile;      // bf16 state, [128 gate rows x d_h]
+  uint8_t* sQ = base;                  // qhat, then Fq at +kTile
+  uint8_t* sK = sQ + 2 * kTile;        // stage s: khat at s*2*kTile, Fk at +kTile
+  uint8_t* sSB = sK + 4 * kTile;       // bf16 state, [128 gate rows x d_h]
   uint8_t* sG = sSB + kTile;
   Bars& b = *reinterpret_cast<Bars*>(sG + kGStages * kGStage);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     mbar_init(&b.q_full, 1);
-    mbar_init(&b.q_empty, 3);   // MMA commit + both feature-map warps
-    mbar_init(&b.fq_full, 2);
-    mbar_init(&b.fq_empty, 1);
+    mbar_init(&b.q_empty, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&b.k_full[s], 1);
-      mbar_init(&b.k_empty[s], 3);  // MMA commit + both feature-map warps
+      mbar_init(&b.k_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&b.fk_full[s], 2);
-      mbar_init(&b.fk_empty[s], 1);
       mbar_init(&b.s_full[s], 1);
       mbar_init(&b.p_full[s], 8);
-      mbar_init(&b.dold_full[s], 2);
-      mbar_init(&b.dold_empty[s], 4);
     }
     for (int s = 0; s < kGStages; ++s) {
       mbar_init(&b.g_full[s], 1);
@@ -194,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&b.o_empty, 4);
     mbar_init(&b.st_full, 1);
     mbar_init(&b.sb_full, 4);
-    mbar_init(&b.sb_empty, 1);
     mbar_init(&b.den_full, 8);
     mbar_init(&b.den_empty, 4);
     mbar_init(&b.drain, 1);
@@ -241,14 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int gx = sp.head * a.m_h + sp.n0;
       for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
         if (!(ok = wait_bar(&b.q_empty, qph ^ 1, b, a))) break;
-        mbar_arrive_expect_tx(&b.q_full, tile_bytes);
+        mbar_arrive_expect_tx(&b.q_full, 2 * tile_bytes);
         tma_load_3d(sQ, &tmQ, &b.q_full, sp.head * DH, ib * kBlk, sp.b);
+        tma_load_3d(sQ + kTile, &tmFQ, &b.q_full, sp.head * DH, ib * kBlk, sp.b);
         q_issued = true;
         qph ^= 1;
         for (int jb = jlo_of(ib, W); ok && jb <= ib; ++jb) {
+          const bool need_fk = is_mixed(jb, ib, W) || is_leaving(jb, ib, W);
           if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
-          mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
-          tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
+          uint8_t* kdst = sK + kr.stage * 2 * kTile;
+          mbar_arrive_expect_tx(&b.k_full[kr.stage], need_fk ? 2 * tile_bytes : tile_bytes);
+          tma_load_3d(kdst, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
+          if (need_fk) tma_load_3d(kdst + kTile, &tmFK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
           kmask |= 1u << kr.stage;
           kph[kr.stage] = kr.phase;
           kr.next(kKStages);
@@ -266,85 +252,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);   // scores
     constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);     // O += P G
-    constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);    // O = Phi(Q) S
-    constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);       // S^T += G^T Phi(K)
+    constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);    // O += Fq S
+    constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);       // S^T += G^T Fk
     const uint64_t qd = smem_desc(smem_u32(sQ), 16, sbo, lay);
-    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
+    const uint64_t fqd = smem_desc(smem_u32(sQ + kTile), 16, sbo, lay);
     const uint64_t kd0 = smem_desc(smem_u32(sK), 16, sbo, lay);
-    const uint64_t fkd0 = smem_desc(smem_u32(sFK), 16, sbo, lay);
-    const uint64_t fkd_mn0 = smem_desc(smem_u32(sFK), tile_bytes, sbo, lay);  // Phi(K~) as MN-major B
+    const uint64_t fkd0 = smem_desc(smem_u32(sK + kTile), 16, sbo, lay);
+    const uint64_t fkmn0 = smem_desc(smem_u32(sK + kTile), tile_bytes, sbo, lay);  // Fk as MN-major B
     const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
     const uint64_t gd0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
     Ring kr, gr;
-    int fkstage = 0;
-    uint32_t fkphase = 0, qph = 0, oph = 0, sbph = 0;
+    uint32_t qph = 0, oph = 0, sbph = 0;
     uint32_t slot = 0;       // score slots used so far (ring of 2)
-    uint32_t blk = 0;        // source blocks processed so far (p_full ring of 2)
+    uint32_t blk = 0;        // source blocks whose P.G has been issued (p_full ring of 2)
     bool first_update = true;
+    // Scores of one source block from khat stage `ks`: cos into the next slot, the
+    // feature-map scores of a mixed block into the one after.  Returns the cos slot.
+    auto issue_scores = [&](int ks, uint32_t kphase, bool mixed, bool& okr) -> uint32_t {
+      const uint32_t cs = slot;
+      if (!(okr = wait_bar(&b.k_full[ks], kphase, b, a))) return cs;
+      tc_fence_after_nc();
+      const uint64_t kd = kd0 + (uint64_t)((ks * 2 * kTile) >> 4);
+      const uint32_t sc = tmem + kColSlot0 + (slot & 1) * 128;
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk)
+        mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+      mma_commit_nc(&b.s_full[slot & 1]);
+      ++slot;
+      if (mixed) {
+        const uint32_t sf = tmem + kColSlot0 + (slot & 1) * 128;
+        const uint64_t fkd = fkd0 + (uint64_t)((ks * 2 * kTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_bf16_ss_nc(sf, fqd + (uint64_t)(kk * 2), fkd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+        mma_commit_nc(&b.s_full[slot & 1]);
+        ++slot;
+      }
+      return cs;
+    };
     for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
       first_update = true;
       for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
         if (!(ok = wait_bar(&b.q_full, qph, b, a))) break;
-        if (!(ok = wait_bar(&b.fq_full, qph, b, a))) break;
         qph ^= 1;
-        // the previous destination block's accumulator has been read; the bf16 state
-        // copy for this block is in place
-        if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
-        if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-        oph ^= 1;
-        sbph ^= 1;
-        tc_fence_after_nc();
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk)
-          mma_bf16_ss_nc(tmem + kColO, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, kk != 0);
-        mma_commit_nc(&b.sb_empty);
         const int jlo = jlo_of(ib, W);
-        bool updated = false;
+        bool copy_ready = false;  // the bf16 state copy for this block's read-out
+        uint32_t next_cs = 0;
+        bool next_issued = false;
         for (int jb = jlo; ok && jb <= ib; ++jb) {
           const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
-          const bool need_fk = mixed || leaving;
-          if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
-          tc_fence_after_nc();
-          const uint64_t kd = kd0 + (uint64_t)((kr.stage * kTile) >> 4);
-          const uint32_t sc = tmem + kColSlot0 + (slot & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk)
-            mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
-          mma_commit_nc(&b.k_empty[kr.stage]);
-          mma_commit_nc(&b.s_full[slot & 1]);
-          kr.next(kKStages);
-          const uint32_t pslot = slot;
-          ++slot;
-          if (need_fk) {
-            if (!(ok = wait_bar(&b.fk_full[fkstage], fkphase, b, a))) break;
-            tc_fence_after_nc();
+          uint32_t cs;
+          if (next_issued) {
+            cs = next_cs;
+            next_issued = false;
+          } else {
+            cs = issue_scores(kr.stage, kr.phase, mixed, ok);
+            if (!ok) break;
           }
-          if (mixed) {
-            const uint32_t sf = tmem + kColSlot0 + (slot & 1) * 128;
-            const uint64_t fkd = fkd0 + (uint64_t)((fkstage * kTile) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk)
-              mma_bf16_ss_nc(sf, fqd + (uint64_t)(kk * 2), fkd + (uint64_t)(kk * 2), idesc_s, kk != 0);
-            mma_commit_nc(&b.s_full[slot & 1]);
-            ++slot;
+          // the next block's scores go first when neither block needs two slots
+          if (jb < ib && !mixed && !is_mixed(jb + 1, ib, W)) {
+            Ring nk = kr;
+            nk.next(kKStages);
+            next_cs = issue_scores(nk.stage, nk.phase, false, ok);
+            if (!ok) break;
+            next_issued = true;
           }
-          // O += P G  (P in the block's cos slot)
+          // O (+)= P G  (P in the block's cos slot); the first overwrites O once the
+          // epilogue has read the previous destination block's accumulator.
           if (!(ok = wait_bar(&b.p_full[blk & 1], (blk >> 1) & 1, b, a))) break;
           ++blk;
+          if (jb == jlo) {
+            if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
+            oph ^= 1;
+          }
           if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
           tc_fence_after_nc();
           const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
-          const uint32_t ptm = tmem + kColSlot0 + (pslot & 1) * 128;
+          const uint32_t ptm = tmem + kColSlot0 + (cs & 1) * 128;
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk) {
             const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
-            mma_bf16_ts_nc(tmem + kColO, ptm + kk * 8, gd + (uint64_t)(goff >> 4), idesc_o, 1u);
+            mma_bf16_ts_nc(tmem + kColO, ptm + kk * 8, gd + (uint64_t)(goff >> 4), idesc_o,
+                           (jb == jlo && kk == 0) ? 0u : 1u);
           }
           if (leaving) {
-            // S^T += G^T Phi(K~): A = G (MN-major), B = Phi(K~) (MN-major)
-            const uint64_t fkmn = fkd_mn0 + (uint64_t)((fkstage * kTile) >> 4);
+            // S^T += G^T Fk once the read-out copy of the previous state is taken
+            if (!copy_ready) {
+              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+              sbph ^= 1;
+              copy_ready = true;
+              tc_fence_after_nc();
+            }
+            const uint64_t fkmn = fkmn0 + (uint64_t)((kr.stage * 2 * kTile) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBlk / 16; ++kk) {
               const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
@@ -352,131 +353,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                              idesc_u, (first_update && kk == 0) ? 0u : 1u);
             }
             first_update = false;
-            updated = true;
           }
           mma_commit_nc(&b.g_empty[gr.stage]);
           gr.next(kGStages);
-          if (need_fk) {
-            mma_commit_nc(&b.fk_empty[fkstage]);
-            if (++fkstage == 2) { fkstage = 0; fkphase ^= 1; }
-          }
+          mma_commit_nc(&b.k_empty[kr.stage]);
+          kr.next(kKStages);
         }
         if (!ok) break;
-        (void)updated;
-        mma_commit_nc(&b.st_full);   // the state now holds every source leaving at ib
+        // read-out of the state before this block: O += Fq S_bf16
+        if (!copy_ready) {
+          if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+          sbph ^= 1;
+          tc_fence_after_nc();
+        }
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_bf16_ss_nc(tmem + kColO, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, 1u);
         mma_commit_nc(&b.q_empty);
-        mma_commit_nc(&b.fq_empty);
+        mma_commit_nc(&b.st_full);
         mma_commit_nc(&b.o_full);
-        gr.next(kGStages);           // the v stage belongs to the epilogue
+        gr.next(kGStages);  // the v stage belongs to the epilogue
       }
     }
     mma_commit(&b.drain);
     mbar_wait(&b.drain, 0, a.timeout_ns);
-  } else if (warp >= kPhiWarp0 && warp < kSoftWarp0) {
-    // ------------------------------------------------------------ feature maps
-    const int pt = threadIdx.x - kPhiWarp0 * 32;  // 0..63: rows pt and pt + 64; z dim pt
-    const float inv_sqrt_dh = rsqrtf((float)DH);
-    bool ok = true;
-    uint32_t qph = 0;
-    Ring kr;
-    int fkstage = 0;
-    uint32_t fkphase = 0;
-    int gib = 0;  // destination blocks done by this CTA
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      const Strip sp = strip_of(a, st);
-      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
-      const float sq = sqrtf(tau), shift = exp2f(-tau * kLog2e);
-      // the state of a new strip is empty
-      if (pt < DH) b.z[0][pt] = 0.f;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
-        const int zc = ib & 1;
-        if (ok) ok = wait_bar(&b.q_full, qph, b, a);
-        if (ok) ok = wait_bar(&b.fq_empty, qph ^ 1, b, a);
-        if (ok) ok = wait_bar(&b.dold_empty[gib & 1], ((gib >> 1) & 1) ^ 1, b, a);
-        // both warps agree on the status; the barrier also completes z of this block
-        ok = named_bar_and(3, 64, ok);
-        if (!ok) break;
-        qph ^= 1;
-        for (int h = 0; h < 2; ++h) {
-          const int r = pt + 64 * h;
-          float dot = 0.f;
-#pragma unroll
-          for (int c = 0; c < DH; c += 8) {
-            const uint32_t off = swz<RB>(r, c);
-            const uint4 qv = ld_shared_v4(smem_u32(sQ) + off);
-            const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float f0 = shift * phi_map(sq * bf16lo(w[e]), inv_sqrt_dh, a.phi_mode);
-              const float f1 = shift * phi_map(sq * bf16hi(w[e]), inv_sqrt_dh, a.phi_mode);
-              o[e] = pack_bf16x2(f0, f1);
-              dot = fmaf(bf16lo(o[e]), b.z[zc][c + 2 * e], dot);
-              dot = fmaf(bf16hi(o[e]), b.z[zc][c + 2 * e + 1], dot);
-            }
-            st_shared_v4(smem_u32(sFQ) + off, make_uint4(o[0], o[1], o[2], o[3]));
-          }
-          b.dold[gib & 1][r] = dot;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&b.fq_full);
-          mbar_arrive(&b.q_empty);
-          mbar_arrive(&b.dold_full[gib & 1]);
-        }
-        // the next block's z starts from this one's
-        if (pt < DH) b.z[zc ^ 1][pt] = b.z[zc][pt];
-        const int jlo = jlo_of(ib, W);
-        for (int jb = jlo; ok && jb <= ib; ++jb) {
-          const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
-          if (ok) ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a);
-          if (ok && (mixed || leaving)) ok = wait_bar(&b.fk_empty[fkstage], fkphase ^ 1, b, a);
-          ok = named_bar_and(3, 64, ok);
-          if (!ok) break;
-          if (mixed || leaving) {
-            uint8_t* fk = sFK + fkstage * kTile;
-            const uint8_t* kt = sK + kr.stage * kTile;
-            for (int h = 0; h < 2; ++h) {
-              const int r = pt + 64 * h;
-#pragma unroll
-              for (int c = 0; c < DH; c += 8) {
-                const uint32_t off = swz<RB>(r, c);
-                const uint4 kv = ld_shared_v4(smem_u32(kt) + off);
-                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  o[e] = pack_bf16x2(phi_map(sq * bf16lo(w[e]), inv_sqrt_dh, a.phi_mode),
-                                     phi_map(sq * bf16hi(w[e]), inv_sqrt_dh, a.phi_mode));
-                st_shared_v4(smem_u32(fk) + off, make_uint4(o[0], o[1], o[2], o[3]));
-              }
-            }
-            if (leaving) {
-              // z += sum over the block's valid sources of phi(k~) (the bf16 values the
-              // state update multiplies, so numerator and denominator agree)
-              named_bar_sync(3, 64);
-              if (pt < DH) {
-                float zs = 0.f;
-                const int nrows = min(kBlk, a.T - jb * kBlk);
-                for (int r = 0; r < nrows; ++r) {
-                  const uint32_t v2 = *reinterpret_cast<const uint32_t*>(fk + (swz<RB>(r, pt & ~1)));
-                  zs += (pt & 1) ? bf16hi(v2) : bf16lo(v2);
-                }
-                b.z[zc ^ 1][pt] += zs;
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&b.fk_full[fkstage]);
-            if (++fkstage == 2) { fkstage = 0; fkphase ^= 1; }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b.k_empty[kr.stage]);
-          kr.next(kKStages);
-        }
-      }
-    }
   } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ weights
     const int wg = (warp - kSoftWarp0) / 4;  // sources [64 wg, 64 wg + 64) of each block
@@ -497,18 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool mixed = is_mixed(jb, ib, W);
           const uint32_t cs = slot;
           const uint32_t sc = tmem + kColSlot0 + (cs & 1) * 128 + lane_off + wg * 64;
-          uint32_t r[2][32], f[2][32];
+          const uint32_t sf = tmem + kColSlot0 + ((cs + 1) & 1) * 128 + lane_off + wg * 64;
           if (ok) ok = wait_bar(&b.s_full[cs & 1], (cs >> 1) & 1, b, a);
           if (ok && mixed) ok = wait_bar(&b.s_full[(cs + 1) & 1], ((cs + 1) >> 1) & 1, b, a);
+          uint32_t r[2][32];
           if (ok) {
             tc_fence_after();
             tmem_ld32(sc, r[0]);
             tmem_ld32(sc + 32, r[1]);
-            if (mixed) {
-              const uint32_t sf = tmem + kColSlot0 + ((cs + 1) & 1) * 128 + lane_off + wg * 64;
-              tmem_ld32(sf, f[0]);
-              tmem_ld32(sf + 32, f[1]);
-            }
             tmem_ld_wait();
           }
           slot += mixed ? 2 : 1;
@@ -519,6 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j0 = jb * kBlk + wg * 64;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
+            uint32_t f[32];
+            if (mixed) {
+              tmem_ld32(sf + q * 32, f);
+              tmem_ld_wait();
+            }
             uint32_t p[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
@@ -529,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float x = 0.f;
                 if (j <= i) {
                   if (j >= i - W + 1) x = ex2_approx(fmaf(c, __uint_as_float(r[q][e + z]), -c));
-                  else x = __uint_as_float(f[q][e + z]);
+                  else x = mixed ? __uint_as_float(f[e + z]) : 0.f;
                 }
                 w[z] = x;
               }
@@ -555,20 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kEpiWarp0) {
-    // ------------------------------------------------------------ state copy + epilogue
+    // ------------------------------------------------------------ epilogue + state copy
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // destination row; also the gate column of S^T
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool issuer = (warp == kEpiWarp0 && lane == 0);
     bool ok = true;
-    uint32_t oph = 0, stph = 0, sbph = 0;
+    uint32_t oph = 0, stph = 0;
     int gpos = 0, gib = 0;
-    // bf16 copy of the state for the read-out of destination block ib (zero until the
-    // first source has left the window)
-    auto copy_state = [&](bool empty) -> bool {
-      if (!wait_bar(&b.sb_empty, sbph ^ 1, b, a)) return false;
-      sbph ^= 1;
-      uint32_t s[DH];
+    // bf16 copy of the state for a destination block's read-out (zero while no source
+    // has left the window)
+    auto copy_state = [&](bool empty) {
+      uint32_t sreg[DH];
       if (!empty) {
         tc_fence_after();
 #pragma unroll
@@ -577,17 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tmem + kColSt + lane_off + c, t16);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) s[c + e] = t16[e];
+          for (int e = 0; e < 16; ++e) sreg[c + e] = t16[e];
         }
       }
 #pragma unroll
       for (int c = 0; c < DH; c += 8) {
         uint4 o = make_uint4(0, 0, 0, 0);
         if (!empty) {
-          o.x = pack_bf16x2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-          o.y = pack_bf16x2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-          o.z = pack_bf16x2(__uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-          o.w = pack_bf16x2(__uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+          o.x = pack_bf16x2(__uint_as_float(sreg[c]), __uint_as_float(sreg[c + 1]));
+          o.y = pack_bf16x2(__uint_as_float(sreg[c + 2]), __uint_as_float(sreg[c + 3]));
+          o.z = pack_bf16x2(__uint_as_float(sreg[c + 4]), __uint_as_float(sreg[c + 5]));
+          o.w = pack_bf16x2(__uint_as_float(sreg[c + 6]), __uint_as_float(sreg[c + 7]));
         }
         st_shared_v4(smem_u32(sSB) + swz<RB>(row, c), o);
       }
@@ -595,45 +494,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.sb_full);
-      return true;
     };
     for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
       const Strip sp = strip_of(a, st);
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
-      if (ok) ok = copy_state(true);  // read-out of block 0: empty state
+      copy_state(true);  // read-out of block 0: empty state
       for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
         const int i = ib * kBlk + row;
-        gpos += ib - jlo_of(ib, W) + 1;      // the block's G stages
+        gpos += ib - jlo_of(ib, W) + 1;  // the block's G stages
         const int sv = gpos % kGStages;
         const uint32_t pv = (gpos / kGStages) & 1;
-        ++gpos;                               // its v stage
-        // state copy for the next destination block, once this block's updates are in
-        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
-        stph ^= 1;
-        if (ok && ib + 1 < a.n_iblk) ok = copy_state(jlo_of(ib + 1, W) == 0);
+        ++gpos;                           // its v stage
         float den = 0.f;
         if (ok) ok = wait_bar(&b.den_full, gib & 1, b, a);
-        if (ok) ok = wait_bar(&b.dold_full[gib & 1], (gib >> 1) & 1, b, a);
         if (ok) {
-          den = b.rowsum[0][row] + b.rowsum[1][row] + b.dold[gib & 1][row];
+          den = b.rowsum[0][row] + b.rowsum[1][row];
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&b.den_empty);
-            mbar_arrive(&b.dold_empty[gib & 1]);
-          }
+          if (lane == 0) mbar_arrive(&b.den_empty);
         }
+        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
         if (ok) ok = wait_bar(&b.o_full, oph, b, a);
         if (ok) ok = wait_bar(&b.g_full[sv], pv, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
+        stph ^= 1;
         oph ^= 1;
+        const bool row_ok = i < a.T;
+        if (row_ok) den += a.den_old[((size_t)sp.b * a.H + sp.head) * a.T + i];
         if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[sp.head] - tau) * kLog2e);
         const float inv = 1.f / den;
+        // the state copy for the next destination block (this block's updates and
+        // read-out are complete), then the accumulator
+        if (ib + 1 < a.n_iblk) copy_state(jlo_of(ib + 1, W) == 0);
         tc_fence_after();
-        const bool row_ok = i < a.T;
         const uint32_t vst = smem_u32(sG + sv * kGStage);
         const int rh = row >> 6, rr = row & 63;
         const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
+        // the accumulator in two 64-column halves; it is released after the second
 #pragma unroll 1
         for (int cq = 0; cq < 2; ++cq) {
           uint32_t o[2][32];
@@ -695,6 +592,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- pre-pass
+
+// Feature map of eq. 8 (mode 0) or plain ELU + 1 (mode 1).  For u <= 0,
+// ELU(u) + 1 = e^u exactly, so only the exponential is evaluated.
+__device__ __forceinline__ float phi_fast(float u, float inv_sqrt_dh, int mode) {
+  const float e1 = u > 0.f ? u + 1.f : ex2_approx(u * kLog2e);
+  if (mode == 1) return e1;
+  return fmaxf(e1 + 1e-4f, 1e-4f) * inv_sqrt_dh;
+}
+
+// Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat); one thread per (row, 8
+// consecutive features of one head).
+__global__ void wango_phi_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* fq,
+                                 __nv_bfloat16* fk, long long rows, int H, int dqk, float s, const float* tau,
+                                 int phi_mode, unsigned* err) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int groups = dqk / 8;
+  if (idx >= rows * groups) return;
+  const long long r = idx / groups;
+  const int c0 = (int)(idx % groups) * 8;
+  const int d_h = dqk / H, a = c0 / d_h;
+  const float t = head_tau(tau, s, a, err, kKernWango);
+  const float sq = sqrtf(t), shift = exp2f(-t * kLog2e), inv_sqrt_dh = rsqrtf((float)d_h);
+  const uint4 qv = *reinterpret_cast<const uint4*>(q + r * dqk + c0);
+  const uint4 kv = *reinterpret_cast<const uint4*>(k + r * dqk + c0);
+  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+  uint32_t fo[4], ko[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    fo[e] = pack_bf16x2(shift * phi_fast(sq * bf16lo(qw[e]), inv_sqrt_dh, phi_mode),
+                        shift * phi_fast(sq * bf16hi(qw[e]), inv_sqrt_dh, phi_mode));
+    ko[e] = pack_bf16x2(phi_fast(sq * bf16lo(kw[e]), inv_sqrt_dh, phi_mode),
+                        phi_fast(sq * bf16hi(kw[e]), inv_sqrt_dh, phi_mode));
+  }
+  *reinterpret_cast<uint4*>(fq + r * dqk + c0) = make_uint4(fo[0], fo[1], fo[2], fo[3]);
+  *reinterpret_cast<uint4*>(fk + r * dqk + c0) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+}
+
+// zb[b][a][jb][c] = sum over the valid sources of block jb of Fk[.][a d_h + c] (the
+// bf16 values the state update multiplies).  grid (n_iblk, H, B), block d_h threads.
+__global__ void wango_blocksum_kernel(const __nv_bfloat16* fk, float* zb, int T, int H, int dqk, int n_iblk) {
+  const int jb = blockIdx.x, a = blockIdx.y, bb = blockIdx.z, c = threadIdx.x;
+  const int d_h = dqk / H;
+  const int j0 = jb * kBlk, j1 = min(T, j0 + kBlk);
+  float s = 0.f;
+  for (int j = j0; j < j1; ++j) s += __bfloat162float(fk[((size_t)bb * T + j) * dqk + a * d_h + c]);
+  zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + c] = s;
+}
+
+// den_old[b][a][i] = Fq_i . z(ib), z(ib) = sum of zb over the blocks jb < jlo(ib) of
+// destination block ib.  grid (n_iblk, H, B), block 128 threads.
+__global__ void wango_denold_kernel(const __nv_bfloat16* fq, const float* zb, float* den_old, int T, int H, int dqk,
+                                    int n_iblk, int W) {
+  __shared__ float z[64];
+  const int ib = blockIdx.x, a = blockIdx.y, bb = blockIdx.z, t = threadIdx.x;
+  const int d_h = dqk / H, jlo = jlo_of(ib, W);
+  if (t < d_h) {
+    float s = 0.f;
+    for (int jb = 0; jb < jlo; ++jb) s += zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + t];
+    z[t] = s;
+  }
+  __syncthreads();
+  const int i = ib * kBlk + t;
+  if (i >= T) return;
+  const __nv_bfloat16* f = fq + ((size_t)bb * T + i) * dqk + a * d_h;
+  float dot = 0.f;
+  for (int c = 0; c < d_h; ++c) dot = fmaf(__bfloat162float(f[c]), z[c], dot);
+  den_old[((size_t)bb * H + a) * T + i] = dot;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -702,13 +669,31 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct AuxLayout {
+  size_t fq, fk, zb, den, total;
+};
+AuxLayout aux_layout(int B, int T, int H, int dqk) {
+  const size_t BT = (size_t)B * T, nI = (size_t)(T + kBlk - 1) / kBlk;
+  AuxLayout L;
+  L.fq = 0;
+  L.fk = L.fq + a256(BT * dqk * 2);
+  L.zb = L.fk + a256(BT * dqk * 2);
+  L.den = L.zb + a256((size_t)B * H * nI * (dqk / H) * 4);
+  L.total = L.den + a256((size_t)B * H * T * 4);
+  return L;
+}
+
 }  // namespace
+
+size_t wango_aux_bytes(int B, int T, int H, int dqk) { return aux_layout(B, T, H, dqk).total; }
 
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   Args a = {};
   a.B = p.B; a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
   a.d_h = p.dqk / p.H; a.m_h = p.m / p.H;
-  a.W = p.window; a.phi_mode = p.phi_mode;
+  a.W = p.window;
   a.n_iblk = ceil_div(p.T, kBlk);
   a.n_ntile = ceil_div(a.m_h, kNg);
   const long long strips = (long long)p.B * p.H * a.n_ntile;
@@ -720,9 +705,31 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.err = p.err;
   a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
   a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
-  CUtensorMap mq, mk, mg, mv, mu;
-  cudaError_t e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
+
+  // pre-pass: feature maps, block sums, older-prefix denominators
+  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk);
+  char* aux = static_cast<char*>(p.aux);
+  __nv_bfloat16* fq = reinterpret_cast<__nv_bfloat16*>(aux + L.fq);
+  __nv_bfloat16* fk = reinterpret_cast<__nv_bfloat16*>(aux + L.fk);
+  float* zb = reinterpret_cast<float*>(aux + L.zb);
+  float* den = reinterpret_cast<float*>(aux + L.den);
+  const long long rows = (long long)p.B * p.T;
+  const long long work = rows * (p.dqk / 8);
+  wango_phi_kernel<<<(unsigned)((work + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, rows, p.H, p.dqk,
+      p.s, p.tau, p.phi_mode, p.err);
+  dim3 g3(a.n_iblk, p.H, p.B);
+  wango_blocksum_kernel<<<g3, a.d_h, 0, s>>>(fk, zb, p.T, p.H, p.dqk, a.n_iblk);
+  wango_denold_kernel<<<g3, kBlk, 0, s>>>(fq, zb, den, p.T, p.H, p.dqk, a.n_iblk, p.window);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  a.den_old = den;
+
+  CUtensorMap mq, mk, mfq, mfk, mg, mv, mu;
+  e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, a.d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mfq, fq, p.B, p.T, p.dqk, kBlk, a.d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mfk, fk, p.B, p.T, p.dqk, kBlk, a.d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
@@ -731,7 +738,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_strips < num_sms() ? a.n_strips : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mg, mv, mu, a);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mfq, mfk, mg, mv, mu, a);
   return cudaGetLastError();
 }
 
