@@ -139,6 +139,32 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return off ^ (((off >> 7) & mask) << 4);
 }
 
+// Weights of 32 sources of one row, written as 16 packed bf16 pairs.
+//   kMode 0: every source is in the window: exp2(c (s - 1)).
+//   kMode 1: window, but sources after the destination (j0 + e > i) get 0.
+//   kMode 2: general: 0 after i, exp2(c (s - 1)) in the window (j >= jw), else the
+//            feature-map score f (older source).
+template <int kMode>
+__device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
+                                          uint32_t (&p)[16], float (&dsum)[4]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float w0 = ex2_approx(fmaf(c, __uint_as_float(r[e]), -c));
+    float w1 = ex2_approx(fmaf(c, __uint_as_float(r[e + 1]), -c));
+    if (kMode == 2) {
+      if (j0 + e < jw) w0 = __uint_as_float(f[e]);
+      if (j0 + e + 1 < jw) w1 = __uint_as_float(f[e + 1]);
+    }
+    if (kMode >= 1) {
+      if (j0 + e > i) w0 = 0.f;
+      if (j0 + e + 1 > i) w1 = 0.f;
+    }
+    const uint32_t pk = pack_bf16x2(w0, w1);
+    dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
+    p[e / 2] = pk;
+  }
+}
+
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     wango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -413,32 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = named_bar_and(1, 256, ok);
           if (!ok) break;
           const int j0 = jb * kBlk + wg * 64;
+          const uint32_t ptm = sc - wg * 64 + wg * 32;  // P columns of these sources
+          const bool diag = jb == ib;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            uint32_t f[32];
+            uint32_t p[16];
             if (mixed) {
+              uint32_t f[32];
               tmem_ld32(sf + q * 32, f);
               tmem_ld_wait();
+              weights32<2>(r[q], f, c, j0 + q * 32, i, i - W + 1, p, dsum);
+            } else if (diag) {
+              weights32<1>(r[q], r[q], c, j0 + q * 32, i, 0, p, dsum);
+            } else {
+              weights32<0>(r[q], r[q], c, j0 + q * 32, i, 0, p, dsum);
             }
-            uint32_t p[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float w[2];
-#pragma unroll
-              for (int z = 0; z < 2; ++z) {
-                const int j = j0 + q * 32 + e + z;
-                float x = 0.f;
-                if (j <= i) {
-                  if (j >= i - W + 1) x = ex2_approx(fmaf(c, __uint_as_float(r[q][e + z]), -c));
-                  else x = mixed ? __uint_as_float(f[e + z]) : 0.f;
-                }
-                w[z] = x;
-              }
-              const uint32_t pk = pack_bf16x2(w[0], w[1]);
-              dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
-              p[e / 2] = pk;
-            }
-            tmem_st16(sc - wg * 64 + wg * 32 + q * 16, p);
+            tmem_st16(ptm + q * 16, p);
           }
           tmem_st_wait();
           tc_fence_before();
