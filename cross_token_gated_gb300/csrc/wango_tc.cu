@@ -23,21 +23,31 @@
 //     (128 jb <= 128 ib + 127 - W): its weights need both scores.  A block "leaves" when
 //     jb < jlo(ib + 1): after its P.G MMA the same G tile updates the state.
 //
-// Roles of the main kernel (16 warps; warps 2-3 idle):
-//   warp 0       TMA: qhat + Fq (one 32 KB buffer), khat + Fk (2-stage ring), and a
-//                3-stage ring of 32 KB stages carrying G blocks (128 sources x 128
-//                columns) and, after a destination block's sources, its v tile.
-//   warp 1       MMA issue (one thread), per destination block:
-//                  per source block: Sc = Qhat Khat^T (f32 slot); mixed: Sf = Fq Fk^T
-//                  (second slot); O (+)= P G; leaving: S^T += G^T Fk (M=128, N=d_h) in
-//                  TMEM; the next block's scores are issued early when slots allow;
-//                  last: O += Fq S_bf16 (read-out of the state before this block).
-//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of each block: exp
-//                (window), the feature-map score (older) or 0 (after i), rounded to bf16,
-//                summed into the row's denominator, written as P over the score slot.
-//   warps 12-15  epilogue O / den * v, u stored by TMA; then the copy S^T (TMEM, f32)
-//                -> S (shared memory, bf16) for the next destination block's read-out.
-// TMEM: O [0,128), S^T [128, 128+d_h), score slots [256,384) and [384,512).
+// Roles of the main kernel (16 warps; warp 3 idle):
+//   warp 0       TMA: qhat and Fq of the destination block (one buffer each), khat
+//                (2-stage ring), Fk of mixed blocks (one buffer), G blocks (128 sources
+//                x 128 columns, 2-stage ring of 32 KB) and the destination block's v
+//                tile (two 32 KB buffers, which also stage u for its TMA store).
+//   warps 1, 2   MMA issue, one thread each, on two SM sub-partitions.  Per destination
+//                block the source blocks go newest first (jb = ib .. jlo), so the
+//                mixed / leaving blocks come last; a unit is a whole block, or one
+//                64-source half of a mixed block.
+//                warp 1: a unit's scores into an f32 TMEM slot (ring of 2): Sc = Qhat
+//                Khat^T (128 columns), or for a half Sc (64 columns) beside Sf = Fq Fk^T
+//                (64 columns); it runs ahead as far as the slots allow.
+//                warp 2: O (+)= P G from the unit's slot, and the row sums of P (P times
+//                a tile of ones, N = 16: the denominator of the weights as applied);
+//                for a leaving block S^T += G^T Fk (M=128, N=d_h) in TMEM; last, the
+//                read-out O += Fq S_bf16 (the state before the block).
+//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of a block (or
+//                [32w, 32w+32) of a half): exp (window), the feature-map score (older) or
+//                0 (after i), rounded to bf16 and written as P over its own cos columns.
+//   warps 12-15  epilogue: gbar = O / den read out of TMEM into registers (rounded to
+//                bf16; O is released right after), u = gbar * v over v in shared memory,
+//                the copy S^T (TMEM, f32) -> S (shared memory, bf16) for the next
+//                destination block's read-out, then u stored by TMA.
+// TMEM: O [0,128), S^T [128, 128+d_h), row sums [192,208), score slots [256,384) and
+// [384,512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
 #include "tg_tc.h"
@@ -51,31 +61,36 @@ using namespace ptx;
 constexpr int kBlk = 128;
 constexpr int kNg = 128;       // gate columns per strip
 constexpr int kKStages = 2;
-constexpr int kGStages = 3;
+constexpr int kGStages = 2;
 constexpr int kThreads = 512;
 constexpr int kSoftWarp0 = 4, kEpiWarp0 = 12;
 constexpr uint32_t kTile = kBlk * 64 * 2;   // 16 KB: a 128 x d_h bf16 tile at d_h = 64
 constexpr uint32_t kGBox = 64 * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;     // 32 KB: 128 rows x 128 columns
-constexpr uint32_t kColO = 0, kColSt = 128, kColSlot0 = 256;
+// TMEM columns: O, the state S^T, the row sums of P, two score slots (P, in bf16 pairs,
+// is written over each warpgroup's own cos columns)
+constexpr uint32_t kColO = 0, kColSt = 128, kColDen = 192, kColSlot0 = 256;
+constexpr uint32_t kOnesBytes = 16 * 32;   // bf16 ones, 16 rows x 16 (K-major, 32-byte swizzle)
 
 struct __align__(8) Bars {
-  uint64_t q_full, q_empty;                     // qhat + Fq of a destination block
-  uint64_t k_full[kKStages], k_empty[kKStages]; // khat (+ Fk) of a source block
-  uint64_t g_full[kGStages], g_empty[kGStages];
-  uint64_t s_full[2], p_full[2];                // score slots; P of source blocks
+  uint64_t qh_full, qh_empty;                   // qhat of a destination block
+  uint64_t fq_full, fq_empty;                   // Fq of a destination block
+  uint64_t k_full[kKStages], k_empty[kKStages]; // khat of a source block
+  uint64_t fk_full, fk_empty;                   // Fk of a mixed block
+  uint64_t g_full[kGStages], g_empty[kGStages]; // G of a source block
+  uint64_t v_full[2], v_empty[2];               // v of a destination block, then its u
+  uint64_t s_full[2], p_full[2];                // score slots; P in them
+  uint64_t slot_free[2];                        // P.G and row sums have read a slot
   uint64_t o_full, o_empty;
   uint64_t st_full;                             // a destination block's MMAs are done
   uint64_t sb_full;                             // bf16 state copy in place
-  uint64_t den_full, den_empty;                 // P row sums -> epilogue
-  uint64_t drain, never;
+  uint64_t drain[2], never;
   uint32_t tmem_base;
   int abort;
-  float rowsum[2][kBlk];
 };
 
-// smem: Q | Fq | (K | Fk) x 2 | S_bf16 | G ring | Bars
-constexpr size_t kSmemBytes = 1024 + kTile * 7 + kGStage * kGStages + sizeof(Bars);
+// smem: Qhat | Fq | K x kKStages | Fk | S_bf16 | G x kGStages | V x 2 | ones | Bars
+constexpr size_t kSmemBytes = 1024 + kTile * (4 + kKStages) + kGStage * (kGStages + 2) + kOnesBytes + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
@@ -98,6 +113,12 @@ __host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
 }
 __device__ __forceinline__ bool is_mixed(int jb, int ib, int W) { return jb * kBlk <= ib * kBlk + kBlk - 1 - W; }
 __device__ __forceinline__ bool is_leaving(int jb, int ib, int W) { return jb < jlo_of(ib + 1, W); }
+// Slot column of P for 16-source step kk of a unit: warpgroup w writes the P of its
+// sources over its own cos columns, at 64 w for a whole block (h < 0, 4 steps each) and
+// at 32 w for a half (2 steps each).
+__device__ __forceinline__ uint32_t p_col(int kk, int h) {
+  return h < 0 ? (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8) : (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
+}
 
 struct Strip {
   int b, head, n0;
@@ -146,7 +167,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 //            feature-map score f (older source).
 template <int kMode>
 __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
-                                          uint32_t (&p)[16], float (&dsum)[4]) {
+                                          uint32_t (&p)[16]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
     float w0 = ex2_approx(fmaf(c, __uint_as_float(r[e]), -c));
@@ -159,9 +180,7 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
       if (j0 + e > i) w0 = 0.f;
       if (j0 + e + 1 > i) w1 = 0.f;
     }
-    const uint32_t pk = pack_bf16x2(w0, w1);
-    dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
-    p[e / 2] = pk;
+    p[e / 2] = pack_bf16x2(w0, w1);
   }
 }
 
@@ -177,24 +196,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t tile_bytes = kBlk * RB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;                  // qhat, then Fq at +kTile
-  uint8_t* sK = sQ + 2 * kTile;        // stage s: khat at s*2*kTile, Fk at +kTile
-  uint8_t* sSB = sK + 4 * kTile;       // bf16 state, [128 gate rows x d_h]
-  uint8_t* sG = sSB + kTile;
-  Bars& b = *reinterpret_cast<Bars*>(sG + kGStages * kGStage);
+  uint8_t* sQ = base;                  // qhat
+  uint8_t* sFQ = sQ + kTile;           // Fq
+  uint8_t* sK = sFQ + kTile;           // khat ring, kKStages tiles
+  uint8_t* sFK = sK + kKStages * kTile;
+  uint8_t* sSB = sFK + kTile;          // bf16 state, [128 gate rows x d_h]
+  uint8_t* sG = sSB + kTile;           // G ring
+  uint8_t* sV = sG + kGStages * kGStage;  // two v / u tiles
+  uint8_t* sOnes = sV + 2 * kGStage;      // B operand of the row-sum MMA
+  Bars& b = *reinterpret_cast<Bars*>(sOnes + kOnesBytes);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(&b.q_full, 1);
-    mbar_init(&b.q_empty, 1);
+    mbar_init(&b.qh_full, 1);
+    mbar_init(&b.qh_empty, 1);
+    mbar_init(&b.fq_full, 1);
+    mbar_init(&b.fq_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&b.s_full[s], 1);
+      mbar_init(&b.p_full[s], 8);
+      mbar_init(&b.slot_free[s], 1);
+      mbar_init(&b.v_full[s], 1);
+      mbar_init(&b.v_empty[s], 1);
+    }
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&b.k_full[s], 1);
       mbar_init(&b.k_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&b.s_full[s], 1);
-      mbar_init(&b.p_full[s], 8);
-    }
+    mbar_init(&b.fk_full, 1);
+    mbar_init(&b.fk_empty, 1);
     for (int s = 0; s < kGStages; ++s) {
       mbar_init(&b.g_full[s], 1);
       mbar_init(&b.g_empty[s], 1);
@@ -203,13 +233,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&b.o_empty, 4);
     mbar_init(&b.st_full, 1);
     mbar_init(&b.sb_full, 4);
-    mbar_init(&b.den_full, 8);
-    mbar_init(&b.den_empty, 4);
-    mbar_init(&b.drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&b.drain[s], 1);
+    }
     mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x < kOnesBytes / 4) reinterpret_cast<uint32_t*>(sOnes)[threadIdx.x] = 0x3f803f80u;
+  fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(&b.tmem_base, 512);
     tmem_relinquish();
@@ -222,187 +254,243 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Order per destination block: qhat; then, newest source block first, khat, Fq
+    // (before the first mixed block, else after the sources), Fk (mixed blocks), G;
+    // then the block's v.
     Ring kr, gr;
     bool ok = true;
-    uint32_t qph = 0, kmask = 0, gmask = 0, kph[kKStages] = {}, gph[kGStages] = {};
-    bool q_issued = false;
-    auto ring_load = [&](const CUtensorMap* map, int x, int y, int bb) -> bool {
-      if (!wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a)) return false;
-      uint8_t* dst = sG + gr.stage * kGStage;
-      if (map) {
-        mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
+    uint32_t kmask = 0, gmask = 0, kph[kKStages] = {}, gph[kGStages] = {}, vmask = 0, vph[2] = {};
+    uint32_t fkph = 0, qh_n = 0, fq_n = 0;  // Fk phase; qhat and Fq loads issued
+    bool fk_issued = false;
+    int dc = 0;  // destination blocks begun
+    auto tile128 = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int bb) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + h * 2 * kGBox + c * kGBox, map, &b.g_full[gr.stage], x + 64 * c, y + 64 * h, bb);
-        gmask |= 1u << gr.stage;
-        gph[gr.stage] = gr.phase;
-      } else {
-        mbar_arrive(&b.g_full[gr.stage]);
-      }
-      gr.next(kGStages);
-      return true;
+        for (int c = 0; c < 2; ++c) tma_load_3d(dst + h * 2 * kGBox + c * kGBox, map, bar, x + 64 * c, y + 64 * h, bb);
     };
     for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
       const Strip sp = strip_of(a, st);
       const int gx = sp.head * a.m_h + sp.n0;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
-        if (!(ok = wait_bar(&b.q_empty, qph ^ 1, b, a))) break;
-        mbar_arrive_expect_tx(&b.q_full, 2 * tile_bytes);
-        tma_load_3d(sQ, &tmQ, &b.q_full, sp.head * DH, ib * kBlk, sp.b);
-        tma_load_3d(sQ + kTile, &tmFQ, &b.q_full, sp.head * DH, ib * kBlk, sp.b);
-        q_issued = true;
-        qph ^= 1;
-        for (int jb = jlo_of(ib, W); ok && jb <= ib; ++jb) {
-          const bool need_fk = is_mixed(jb, ib, W) || is_leaving(jb, ib, W);
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
+        const uint32_t dp = dc & 1;
+        if (!(ok = wait_bar(&b.qh_empty, dp ^ 1, b, a))) break;
+        mbar_arrive_expect_tx(&b.qh_full, tile_bytes);
+        tma_load_3d(sQ, &tmQ, &b.qh_full, sp.head * DH, ib * kBlk, sp.b);
+        ++qh_n;
+        bool fq_loaded = false;
+        auto load_fq = [&]() -> bool {
+          if (!wait_bar(&b.fq_empty, dp ^ 1, b, a)) return false;
+          mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
+          tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
+          ++fq_n;
+          fq_loaded = true;
+          return true;
+        };
+        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
           if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
-          uint8_t* kdst = sK + kr.stage * 2 * kTile;
-          mbar_arrive_expect_tx(&b.k_full[kr.stage], need_fk ? 2 * tile_bytes : tile_bytes);
-          tma_load_3d(kdst, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
-          if (need_fk) tma_load_3d(kdst + kTile, &tmFK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
+          mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
+          tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
           kmask |= 1u << kr.stage;
           kph[kr.stage] = kr.phase;
           kr.next(kKStages);
-          ok = ring_load(&tmG, gx, jb * kBlk, sp.b);
+          if (is_mixed(jb, ib, W)) {
+            if (!fq_loaded && !(ok = load_fq())) break;
+            if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
+            mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
+            tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
+            fk_issued = true;
+            fkph ^= 1;
+          }
+          if (!(ok = wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a))) break;
+          mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
+          tile128(sG + gr.stage * kGStage, &tmG, &b.g_full[gr.stage], gx, jb * kBlk, sp.b);
+          gmask |= 1u << gr.stage;
+          gph[gr.stage] = gr.phase;
+          gr.next(kGStages);
         }
-        if (ok) ok = ring_load(a.has_v ? &tmV : nullptr, gx, ib * kBlk, sp.b);
+        if (!ok) break;
+        if (!fq_loaded && !(ok = load_fq())) break;
+        const int vb = dc & 1;
+        const uint32_t vp = (dc >> 1) & 1;
+        if (!(ok = wait_bar(&b.v_empty[vb], vp ^ 1, b, a))) break;
+        if (a.has_v) {
+          mbar_arrive_expect_tx(&b.v_full[vb], kGStage);
+          tile128(sV + vb * kGStage, &tmV, &b.v_full[vb], gx, ib * kBlk, sp.b);
+          vmask |= 1u << vb;
+          vph[vb] = vp;
+        } else {
+          mbar_arrive(&b.v_full[vb]);
+        }
       }
     }
-    if (q_issued) mbar_wait(&b.q_full, qph ^ 1, a.timeout_ns);
+    // no copy may be in flight when the CTA exits
+    if (qh_n) mbar_wait(&b.qh_full, (qh_n - 1) & 1, a.timeout_ns);
+    if (fq_n) mbar_wait(&b.fq_full, (fq_n - 1) & 1, a.timeout_ns);
+    if (fk_issued) mbar_wait(&b.fk_full, fkph ^ 1, a.timeout_ns);
     for (int s = 0; s < kKStages; ++s)
       if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
     for (int s = 0; s < kGStages; ++s)
       if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
+    for (int s = 0; s < 2; ++s)
+      if (vmask & (1u << s)) mbar_wait(&b.v_full[s], vph[s], a.timeout_ns);
   } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);   // scores
-    constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);     // O += P G
-    constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);    // O += Fq S
-    constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);       // S^T += G^T Fk
+    // ------------------------------------------------------------ MMA issue: scores
+    // Units in order; unit u's scores go into slot u & 1 once the P.G and row sums of
+    // unit u - 2 (the slot's previous user) have completed.
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);  // 128 sources
+    constexpr uint32_t idesc_h = idesc_bf16_f32(kBlk, 64, false, false);    // 64 sources
     const uint64_t qd = smem_desc(smem_u32(sQ), 16, sbo, lay);
-    const uint64_t fqd = smem_desc(smem_u32(sQ + kTile), 16, sbo, lay);
+    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
     const uint64_t kd0 = smem_desc(smem_u32(sK), 16, sbo, lay);
-    const uint64_t fkd0 = smem_desc(smem_u32(sK + kTile), 16, sbo, lay);
-    const uint64_t fkmn0 = smem_desc(smem_u32(sK + kTile), tile_bytes, sbo, lay);  // Fk as MN-major B
+    const uint64_t fkd = smem_desc(smem_u32(sFK), 16, sbo, lay);
+    bool ok = true;
+    Ring ks;
+    uint32_t u = 0, fkph = 0;
+    int dc = 0;
+    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
+        const int jlo = jlo_of(ib, W);
+        for (int jb = ib; ok && jb >= jlo; --jb) {
+          const bool mixed = is_mixed(jb, ib, W);
+          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
+            if (u >= 2 && !(ok = wait_bar(&b.slot_free[u & 1], ((u - 2) >> 1) & 1, b, a))) break;
+            if (!(ok = wait_bar(&b.qh_full, dc & 1, b, a))) break;
+            if (!(ok = wait_bar(&b.k_full[ks.stage], ks.phase, b, a))) break;
+            if (h >= 0 && !(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
+            if (h >= 0 && !(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
+            tc_fence_after_nc();
+            const uint64_t kd = kd0 + (uint64_t)((ks.stage * kTile) >> 4);
+            const uint32_t sc = tmem + kColSlot0 + (u & 1) * 128;
+            if (h < 0) {
+#pragma unroll
+              for (int kk = 0; kk < DH / 16; ++kk)
+                mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+            } else {
+              // cos scores of the half's 64 sources in columns [0, 64), feature-map
+              // scores in [64, 128)
+              const uint64_t hoff = (uint64_t)((h * 64 * RB) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < DH / 16; ++kk)
+                mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
+#pragma unroll
+              for (int kk = 0; kk < DH / 16; ++kk)
+                mma_bf16_ss_nc(sc + 64, fqd + (uint64_t)(kk * 2), fkd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
+            }
+            mma_commit_nc(&b.s_full[u & 1]);
+            ++u;
+            if (h != 0) {  // the block's last unit releases its khat
+              mma_commit_nc(&b.k_empty[ks.stage]);
+              ks.next(kKStages);
+            }
+            if (h == 1) fkph ^= 1;
+          }
+        }
+        if (ok) mma_commit_nc(&b.qh_empty);
+      }
+    }
+    mma_commit(&b.drain[0]);
+    mbar_wait(&b.drain[0], 0, a.timeout_ns);
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue: P.G, state
+    constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);   // O += P G
+    constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);  // O += Fq S
+    constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);     // S^T += G^T Fk
+    constexpr uint32_t idesc_d = idesc_bf16_f32(kBlk, 16, false, false);   // den += P 1
+    const uint64_t onesd = smem_desc(smem_u32(sOnes), 16, 256, kSwizzle32B);
+    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
+    const uint64_t fkmn = smem_desc(smem_u32(sFK), tile_bytes, sbo, lay);  // Fk as MN-major B
     const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
     const uint64_t gd0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
-    Ring kr, gr;
-    uint32_t qph = 0, oph = 0, sbph = 0;
-    uint32_t slot = 0;       // score slots used so far (ring of 2)
-    uint32_t blk = 0;        // source blocks whose P.G has been issued (p_full ring of 2)
-    bool first_update = true;
-    // Scores of one source block from khat stage `ks`: cos into the next slot, the
-    // feature-map scores of a mixed block into the one after.  Returns the cos slot.
-    auto issue_scores = [&](int ks, uint32_t kphase, bool mixed, bool& okr) -> uint32_t {
-      const uint32_t cs = slot;
-      if (!(okr = wait_bar(&b.k_full[ks], kphase, b, a))) return cs;
-      tc_fence_after_nc();
-      const uint64_t kd = kd0 + (uint64_t)((ks * 2 * kTile) >> 4);
-      const uint32_t sc = tmem + kColSlot0 + (slot & 1) * 128;
-#pragma unroll
-      for (int kk = 0; kk < DH / 16; ++kk)
-        mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
-      mma_commit_nc(&b.s_full[slot & 1]);
-      ++slot;
-      if (mixed) {
-        const uint32_t sf = tmem + kColSlot0 + (slot & 1) * 128;
-        const uint64_t fkd = fkd0 + (uint64_t)((ks * 2 * kTile) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk)
-          mma_bf16_ss_nc(sf, fqd + (uint64_t)(kk * 2), fkd + (uint64_t)(kk * 2), idesc_s, kk != 0);
-        mma_commit_nc(&b.s_full[slot & 1]);
-        ++slot;
-      }
-      return cs;
-    };
+    Ring gr;
+    uint32_t u = 0, oph = 0, sbph = 0;
+    int dc = 0;
     for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      first_update = true;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
-        if (!(ok = wait_bar(&b.q_full, qph, b, a))) break;
-        qph ^= 1;
+      bool first_update = true;
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
         const int jlo = jlo_of(ib, W);
-        bool copy_ready = false;  // the bf16 state copy for this block's read-out
-        uint32_t next_cs = 0;
-        bool next_issued = false;
-        for (int jb = jlo; ok && jb <= ib; ++jb) {
+        bool copy_ready = false;
+        for (int jb = ib; ok && jb >= jlo; --jb) {
           const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
-          uint32_t cs;
-          if (next_issued) {
-            cs = next_cs;
-            next_issued = false;
-          } else {
-            cs = issue_scores(kr.stage, kr.phase, mixed, ok);
-            if (!ok) break;
-          }
-          // the next block's scores go first when neither block needs two slots
-          if (jb < ib && !mixed && !is_mixed(jb + 1, ib, W)) {
-            Ring nk = kr;
-            nk.next(kKStages);
-            next_cs = issue_scores(nk.stage, nk.phase, false, ok);
-            if (!ok) break;
-            next_issued = true;
-          }
-          // O (+)= P G  (P in the block's cos slot); the first overwrites O once the
-          // epilogue has read the previous destination block's accumulator.
-          if (!(ok = wait_bar(&b.p_full[blk & 1], (blk >> 1) & 1, b, a))) break;
-          ++blk;
-          if (jb == jlo) {
-            if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
-            oph ^= 1;
-          }
-          if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
-          tc_fence_after_nc();
-          const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
-          const uint32_t ptm = tmem + kColSlot0 + (cs & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk) {
-            const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
-            mma_bf16_ts_nc(tmem + kColO, ptm + kk * 8, gd + (uint64_t)(goff >> 4), idesc_o,
-                           (jb == jlo && kk == 0) ? 0u : 1u);
-          }
-          if (leaving) {
-            // S^T += G^T Fk once the read-out copy of the previous state is taken
-            if (!copy_ready) {
-              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-              sbph ^= 1;
-              copy_ready = true;
-              tc_fence_after_nc();
+          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
+            // O (+)= P G; the first unit overwrites O once the epilogue has read the
+            // previous destination block's accumulator.
+            if (!(ok = wait_bar(&b.p_full[u & 1], (u >> 1) & 1, b, a))) break;
+            const bool first = jb == ib && h <= 0;
+            if (first) {
+              if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
+              oph ^= 1;
             }
-            const uint64_t fkmn = fkmn0 + (uint64_t)((kr.stage * 2 * kTile) >> 4);
+            if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
+            tc_fence_after_nc();
+            const uint32_t ptm = tmem + kColSlot0 + (u & 1) * 128;
+            const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
+            // 16-source steps of the block: all 8, or the 4 of half h.  Each step also
+            // adds P's row sums (P times a tile of ones) into the denominator columns:
+            // the denominator of the weights as applied.
+            if (h < 0) {
 #pragma unroll
-            for (int kk = 0; kk < kBlk / 16; ++kk) {
-              const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
-              mma_bf16_ss_nc(tmem + kColSt, gd + (uint64_t)(goff >> 4), fkmn + (uint64_t)((kk * 16 * RB) >> 4),
-                             idesc_u, (first_update && kk == 0) ? 0u : 1u);
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
+                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gd + (uint64_t)(goff >> 4), idesc_o, acc);
+                mma_bf16_ts_nc(tmem + kColDen, ptm + p_col(kk, h), onesd, idesc_d, acc);
+              }
+            } else {
+              const uint64_t gh = gd + (uint64_t)((h * 2 * kGBox) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gh + (uint64_t)((kk * 2048) >> 4), idesc_o, acc);
+                mma_bf16_ts_nc(tmem + kColDen, ptm + p_col(kk, h), onesd, idesc_d, acc);
+              }
             }
-            first_update = false;
+            if (leaving) {
+              // S^T += G^T Fk over this unit's sources, once the read-out copy of the
+              // previous state is taken (a leaving block is always mixed: h >= 0)
+              if (!copy_ready) {
+                if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+                sbph ^= 1;
+                copy_ready = true;
+                tc_fence_after_nc();
+              }
+              const uint64_t gh = gd + (uint64_t)((h * 2 * kGBox) >> 4);
+              const uint64_t fh = fkmn + (uint64_t)((h * 64 * RB) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss_nc(tmem + kColSt, gh + (uint64_t)((kk * 2048) >> 4), fh + (uint64_t)((kk * 16 * RB) >> 4),
+                               idesc_u, (first_update && kk == 0) ? 0u : 1u);
+              first_update = false;
+            }
+            mma_commit_nc(&b.slot_free[u & 1]);
+            ++u;
+            if (h != 0) {  // the block's last unit releases its G and Fk
+              mma_commit_nc(&b.g_empty[gr.stage]);
+              gr.next(kGStages);
+              if (h == 1) mma_commit_nc(&b.fk_empty);
+            }
           }
-          mma_commit_nc(&b.g_empty[gr.stage]);
-          gr.next(kGStages);
-          mma_commit_nc(&b.k_empty[kr.stage]);
-          kr.next(kKStages);
         }
         if (!ok) break;
         // read-out of the state before this block: O += Fq S_bf16
         if (!copy_ready) {
           if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
           sbph ^= 1;
-          tc_fence_after_nc();
         }
+        if (!(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
+        tc_fence_after_nc();
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk)
           mma_bf16_ss_nc(tmem + kColO, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, 1u);
-        mma_commit_nc(&b.q_empty);
+        mma_commit_nc(&b.fq_empty);
         mma_commit_nc(&b.st_full);
         mma_commit_nc(&b.o_full);
-        gr.next(kGStages);  // the v stage belongs to the epilogue
       }
     }
-    mma_commit(&b.drain);
-    mbar_wait(&b.drain, 0, a.timeout_ns);
+    mma_commit(&b.drain[1]);
+    mbar_wait(&b.drain[1], 0, a.timeout_ns);
   } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ weights
     const int wg = (warp - kSoftWarp0) / 4;  // sources [64 wg, 64 wg + 64) of each block
@@ -410,65 +498,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
-    uint32_t slot = 0, blk = 0;
-    int gib = 0;
+    uint32_t unit = 0;  // units processed
     for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
       const Strip sp = strip_of(a, st);
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
       const float c = tau * kLog2e;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
+      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
         const int i = ib * kBlk + row;
-        float dsum[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int jb = jlo_of(ib, W); jb <= ib; ++jb) {
+        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
           const bool mixed = is_mixed(jb, ib, W);
-          const uint32_t cs = slot;
-          const uint32_t sc = tmem + kColSlot0 + (cs & 1) * 128 + lane_off + wg * 64;
-          const uint32_t sf = tmem + kColSlot0 + ((cs + 1) & 1) * 128 + lane_off + wg * 64;
-          if (ok) ok = wait_bar(&b.s_full[cs & 1], (cs >> 1) & 1, b, a);
-          if (ok && mixed) ok = wait_bar(&b.s_full[(cs + 1) & 1], ((cs + 1) >> 1) & 1, b, a);
-          uint32_t r[2][32];
-          if (ok) {
+          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
+            const uint32_t n = unit++;
+            const uint32_t sl = tmem + kColSlot0 + (n & 1) * 128 + lane_off;
+            if (!(ok = wait_bar(&b.s_full[n & 1], (n >> 1) & 1, b, a))) break;
+            uint32_t r[2][32];
             tc_fence_after();
-            tmem_ld32(sc, r[0]);
-            tmem_ld32(sc + 32, r[1]);
-            tmem_ld_wait();
-          }
-          slot += mixed ? 2 : 1;
-          // P overwrites the first half of the cos slot: both warpgroups must have
-          // read their scores first.  The barrier also ANDs their status.
-          ok = named_bar_and(1, 256, ok);
-          if (!ok) break;
-          const int j0 = jb * kBlk + wg * 64;
-          const uint32_t ptm = sc - wg * 64 + wg * 32;  // P columns of these sources
-          const bool diag = jb == ib;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t p[16];
-            if (mixed) {
-              uint32_t f[32];
-              tmem_ld32(sf + q * 32, f);
-              tmem_ld_wait();
-              weights32<2>(r[q], f, c, j0 + q * 32, i, i - W + 1, p, dsum);
-            } else if (diag) {
-              weights32<1>(r[q], r[q], c, j0 + q * 32, i, 0, p, dsum);
-            } else {
-              weights32<0>(r[q], r[q], c, j0 + q * 32, i, 0, p, dsum);
+            if (h < 0) {  // cos scores of sources [64 wg, 64 wg + 64)
+              tmem_ld32(sl + wg * 64, r[0]);
+              tmem_ld32(sl + wg * 64 + 32, r[1]);
+            } else {      // cos and feature-map scores of sources [32 wg, 32 wg + 32) of the half
+              tmem_ld32(sl + wg * 32, r[0]);
+              tmem_ld32(sl + 64 + wg * 32, r[1]);
             }
-            tmem_st16(ptm + q * 16, p);
+            tmem_ld_wait();
+            // P (bf16 pairs) over this warpgroup's own cos columns, so the two
+            // warpgroups need not wait for each other
+            if (h < 0) {
+              const int j0 = jb * kBlk + wg * 64;
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                uint32_t p[16];
+                if (jb == ib) weights32<1>(r[q], r[q], c, j0 + q * 32, i, 0, p);
+                else weights32<0>(r[q], r[q], c, j0 + q * 32, i, 0, p);
+                tmem_st16(sl + wg * 64 + q * 16, p);
+              }
+            } else {
+              uint32_t p[16];
+              weights32<2>(r[0], r[1], c, jb * kBlk + h * 64 + wg * 32, i, i - W + 1, p);
+              tmem_st16(sl + wg * 32, p);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b.p_full[n & 1]);
           }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b.p_full[blk & 1]);
-          ++blk;
         }
-        if (!ok) break;
-        if (ok) ok = wait_bar(&b.den_empty, ((gib & 1) ^ 1), b, a);
-        ok = named_bar_and(1, 256, ok);
-        if (!ok) break;
-        b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b.den_full);
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -479,32 +553,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = (warp == kEpiWarp0 && lane == 0);
     bool ok = true;
     uint32_t oph = 0, stph = 0;
-    int gpos = 0, gib = 0;
+    int gib = 0;
     // bf16 copy of the state for a destination block's read-out (zero while no source
     // has left the window)
     auto copy_state = [&](bool empty) {
-      uint32_t sreg[DH];
-      if (!empty) {
-        tc_fence_after();
+      if (!empty) tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < DH; c += 16) {
-          uint32_t t16[16];
-          tmem_ld16(tmem + kColSt + lane_off + c, t16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sreg[c + e] = t16[e];
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < DH; c += 8) {
-        uint4 o = make_uint4(0, 0, 0, 0);
+      for (int c0 = 0; c0 < DH; c0 += 16) {
+        uint32_t t16[16];
         if (!empty) {
-          o.x = pack_bf16x2(__uint_as_float(sreg[c]), __uint_as_float(sreg[c + 1]));
-          o.y = pack_bf16x2(__uint_as_float(sreg[c + 2]), __uint_as_float(sreg[c + 3]));
-          o.z = pack_bf16x2(__uint_as_float(sreg[c + 4]), __uint_as_float(sreg[c + 5]));
-          o.w = pack_bf16x2(__uint_as_float(sreg[c + 6]), __uint_as_float(sreg[c + 7]));
+          tmem_ld16(tmem + kColSt + lane_off + c0, t16);
+          tmem_ld_wait();
         }
-        st_shared_v4(smem_u32(sSB) + swz<RB>(row, c), o);
+#pragma unroll
+        for (int c = 0; c < 16; c += 8) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (!empty) {
+            o.x = pack_bf16x2(__uint_as_float(t16[c]), __uint_as_float(t16[c + 1]));
+            o.y = pack_bf16x2(__uint_as_float(t16[c + 2]), __uint_as_float(t16[c + 3]));
+            o.z = pack_bf16x2(__uint_as_float(t16[c + 4]), __uint_as_float(t16[c + 5]));
+            o.w = pack_bf16x2(__uint_as_float(t16[c + 6]), __uint_as_float(t16[c + 7]));
+          }
+          st_shared_v4(smem_u32(sSB) + swz<RB>(row, c0 + c), o);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -515,72 +586,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Strip sp = strip_of(a, st);
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
       copy_state(true);  // read-out of block 0: empty state
+      const float null_w = a.null_bias ? exp2f((a.null_bias[sp.head] - tau) * kLog2e) : 0.f;
       for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
         const int i = ib * kBlk + row;
-        gpos += ib - jlo_of(ib, W) + 1;  // the block's G stages
-        const int sv = gpos % kGStages;
-        const uint32_t pv = (gpos / kGStages) & 1;
-        ++gpos;                           // its v stage
-        float den = 0.f;
-        if (ok) ok = wait_bar(&b.den_full, gib & 1, b, a);
-        if (ok) {
-          den = b.rowsum[0][row] + b.rowsum[1][row];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b.den_empty);
-        }
-        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
+        const bool row_ok = i < a.T;
+        const int sv = gib & 1;  // v tile buffer
+        const uint32_t pv = (gib >> 1) & 1;
+        // older-prefix denominator, fetched before the waits
+        float den = row_ok ? a.den_old[((size_t)sp.b * a.H + sp.head) * a.T + i] : 0.f;
+        den += (float)(i + 1) * null_w;
         if (ok) ok = wait_bar(&b.o_full, oph, b, a);
-        if (ok) ok = wait_bar(&b.g_full[sv], pv, b, a);
+        ok = named_bar_and(2, 128, ok);
+        if (!ok) break;
+        oph ^= 1;
+        tc_fence_after();
+        // + the row sum of this block's per-pair weights, as applied (bf16)
+        den += __uint_as_float(tmem_ld1_wait(tmem + kColDen + lane_off));
+        const float inv = 1.f / den;
+        // gbar = O / den, rounded to bf16, in registers; the accumulator is released as
+        // soon as it has been read
+        uint32_t gb[kNg / 2];
+#pragma unroll
+        for (int c0 = 0; c0 < kNg; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + kColO + lane_off + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            gb[(c0 + e) / 2] = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.o_empty);
+        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
+        if (ok) ok = wait_bar(&b.v_full[sv], pv, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
         stph ^= 1;
-        oph ^= 1;
-        const bool row_ok = i < a.T;
-        if (row_ok) den += a.den_old[((size_t)sp.b * a.H + sp.head) * a.T + i];
-        if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[sp.head] - tau) * kLog2e);
-        const float inv = 1.f / den;
-        // the state copy for the next destination block (this block's updates and
-        // read-out are complete), then the accumulator
-        if (ib + 1 < a.n_iblk) copy_state(jlo_of(ib + 1, W) == 0);
-        tc_fence_after();
-        const uint32_t vst = smem_u32(sG + sv * kGStage);
+        // u = gbar * v, written over v in shared memory (the TMA store's source)
+        const uint32_t vst = smem_u32(sV + sv * kGStage);
         const int rh = row >> 6, rr = row & 63;
         const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
-        // the accumulator in two 64-column halves; it is released after the second
-#pragma unroll 1
+#pragma unroll
         for (int cq = 0; cq < 2; ++cq) {
-          uint32_t o[2][32];
-          tmem_ld32(tmem + kColO + lane_off + cq * 64, o[0]);
-          tmem_ld32(tmem + kColO + lane_off + cq * 64 + 32, o[1]);
-          tmem_ld_wait();
-          if (cq == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&b.o_empty);
-          }
           const int col0 = sp.n0 + cq * 64;
           const bool straddle = col0 < a.m_h && col0 + 64 > a.m_h;
           const uint32_t box = vst + rh * 2 * kGBox + cq * kGBox + rr * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
-            const uint4 vv = a.has_v ? ld_shared_v4(addr) : make_uint4(0, 0, 0, 0);
-            const uint32_t* o8 = &o[k >> 2][(k & 3) * 8];
+            const uint32_t* g4 = &gb[cq * 32 + k * 4];
             uint32_t u[4];
+            if (a.has_v) {
+              const uint4 vv = ld_shared_v4(addr);
+              u[0] = mul_bf16x2(g4[0], vv.x);
+              u[1] = mul_bf16x2(g4[1], vv.y);
+              u[2] = mul_bf16x2(g4[2], vv.z);
+              u[3] = mul_bf16x2(g4[3], vv.w);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float y0 = __uint_as_float(o8[2 * e]) * inv, y1 = __uint_as_float(o8[2 * e + 1]) * inv;
-              if (a.has_v) {
-                const uint32_t vw = e == 0 ? vv.x : e == 1 ? vv.y : e == 2 ? vv.z : vv.w;
-                y0 *= bf16lo(vw);
-                y1 *= bf16hi(vw);
-              }
-              u[e] = pack_bf16x2(y0, y1);
+              for (int e = 0; e < 4; ++e) u[e] = g4[e];
             }
             if (!straddle) st_shared_v4(addr, make_uint4(u[0], u[1], u[2], u[3]));
             else if (row_ok && col0 + 8 * k < a.m_h) st_global_v4(a.out + grow + col0 + 8 * k, u[0], u[1], u[2], u[3]);
           }
         }
+        // the state copy for the next destination block (this block's updates and
+        // read-out are complete; the next block updates the state only after it)
+        if (ib + 1 < a.n_iblk) copy_state(jlo_of(ib + 1, W) == 0);
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (issuer) {
@@ -590,12 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cq = 0; cq < 2; ++cq) {
               const int col0 = sp.n0 + cq * 64;
               if (col0 + 64 > a.m_h) continue;
-              tma_store_3d(&tmU, sG + sv * kGStage + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
+              tma_store_3d(&tmU, sV + sv * kGStage + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
             }
           }
           bulk_commit_group();
           bulk_wait_group_read0();
-          mbar_arrive(&b.g_empty[sv]);
+          mbar_arrive(&b.v_empty[sv]);
         }
       }
     }

@@ -53,6 +53,8 @@ SMALL = [
     (1, 200, 2, 128, 1040, 200),  # W = T: no older prefix
     (2, 130, 4, 128, 544, 300),   # W > T, four heads of d_h = 32
     (1, 300, 2, 128, 2096, 129),  # ragged window boundary
+    (1, 700, 2, 128, 272, 200),   # two mixed blocks in a row, window > one block
+    (2, 520, 2, 64, 144, 100),    # W < block: the diagonal block is mixed too
 ]
 
 
