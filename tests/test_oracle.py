@@ -338,6 +338,23 @@ def test_block_rope_relative_position():
     assert not np.allclose(on["q"][0, 1], off["q"][0, 1])
 
 
+def test_model_logits_one_hot_closed_form():
+    """h_t = c e_k gives RMSNorm(h_t) = sign(c) sqrt(d) gamma_k e_k (eps = 0); with the
+    one-hot tied matrix E[v] = e_(v mod d) the logit of v is that value when
+    v mod d == k and 0 otherwise.  Pins the normaliser's sqrt(d), the gain's index and
+    the orientation of E."""
+    d, vocab = 8, 19
+    E = np.zeros((vocab, d))
+    E[np.arange(vocab), np.arange(vocab) % d] = 1.0
+    gam = 1.0 + np.arange(d) / 10.0
+    for k, c in ((3, 2.5), (6, -0.7)):
+        h = np.zeros((1, d))
+        h[0, k] = c
+        got = oracle.final_logits(h, gam, E, rms_eps=0.0)[0]
+        want = np.where(np.arange(vocab) % d == k, np.sign(c) * np.sqrt(d) * gam[k], 0.0)
+        np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-14)
+
+
 def test_model_logits_rmsnorm_scale_invariance():
     """Final RMSNorm then tied logits: logits(c * h) = logits(h) for eps -> 0, and
     logits equal RMSNorm(h) @ E^T (numpy matrix product)."""
