@@ -511,28 +511,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t n = unit++;
             const uint32_t sl = tmem + kColSlot0 + (n & 1) * 128 + lane_off;
             if (!(ok = wait_bar(&b.s_full[n & 1], (n >> 1) & 1, b, a))) break;
-            uint32_t r[2][32];
             tc_fence_after();
-            if (h < 0) {  // cos scores of sources [64 wg, 64 wg + 64)
-              tmem_ld32(sl + wg * 64, r[0]);
-              tmem_ld32(sl + wg * 64 + 32, r[1]);
-            } else {      // cos and feature-map scores of sources [32 wg, 32 wg + 32) of the half
-              tmem_ld32(sl + wg * 32, r[0]);
-              tmem_ld32(sl + 64 + wg * 32, r[1]);
-            }
-            tmem_ld_wait();
             // P (bf16 pairs) over this warpgroup's own cos columns, so the two
-            // warpgroups need not wait for each other
-            if (h < 0) {
+            // warpgroups need not wait for each other.  One 32-source group at a time
+            // (a rolled loop keeps the code small).
+            if (h < 0) {  // cos scores of sources [64 wg, 64 wg + 64); causal limit on the diagonal
               const int j0 = jb * kBlk + wg * 64;
-#pragma unroll
+              const int ilim = jb == ib ? i : 0x7fffffff;
+#pragma unroll 1
               for (int q = 0; q < 2; ++q) {
-                uint32_t p[16];
-                if (jb == ib) weights32<1>(r[q], r[q], c, j0 + q * 32, i, 0, p);
-                else weights32<0>(r[q], r[q], c, j0 + q * 32, i, 0, p);
+                uint32_t rq[32], p[16];
+                tmem_ld32(sl + wg * 64 + q * 32, rq);
+                tmem_ld_wait();
+                weights32<1>(rq, rq, c, j0 + q * 32, ilim, 0, p);
                 tmem_st16(sl + wg * 64 + q * 16, p);
               }
-            } else {
+            } else {      // cos and feature-map scores of sources [32 wg, 32 wg + 32) of the half
+              uint32_t r[2][32];
+              tmem_ld32(sl + wg * 32, r[0]);
+              tmem_ld32(sl + 64 + wg * 32, r[1]);
+              tmem_ld_wait();
               uint32_t p[16];
               weights32<2>(r[0], r[1], c, jb * kBlk + h * 64 + wg * 32, i, i - W + 1, p);
               tmem_st16(sl + wg * 32, p);
