@@ -139,23 +139,27 @@ __device__ __forceinline__ uint32_t qk_layout(int d_h) {
 // 64 scores of one row (columns [64w, 64w+64) of a block): weights exp2(c (s - 1)),
 // with sources after the destination zeroed on the diagonal block, rounded to bf16
 // and written as P at TMEM columns [32w, 32w+32) of the score buffer; the rounded
-// weights are added to four partial denominators.
+// weights are added to two partial denominators, each a pair of f32.  The exponent
+// argument and the sums use packed f32x2 arithmetic (two values per instruction).
 template <bool kDiag>
 __device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p_tm, float c, int row,
-                                          int src0, float (&dsum)[4]) {
+                                          int src0, uint64_t (&dsum2)[2]) {
+  const uint64_t cc = f32x2_pack(c, c), nc = f32x2_pack(-c, -c);
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     uint32_t p[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      float w0 = ex2_approx(fmaf(c, __uint_as_float(r[q][e]), -c));
-      float w1 = ex2_approx(fmaf(c, __uint_as_float(r[q][e + 1]), -c));
+      float x0, x1;
+      f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), cc, nc), x0, x1);
+      float w0 = ex2_approx(x0);
+      float w1 = ex2_approx(x1);
       if (kDiag) {
         if (src0 + q * 32 + e > row) w0 = 0.f;
         if (src0 + q * 32 + e + 1 > row) w1 = 0.f;
       }
       const uint32_t pk = pack_bf16x2(w0, w1);
-      dsum[(e >> 1) & 3] += bf16lo(pk) + bf16hi(pk);
+      dsum2[(e >> 1) & 1] = add_f32x2(dsum2[(e >> 1) & 1], bf16x2_widen(pk));
       p[e / 2] = pk;
     }
     tmem_st16(p_tm + q * 16, p);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = seq.t;
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       const float c = tau * kLog2e;
-      float dsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      uint64_t dsum2[2] = {0, 0};  // independent partial sums, pairs of f32
       const int nj = t.ib + 1;
       for (int j = 0; j < nj; ++j, ++J) {
         const uint32_t buf = J & 1;
@@ -380,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = named_bar_and(1, 256, ok);
         if (!ok) break;
         const int src0 = (j - t.ib) * kBlk + wg * 64;  // relative to the destination block
-        if (src0 + 63 > 0) softmax64<true>(r, stm + wg * 32, c, row, src0, dsum);
-        else softmax64<false>(r, stm + wg * 32, c, row, src0, dsum);
+        if (src0 + 63 > 0) softmax64<true>(r, stm + wg * 32, c, row, src0, dsum2);
+        else softmax64<false>(r, stm + wg * 32, c, row, src0, dsum2);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -393,7 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = wait_bar(&b.den_empty, ((tc & 1) ^ 1), b, a);
       ok = named_bar_and(1, 256, ok);
       if (!ok) break;
-      b.rowsum[wg][row] = (dsum[0] + dsum[1]) + (dsum[2] + dsum[3]);
+      float d0, d1, d2, d3;
+      f32x2_unpack(dsum2[0], d0, d1);
+      f32x2_unpack(dsum2[1], d2, d3);
+      b.rowsum[wg][row] = (d0 + d1) + (d2 + d3);
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.den_full);
     }

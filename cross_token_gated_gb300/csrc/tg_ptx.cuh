@@ -243,6 +243,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// Packed pairs of f32 (Blackwell f32x2 arithmetic: one instruction for two lanes' worth).
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// A packed bf16 pair widened to two f32 (exact): low half, high half.
+__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t pk) {
+  return f32x2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
+}
+
 // One column, waited for inside the same statement (the value is usable on return).
 __device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr) {
   uint32_t r;

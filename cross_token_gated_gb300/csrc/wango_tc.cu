@@ -168,10 +168,13 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <int kMode>
 __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
                                           uint32_t (&p)[16]) {
+  const uint64_t cc = f32x2_pack(c, c), nc = f32x2_pack(-c, -c);
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    float w0 = ex2_approx(fmaf(c, __uint_as_float(r[e]), -c));
-    float w1 = ex2_approx(fmaf(c, __uint_as_float(r[e + 1]), -c));
+    float x0, x1;  // c (s - 1) for two sources in one packed f32x2 instruction
+    f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), cc, nc), x0, x1);
+    float w0 = ex2_approx(x0);
+    float w1 = ex2_approx(x1);
     if (kMode == 2) {
       if (j0 + e < jw) w0 = __uint_as_float(f[e]);
       if (j0 + e + 1 < jw) w1 = __uint_as_float(f[e + 1]);
