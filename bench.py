@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-also", action="store_true")
     ap.add_argument("--agg-only", choices=["tango", "wango"],
                     help="only run one aggregation kernel (for profiler captures)")
+    ap.add_argument("--block-only", action="store_true",
+                    help="only run the block forward at batch --agg-B (for profiler captures)")
     ap.add_argument("--agg-B", type=int, default=2)
     ap.add_argument("--agg-T", type=int, default=2048)
     ap.add_argument("--agg-iters", type=int, default=3)
@@ -217,6 +219,9 @@ def main():
         return
     if args.agg_only:
         run_agg_only(args)
+        return
+    if args.block_only:
+        run_block_only(args)
         return
     import torch
     import torch.distributed as dist
@@ -441,6 +446,32 @@ def run_agg_only(args):
     st, word = tg.tg_check_device_error()
     dt = (time.perf_counter() - t0) / args.agg_iters
     print(json.dumps({"agg_only": args.agg_only, "B": b, "T": t_len, "status": st, "word": word,
+                      "wall_ms_per_launch": dt * 1e3}))
+    if st != tg.TG_OK:
+        sys.exit(1)
+
+
+def run_block_only(args):
+    """A few block forwards (TANGO) at batch --agg-B and T = --agg-T, for profiler
+    captures of the GEMMs; prints one timing line."""
+    import torch
+
+    import cross_token_gated_gb300 as tg
+    from cross_token_gated_gb300 import synth
+    dev = torch.device("cuda", 0)
+    b, t_len = args.agg_B, args.agg_T
+    h, w = synth.block_inputs(b, t_len, D, DQK, M, seed=0, dtype="bf16")
+    hd = h.to(dev)
+    wd = {n: x.to(dev) for n, x in w.items()}
+    out = torch.empty_like(hd)
+    ws = tg.block_workspace(b, t_len, D, H, DQK, M, dtype=tg.TG_BF16, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.agg_iters):
+        tg.tango_block_forward(hd, wd, out, H=H, ws=ws)
+    st, word = tg.tg_check_device_error()
+    dt = (time.perf_counter() - t0) / args.agg_iters
+    print(json.dumps({"block_only": True, "B": b, "T": t_len, "status": st, "word": word,
                       "wall_ms_per_launch": dt * 1e3}))
     if st != tg.TG_OK:
         sys.exit(1)

@@ -8,7 +8,9 @@
 // in tensor memory.  Persistent kernel, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer (4-stage ring of 128x64 A and 256x64 B tiles, 128B swizzle)
 //   warp 1      TMEM allocator and MMA issuer (128x256x16 tcgen05.mma, one thread)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, fused elementwise, bf16 stores
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, fused elementwise, bf16 out:
+//               g and v through shared memory and TMA stores (64-column chunks),
+//               q/k and the residual output by direct stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile overlap the
 // main loop of the next.  Every wait is bounded; on expiry the kernel records a
 // timeout in the error word and all roles leave their loops.
@@ -29,6 +31,7 @@ constexpr int kStages = 4;
 constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kThreads = 192;
+constexpr uint32_t kOutBytes = BM * 64 * 2;  // 16 KB: one 128 x 64 bf16 output chunk (staging for TMA)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum Seg : int { kSegQK = 0, kSegG = 1, kSegV = 2, kSegOut = 3 };
@@ -53,7 +56,8 @@ struct __align__(8) Bars {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 2 * kOutBytes + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Tile {
   int seg, nb, mb;
@@ -137,12 +141,14 @@ __device__ __forceinline__ void rope_norm_store(uint32_t taddr, __nv_bfloat16* d
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                   const __grid_constant__ CUtensorMap tmB3, const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmOG,
+                   const __grid_constant__ CUtensorMap tmOV, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + kStages * kABytes;
-  Bars& b = *reinterpret_cast<Bars*>(sB + kStages * kBBytes);
+  uint8_t* sOut = sB + kStages * kBBytes;  // two output chunks staged for TMA stores
+  Bars& b = *reinterpret_cast<Bars*>(sOut + 2 * kOutBytes);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int ntiles = a.n_mblk * (a.nb_qk + a.nb_g + a.nb_v + a.nb_out);
   const int nkb = (a.K + BK - 1) / BK;
@@ -238,11 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. 32*quarter+31
-    int acc = 0;
+    const int lrow = quarter * 32 + lane;  // row of the tile
+    const bool issuer = warp == 2 && lane == 0;
+    int acc = 0, ob = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(a, t);
-      if (!wait_bar(&b.acc_full[acc], acc_phase, b, a.err)) break;
+      bool ok = wait_bar(&b.acc_full[acc], acc_phase, b, a.err);
+      // the four epilogue warps agree (they meet at named barriers below)
+      if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
       const int row = tl.mb * BM + quarter * 32 + lane;
       const uint32_t trow = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
@@ -257,13 +267,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (d_h == 32) rope_norm_store<32>(trow + col, dst, t_pos, valid, a);
           else rope_norm_store<16>(trow + col, dst, t_pos, valid, a);
         }
-      } else {
-        const int N = tl.seg == kSegOut ? a.d : a.m;
+      } else if (tl.seg != kSegOut) {
+        // g = SiLU(x W_g^T) or v = x W_v^T: 64-column chunks in bf16, staged in shared
+        // memory (128-byte swizzle) and written by TMA stores, two buffers in turn
+        const CUtensorMap* om = tl.seg == kSegG ? &tmOG : &tmOV;
         const int n0 = tl.nb * BN;
-        __nv_bfloat16* dst;
-        if (tl.seg == kSegG) dst = a.g;
-        else if (tl.seg == kSegV) dst = a.v;
-        else dst = a.h_out;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          uint32_t r[2][32];
+          tmem_ld32(trow + c0, r[0]);
+          tmem_ld32(trow + c0 + 32, r[1]);
+          tmem_ld_wait();
+          if (n0 + c0 >= a.m) continue;  // the same for every thread of the CTA
+          if (issuer) bulk_wait_group_read1();  // this buffer's previous store has read it
+          named_bar_sync(1, 128);
+          const uint32_t sb = smem_u32(sOut + ob * kOutBytes) + (uint32_t)lrow * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* x = &r[k >> 2][(k & 3) * 8];
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = tl.seg == kSegG ? silu(__uint_as_float(x[e])) : __uint_as_float(x[e]);
+            st_shared_v4(sb + (uint32_t)((k ^ (lrow & 7)) << 4),
+                         make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                    pack_bf16x2(y[6], y[7])));
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (issuer) {
+            tma_store_2d(om, sOut + ob * kOutBytes, n0 + c0, tl.mb * BM);  // rows past M are clipped
+            bulk_commit_group();
+          }
+          ob ^= 1;
+        }
+      } else {
+        const int N = a.d;
+        const int n0 = tl.nb * BN;
+        __nv_bfloat16* dst = a.h_out;
         const size_t rowoff = (size_t)row * N;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -274,10 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float y[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(r[c]);
-          if (tl.seg == kSegG) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) y[c] = silu(y[c]);
-          } else if (tl.seg == kSegOut) {
+          {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               if (n0 + c0 + 8 * u >= N) break;
@@ -303,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
+  if (warp == 2 && lane == 0) bulk_wait_group0();  // every TMA store has completed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -319,20 +357,23 @@ int num_sms() {
 }
 
 cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& m2,
-                   const CUtensorMap& m3, const GemmArgs& a, cudaStream_t s) {
+                   const CUtensorMap& m3, const CUtensorMap& mog, const CUtensorMap& mov, const GemmArgs& a,
+                   cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int ntiles = a.n_mblk * (a.nb_qk + a.nb_g + a.nb_v + a.nb_out);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mA, m0, m1, m2, m3, a);
+  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mA, m0, m1, m2, m3, mog, mov, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
-  CUtensorMap mA, mq, mk, mg, mv;
+  CUtensorMap mA, mq, mk, mg, mv, mog, mov;
   cudaError_t e = make_tmap_2d(&mA, p.x, p.M, p.d, p.d, BM, BK);
+  if (e == cudaSuccess) e = make_tmap_2d(&mog, p.g, p.M, p.m, p.m, BM, 64);
+  if (e == cudaSuccess) e = make_tmap_2d(&mov, p.v, p.M, p.m, p.m, BM, 64);
   if (e == cudaSuccess) e = make_tmap_2d(&mq, p.Wq, p.dqk, p.d, p.d, p.dqk, BK);
   if (e == cudaSuccess) e = make_tmap_2d(&mk, p.Wk, p.dqk, p.d, p.d, p.dqk, BK);
   if (e == cudaSuccess) e = make_tmap_2d(&mg, p.Wg, p.m, p.d, p.d, BN, BK);
@@ -352,7 +393,7 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   a.g = static_cast<__nv_bfloat16*>(p.g);
   a.v = static_cast<__nv_bfloat16*>(p.v);
   a.err = p.err;
-  return launch(mA, mq, mk, mg, mv, a, s);
+  return launch(mA, mq, mk, mg, mv, mog, mov, a, s);
 }
 
 cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_out, int M, int d, int m,
@@ -370,7 +411,7 @@ cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_
   a.h = static_cast<const __nv_bfloat16*>(h);
   a.h_out = static_cast<__nv_bfloat16*>(h_out);
   a.err = err;
-  return launch(mA, mo, mo, mo, mo, a, s);
+  return launch(mA, mo, mo, mo, mo, mo, mo, a, s);
 }
 
 }  // namespace tg
