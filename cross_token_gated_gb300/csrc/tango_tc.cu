@@ -14,12 +14,13 @@
 //   warp 0       TMA: qhat tiles (2 buffers), khat blocks (2-stage ring), and one ring
 //                of 32 KB stages (5 of them) that carries, per tile, G in half blocks
 //                of 64 sources x 256 columns and then the tile's v (2 stages).
-//   warp 1       TMEM allocation; MMA issue from one thread:
-//                  S_j = Qhat Khat_j^T   (M=128, N=128, K=d_h)     -> TMEM S[J % 2]
-//                  O  += P_j G_j         (M=128, N=256, K=64 x 2)  A = P_j from TMEM
-//                J counts source blocks over all tiles of the CTA.  S_{j+1} is issued
-//                before O += P_j G_j.  The issue path keeps descriptors in registers
-//                and avoids compiler memory barriers.
+//   warps 1, 2   MMA issue, one thread each on two SM sub-partitions (J counts source
+//                blocks over all tiles of the CTA):
+//                  warp 2: S_J = Qhat Khat_J^T (M=128, N=128, K=d_h) -> TMEM slot J % 2,
+//                          once the P.G of block J - 2 has completed;
+//                  warp 1: O += P_J G_J (M=128, N=256, K=64 x 2), A = P_J from TMEM;
+//                          warp 1 also allocates TMEM.
+//                Both keep descriptors in registers and avoid compiler memory barriers.
 //   warps 4-11   softmax: warpgroup w takes columns [64w, 64w+64) of every score block;
 //                one row per thread from TMEM, exp2(tau log2e (s - 1)) with the causal
 //                mask on the diagonal block, rounded to bf16; the ROUNDED weights are
@@ -59,7 +60,8 @@ struct __align__(8) Bars {
   uint64_t g_full[kGStages], g_empty[kGStages];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, o_empty, den_full, den_empty;
-  uint64_t drain, never;
+  uint64_t slot_free[2];                         // the P.G of a slot's block has completed
+  uint64_t drain[2], never;
   uint32_t tmem_base;
   int abort;
   float rowsum[2][kBlk];
@@ -218,7 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&b.o_empty, 4);
     mbar_init(&b.den_full, 8);
     mbar_init(&b.den_empty, 4);
-    mbar_init(&b.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.slot_free[i], 1);
+      mbar_init(&b.drain[i], 1);
+    }
     mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
@@ -283,10 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
     for (int s = 0; s < kGStages; ++s)
       if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue: scores
+    // S_J = Qhat Khat_J^T into slot J % 2 once the P.G of block J - 2 (the slot's
+    // previous user) has completed.
     const uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);
-    const uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);
     const uint32_t lay = qk_layout(a.d_h);
     const uint32_t sbo = 8u * a.d_h * 2u;
     const int ksteps = a.d_h / 16;
@@ -294,44 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ((byte offset) >> 4 added to the low bits, which never carry: smem < 256 KB).
     const uint64_t qdesc0 = smem_desc(smem_u32(sQ), 16, sbo, lay);
     const uint64_t kdesc0 = smem_desc(smem_u32(sK), 16, sbo, lay);
-    const uint64_t gdesc0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
     bool ok = true;
-    if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
-    Ring kr, gr;
-    uint32_t ophase = 0;
-    uint32_t J = 0;  // source blocks issued by this CTA
-    // O += P_jj G_jj (two half blocks); the tile's first block overwrites O once the
-    // epilogue has read the previous tile's accumulator out of TMEM.
-    auto issue_pg = [&](uint32_t jj, bool first) -> bool {
-      const uint32_t buf = jj & 1;
-      if (!wait_bar(&b.p_full[buf], (jj >> 1) & 1, b, a)) return false;
-      if (first) {
-        if (!wait_bar(&b.o_empty, ophase ^ 1, b, a)) return false;
-        ophase ^= 1;
-      }
-      const uint32_t ptm = tmem + kColS0 + buf * 128;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!wait_bar(&b.g_full[gr.stage], gr.phase, b, a)) return false;
-        tc_fence_after_nc();
-        const uint64_t gd = gdesc0 + (uint64_t)((gr.stage * kGStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk)
-          mma_bf16_ts_nc(tmem + kColO, ptm + h * 32 + kk * 8, gd + (uint64_t)(kk * (2048 >> 4)), idesc_o,
-                         (first && h == 0 && kk == 0) ? 0u : 1u);
-        mma_commit_nc(&b.g_empty[gr.stage]);
-        gr.next(kGStages);
-      }
-      return true;
-    };
+    Ring kr;
+    uint32_t J = 0;  // source blocks of this CTA
     TileSeq seq;
     int tc = 0;
-    for (bool have = ok && seq.first(a); ok && have; have = seq.next(a), ++tc) {
+    for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
       const int qb = tc & 1;
       if (!(ok = wait_bar(&b.q_full[qb], (tc >> 1) & 1, b, a))) break;
       const uint64_t qd = qdesc0 + (uint64_t)((qb * kQKMax) >> 4);
       const int nj = seq.t.ib + 1;
       for (int j = 0; j < nj; ++j, ++J) {
+        if (J >= 2 && !(ok = wait_bar(&b.slot_free[J & 1], ((J - 2) >> 1) & 1, b, a))) break;
         if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
         tc_fence_after_nc();
         const uint64_t kd = kdesc0 + (uint64_t)((kr.stage * kQKMax) >> 4);
@@ -342,16 +322,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_nc(&b.s_full[J & 1]);
         kr.next(kKStages);
         if (j == nj - 1) mma_commit_nc(&b.q_empty[qb]);
-        if (j >= 1 && !(ok = issue_pg(J - 1, j == 1))) break;
+      }
+    }
+    mma_commit(&b.drain[0]);
+    mbar_wait(&b.drain[0], 0, a.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue: P.G
+    const uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);
+    const uint64_t gdesc0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
+    bool ok = true;
+    if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
+    Ring gr;
+    uint32_t ophase = 0;
+    uint32_t J = 0;  // source blocks of this CTA
+    TileSeq seq;
+    for (bool have = ok && seq.first(a); ok && have; have = seq.next(a)) {
+      const int nj = seq.t.ib + 1;
+      for (int j = 0; j < nj; ++j, ++J) {
+        // O += P_J G_J (two half blocks); the tile's first block overwrites O once the
+        // epilogue has read the previous tile's accumulator out of TMEM.
+        const uint32_t buf = J & 1;
+        if (!(ok = wait_bar(&b.p_full[buf], (J >> 1) & 1, b, a))) break;
+        if (j == 0) {
+          if (!(ok = wait_bar(&b.o_empty, ophase ^ 1, b, a))) break;
+          ophase ^= 1;
+        }
+        const uint32_t ptm = tmem + kColS0 + buf * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
+          tc_fence_after_nc();
+          const uint64_t gd = gdesc0 + (uint64_t)((gr.stage * kGStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            mma_bf16_ts_nc(tmem + kColO, ptm + h * 32 + kk * 8, gd + (uint64_t)(kk * (2048 >> 4)), idesc_o,
+                           (j == 0 && h == 0 && kk == 0) ? 0u : 1u);
+          mma_commit_nc(&b.g_empty[gr.stage]);
+          gr.next(kGStages);
+        }
+        if (!ok) break;
+        mma_commit_nc(&b.slot_free[buf]);
       }
       if (!ok) break;
-      if (!(ok = issue_pg(J - 1, nj == 1))) break;
       mma_commit_nc(&b.o_full);
       gr.next(kGStages);  // the tile's two v stages belong to the epilogue
       gr.next(kGStages);
     }
-    mma_commit(&b.drain);
-    mbar_wait(&b.drain, 0, a.timeout_ns);
+    mma_commit(&b.drain[1]);
+    mbar_wait(&b.drain[1], 0, a.timeout_ns);
   } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ softmax
     const int wg = (warp - kSoftWarp0) / 4;  // columns [64 wg, 64 wg + 64) of every block
