@@ -70,7 +70,7 @@ size_t agg_qk_bytes(const tg_agg_params* p) {
 }
 // Feature-map scratch of the tensor-core WANGO path.
 size_t agg_aux_bytes(const tg_agg_params* p, bool wango) {
-  return (wango && p->dtype == TG_BF16) ? wango_aux_bytes(p->B, p->T, p->H, p->d_qk) : 0;
+  return (wango && p->dtype == TG_BF16) ? wango_aux_bytes(p->B, p->T, p->H, p->d_qk, p->m, p->window) : 0;
 }
 size_t agg_ws_bytes(const tg_agg_params* p, bool wango) { return agg_qk_bytes(p) + agg_aux_bytes(p, wango); }
 

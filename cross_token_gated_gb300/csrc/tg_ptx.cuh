@@ -278,6 +278,22 @@ __device__ __forceinline__ uint64_t bf16x2_widen(uint32_t pk) {
   return f32x2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
 }
 
+// Flags between CTAs of one launch (all resident): release store / acquire load at GPU
+// scope, and four f32 read at L2 (never from a possibly stale L1 line).
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_global_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
 // One column, waited for inside the same statement (the value is usable on return).
 __device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr) {
   uint32_t r;

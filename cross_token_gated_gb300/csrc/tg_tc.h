@@ -23,8 +23,9 @@ cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_
 cudaError_t launch_tango_tc(const AggArgs& a, cudaStream_t s);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
 // Scratch bytes the tensor-core WANGO path needs in AggArgs::aux (256-byte aligned):
-// e^-tau phi(q~) and phi(k~) in bf16, per-block sums of phi(k~), and the older-prefix
-// denominator of every destination.
-size_t wango_aux_bytes(int B, int T, int H, int dqk);
+// e^-tau phi(q~) and phi(k~) in bf16, per-block sums of phi(k~), the older-prefix
+// denominator of every destination, and, when strips are split into segments, the
+// states handed from one segment to the next with their flags.
+size_t wango_aux_bytes(int B, int T, int H, int dqk, int m, int W);
 
 }  // namespace tg

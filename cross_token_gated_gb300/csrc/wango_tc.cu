@@ -96,6 +96,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct Args {
   int B, T, H, dqk, m, d_h, m_h, W;
   int n_iblk, n_ntile, n_strips;
+  int nseg, seg_len, n_items;  // each strip's destination blocks in nseg segments
+  float* seg_state;            // [n_strips, nseg - 1, kNg, d_h] f32 state at segment ends
+  int* seg_flag;               // [n_strips, nseg - 1], 0 until that state is written
   float s;
   const float* tau;
   const float* null_bias;
@@ -123,6 +126,29 @@ __device__ __forceinline__ uint32_t p_col(int kk, int h) {
 struct Strip {
   int b, head, n0;
 };
+// A work item: destination blocks [ib0, ib1) of one strip, segment `seg` of nseg.
+// Items are numbered segment-major, so every strip's segment k comes before any
+// segment k + 1.  A segment that ends with a non-empty state hands it (f32) to the
+// next segment through global memory and a per-strip flag.
+struct Item {
+  int st, seg, ib0, ib1;
+};
+template <bool kSeg>
+__device__ __forceinline__ Item item_of(const Args& a, int w) {
+  Item it;
+  if (kSeg) {
+    it.seg = w / a.n_strips;
+    it.st = w % a.n_strips;
+    it.ib0 = it.seg * a.seg_len;
+    it.ib1 = min(a.n_iblk, it.ib0 + a.seg_len);
+  } else {  // one segment per strip
+    it.seg = 0;
+    it.st = w;
+    it.ib0 = 0;
+    it.ib1 = a.n_iblk;
+  }
+  return it;
+}
 __device__ __forceinline__ Strip strip_of(const Args& a, int s) {
   Strip r;
   r.n0 = (s % a.n_ntile) * kNg;
@@ -141,6 +167,18 @@ __device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
   if (mbar_try_wait_nc(smem_u32(bar), parity)) return true;
   return wait_slow(bar, parity, b, a);
+}
+
+// Waits, bounded, until another CTA of this launch sets *flag (acquire).
+__device__ __forceinline__ bool wait_flag(const int* flag, const Args& a) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(flag) == 0) {
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      record_error(a.err, kErrTimeout | kKernWango);
+      return false;
+    }
+  }
+  return true;
 }
 
 struct Ring {
@@ -187,7 +225,65 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
   }
 }
 
+// Segment handoff, run once per work item (kept out of line: the hot loops stay small).
+// The previous segment's state, one thread's gate column of d_h f32 at src, into TMEM
+// at t_st (for the updates) and as bf16 into shared memory at s_sb (for the read-out).
+// Called by all four epilogue warps; returns false (for all of them) if the wait for
+// the previous segment timed out.
 template <int DH>
+__device__ __noinline__ bool import_state(const Args& a, size_t slot, uint32_t t_st, uint32_t s_sb, int row,
+                                          uint64_t* sb_full, int lane, bool issuer) {
+  constexpr int RB = DH * 2;
+  bool ok = true;
+  if (issuer) ok = wait_flag(&a.seg_flag[slot], a);
+  if (!named_bar_and(2, 128, ok)) return false;
+  const float* src = a.seg_state + (slot * kNg + row) * DH;
+#pragma unroll 1
+  for (int c0 = 0; c0 < DH; c0 += 16) {
+    uint32_t t16[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 x = ld_global_cg_v4(src + c0 + 4 * q);
+      t16[4 * q] = x.x; t16[4 * q + 1] = x.y; t16[4 * q + 2] = x.z; t16[4 * q + 3] = x.w;
+    }
+    tmem_st16(t_st + c0, t16);
+#pragma unroll
+    for (int c = 0; c < 16; c += 8) {
+      const uint4 o = make_uint4(pack_bf16x2(__uint_as_float(t16[c]), __uint_as_float(t16[c + 1])),
+                                 pack_bf16x2(__uint_as_float(t16[c + 2]), __uint_as_float(t16[c + 3])),
+                                 pack_bf16x2(__uint_as_float(t16[c + 4]), __uint_as_float(t16[c + 5])),
+                                 pack_bf16x2(__uint_as_float(t16[c + 6]), __uint_as_float(t16[c + 7])));
+      st_shared_v4(s_sb + swz<RB>(row, c0 + c), o);
+    }
+  }
+  tmem_st_wait();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sb_full);
+  return true;
+}
+// This segment's final state (one thread's gate column, TMEM at t_st) to global
+// memory, then the flag for the next segment.  Called by all four epilogue warps.
+template <int DH>
+__device__ __noinline__ void export_state(const Args& a, size_t slot, uint32_t t_st, int row, bool issuer) {
+  float* dst = a.seg_state + (slot * kNg + row) * DH;
+  tc_fence_after();
+#pragma unroll 1
+  for (int c0 = 0; c0 < DH; c0 += 16) {
+    uint32_t t16[16];
+    tmem_ld16(t_st + c0, t16);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_global_v4(dst + c0 + 4 * q, t16[4 * q], t16[4 * q + 1], t16[4 * q + 2], t16[4 * q + 3]);
+  }
+  __threadfence();
+  named_bar_sync(2, 128);  // every epilogue thread has written and fenced its part
+  if (issuer) st_release_gpu(&a.seg_flag[slot], 1);
+}
+
+template <int DH, bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     wango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
@@ -263,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring kr, gr;
     bool ok = true;
     uint32_t kmask = 0, gmask = 0, kph[kKStages] = {}, gph[kGStages] = {}, vmask = 0, vph[2] = {};
-    uint32_t fkph = 0, qh_n = 0, fq_n = 0;  // Fk phase; qhat and Fq loads issued
-    bool fk_issued = false;
+    uint32_t fkph = 0;                               // phase of the Fk buffer
+    uint32_t qh_n = 0, fq_n = 0, fk_n = 0;             // loads issued
     int dc = 0;  // destination blocks begun
     auto tile128 = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int bb) {
 #pragma unroll
@@ -272,10 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) tma_load_3d(dst + h * 2 * kGBox + c * kGBox, map, bar, x + 64 * c, y + 64 * h, bb);
     };
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      const Strip sp = strip_of(a, st);
+    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      const Item it = item_of<kSeg>(a, w);
+      const Strip sp = strip_of(a, it.st);
       const int gx = sp.head * a.m_h + sp.n0;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
         const uint32_t dp = dc & 1;
         if (!(ok = wait_bar(&b.qh_empty, dp ^ 1, b, a))) break;
         mbar_arrive_expect_tx(&b.qh_full, tile_bytes);
@@ -302,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
             mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
             tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
-            fk_issued = true;
+            ++fk_n;
             fkph ^= 1;
           }
           if (!(ok = wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a))) break;
@@ -330,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no copy may be in flight when the CTA exits
     if (qh_n) mbar_wait(&b.qh_full, (qh_n - 1) & 1, a.timeout_ns);
     if (fq_n) mbar_wait(&b.fq_full, (fq_n - 1) & 1, a.timeout_ns);
-    if (fk_issued) mbar_wait(&b.fk_full, fkph ^ 1, a.timeout_ns);
+    if (fk_n) mbar_wait(&b.fk_full, (fk_n - 1) & 1, a.timeout_ns);
     for (int s = 0; s < kKStages; ++s)
       if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
     for (int s = 0; s < kGStages; ++s)
@@ -351,8 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring ks;
     uint32_t u = 0, fkph = 0;
     int dc = 0;
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
+    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      const Item it = item_of<kSeg>(a, w);
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
         const int jlo = jlo_of(ib, W);
         for (int jb = ib; ok && jb >= jlo; --jb) {
           const bool mixed = is_mixed(jb, ib, W);
@@ -410,9 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring gr;
     uint32_t u = 0, oph = 0, sbph = 0;
     int dc = 0;
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      bool first_update = true;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++dc) {
+    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      const Item it = item_of<kSeg>(a, w);
+      // a later segment starts from the state its predecessor handed over
+      bool first_update = !(kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0);
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
         const int jlo = jlo_of(ib, W);
         bool copy_ready = false;
         for (int jb = ib; ok && jb >= jlo; --jb) {
@@ -502,11 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
     uint32_t unit = 0;  // units processed
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      const Strip sp = strip_of(a, st);
+    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      const Item it = item_of<kSeg>(a, w);
+      const Strip sp = strip_of(a, it.st);
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
       const float c = tau * kLog2e;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib) {
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib) {
         const int i = ib * kBlk + row;
         for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
           const bool mixed = is_mixed(jb, ib, W);
@@ -583,12 +684,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.sb_full);
     };
-    for (int st = blockIdx.x; ok && st < a.n_strips; st += gridDim.x) {
-      const Strip sp = strip_of(a, st);
+    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      const Item it = item_of<kSeg>(a, w);
+      if (it.ib0 >= it.ib1) continue;
+      const Strip sp = strip_of(a, it.st);
+
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
-      copy_state(true);  // read-out of block 0: empty state
+      // the state before the first destination block: empty, or the previous
+      // segment's (into TMEM for the updates, bf16 into shared memory for the read-out)
+      if (kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0) {
+        if (!import_state<DH>(a, (size_t)it.st * (a.nseg - 1) + (it.seg - 1), tmem + kColSt + lane_off,
+                              smem_u32(sSB), row, &b.sb_full, lane, issuer))
+          break;
+      } else {
+        copy_state(true);
+      }
       const float null_w = a.null_bias ? exp2f((a.null_bias[sp.head] - tau) * kLog2e) : 0.f;
-      for (int ib = 0; ok && ib < a.n_iblk; ++ib, ++gib) {
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++gib) {
         const int i = ib * kBlk + row;
         const bool row_ok = i < a.T;
         const int sv = gib & 1;  // v tile buffer
@@ -654,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the state copy for the next destination block (this block's updates and
         // read-out are complete; the next block updates the state only after it)
-        if (ib + 1 < a.n_iblk) copy_state(jlo_of(ib + 1, W) == 0);
+        if (ib + 1 < it.ib1) copy_state(jlo_of(ib + 1, W) == 0);
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (issuer) {
@@ -672,6 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&b.v_empty[sv]);
         }
       }
+      // hand this segment's final state to the next segment of the strip (the last
+      // block's updates are complete: its st_full was waited for above)
+      if (kSeg && ok && it.seg + 1 < a.nseg && jlo_of(it.ib1, W) > 0)
+        export_state<DH>(a, (size_t)it.st * (a.nseg - 1) + it.seg, tmem + kColSt + lane_off, row, issuer);
     }
   }
   tc_fence_before();
@@ -761,23 +877,52 @@ int num_sms() {
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Segments per strip: the count that minimises the estimated makespan on `sms`
+// persistent CTAs, a destination block costing 1.  Segment k + 1 of a strip waits for
+// segment k to finish; items run segment-major, so with more than one round the
+// wait is normally over before it starts.
+int choose_nseg(long long strips, int n_iblk, int W, int sms) {
+  (void)W;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int nseg = 1; nseg <= 4 && nseg <= n_iblk; ++nseg) {
+    const int len = (n_iblk + nseg - 1) / nseg;
+    const long long items = strips * nseg;
+    const long long rounds = (items + sms - 1) / sms;
+    // a segment cannot start before its predecessor ends: at least nseg rounds
+    const double cost = (double)(rounds > nseg ? rounds : nseg) * len;
+    if (nseg == 1 || cost < 0.95 * best_cost) {  // more segments only for a clear gain
+      best = nseg;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 struct AuxLayout {
-  size_t fq, fk, zb, den, total;
+  size_t fq, fk, zb, den, seg, flag, total;
+  int nseg;
 };
-AuxLayout aux_layout(int B, int T, int H, int dqk) {
+AuxLayout aux_layout(int B, int T, int H, int dqk, int m, int W) {
   const size_t BT = (size_t)B * T, nI = (size_t)(T + kBlk - 1) / kBlk;
+  const int d_h = dqk / H;
+  const long long strips = (long long)B * H * ((m / H + kNg - 1) / kNg);
   AuxLayout L;
+  L.nseg = choose_nseg(strips, (int)nI, W, num_sms());
+  const size_t handoffs = (size_t)strips * (L.nseg - 1);
   L.fq = 0;
   L.fk = L.fq + a256(BT * dqk * 2);
   L.zb = L.fk + a256(BT * dqk * 2);
-  L.den = L.zb + a256((size_t)B * H * nI * (dqk / H) * 4);
-  L.total = L.den + a256((size_t)B * H * T * 4);
+  L.den = L.zb + a256((size_t)B * H * nI * d_h * 4);
+  L.seg = L.den + a256((size_t)B * H * T * 4);
+  L.flag = L.seg + a256(handoffs * kNg * d_h * 4);
+  L.total = L.flag + a256(handoffs * 4);
   return L;
 }
 
 }  // namespace
 
-size_t wango_aux_bytes(int B, int T, int H, int dqk) { return aux_layout(B, T, H, dqk).total; }
+size_t wango_aux_bytes(int B, int T, int H, int dqk, int m, int W) { return aux_layout(B, T, H, dqk, m, W).total; }
 
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   Args a = {};
@@ -789,6 +934,11 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   const long long strips = (long long)p.B * p.H * a.n_ntile;
   if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.n_strips = (int)strips;
+  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk, p.m, p.window);
+  a.nseg = L.nseg;
+  a.seg_len = ceil_div(a.n_iblk, a.nseg);
+  if (strips * a.nseg > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_items = a.n_strips * a.nseg;
   a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
   a.has_v = p.v != nullptr;
   a.out = static_cast<__nv_bfloat16*>(p.out);
@@ -797,8 +947,13 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
 
   // pre-pass: feature maps, block sums, older-prefix denominators
-  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk);
   char* aux = static_cast<char*>(p.aux);
+  a.seg_state = reinterpret_cast<float*>(aux + L.seg);
+  a.seg_flag = reinterpret_cast<int*>(aux + L.flag);
+  if (a.nseg > 1) {  // no segment's state is ready yet
+    const cudaError_t me = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
+    if (me != cudaSuccess) return me;
+  }
   __nv_bfloat16* fq = reinterpret_cast<__nv_bfloat16*>(aux + L.fq);
   __nv_bfloat16* fk = reinterpret_cast<__nv_bfloat16*>(aux + L.fk);
   float* zb = reinterpret_cast<float*>(aux + L.zb);
@@ -824,10 +979,13 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
   if (e != cudaSuccess) return e;
-  auto kern = a.d_h == 64 ? wango_tc_kernel<64> : a.d_h == 32 ? wango_tc_kernel<32> : wango_tc_kernel<16>;
+  auto kern = a.nseg > 1 ? (a.d_h == 64 ? wango_tc_kernel<64, true> : a.d_h == 32 ? wango_tc_kernel<32, true>
+                                                                                  : wango_tc_kernel<16, true>)
+                         : (a.d_h == 64 ? wango_tc_kernel<64, false> : a.d_h == 32 ? wango_tc_kernel<32, false>
+                                                                                   : wango_tc_kernel<16, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = a.n_strips < num_sms() ? a.n_strips : num_sms();
+  const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
   kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mfq, mfk, mg, mv, mu, a);
   return cudaGetLastError();
 }

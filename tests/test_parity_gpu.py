@@ -119,6 +119,22 @@ def test_agg_parity_70m_shape_sampled(kind):
     assert rel_err(got, ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_agg_parity_long_context_sampled(kind):
+    """bf16 at the long-context shape (B=1, T=8192, m=28480, q/k width 128, W=256).
+    Few strips for many destination blocks: the WANGO kernel splits each strip into
+    segments, and a later segment starts by rebuilding the state.  Oracle rows are
+    sampled around the segment and window boundaries."""
+    B, T, H, dqk, m, W = 1, 8192, 2, 128, 28480, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=3, dtype="bf16")
+    out = run_agg(kind, q, k, g, v, H, W)
+    extra = [0, 255, 256, 4095, 4096, 4097, 4223, 4224, 4351, 4352, 8191]
+    rows = synth.random_rows(B, T, 24, seed=2, extra=extra)
+    ref = ref_agg(kind, q, k, g, v, H, W, rows=rows)
+    got = out.reshape(B * T, m)[torch.from_numpy(rows).cuda()]
+    assert rel_err(got, ref) <= TOL["bf16"]
+
+
 # ------------------------------------------------------------------ block forward
 
 def run_block(h, w, H, mode, W, **kw):
