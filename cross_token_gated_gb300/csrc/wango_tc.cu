@@ -836,21 +836,40 @@ __global__ void wango_phi_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
   *reinterpret_cast<uint4*>(fk + r * dqk + c0) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
 }
 
-// zb[b][a][jb][c] = sum over the valid sources of block jb of Fk[.][a d_h + c] (the
-// bf16 values the state update multiplies).  grid (n_iblk, H, B), block d_h threads.
-__global__ void wango_blocksum_kernel(const __nv_bfloat16* fk, float* zb, int T, int H, int dqk, int n_iblk) {
-  const int jb = blockIdx.x, a = blockIdx.y, bb = blockIdx.z, c = threadIdx.x;
-  const int d_h = dqk / H;
+// zb[b, a, jb, c] = sum over the valid sources of block jb of Fk[., a*d_h + c] (the bf16
+// values the state update multiplies).  grid
+// (n_iblk, H, B), 256 threads: thread (g, p) sums column pair p over rows g, g + 8, ...
+// (bf16x2 loads, one head row per warp), then the eight row groups are added.
+__global__ void __launch_bounds__(256) wango_blocksum_kernel(const __nv_bfloat16* fk, float* zb, int T, int H,
+                                                             int dqk, int n_iblk) {
+  __shared__ float part[8][64];
+  const int jb = blockIdx.x, a = blockIdx.y, bb = blockIdx.z;
+  const int d_h = dqk / H, npair = d_h / 2;
+  const int p = threadIdx.x % 32, g = threadIdx.x / 32;
   const int j0 = jb * kBlk, j1 = min(T, j0 + kBlk);
-  float s = 0.f;
-  for (int j = j0; j < j1; ++j) s += __bfloat162float(fk[((size_t)bb * T + j) * dqk + a * d_h + c]);
-  zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + c] = s;
+  float s0 = 0.f, s1 = 0.f;
+  if (p < npair) {
+    for (int j = j0 + g; j < j1; j += 8) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(fk + ((size_t)bb * T + j) * dqk + a * d_h + 2 * p);
+      s0 += bf16lo(w);
+      s1 += bf16hi(w);
+    }
+    part[g][2 * p] = s0;
+    part[g][2 * p + 1] = s1;
+  }
+  __syncthreads();
+  if (threadIdx.x < d_h) {
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t += part[q][threadIdx.x];
+    zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + threadIdx.x] = t;
+  }
 }
-
-// den_old[b][a][i] = Fq_i . z(ib), z(ib) = sum of zb over the blocks jb < jlo(ib) of
-// destination block ib.  grid (n_iblk, H, B), block 128 threads.
-__global__ void wango_denold_kernel(const __nv_bfloat16* fq, const float* zb, float* den_old, int T, int H, int dqk,
-                                    int n_iblk, int W) {
+// den_old[b, a, i] = Fq_i . z with z the sum of zb over the blocks older than the window of
+// i's destination block ib (jb < jlo(ib)).  grid (n_iblk, H, B), 128 threads, one row
+// each; Fq is read 16 bytes at a time.
+__global__ void __launch_bounds__(128) wango_denold_kernel(const __nv_bfloat16* fq, const float* zb, float* den_old,
+                                                           int T, int H, int dqk, int n_iblk, int W) {
   __shared__ float z[64];
   const int ib = blockIdx.x, a = blockIdx.y, bb = blockIdx.z, t = threadIdx.x;
   const int d_h = dqk / H, jlo = jlo_of(ib, W);
@@ -864,7 +883,15 @@ __global__ void wango_denold_kernel(const __nv_bfloat16* fq, const float* zb, fl
   if (i >= T) return;
   const __nv_bfloat16* f = fq + ((size_t)bb * T + i) * dqk + a * d_h;
   float dot = 0.f;
-  for (int c = 0; c < d_h; ++c) dot = fmaf(__bfloat162float(f[c]), z[c], dot);
+  for (int c = 0; c < d_h; c += 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(f + c);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      dot = fmaf(bf16lo(ww[e]), z[c + 2 * e], dot);
+      dot = fmaf(bf16hi(ww[e]), z[c + 2 * e + 1], dot);
+    }
+  }
   den_old[((size_t)bb * H + a) * T + i] = dot;
 }
 
@@ -964,7 +991,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
       static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, rows, p.H, p.dqk,
       p.s, p.tau, p.phi_mode, p.err);
   dim3 g3(a.n_iblk, p.H, p.B);
-  wango_blocksum_kernel<<<g3, a.d_h, 0, s>>>(fk, zb, p.T, p.H, p.dqk, a.n_iblk);
+  wango_blocksum_kernel<<<g3, 256, 0, s>>>(fk, zb, p.T, p.H, p.dqk, a.n_iblk);
   wango_denold_kernel<<<g3, kBlk, 0, s>>>(fq, zb, den, p.T, p.H, p.dqk, a.n_iblk, p.window);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
