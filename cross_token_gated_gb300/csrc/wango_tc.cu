@@ -35,18 +35,19 @@
 //                warp 1: a unit's scores into an f32 TMEM slot (ring of 2): Sc = Qhat
 //                Khat^T (128 columns), or for a half Sc (64 columns) beside Sf = Fq Fk^T
 //                (64 columns); it runs ahead as far as the slots allow.
-//                warp 2: O (+)= P G from the unit's slot, and the row sums of P (P times
-//                a tile of ones, N = 16: the denominator of the weights as applied);
-//                for a leaving block S^T += G^T Fk (M=128, N=d_h) in TMEM; last, the
-//                read-out O += Fq S_bf16 (the state before the block).
+//                warp 2: O (+)= P G from the unit's slot; for a leaving block
+//                S^T += G^T Fk (M=128, N=d_h) in TMEM; last, the read-out O += Fq S_bf16
+//                (the state before the block).
 //   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of a block (or
 //                [32w, 32w+32) of a half): exp (window), the feature-map score (older) or
-//                0 (after i), rounded to bf16 and written as P over its own cos columns.
+//                0 (after i), rounded to bf16 and written as P over its own cos columns;
+//                the row sums of the bf16 weights (the denominator as applied) go to
+//                the epilogue through shared memory.
 //   warps 12-15  epilogue: gbar = O / den read out of TMEM into registers (rounded to
 //                bf16; O is released right after), u = gbar * v over v in shared memory,
 //                the copy S^T (TMEM, f32) -> S (shared memory, bf16) for the next
 //                destination block's read-out, then u stored by TMA.
-// TMEM: O [0,128), S^T [128, 128+d_h), row sums [192,208), score slots [256,384) and
+// TMEM: O [0,128), S^T [128, 128+d_h), score slots [256,384) and
 // [384,512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -69,8 +70,7 @@ constexpr uint32_t kGBox = 64 * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;     // 32 KB: 128 rows x 128 columns
 // TMEM columns: O, the state S^T, the row sums of P, two score slots (P, in bf16 pairs,
 // is written over each warpgroup's own cos columns)
-constexpr uint32_t kColO = 0, kColSt = 128, kColDen = 192, kColSlot0 = 256;
-constexpr uint32_t kOnesBytes = 16 * 32;   // bf16 ones, 16 rows x 16 (K-major, 32-byte swizzle)
+constexpr uint32_t kColO = 0, kColSt = 128, kColSlot0 = 256;
 
 struct __align__(8) Bars {
   uint64_t qh_full, qh_empty;                   // qhat of a destination block
@@ -84,13 +84,15 @@ struct __align__(8) Bars {
   uint64_t o_full, o_empty;
   uint64_t st_full;                             // a destination block's MMAs are done
   uint64_t sb_full;                             // bf16 state copy in place
+  uint64_t den_full, den_empty;                 // the weights' row sums -> epilogue
   uint64_t drain[2], never;
   uint32_t tmem_base;
   int abort;
+  float rowsum[2][kBlk];                        // per warpgroup, per destination row
 };
 
 // smem: Qhat | Fq | K x kKStages | Fk | S_bf16 | G x kGStages | V x 2 | ones | Bars
-constexpr size_t kSmemBytes = 1024 + kTile * (4 + kKStages) + kGStage * (kGStages + 2) + kOnesBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kTile * (4 + kKStages) + kGStage * (kGStages + 2) + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
@@ -205,7 +207,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 //            feature-map score f (older source).
 template <int kMode>
 __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
-                                          uint32_t (&p)[16]) {
+                                          uint32_t (&p)[16], uint64_t (&dsum2)[2]) {
   const uint64_t cc = f32x2_pack(c, c), nc = f32x2_pack(-c, -c);
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
@@ -221,7 +223,10 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
       if (j0 + e > i) w0 = 0.f;
       if (j0 + e + 1 > i) w1 = 0.f;
     }
-    p[e / 2] = pack_bf16x2(w0, w1);
+    const uint32_t pk = pack_bf16x2(w0, w1);
+    // the row sum of the weights as applied (bf16), two f32 lanes per instruction
+    dsum2[(e >> 1) & 1] = add_f32x2(dsum2[(e >> 1) & 1], bf16x2_widen(pk));
+    p[e / 2] = pk;
   }
 }
 
@@ -302,8 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSB = sFK + kTile;          // bf16 state, [128 gate rows x d_h]
   uint8_t* sG = sSB + kTile;           // G ring
   uint8_t* sV = sG + kGStages * kGStage;  // two v / u tiles
-  uint8_t* sOnes = sV + 2 * kGStage;      // B operand of the row-sum MMA
-  Bars& b = *reinterpret_cast<Bars*>(sOnes + kOnesBytes);
+  Bars& b = *reinterpret_cast<Bars*>(sV + 2 * kGStage);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -335,11 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&b.drain[s], 1);
     }
+    mbar_init(&b.den_full, 8);
+    mbar_init(&b.den_empty, 4);
     mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < kOnesBytes / 4) reinterpret_cast<uint32_t*>(sOnes)[threadIdx.x] = 0x3f803f80u;
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(&b.tmem_base, 512);
@@ -497,8 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);   // O += P G
     constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);  // O += Fq S
     constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);     // S^T += G^T Fk
-    constexpr uint32_t idesc_d = idesc_bf16_f32(kBlk, 16, false, false);   // den += P 1
-    const uint64_t onesd = smem_desc(smem_u32(sOnes), 16, 256, kSwizzle32B);
     const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
     const uint64_t fkmn = smem_desc(smem_u32(sFK), tile_bytes, sbo, lay);  // Fk as MN-major B
     const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
@@ -530,25 +533,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_nc();
             const uint32_t ptm = tmem + kColSlot0 + (u & 1) * 128;
             const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
-            // 16-source steps of the block: all 8, or the 4 of half h.  Each step also
-            // adds P's row sums (P times a tile of ones) into the denominator columns:
-            // the denominator of the weights as applied.
+            // 16-source steps of the block: all 8, or the 4 of half h
             if (h < 0) {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
-                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gd + (uint64_t)(goff >> 4), idesc_o, acc);
-                mma_bf16_ts_nc(tmem + kColDen, ptm + p_col(kk, h), onesd, idesc_d, acc);
+                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gd + (uint64_t)(goff >> 4), idesc_o,
+                               (first && kk == 0) ? 0u : 1u);
               }
             } else {
               const uint64_t gh = gd + (uint64_t)((h * 2 * kGBox) >> 4);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gh + (uint64_t)((kk * 2048) >> 4), idesc_o, acc);
-                mma_bf16_ts_nc(tmem + kColDen, ptm + p_col(kk, h), onesd, idesc_d, acc);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gh + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                               (first && kk == 0) ? 0u : 1u);
             }
             if (leaving) {
               // S^T += G^T Fk over this unit's sources, once the read-out copy of the
@@ -602,13 +600,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
     uint32_t unit = 0;  // units processed
+    int gib = 0;        // destination blocks processed
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
       const Strip sp = strip_of(a, it.st);
       const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
       const float c = tau * kLog2e;
-      for (int ib = it.ib0; ok && ib < it.ib1; ++ib) {
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++gib) {
         const int i = ib * kBlk + row;
+        uint64_t dsum2[2] = {0, 0};  // this row's sum of the weights over this warpgroup's sources
         for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
           const bool mixed = is_mixed(jb, ib, W);
           for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t rq[32], p[16];
                 tmem_ld32(sl + wg * 64 + q * 32, rq);
                 tmem_ld_wait();
-                weights32<1>(rq, rq, c, j0 + q * 32, ilim, 0, p);
+                weights32<1>(rq, rq, c, j0 + q * 32, ilim, 0, p, dsum2);
                 tmem_st16(sl + wg * 64 + q * 16, p);
               }
             } else {      // cos and feature-map scores of sources [32 wg, 32 wg + 32) of the half
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld32(sl + 64 + wg * 32, r[1]);
               tmem_ld_wait();
               uint32_t p[16];
-              weights32<2>(r[0], r[1], c, jb * kBlk + h * 64 + wg * 32, i, i - W + 1, p);
+              weights32<2>(r[0], r[1], c, jb * kBlk + h * 64 + wg * 32, i, i - W + 1, p, dsum2);
               tmem_st16(sl + wg * 32, p);
             }
             tmem_st_wait();
@@ -645,6 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&b.p_full[n & 1]);
           }
         }
+        if (!ok) break;
+        // the row sums of this destination block -> epilogue
+        if (!(ok = wait_bar(&b.den_empty, (gib & 1) ^ 1, b, a))) break;
+        float d0, d1, d2, d3;
+        f32x2_unpack(dsum2[0], d0, d1);
+        f32x2_unpack(dsum2[1], d2, d3);
+        b.rowsum[wg][row] = (d0 + d1) + (d2 + d3);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.den_full);
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -708,13 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // older-prefix denominator, fetched before the waits
         float den = row_ok ? a.den_old[((size_t)sp.b * a.H + sp.head) * a.T + i] : 0.f;
         den += (float)(i + 1) * null_w;
+        if (ok) ok = wait_bar(&b.den_full, gib & 1, b, a);
+        if (ok) {
+          den += b.rowsum[0][row] + b.rowsum[1][row];  // this block's per-pair weights, as applied
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b.den_empty);
+        }
         if (ok) ok = wait_bar(&b.o_full, oph, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
         oph ^= 1;
         tc_fence_after();
-        // + the row sum of this block's per-pair weights, as applied (bf16)
-        den += __uint_as_float(tmem_ld1_wait(tmem + kColDen + lane_off));
         const float inv = 1.f / den;
         // gbar = O / den, rounded to bf16, in registers; the accumulator is released as
         // soon as it has been read
