@@ -202,7 +202,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 
 // Weights of 32 sources of one row, written as 16 packed bf16 pairs.
 //   kMode 0: every source is in the window: exp2(c (s - 1)).
-//   kMode 1: window, but sources after the destination (j0 + e > i) get 0.
 //   kMode 2: general: 0 after i, exp2(c (s - 1)) in the window (j >= jw), else the
 //            feature-map score f (older source).
 template <int kMode>
@@ -218,8 +217,6 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
     if (kMode == 2) {
       if (j0 + e < jw) w0 = __uint_as_float(f[e]);
       if (j0 + e + 1 < jw) w1 = __uint_as_float(f[e + 1]);
-    }
-    if (kMode >= 1) {
       if (j0 + e > i) w0 = 0.f;
       if (j0 + e + 1 > i) w1 = 0.f;
     }
@@ -617,27 +614,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bar(&b.s_full[n & 1], (n >> 1) & 1, b, a))) break;
             tc_fence_after();
             // P (bf16 pairs) over this warpgroup's own cos columns, so the two
-            // warpgroups need not wait for each other.  One 32-source group at a time
-            // (a rolled loop keeps the code small).
-            if (h < 0) {  // cos scores of sources [64 wg, 64 wg + 64); causal limit on the diagonal
-              const int j0 = jb * kBlk + wg * 64;
-              const int ilim = jb == ib ? i : 0x7fffffff;
+            // warpgroups need not wait for each other.  One 32-source chunk at a time (a
+            // rolled loop with one copy of each weight form keeps the code small): two per
+            // warpgroup for a whole block, one for a half of a mixed block, whose
+            // feature-map scores sit 64 columns after the cos scores.  Each chunk is
+            // classified for this warp's 32 rows: after every row (zero weights), inside
+            // every row's window (exp only) or general.
+            const int nq = h < 0 ? 2 : 1;
+            const int i0 = ib * kBlk + quarter * 32;
 #pragma unroll 1
-              for (int q = 0; q < 2; ++q) {
-                uint32_t rq[32], p[16];
-                tmem_ld32(sl + wg * 64 + q * 32, rq);
-                tmem_ld_wait();
-                weights32<1>(rq, rq, c, j0 + q * 32, ilim, 0, p, dsum2);
-                tmem_st16(sl + wg * 64 + q * 16, p);
-              }
-            } else {      // cos and feature-map scores of sources [32 wg, 32 wg + 32) of the half
-              uint32_t r[2][32];
-              tmem_ld32(sl + wg * 32, r[0]);
-              tmem_ld32(sl + 64 + wg * 32, r[1]);
-              tmem_ld_wait();
+            for (int q = 0; q < nq; ++q) {
+              const int off = h < 0 ? wg * 64 + q * 32 : h * 64 + wg * 32;  // first source in the block
+              const uint32_t cs = sl + (uint32_t)(h < 0 ? off : wg * 32);     // its cos score column
+              const uint32_t pc = sl + (uint32_t)(h < 0 ? wg * 64 + q * 16 : wg * 32);
+              const int js = jb * kBlk + off;
               uint32_t p[16];
-              weights32<2>(r[0], r[1], c, jb * kBlk + h * 64 + wg * 32, i, i - W + 1, p, dsum2);
-              tmem_st16(sl + wg * 32, p);
+              if (js > i0 + 31) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) p[e] = 0u;
+              } else if (js + 31 <= i0 && js >= i0 + 32 - W) {
+                uint32_t rq[32];
+                tmem_ld32(cs, rq);
+                tmem_ld_wait();
+                weights32<0>(rq, rq, c, js, i, 0, p, dsum2);
+              } else {  // a whole block has no older sources: its cos scores stand in for f
+                uint32_t r[2][32];
+                tmem_ld32(cs, r[0]);
+                tmem_ld32(h < 0 ? cs : cs + 64, r[1]);
+                tmem_ld_wait();
+                weights32<2>(r[0], r[1], c, js, i, h < 0 ? -0x7fffffff - 1 : i - W + 1, p, dsum2);
+              }
+              tmem_st16(pc, p);
             }
             tmem_st_wait();
             tc_fence_before();
