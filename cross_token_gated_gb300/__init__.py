@@ -7,7 +7,8 @@ the library cannot be loaded, every call raises.
 
 Functions (same names as the C ABI):
   tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_block_forward,
-  tg_workspace_size, tg_status_string, tg_check_device_error, tg_version
+  tango_model_forward, tg_workspace_size, tg_status_string, tg_check_device_error,
+  tg_version
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ TG_F32, TG_BF16 = 0, 1
 TG_FLAG_QK_NORMALIZED = 0x1
 TG_FLAG_DEBUG_TIMEOUT = 0x100
 TG_MODE_TANGO, TG_MODE_WANGO = 0, 1
-TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK = 0, 1, 2
+TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL = 0, 1, 2, 3
 
 HEADER = os.path.join(_build.INCLUDE, "tango.h")
 
@@ -51,6 +52,17 @@ class tg_block_weights(ctypes.Structure):
 class tg_block_params(ctypes.Structure):
     _fields_ = [("agg", tg_agg_params), ("d", ctypes.c_int), ("mode", ctypes.c_int),
                 ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
+
+
+class tg_model_weights(ctypes.Structure):
+    _fields_ = [("embedding", ctypes.c_void_p), ("final_gamma", ctypes.c_void_p),
+                ("sets", ctypes.POINTER(tg_block_weights))]
+
+
+class tg_model_params(ctypes.Structure):
+    _fields_ = [("block", tg_block_params), ("vocab", ctypes.c_int), ("n_apps", ctypes.c_int),
+                ("n_sets", ctypes.c_int), ("set_of_app", ctypes.POINTER(ctypes.c_int)),
+                ("final_rms_eps", ctypes.c_float)]
 
 
 _lib = None
@@ -86,6 +98,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.tango_aggregate_noalloc.restype = ctypes.c_int
         lib.tango_block_forward.argtypes = [P(tg_block_params), P(tg_block_weights), vp, vp, vp, sz, vp]
         lib.tango_block_forward.restype = ctypes.c_int
+        lib.tango_model_forward.argtypes = [P(tg_model_params), P(tg_model_weights), vp, vp, vp, sz, vp]
+        lib.tango_model_forward.restype = ctypes.c_int
         lib.tg_workspace_size.argtypes = [ctypes.c_int, vp]
         lib.tg_workspace_size.restype = sz
         lib.tg_status_string.argtypes = [ctypes.c_int]
@@ -248,3 +262,49 @@ def block_workspace(B, T, d, H, d_qk, m, *, dtype, mode=TG_MODE_TANGO, window=1,
     """Allocates a workspace tensor large enough for tango_block_forward."""
     p = block_params(B, T, d, H, d_qk, m, dtype=dtype, mode=mode, window=window)
     return _workspace(tg_workspace_size(TG_WS_BLOCK, p), device, None)
+
+
+def model_params(B, T, d, H, d_qk, m, vocab, *, dtype, n_apps=4, n_sets=1, set_of_app=None,
+                 mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None, window=1, phi_mode=0, rms_eps=1e-6,
+                 rope_base=10000.0, final_rms_eps=1e-6):
+    """tg_model_params; the returned structure keeps its set_of_app array alive."""
+    table = None
+    if set_of_app is not None:
+        table = (ctypes.c_int * len(set_of_app))(*[int(x) for x in set_of_app])
+    p = tg_model_params(block_params(B, T, d, H, d_qk, m, dtype=dtype, mode=mode, s=s, tau=tau,
+                                     null_bias=null_bias, window=window, phi_mode=phi_mode, rms_eps=rms_eps,
+                                     rope_base=rope_base),
+                        int(vocab), int(n_apps), int(n_sets),
+                        ctypes.cast(table, ctypes.POINTER(ctypes.c_int)) if table is not None else None,
+                        float(final_rms_eps))
+    p._table = table
+    return p
+
+
+def tango_model_forward(ids, embedding, final_gamma, sets, logits, *, H, n_apps=4, set_of_app=None,
+                        mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None, window=1, phi_mode=0,
+                        rms_eps=1e-6, rope_base=10000.0, final_rms_eps=1e-6, ws=None, stream=None):
+    """The shared-block language model (sec. 2.3): embedding, n_apps block applications,
+    final RMSNorm, tied logits.  ids: device int32 [B, T]; embedding [vocab, d];
+    final_gamma [d]; sets: list of weight dicts (gamma, Wq, Wk, Wg, Wv, Wo) of one gate
+    width; logits [B, T, vocab], written."""
+    if ids.dtype != torch.int32:
+        raise TypeError("ids must be an int32 tensor")
+    B, T = ids.shape
+    vocab, d = embedding.shape
+    d_qk, m = sets[0]["Wq"].shape[0], sets[0]["Wg"].shape[0]
+    p = model_params(B, T, d, H, d_qk, m, vocab, dtype=_dtype_code(embedding), n_apps=n_apps,
+                     n_sets=len(sets), set_of_app=set_of_app, mode=mode, s=s, tau=tau, null_bias=null_bias,
+                     window=window, phi_mode=phi_mode, rms_eps=rms_eps, rope_base=rope_base,
+                     final_rms_eps=final_rms_eps)
+    arr = (tg_block_weights * len(sets))(
+        *[tg_block_weights(*[_ptr(w[n]) for n in ("gamma", "Wq", "Wk", "Wg", "Wv", "Wo")]) for w in sets])
+    w = tg_model_weights(_ptr(embedding), _ptr(final_gamma), ctypes.cast(arr, ctypes.POINTER(tg_block_weights)))
+    need = load().tg_workspace_size(TG_WS_MODEL, ctypes.byref(p))
+    wbuf = _workspace(need, ids.device, ws)
+    wp, wn = _ws_ptr(wbuf)
+    st = load().tango_model_forward(ctypes.byref(p), ctypes.byref(w), _ptr(ids), _ptr(logits), wp, wn,
+                                    _stream(stream))
+    if st != TG_OK:
+        raise TgError(st, "tango_model_forward")
+    return logits

@@ -74,27 +74,50 @@ size_t agg_aux_bytes(const tg_agg_params* p, bool wango) {
 }
 size_t agg_ws_bytes(const tg_agg_params* p, bool wango) { return agg_qk_bytes(p) + agg_aux_bytes(p, wango); }
 
+// Per-head gate pitch of a block's internal g, u and gate-indexed weights: on the
+// tensor-core path m_h rounded up to a multiple of 8 (TMA wants 16-byte pitches and
+// head offsets), else m_h.  The padded entries are zero in W_g, W_v and W_o, so g, v
+// and u are zero there and add nothing to h_out.
+int gate_pitch(const tg_agg_params& a) {
+  const int m_h = a.m / a.H;
+  return a.dtype == TG_BF16 ? (m_h + 7) / 8 * 8 : m_h;
+}
+// The aggregation as the block runs it: gate width H * gate_pitch.
+tg_agg_params block_agg(const tg_block_params* p) {
+  tg_agg_params a = p->agg;
+  a.m = a.H * gate_pitch(p->agg);
+  return a;
+}
+
 struct BlockWs {
-  size_t x, q, k, g, v, aux, total;
+  size_t x, q, k, g, v, aux, wg, wv, wo, total;
+  bool padded;
 };
 
 BlockWs block_ws_layout(const tg_block_params* p) {
-  const tg_agg_params& a = p->agg;
+  const tg_agg_params a = block_agg(p);
   const size_t es = elem_size(a.dtype), BT = (size_t)a.B * a.T;
   BlockWs w;
+  w.padded = a.m != p->agg.m;
   w.x = 0;
   w.q = w.x + align256(BT * p->d * es);
   w.k = w.q + align256(BT * a.d_qk * es);
   w.g = w.k + align256(BT * a.d_qk * es);
   w.v = w.g + align256(BT * a.m * es);
   w.aux = w.v + align256(BT * a.m * es);
-  w.total = w.aux + agg_aux_bytes(&a, p->mode == TG_MODE_WANGO);
+  w.wg = w.aux + agg_aux_bytes(&a, p->mode == TG_MODE_WANGO);
+  const size_t wbytes = w.padded ? align256((size_t)a.m * p->d * es) : 0;
+  w.wv = w.wg + wbytes;
+  w.wo = w.wv + wbytes;
+  w.total = w.wo + wbytes;
   return w;
 }
 
 tg_status validate_block(const tg_block_params* p) {
   if (!p) return TG_ERR_INVALID_ARG;
-  tg_status st = validate_agg(&p->agg, p->mode == TG_MODE_WANGO);
+  if (p->agg.H < 1 || p->agg.m < 1 || p->agg.m % p->agg.H != 0) return TG_ERR_INVALID_ARG;
+  const tg_agg_params a = block_agg(p);
+  tg_status st = validate_agg(&a, p->mode == TG_MODE_WANGO);
   if (st != TG_OK) return st;
   if (p->agg.flags != 0) return TG_ERR_INVALID_ARG;
   if (p->d < 1 || !(p->rms_eps > 0.f) || !(p->rope_base >= 0.f)) return TG_ERR_INVALID_ARG;
@@ -102,6 +125,49 @@ tg_status validate_block(const tg_block_params* p) {
   if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
   if (p->agg.dtype == TG_BF16 && p->d % 64 != 0) return TG_ERR_UNSUPPORTED;
   return TG_OK;
+}
+
+// ---- model forward (sec. 2.3 eq. 11; the revision's gated-projection sets)
+constexpr int kMaxApps = 64, kMaxSets = 16;
+
+tg_status validate_model(const tg_model_params* p) {
+  if (!p) return TG_ERR_INVALID_ARG;
+  tg_status st = validate_block(&p->block);
+  if (st != TG_OK) return st;
+  if (p->vocab < 1 || p->n_apps < 1 || p->n_apps > kMaxApps || p->n_sets < 1 || p->n_sets > kMaxSets)
+    return TG_ERR_INVALID_ARG;
+  if (!(p->final_rms_eps > 0.f)) return TG_ERR_INVALID_ARG;
+  if (p->set_of_app) {
+    for (int r = 0; r < p->n_apps; ++r)
+      if (p->set_of_app[r] < 0 || p->set_of_app[r] >= p->n_sets) return TG_ERR_INVALID_ARG;
+  } else if (p->n_sets != 1 && p->n_sets != 3) {
+    return TG_ERR_INVALID_ARG;  // no default assignment for this many sets
+  }
+  if (p->block.agg.dtype == TG_BF16 && p->vocab % 8 != 0) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+// The set used by application r: the caller's table, else all set 0 (one set) or the
+// first / middle / last assignment of three sets.
+int set_of(const tg_model_params* p, int r) {
+  if (p->set_of_app) return p->set_of_app[r];
+  if (p->n_sets == 1) return 0;
+  return r == 0 ? 0 : (r == p->n_apps - 1 ? 2 : 1);
+}
+
+struct ModelWs {
+  size_t h, x, block, total;
+};
+
+ModelWs model_ws_layout(const tg_model_params* p) {
+  const tg_agg_params& a = p->block.agg;
+  const size_t hb = align256((size_t)a.B * a.T * p->block.d * elem_size(a.dtype));
+  ModelWs w;
+  w.h = 0;
+  w.x = hb;
+  w.block = 2 * hb;
+  w.total = w.block + block_ws_layout(&p->block).total;
+  return w;
 }
 
 tg_status check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -176,7 +242,7 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
   if (st != TG_OK) return st;
   if (!w || !w->rms_gamma || !w->Wq || !w->Wk || !w->Wg || !w->Wv || !w->Wo || !h || !h_out)
     return TG_ERR_INVALID_ARG;
-  const tg_agg_params& ap = p->agg;
+  const tg_agg_params ap = block_agg(p);  // gate width padded per head where needed
   if (ap.dtype == TG_BF16) {
     const void* ptrs[] = {w->rms_gamma, w->Wq, w->Wk, w->Wg, w->Wv, w->Wo, h, h_out};
     for (const void* x : ptrs)
@@ -222,8 +288,19 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
     e = launch_gemm_simt(ap.dtype, vb, w->Wo, h_out, h, M, d, ap.m, d, kEpiResidual, stream);
     return cuda_status(e);
   }
+  const void *Wg = w->Wg, *Wv = w->Wv, *Wo = w->Wo;
+  if (L.padded) {  // each head's gate rows (W_g, W_v) and columns (W_o) at the padded pitch
+    const int m_h = p->agg.m / ap.H, m_hp = ap.m / ap.H;
+    e = launch_pad_gate(ap.dtype, w->Wg, base + L.wg, ap.m, d, 0, ap.H, m_h, m_hp, stream);
+    if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wv, base + L.wv, ap.m, d, 0, ap.H, m_h, m_hp, stream);
+    if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wo, base + L.wo, d, ap.m, 1, ap.H, m_h, m_hp, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    Wg = base + L.wg;
+    Wv = base + L.wv;
+    Wo = base + L.wo;
+  }
   ProjArgs pa;
-  pa.x = x; pa.Wq = w->Wq; pa.Wk = w->Wk; pa.Wg = w->Wg; pa.Wv = w->Wv;
+  pa.x = x; pa.Wq = w->Wq; pa.Wk = w->Wk; pa.Wg = Wg; pa.Wv = Wv;
   pa.q = qb; pa.k = kb; pa.g = gb; pa.v = vb;
   pa.M = M; pa.d = d; pa.T = ap.T; pa.H = ap.H; pa.dqk = ap.d_qk; pa.m = ap.m;
   pa.rope_base = p->rope_base; pa.err = a.err;
@@ -231,7 +308,43 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
   if (e != cudaSuccess) return TG_ERR_CUDA;
   e = p->mode == TG_MODE_WANGO ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
-  e = launch_out_tc(vb, w->Wo, h, h_out, M, d, ap.m, a.err, stream);
+  e = launch_out_tc(vb, Wo, h, h_out, M, d, ap.m, a.err, stream);
+  return cuda_status(e);
+}
+
+tg_status tango_model_forward(const tg_model_params* p, const tg_model_weights* w, const int* ids, void* logits,
+                              void* ws, size_t ws_bytes, tg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  tg_status st = validate_model(p);
+  if (st != TG_OK) return st;
+  if (!w || !w->embedding || !w->final_gamma || !w->sets || !ids || !logits) return TG_ERR_INVALID_ARG;
+  const tg_agg_params& ap = p->block.agg;
+  if (ap.dtype == TG_BF16 && !(aligned16(w->embedding) && aligned16(w->final_gamma) && aligned16(logits)))
+    return TG_ERR_UNSUPPORTED;
+  const ModelWs L = model_ws_layout(p);
+  st = check_ws(ws, ws_bytes, L.total);
+  if (st != TG_OK) return st;
+  char* base = static_cast<char*>(ws);
+  void *h = base + L.h, *x = base + L.x, *bws = base + L.block;
+  const long long BT = (long long)ap.B * ap.T;
+  const int d = p->block.d;
+  unsigned* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return TG_ERR_CUDA;
+
+  // h^(0): token embeddings (the tied matrix)
+  if (launch_embed(ap.dtype, ids, w->embedding, h, BT, d, p->vocab, err, stream) != cudaSuccess) return TG_ERR_CUDA;
+  // eq. 11: h^(r+1) = Block(h^(r)), in place
+  for (int r = 0; r < p->n_apps; ++r) {
+    st = tango_block_forward(&p->block, &w->sets[set_of(p, r)], h, h, bws, L.total - L.block, stream_);
+    if (st != TG_OK) return st;
+  }
+  // final RMSNorm, then logits against the tied embedding: x E^T
+  if (launch_rmsnorm(ap.dtype, h, w->final_gamma, x, BT, d, p->final_rms_eps, stream) != cudaSuccess)
+    return TG_ERR_CUDA;
+  cudaError_t e = ap.dtype == TG_BF16
+                      ? launch_matmul_tc(x, w->embedding, logits, (int)BT, p->vocab, d, err, stream)
+                      : launch_gemm_simt(ap.dtype, x, w->embedding, logits, nullptr, (int)BT, p->vocab, d, p->vocab,
+                                         kEpiStore, stream);
   return cuda_status(e);
 }
 
@@ -246,6 +359,11 @@ size_t tg_workspace_size(int which, const void* params) {
     const tg_block_params* p = static_cast<const tg_block_params*>(params);
     if (validate_block(p) != TG_OK) return 0;
     return block_ws_layout(p).total;
+  }
+  if (which == TG_WS_MODEL) {
+    const tg_model_params* p = static_cast<const tg_model_params*>(params);
+    if (validate_model(p) != TG_OK) return 0;
+    return model_ws_layout(p).total;
   }
   return 0;
 }

@@ -3,6 +3,7 @@
 //   projection  [q | k | g | v] = x [W_q | W_k | W_g | W_v]^T      (eq. 2)
 //               epilogues: RoPE then unit norm per head (q, k), SiLU (g), none (v)
 //   output      h_out = h + u W_o^T                                 (eq. 3)
+//   plain       C = A B^T, bf16 out (the tied-embedding logits of sec. 2.3)
 //
 // C[M, N] = A[M, K] * B[N, K]^T with both operands K-major bf16, fp32 accumulation
 // in tensor memory.  Persistent kernel, one CTA per SM, warp-specialised:
@@ -394,6 +395,25 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   a.v = static_cast<__nv_bfloat16*>(p.v);
   a.err = p.err;
   return launch(mA, mq, mk, mg, mv, mog, mov, a, s);
+}
+
+cudaError_t launch_matmul_tc(const void* A, const void* B, void* C, int M, int N, int K, unsigned* err,
+                             cudaStream_t s) {
+  // the identity-epilogue segment alone: 128 x 256 tiles, bf16 out through TMA stores
+  CUtensorMap mA, mB, mC;
+  cudaError_t e = make_tmap_2d(&mA, A, M, K, K, BM, BK);
+  if (e == cudaSuccess) e = make_tmap_2d(&mB, B, N, K, K, BN, BK);
+  if (e == cudaSuccess) e = make_tmap_2d(&mC, C, M, N, N, BM, 64);
+  if (e != cudaSuccess) return e;
+  GemmArgs a = {};
+  a.M = M; a.K = K;
+  a.n_mblk = ceil_div(M, BM);
+  a.nb_v = ceil_div(N, BN);
+  a.m_major = 0;
+  a.T = 1; a.H = 1; a.m = N; a.d = 0;
+  a.v = static_cast<__nv_bfloat16*>(C);
+  a.err = err;
+  return launch(mA, mB, mB, mB, mB, mC, mC, a, s);
 }
 
 cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_out, int M, int d, int m,

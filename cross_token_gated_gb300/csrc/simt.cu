@@ -411,6 +411,71 @@ cudaError_t launch_rmsnorm(tg_dtype dt, const void* h, const void* gamma, void* 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------- model helpers
+
+// Token-embedding lookup (sec. 2.3): h[r, :] = E[ids[r], :], one warp per row.  An id
+// outside [0, vocab) is flagged in the error word and its row is written as zeros.
+template <typename T>
+__global__ void embed_kernel(const int* ids, const T* E, T* h, long long rows, int d, int vocab, unsigned* err) {
+  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int id = ids[r];
+  const bool ok = id >= 0 && id < vocab;
+  if (!ok && lane == 0) record_error(err, kErrValue | kKernModel);
+  const T* src = E + (long long)(ok ? id : 0) * d;
+  T* dst = h + r * d;
+  for (int c = lane; c < d; c += 32) dst[c] = ok ? src[c] : T(0.f);
+}
+
+// Copy of a gate-indexed weight with each head's block of m_h entries moved to a
+// pitch of m_hp (>= m_h) entries, zeros after it.  axis 0: src [H*m_h, C] -> dst
+// [H*m_hp, C] (W_g, W_v); axis 1: src [R, H*m_h] -> dst [R, H*m_hp] (W_o).  R, C are
+// the destination's extents.  A plain element copy; no arithmetic.
+template <typename T>
+__global__ void pad_gate_kernel(const T* src, T* dst, long long R, long long C, int axis, int H, int m_h,
+                                int m_hp) {
+  const long long n = R * C;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+    const long long r = e / C, c = e % C;
+    const long long gi = axis == 0 ? r : c;  // padded gate index
+    const int head = (int)(gi / m_hp), j = (int)(gi % m_hp);
+    T x = T(0.f);
+    if (j < m_h) {
+      const long long sg = (long long)head * m_h + j;  // unpadded gate index
+      x = axis == 0 ? src[sg * C + c] : src[r * ((long long)H * m_h) + sg];
+    }
+    dst[e] = x;
+  }
+}
+
+cudaError_t launch_embed(tg_dtype dt, const int* ids, const void* E, void* h, long long rows, int d, int vocab,
+                         unsigned* err, cudaStream_t s) {
+  const int warps = 8;
+  const unsigned blocks = (unsigned)((rows + warps - 1) / warps);
+  if (dt == TG_F32)
+    embed_kernel<float><<<blocks, warps * 32, 0, s>>>(ids, static_cast<const float*>(E), static_cast<float*>(h),
+                                                      rows, d, vocab, err);
+  else
+    embed_kernel<__nv_bfloat16><<<blocks, warps * 32, 0, s>>>(ids, static_cast<const __nv_bfloat16*>(E),
+                                                              static_cast<__nv_bfloat16*>(h), rows, d, vocab, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_gate(tg_dtype dt, const void* src, void* dst, long long R, long long C, int axis, int H,
+                            int m_h, int m_hp, cudaStream_t s) {
+  const long long n = R * C;
+  const long long want = (n + 255) / 256;
+  const unsigned blocks = (unsigned)(want < 4096 ? (want > 0 ? want : 1) : 4096);
+  if (dt == TG_F32)
+    pad_gate_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(src), static_cast<float*>(dst), R, C,
+                                                  axis, H, m_h, m_hp);
+  else
+    pad_gate_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
+                                                          static_cast<__nv_bfloat16*>(dst), R, C, axis, H, m_h, m_hp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_simt(tg_dtype dt, const void* A, const void* B, void* C, const void* R, int M, int N,
                              int K, int ldc, int epi, cudaStream_t s) {
   dim3 grid((N + 63) / 64, (M + 63) / 64);

@@ -40,6 +40,13 @@ cudaError_t launch_rmsnorm(tg_dtype dt, const void* h, const void* gamma, void* 
 // C[M, N] (row pitch ldc) = epi(A[M, K] * B[N, K]^T), fp32 accumulation.
 cudaError_t launch_gemm_simt(tg_dtype dt, const void* A, const void* B, void* C, const void* R, int M, int N,
                              int K, int ldc, int epi, cudaStream_t s);
+// h[r, :] = E[ids[r], :] (sec. 2.3); ids outside [0, vocab) give zero rows and an error flag.
+cudaError_t launch_embed(tg_dtype dt, const int* ids, const void* E, void* h, long long rows, int d, int vocab,
+                         unsigned* err, cudaStream_t s);
+// Gate-indexed weight with each head's m_h entries at a pitch of m_hp, zero-padded;
+// axis 0 pads rows (W_g, W_v), axis 1 columns (W_o).  R, C: destination extents.
+cudaError_t launch_pad_gate(tg_dtype dt, const void* src, void* dst, long long R, long long C, int axis, int H,
+                            int m_h, int m_hp, cudaStream_t s);
 cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
 cudaError_t launch_wango_simt(const AggArgs& a, cudaStream_t s);
 

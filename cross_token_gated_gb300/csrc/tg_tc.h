@@ -20,6 +20,10 @@ cudaError_t launch_proj_tc(const ProjArgs& a, cudaStream_t s);
 // h_out [M, d] = h + u [M, m] * Wo [d, m]^T
 cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_out, int M, int d, int m,
                           unsigned* err, cudaStream_t s);
+// C [M, N] = A [M, K] * B [N, K]^T, bf16 in and out, fp32 accumulation; K % 8 == 0,
+// N % 8 == 0 and 16-byte-aligned bases (TMA).
+cudaError_t launch_matmul_tc(const void* A, const void* B, void* C, int M, int N, int K, unsigned* err,
+                             cudaStream_t s);
 cudaError_t launch_tango_tc(const AggArgs& a, cudaStream_t s);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
 // Scratch bytes the tensor-core WANGO path needs in AggArgs::aux (256-byte aligned):

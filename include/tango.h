@@ -6,6 +6,9 @@
  *   - tango_aggregate      sec. 2.1 eq. 5 with the full-prefix weights of sec. 2.2 eq. 6
  *   - wango_aggregate      sec. 2.1 eq. 5 with the windowed weights of sec. 2.2 eqs. 7-10
  *   - tango_block_forward  one block application, sec. 2.1 eqs. 2-3 around either of the above
+ *   - tango_model_forward  the language model of sec. 2.3: token embedding, the shared block
+ *                          applied n times (eq. 11), final RMSNorm and tied logits; with
+ *                          one weight set, or with the revision's gated-projection sets
  *
  * Conventions shared by every call:
  *   - Every pointer argument named as "device" is a CUDA device pointer owned by the
@@ -63,6 +66,7 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 #define TG_WS_TANGO 0 /* params: const tg_agg_params*   */
 #define TG_WS_WANGO 1 /* params: const tg_agg_params*   */
 #define TG_WS_BLOCK 2 /* params: const tg_block_params* */
+#define TG_WS_MODEL 3 /* params: const tg_model_params* */
 
 #define TG_MAX_HEADS 64
 
@@ -153,12 +157,65 @@ typedef struct {
  * h: device [B, T, d], read.  h_out: device [B, T, d], written; may alias h.
  * ws: device scratch of at least tg_workspace_size(TG_WS_BLOCK, p) bytes, 256-byte
  * aligned.  On return it holds, in this order, each region starting on a 256-byte
- * boundary: x [B*T, d], unit q [B*T, d_qk], unit k [B*T, d_qk], g [B*T, m] and
- * u = gbar * v [B*T, m] (v is overwritten in place).
+ * boundary: x [B*T, d], unit q [B*T, d_qk], unit k [B*T, d_qk], g [B*T, m'] and
+ * u = gbar * v [B*T, m'] (v is overwritten in place).
+ * Gate width: the aggregate calls need m_h % 8 == 0 in bf16; the block does not.  In
+ * bf16 it keeps each head's gates at a pitch of m_hp = m_h rounded up to a multiple
+ * of 8, m' = H * m_hp: it copies W_g, W_v (rows) and W_o (columns) into the end of ws
+ * at that pitch with zeros in the added entries, so g, v and u are zero there and
+ * h_out is the unpadded block's.  Otherwise (fp32, or m_h % 8 == 0) m' = m and no copy
+ * is made.
  */
 tg_status tango_block_forward(const tg_block_params *p, const tg_block_weights *w,
                               const void *h, void *h_out, void *ws, size_t ws_bytes,
                               tg_stream_t stream);
+
+/*
+ * A language model built from one shared block (sec. 2.3): token embedding with the
+ * tied matrix E, n_apps block applications h^(r+1) = Block(h^(r)) (eq. 11), a final
+ * RMSNorm and logits = RMSNorm(h) E^T.  No application embedding is added and the
+ * token embeddings are not re-added between applications.
+ */
+typedef struct {
+    const void *embedding;          /* device [vocab, d]: input lookup and output matrix */
+    const void *final_gamma;        /* device [d]: gain of the final RMSNorm              */
+    const tg_block_weights *sets;   /* HOST array [n_sets] of weight sets (device
+                                       pointers); the sets may share rms_gamma, Wq and Wk */
+} tg_model_weights;
+
+/*
+ * block          every application's parameters (B, T, H, d_qk, m, s/tau, null_bias,
+ *                window, phi_mode, dtype, d, mode, rms_eps, rope_base); m is the gate
+ *                width of every set
+ * vocab          rows of the embedding (>= 1; bf16 needs vocab % 8 == 0)
+ * n_apps         block applications (1..64)
+ * n_sets         weight sets (1..16)
+ * set_of_app     HOST int[n_apps]: the set of each application, or NULL for the
+ *                default: set 0 everywhere (n_sets == 1), or set 0 for the first
+ *                application, set 2 for the last and set 1 for the others (n_sets ==
+ *                3, the revision's first / middle / last assignment); NULL with any
+ *                other n_sets is TG_ERR_INVALID_ARG
+ * final_rms_eps  epsilon of the final RMSNorm (> 0)
+ */
+typedef struct {
+    tg_block_params block;
+    int vocab;
+    int n_apps;
+    int n_sets;
+    const int *set_of_app;
+    float final_rms_eps;
+} tg_model_params;
+
+/*
+ * ids: device int32 [B, T] token ids; an id outside [0, vocab) gives a zero embedding
+ * row and TG_ERR_DEVICE (kernel code 4) through tg_check_device_error().  logits:
+ * device [B, T, vocab], written.  ws: device scratch of at least
+ * tg_workspace_size(TG_WS_MODEL, p) bytes, 256-byte aligned: the residual stream
+ * [B*T, d], the final normalised x [B*T, d], then one block's workspace.  Each
+ * application is a tango_block_forward call and returns its errors.
+ */
+tg_status tango_model_forward(const tg_model_params *p, const tg_model_weights *w, const int *ids,
+                              void *logits, void *ws, size_t ws_bytes, tg_stream_t stream);
 
 /*
  * tango_aggregate for callers that cannot allocate device memory: runtimes that
@@ -199,7 +256,7 @@ const char *tg_status_string(tg_status s);
  * Returns TG_OK, TG_ERR_TIMEOUT or TG_ERR_DEVICE (the first kind recorded), or
  * TG_ERR_CUDA if the synchronisation itself failed.  If `detail` is not NULL it
  * receives the raw word (bit 0: timeout, bit 1: value out of range; bits 8..15:
- * the kernel that recorded it, 1 = TANGO, 2 = WANGO, 3 = GEMM).
+ * the kernel that recorded it, 1 = TANGO, 2 = WANGO, 3 = GEMM, 4 = embedding lookup).
  */
 tg_status tg_check_device_error(tg_stream_t stream, unsigned *detail);
 

@@ -229,5 +229,34 @@ def final_logits(h, gamma, E, *, rms_eps=1e-6):
     return out
 
 
+def default_sets(n_apps, n_sets):
+    """Set of each application when the caller gives no table: set 0 throughout for one
+    set; for three sets (the revision's abstract and Table 2: narrower gated-projection
+    sets for the first, middle and last applications) set 0 first, set 2 last and set 1
+    in between."""
+    if n_sets == 1:
+        return [0] * n_apps
+    if n_sets != 3:
+        raise ValueError("no default assignment for this many sets")
+    return [0 if r == 0 else (2 if r == n_apps - 1 else 1) for r in range(n_apps)]
+
+
+def model_forward(ids, E, final_gamma, sets, *, H, tau, n_apps=4, set_of_app=None, mode=0, window=1,
+                  phi_mode=0, null_bias=None, rms_eps=1e-6, final_rms_eps=1e-6, rope_base=10000.0):
+    """The shared-block language model (sec. 2.3 eq. 11): h^(0) = E[ids]; n_apps block
+    applications, application r with weight set set_of_app[r]; then the final RMSNorm
+    and the tied logits.  Nothing is added between applications.  ids [nb, T'];
+    returns logits [nb, T', vocab] in fp64.  By causality the logits of the first T'
+    positions depend only on the first T' ids, so a prefix of a longer sequence may be
+    passed."""
+    ids = np.asarray(ids, dtype=np.int64)
+    table = default_sets(n_apps, len(sets)) if set_of_app is None else list(set_of_app)
+    h = embed(ids, E)
+    for r in range(n_apps):
+        h = block_forward(h, sets[table[r]], H=H, tau=tau, mode=mode, window=window, phi_mode=phi_mode,
+                          null_bias=null_bias, rms_eps=rms_eps, rope_base=rope_base)
+    return final_logits(h, final_gamma, E, rms_eps=final_rms_eps)
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -104,6 +104,61 @@ def test_block_validation(lib):
         tg.TG_ERR_WORKSPACE
 
 
+def test_block_pads_unaligned_head_gate_width(lib):
+    """The block accepts a bf16 head gate width that is not a multiple of 8 (the
+    three-set width 9,494 = 2 x 4,747): its g and u use a pitch of 4,752 per head and the
+    padded W_g, W_v, W_o copies sit at the end of the workspace."""
+    B, T, d, dqk, H = 2, 64, 512, 128, 2
+    BT = B * T
+    bp = tg.block_params(B, T, d, H, dqk, 2 * 4747, dtype=tg.TG_BF16)
+    mp = 2 * 4752
+    def a256(x):
+        return (x + 255) // 256 * 256
+    want = a256(BT * d * 2) + 2 * a256(BT * dqk * 2) + 2 * a256(BT * mp * 2) + 3 * a256(mp * d * 2)
+    assert tg.tg_workspace_size(tg.TG_WS_BLOCK, bp) == want
+    # fp32 runs on the CUDA cores at the caller's width: no padding, no copies
+    bp = tg.block_params(B, T, d, H, dqk, 2 * 4747, dtype=tg.TG_F32)
+    assert tg.tg_workspace_size(tg.TG_WS_BLOCK, bp) == \
+        a256(BT * d * 4) + 2 * a256(BT * dqk * 4) + 2 * a256(BT * 2 * 4747 * 4)
+
+
+def _model(**kw):
+    base = dict(B=2, T=64, d=512, H=2, d_qk=128, m=256, vocab=1000, dtype=tg.TG_BF16)
+    base.update(kw)
+    args = [base.pop(x) for x in ("B", "T", "d", "H", "d_qk", "m", "vocab")]
+    return tg.model_params(*args, **base)
+
+
+def test_model_workspace_and_validation(lib):
+    raw = tg.load()
+    p = _model()
+    bp = tg.block_params(2, 64, 512, 2, 128, 256, dtype=tg.TG_BF16)
+    hb = 2 * 64 * 512 * 2
+    assert tg.tg_workspace_size(tg.TG_WS_MODEL, p) == 2 * hb + tg.tg_workspace_size(tg.TG_WS_BLOCK, bp)
+    for bad, status in [(dict(vocab=0), tg.TG_ERR_INVALID_ARG),
+                        (dict(n_apps=0), tg.TG_ERR_INVALID_ARG),
+                        (dict(n_apps=65), tg.TG_ERR_INVALID_ARG),
+                        (dict(n_sets=2), tg.TG_ERR_INVALID_ARG),          # no default for two sets
+                        (dict(n_sets=3, set_of_app=[0, 1, 3, 2]), tg.TG_ERR_INVALID_ARG),
+                        (dict(final_rms_eps=0.0), tg.TG_ERR_INVALID_ARG),
+                        (dict(vocab=1001), tg.TG_ERR_UNSUPPORTED),        # bf16 logits pitch
+                        (dict(d=60), tg.TG_ERR_UNSUPPORTED)]:
+        q = _model(**bad)
+        assert tg.tg_workspace_size(tg.TG_WS_MODEL, q) == 0
+        sets = (tg.tg_block_weights * 1)(tg.tg_block_weights(*([256] * 6)))
+        w = tg.tg_model_weights(256, 256, ctypes.cast(sets, ctypes.POINTER(tg.tg_block_weights)))
+        assert raw.tango_model_forward(ctypes.byref(q), ctypes.byref(w), 256, 256, None, 0, None) == status
+    assert tg.tg_workspace_size(tg.TG_WS_MODEL, _model(n_sets=2, set_of_app=[0, 1, 1, 0])) > 0
+    assert tg.tg_workspace_size(tg.TG_WS_MODEL, _model(vocab=1001, dtype=tg.TG_F32)) > 0
+    sets = (tg.tg_block_weights * 1)(tg.tg_block_weights(*([256] * 6)))
+    w = tg.tg_model_weights(256, None, ctypes.cast(sets, ctypes.POINTER(tg.tg_block_weights)))
+    assert raw.tango_model_forward(ctypes.byref(p), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    w = tg.tg_model_weights(256, 256, ctypes.cast(sets, ctypes.POINTER(tg.tg_block_weights)))
+    assert raw.tango_model_forward(ctypes.byref(p), ctypes.byref(w), 256, 256, None, 0, None) == \
+        tg.TG_ERR_WORKSPACE
+
+
 def test_binding_has_no_fallback(monkeypatch, tmp_path):
     """Without the library the binding raises instead of computing anything itself."""
     monkeypatch.setattr(tg, "_lib", None)

@@ -369,3 +369,68 @@ def test_model_logits_rmsnorm_scale_invariance():
     assert rel(a, x @ E.T) < 1e-13
     ids = np.array([[3, 0, 19]])
     np.testing.assert_array_equal(oracle.embed(ids, E), E[ids])
+
+
+# ------------------------------------------------------------------ model forward
+
+def _model_setup(n_sets, seed=70, d=16, H=2, dqk=8, m=12, vocab=11, B=2, T=7):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, vocab, size=(B, T))
+    E = 0.5 * rng.standard_normal((vocab, d))
+    shared = {"gamma": 1.0 + 0.1 * rng.standard_normal(d), "Wq": rng.standard_normal((dqk, d)) / 4,
+              "Wk": rng.standard_normal((dqk, d)) / 4}
+    sets = [dict(shared, Wg=rng.standard_normal((m, d)) / 4, Wv=rng.standard_normal((m, d)) / 4,
+                 Wo=rng.standard_normal((d, m)) / 4) for _ in range(n_sets)]
+    gam_f = 1.0 + 0.1 * rng.standard_normal(d)
+    return ids, E, gam_f, sets, H
+
+
+def test_model_default_set_assignment():
+    """The revision assigns three narrower gated-projection sets to the first, middle and
+    last applications; one set serves every application."""
+    assert oracle.default_sets(4, 3) == [0, 1, 1, 2]
+    assert oracle.default_sets(8, 3) == [0, 1, 1, 1, 1, 1, 1, 2]
+    assert oracle.default_sets(4, 1) == [0, 0, 0, 0]
+    with pytest.raises(ValueError):
+        oracle.default_sets(4, 2)
+
+
+def test_model_zero_output_projection_is_identity():
+    """W_o = 0 makes every application the identity (h_out = h + W_o u = h), so the model
+    reduces to the final RMSNorm of the embeddings against the tied matrix."""
+    ids, E, gam_f, sets, H = _model_setup(3)
+    for w in sets:
+        w["Wo"] = np.zeros_like(w["Wo"])
+    got = oracle.model_forward(ids, E, gam_f, sets, H=H, tau=10.0)
+    assert rel(got, oracle.final_logits(E[ids], gam_f, E)) < 1e-14
+
+
+@pytest.mark.parametrize("live,apps", [(0, 1), (1, 2), (2, 1)])
+def test_model_sets_applied_first_middle_last(live, apps):
+    """With W_o zero in all sets but one, only the applications of that set act: set 0
+    once (first), set 1 twice (the two middle applications of four), set 2 once (last)."""
+    ids, E, gam_f, sets, H = _model_setup(3, seed=71)
+    for s, w in enumerate(sets):
+        if s != live:
+            w["Wo"] = np.zeros_like(w["Wo"])
+    got = oracle.model_forward(ids, E, gam_f, sets, H=H, tau=10.0, n_apps=4)
+    h = E[ids]
+    for _ in range(apps):
+        h = oracle.block_forward(h, sets[live], H=H, tau=10.0)
+    assert rel(got, oracle.final_logits(h, gam_f, E)) < 1e-13
+    h1 = oracle.block_forward(E[ids], sets[live], H=H, tau=10.0)  # a different count is far off
+    if apps != 1:
+        assert rel(got, oracle.final_logits(h1, gam_f, E)) > 1e-3
+
+
+def test_model_prefix_causality():
+    """Positions before T' depend only on the first T' tokens (every step is causal), so
+    the logits of a prefix run equal the leading rows of the full run."""
+    ids, E, gam_f, sets, H = _model_setup(1, seed=72, T=9)
+    full = oracle.model_forward(ids, E, gam_f, sets, H=H, tau=10.0, mode=1, window=3)
+    pre = oracle.model_forward(ids[:, :4], E, gam_f, sets, H=H, tau=10.0, mode=1, window=3)
+    assert rel(pre, full[:, :4]) < 1e-13
+    changed = ids.copy()
+    changed[:, 6] = (changed[:, 6] + 1) % E.shape[0]
+    alt = oracle.model_forward(changed, E, gam_f, sets, H=H, tau=10.0, mode=1, window=3)
+    assert rel(alt[:, :6], full[:, :6]) < 1e-13 and rel(alt[:, 6:], full[:, 6:]) > 1e-6

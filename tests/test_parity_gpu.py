@@ -205,3 +205,87 @@ def test_bounded_wait_timeout_reports_status():
     assert tg.tg_check_device_error() == (tg.TG_OK, 0)      # the word was cleared
     out = run_agg("tango", q, k, g, v, H)
     assert rel_err(out, ref_agg("tango", q, k, g, v, H)) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ model forward
+
+def model_tol(dtype, n_apps=4):
+    """Tolerance of the model's logits: the per-operation bound times sqrt(n_apps).  Each
+    application adds its own storage roundings (h, x, q, k, g, v, u) and the residual
+    path carries earlier errors forward, so independent per-application errors add in
+    quadrature.  Measured on GB300 (bf16, d=128): max relative error 0.4-0.85 % after one
+    application and 1.1-2.4 % after four; RMS 0.55 % -> 1.2 %, the sqrt(4) growth."""
+    return TOL[dtype] * float(np.sqrt(n_apps))
+
+
+def model_setup(B, T, d, dqk, m, vocab, n_sets, seed, dtype):
+    """Token ids, the tied embedding N(0, 0.02^2), unit final gain and n_sets weight sets
+    that share gamma, W_q and W_k (each set owns W_g, W_v, W_o)."""
+    ids, E = synth.model_inputs(B, T, d, vocab, seed=seed, dtype=dtype)
+    _, w = synth.block_inputs(1, 1, d, dqk, m, seed=seed + 1, dtype=dtype)
+    sets = [w] + [dict(w, **synth.gated_set(d, m, seed + 2 + k, dtype=dtype)) for k in range(n_sets - 1)]
+    gam_f = synth.cast(np.ones(d, dtype=np.float32), dtype)
+    return ids, E, gam_f, sets
+
+
+def run_model(ids, E, gam_f, sets, H, mode, W, n_apps=4):
+    B, T = ids.shape
+    logits = torch.empty(B, T, E.shape[0], dtype=E.dtype, device="cuda")
+    tg.tango_model_forward(ids.to(torch.int32).cuda(), E.cuda(), gam_f.cuda(),
+                           [{n: t.cuda() for n, t in w.items()} for w in sets], logits, H=H, n_apps=n_apps,
+                           mode=mode, window=W)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    return logits
+
+
+def ref_model(ids, E, gam_f, sets, H, mode, W, n_apps=4):
+    return oracle.model_forward(ids.numpy(), synth.oracle_view(E), synth.oracle_view(gam_f),
+                                [{n: synth.oracle_view(t) for n, t in w.items()} for w in sets], H=H,
+                                tau=10.0, n_apps=n_apps, mode=mode, window=W, rope_base=10000.0,
+                                rms_eps=1e-6, final_rms_eps=1e-6)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_model_tiny_fp32(mode):
+    """Four applications of the tiny block (d=64, m=256, q/k width 32, W=16) with a
+    1,000-entry tied embedding, fp32, every logit compared."""
+    ids, E, gam_f, sets = model_setup(1, 64, 64, 32, 256, 1000, 1, seed=40, dtype="f32")
+    out = run_model(ids, E, gam_f, sets, 2, mode, 16)
+    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 16)) <= model_tol("f32")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_model_bf16_small(mode):
+    ids, E, gam_f, sets = model_setup(2, 100, 128, 64, 512, 1000, 1, seed=41, dtype="bf16")
+    out = run_model(ids, E, gam_f, sets, 2, mode, 32)
+    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 32)) <= model_tol("bf16")
+    # one application alone meets the per-operation bound
+    one = run_model(ids, E, gam_f, sets, 2, mode, 32, n_apps=1)
+    assert rel_err(one, ref_model(ids, E, gam_f, sets, 2, mode, 32, n_apps=1)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_model_three_sets_unaligned_gate_width(mode):
+    """Three gated-projection sets (first / middle / last applications) with a head gate
+    width of 47, which the bf16 block pads to 48 internally."""
+    ids, E, gam_f, sets = model_setup(2, 150, 128, 64, 94, 1000, 3, seed=42, dtype="bf16")
+    out = run_model(ids, E, gam_f, sets, 2, mode, 64)
+    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 64)) <= model_tol("bf16")
+    # the assignment matters: swapping the first and last sets changes the logits
+    swapped = run_model(ids, E, gam_f, [sets[2], sets[1], sets[0]], 2, mode, 64)
+    assert rel_err(swapped, ref_model(ids, E, gam_f, sets, 2, mode, 64)) > 3 * model_tol("bf16")
+
+
+@pytest.mark.parametrize("m,n_sets", [(28480, 1), (9494, 3)])
+def test_model_shared_block_config_sampled(m, n_sets):
+    """The shared-block model configuration: B=16, T=1024, d=512, q/k width 128, four
+    TANGO applications, 32,768-entry tied embedding, bf16; one set of m=28,480 or three
+    sets of m=9,494.  Sequences 0 and 15 are compared on their first 128 positions,
+    which by causality the oracle computes from those positions' tokens alone."""
+    B, T, d, dqk, vocab, Tp = 16, 1024, 512, 128, 32768, 128
+    ids, E, gam_f, sets = model_setup(B, T, d, dqk, m, vocab, n_sets, seed=43, dtype="bf16")
+    out = run_model(ids, E, gam_f, sets, 2, 0, 1)
+    got = out[[0, 15], :Tp]
+    ref = ref_model(ids[[0, 15], :Tp], E, gam_f, sets, 2, 0, 1)
+    assert rel_err(got, ref) <= model_tol("bf16")
