@@ -9,46 +9,31 @@
 //   S = sum phi(k~_j) g_j^T (d_h x gate columns),   z = sum phi(k~_j),
 // read out as  e^-tau phi(q~_i)^T S  and  e^-tau phi(q~_i)^T z.
 //
-// Two stages:
-//  1. wango_prep (CUDA cores): Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat)
-//     in bf16; per 128-source block the column sums of Fk; and per destination the
-//     older-prefix denominator Fq_i . z, z summed over the blocks older than the
-//     destination block's window (the same blocks the state holds below).
-//  2. wango_tc_kernel: one CTA walks, in order, the 128-row destination blocks ib of one
-//     (batch, head, 128-column gate tile) -- a "strip"; persistent CTAs take strips
-//     round-robin.  For destination block ib the per-pair sources are the blocks
-//        jb = jlo(ib) .. ib,   jlo(ib) = floor(max(0, 128 ib - W + 1) / 128),
-//     and the state holds every source j < 128 jlo(ib), older than the window for every
-//     destination of the block.  A block is "mixed" when it also holds older pairs
-//     (128 jb <= 128 ib + 127 - W): its weights need both scores.  A block "leaves" when
-//     jb < jlo(ib + 1): after its P.G MMA the same G tile updates the state.
+// Destination blocks ib (128 rows) take per-pair weights from the source blocks
+//     jb = jlo(ib) .. ib,   jlo(ib) = floor(max(0, 128 ib - W + 1) / 128);
+// the state holds every source j < 128 jlo(ib), older than the window for every
+// destination of the block.  A source block is "mixed" when it also holds older pairs
+// (128 jb <= 128 ib + 127 - W): its weights need the feature-map score too.  It
+// "leaves" when jb < jlo(ib + 1): after its P.G the same G tile updates the state.
 //
-// Roles of the main kernel (16 warps; warp 3 idle):
-//   warp 0       TMA: qhat and Fq of the destination block (one buffer each), khat
-//                (2-stage ring), Fk of mixed blocks (one buffer), G blocks (128 sources
-//                x 128 columns, 2-stage ring of 32 KB) and the destination block's v
-//                tile (two 32 KB buffers, which also stage u for its TMA store).
-//   warps 1, 2   MMA issue, one thread each, on two SM sub-partitions.  Per destination
-//                block the source blocks go newest first (jb = ib .. jlo), so the
-//                mixed / leaving blocks come last; a unit is a whole block, or one
-//                64-source half of a mixed block.
-//                warp 1: a unit's scores into an f32 TMEM slot (ring of 2): Sc = Qhat
-//                Khat^T (128 columns), or for a half Sc (64 columns) beside Sf = Fq Fk^T
-//                (64 columns); it runs ahead as far as the slots allow.
-//                warp 2: O (+)= P G from the unit's slot; for a leaving block
-//                S^T += G^T Fk (M=128, N=d_h) in TMEM; last, the read-out O += Fq S_bf16
-//                (the state before the block).
-//   warps 4-11   weights: warpgroup w takes sources [64w, 64w+64) of a block (or
-//                [32w, 32w+32) of a half): exp (window), the feature-map score (older) or
-//                0 (after i), rounded to bf16 and written as P over its own cos columns;
-//                the row sums of the bf16 weights (the denominator as applied) go to
-//                the epilogue through shared memory.
-//   warps 12-15  epilogue: gbar = O / den read out of TMEM into registers (rounded to
-//                bf16; O is released right after), u = gbar * v over v in shared memory,
-//                the copy S^T (TMEM, f32) -> S (shared memory, bf16) for the next
-//                destination block's read-out, then u stored by TMA.
-// TMEM: O [0,128), S^T [128, 128+d_h), score slots [256,384) and
-// [384,512).
+// The weights depend on q and k only, not on the gate column, so they are computed
+// once per destination block and shared by every gate column:
+//  1. Pre-pass (CUDA cores): Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat)
+//     in bf16; the column sums of Fk per source block; the older-prefix denominator
+//     Fq_i . z of every destination (z over the blocks below its block's window).
+//  2. wango_p_kernel (tcgen05): per (batch, head, destination block) the scores
+//     Qhat Khat^T (and Fq Fk^T for mixed blocks) in TMEM, the weights in bf16 written
+//     to global memory as P [destination, (ib - jb) * 128 + source], and the full
+//     denominator (the row sums of the bf16 weights as applied, the older prefix and
+//     the null term).  P is a band of T x (W + 128) per head: linear in T.
+//  3. wango_g_kernel (tcgen05): per (batch, head, 128-column gate strip) the
+//     destination blocks in order: O = sum_jb P_jb G_jb with both operands loaded by
+//     TMA, the state update S^T += G^T Fk for leaving blocks, the read-out
+//     O += Fq S_bf16 of the state before the block, and u = O / den * v.  Persistent
+//     CTAs take strips (or segments of strips) round-robin; O is double-buffered in
+//     TMEM so one block's epilogue overlaps the next block's MMAs.
+#include <algorithm>
+
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
 #include "tg_tc.h"
@@ -60,57 +45,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kBlk = 128;
-constexpr int kNg = 128;       // gate columns per strip
-constexpr int kKStages = 2;
-constexpr int kGStages = 2;
-constexpr int kThreads = 512;
-constexpr int kSoftWarp0 = 4, kEpiWarp0 = 12;
+constexpr int kNg = 128;                    // gate columns per strip
 constexpr uint32_t kTile = kBlk * 64 * 2;   // 16 KB: a 128 x d_h bf16 tile at d_h = 64
 constexpr uint32_t kGBox = 64 * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;     // 32 KB: 128 rows x 128 columns
-// TMEM columns: O, the state S^T, the row sums of P, two score slots (P, in bf16 pairs,
-// is written over each warpgroup's own cos columns)
-constexpr uint32_t kColO = 0, kColSt = 128, kColSlot0 = 256;
-
-struct __align__(8) Bars {
-  uint64_t qh_full, qh_empty;                   // qhat of a destination block
-  uint64_t fq_full, fq_empty;                   // Fq of a destination block
-  uint64_t k_full[kKStages], k_empty[kKStages]; // khat of a source block
-  uint64_t fk_full, fk_empty;                   // Fk of a mixed block
-  uint64_t g_full[kGStages], g_empty[kGStages]; // G of a source block
-  uint64_t v_full[2], v_empty[2];               // v of a destination block, then its u
-  uint64_t s_full[2], p_full[2];                // score slots; P in them
-  uint64_t slot_free[2];                        // P.G and row sums have read a slot
-  uint64_t o_full, o_empty;
-  uint64_t st_full;                             // a destination block's MMAs are done
-  uint64_t sb_full;                             // bf16 state copy in place
-  uint64_t den_full, den_empty;                 // the weights' row sums -> epilogue
-  uint64_t drain[2], never;
-  uint32_t tmem_base;
-  int abort;
-  float rowsum[2][kBlk];                        // per warpgroup, per destination row
-};
-
-// smem: Qhat | Fq | K x kKStages | Fk | S_bf16 | G x kGStages | V x 2 | ones | Bars
-constexpr size_t kSmemBytes = 1024 + kTile * (4 + kKStages) + kGStage * (kGStages + 2) + sizeof(Bars);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-struct Args {
-  int B, T, H, dqk, m, d_h, m_h, W;
-  int n_iblk, n_ntile, n_strips;
-  int nseg, seg_len, n_items;  // each strip's destination blocks in nseg segments
-  float* seg_state;            // [n_strips, nseg - 1, kNg, d_h] f32 state at segment ends
-  int* seg_flag;               // [n_strips, nseg - 1], 0 until that state is written
-  float s;
-  const float* tau;
-  const float* null_bias;
-  const float* den_old;  // [B, H, T]
-  int has_v;
-  __nv_bfloat16* out;
-  unsigned* err;
-  uint64_t timeout_ns;
-  int debug_timeout;
-};
 
 __host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
   const int lo = ib * kBlk - W + 1;
@@ -118,70 +56,6 @@ __host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
 }
 __device__ __forceinline__ bool is_mixed(int jb, int ib, int W) { return jb * kBlk <= ib * kBlk + kBlk - 1 - W; }
 __device__ __forceinline__ bool is_leaving(int jb, int ib, int W) { return jb < jlo_of(ib + 1, W); }
-// Slot column of P for 16-source step kk of a unit: warpgroup w writes the P of its
-// sources over its own cos columns, at 64 w for a whole block (h < 0, 4 steps each) and
-// at 32 w for a half (2 steps each).
-__device__ __forceinline__ uint32_t p_col(int kk, int h) {
-  return h < 0 ? (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8) : (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
-}
-
-struct Strip {
-  int b, head, n0;
-};
-// A work item: destination blocks [ib0, ib1) of one strip, segment `seg` of nseg.
-// Items are numbered segment-major, so every strip's segment k comes before any
-// segment k + 1.  A segment that ends with a non-empty state hands it (f32) to the
-// next segment through global memory and a per-strip flag.
-struct Item {
-  int st, seg, ib0, ib1;
-};
-template <bool kSeg>
-__device__ __forceinline__ Item item_of(const Args& a, int w) {
-  Item it;
-  if (kSeg) {
-    it.seg = w / a.n_strips;
-    it.st = w % a.n_strips;
-    it.ib0 = it.seg * a.seg_len;
-    it.ib1 = min(a.n_iblk, it.ib0 + a.seg_len);
-  } else {  // one segment per strip
-    it.seg = 0;
-    it.st = w;
-    it.ib0 = 0;
-    it.ib1 = a.n_iblk;
-  }
-  return it;
-}
-__device__ __forceinline__ Strip strip_of(const Args& a, int s) {
-  Strip r;
-  r.n0 = (s % a.n_ntile) * kNg;
-  r.head = (s / a.n_ntile) % a.H;
-  r.b = s / (a.n_ntile * a.H);
-  return r;
-}
-
-__device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
-  if (*(volatile int*)&b.abort) return false;
-  if (mbar_wait(bar, parity, a.timeout_ns)) return true;
-  *(volatile int*)&b.abort = 1;
-  record_error(a.err, kErrTimeout | kKernWango);
-  return false;
-}
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
-  if (mbar_try_wait_nc(smem_u32(bar), parity)) return true;
-  return wait_slow(bar, parity, b, a);
-}
-
-// Waits, bounded, until another CTA of this launch sets *flag (acquire).
-__device__ __forceinline__ bool wait_flag(const int* flag, const Args& a) {
-  const uint64_t t0 = globaltimer_ns();
-  while (ld_acquire_gpu(flag) == 0) {
-    if (globaltimer_ns() - t0 > a.timeout_ns) {
-      record_error(a.err, kErrTimeout | kKernWango);
-      return false;
-    }
-  }
-  return true;
-}
 
 struct Ring {
   int stage = 0;
@@ -190,6 +64,22 @@ struct Ring {
     if (++stage == n) { stage = 0; phase ^= 1; }
   }
 };
+
+// Bounded waits: on expiry the kernel records a timeout and sets its abort flag, after
+// which every role leaves its loops.  Bars needs `abort`, Args `err` and `timeout_ns`.
+template <typename Bars, typename Args>
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+  if (*(volatile int*)&b.abort) return false;
+  if (mbar_wait(bar, parity, a.timeout_ns)) return true;
+  *(volatile int*)&b.abort = 1;
+  record_error(a.err, kErrTimeout | kKernWango);
+  return false;
+}
+template <typename Bars, typename Args>
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
+  if (mbar_try_wait_nc(smem_u32(bar), parity)) return true;
+  return wait_slow(bar, parity, b, a);
+}
 
 // Byte offset of element column c (16-bit elements) of row r in a tile whose rows
 // are RB bytes wide, stored with the matching TMA/UMMA swizzle (RB = 32, 64, 128).
@@ -204,6 +94,8 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 //   kMode 0: every source is in the window: exp2(c (s - 1)).
 //   kMode 2: general: 0 after i, exp2(c (s - 1)) in the window (j >= jw), else the
 //            feature-map score f (older source).
+// dsum2 accumulates the row sum of the weights as rounded to bf16 (the denominator
+// as applied), two f32 lanes per packed instruction.
 template <int kMode>
 __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
                                           uint32_t (&p)[16], uint64_t (&dsum2)[2]) {
@@ -221,10 +113,341 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
       if (j0 + e + 1 > i) w1 = 0.f;
     }
     const uint32_t pk = pack_bf16x2(w0, w1);
-    // the row sum of the weights as applied (bf16), two f32 lanes per instruction
     dsum2[(e >> 1) & 1] = add_f32x2(dsum2[(e >> 1) & 1], bf16x2_widen(pk));
     p[e / 2] = pk;
   }
+}
+
+// ================================================================= weights (P) kernel
+
+constexpr int kPThreads = 384;  // warp 0 TMA, warp 1 scores (and TMEM), warps 4-11 weights
+constexpr int kPWeightWarp0 = 4;
+constexpr int kPSlots = 2;      // 128-column score slots in TMEM
+
+struct __align__(8) PBars {
+  uint64_t qh_full, fq_full;       // qhat and Fq of the destination block
+  uint64_t k_full[2], k_empty[2];  // khat ring
+  uint64_t fk_full, fk_empty;      // Fk of a mixed block
+  uint64_t s_full[kPSlots], slot_free[kPSlots];
+  uint64_t rs_full;                // both warpgroups' row sums are in shared memory
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float rowsum[2][kBlk];           // per warpgroup, per destination row
+};
+// smem: Qhat | Fq | K x 2 | Fk | Bars
+constexpr size_t kPSmemBytes = 1024 + kTile * 5 + sizeof(PBars);
+
+struct PArgs {
+  int B, T, T_pad, H, dqk, d_h, W, n_iblk, ldp;
+  float s;
+  const float* tau;
+  const float* null_bias;
+  const float* den_old;  // [B, H, T]
+  __nv_bfloat16* P;      // [B * H, T_pad, ldp]
+  float* den;            // [B * H, T_pad]
+  unsigned* err;
+  uint64_t timeout_ns;
+};
+
+// One CTA per (destination block ib, head, batch).  Work units, newest source block
+// first: a whole block (cos scores, 128 columns of a slot), or one 64-source half of a
+// mixed block (cos scores in columns [0, 64) of the slot, feature-map scores in
+// [64, 128)).  The weight warps turn a unit's scores into bf16 weights and write them
+// to P; warpgroup w takes sources [64 w, 64 w + 64) of a block or [32 w, 32 w + 32) of
+// a half.
+template <int DH>
+__global__ void __launch_bounds__(kPThreads, 1)
+    wango_p_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
+                   const PArgs a) {
+  constexpr int RB = DH * 2;  // bytes per row of the q/k/feature tiles
+  constexpr uint32_t lay = DH == 64 ? kSwizzle128B : DH == 32 ? kSwizzle64B : kSwizzle32B;
+  constexpr uint32_t sbo = 8u * RB;
+  constexpr uint32_t tile_bytes = kBlk * RB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sFQ = sQ + kTile;
+  uint8_t* sK = sFQ + kTile;  // 2 tiles
+  uint8_t* sFK = sK + 2 * kTile;
+  PBars& b = *reinterpret_cast<PBars*>(sFK + kTile);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int ib = blockIdx.x, head = blockIdx.y, bb = blockIdx.z;
+  const int W = a.W, jlo = jlo_of(ib, W);
+  const bool any_mixed = is_mixed(jlo, ib, W);  // the oldest source block is mixed if any is
+
+  if (threadIdx.x == 0) {
+    mbar_init(&b.qh_full, 1);
+    mbar_init(&b.fq_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&b.k_full[s], 1);
+      mbar_init(&b.k_empty[s], 1);
+    }
+    mbar_init(&b.fk_full, 1);
+    mbar_init(&b.fk_empty, 1);
+    for (int s = 0; s < kPSlots; ++s) {
+      mbar_init(&b.s_full[s], 1);
+      mbar_init(&b.slot_free[s], 8);
+    }
+    mbar_init(&b.rs_full, 8);
+    mbar_init(&b.drain, 1);
+    b.abort = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(&b.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    bool ok = true;
+    mbar_arrive_expect_tx(&b.qh_full, tile_bytes);
+    tma_load_3d(sQ, &tmQ, &b.qh_full, head * DH, ib * kBlk, bb);
+    if (any_mixed) {
+      mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
+      tma_load_3d(sFQ, &tmFQ, &b.fq_full, head * DH, ib * kBlk, bb);
+    }
+    Ring kr;
+    uint32_t kmask = 0, kph[2] = {}, fkph = 0, fk_n = 0;
+    for (int jb = ib; ok && jb >= jlo; --jb) {
+      if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
+      mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
+      tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], head * DH, jb * kBlk, bb);
+      kmask |= 1u << kr.stage;
+      kph[kr.stage] = kr.phase;
+      kr.next(2);
+      if (is_mixed(jb, ib, W)) {
+        if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
+        mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
+        tma_load_3d(sFK, &tmFK, &b.fk_full, head * DH, jb * kBlk, bb);
+        fkph ^= 1;
+        ++fk_n;
+      }
+    }
+    // no copy may be in flight when the CTA exits
+    mbar_wait(&b.qh_full, 0, a.timeout_ns);
+    if (any_mixed) mbar_wait(&b.fq_full, 0, a.timeout_ns);
+    if (fk_n) mbar_wait(&b.fk_full, (fk_n - 1) & 1, a.timeout_ns);
+    for (int s = 0; s < 2; ++s)
+      if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issue: scores
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);  // 128 sources
+    constexpr uint32_t idesc_h = idesc_bf16_f32(kBlk, 64, false, false);    // 64 sources
+    const uint64_t qd = smem_desc(smem_u32(sQ), 16, sbo, lay);
+    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
+    const uint64_t kd0 = smem_desc(smem_u32(sK), 16, sbo, lay);
+    const uint64_t fkd = smem_desc(smem_u32(sFK), 16, sbo, lay);
+    bool ok = wait_bar(&b.qh_full, 0, b, a);
+    if (ok && any_mixed) ok = wait_bar(&b.fq_full, 0, b, a);
+    Ring ks;
+    uint32_t u = 0, fkph = 0;
+    for (int jb = ib; ok && jb >= jlo; --jb) {
+      const bool mixed = is_mixed(jb, ib, W);
+      for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
+        const int slot = u & 1;
+        if (u >= 2 && !(ok = wait_bar(&b.slot_free[slot], ((u - 2) >> 1) & 1, b, a))) break;
+        if (!(ok = wait_bar(&b.k_full[ks.stage], ks.phase, b, a))) break;
+        if (h >= 0 && !(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
+        tc_fence_after_nc();
+        const uint64_t kd = kd0 + (uint64_t)((ks.stage * kTile) >> 4);
+        const uint32_t sc = tmem + (uint32_t)(slot * 128);
+        if (h < 0) {
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk)
+            mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
+        } else {
+          const uint64_t hoff = (uint64_t)((h * 64 * RB) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk)
+            mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk)
+            mma_bf16_ss_nc(sc + 64, fqd + (uint64_t)(kk * 2), fkd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
+        }
+        mma_commit_nc(&b.s_full[slot]);
+        ++u;
+        if (h != 0) {  // the block's last unit releases its khat
+          mma_commit_nc(&b.k_empty[ks.stage]);
+          ks.next(2);
+        }
+        if (h == 1) {
+          mma_commit_nc(&b.fk_empty);
+          fkph ^= 1;
+        }
+      }
+    }
+    mma_commit(&b.drain);
+    mbar_wait(&b.drain, 0, a.timeout_ns);
+  } else if (warp >= kPWeightWarp0 && warp < kPWeightWarp0 + 8) {
+    // ------------------------------------------------------------ weights -> P, row sums
+    const int wg = (warp - kPWeightWarp0) / 4;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int i = ib * kBlk + row;
+    const int i0 = ib * kBlk + quarter * 32;
+    const float tau = head_tau(a.tau, a.s, head, a.err, kKernWango);
+    const float c = tau * kLog2e;
+    __nv_bfloat16* prow = a.P + ((size_t)(bb * a.H + head) * a.T_pad + i) * a.ldp;
+    uint64_t dsum2[2] = {0, 0};
+    bool ok = true;
+    uint32_t u = 0;
+    for (int jb = ib; ok && jb >= jlo; --jb) {
+      const bool mixed = is_mixed(jb, ib, W);
+      for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h, ++u) {
+        const int slot = u & 1;
+        const uint32_t sl = tmem + (uint32_t)(slot * 128) + lane_off;
+        if (!(ok = wait_bar(&b.s_full[slot], (u >> 1) & 1, b, a))) break;
+        tc_fence_after();
+        // One 32-source chunk at a time: two per warpgroup for a whole block, one for a
+        // half, whose feature-map scores sit 64 columns after its cos scores.  Each
+        // chunk is classified for this warp's 32 rows: after every row (zero weights),
+        // inside every row's window (exp only) or general.
+        const int nq = h < 0 ? 2 : 1;
+#pragma unroll 1
+        for (int q = 0; q < nq; ++q) {
+          const int off = h < 0 ? wg * 64 + q * 32 : h * 64 + wg * 32;  // first source in the block
+          const uint32_t cs = sl + (uint32_t)(h < 0 ? off : wg * 32);     // its cos score column
+          const int js = jb * kBlk + off;
+          uint32_t p[16];
+          if (js > i0 + 31) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) p[e] = 0u;
+          } else if (js + 31 <= i0 && js >= i0 + 32 - W) {
+            uint32_t rq[32];
+            tmem_ld32(cs, rq);
+            tmem_ld_wait();
+            weights32<0>(rq, rq, c, js, i, 0, p, dsum2);
+          } else {  // a whole block has no older sources: its cos scores stand in for f
+            uint32_t r[2][32];
+            tmem_ld32(cs, r[0]);
+            tmem_ld32(h < 0 ? cs : cs + 64, r[1]);
+            tmem_ld_wait();
+            weights32<2>(r[0], r[1], c, js, i, h < 0 ? -0x7fffffff - 1 : i - W + 1, p, dsum2);
+          }
+          __nv_bfloat16* dst = prow + (ib - jb) * kBlk + off;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) st_global_v4(dst + 2 * e, p[e], p[e + 1], p[e + 2], p[e + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b.slot_free[slot]);
+      }
+    }
+    // den = row sums of the weights as applied + older prefix + null term
+    float d0, d1, d2, d3;
+    f32x2_unpack(dsum2[0], d0, d1);
+    f32x2_unpack(dsum2[1], d2, d3);
+    b.rowsum[wg][row] = (d0 + d1) + (d2 + d3);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&b.rs_full);
+    if (ok && wg == 0 && (ok = wait_bar(&b.rs_full, 0, b, a))) {
+      float den = 1.f;  // rows past T: any finite value
+      if (i < a.T) {
+        const float null_w = a.null_bias ? exp2f((a.null_bias[head] - tau) * kLog2e) : 0.f;
+        den = b.rowsum[0][row] + b.rowsum[1][row] + a.den_old[((size_t)bb * a.H + head) * a.T + i] +
+              (float)(i + 1) * null_w;
+      }
+      a.den[(size_t)(bb * a.H + head) * a.T_pad + i] = den;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ================================================================= gate-strip kernel
+
+constexpr int kGThreads = 256;  // warp 0 TMA, warp 1 MMA (and TMEM), warps 4-7 epilogue
+constexpr int kEpiWarp0 = 4;
+constexpr int kStages = 4;                                 // P/G ring, half a source block each
+constexpr uint32_t kPBox = kBlk * 64 * 2;                  // 16 KB: 128 destinations x 64 sources
+constexpr uint32_t kStageBytes = kPBox + 2 * kGBox;        // + G of 64 sources x 128 columns
+constexpr uint32_t kColO = 0, kColSt = 256;                // O double buffer [0, 256); S^T
+
+struct __align__(8) GBars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t fk_full, fk_empty;  // Fk of a leaving block
+  uint64_t fq_full, fq_empty;  // Fq of the destination block (the read-out)
+  uint64_t o_full[2], o_empty[2];
+  uint64_t sb_full;            // bf16 state copy in place for the next read-out
+  uint64_t drain, never;
+  uint32_t tmem_base;
+  int abort;
+};
+// smem: stages | Fk | Fq | S_bf16 | U staging | Bars
+constexpr size_t kGSmemBytes = 1024 + kStages * kStageBytes + 3 * kTile + kGStage + sizeof(GBars);
+static_assert(kGSmemBytes <= 232448, "shared memory budget");
+
+struct GArgs {
+  int B, T, T_pad, H, dqk, m, d_h, m_h, W;
+  int n_iblk, n_ntile, n_strips;
+  int nseg, seg_len, n_items;  // each strip's destination blocks in nseg segments
+  float* seg_state;            // [n_strips, nseg - 1, kNg, d_h] f32 state at segment ends
+  int* seg_flag;               // [n_strips, nseg - 1], 0 until that state is written
+  const float* den;            // [B * H, T_pad]
+  const __nv_bfloat16* v;      // may be NULL (then u = gbar)
+  __nv_bfloat16* out;
+  unsigned* err;
+  uint64_t timeout_ns;
+  int debug_timeout;
+};
+
+struct Strip {
+  int b, head, n0;
+};
+// A work item: destination blocks [ib0, ib1) of one strip, segment `seg` of nseg.
+// Items are numbered segment-major, so every strip's segment k comes before any
+// segment k + 1.  A segment that ends with a non-empty state hands it (f32) to the
+// next segment through global memory and a per-strip flag.
+struct Item {
+  int st, seg, ib0, ib1;
+};
+template <bool kSeg>
+__device__ __forceinline__ Item item_of(const GArgs& a, int w) {
+  Item it;
+  if (kSeg) {
+    it.seg = w / a.n_strips;
+    it.st = w % a.n_strips;
+    it.ib0 = it.seg * a.seg_len;
+    it.ib1 = min(a.n_iblk, it.ib0 + a.seg_len);
+  } else {  // one segment per strip
+    it.seg = 0;
+    it.st = w;
+    it.ib0 = 0;
+    it.ib1 = a.n_iblk;
+  }
+  return it;
+}
+__device__ __forceinline__ Strip strip_of(const GArgs& a, int s) {
+  Strip r;
+  r.n0 = (s % a.n_ntile) * kNg;
+  r.head = (s / a.n_ntile) % a.H;
+  r.b = s / (a.n_ntile * a.H);
+  return r;
+}
+
+// Waits, bounded, until another CTA of this launch sets *flag (acquire).
+__device__ __forceinline__ bool wait_flag(const int* flag, const GArgs& a) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(flag) == 0) {
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      record_error(a.err, kErrTimeout | kKernWango);
+      return false;
+    }
+  }
+  return true;
 }
 
 // Segment handoff, run once per work item (kept out of line: the hot loops stay small).
@@ -233,7 +456,7 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
 // Called by all four epilogue warps; returns false (for all of them) if the wait for
 // the previous segment timed out.
 template <int DH>
-__device__ __noinline__ bool import_state(const Args& a, size_t slot, uint32_t t_st, uint32_t s_sb, int row,
+__device__ __noinline__ bool import_state(const GArgs& a, size_t slot, uint32_t t_st, uint32_t s_sb, int row,
                                           uint64_t* sb_full, int lane, bool issuer) {
   constexpr int RB = DH * 2;
   bool ok = true;
@@ -268,7 +491,7 @@ __device__ __noinline__ bool import_state(const Args& a, size_t slot, uint32_t t
 // This segment's final state (one thread's gate column, TMEM at t_st) to global
 // memory, then the flag for the next segment.  Called by all four epilogue warps.
 template <int DH>
-__device__ __noinline__ void export_state(const Args& a, size_t slot, uint32_t t_st, int row, bool issuer) {
+__device__ __noinline__ void export_state(const GArgs& a, size_t slot, uint32_t t_st, int row, bool issuer) {
   float* dst = a.seg_state + (slot * kNg + row) * DH;
   tc_fence_after();
 #pragma unroll 1
@@ -285,59 +508,49 @@ __device__ __noinline__ void export_state(const Args& a, size_t slot, uint32_t t
   if (issuer) st_release_gpu(&a.seg_flag[slot], 1);
 }
 
+// Position, among a destination block's source blocks (newest first), after which the
+// read-out of the older state is issued: the second block when there is one, so the
+// bf16 state copy of the previous block's epilogue has time to arrive.
+__device__ __forceinline__ int readout_pos(int ib, int W) { return ib - jlo_of(ib, W) >= 1 ? 1 : 0; }
+
+// Roles: warp 0 TMA (Fq of the destination block, Fk of leaving blocks, and the ring
+// of P/G stages, half a source block each); warp 1 one thread issuing the MMAs; warps
+// 4-7 the epilogue (one destination row per thread).
 template <int DH, bool kSeg>
-__global__ void __launch_bounds__(kThreads, 1)
-    wango_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
-                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmU, const Args a) {
-  constexpr int RB = DH * 2;  // bytes per row of the q/k/feature tiles
+__global__ void __launch_bounds__(kGThreads, 1)
+    wango_g_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmG,
+                   const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
+                   const __grid_constant__ CUtensorMap tmU, const GArgs a) {
+  constexpr int RB = DH * 2;
   constexpr uint32_t lay = DH == 64 ? kSwizzle128B : DH == 32 ? kSwizzle64B : kSwizzle32B;
   constexpr uint32_t sbo = 8u * RB;
   constexpr uint32_t tile_bytes = kBlk * RB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;                  // qhat
-  uint8_t* sFQ = sQ + kTile;           // Fq
-  uint8_t* sK = sFQ + kTile;           // khat ring, kKStages tiles
-  uint8_t* sFK = sK + kKStages * kTile;
-  uint8_t* sSB = sFK + kTile;          // bf16 state, [128 gate rows x d_h]
-  uint8_t* sG = sSB + kTile;           // G ring
-  uint8_t* sV = sG + kGStages * kGStage;  // two v / u tiles
-  Bars& b = *reinterpret_cast<Bars*>(sV + 2 * kGStage);
+  uint8_t* sS = base;                          // P/G stages
+  uint8_t* sFK = sS + kStages * kStageBytes;
+  uint8_t* sFQ = sFK + kTile;
+  uint8_t* sSB = sFQ + kTile;                  // bf16 state, [128 gate rows x d_h]
+  uint8_t* sU = sSB + kTile;                   // u staging for the TMA store
+  GBars& b = *reinterpret_cast<GBars*>(sU + kGStage);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int W = a.W;
 
   if (threadIdx.x == 0) {
-    mbar_init(&b.qh_full, 1);
-    mbar_init(&b.qh_empty, 1);
-    mbar_init(&b.fq_full, 1);
-    mbar_init(&b.fq_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&b.s_full[s], 1);
-      mbar_init(&b.p_full[s], 8);
-      mbar_init(&b.slot_free[s], 1);
-      mbar_init(&b.v_full[s], 1);
-      mbar_init(&b.v_empty[s], 1);
-    }
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&b.k_full[s], 1);
-      mbar_init(&b.k_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&b.full[s], 1);
+      mbar_init(&b.empty[s], 1);
     }
     mbar_init(&b.fk_full, 1);
     mbar_init(&b.fk_empty, 1);
-    for (int s = 0; s < kGStages; ++s) {
-      mbar_init(&b.g_full[s], 1);
-      mbar_init(&b.g_empty[s], 1);
-    }
-    mbar_init(&b.o_full, 1);
-    mbar_init(&b.o_empty, 4);
-    mbar_init(&b.st_full, 1);
-    mbar_init(&b.sb_full, 4);
+    mbar_init(&b.fq_full, 1);
+    mbar_init(&b.fq_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&b.drain[s], 1);
+      mbar_init(&b.o_full[s], 1);
+      mbar_init(&b.o_empty[s], 4);
     }
-    mbar_init(&b.den_full, 8);
-    mbar_init(&b.den_empty, 4);
+    mbar_init(&b.sb_full, 4);
+    mbar_init(&b.drain, 1);
     mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
@@ -351,331 +564,142 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = b.tmem_base;
-  const int W = a.W;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
-    // Order per destination block: qhat; then, newest source block first, khat, Fq
-    // (before the first mixed block, else after the sources), Fk (mixed blocks), G;
-    // then the block's v.
-    Ring kr, gr;
+    Ring sr;
     bool ok = true;
-    uint32_t kmask = 0, gmask = 0, kph[kKStages] = {}, gph[kGStages] = {}, vmask = 0, vph[2] = {};
-    uint32_t fkph = 0;                               // phase of the Fk buffer
-    uint32_t qh_n = 0, fq_n = 0, fk_n = 0;             // loads issued
-    int dc = 0;  // destination blocks begun
-    auto tile128 = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int bb) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) tma_load_3d(dst + h * 2 * kGBox + c * kGBox, map, bar, x + 64 * c, y + 64 * h, bb);
-    };
+    uint32_t smask = 0, sph[kStages] = {}, fkph = 0, fq_n = 0, fk_n = 0;
+    int dc = 0;
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
       const Strip sp = strip_of(a, it.st);
-      const int gx = sp.head * a.m_h + sp.n0;
+      const int gx = sp.head * a.m_h + sp.n0, pz = sp.b * a.H + sp.head;
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
-        const uint32_t dp = dc & 1;
-        if (!(ok = wait_bar(&b.qh_empty, dp ^ 1, b, a))) break;
-        mbar_arrive_expect_tx(&b.qh_full, tile_bytes);
-        tma_load_3d(sQ, &tmQ, &b.qh_full, sp.head * DH, ib * kBlk, sp.b);
-        ++qh_n;
-        bool fq_loaded = false;
-        auto load_fq = [&]() -> bool {
-          if (!wait_bar(&b.fq_empty, dp ^ 1, b, a)) return false;
-          mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
-          tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
-          ++fq_n;
-          fq_loaded = true;
-          return true;
-        };
+        if (!(ok = wait_bar(&b.fq_empty, (dc & 1) ^ 1, b, a))) break;
+        mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
+        tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
+        ++fq_n;
         for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
-          if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
-          mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
-          tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], sp.head * DH, jb * kBlk, sp.b);
-          kmask |= 1u << kr.stage;
-          kph[kr.stage] = kr.phase;
-          kr.next(kKStages);
-          if (is_mixed(jb, ib, W)) {
-            if (!fq_loaded && !(ok = load_fq())) break;
+          if (is_leaving(jb, ib, W)) {
             if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
             mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
             tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
-            ++fk_n;
             fkph ^= 1;
+            ++fk_n;
           }
-          if (!(ok = wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a))) break;
-          mbar_arrive_expect_tx(&b.g_full[gr.stage], kGStage);
-          tile128(sG + gr.stage * kGStage, &tmG, &b.g_full[gr.stage], gx, jb * kBlk, sp.b);
-          gmask |= 1u << gr.stage;
-          gph[gr.stage] = gr.phase;
-          gr.next(kGStages);
-        }
-        if (!ok) break;
-        if (!fq_loaded && !(ok = load_fq())) break;
-        const int vb = dc & 1;
-        const uint32_t vp = (dc >> 1) & 1;
-        if (!(ok = wait_bar(&b.v_empty[vb], vp ^ 1, b, a))) break;
-        if (a.has_v) {
-          mbar_arrive_expect_tx(&b.v_full[vb], kGStage);
-          tile128(sV + vb * kGStage, &tmV, &b.v_full[vb], gx, ib * kBlk, sp.b);
-          vmask |= 1u << vb;
-          vph[vb] = vp;
-        } else {
-          mbar_arrive(&b.v_full[vb]);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!(ok = wait_bar(&b.empty[sr.stage], sr.phase ^ 1, b, a))) break;
+            uint8_t* st = sS + sr.stage * kStageBytes;
+            mbar_arrive_expect_tx(&b.full[sr.stage], kStageBytes);
+            tma_load_3d(st, &tmP, &b.full[sr.stage], (ib - jb) * kBlk + 64 * hh, ib * kBlk, pz);
+            tma_load_3d(st + kPBox, &tmG, &b.full[sr.stage], gx, jb * kBlk + 64 * hh, sp.b);
+            tma_load_3d(st + kPBox + kGBox, &tmG, &b.full[sr.stage], gx + 64, jb * kBlk + 64 * hh, sp.b);
+            smask |= 1u << sr.stage;
+            sph[sr.stage] = sr.phase;
+            sr.next(kStages);
+          }
         }
       }
     }
     // no copy may be in flight when the CTA exits
-    if (qh_n) mbar_wait(&b.qh_full, (qh_n - 1) & 1, a.timeout_ns);
     if (fq_n) mbar_wait(&b.fq_full, (fq_n - 1) & 1, a.timeout_ns);
     if (fk_n) mbar_wait(&b.fk_full, (fk_n - 1) & 1, a.timeout_ns);
-    for (int s = 0; s < kKStages; ++s)
-      if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
-    for (int s = 0; s < kGStages; ++s)
-      if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
-    for (int s = 0; s < 2; ++s)
-      if (vmask & (1u << s)) mbar_wait(&b.v_full[s], vph[s], a.timeout_ns);
+    for (int s = 0; s < kStages; ++s)
+      if (smask & (1u << s)) mbar_wait(&b.full[s], sph[s], a.timeout_ns);
   } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issue: scores
-    // Units in order; unit u's scores go into slot u & 1 once the P.G and row sums of
-    // unit u - 2 (the slot's previous user) have completed.
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);  // 128 sources
-    constexpr uint32_t idesc_h = idesc_bf16_f32(kBlk, 64, false, false);    // 64 sources
-    const uint64_t qd = smem_desc(smem_u32(sQ), 16, sbo, lay);
-    const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
-    const uint64_t kd0 = smem_desc(smem_u32(sK), 16, sbo, lay);
-    const uint64_t fkd = smem_desc(smem_u32(sFK), 16, sbo, lay);
-    bool ok = true;
-    Ring ks;
-    uint32_t u = 0, fkph = 0;
-    int dc = 0;
-    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
-      const Item it = item_of<kSeg>(a, w);
-      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
-        const int jlo = jlo_of(ib, W);
-        for (int jb = ib; ok && jb >= jlo; --jb) {
-          const bool mixed = is_mixed(jb, ib, W);
-          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
-            if (u >= 2 && !(ok = wait_bar(&b.slot_free[u & 1], ((u - 2) >> 1) & 1, b, a))) break;
-            if (!(ok = wait_bar(&b.qh_full, dc & 1, b, a))) break;
-            if (!(ok = wait_bar(&b.k_full[ks.stage], ks.phase, b, a))) break;
-            if (h >= 0 && !(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
-            if (h >= 0 && !(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
-            tc_fence_after_nc();
-            const uint64_t kd = kd0 + (uint64_t)((ks.stage * kTile) >> 4);
-            const uint32_t sc = tmem + kColSlot0 + (u & 1) * 128;
-            if (h < 0) {
-#pragma unroll
-              for (int kk = 0; kk < DH / 16; ++kk)
-                mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
-            } else {
-              // cos scores of the half's 64 sources in columns [0, 64), feature-map
-              // scores in [64, 128)
-              const uint64_t hoff = (uint64_t)((h * 64 * RB) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < DH / 16; ++kk)
-                mma_bf16_ss_nc(sc, qd + (uint64_t)(kk * 2), kd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
-#pragma unroll
-              for (int kk = 0; kk < DH / 16; ++kk)
-                mma_bf16_ss_nc(sc + 64, fqd + (uint64_t)(kk * 2), fkd + hoff + (uint64_t)(kk * 2), idesc_h, kk != 0);
-            }
-            mma_commit_nc(&b.s_full[u & 1]);
-            ++u;
-            if (h != 0) {  // the block's last unit releases its khat
-              mma_commit_nc(&b.k_empty[ks.stage]);
-              ks.next(kKStages);
-            }
-            if (h == 1) fkph ^= 1;
-          }
-        }
-        if (ok) mma_commit_nc(&b.qh_empty);
-      }
-    }
-    mma_commit(&b.drain[0]);
-    mbar_wait(&b.drain[0], 0, a.timeout_ns);
-  } else if (warp == 2 && lane == 0) {
-    // ------------------------------------------------------------ MMA issue: P.G, state
+    // ------------------------------------------------------------ MMA issue
     constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);   // O += P G
     constexpr uint32_t idesc_r = idesc_bf16_f32(kBlk, kNg, false, false);  // O += Fq S
     constexpr uint32_t idesc_u = idesc_bf16_f32(kBlk, DH, true, true);     // S^T += G^T Fk
     const uint64_t fqd = smem_desc(smem_u32(sFQ), 16, sbo, lay);
     const uint64_t fkmn = smem_desc(smem_u32(sFK), tile_bytes, sbo, lay);  // Fk as MN-major B
     const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
-    const uint64_t gd0 = smem_desc(smem_u32(sG), kGBox, 1024, kSwizzle128B);
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
-    Ring gr;
-    uint32_t u = 0, oph = 0, sbph = 0;
+    Ring sr;
+    uint32_t sbph = 0, fkph = 0;
     int dc = 0;
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
       // a later segment starts from the state its predecessor handed over
       bool first_update = !(kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0);
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
-        const int jlo = jlo_of(ib, W);
-        bool copy_ready = false;
-        for (int jb = ib; ok && jb >= jlo; --jb) {
-          const bool mixed = is_mixed(jb, ib, W), leaving = is_leaving(jb, ib, W);
-          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
-            // O (+)= P G; the first unit overwrites O once the epilogue has read the
-            // previous destination block's accumulator.
-            if (!(ok = wait_bar(&b.p_full[u & 1], (u >> 1) & 1, b, a))) break;
-            const bool first = jb == ib && h <= 0;
-            if (first) {
-              if (!(ok = wait_bar(&b.o_empty, oph ^ 1, b, a))) break;
-              oph ^= 1;
+        const int ob = dc & 1;
+        if (!(ok = wait_bar(&b.o_empty[ob], ((dc >> 1) & 1) ^ 1, b, a))) break;
+        tc_fence_after_nc();
+        const uint32_t od = tmem + kColO + (uint32_t)(ob * kNg);
+        const int rpos = readout_pos(ib, W);
+        bool copy_ready = false, first = true;
+        int idx = 0;
+        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb, ++idx) {
+          const bool leaving = is_leaving(jb, ib, W);
+          if (leaving) {  // the read-out copy of the state must be taken before it changes
+            if (!copy_ready) {
+              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+              sbph ^= 1;
+              copy_ready = true;
             }
-            if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
+            if (!(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
+          }
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!(ok = wait_bar(&b.full[sr.stage], sr.phase, b, a))) break;
             tc_fence_after_nc();
-            const uint32_t ptm = tmem + kColSlot0 + (u & 1) * 128;
-            const uint64_t gd = gd0 + (uint64_t)((gr.stage * kGStage) >> 4);
-            // 16-source steps of the block: all 8, or the 4 of half h
-            if (h < 0) {
+            const uint32_t saddr = smem_u32(sS + sr.stage * kStageBytes);
+            const uint64_t pd = smem_desc(saddr, 16, 1024, kSwizzle128B);           // P, K-major
+            const uint64_t gd = smem_desc(saddr + kPBox, kGBox, 1024, kSwizzle128B);  // G, MN-major
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t goff = (uint32_t)((kk >> 2) * 2 * kGBox + (kk & 3) * 2048);
-                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gd + (uint64_t)(goff >> 4), idesc_o,
-                               (first && kk == 0) ? 0u : 1u);
-              }
-            } else {
-              const uint64_t gh = gd + (uint64_t)((h * 2 * kGBox) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ts_nc(tmem + kColO, ptm + p_col(kk, h), gh + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                               (first && kk == 0) ? 0u : 1u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss_nc(od, pd + (uint64_t)(kk * 2), gd + (uint64_t)(kk * 128), idesc_o,
+                             (first && kk == 0) ? 0u : 1u);
+            first = false;
             if (leaving) {
-              // S^T += G^T Fk over this unit's sources, once the read-out copy of the
-              // previous state is taken (a leaving block is always mixed: h >= 0)
-              if (!copy_ready) {
-                if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-                sbph ^= 1;
-                copy_ready = true;
-                tc_fence_after_nc();
-              }
-              const uint64_t gh = gd + (uint64_t)((h * 2 * kGBox) >> 4);
-              const uint64_t fh = fkmn + (uint64_t)((h * 64 * RB) >> 4);
+              const uint64_t fh = fkmn + (uint64_t)((64 * hh * RB) >> 4);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss_nc(tmem + kColSt, gh + (uint64_t)((kk * 2048) >> 4), fh + (uint64_t)((kk * 16 * RB) >> 4),
+                mma_bf16_ss_nc(tmem + kColSt, gd + (uint64_t)(kk * 128), fh + (uint64_t)((kk * 16 * RB) >> 4),
                                idesc_u, (first_update && kk == 0) ? 0u : 1u);
               first_update = false;
             }
-            mma_commit_nc(&b.slot_free[u & 1]);
-            ++u;
-            if (h != 0) {  // the block's last unit releases its G and Fk
-              mma_commit_nc(&b.g_empty[gr.stage]);
-              gr.next(kGStages);
-              if (h == 1) mma_commit_nc(&b.fk_empty);
+            mma_commit_nc(&b.empty[sr.stage]);
+            sr.next(kStages);
+          }
+          if (!ok) break;
+          if (leaving) {
+            mma_commit_nc(&b.fk_empty);
+            fkph ^= 1;
+          }
+          if (idx == rpos) {  // read-out of the state before this block: O += Fq S_bf16
+            if (!copy_ready) {
+              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+              sbph ^= 1;
+              copy_ready = true;
             }
+            if (!(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
+            tc_fence_after_nc();
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk)
+              mma_bf16_ss_nc(od, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, 1u);
+            mma_commit_nc(&b.fq_empty);
           }
         }
         if (!ok) break;
-        // read-out of the state before this block: O += Fq S_bf16
-        if (!copy_ready) {
-          if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-          sbph ^= 1;
-        }
-        if (!(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
-        tc_fence_after_nc();
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk)
-          mma_bf16_ss_nc(tmem + kColO, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, 1u);
-        mma_commit_nc(&b.fq_empty);
-        mma_commit_nc(&b.st_full);
-        mma_commit_nc(&b.o_full);
+        mma_commit_nc(&b.o_full[ob]);  // also: this block's updates and read-out are complete
       }
     }
-    mma_commit(&b.drain[1]);
-    mbar_wait(&b.drain[1], 0, a.timeout_ns);
-  } else if (warp >= kSoftWarp0 && warp < kEpiWarp0) {
-    // ------------------------------------------------------------ weights
-    const int wg = (warp - kSoftWarp0) / 4;  // sources [64 wg, 64 wg + 64) of each block
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    bool ok = true;
-    uint32_t unit = 0;  // units processed
-    int gib = 0;        // destination blocks processed
-    for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
-      const Item it = item_of<kSeg>(a, w);
-      const Strip sp = strip_of(a, it.st);
-      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
-      const float c = tau * kLog2e;
-      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++gib) {
-        const int i = ib * kBlk + row;
-        uint64_t dsum2[2] = {0, 0};  // this row's sum of the weights over this warpgroup's sources
-        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
-          const bool mixed = is_mixed(jb, ib, W);
-          for (int h = mixed ? 0 : -1; h <= (mixed ? 1 : -1); ++h) {
-            const uint32_t n = unit++;
-            const uint32_t sl = tmem + kColSlot0 + (n & 1) * 128 + lane_off;
-            if (!(ok = wait_bar(&b.s_full[n & 1], (n >> 1) & 1, b, a))) break;
-            tc_fence_after();
-            // P (bf16 pairs) over this warpgroup's own cos columns, so the two
-            // warpgroups need not wait for each other.  One 32-source chunk at a time (a
-            // rolled loop with one copy of each weight form keeps the code small): two per
-            // warpgroup for a whole block, one for a half of a mixed block, whose
-            // feature-map scores sit 64 columns after the cos scores.  Each chunk is
-            // classified for this warp's 32 rows: after every row (zero weights), inside
-            // every row's window (exp only) or general.
-            const int nq = h < 0 ? 2 : 1;
-            const int i0 = ib * kBlk + quarter * 32;
-#pragma unroll 1
-            for (int q = 0; q < nq; ++q) {
-              const int off = h < 0 ? wg * 64 + q * 32 : h * 64 + wg * 32;  // first source in the block
-              const uint32_t cs = sl + (uint32_t)(h < 0 ? off : wg * 32);     // its cos score column
-              const uint32_t pc = sl + (uint32_t)(h < 0 ? wg * 64 + q * 16 : wg * 32);
-              const int js = jb * kBlk + off;
-              uint32_t p[16];
-              if (js > i0 + 31) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) p[e] = 0u;
-              } else if (js + 31 <= i0 && js >= i0 + 32 - W) {
-                uint32_t rq[32];
-                tmem_ld32(cs, rq);
-                tmem_ld_wait();
-                weights32<0>(rq, rq, c, js, i, 0, p, dsum2);
-              } else {  // a whole block has no older sources: its cos scores stand in for f
-                uint32_t r[2][32];
-                tmem_ld32(cs, r[0]);
-                tmem_ld32(h < 0 ? cs : cs + 64, r[1]);
-                tmem_ld_wait();
-                weights32<2>(r[0], r[1], c, js, i, h < 0 ? -0x7fffffff - 1 : i - W + 1, p, dsum2);
-              }
-              tmem_st16(pc, p);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&b.p_full[n & 1]);
-          }
-        }
-        if (!ok) break;
-        // the row sums of this destination block -> epilogue
-        if (!(ok = wait_bar(&b.den_empty, (gib & 1) ^ 1, b, a))) break;
-        float d0, d1, d2, d3;
-        f32x2_unpack(dsum2[0], d0, d1);
-        f32x2_unpack(dsum2[1], d2, d3);
-        b.rowsum[wg][row] = (d0 + d1) + (d2 + d3);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b.den_full);
-      }
-    }
-  } else if (warp >= kEpiWarp0) {
+    mma_commit(&b.drain);
+    mbar_wait(&b.drain, 0, a.timeout_ns);
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue + state copy
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // destination row; also the gate column of S^T
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool issuer = (warp == kEpiWarp0 && lane == 0);
     bool ok = true;
-    uint32_t oph = 0, stph = 0;
     int gib = 0;
     // bf16 copy of the state for a destination block's read-out (zero while no source
     // has left the window)
     auto copy_state = [&](bool empty) {
-      if (!empty) tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < DH; c0 += 16) {
         uint32_t t16[16];
@@ -704,8 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_of<kSeg>(a, w);
       if (it.ib0 >= it.ib1) continue;
       const Strip sp = strip_of(a, it.st);
-
-      const float tau = head_tau(a.tau, a.s, sp.head, a.err, kKernWango);
       // the state before the first destination block: empty, or the previous
       // segment's (into TMEM for the updates, bf16 into shared memory for the read-out)
       if (kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0) {
@@ -715,26 +737,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         copy_state(true);
       }
-      const float null_w = a.null_bias ? exp2f((a.null_bias[sp.head] - tau) * kLog2e) : 0.f;
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++gib) {
+        const int ob = gib & 1;
         const int i = ib * kBlk + row;
         const bool row_ok = i < a.T;
-        const int sv = gib & 1;  // v tile buffer
-        const uint32_t pv = (gib >> 1) & 1;
-        // older-prefix denominator, fetched before the waits
-        float den = row_ok ? a.den_old[((size_t)sp.b * a.H + sp.head) * a.T + i] : 0.f;
-        den += (float)(i + 1) * null_w;
-        if (ok) ok = wait_bar(&b.den_full, gib & 1, b, a);
-        if (ok) {
-          den += b.rowsum[0][row] + b.rowsum[1][row];  // this block's per-pair weights, as applied
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b.den_empty);
+        // before the wait: the denominator and this row's 128 columns of v
+        const float den = a.den[(size_t)(sp.b * a.H + sp.head) * a.T_pad + i];
+        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
+        uint4 vv[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int col = sp.n0 + 8 * k;
+          vv[k] = (a.v && row_ok && col < a.m_h) ? ld_global_v4(a.v + grow + col) : make_uint4(0, 0, 0, 0);
         }
-        if (ok) ok = wait_bar(&b.o_full, oph, b, a);
+        if (ok) ok = wait_bar(&b.o_full[ob], (gib >> 1) & 1, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
-        oph ^= 1;
         tc_fence_after();
+        // the state after this block, for the next block's read-out (this block's
+        // updates and read-out are complete; the next block updates it only after)
+        if (ib + 1 < it.ib1) copy_state(jlo_of(ib + 1, W) == 0);
         const float inv = 1.f / den;
         // gbar = O / den, rounded to bf16, in registers; the accumulator is released as
         // soon as it has been read
@@ -742,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kNg; c0 += 32) {
           uint32_t o[32];
-          tmem_ld32(tmem + kColO + lane_off + c0, o);
+          tmem_ld32(tmem + kColO + (uint32_t)(ob * kNg) + lane_off + c0, o);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
@@ -750,43 +772,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&b.o_empty);
-        if (ok) ok = wait_bar(&b.st_full, stph, b, a);
-        if (ok) ok = wait_bar(&b.v_full[sv], pv, b, a);
-        ok = named_bar_and(2, 128, ok);
-        if (!ok) break;
-        stph ^= 1;
-        // u = gbar * v, written over v in shared memory (the TMA store's source)
-        const uint32_t vst = smem_u32(sV + sv * kGStage);
+        if (lane == 0) mbar_arrive(&b.o_empty[ob]);
+        // u = gbar * v into the staging tile (once the previous store has read it)
+        if (issuer) bulk_wait_group_read0();
+        named_bar_sync(2, 128);
         const int rh = row >> 6, rr = row & 63;
-        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
 #pragma unroll
         for (int cq = 0; cq < 2; ++cq) {
           const int col0 = sp.n0 + cq * 64;
           const bool straddle = col0 < a.m_h && col0 + 64 > a.m_h;
-          const uint32_t box = vst + rh * 2 * kGBox + cq * kGBox + rr * 128;
+          const uint32_t box = smem_u32(sU) + rh * 2 * kGBox + cq * kGBox + rr * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
             const uint32_t* g4 = &gb[cq * 32 + k * 4];
+            const uint4 v4 = vv[cq * 8 + k];
             uint32_t u[4];
-            if (a.has_v) {
-              const uint4 vv = ld_shared_v4(addr);
-              u[0] = mul_bf16x2(g4[0], vv.x);
-              u[1] = mul_bf16x2(g4[1], vv.y);
-              u[2] = mul_bf16x2(g4[2], vv.z);
-              u[3] = mul_bf16x2(g4[3], vv.w);
+            if (a.v) {
+              u[0] = mul_bf16x2(g4[0], v4.x);
+              u[1] = mul_bf16x2(g4[1], v4.y);
+              u[2] = mul_bf16x2(g4[2], v4.z);
+              u[3] = mul_bf16x2(g4[3], v4.w);
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e) u[e] = g4[e];
             }
-            if (!straddle) st_shared_v4(addr, make_uint4(u[0], u[1], u[2], u[3]));
+            if (!straddle) st_shared_v4(box + (uint32_t)((k ^ (rr & 7)) << 4), make_uint4(u[0], u[1], u[2], u[3]));
             else if (row_ok && col0 + 8 * k < a.m_h) st_global_v4(a.out + grow + col0 + 8 * k, u[0], u[1], u[2], u[3]);
           }
         }
-        // the state copy for the next destination block (this block's updates and
-        // read-out are complete; the next block updates the state only after it)
-        if (ib + 1 < it.ib1) copy_state(jlo_of(ib + 1, W) == 0);
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
         if (issuer) {
@@ -796,19 +809,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cq = 0; cq < 2; ++cq) {
               const int col0 = sp.n0 + cq * 64;
               if (col0 + 64 > a.m_h) continue;
-              tma_store_3d(&tmU, sV + sv * kGStage + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
+              tma_store_3d(&tmU, sU + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
             }
           }
           bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&b.v_empty[sv]);
         }
       }
       // hand this segment's final state to the next segment of the strip (the last
-      // block's updates are complete: its st_full was waited for above)
+      // block's updates are complete: its o_full was waited for above)
       if (kSeg && ok && it.seg + 1 < a.nseg && jlo_of(it.ib1, W) > 0)
         export_state<DH>(a, (size_t)it.st * (a.nseg - 1) + it.seg, tmem + kColSt + lane_off, row, issuer);
     }
+    if (issuer) bulk_wait_group0();  // every store has completed
   }
   tc_fence_before();
   __syncthreads();
@@ -817,7 +829,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
-
 // ---------------------------------------------------------------- pre-pass
 
 // Feature map of eq. 8 (mode 0) or plain ELU + 1 (mode 1).  For u <= 0,
@@ -946,25 +957,58 @@ int choose_nseg(long long strips, int n_iblk, int W, int sms) {
   return best;
 }
 
+// Source blocks per destination block at most: the width of P in 128-source blocks.
+int max_sources(int n_iblk, int W) {
+  int n = 1;
+  for (int ib = 0; ib < n_iblk; ++ib) n = std::max(n, ib - jlo_of(ib, W) + 1);
+  return n;
+}
+
 struct AuxLayout {
-  size_t fq, fk, zb, den, seg, flag, total;
-  int nseg;
+  size_t fq, fk, zb, den_old, P, den, seg, flag, total;
+  int nseg, T_pad, ldp;
 };
 AuxLayout aux_layout(int B, int T, int H, int dqk, int m, int W) {
-  const size_t BT = (size_t)B * T, nI = (size_t)(T + kBlk - 1) / kBlk;
+  const size_t BT = (size_t)B * T;
+  const int nI = (T + kBlk - 1) / kBlk;
   const int d_h = dqk / H;
   const long long strips = (long long)B * H * ((m / H + kNg - 1) / kNg);
   AuxLayout L;
-  L.nseg = choose_nseg(strips, (int)nI, W, num_sms());
+  L.T_pad = nI * kBlk;
+  L.ldp = max_sources(nI, W) * kBlk;
+  L.nseg = choose_nseg(strips, nI, W, num_sms());
   const size_t handoffs = (size_t)strips * (L.nseg - 1);
   L.fq = 0;
   L.fk = L.fq + a256(BT * dqk * 2);
   L.zb = L.fk + a256(BT * dqk * 2);
-  L.den = L.zb + a256((size_t)B * H * nI * d_h * 4);
-  L.seg = L.den + a256((size_t)B * H * T * 4);
+  L.den_old = L.zb + a256((size_t)B * H * nI * d_h * 4);
+  L.P = L.den_old + a256((size_t)B * H * T * 4);
+  L.den = L.P + a256((size_t)B * H * L.T_pad * L.ldp * 2);
+  L.seg = L.den + a256((size_t)B * H * L.T_pad * 4);
   L.flag = L.seg + a256(handoffs * kNg * d_h * 4);
   L.total = L.flag + a256(handoffs * 4);
   return L;
+}
+
+template <int DH>
+cudaError_t launch_p(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mfq, const CUtensorMap& mfk,
+                     const PArgs& a, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(wango_p_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kPSmemBytes);
+  if (e != cudaSuccess) return e;
+  wango_p_kernel<DH><<<dim3(a.n_iblk, a.H, a.B), kPThreads, kPSmemBytes, s>>>(mq, mk, mfq, mfk, a);
+  return cudaGetLastError();
+}
+
+template <int DH>
+cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtensorMap& mfq, const CUtensorMap& mfk,
+                     const CUtensorMap& mu, const GArgs& a, cudaStream_t s) {
+  auto kern = a.nseg > 1 ? wango_g_kernel<DH, true> : wango_g_kernel<DH, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
+  kern<<<grid, kGThreads, kGSmemBytes, s>>>(mp, mg, mfq, mfk, mu, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -972,69 +1016,77 @@ AuxLayout aux_layout(int B, int T, int H, int dqk, int m, int W) {
 size_t wango_aux_bytes(int B, int T, int H, int dqk, int m, int W) { return aux_layout(B, T, H, dqk, m, W).total; }
 
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
-  Args a = {};
-  a.B = p.B; a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
-  a.d_h = p.dqk / p.H; a.m_h = p.m / p.H;
-  a.W = p.window;
-  a.n_iblk = ceil_div(p.T, kBlk);
-  a.n_ntile = ceil_div(a.m_h, kNg);
-  const long long strips = (long long)p.B * p.H * a.n_ntile;
-  if (strips > 0x7fffffffLL) return cudaErrorInvalidValue;
-  a.n_strips = (int)strips;
+  const int d_h = p.dqk / p.H, m_h = p.m / p.H;
+  const int n_iblk = ceil_div(p.T, kBlk);
   const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk, p.m, p.window);
-  a.nseg = L.nseg;
-  a.seg_len = ceil_div(a.n_iblk, a.nseg);
-  if (strips * a.nseg > 0x7fffffffLL) return cudaErrorInvalidValue;
-  a.n_items = a.n_strips * a.nseg;
-  a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
-  a.has_v = p.v != nullptr;
-  a.out = static_cast<__nv_bfloat16*>(p.out);
-  a.err = p.err;
-  a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
-  a.timeout_ns = a.debug_timeout ? 1000000ull : 2000000000ull;
-
-  // pre-pass: feature maps, block sums, older-prefix denominators
+  const bool debug = (p.flags & TG_FLAG_DEBUG_TIMEOUT) != 0;
+  const uint64_t timeout_ns = debug ? 1000000ull : 2000000000ull;
   char* aux = static_cast<char*>(p.aux);
-  a.seg_state = reinterpret_cast<float*>(aux + L.seg);
-  a.seg_flag = reinterpret_cast<int*>(aux + L.flag);
-  if (a.nseg > 1) {  // no segment's state is ready yet
-    const cudaError_t me = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
-    if (me != cudaSuccess) return me;
-  }
   __nv_bfloat16* fq = reinterpret_cast<__nv_bfloat16*>(aux + L.fq);
   __nv_bfloat16* fk = reinterpret_cast<__nv_bfloat16*>(aux + L.fk);
   float* zb = reinterpret_cast<float*>(aux + L.zb);
+  float* den_old = reinterpret_cast<float*>(aux + L.den_old);
+  __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(aux + L.P);
   float* den = reinterpret_cast<float*>(aux + L.den);
+
+  // pre-pass: feature maps, block sums, older-prefix denominators
   const long long rows = (long long)p.B * p.T;
   const long long work = rows * (p.dqk / 8);
   wango_phi_kernel<<<(unsigned)((work + 255) / 256), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, rows, p.H, p.dqk,
       p.s, p.tau, p.phi_mode, p.err);
-  dim3 g3(a.n_iblk, p.H, p.B);
-  wango_blocksum_kernel<<<g3, 256, 0, s>>>(fk, zb, p.T, p.H, p.dqk, a.n_iblk);
-  wango_denold_kernel<<<g3, kBlk, 0, s>>>(fq, zb, den, p.T, p.H, p.dqk, a.n_iblk, p.window);
+  dim3 g3(n_iblk, p.H, p.B);
+  wango_blocksum_kernel<<<g3, 256, 0, s>>>(fk, zb, p.T, p.H, p.dqk, n_iblk);
+  wango_denold_kernel<<<g3, kBlk, 0, s>>>(fq, zb, den_old, p.T, p.H, p.dqk, n_iblk, p.window);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  a.den_old = den;
 
-  CUtensorMap mq, mk, mfq, mfk, mg, mv, mu;
-  e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, a.d_h);
-  if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, a.d_h);
-  if (e == cudaSuccess) e = make_tmap_3d(&mfq, fq, p.B, p.T, p.dqk, kBlk, a.d_h);
-  if (e == cudaSuccess) e = make_tmap_3d(&mfk, fk, p.B, p.T, p.dqk, kBlk, a.d_h);
+  CUtensorMap mq, mk, mfq, mfk, mp, mg, mu;
+  e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mfq, fq, p.B, p.T, p.dqk, kBlk, d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mfk, fk, p.B, p.T, p.dqk, kBlk, d_h);
+  if (e == cudaSuccess) e = make_tmap_3d(&mp, P, (uint64_t)p.B * p.H, L.T_pad, L.ldp, kBlk, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
   if (e != cudaSuccess) return e;
-  auto kern = a.nseg > 1 ? (a.d_h == 64 ? wango_tc_kernel<64, true> : a.d_h == 32 ? wango_tc_kernel<32, true>
-                                                                                  : wango_tc_kernel<16, true>)
-                         : (a.d_h == 64 ? wango_tc_kernel<64, false> : a.d_h == 32 ? wango_tc_kernel<32, false>
-                                                                                   : wango_tc_kernel<16, false>);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+
+  // weights P and the denominators, once per destination block
+  PArgs pa = {};
+  pa.B = p.B; pa.T = p.T; pa.T_pad = L.T_pad; pa.H = p.H; pa.dqk = p.dqk; pa.d_h = d_h; pa.W = p.window;
+  pa.n_iblk = n_iblk; pa.ldp = L.ldp;
+  pa.s = p.s; pa.tau = p.tau; pa.null_bias = p.null_bias; pa.den_old = den_old;
+  pa.P = P; pa.den = den; pa.err = p.err; pa.timeout_ns = timeout_ns;
+  e = d_h == 64 ? launch_p<64>(mq, mk, mfq, mfk, pa, s)
+                : d_h == 32 ? launch_p<32>(mq, mk, mfq, mfk, pa, s) : launch_p<16>(mq, mk, mfq, mfk, pa, s);
   if (e != cudaSuccess) return e;
-  const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mfq, mfk, mg, mv, mu, a);
-  return cudaGetLastError();
+
+  // the gate strips
+  GArgs a = {};
+  a.B = p.B; a.T = p.T; a.T_pad = L.T_pad; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
+  a.d_h = d_h; a.m_h = m_h; a.W = p.window;
+  a.n_iblk = n_iblk;
+  a.n_ntile = ceil_div(m_h, kNg);
+  const long long strips = (long long)p.B * p.H * a.n_ntile;
+  if (strips * L.nseg > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.n_strips = (int)strips;
+  a.nseg = L.nseg;
+  a.seg_len = ceil_div(n_iblk, a.nseg);
+  a.n_items = a.n_strips * a.nseg;
+  a.seg_state = reinterpret_cast<float*>(aux + L.seg);
+  a.seg_flag = reinterpret_cast<int*>(aux + L.flag);
+  a.den = den;
+  a.v = static_cast<const __nv_bfloat16*>(p.v);
+  a.out = static_cast<__nv_bfloat16*>(p.out);
+  a.err = p.err;
+  a.debug_timeout = debug ? 1 : 0;
+  a.timeout_ns = timeout_ns;
+  if (a.nseg > 1) {  // no segment's state is ready yet
+    e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
+  return d_h == 64 ? launch_g<64>(mp, mg, mfq, mfk, mu, a, s)
+                   : d_h == 32 ? launch_g<32>(mp, mg, mfq, mfk, mu, a, s) : launch_g<16>(mp, mg, mfq, mfk, mu, a, s);
 }
 
 }  // namespace tg
