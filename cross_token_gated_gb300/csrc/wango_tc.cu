@@ -55,7 +55,6 @@ __host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
   return lo > 0 ? lo / kBlk : 0;
 }
 __device__ __forceinline__ bool is_mixed(int jb, int ib, int W) { return jb * kBlk <= ib * kBlk + kBlk - 1 - W; }
-__device__ __forceinline__ bool is_leaving(int jb, int ib, int W) { return jb < jlo_of(ib + 1, W); }
 
 struct Ring {
   int stage = 0;
@@ -371,29 +370,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 constexpr int kGThreads = 256;  // warp 0 TMA, warp 1 MMA (and TMEM), warps 4-7 epilogue
 constexpr int kEpiWarp0 = 4;
-constexpr int kStages = 4;                                 // P/G ring, half a source block each
-constexpr uint32_t kPBox = kBlk * 64 * 2;                  // 16 KB: 128 destinations x 64 sources
-constexpr uint32_t kStageBytes = kPBox + 2 * kGBox;        // + G of 64 sources x 128 columns
-constexpr uint32_t kColO = 0, kColSt = 256;                // O double buffer [0, 256); S^T
+constexpr int kPStages = 3;                 // P ring: 128 destinations x 64 sources per stage
+constexpr uint32_t kPBox = kBlk * 64 * 2;   // 16 KB
+constexpr int kGSlots = 3;                  // G tiles (128 sources x 128 columns) kept in place
+constexpr uint32_t kColO = 0, kColSt = 256; // O double buffer [0, 256); S^T
 
 struct __align__(8) GBars {
-  uint64_t full[kStages], empty[kStages];
-  uint64_t fk_full, fk_empty;  // Fk of a leaving block
+  uint64_t pfull[kPStages], pempty[kPStages];
+  uint64_t gfull[kGSlots], gempty[kGSlots];
+  uint64_t fk_full, fk_empty;  // Fk of the block's leaving source block
   uint64_t fq_full, fq_empty;  // Fq of the destination block (the read-out)
   uint64_t o_full[2], o_empty[2];
+  uint64_t st_full;            // the block's read-out and state update are complete
   uint64_t sb_full;            // bf16 state copy in place for the next read-out
+  uint64_t v_full;             // the destination block's v in the staging tile
   uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
 };
-// smem: stages | Fk | Fq | S_bf16 | U staging | Bars
-constexpr size_t kGSmemBytes = 1024 + kStages * kStageBytes + 3 * kTile + kGStage + sizeof(GBars);
+// smem: P stages | G slots | Fk | Fq | S_bf16 | U staging | Bars
+constexpr size_t kGSmemBytes =
+    1024 + kPStages * kPBox + kGSlots * kGStage + 3 * kTile + kGStage + sizeof(GBars);
 static_assert(kGSmemBytes <= 232448, "shared memory budget");
 
 struct GArgs {
   int B, T, T_pad, H, dqk, m, d_h, m_h, W;
   int n_iblk, n_ntile, n_strips;
   int nseg, seg_len, n_items;  // each strip's destination blocks in nseg segments
+  int reuse;                   // every destination block has at most kGSlots source blocks
   float* seg_state;            // [n_strips, nseg - 1, kNg, d_h] f32 state at segment ends
   int* seg_flag;               // [n_strips, nseg - 1], 0 until that state is written
   const float* den;            // [B * H, T_pad]
@@ -508,38 +512,52 @@ __device__ __noinline__ void export_state(const GArgs& a, size_t slot, uint32_t 
   if (issuer) st_release_gpu(&a.seg_flag[slot], 1);
 }
 
-// Position, among a destination block's source blocks (newest first), after which the
-// read-out of the older state is issued: the second block when there is one, so the
-// bf16 state copy of the previous block's epilogue has time to arrive.
-__device__ __forceinline__ int readout_pos(int ib, int W) { return ib - jlo_of(ib, W) >= 1 ? 1 : 0; }
+// Schedule of one destination block ib in the gate-strip kernel, followed identically
+// by the TMA and MMA threads:
+//  - at its start, the read-out O = Fq S_bf16 of the state before the block (the first
+//    MMA into O), then the update S^T += G^T Fk of its leaving source block jlo (if
+//    jlo(ib + 1) > jlo), then P.G over the source blocks oldest first, jlo .. ib;
+//  - G tiles stay in kGSlots slots (tile jb in slot jb % kGSlots) for as long as later
+//    blocks of the same work item need them, when every block has at most kGSlots
+//    source blocks ("reuse"); a block then loads only its newest tile, prefetched
+//    during the previous block.  Otherwise every use loads its tile into the next slot.
+//  - the next block's Fq, Fk and (reuse) newest G tile are prefetched after the P
+//    stages of this block's source block prefetch_pos.
+__device__ __forceinline__ int prefetch_pos(int ib, int W) { return ib - jlo_of(ib, W) >= 1 ? 1 : 0; }
+__device__ __forceinline__ bool has_leaving(int ib, int W) { return jlo_of(ib + 1, W) > jlo_of(ib, W); }
 
-// Roles: warp 0 TMA (Fq of the destination block, Fk of leaving blocks, and the ring
-// of P/G stages, half a source block each); warp 1 one thread issuing the MMAs; warps
-// 4-7 the epilogue (one destination row per thread).
+// Roles: warp 0 TMA; warp 1 one thread issuing the MMAs; warps 4-7 the epilogue (one
+// destination row per thread).
 template <int DH, bool kSeg>
 __global__ void __launch_bounds__(kGThreads, 1)
     wango_g_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
-                   const __grid_constant__ CUtensorMap tmU, const GArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmU, const GArgs a) {
   constexpr int RB = DH * 2;
   constexpr uint32_t lay = DH == 64 ? kSwizzle128B : DH == 32 ? kSwizzle64B : kSwizzle32B;
   constexpr uint32_t sbo = 8u * RB;
   constexpr uint32_t tile_bytes = kBlk * RB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sS = base;                          // P/G stages
-  uint8_t* sFK = sS + kStages * kStageBytes;
+  uint8_t* sP = base;                          // P stages
+  uint8_t* sG = sP + kPStages * kPBox;         // G slots
+  uint8_t* sFK = sG + kGSlots * kGStage;
   uint8_t* sFQ = sFK + kTile;
   uint8_t* sSB = sFQ + kTile;                  // bf16 state, [128 gate rows x d_h]
-  uint8_t* sU = sSB + kTile;                   // u staging for the TMA store
+  uint8_t* sU = sSB + kTile;                   // v of the destination block, overwritten by u
   GBars& b = *reinterpret_cast<GBars*>(sU + kGStage);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int W = a.W;
+  const bool reuse = a.reuse != 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&b.full[s], 1);
-      mbar_init(&b.empty[s], 1);
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&b.pfull[s], 1);
+      mbar_init(&b.pempty[s], 1);
+    }
+    for (int s = 0; s < kGSlots; ++s) {
+      mbar_init(&b.gfull[s], 1);
+      mbar_init(&b.gempty[s], 1);
     }
     mbar_init(&b.fk_full, 1);
     mbar_init(&b.fk_empty, 1);
@@ -549,7 +567,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(&b.o_full[s], 1);
       mbar_init(&b.o_empty[s], 4);
     }
+    mbar_init(&b.st_full, 1);
     mbar_init(&b.sb_full, 4);
+    mbar_init(&b.v_full, 1);
     mbar_init(&b.drain, 1);
     mbar_init(&b.never, 1);
     b.abort = 0;
@@ -567,37 +587,66 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
-    Ring sr;
+    Ring pr;
     bool ok = true;
-    uint32_t smask = 0, sph[kStages] = {}, fkph = 0, fq_n = 0, fk_n = 0;
-    int dc = 0;
+    uint32_t gload[kGSlots] = {}, fq_n = 0, fk_n = 0;  // loads issued (slot phases)
+    uint32_t pmask = 0, pph[kPStages] = {};
+    int gseq = 0;  // slot counter when tiles are not kept
+    Strip sp = {};
+    int gx = 0, pz = 0;
+    auto load_g = [&](int jb) -> bool {
+      const int s = reuse ? jb % kGSlots : (gseq++ % kGSlots);
+      if (!wait_bar(&b.gempty[s], (gload[s] & 1) ^ 1, b, a)) return false;
+      ++gload[s];
+      uint8_t* dst = sG + s * kGStage;
+      mbar_arrive_expect_tx(&b.gfull[s], kGStage);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(dst + h * 2 * kGBox + c * kGBox, &tmG, &b.gfull[s], gx + 64 * c, jb * kBlk + 64 * h, sp.b);
+      return true;
+    };
+    auto load_fq = [&](int ib) -> bool {
+      if (!wait_bar(&b.fq_empty, (fq_n & 1) ^ 1, b, a)) return false;
+      ++fq_n;
+      mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
+      tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
+      return true;
+    };
+    auto load_fk = [&](int jb) -> bool {
+      if (!wait_bar(&b.fk_empty, (fk_n & 1) ^ 1, b, a)) return false;
+      ++fk_n;
+      mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
+      tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
+      return true;
+    };
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
-      const Strip sp = strip_of(a, it.st);
-      const int gx = sp.head * a.m_h + sp.n0, pz = sp.b * a.H + sp.head;
-      for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
-        if (!(ok = wait_bar(&b.fq_empty, (dc & 1) ^ 1, b, a))) break;
-        mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
-        tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
-        ++fq_n;
-        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb) {
-          if (is_leaving(jb, ib, W)) {
-            if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
-            mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
-            tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
-            fkph ^= 1;
-            ++fk_n;
-          }
+      if (it.ib0 >= it.ib1) continue;
+      sp = strip_of(a, it.st);
+      gx = sp.head * a.m_h + sp.n0;
+      pz = sp.b * a.H + sp.head;
+      // the first block's read-out and update operands
+      if (!(ok = load_fq(it.ib0))) break;
+      if (has_leaving(it.ib0, W) && !(ok = load_fk(jlo_of(it.ib0, W)))) break;
+      for (int ib = it.ib0; ok && ib < it.ib1; ++ib) {
+        const int jlo = jlo_of(ib, W), ppos = prefetch_pos(ib, W);
+        for (int jb = jlo; ok && jb <= ib; ++jb) {
+          if ((!reuse || ib == it.ib0) && !(ok = load_g(jb))) break;
           for (int hh = 0; hh < 2; ++hh) {
-            if (!(ok = wait_bar(&b.empty[sr.stage], sr.phase ^ 1, b, a))) break;
-            uint8_t* st = sS + sr.stage * kStageBytes;
-            mbar_arrive_expect_tx(&b.full[sr.stage], kStageBytes);
-            tma_load_3d(st, &tmP, &b.full[sr.stage], (ib - jb) * kBlk + 64 * hh, ib * kBlk, pz);
-            tma_load_3d(st + kPBox, &tmG, &b.full[sr.stage], gx, jb * kBlk + 64 * hh, sp.b);
-            tma_load_3d(st + kPBox + kGBox, &tmG, &b.full[sr.stage], gx + 64, jb * kBlk + 64 * hh, sp.b);
-            smask |= 1u << sr.stage;
-            sph[sr.stage] = sr.phase;
-            sr.next(kStages);
+            if (!(ok = wait_bar(&b.pempty[pr.stage], pr.phase ^ 1, b, a))) break;
+            mbar_arrive_expect_tx(&b.pfull[pr.stage], kPBox);
+            tma_load_3d(sP + pr.stage * kPBox, &tmP, &b.pfull[pr.stage], (ib - jb) * kBlk + 64 * hh, ib * kBlk,
+                        pz);
+            pmask |= 1u << pr.stage;
+            pph[pr.stage] = pr.phase;
+            pr.next(kPStages);
+          }
+          if (ok && jb - jlo == ppos && ib + 1 < it.ib1) {  // operands of the next block
+            if (reuse && !(ok = load_g(ib + 1))) break;
+            if (!(ok = load_fq(ib + 1))) break;
+            if (has_leaving(ib + 1, W) && !(ok = load_fk(jlo_of(ib + 1, W)))) break;
           }
         }
       }
@@ -605,8 +654,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // no copy may be in flight when the CTA exits
     if (fq_n) mbar_wait(&b.fq_full, (fq_n - 1) & 1, a.timeout_ns);
     if (fk_n) mbar_wait(&b.fk_full, (fk_n - 1) & 1, a.timeout_ns);
-    for (int s = 0; s < kStages; ++s)
-      if (smask & (1u << s)) mbar_wait(&b.full[s], sph[s], a.timeout_ns);
+    for (int s = 0; s < kGSlots; ++s)
+      if (gload[s]) mbar_wait(&b.gfull[s], (gload[s] - 1) & 1, a.timeout_ns);
+    for (int s = 0; s < kPStages; ++s)
+      if (pmask & (1u << s)) mbar_wait(&b.pfull[s], pph[s], a.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t idesc_o = idesc_bf16_f32(kBlk, kNg, false, true);   // O += P G
@@ -617,74 +668,88 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const uint64_t sbd = smem_desc(smem_u32(sSB), 16, sbo, lay);
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
-    Ring sr;
-    uint32_t sbph = 0, fkph = 0;
-    int dc = 0;
+    Ring pr;
+    uint32_t guse[kGSlots] = {}, sbph = 0, fkph = 0, fqph = 0;
+    int gseq = 0, dc = 0;
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
       // a later segment starts from the state its predecessor handed over
       bool first_update = !(kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0);
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++dc) {
         const int ob = dc & 1;
+        const int jlo = jlo_of(ib, W);
+        const bool leave = has_leaving(ib, W);
         if (!(ok = wait_bar(&b.o_empty[ob], ((dc >> 1) & 1) ^ 1, b, a))) break;
+        // read-out of the state before this block: O = Fq S_bf16
+        if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
+        sbph ^= 1;
+        if (!(ok = wait_bar(&b.fq_full, fqph, b, a))) break;
+        fqph ^= 1;
         tc_fence_after_nc();
         const uint32_t od = tmem + kColO + (uint32_t)(ob * kNg);
-        const int rpos = readout_pos(ib, W);
-        bool copy_ready = false, first = true;
-        int idx = 0;
-        for (int jb = ib; ok && jb >= jlo_of(ib, W); --jb, ++idx) {
-          const bool leaving = is_leaving(jb, ib, W);
-          if (leaving) {  // the read-out copy of the state must be taken before it changes
-            if (!copy_ready) {
-              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-              sbph ^= 1;
-              copy_ready = true;
-            }
-            if (!(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
-          }
-          for (int hh = 0; hh < 2; ++hh) {
-            if (!(ok = wait_bar(&b.full[sr.stage], sr.phase, b, a))) break;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_bf16_ss_nc(od, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, kk != 0 ? 1u : 0u);
+        mma_commit_nc(&b.fq_empty);
+        // G tile of source block jb: its slot, waiting for the load when this is the use
+        // it was loaded for
+        int cur_slot = -1, cur_jb = -1;
+        auto tile = [&](int jb) -> int {
+          if (jb == cur_jb) return cur_slot;
+          const bool loaded_now = !reuse || ib == it.ib0 || jb == ib;
+          const int s = reuse ? jb % kGSlots : (gseq++ % kGSlots);
+          if (loaded_now) {
+            if (!(ok = wait_bar(&b.gfull[s], guse[s] & 1, b, a))) return -1;
+            ++guse[s];
             tc_fence_after_nc();
-            const uint32_t saddr = smem_u32(sS + sr.stage * kStageBytes);
-            const uint64_t pd = smem_desc(saddr, 16, 1024, kSwizzle128B);           // P, K-major
-            const uint64_t gd = smem_desc(saddr + kPBox, kGBox, 1024, kSwizzle128B);  // G, MN-major
+          }
+          cur_jb = jb;
+          cur_slot = s;
+          return s;
+        };
+        // the leaving block enters the state: S^T += G^T Fk (after the read-out copy)
+        if (leave) {
+          const int s = tile(jlo);
+          if (s < 0) break;
+          if (!(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
+          fkph ^= 1;
+          tc_fence_after_nc();
+          const uint32_t gaddr = smem_u32(sG + s * kGStage);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t gd = smem_desc(gaddr + hh * 2 * kGBox, kGBox, 1024, kSwizzle128B);
+            const uint64_t fh = fkmn + (uint64_t)((64 * hh * RB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss_nc(od, pd + (uint64_t)(kk * 2), gd + (uint64_t)(kk * 128), idesc_o,
-                             (first && kk == 0) ? 0u : 1u);
-            first = false;
-            if (leaving) {
-              const uint64_t fh = fkmn + (uint64_t)((64 * hh * RB) >> 4);
+              mma_bf16_ss_nc(tmem + kColSt, gd + (uint64_t)(kk * 128), fh + (uint64_t)((kk * 16 * RB) >> 4),
+                             idesc_u, (first_update && hh == 0 && kk == 0) ? 0u : 1u);
+          }
+          first_update = false;
+          mma_commit_nc(&b.fk_empty);
+        }
+        mma_commit_nc(&b.st_full);
+        // O += P G over the source blocks, oldest first
+        for (int jb = jlo; ok && jb <= ib; ++jb) {
+          const int s = tile(jb);
+          if (s < 0) break;
+          const uint32_t gaddr = smem_u32(sG + s * kGStage);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!(ok = wait_bar(&b.pfull[pr.stage], pr.phase, b, a))) break;
+            tc_fence_after_nc();
+            const uint64_t pd = smem_desc(smem_u32(sP + pr.stage * kPBox), 16, 1024, kSwizzle128B);   // K-major
+            const uint64_t gd = smem_desc(gaddr + hh * 2 * kGBox, kGBox, 1024, kSwizzle128B);         // MN-major
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss_nc(tmem + kColSt, gd + (uint64_t)(kk * 128), fh + (uint64_t)((kk * 16 * RB) >> 4),
-                               idesc_u, (first_update && kk == 0) ? 0u : 1u);
-              first_update = false;
-            }
-            mma_commit_nc(&b.empty[sr.stage]);
-            sr.next(kStages);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss_nc(od, pd + (uint64_t)(kk * 2), gd + (uint64_t)(kk * 128), idesc_o, 1u);
+            mma_commit_nc(&b.pempty[pr.stage]);
+            pr.next(kPStages);
           }
           if (!ok) break;
-          if (leaving) {
-            mma_commit_nc(&b.fk_empty);
-            fkph ^= 1;
-          }
-          if (idx == rpos) {  // read-out of the state before this block: O += Fq S_bf16
-            if (!copy_ready) {
-              if (!(ok = wait_bar(&b.sb_full, sbph, b, a))) break;
-              sbph ^= 1;
-              copy_ready = true;
-            }
-            if (!(ok = wait_bar(&b.fq_full, dc & 1, b, a))) break;
-            tc_fence_after_nc();
-#pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk)
-              mma_bf16_ss_nc(od, fqd + (uint64_t)(kk * 2), sbd + (uint64_t)(kk * 2), idesc_r, 1u);
-            mma_commit_nc(&b.fq_empty);
-          }
+          // release the tile after its last use in this work item
+          if (!reuse || ib + 1 == it.ib1 || jb < jlo_of(ib + 1, W)) mma_commit_nc(&b.gempty[s]);
         }
         if (!ok) break;
-        mma_commit_nc(&b.o_full[ob]);  // also: this block's updates and read-out are complete
+        mma_commit_nc(&b.o_full[ob]);
       }
     }
     mma_commit(&b.drain);
@@ -724,10 +789,24 @@ __global__ void __launch_bounds__(kGThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&b.sb_full);
     };
+    // the destination block's v (128 rows x 128 columns) into the staging tile, once
+    // the previous u store has read it; issued by one thread
+    uint32_t v_n = 0;
+    auto load_v = [&](const Strip& sp, int ib) {
+      bulk_wait_group_read0();
+      mbar_arrive_expect_tx(&b.v_full, kGStage);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sU + h * 2 * kGBox + c * kGBox, &tmV, &b.v_full, sp.head * a.m_h + sp.n0 + 64 * c,
+                      ib * kBlk + 64 * h, sp.b);
+    };
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
       if (it.ib0 >= it.ib1) continue;
       const Strip sp = strip_of(a, it.st);
+      if (issuer && a.v) load_v(sp, it.ib0);
       // the state before the first destination block: empty, or the previous
       // segment's (into TMEM for the updates, bf16 into shared memory for the read-out)
       if (kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0) {
@@ -741,22 +820,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int ob = gib & 1;
         const int i = ib * kBlk + row;
         const bool row_ok = i < a.T;
-        // before the wait: the denominator and this row's 128 columns of v
         const float den = a.den[(size_t)(sp.b * a.H + sp.head) * a.T_pad + i];
         const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
-        uint4 vv[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int col = sp.n0 + 8 * k;
-          vv[k] = (a.v && row_ok && col < a.m_h) ? ld_global_v4(a.v + grow + col) : make_uint4(0, 0, 0, 0);
-        }
-        if (ok) ok = wait_bar(&b.o_full[ob], (gib >> 1) & 1, b, a);
+        // the state after this block's update, for the next block's read-out (this
+        // block's read-out and update are complete; the next block changes it only after
+        // its own read-out)
+        if (ok) ok = wait_bar(&b.st_full, gib & 1, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
         tc_fence_after();
-        // the state after this block, for the next block's read-out (this block's
-        // updates and read-out are complete; the next block updates it only after)
         if (ib + 1 < it.ib1) copy_state(jlo_of(ib + 1, W) == 0);
+        if (ok) ok = wait_bar(&b.o_full[ob], (gib >> 1) & 1, b, a);
+        if (ok && a.v) ok = wait_bar(&b.v_full, v_n & 1, b, a);
+        ok = named_bar_and(2, 128, ok);
+        if (!ok) break;
+        if (a.v) ++v_n;
+        tc_fence_after();
         const float inv = 1.f / den;
         // gbar = O / den, rounded to bf16, in registers; the accumulator is released as
         // soon as it has been read
@@ -773,9 +852,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&b.o_empty[ob]);
-        // u = gbar * v into the staging tile (once the previous store has read it)
-        if (issuer) bulk_wait_group_read0();
-        named_bar_sync(2, 128);
+        if (!a.v) {  // without v the tile is written from scratch: the previous store must have read it
+          if (issuer) bulk_wait_group_read0();
+          named_bar_sync(2, 128);
+        }
+        // u = gbar * v, written over v in the staging tile (each thread its own row)
         const int rh = row >> 6, rr = row & 63;
 #pragma unroll
         for (int cq = 0; cq < 2; ++cq) {
@@ -784,19 +865,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint32_t box = smem_u32(sU) + rh * 2 * kGBox + cq * kGBox + rr * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
+            const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
             const uint32_t* g4 = &gb[cq * 32 + k * 4];
-            const uint4 v4 = vv[cq * 8 + k];
             uint32_t u[4];
             if (a.v) {
-              u[0] = mul_bf16x2(g4[0], v4.x);
-              u[1] = mul_bf16x2(g4[1], v4.y);
-              u[2] = mul_bf16x2(g4[2], v4.z);
-              u[3] = mul_bf16x2(g4[3], v4.w);
+              const uint4 vv = ld_shared_v4(addr);
+              u[0] = mul_bf16x2(g4[0], vv.x);
+              u[1] = mul_bf16x2(g4[1], vv.y);
+              u[2] = mul_bf16x2(g4[2], vv.z);
+              u[3] = mul_bf16x2(g4[3], vv.w);
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e) u[e] = g4[e];
             }
-            if (!straddle) st_shared_v4(box + (uint32_t)((k ^ (rr & 7)) << 4), make_uint4(u[0], u[1], u[2], u[3]));
+            if (!straddle) st_shared_v4(addr, make_uint4(u[0], u[1], u[2], u[3]));
             else if (row_ok && col0 + 8 * k < a.m_h) st_global_v4(a.out + grow + col0 + 8 * k, u[0], u[1], u[2], u[3]);
           }
         }
@@ -807,16 +889,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int y = ib * kBlk + 64 * h;
             if (y >= a.T) continue;
             for (int cq = 0; cq < 2; ++cq) {
-              const int col0 = sp.n0 + cq * 64;
-              if (col0 + 64 > a.m_h) continue;
-              tma_store_3d(&tmU, sU + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + col0, y, sp.b);
+              const int c = sp.n0 + cq * 64;
+              if (c + 64 > a.m_h) continue;
+              tma_store_3d(&tmU, sU + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + c, y, sp.b);
             }
           }
           bulk_commit_group();
+          if (a.v && ib + 1 < it.ib1) load_v(sp, ib + 1);  // the next block's v, once the store has read u
         }
       }
       // hand this segment's final state to the next segment of the strip (the last
-      // block's updates are complete: its o_full was waited for above)
+      // block's update is complete: its st_full was waited for above)
       if (kSeg && ok && it.seg + 1 < a.nseg && jlo_of(it.ib1, W) > 0)
         export_state<DH>(a, (size_t)it.st * (a.nseg - 1) + it.seg, tmem + kColSt + lane_off, row, issuer);
     }
@@ -1002,12 +1085,12 @@ cudaError_t launch_p(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 
 template <int DH>
 cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtensorMap& mfq, const CUtensorMap& mfk,
-                     const CUtensorMap& mu, const GArgs& a, cudaStream_t s) {
+                     const CUtensorMap& mv, const CUtensorMap& mu, const GArgs& a, cudaStream_t s) {
   auto kern = a.nseg > 1 ? wango_g_kernel<DH, true> : wango_g_kernel<DH, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
-  kern<<<grid, kGThreads, kGSmemBytes, s>>>(mp, mg, mfq, mfk, mu, a);
+  kern<<<grid, kGThreads, kGSmemBytes, s>>>(mp, mg, mfq, mfk, mv, mu, a);
   return cudaGetLastError();
 }
 
@@ -1041,13 +1124,14 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mk, mfq, mfk, mp, mg, mu;
+  CUtensorMap mq, mk, mfq, mfk, mp, mg, mv, mu;
   e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mfq, fq, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mfk, fk, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mp, P, (uint64_t)p.B * p.H, L.T_pad, L.ldp, kBlk, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
   if (e != cudaSuccess) return e;
 
@@ -1073,6 +1157,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.nseg = L.nseg;
   a.seg_len = ceil_div(n_iblk, a.nseg);
   a.n_items = a.n_strips * a.nseg;
+  a.reuse = L.ldp / kBlk <= kGSlots ? 1 : 0;
   a.seg_state = reinterpret_cast<float*>(aux + L.seg);
   a.seg_flag = reinterpret_cast<int*>(aux + L.flag);
   a.den = den;
@@ -1085,8 +1170,9 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
     e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  return d_h == 64 ? launch_g<64>(mp, mg, mfq, mfk, mu, a, s)
-                   : d_h == 32 ? launch_g<32>(mp, mg, mfq, mfk, mu, a, s) : launch_g<16>(mp, mg, mfq, mfk, mu, a, s);
+  return d_h == 64 ? launch_g<64>(mp, mg, mfq, mfk, mv, mu, a, s)
+                   : d_h == 32 ? launch_g<32>(mp, mg, mfq, mfk, mv, mu, a, s)
+                               : launch_g<16>(mp, mg, mfq, mfk, mv, mu, a, s);
 }
 
 }  // namespace tg

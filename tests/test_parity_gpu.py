@@ -55,6 +55,8 @@ SMALL = [
     (1, 300, 2, 128, 2096, 129),  # ragged window boundary
     (1, 700, 2, 128, 272, 200),   # two mixed blocks in a row, window > one block
     (2, 520, 2, 64, 144, 100),    # W < block: the diagonal block is mixed too
+    (1, 700, 2, 128, 272, 400),   # five source blocks per destination block
+    (1, 700, 2, 64, 144, 700),    # W = T: every earlier block is a source block
 ]
 
 
