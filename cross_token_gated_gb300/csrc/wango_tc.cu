@@ -521,8 +521,9 @@ __device__ __noinline__ void export_state(const GArgs& a, size_t slot, uint32_t 
 //    blocks of the same work item need them, when every block has at most kGSlots
 //    source blocks ("reuse"); a block then loads only its newest tile, prefetched
 //    during the previous block.  Otherwise every use loads its tile into the next slot.
-//  - the next block's Fq, Fk and (reuse) newest G tile are prefetched after the P
-//    stages of this block's source block prefetch_pos.
+//  - the next block's Fq and Fk are prefetched after the P stages of this block's
+//    source block prefetch_pos, and (reuse) its newest G tile after this block's last
+//    P stages.
 __device__ __forceinline__ int prefetch_pos(int ib, int W) { return ib - jlo_of(ib, W) >= 1 ? 1 : 0; }
 __device__ __forceinline__ bool has_leaving(int ib, int W) { return jlo_of(ib + 1, W) > jlo_of(ib, W); }
 
@@ -643,11 +644,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             pph[pr.stage] = pr.phase;
             pr.next(kPStages);
           }
-          if (ok && jb - jlo == ppos && ib + 1 < it.ib1) {  // operands of the next block
-            if (reuse && !(ok = load_g(ib + 1))) break;
+          if (ok && jb - jlo == ppos && ib + 1 < it.ib1) {  // the next block's read-out and update
             if (!(ok = load_fq(ib + 1))) break;
             if (has_leaving(ib + 1, W) && !(ok = load_fk(jlo_of(ib + 1, W)))) break;
           }
+          // the next block's newest G tile, behind this block's P loads (a tile from HBM
+          // would hold up the P loads queued after it)
+          if (ok && jb == ib && reuse && ib + 1 < it.ib1 && !(ok = load_g(ib + 1))) break;
         }
       }
     }
