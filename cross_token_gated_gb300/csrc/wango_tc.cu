@@ -19,13 +19,13 @@
 // The weights depend on q and k only, not on the gate column, so they are computed
 // once per destination block and shared by every gate column:
 //  1. Pre-pass (CUDA cores): Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat)
-//     in bf16; the column sums of Fk per source block; the older-prefix denominator
-//     Fq_i . z of every destination (z over the blocks below its block's window).
+//     in bf16, and the column sums of Fk per source block.
 //  2. wango_p_kernel (tcgen05): per (batch, head, destination block) the scores
 //     Qhat Khat^T (and Fq Fk^T for mixed blocks) in TMEM, the weights in bf16 written
 //     to global memory as P [destination, (ib - jb) * 128 + source], and the full
-//     denominator (the row sums of the bf16 weights as applied, the older prefix and
-//     the null term).  P is a band of T x (W + 128) per head: linear in T.
+//     denominator (the row sums of the bf16 weights as applied, the older prefix
+//     Fq_i . z with z the column sums of Fk below the window, and the null term).  P is
+//     a band of T x (W + 128) per head: linear in T.
 //  3. wango_g_kernel (tcgen05): per (batch, head, 128-column gate strip) the
 //     destination blocks in order: O = sum_jb P_jb G_jb with both operands loaded by
 //     TMA, the state update S^T += G^T Fk for leaving blocks, the read-out
@@ -133,6 +133,7 @@ struct __align__(8) PBars {
   uint32_t tmem_base;
   int abort;
   float rowsum[2][kBlk];           // per warpgroup, per destination row
+  float z[64];                     // sum of Fk over the sources below the block's window
 };
 // smem: Qhat | Fq | K x 2 | Fk | Bars
 constexpr size_t kPSmemBytes = 1024 + kTile * 5 + sizeof(PBars);
@@ -142,7 +143,8 @@ struct PArgs {
   float s;
   const float* tau;
   const float* null_bias;
-  const float* den_old;  // [B, H, T]
+  const float* zb;                 // [B, H, n_iblk, d_h] per-block column sums of Fk
+  const __nv_bfloat16* fq;         // [B, T, dqk] Fq
   __nv_bfloat16* P;      // [B * H, T_pad, ldp]
   float* den;            // [B * H, T_pad]
   unsigned* err;
@@ -297,6 +299,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const float c = tau * kLog2e;
     __nv_bfloat16* prow = a.P + ((size_t)(bb * a.H + head) * a.T_pad + i) * a.ldp;
     uint64_t dsum2[2] = {0, 0};
+    // z = the column sums of Fk over the blocks below the window (jb < jlo), for the
+    // older-prefix denominator Fq_i . z
+    {
+      const int t = threadIdx.x - kPWeightWarp0 * 32;
+      if (t < a.d_h) {
+        const float* zr = a.zb + ((size_t)bb * a.H + head) * a.n_iblk * a.d_h + t;
+        float zs = 0.f;
+        for (int j = 0; j < jlo; ++j) zs += zr[(size_t)j * a.d_h];
+        b.z[t] = zs;
+      }
+      named_bar_sync(1, 256);
+    }
     bool ok = true;
     uint32_t u = 0;
     for (int jb = ib; ok && jb >= jlo; --jb) {
@@ -352,8 +366,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
       float den = 1.f;  // rows past T: any finite value
       if (i < a.T) {
         const float null_w = a.null_bias ? exp2f((a.null_bias[head] - tau) * kLog2e) : 0.f;
-        den = b.rowsum[0][row] + b.rowsum[1][row] + a.den_old[((size_t)bb * a.H + head) * a.T + i] +
-              (float)(i + 1) * null_w;
+        const __nv_bfloat16* f = a.fq + ((size_t)bb * a.T + i) * a.dqk + (size_t)head * a.d_h;
+        float older = 0.f;
+        for (int c = 0; c < a.d_h; c += 8) {
+          const uint4 w = *reinterpret_cast<const uint4*>(f + c);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            older = fmaf(bf16lo(ww[e]), b.z[c + 2 * e], older);
+            older = fmaf(bf16hi(ww[e]), b.z[c + 2 * e + 1], older);
+          }
+        }
+        den = b.rowsum[0][row] + b.rowsum[1][row] + older + (float)(i + 1) * null_w;
       }
       a.den[(size_t)(bb * a.H + head) * a.T_pad + i] = den;
     }
@@ -925,91 +949,57 @@ __device__ __forceinline__ float phi_fast(float u, float inv_sqrt_dh, int mode) 
   return fmaxf(e1 + 1e-4f, 1e-4f) * inv_sqrt_dh;
 }
 
-// Fq = e^-tau phi(sqrt(tau) qhat), Fk = phi(sqrt(tau) khat); one thread per (row, 8
-// consecutive features of one head).
-__global__ void wango_phi_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* fq,
-                                 __nv_bfloat16* fk, long long rows, int H, int dqk, float s, const float* tau,
-                                 int phi_mode, unsigned* err) {
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int groups = dqk / 8;
-  if (idx >= rows * groups) return;
-  const long long r = idx / groups;
-  const int c0 = (int)(idx % groups) * 8;
-  const int d_h = dqk / H, a = c0 / d_h;
-  const float t = head_tau(tau, s, a, err, kKernWango);
-  const float sq = sqrtf(t), shift = exp2f(-t * kLog2e), inv_sqrt_dh = rsqrtf((float)d_h);
-  const uint4 qv = *reinterpret_cast<const uint4*>(q + r * dqk + c0);
-  const uint4 kv = *reinterpret_cast<const uint4*>(k + r * dqk + c0);
-  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
-  uint32_t fo[4], ko[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    fo[e] = pack_bf16x2(shift * phi_fast(sq * bf16lo(qw[e]), inv_sqrt_dh, phi_mode),
-                        shift * phi_fast(sq * bf16hi(qw[e]), inv_sqrt_dh, phi_mode));
-    ko[e] = pack_bf16x2(phi_fast(sq * bf16lo(kw[e]), inv_sqrt_dh, phi_mode),
-                        phi_fast(sq * bf16hi(kw[e]), inv_sqrt_dh, phi_mode));
-  }
-  *reinterpret_cast<uint4*>(fq + r * dqk + c0) = make_uint4(fo[0], fo[1], fo[2], fo[3]);
-  *reinterpret_cast<uint4*>(fk + r * dqk + c0) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-}
-
-// zb[b, a, jb, c] = sum over the valid sources of block jb of Fk[., a*d_h + c] (the bf16
-// values the state update multiplies).  grid
-// (n_iblk, H, B), 256 threads: thread (g, p) sums column pair p over rows g, g + 8, ...
-// (bf16x2 loads, one head row per warp), then the eight row groups are added.
-__global__ void __launch_bounds__(256) wango_blocksum_kernel(const __nv_bfloat16* fk, float* zb, int T, int H,
-                                                             int dqk, int n_iblk) {
-  __shared__ float part[8][64];
+// Per (source block jb, head a, batch b), one thread per row of the block:
+// Fq = e^-tau phi(sqrt(tau) qhat) and Fk = phi(sqrt(tau) khat) in bf16, and
+// zb[b, a, jb, c] = the sum over the block's valid rows of Fk[., a d_h + c] as rounded to
+// bf16 (the values the state update multiplies).
+__global__ void __launch_bounds__(kBlk) wango_phi_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                                        __nv_bfloat16* fq, __nv_bfloat16* fk, float* zb, int T,
+                                                        int H, int dqk, int n_iblk, float s, const float* tau,
+                                                        int phi_mode, unsigned* err) {
+  __shared__ float part[kBlk / 32][64];
   const int jb = blockIdx.x, a = blockIdx.y, bb = blockIdx.z;
-  const int d_h = dqk / H, npair = d_h / 2;
-  const int p = threadIdx.x % 32, g = threadIdx.x / 32;
-  const int j0 = jb * kBlk, j1 = min(T, j0 + kBlk);
-  float s0 = 0.f, s1 = 0.f;
-  if (p < npair) {
-    for (int j = j0 + g; j < j1; j += 8) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(fk + ((size_t)bb * T + j) * dqk + a * d_h + 2 * p);
-      s0 += bf16lo(w);
-      s1 += bf16hi(w);
-    }
-    part[g][2 * p] = s0;
-    part[g][2 * p + 1] = s1;
-  }
-  __syncthreads();
-  if (threadIdx.x < d_h) {
-    float t = 0.f;
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int d_h = dqk / H, i = jb * kBlk + t;
+  const float tt = head_tau(tau, s, a, err, kKernWango);
+  const float sq = sqrtf(tt), shift = exp2f(-tt * kLog2e), inv_sqrt_dh = rsqrtf((float)d_h);
+  float fkv[64];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) t += part[q][threadIdx.x];
-    zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + threadIdx.x] = t;
-  }
-}
-// den_old[b, a, i] = Fq_i . z with z the sum of zb over the blocks older than the window of
-// i's destination block ib (jb < jlo(ib)).  grid (n_iblk, H, B), 128 threads, one row
-// each; Fq is read 16 bytes at a time.
-__global__ void __launch_bounds__(128) wango_denold_kernel(const __nv_bfloat16* fq, const float* zb, float* den_old,
-                                                           int T, int H, int dqk, int n_iblk, int W) {
-  __shared__ float z[64];
-  const int ib = blockIdx.x, a = blockIdx.y, bb = blockIdx.z, t = threadIdx.x;
-  const int d_h = dqk / H, jlo = jlo_of(ib, W);
-  if (t < d_h) {
-    float s = 0.f;
-    for (int jb = 0; jb < jlo; ++jb) s += zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + t];
-    z[t] = s;
-  }
-  __syncthreads();
-  const int i = ib * kBlk + t;
-  if (i >= T) return;
-  const __nv_bfloat16* f = fq + ((size_t)bb * T + i) * dqk + a * d_h;
-  float dot = 0.f;
-  for (int c = 0; c < d_h; c += 8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(f + c);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  for (int c = 0; c < 64; ++c) fkv[c] = 0.f;
+  if (i < T) {
+    const size_t off = ((size_t)bb * T + i) * dqk + (size_t)a * d_h;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      dot = fmaf(bf16lo(ww[e]), z[c + 2 * e], dot);
-      dot = fmaf(bf16hi(ww[e]), z[c + 2 * e + 1], dot);
+    for (int c0 = 0; c0 < 64; c0 += 8) {
+      if (c0 >= d_h) break;
+      const uint4 qv = *reinterpret_cast<const uint4*>(q + off + c0);
+      const uint4 kv = *reinterpret_cast<const uint4*>(k + off + c0);
+      const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+      uint32_t fo[4], ko[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        fo[e] = pack_bf16x2(shift * phi_fast(sq * bf16lo(qw[e]), inv_sqrt_dh, phi_mode),
+                            shift * phi_fast(sq * bf16hi(qw[e]), inv_sqrt_dh, phi_mode));
+        ko[e] = pack_bf16x2(phi_fast(sq * bf16lo(kw[e]), inv_sqrt_dh, phi_mode),
+                            phi_fast(sq * bf16hi(kw[e]), inv_sqrt_dh, phi_mode));
+        fkv[c0 + 2 * e] = bf16lo(ko[e]);
+        fkv[c0 + 2 * e + 1] = bf16hi(ko[e]);
+      }
+      *reinterpret_cast<uint4*>(fq + off + c0) = make_uint4(fo[0], fo[1], fo[2], fo[3]);
+      *reinterpret_cast<uint4*>(fk + off + c0) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
     }
   }
-  den_old[((size_t)bb * H + a) * T + i] = dot;
+  // column sums over the block's rows: across each warp, then across the four warps
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    if (c >= d_h) break;
+    float v = fkv[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) part[wp][c] = v;
+  }
+  __syncthreads();
+  if (t < d_h)
+    zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + t] = (part[0][t] + part[1][t]) + (part[2][t] + part[3][t]);
 }
 
 int num_sms() {
@@ -1051,7 +1041,7 @@ int max_sources(int n_iblk, int W) {
 }
 
 struct AuxLayout {
-  size_t fq, fk, zb, den_old, P, den, seg, flag, total;
+  size_t fq, fk, zb, P, den, seg, flag, total;
   int nseg, T_pad, ldp;
 };
 AuxLayout aux_layout(int B, int T, int H, int dqk, int m, int W) {
@@ -1067,8 +1057,7 @@ AuxLayout aux_layout(int B, int T, int H, int dqk, int m, int W) {
   L.fq = 0;
   L.fk = L.fq + a256(BT * dqk * 2);
   L.zb = L.fk + a256(BT * dqk * 2);
-  L.den_old = L.zb + a256((size_t)B * H * nI * d_h * 4);
-  L.P = L.den_old + a256((size_t)B * H * T * 4);
+  L.P = L.zb + a256((size_t)B * H * nI * d_h * 4);
   L.den = L.P + a256((size_t)B * H * L.T_pad * L.ldp * 2);
   L.seg = L.den + a256((size_t)B * H * L.T_pad * 4);
   L.flag = L.seg + a256(handoffs * kNg * d_h * 4);
@@ -1111,19 +1100,13 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   __nv_bfloat16* fq = reinterpret_cast<__nv_bfloat16*>(aux + L.fq);
   __nv_bfloat16* fk = reinterpret_cast<__nv_bfloat16*>(aux + L.fk);
   float* zb = reinterpret_cast<float*>(aux + L.zb);
-  float* den_old = reinterpret_cast<float*>(aux + L.den_old);
   __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(aux + L.P);
   float* den = reinterpret_cast<float*>(aux + L.den);
 
-  // pre-pass: feature maps, block sums, older-prefix denominators
-  const long long rows = (long long)p.B * p.T;
-  const long long work = rows * (p.dqk / 8);
-  wango_phi_kernel<<<(unsigned)((work + 255) / 256), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, rows, p.H, p.dqk,
-      p.s, p.tau, p.phi_mode, p.err);
-  dim3 g3(n_iblk, p.H, p.B);
-  wango_blocksum_kernel<<<g3, 256, 0, s>>>(fk, zb, p.T, p.H, p.dqk, n_iblk);
-  wango_denold_kernel<<<g3, kBlk, 0, s>>>(fq, zb, den_old, p.T, p.H, p.dqk, n_iblk, p.window);
+  // pre-pass: feature maps and their per-block column sums
+  wango_phi_kernel<<<dim3(n_iblk, p.H, p.B), kBlk, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, zb, p.T, p.H, p.dqk,
+      n_iblk, p.s, p.tau, p.phi_mode, p.err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1142,7 +1125,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   PArgs pa = {};
   pa.B = p.B; pa.T = p.T; pa.T_pad = L.T_pad; pa.H = p.H; pa.dqk = p.dqk; pa.d_h = d_h; pa.W = p.window;
   pa.n_iblk = n_iblk; pa.ldp = L.ldp;
-  pa.s = p.s; pa.tau = p.tau; pa.null_bias = p.null_bias; pa.den_old = den_old;
+  pa.s = p.s; pa.tau = p.tau; pa.null_bias = p.null_bias; pa.zb = zb; pa.fq = fq;
   pa.P = P; pa.den = den; pa.err = p.err; pa.timeout_ns = timeout_ns;
   e = d_h == 64 ? launch_p<64>(mq, mk, mfq, mfk, pa, s)
                 : d_h == 32 ? launch_p<32>(mq, mk, mfq, mfk, pa, s) : launch_p<16>(mq, mk, mfq, mfk, pa, s);
