@@ -124,6 +124,8 @@ tg_status validate_block(const tg_block_params* p) {
   if (p->mode != TG_MODE_TANGO && p->mode != TG_MODE_WANGO) return TG_ERR_INVALID_ARG;
   if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
   if (p->agg.dtype == TG_BF16 && p->d % 64 != 0) return TG_ERR_UNSUPPORTED;
+  // the projection GEMM takes q and k in one 256-column tile, or in 256-column tiles
+  if (p->agg.dtype == TG_BF16 && 2 * p->agg.d_qk > 256 && p->agg.d_qk % 256 != 0) return TG_ERR_UNSUPPORTED;
   return TG_OK;
 }
 

@@ -190,10 +190,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dA = sA + stage * kABytes;
         uint8_t* dB = sB + stage * kBBytes;
         const int k0 = kb * BK;
-        if (tl.seg == kSegQK) {
+        if (tl.seg == kSegQK && a.nb_qk == 1) {  // q and k rows in one tile (2 d_qk <= 256)
           mbar_arrive_expect_tx(&b.full[stage], kABytes + 2u * a.dqk * 128u);
           tma_load_2d(dB, &tmB0, &b.full[stage], k0, 0);
           tma_load_2d(dB + a.dqk * 128, &tmB1, &b.full[stage], k0, 0);
+        } else if (tl.seg == kSegQK) {  // 256 rows of W_q (first half of the n-blocks) or W_k
+          const int nq = a.nb_qk / 2;
+          mbar_arrive_expect_tx(&b.full[stage], kABytes + kBBytes);
+          tma_load_2d(dB, tl.nb < nq ? &tmB0 : &tmB1, &b.full[stage], k0, (tl.nb % nq) * BN);
         } else {
           mbar_arrive_expect_tx(&b.full[stage], kABytes + kBBytes);
           const CUtensorMap* mb = tl.seg == kSegG ? &tmB2 : tl.seg == kSegV ? &tmB3 : &tmB0;
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(a, t);
-      const int N = tl.seg == kSegQK ? 2 * a.dqk : BN;
+      const int N = (tl.seg == kSegQK && a.nb_qk == 1) ? 2 * a.dqk : BN;
       const uint32_t idesc = idesc_bf16_f32(BM, N, false, false);
       if (!wait_bar(&b.acc_empty[acc], acc_phase ^ 1, b, a.err)) break;
       tc_fence_after();
@@ -260,10 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tl.seg == kSegQK) {
         const bool valid = row < a.M;
         const int d_h = a.dqk / a.H, t_pos = valid ? row % a.T : 0;
-        for (int hh = 0; hh < 2 * a.H; ++hh) {
-          const int head = hh % a.H;
-          __nv_bfloat16* dst = (hh < a.H ? a.q : a.k) + (size_t)(valid ? row : 0) * a.dqk + head * d_h;
-          const uint32_t col = (uint32_t)((hh < a.H ? 0 : a.dqk) + head * d_h);
+        // the tile's heads: all q then all k heads (one tile), or 256 / d_h heads of q or k
+        const int nheads = a.nb_qk == 1 ? 2 * a.H : BN / d_h;
+        const int nq = a.nb_qk / 2;
+        for (int hh = 0; hh < nheads; ++hh) {
+          const bool is_q = a.nb_qk == 1 ? hh < a.H : tl.nb < nq;
+          const int head = a.nb_qk == 1 ? hh % a.H : (tl.nb % nq) * (BN / d_h) + hh;
+          __nv_bfloat16* dst = (is_q ? a.q : a.k) + (size_t)(valid ? row : 0) * a.dqk + head * d_h;
+          const uint32_t col = (uint32_t)(a.nb_qk == 1 ? (is_q ? 0 : a.dqk) + head * d_h : hh * d_h);
           if (d_h == 64) rope_norm_store<64>(trow + col, dst, t_pos, valid, a);
           else if (d_h == 32) rope_norm_store<32>(trow + col, dst, t_pos, valid, a);
           else rope_norm_store<16>(trow + col, dst, t_pos, valid, a);
@@ -375,15 +383,18 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   cudaError_t e = make_tmap_2d(&mA, p.x, p.M, p.d, p.d, BM, BK);
   if (e == cudaSuccess) e = make_tmap_2d(&mog, p.g, p.M, p.m, p.m, BM, 64);
   if (e == cudaSuccess) e = make_tmap_2d(&mov, p.v, p.M, p.m, p.m, BM, 64);
-  if (e == cudaSuccess) e = make_tmap_2d(&mq, p.Wq, p.dqk, p.d, p.d, p.dqk, BK);
-  if (e == cudaSuccess) e = make_tmap_2d(&mk, p.Wk, p.dqk, p.d, p.d, p.dqk, BK);
+  // q/k: one tile of 2 d_qk <= 256 rows, or 256-row tiles of W_q then W_k (d_qk % 256 == 0)
+  const uint32_t qk_box = 2 * p.dqk <= BN ? (uint32_t)p.dqk : (uint32_t)BN;
+  if (e == cudaSuccess) e = make_tmap_2d(&mq, p.Wq, p.dqk, p.d, p.d, qk_box, BK);
+  if (e == cudaSuccess) e = make_tmap_2d(&mk, p.Wk, p.dqk, p.d, p.d, qk_box, BK);
   if (e == cudaSuccess) e = make_tmap_2d(&mg, p.Wg, p.m, p.d, p.d, BN, BK);
   if (e == cudaSuccess) e = make_tmap_2d(&mv, p.Wv, p.m, p.d, p.d, BN, BK);
   if (e != cudaSuccess) return e;
   GemmArgs a = {};
   a.M = p.M; a.K = p.d;
   a.n_mblk = ceil_div(p.M, BM);
-  a.nb_qk = 1; a.nb_g = ceil_div(p.m, BN); a.nb_v = a.nb_g; a.nb_out = 0;
+  a.nb_qk = 2 * p.dqk <= BN ? 1 : 2 * p.dqk / BN;
+  a.nb_g = ceil_div(p.m, BN); a.nb_v = a.nb_g; a.nb_out = 0;
   a.m_major = 0;
   a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m; a.d = p.d;
   const int d_h = p.dqk / p.H;

@@ -122,6 +122,14 @@ def test_block_pads_unaligned_head_gate_width(lib):
         a256(BT * d * 4) + 2 * a256(BT * dqk * 4) + 2 * a256(BT * 2 * 4747 * 4)
 
 
+def test_block_qk_width_rule(lib):
+    """bf16 blocks take q and k in one 256-column projection tile (d_qk <= 128) or in
+    256-column tiles (d_qk a multiple of 256, e.g. the paper's 16 heads of 32)."""
+    for dqk, H, ok in ((128, 2, True), (512, 16, True), (256, 8, True), (384, 12, False)):
+        bp = tg.block_params(2, 64, 512, H, dqk, 256 * H, dtype=tg.TG_BF16)
+        assert (tg.tg_workspace_size(tg.TG_WS_BLOCK, bp) > 0) == ok, dqk
+
+
 def _model(**kw):
     base = dict(B=2, T=64, d=512, H=2, d_qk=128, m=256, vocab=1000, dtype=tg.TG_BF16)
     base.update(kw)

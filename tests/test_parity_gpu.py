@@ -291,3 +291,17 @@ def test_model_shared_block_config_sampled(m, n_sets):
     got = out[[0, 15], :Tp]
     ref = ref_model(ids[[0, 15], :Tp], E, gam_f, sets, 2, 0, 1)
     assert rel_err(got, ref) <= model_tol("bf16")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_block_paper_head_geometry(mode):
+    """The paper's own head geometry (sec. 2.3: H=16 heads of d_h=32, F=28,480, i.e. 1,780
+    gate columns per head, which the bf16 block pads to 1,784; WANGO window 64), d=512,
+    T=300 (ragged), every output compared."""
+    B, T, d, dqk, m, H, W = 1, 300, 512, 512, 28480, 16, 64
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=11, dtype="bf16")
+    out = run_block(h, w, H, mode, W)
+    ref = ref_block(h, w, H, mode, W)
+    h64 = h.double().numpy()
+    assert rel_err(out, ref) <= TOL["bf16"]
+    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
