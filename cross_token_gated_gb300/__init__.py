@@ -6,9 +6,9 @@ kernels.  PyTorch supplies device memory and streams.  There is no fallback: if
 the library cannot be loaded, every call raises.
 
 Functions (same names as the C ABI):
-  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_block_forward,
-  tango_model_forward, tg_workspace_size, tg_status_string, tg_check_device_error,
-  tg_version
+  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, wango_decode_step,
+  tango_block_forward, tango_model_forward, tg_workspace_size, tg_status_string,
+  tg_check_device_error, tg_version
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ TG_F32, TG_BF16 = 0, 1
 TG_FLAG_QK_NORMALIZED = 0x1
 TG_FLAG_DEBUG_TIMEOUT = 0x100
 TG_MODE_TANGO, TG_MODE_WANGO = 0, 1
-TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL = 0, 1, 2, 3
+TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL, TG_WS_DECODE = 0, 1, 2, 3, 4
 
 HEADER = os.path.join(_build.INCLUDE, "tango.h")
 
@@ -98,6 +98,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.tango_aggregate_noalloc.restype = ctypes.c_int
         lib.tango_block_forward.argtypes = [P(tg_block_params), P(tg_block_weights), vp, vp, vp, sz, vp]
         lib.tango_block_forward.restype = ctypes.c_int
+        lib.wango_decode_step.argtypes = [P(tg_agg_params), ctypes.c_longlong, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.wango_decode_step.restype = ctypes.c_int
         lib.tango_model_forward.argtypes = [P(tg_model_params), P(tg_model_weights), vp, vp, vp, sz, vp]
         lib.tango_model_forward.restype = ctypes.c_int
         lib.tg_workspace_size.argtypes = [ctypes.c_int, vp]
@@ -308,3 +310,25 @@ def tango_model_forward(ids, embedding, final_gamma, sets, logits, *, H, n_apps=
     if st != TG_OK:
         raise TgError(st, "tango_model_forward")
     return logits
+
+
+def decode_state(B, H, d_qk, m, *, window, dtype, device="cuda"):
+    """Allocates a state buffer for wango_decode_step (cleared by the step at pos 0)."""
+    p = agg_params(B, 1, H, d_qk, m, dtype=dtype, window=window)
+    return _workspace(tg_workspace_size(TG_WS_DECODE, p), device, None)
+
+
+def wango_decode_step(q, k, g, v, out, state, pos, *, H, window, s=10.0, tau=None, null_bias=None,
+                      phi_mode=0, flags=0, stream=None):
+    """One autoregressive WANGO step for B sequences at position pos.  q, k [B, d_qk];
+    g, v, out [B, m]; state from decode_state(), kept between steps (pos = 0, 1, ...)."""
+    B, d_qk = q.shape
+    m = g.shape[-1]
+    p = agg_params(B, 1, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias, window=window,
+                   phi_mode=phi_mode, flags=flags)
+    wp, wn = _ws_ptr(state)
+    st = load().wango_decode_step(ctypes.byref(p), int(pos), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(out),
+                                  wp, wn, _stream(stream))
+    if st != TG_OK:
+        raise TgError(st, "wango_decode_step")
+    return out

@@ -172,6 +172,37 @@ ModelWs model_ws_layout(const tg_model_params* p) {
   return w;
 }
 
+// ---- WANGO decode step
+tg_status validate_decode(const tg_agg_params* p) {
+  if (!p) return TG_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->H > TG_MAX_HEADS || p->d_qk < 1 || p->m < 1) return TG_ERR_INVALID_ARG;
+  if (p->d_qk % p->H != 0 || p->m % p->H != 0) return TG_ERR_INVALID_ARG;
+  if (p->dtype != TG_F32 && p->dtype != TG_BF16) return TG_ERR_INVALID_ARG;
+  if (!p->tau && !(p->s >= 0.f && p->s <= 20.f)) return TG_ERR_INVALID_ARG;
+  if (p->window < 1 || (p->phi_mode != 0 && p->phi_mode != 1)) return TG_ERR_INVALID_ARG;
+  if (p->flags & ~TG_FLAG_QK_NORMALIZED) return TG_ERR_INVALID_ARG;
+  if (p->d_qk / p->H > 128) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+struct DecodeWs {
+  size_t S, z, ring_k, ring_g, w, fq, fk, inv, total;
+};
+DecodeWs decode_ws_layout(const tg_agg_params* p) {
+  const size_t B = p->B, H = p->H, W = p->window, d_h = p->d_qk / p->H;
+  DecodeWs L;
+  L.S = 0;
+  L.z = L.S + align256(B * d_h * p->m * 4);
+  L.ring_k = L.z + align256(B * H * d_h * 4);
+  L.ring_g = L.ring_k + align256(B * H * W * d_h * elem_size(p->dtype));
+  L.w = L.ring_g + align256(B * W * p->m * elem_size(p->dtype));
+  L.fq = L.w + align256(B * H * W * 4);
+  L.fk = L.fq + align256(B * H * d_h * 4);
+  L.inv = L.fk + align256(B * H * d_h * 4);
+  L.total = L.inv + align256(B * H * 4);
+  return L;
+}
+
 tg_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (need == 0) return TG_OK;
   if (!ws || ws_bytes < need) return TG_ERR_WORKSPACE;
@@ -350,6 +381,33 @@ tg_status tango_model_forward(const tg_model_params* p, const tg_model_weights* 
   return cuda_status(e);
 }
 
+tg_status wango_decode_step(const tg_agg_params* p, long long pos, const void* q, const void* k, const void* g,
+                            const void* v, void* out, void* state, size_t state_bytes, tg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  tg_status st = validate_decode(p);
+  if (st != TG_OK) return st;
+  if (pos < 0 || !q || !k || !g || !out) return TG_ERR_INVALID_ARG;
+  const DecodeWs L = decode_ws_layout(p);
+  st = check_ws(state, state_bytes, L.total);
+  if (st != TG_OK) return st;
+  char* base = static_cast<char*>(state);
+  if (pos == 0 && cudaMemsetAsync(state, 0, L.total, stream) != cudaSuccess) return TG_ERR_CUDA;
+  DecodeState ds;
+  ds.S = reinterpret_cast<float*>(base + L.S);
+  ds.z = reinterpret_cast<float*>(base + L.z);
+  ds.ring_k = base + L.ring_k;
+  ds.ring_g = base + L.ring_g;
+  ds.w = reinterpret_cast<float*>(base + L.w);
+  ds.fq = reinterpret_cast<float*>(base + L.fq);
+  ds.fk_leave = reinterpret_cast<float*>(base + L.fk);
+  ds.inv_den = reinterpret_cast<float*>(base + L.inv);
+  unsigned* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return TG_ERR_CUDA;
+  return cuda_status(launch_wango_decode(p->dtype, p->B, p->H, p->d_qk, p->m, p->window, pos, p->s, p->tau,
+                                         p->null_bias, p->phi_mode, (p->flags & TG_FLAG_QK_NORMALIZED) ? 1 : 0, q,
+                                         k, g, v, out, ds, err, stream));
+}
+
 size_t tg_workspace_size(int which, const void* params) {
   if (!params) return 0;
   if (which == TG_WS_TANGO || which == TG_WS_WANGO) {
@@ -361,6 +419,11 @@ size_t tg_workspace_size(int which, const void* params) {
     const tg_block_params* p = static_cast<const tg_block_params*>(params);
     if (validate_block(p) != TG_OK) return 0;
     return block_ws_layout(p).total;
+  }
+  if (which == TG_WS_DECODE) {
+    const tg_agg_params* p = static_cast<const tg_agg_params*>(params);
+    if (validate_decode(p) != TG_OK) return 0;
+    return decode_ws_layout(p).total;
   }
   if (which == TG_WS_MODEL) {
     const tg_model_params* p = static_cast<const tg_model_params*>(params);

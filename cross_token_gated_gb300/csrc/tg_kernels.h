@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "tango.h"
@@ -28,6 +29,26 @@ struct AggArgs {
 };
 
 enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
+
+// WANGO decode state (one buffer, regions 256-byte aligned): the running sums S
+// [B, H, d_h, m_h] and z [B, H, d_h] in f32, the ring of the last W tokens' unit k
+// [B, H, W, d_h] and g [B, W, m] (both in the storage type), and per-step scratch: the window
+// weights by ring slot [B, H, W], e^-tau phi(q~) and phi(k~_leave) [B, H, d_h], and
+// 1 / denominator [B, H].
+struct DecodeState {
+  float* S;
+  float* z;
+  void* ring_k;
+  void* ring_g;
+  float* w;
+  float* fq;
+  float* fk_leave;
+  float* inv_den;
+};
+cudaError_t launch_wango_decode(tg_dtype dt, int B, int H, int dqk, int m, int W, long long pos, float s,
+                                const float* tau, const float* null_bias, int phi_mode, int qk_normalized,
+                                const void* q, const void* k, const void* g, const void* v, void* out,
+                                const DecodeState& st, unsigned* err, cudaStream_t stream);
 
 // ---- CUDA-core kernels (simt.cu) -------------------------------------------
 // Per (row, head): optional RoPE at position row % T, then optional unit

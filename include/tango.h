@@ -6,6 +6,8 @@
  *   - tango_aggregate      sec. 2.1 eq. 5 with the full-prefix weights of sec. 2.2 eq. 6
  *   - wango_aggregate      sec. 2.1 eq. 5 with the windowed weights of sec. 2.2 eqs. 7-10
  *   - tango_block_forward  one block application, sec. 2.1 eqs. 2-3 around either of the above
+ *   - wango_decode_step    one autoregressive token of the windowed aggregation (eqs. 7-10)
+ *                          from a constant-size state
  *   - tango_model_forward  the language model of sec. 2.3: token embedding, the shared block
  *                          applied n times (eq. 11), final RMSNorm and tied logits; with
  *                          one weight set, or with the revision's gated-projection sets
@@ -67,6 +69,7 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 #define TG_WS_WANGO 1 /* params: const tg_agg_params*   */
 #define TG_WS_BLOCK 2 /* params: const tg_block_params* */
 #define TG_WS_MODEL 3 /* params: const tg_model_params* */
+#define TG_WS_DECODE 4 /* params: const tg_agg_params*: bytes of the wango_decode_step state */
 
 #define TG_MAX_HEADS 64
 
@@ -125,6 +128,29 @@ tg_status tango_aggregate(const tg_agg_params *p, const void *q, const void *k, 
 tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, const void *g,
                           const void *v, void *out, void *ws, size_t ws_bytes,
                           tg_stream_t stream);
+
+/*
+ * One autoregressive step of the windowed aggregation (sec. 2.2 eqs. 7-10) for B
+ * sequences that are all at position pos.  For destination i = pos the output equals row
+ * i of wango_aggregate over the sequence so far: window sources i-W < j <= i get
+ * e^{l_ij}, older sources enter through the running sums S = sum phi(k~_j) g_j^T and
+ * z = sum phi(k~_j) (eq. 10).
+ *   p         as for wango_aggregate; T is ignored; flags may hold TG_FLAG_QK_NORMALIZED
+ *   q, k      device [B, d_qk]: this token's query and key (unit-normalised per head
+ *             unless TG_FLAG_QK_NORMALIZED)
+ *   g, v      device [B, m]: this token's gate and feature; v may be NULL (out = gbar)
+ *   out       device [B, m], written
+ *   state     device buffer of tg_workspace_size(TG_WS_DECODE, p) bytes, 256-byte aligned,
+ *             owned by the caller and kept between steps: S and z in f32, a ring of the
+ *             last W tokens' unit k and g (storage type), and per-step scratch.  The call with pos == 0
+ *             clears it; steps must then come in order pos = 0, 1, 2, ...
+ * Requirements: d_h <= 128.  Arithmetic is fp32 for either storage type; the weights
+ * are not rounded to bf16.  The step reads the ring (W g vectors) and S, and rewrites
+ * S: it is bound by HBM bandwidth.
+ */
+tg_status wango_decode_step(const tg_agg_params *p, long long pos, const void *q, const void *k,
+                            const void *g, const void *v, void *out, void *state,
+                            size_t state_bytes, tg_stream_t stream);
 
 /* Weights of one block, all of the block's dtype, row-major [out, in]. */
 typedef struct {

@@ -174,3 +174,26 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         tg.load(build_if_missing=False)
     monkeypatch.undo()
+
+
+def test_decode_state_size_and_validation(lib):
+    """The decode state: S [B, d_h, m] and z in f32, the ring of W unit keys and gates
+    (storage type), and per-step scratch, each region 256-byte aligned."""
+    raw = tg.load()
+    B, H, dqk, m, W = 2, 2, 128, 512, 16
+    p = tg.agg_params(B, 1, H, dqk, m, dtype=tg.TG_BF16, window=W)
+    def a256(x):
+        return (x + 255) // 256 * 256
+    d_h = dqk // H
+    want = (a256(B * d_h * m * 4) + a256(B * H * d_h * 4) + a256(B * H * W * d_h * 2) + a256(B * W * m * 2)
+            + a256(B * H * W * 4) + 2 * a256(B * H * d_h * 4) + a256(B * H * 4))
+    assert tg.tg_workspace_size(tg.TG_WS_DECODE, p) == want
+    for bad in (dict(window=0), dict(phi_mode=3), dict(flags=tg.TG_FLAG_DEBUG_TIMEOUT)):
+        q = tg.agg_params(B, 1, H, dqk, m, dtype=tg.TG_BF16, **dict(dict(window=W), **bad))
+        assert tg.tg_workspace_size(tg.TG_WS_DECODE, q) == 0
+        assert raw.wango_decode_step(ctypes.byref(q), 0, 256, 256, 256, None, 256, None, 0, None) == \
+            tg.TG_ERR_INVALID_ARG
+    assert raw.wango_decode_step(ctypes.byref(p), -1, 256, 256, 256, None, 256, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    assert raw.wango_decode_step(ctypes.byref(p), 0, 256, 256, 256, None, 256, None, 0, None) == \
+        tg.TG_ERR_WORKSPACE

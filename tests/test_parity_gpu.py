@@ -305,3 +305,52 @@ def test_block_paper_head_geometry(mode):
     h64 = h.double().numpy()
     assert rel_err(out, ref) <= TOL["bf16"]
     assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ WANGO decode step
+
+def run_decode(q, k, g, v, H, W, **kw):
+    """Feeds the sequence one position at a time through wango_decode_step."""
+    B, T, dqk = q.shape
+    m = g.shape[-1]
+    qd, kd, gd = q.cuda(), k.cuda(), g.cuda()
+    vd = v.cuda() if v is not None else None
+    out = torch.empty_like(gd)
+    st = tg.decode_state(B, H, dqk, m, window=W, dtype=tg._dtype_code(gd))
+    step_out = torch.empty(B, m, dtype=gd.dtype, device="cuda")
+    for i in range(T):
+        tg.wango_decode_step(qd[:, i].contiguous(), kd[:, i].contiguous(), gd[:, i].contiguous(),
+                             vd[:, i].contiguous() if vd is not None else None, step_out, st, i, H=H, window=W,
+                             **kw)
+        out[:, i] = step_out
+    status, word = tg.tg_check_device_error()
+    assert status == tg.TG_OK, (status, hex(word))
+    return out
+
+
+@pytest.mark.parametrize("dtype,case", [
+    ("bf16", (2, 100, 2, 32, 256, 16)),
+    ("bf16", (1, 64, 2, 32, 256, 1)),      # W = 1: every earlier source is older
+    ("bf16", (2, 80, 2, 64, 144, 200)),    # W > T: no older prefix
+    ("bf16", (1, 600, 2, 128, 2048, 256)),  # the benchmark window, three steps of state
+    ("f32", (1, 50, 2, 32, 256, 7)),
+])
+def test_decode_steps_match_the_whole_sequence(dtype, case):
+    """T decode steps reproduce every row of WANGO over the whole sequence (the oracle's
+    running-sum evaluation of eq. 10)."""
+    B, T, H, dqk, m, W = case
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=21, dtype=dtype)
+    out = run_decode(q, k, g, v, H, W)
+    ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g, v)], H=H, tau=10.0, window=W)
+    assert rel_err(out, ref) <= TOL[dtype]
+
+
+def test_decode_null_gate_tau_array_and_gbar():
+    B, T, H, dqk, m, W = 2, 70, 2, 64, 256, 20
+    q, k, g, _ = synth.agg_inputs(B, T, dqk, m, seed=22, dtype="bf16")
+    tau = torch.tensor([3.0, 12.0], dtype=torch.float32)
+    nb = torch.tensor([-1.0, 0.5], dtype=torch.float32)
+    out = run_decode(q, k, g, None, H, W, tau=tau.cuda(), null_bias=nb.cuda(), phi_mode=1)
+    ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g)], None, H=H, tau=tau.numpy(), window=W,
+                            null_bias=nb.numpy(), phi_mode=1)
+    assert rel_err(out, ref) <= TOL["bf16"]
