@@ -121,9 +121,9 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   }
 }
 
-// grid (ceil(m / 256), B), 256 threads, one gate column per thread.
+// grid (ceil(m / 128), B), 128 threads, one gate column per thread.
 template <typename T>
-__global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a) {
+__global__ void __launch_bounds__(128) wango_decode_gate_kernel(const DecodeArgs<T> a) {
   const int bb = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= a.m) return;
@@ -136,19 +136,39 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
   const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * W * a.m + c;
   const float gi = io<T>::ld(a.g + (size_t)bb * a.m + c);
   const float* wv = a.st.w + (size_t)bh * W;
-  // window: the current token from its input, the others from the ring
-  float num = 0.f;
-  for (int s = 0; s < W; ++s) num = fmaf(wv[s], s == cur ? gi : io<T>::ld(ring_g + (size_t)s * a.m), num);
+  // window: the current token from its input, the others from the ring (four
+  // independent sums, so that many loads are in flight)
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int s = 0;
+#pragma unroll 2
+  for (; s + 4 <= W; s += 4) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float gv = s + e == cur ? gi : io<T>::ld(ring_g + (size_t)(s + e) * a.m);
+      acc[e] = fmaf(wv[s + e], gv, acc[e]);
+    }
+  }
+  for (; s < W; ++s) acc[0] = fmaf(wv[s], s == cur ? gi : io<T>::ld(ring_g + (size_t)s * a.m), acc[0]);
   // older prefix and the leaving source's update of S (after its read-out)
   float* S = a.st.S + (size_t)bh * d_h * a.m_h + cl;
   const float* fq = a.st.fq + (size_t)bh * d_h;
   const float* fkl = a.st.fk_leave + (size_t)bh * d_h;
   const float gl = lslot < 0 ? 0.f : (lslot == cur ? gi : io<T>::ld(ring_g + (size_t)lslot * a.m));
-  for (int d = 0; d < d_h; ++d) {
+  int d = 0;
+  for (; d + 4 <= d_h; d += 4) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float sv = S[(size_t)(d + e) * a.m_h];
+      acc[e] = fmaf(fq[d + e], sv, acc[e]);
+      if (lslot >= 0) S[(size_t)(d + e) * a.m_h] = fmaf(fkl[d + e], gl, sv);
+    }
+  }
+  for (; d < d_h; ++d) {
     const float sv = S[(size_t)d * a.m_h];
-    num = fmaf(fq[d], sv, num);
+    acc[0] = fmaf(fq[d], sv, acc[0]);
     if (lslot >= 0) S[(size_t)d * a.m_h] = fmaf(fkl[d], gl, sv);
   }
+  const float num = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   const float gbar = num * a.st.inv_den[bh];
   const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * a.m + c) : gbar;
   io<T>::st(a.out + (size_t)bb * a.m + c, u);
@@ -159,7 +179,7 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
 template <typename T>
 cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
   wango_decode_scores_kernel<T><<<dim3(a.H, a.B), 256, 0, s>>>(a);
-  wango_decode_gate_kernel<T><<<dim3((a.m + 255) / 256, a.B), 256, 0, s>>>(a);
+  wango_decode_gate_kernel<T><<<dim3((a.m + 127) / 128, a.B), 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
