@@ -168,15 +168,6 @@ __device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p
   }
 }
 
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t o_lo, uint32_t o_hi, uint32_t v, float inv, bool has_v) {
-  float y0 = __uint_as_float(o_lo) * inv, y1 = __uint_as_float(o_hi) * inv;
-  if (has_v) {
-    y0 *= bf16lo(v);
-    y1 *= bf16hi(v);
-  }
-  return pack_bf16x2(y0, y1);
-}
-
 // Ring position: stage index and the parity of its current phase.
 struct Ring {
   int stage = 0;
@@ -456,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
       const float inv = 1.f / den;
+      const uint64_t inv2 = f32x2_pack(inv, inv), zero2 = f32x2_pack(0.f, 0.f);
       tc_fence_after();
       const bool row_ok = i < a.T;
       const int rr = row & 63;
@@ -480,11 +472,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t addr = box + (uint32_t)((k ^ (rr & 7)) << 4);
           const uint4 vv = a.has_v ? ld_shared_v4(addr) : make_uint4(0, 0, 0, 0);
           const uint32_t* ok8 = &o[k >> 2][(k & 3) * 8];
+          // gbar = O / den in bf16 pairs (a packed f32x2 scale), then one bf16x2 product
+          // with v
+          uint32_t gq[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float y0, y1;
+            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(ok8[2 * e]), __uint_as_float(ok8[2 * e + 1])), inv2,
+                                   zero2),
+                         y0, y1);
+            gq[e] = pack_bf16x2(y0, y1);
+          }
           uint4 uu;
-          uu.x = mul_bf16x2(ok8[0], ok8[1], vv.x, inv, a.has_v);
-          uu.y = mul_bf16x2(ok8[2], ok8[3], vv.y, inv, a.has_v);
-          uu.z = mul_bf16x2(ok8[4], ok8[5], vv.z, inv, a.has_v);
-          uu.w = mul_bf16x2(ok8[6], ok8[7], vv.w, inv, a.has_v);
+          uu.x = a.has_v ? ptx::mul_bf16x2(gq[0], vv.x) : gq[0];
+          uu.y = a.has_v ? ptx::mul_bf16x2(gq[1], vv.y) : gq[1];
+          uu.z = a.has_v ? ptx::mul_bf16x2(gq[2], vv.z) : gq[2];
+          uu.w = a.has_v ? ptx::mul_bf16x2(gq[3], vv.w) : gq[3];
           if (!straddle) {
             st_shared_v4(addr, uu);
           } else if (row_ok && col0 + 8 * k < a.m_h) {
