@@ -11,9 +11,10 @@
 // (batch, head, gate tile), so every unit costs nI+1 source blocks and the units
 // of one gate tile, which share G and khat, run side by side out of L2.
 //
-//   warp 0       TMA: qhat tiles (2 buffers), khat blocks (2-stage ring), and one ring
-//                of 32 KB stages (5 of them) that carries, per tile, G in half blocks
-//                of 64 sources x 256 columns and then the tile's v (2 stages).
+//   warp 0       TMA: one ring of 32 KB stages (5 of them) that carries, per tile, G in
+//                half blocks of 64 sources x 256 columns and then the tile's v (2 stages).
+//   warp 3       TMA: qhat tiles (2 buffers) and khat blocks (2-stage ring), in a thread of
+//                their own so that score loads never wait behind the G ring.
 //   warps 1, 2   MMA issue, one thread each on two SM sub-partitions (J counts source
 //                blocks over all tiles of the CTA):
 //                  warp 2: S_J = Qhat Khat_J^T (M=128, N=128, K=d_h) -> TMEM slot J % 2,
@@ -26,7 +27,8 @@
 //                mask on the diagonal block, rounded to bf16; the ROUNDED weights are
 //                summed into the row's denominator; P (bf16) is written back over S
 //                once both warpgroups have read their scores.
-//   warps 12-15  epilogue: O / den from TMEM times v from shared memory; u is written
+//   warps 12-15  epilogue: O / den from TMEM in bf16 pairs, times v from shared memory
+//                (a bf16x2 product); u is written
 //                over v in shared memory and stored by TMA, while the softmax warps
 //                already work on the next tile.  (A 64-column box that straddles the
 //                end of a head's gate columns is written directly instead.)
@@ -229,12 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = b.tmem_base;
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ TMA producer
-    Ring kr, gr;
+    // ------------------------------------------------------------ TMA: G and v
+    Ring gr;
     bool ok = true;
-    uint32_t qmask = 0, kmask = 0, gmask = 0, qph[kQBufs] = {}, kph[kKStages] = {}, gph[kGStages] = {};
+    uint32_t gmask = 0, gph[kGStages] = {};
     TileSeq seq;
-    int tc = 0;
     auto ring_load = [&](const CUtensorMap* map, int x, int y, int bb) -> bool {
       if (!wait_bar(&b.g_empty[gr.stage], gr.phase ^ 1, b, a)) return false;
       uint8_t* dst = sG + gr.stage * kGStage;
@@ -250,6 +251,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       gr.next(kGStages);
       return true;
     };
+    for (bool have = seq.first(a); ok && have; have = seq.next(a)) {
+      const Tile& t = seq.t;
+      const int i0 = t.ib * kBlk;
+      const int gx = t.head * a.m_h + t.n0;
+      for (int j = 0; ok && j <= t.ib; ++j)
+        for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, j * kBlk + h * kHalf, t.b);
+      // the tile's v, rows [i0, i0+64) and [i0+64, i0+128), for the epilogue
+      for (int h = 0; ok && h < 2; ++h) ok = ring_load(a.has_v ? &tmV : nullptr, gx, i0 + h * kHalf, t.b);
+    }
+    // Copies still in flight land before the CTA exits.
+    for (int s = 0; s < kGStages; ++s)
+      if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
+  } else if (warp == 3 && lane == 0) {
+    // ------------------------------------------------------------ TMA: qhat and khat
+    // (a thread of its own, so that score loads never queue behind the G ring)
+    Ring kr;
+    bool ok = true;
+    uint32_t qmask = 0, kmask = 0, qph[kQBufs] = {}, kph[kKStages] = {};
+    TileSeq seq;
+    int tc = 0;
     for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
       const Tile& t = seq.t;
       const int i0 = t.ib * kBlk, qb = tc & 1;
@@ -259,7 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sQ + qb * kQKMax, &tmQ, &b.q_full[qb], t.head * a.d_h, i0, t.b);
       qmask |= 1u << qb;
       qph[qb] = qp;
-      const int gx = t.head * a.m_h + t.n0;
       for (int j = 0; ok && j <= t.ib; ++j) {
         if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
         mbar_arrive_expect_tx(&b.k_full[kr.stage], qk_bytes);
@@ -267,18 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         kmask |= 1u << kr.stage;
         kph[kr.stage] = kr.phase;
         kr.next(kKStages);
-        for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, j * kBlk + h * kHalf, t.b);
       }
-      // the tile's v, rows [i0, i0+64) and [i0+64, i0+128), for the epilogue
-      for (int h = 0; ok && h < 2; ++h) ok = ring_load(a.has_v ? &tmV : nullptr, gx, i0 + h * kHalf, t.b);
     }
-    // Copies still in flight land before the CTA exits.
     for (int s = 0; s < kQBufs; ++s)
       if (qmask & (1u << s)) mbar_wait(&b.q_full[s], qph[s], a.timeout_ns);
     for (int s = 0; s < kKStages; ++s)
       if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
-    for (int s = 0; s < kGStages; ++s)
-      if (gmask & (1u << s)) mbar_wait(&b.g_full[s], gph[s], a.timeout_ns);
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------------------ MMA issue: scores
     // S_J = Qhat Khat_J^T into slot J % 2 once the P.G of block J - 2 (the slot's
