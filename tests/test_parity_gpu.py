@@ -354,3 +354,15 @@ def test_decode_null_gate_tau_array_and_gbar():
     ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g)], None, H=H, tau=tau.numpy(), window=W,
                             null_bias=nb.numpy(), phi_mode=1)
     assert rel_err(out, ref) <= TOL["bf16"]
+
+
+def test_wango_segments_hand_over_the_state():
+    """160 gate strips for 152 SMs and 8 destination blocks: the launcher splits every
+    strip into four segments of two blocks, and each later segment starts from the state
+    its predecessor hands over through global memory.  Every row compared against the
+    oracle's running sums."""
+    B, T, H, dqk, m, W = 1, 1024, 2, 128, 20480, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=31, dtype="bf16")
+    out = run_agg("wango", q, k, g, v, H, W)
+    ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g, v)], H=H, tau=10.0, window=W)
+    assert rel_err(out, ref) <= TOL["bf16"]
