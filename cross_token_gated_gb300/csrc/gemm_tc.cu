@@ -10,7 +10,8 @@
 //   warp 0      TMA producer (4-stage ring of 128x64 A and 256x64 B tiles, 128B swizzle)
 //   warp 1      TMEM allocator and MMA issuer (128x256x16 tcgen05.mma, one thread)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, fused elementwise, bf16 out:
-//               g and v through shared memory and TMA stores (64-column chunks),
+//               g and v through shared memory and TMA stores (64-column chunks,
+//               L2 evict-first),
 //               q/k and the residual output by direct stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile overlap the
 // main loop of the next.  Every wait is bounded; on expiry the kernel records a
@@ -34,6 +35,7 @@ constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kOutBytes = BM * 64 * 2;  // 16 KB: one 128 x 64 bf16 output chunk (staging for TMA)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kPrefetch = 8;  // output GEMM: u boxes asked into L2 this many k-blocks ahead
 
 enum Seg : int { kSegQK = 0, kSegG = 1, kSegV = 2, kSegOut = 3 };
 
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(dB, mb, &b.full[stage], k0, tl.nb * BN);
         }
         tma_load_2d(dA, &tmA, &b.full[stage], k0, tl.mb * BM);
+        // u comes from HBM, further ahead than the 4 stages reach: ask for it into L2 early
+        if (tl.seg == kSegOut && kb + kPrefetch < nkb) tma_prefetch_l2_2d(&tmA, k0 + kPrefetch * BK, tl.mb * BM);
         issued_mask |= 1 << stage;
         issued_phase[stage] = phase;
         if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -304,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (issuer) {
-            tma_store_2d(om, sOut + ob * kOutBytes, n0 + c0, tl.mb * BM);  // rows past M are clipped
+            // rows past M are clipped; g and v stream out evict-first, so x and the
+            // weights stay in L2 for the other tiles
+            tma_store_2d_hint(om, sOut + ob * kOutBytes, n0 + c0, tl.mb * BM, l2_evict_first());
             bulk_commit_group();
           }
           ob ^= 1;

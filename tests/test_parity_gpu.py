@@ -179,6 +179,20 @@ def test_block_bf16_small(mode, shape):
     assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_block_output_gemm_many_tiles(mode):
+    """d=1024 and B*T=5000 rows give 40 row blocks of 4 output tiles, 160 tiles for 152
+    SMs: the persistent output GEMM takes a second tile on some CTAs, with K = m = 256
+    (4 k-blocks a tile).  Every row is compared, the last row block being ragged (8 rows)."""
+    B, T, d, dqk, m, H, W = 2, 2500, 1024, 128, 256, 2, 100
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=11, dtype="bf16")
+    out = run_block(h, w, H, mode, W)
+    ref = ref_block(h, w, H, mode, W)
+    h64 = h.double().numpy()
+    assert rel_err(out, ref) <= TOL["bf16"]
+    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+
+
 def test_block_70m_shape_sampled_sequences():
     """The benchmarked configuration (B=8, T=2048, d=512, m=28480, q/k width 128, TANGO,
     bf16): sequences 0 and 7 compared in full against the oracle."""
