@@ -9,7 +9,7 @@
 // Two kernels per step:
 //   wango_decode_scores_kernel  per (head, batch): unit q and k, the window weights, the
 //       feature maps, the denominator, z's update and the ring's khat slot.
-//   wango_decode_gate_kernel    per 256 gate columns and batch (HBM-bound): the window
+//   wango_decode_gate_kernel    per 128 gate columns and batch (HBM-bound): the window
 //       sum over the ring of g, the older-prefix read-out from S, u = gbar * v, the
 //       leaving token's rank-1 update of S and the ring's g slot.
 #include <math.h>
@@ -58,6 +58,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 template <typename T>
 __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeArgs<T> a) {
   __shared__ float qh[kMaxDh], kh[kMaxDh], red[8];
+  __shared__ __align__(16) unsigned char kstage[32768];  // a chunk of the ring's keys
   const int head = blockIdx.x, bb = blockIdx.y, t = threadIdx.x;
   const int d_h = a.d_h, W = a.W;
   const long long i = a.pos;
@@ -90,20 +91,40 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   __syncthreads();
   if (t < d_h) io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
   __syncthreads();
-  // window weights, one ring slot per thread: slot s holds source j = the largest j <= i
-  // with j = s (mod W)
+  // window weights: the ring's keys pass through shared memory in chunks (one coalesced
+  // copy each), then one ring slot per thread; slot s holds source j = the largest
+  // j <= i with j = s (mod W).  The dot product starts at column s (mod d_h), so the
+  // threads of a warp read different banks.
   float* wv = a.st.w + (size_t)bh * W;
+  T* ks = reinterpret_cast<T*>(kstage);
+  const int per = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
   float wsum = 0.f;
-  for (int s = t; s < W; s += blockDim.x) {
-    const long long j = i - (long long)((cur - s + W) % W);
-    float w = 0.f;
-    if (j >= 0) {
-      float dot = 0.f;
-      for (int c = 0; c < d_h; ++c) dot = fmaf(qh[c], io<T>::ld(ring_k + (size_t)s * d_h + c), dot);
-      w = expf(tau * (dot - 1.f));
+  for (int s0 = 0; s0 < W; s0 += per) {
+    const int n = min(per, W - s0);
+    const T* src = ring_k + (size_t)s0 * d_h;
+    const size_t bytes = (size_t)n * d_h * sizeof(T);
+    __syncthreads();  // the previous chunk has been read
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && bytes % 16 == 0) {
+      for (size_t x = t; x < bytes / 16; x += blockDim.x)
+        reinterpret_cast<uint4*>(kstage)[x] = reinterpret_cast<const uint4*>(src)[x];
+    } else {
+      for (int x = t; x < n * d_h; x += blockDim.x) ks[x] = src[x];
     }
-    wv[s] = w;
-    wsum += w;
+    __syncthreads();
+    for (int sl = t; sl < n; sl += blockDim.x) {
+      const int s = s0 + sl;
+      const long long j = i - (long long)((cur - s + W) % W);
+      float w = 0.f;
+      if (j >= 0) {
+        const T* kr = ks + (size_t)sl * d_h;
+        float dot = 0.f;
+        for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1)
+          dot = fmaf(qh[c], io<T>::ld(kr + c), dot);
+        w = expf(tau * (dot - 1.f));
+      }
+      wv[s] = w;
+      wsum += w;
+    }
   }
   wsum = block_sum(wsum, red);
   // older prefix: e^-tau phi(q~) . z, then z += phi(k~_leave)
@@ -121,65 +142,164 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   }
 }
 
-// grid (ceil(m / 128), B), 128 threads, one gate column per thread.
-template <typename T>
-__global__ void __launch_bounds__(128) wango_decode_gate_kernel(const DecodeArgs<T> a) {
-  const int bb = blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= a.m) return;
-  const int head = c / a.m_h, cl = c % a.m_h;
-  const int bh = bb * a.H + head, d_h = a.d_h, W = a.W;
+// Gate kernel layout: a CTA takes 128 gate columns of one sequence as 16 groups of 8
+// columns, and its 256 threads split each group's work 16 ways ("slices"): slice r sums
+// the ring slots r, r + 16, ... and the state rows r, r + 16, ...  The slices' partial
+// sums meet in shared memory.  A thread moves 8 columns at a time (16-byte loads of
+// bf16, two of f32) when every row pitch and base allows it and no group straddles a
+// head; otherwise it takes its 8 columns one by one.
+constexpr int kGateCols = 128, kGroup = 8, kSlices = 16;
+
+template <typename T, bool VEC>
+struct Cols8 {
+  // the 8 columns [c0, c0 + 8) of row p (columns at or past `lim` read as 0)
+  static __device__ __forceinline__ void ld(const T* p, int c0, int lim, float* x) {
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) x[e] = c0 + e < lim ? io<T>::ld(p + c0 + e) : 0.f;
+  }
+};
+template <>
+struct Cols8<__nv_bfloat16, true> {
+  static __device__ __forceinline__ void ld(const __nv_bfloat16* p, int c0, int, float* x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + c0);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = __uint_as_float(w[e] << 16);
+      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+};
+template <>
+struct Cols8<float, true> {
+  static __device__ __forceinline__ void ld(const float* p, int c0, int, float* x) {
+    const float4 u = *reinterpret_cast<const float4*>(p + c0), v = *reinterpret_cast<const float4*>(p + c0 + 4);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+  }
+};
+template <bool VEC>
+__device__ __forceinline__ void ld_f32x8(const float* p, int c0, int lim, float* x) {
+  Cols8<float, VEC>::ld(p, c0, lim, x);
+}
+template <bool VEC>
+__device__ __forceinline__ void st_f32x8(float* p, int c0, int lim, const float* x) {
+  if (VEC) {
+    *reinterpret_cast<float4*>(p + c0) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(p + c0 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e)
+      if (c0 + e < lim) p[c0 + e] = x[e];
+  }
+}
+
+// grid (ceil(m / 128), B), 256 threads.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a) {
+  __shared__ float red[kSlices][kGateCols + 4];
+  const int bb = blockIdx.y, grp = threadIdx.x % kSlices, sl = threadIdx.x / kSlices;
+  const int col0 = blockIdx.x * kGateCols, d_h = a.d_h, W = a.W, m = a.m;
+  const int c0 = col0 + grp * kGroup;  // first of this thread's 8 columns
   const long long i = a.pos;
   const int cur = (int)(i % W);
   const long long jl = i - W + 1;
   const int lslot = jl >= 0 ? (int)(jl % W) : -1;
-  const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * W * a.m + c;
-  const float gi = io<T>::ld(a.g + (size_t)bb * a.m + c);
-  const float* wv = a.st.w + (size_t)bh * W;
-  // window: the current token from its input, the others from the ring (four
-  // independent sums, so that many loads are in flight)
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int s = 0;
+  const T* gin = a.g + (size_t)bb * m;
+  const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * W * m;
+  float acc[kGroup];
+#pragma unroll
+  for (int e = 0; e < kGroup; ++e) acc[e] = 0.f;
+  if (c0 < m) {
+    // the head of the group's first column; with VEC the whole group shares it, and
+    // otherwise each column takes its own head below
+    const int head0 = c0 / a.m_h;
+    const int lim = m;
+    // window: ring slots sl, sl + 16, ...; the current token's slot from the input
+    float x[kGroup];
 #pragma unroll 2
-  for (; s + 4 <= W; s += 4) {
+    for (int s = sl; s < W; s += kSlices) {
+      Cols8<T, VEC>::ld(s == cur ? gin : ring_g + (size_t)s * m, c0, lim, x);
+      if (VEC) {
+        const float w = a.st.w[(size_t)(bb * a.H + head0) * W + s];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float gv = s + e == cur ? gi : io<T>::ld(ring_g + (size_t)(s + e) * a.m);
-      acc[e] = fmaf(wv[s + e], gv, acc[e]);
+        for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const int hd = min(c0 + e, m - 1) / a.m_h;
+          acc[e] = fmaf(a.st.w[(size_t)(bb * a.H + hd) * W + s], x[e], acc[e]);
+        }
+      }
+    }
+    // older prefix: rows sl, sl + 16, ... of S, read out and then updated by the source
+    // that leaves the window
+    float gl[kGroup];
+    if (lslot >= 0) Cols8<T, VEC>::ld(lslot == cur ? gin : ring_g + (size_t)lslot * m, c0, lim, gl);
+#pragma unroll 1
+    for (int d = sl; d < d_h; d += kSlices) {
+      if (VEC) {
+        const size_t bh = (size_t)bb * a.H + head0;
+        float* Srow = a.st.S + (bh * d_h + d) * a.m_h;
+        const int cl = c0 - head0 * a.m_h;
+        float sv[kGroup];
+        ld_f32x8<true>(Srow, cl, a.m_h, sv);
+        const float fq = a.st.fq[bh * d_h + d];
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(fq, sv[e], acc[e]);
+        if (lslot >= 0) {
+          const float fk = a.st.fk_leave[bh * d_h + d];
+#pragma unroll
+          for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, gl[e], sv[e]);
+          st_f32x8<true>(Srow, cl, a.m_h, sv);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const int c = c0 + e;
+          if (c >= m) break;
+          const int hd = c / a.m_h;
+          const size_t bh = (size_t)bb * a.H + hd;
+          float* sp = a.st.S + (bh * d_h + d) * a.m_h + (c - hd * a.m_h);
+          const float sv = *sp;
+          acc[e] = fmaf(a.st.fq[bh * d_h + d], sv, acc[e]);
+          if (lslot >= 0) *sp = fmaf(a.st.fk_leave[bh * d_h + d], gl[e], sv);
+        }
+      }
     }
   }
-  for (; s < W; ++s) acc[0] = fmaf(wv[s], s == cur ? gi : io<T>::ld(ring_g + (size_t)s * a.m), acc[0]);
-  // older prefix and the leaving source's update of S (after its read-out)
-  float* S = a.st.S + (size_t)bh * d_h * a.m_h + cl;
-  const float* fq = a.st.fq + (size_t)bh * d_h;
-  const float* fkl = a.st.fk_leave + (size_t)bh * d_h;
-  const float gl = lslot < 0 ? 0.f : (lslot == cur ? gi : io<T>::ld(ring_g + (size_t)lslot * a.m));
-  int d = 0;
-  for (; d + 4 <= d_h; d += 4) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float sv = S[(size_t)(d + e) * a.m_h];
-      acc[e] = fmaf(fq[d + e], sv, acc[e]);
-      if (lslot >= 0) S[(size_t)(d + e) * a.m_h] = fmaf(fkl[d + e], gl, sv);
+  for (int e = 0; e < kGroup; ++e) red[sl][grp * kGroup + e] = acc[e];
+  __syncthreads();
+  // one column per thread: the slices' sums, the denominator, u = gbar * v, and the
+  // current token's g into its ring slot
+  if (threadIdx.x < kGateCols) {
+    const int c = col0 + threadIdx.x;
+    if (c < m) {
+      float num = 0.f;
+#pragma unroll
+      for (int r = 0; r < kSlices; ++r) num += red[r][threadIdx.x];
+      const int hd = c / a.m_h;
+      const float gbar = num * a.st.inv_den[bb * a.H + hd];
+      const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * m + c) : gbar;
+      io<T>::st(a.out + (size_t)bb * m + c, u);
+      io<T>::st(const_cast<T*>(ring_g) + (size_t)cur * m + c, io<T>::ld(gin + c));
     }
   }
-  for (; d < d_h; ++d) {
-    const float sv = S[(size_t)d * a.m_h];
-    acc[0] = fmaf(fq[d], sv, acc[0]);
-    if (lslot >= 0) S[(size_t)d * a.m_h] = fmaf(fkl[d], gl, sv);
-  }
-  const float num = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-  const float gbar = num * a.st.inv_den[bh];
-  const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * a.m + c) : gbar;
-  io<T>::st(a.out + (size_t)bb * a.m + c, u);
-  // the current token's g into its ring slot
-  io<T>::st(const_cast<T*>(ring_g) + (size_t)cur * a.m, gi);
 }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 template <typename T>
 cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
   wango_decode_scores_kernel<T><<<dim3(a.H, a.B), 256, 0, s>>>(a);
-  wango_decode_gate_kernel<T><<<dim3((a.m + 127) / 128, a.B), 128, 0, s>>>(a);
+  // 8-column vectors when every row of g, the ring and S starts 16-byte aligned and no
+  // 8-column group straddles a head
+  const bool vec = (a.m * sizeof(T)) % 16 == 0 && a.m_h % kGroup == 0 && aligned16(a.g) &&
+                   aligned16(a.st.ring_g) && aligned16(a.st.S);
+  const dim3 grid((a.m + kGateCols - 1) / kGateCols, a.B);
+  if (vec) wango_decode_gate_kernel<T, true><<<grid, 256, 0, s>>>(a);
+  else wango_decode_gate_kernel<T, false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
