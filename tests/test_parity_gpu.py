@@ -348,6 +348,11 @@ def run_decode(q, k, g, v, H, W, **kw):
     ("bf16", (2, 80, 2, 64, 144, 200)),    # W > T: no older prefix
     ("bf16", (1, 600, 2, 128, 2048, 256)),  # the benchmark window, three steps of state
     ("f32", (1, 50, 2, 32, 256, 7)),
+    # per-column gate path: 8-column groups straddle heads (the paper's m_h = 1,780), an
+    # odd bf16 width with unaligned rows, an fp32 width that is no multiple of 8
+    ("bf16", (2, 90, 2, 64, 3560, 40)),
+    ("bf16", (1, 50, 2, 32, 206, 12)),
+    ("f32", (1, 60, 2, 32, 150, 9)),
 ])
 def test_decode_steps_match_the_whole_sequence(dtype, case):
     """T decode steps reproduce every row of WANGO over the whole sequence (the oracle's
