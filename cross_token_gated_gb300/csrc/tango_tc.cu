@@ -28,10 +28,12 @@
 //                summed into the row's denominator; P (bf16) is written back over S
 //                once both warpgroups have read their scores.
 //   warps 12-15  epilogue: O / den from TMEM in bf16 pairs, times v from shared memory
-//                (a bf16x2 product); u is written
-//                over v in shared memory and stored by TMA, while the softmax warps
-//                already work on the next tile.  (A 64-column box that straddles the
-//                end of a head's gate columns is written directly instead.)
+//                (a bf16x2 product); u is written over v in shared memory, 64 columns at
+//                a time, and each row half (two warps) stores its box by TMA as soon as
+//                the chunk is done, so the stores overlap the next chunks and each ring
+//                stage is freed by its own half.  The softmax warps meanwhile work on the
+//                next tile.  (A 64-column box that straddles the end of a head's gate
+//                columns is written directly instead.)
 // TMEM: O in columns [0, 256), S[0] in [256, 384), S[1] in [384, 512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -432,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t otm = tmem + kColO + ((uint32_t)(quarter * 32) << 16);
-    const bool issuer = (warp == kEpiWarp0 && lane == 0);
+    const int hh = quarter >> 1;  // row half: rows [64 hh, 64 hh + 64), ring stage sa or sb
+    const bool hissuer = lane == 0 && (warp & 1) == 0;
     bool ok = true;
     uint32_t ophase = 0;
     int gpos = 0;  // ring stages consumed so far (G and v)
@@ -508,24 +511,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_global_v4(a.out + grow + col0 + 8 * k, uu.x, uu.y, uu.z, uu.w);
           }
         }
-      }
-      // u is in shared memory; one thread stores the whole 64-column boxes.
-      fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      if (issuer) {
-        for (int h = 0; h < 2; ++h) {
-          const int y = t.ib * kBlk + h * kHalf;
-          if (y >= a.T) continue;
-          for (int cq = 0; cq < 4; ++cq) {
-            const int col0 = t.n0 + cq * 64;
-            if (col0 + 64 > a.m_h) continue;
-            tma_store_3d(&tmU, sG + (h == 0 ? sa : sb) * kGStage + cq * kGBox, t.head * a.m_h + col0, y, t.b);
-          }
+        // this chunk of u is in shared memory: each row half stores its box now, so the
+        // stores overlap the next chunks
+        fence_proxy_async_smem();
+        named_bar_sync(3 + hh, 64);
+        if (hissuer) {
+          const int y = t.ib * kBlk + hh * kHalf;
+          if (y < a.T && !straddle && col0 + 64 <= a.m_h)
+            tma_store_3d(&tmU, sG + (hh == 0 ? sa : sb) * kGStage + cq * kGBox, t.head * a.m_h + col0, y, t.b);
+          bulk_commit_group();
         }
-        bulk_commit_group();
+      }
+      // the row half's stage is free once its stores have read it
+      if (hissuer) {
         bulk_wait_group_read0();
-        mbar_arrive(&b.g_empty[sa]);
-        mbar_arrive(&b.g_empty[sb]);
+        mbar_arrive(&b.g_empty[hh == 0 ? sa : sb]);
       }
     }
   }
