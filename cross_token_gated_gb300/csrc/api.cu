@@ -268,9 +268,11 @@ tg_status wango_aggregate(const tg_agg_params* p, const void* q, const void* k, 
   return aggregate(true, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
-tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* w, const void* h, void* h_out,
-                              void* ws, size_t ws_bytes, tg_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+// The block forward; with pad_weights false the workspace already holds this weight
+// set's per-head padded W_g, W_v, W_o (the model forward's consecutive applications of
+// one set).
+static tg_status block_forward(const tg_block_params* p, const tg_block_weights* w, const void* h, void* h_out,
+                               void* ws, size_t ws_bytes, cudaStream_t stream, bool pad_weights) {
   tg_status st = validate_block(p);
   if (st != TG_OK) return st;
   if (!w || !w->rms_gamma || !w->Wq || !w->Wk || !w->Wg || !w->Wv || !w->Wo || !h || !h_out)
@@ -324,10 +326,12 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
   const void *Wg = w->Wg, *Wv = w->Wv, *Wo = w->Wo;
   if (L.padded) {  // each head's gate rows (W_g, W_v) and columns (W_o) at the padded pitch
     const int m_h = p->agg.m / ap.H, m_hp = ap.m / ap.H;
-    e = launch_pad_gate(ap.dtype, w->Wg, base + L.wg, ap.m, d, 0, ap.H, m_h, m_hp, stream);
-    if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wv, base + L.wv, ap.m, d, 0, ap.H, m_h, m_hp, stream);
-    if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wo, base + L.wo, d, ap.m, 1, ap.H, m_h, m_hp, stream);
-    if (e != cudaSuccess) return TG_ERR_CUDA;
+    if (pad_weights) {
+      e = launch_pad_gate(ap.dtype, w->Wg, base + L.wg, ap.m, d, 0, ap.H, m_h, m_hp, stream);
+      if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wv, base + L.wv, ap.m, d, 0, ap.H, m_h, m_hp, stream);
+      if (e == cudaSuccess) e = launch_pad_gate(ap.dtype, w->Wo, base + L.wo, d, ap.m, 1, ap.H, m_h, m_hp, stream);
+      if (e != cudaSuccess) return TG_ERR_CUDA;
+    }
     Wg = base + L.wg;
     Wv = base + L.wv;
     Wo = base + L.wo;
@@ -343,6 +347,11 @@ tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* 
   if (e != cudaSuccess) return TG_ERR_CUDA;
   e = launch_out_tc(vb, Wo, h, h_out, M, d, ap.m, a.err, stream);
   return cuda_status(e);
+}
+
+tg_status tango_block_forward(const tg_block_params* p, const tg_block_weights* w, const void* h, void* h_out,
+                              void* ws, size_t ws_bytes, tg_stream_t stream) {
+  return block_forward(p, w, h, h_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 tg_status tango_model_forward(const tg_model_params* p, const tg_model_weights* w, const int* ids, void* logits,
@@ -367,8 +376,11 @@ tg_status tango_model_forward(const tg_model_params* p, const tg_model_weights* 
   // h^(0): token embeddings (the tied matrix)
   if (launch_embed(ap.dtype, ids, w->embedding, h, BT, d, p->vocab, err, stream) != cudaSuccess) return TG_ERR_CUDA;
   // eq. 11: h^(r+1) = Block(h^(r)), in place
+  // (a set's padded gate weights stay in the block workspace while the next application
+  // uses the same set)
   for (int r = 0; r < p->n_apps; ++r) {
-    st = tango_block_forward(&p->block, &w->sets[set_of(p, r)], h, h, bws, L.total - L.block, stream_);
+    const bool new_set = r == 0 || set_of(p, r) != set_of(p, r - 1);
+    st = block_forward(&p->block, &w->sets[set_of(p, r)], h, h, bws, L.total - L.block, stream, new_set);
     if (st != TG_OK) return st;
   }
   // final RMSNorm, then logits against the tied embedding: x E^T

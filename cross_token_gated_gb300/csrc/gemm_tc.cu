@@ -45,7 +45,8 @@ struct GemmArgs {
   int nb_qk, nb_g, nb_v, nb_out;  // n-blocks per segment (projection: 1, g, g, 0; output: 0, 0, 0, n)
   int m_major;        // tile order: 1 = m-block outer (output GEMM), 0 = n-block outer
   int T, H, dqk, m, d;
-  double inv_freq[32];  // RoPE frequencies base^(-2c/d_h)
+  // RoPE frequencies over pi, base^(-2c/d_h) / pi, as float pairs hi + lo
+  float rope_hi[32], rope_lo[32];
   int rope;
   __nv_bfloat16 *q, *k, *g, *v;
   const __nv_bfloat16* h;
@@ -120,11 +121,14 @@ __device__ __forceinline__ void rope_norm_store(uint32_t taddr, __nv_bfloat16* d
   if (a.rope) {
 #pragma unroll
     for (int c = 0; c < DH / 2; ++c) {
-      // angle in double, reduced to [-pi, pi] before the fp32 sincos
-      double th = (double)t * a.inv_freq[c];
-      th -= 6.283185307179586 * rint(th * 0.15915494309189535);
+      // angle / pi = t (hi + lo).  t * hi is kept exactly as its rounded product p plus
+      // the product's error pe; whole turns (even multiples) leave p exactly; sincospi
+      // then sees the angle to fp32 precision at any position t < 2^24
+      const float tf = (float)t, p = tf * a.rope_hi[c];
+      const float pe = fmaf(tf, a.rope_hi[c], -p);
+      const float turn = (p - 2.f * rintf(0.5f * p)) + (pe + tf * a.rope_lo[c]);
       float sn, cs;
-      sincosf((float)th, &sn, &cs);
+      sincospif(turn, &sn, &cs);
       const float x1 = x[c], x2 = x[c + DH / 2];
       x[c] = x1 * cs - x2 * sn;
       x[c + DH / 2] = x1 * sn + x2 * cs;
@@ -405,7 +409,11 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m; a.d = p.d;
   const int d_h = p.dqk / p.H;
   a.rope = p.rope_base > 0.f;
-  for (int c = 0; c < 32; ++c) a.inv_freq[c] = c < d_h / 2 ? pow((double)p.rope_base, -2.0 * c / d_h) : 0.0;
+  for (int c = 0; c < 32; ++c) {
+    const double g = c < d_h / 2 ? pow((double)p.rope_base, -2.0 * c / d_h) / 3.141592653589793 : 0.0;
+    a.rope_hi[c] = (float)g;
+    a.rope_lo[c] = (float)(g - (double)a.rope_hi[c]);
+  }
   a.q = static_cast<__nv_bfloat16*>(p.q);
   a.k = static_cast<__nv_bfloat16*>(p.k);
   a.g = static_cast<__nv_bfloat16*>(p.g);

@@ -432,20 +432,61 @@ __global__ void embed_kernel(const int* ids, const T* E, T* h, long long rows, i
 // pitch of m_hp (>= m_h) entries, zeros after it.  axis 0: src [H*m_h, C] -> dst
 // [H*m_hp, C] (W_g, W_v); axis 1: src [R, H*m_h] -> dst [R, H*m_hp] (W_o).  R, C are
 // the destination's extents.  A plain element copy; no arithmetic.
+// Destination rows blockIdx.y, + gridDim.y, ...; each thread takes 8 consecutive
+// destination elements (2048 per block along a row), written as one 16-byte vector when
+// `vec` (row pitch and bases allow it).  W_g/W_v rows copy whole source rows; a W_o row
+// gathers each head's columns, whose source offsets need not be aligned.
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
 template <typename T>
-__global__ void pad_gate_kernel(const T* src, T* dst, long long R, long long C, int axis, int H, int m_h,
-                                int m_hp) {
-  const long long n = R * C;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
-    const long long r = e / C, c = e % C;
-    const long long gi = axis == 0 ? r : c;  // padded gate index
-    const int head = (int)(gi / m_hp), j = (int)(gi % m_hp);
-    T x = T(0.f);
-    if (j < m_h) {
-      const long long sg = (long long)head * m_h + j;  // unpadded gate index
-      x = axis == 0 ? src[sg * C + c] : src[r * ((long long)H * m_h) + sg];
+__device__ __forceinline__ void store8(T* p, const T* v, int n, bool vec) {
+  if (vec && n == 8) {
+    static_assert(sizeof(T) == 2 || sizeof(T) == 4, "element size");
+    if constexpr (sizeof(T) == 2) {
+      *reinterpret_cast<uint4*>(p) =
+          make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    } else {
+      *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
-    dst[e] = x;
+  } else {
+    for (int e = 0; e < n; ++e) p[e] = v[e];
+  }
+}
+template <typename T>
+__global__ void __launch_bounds__(256) pad_gate_kernel(const T* src, T* dst, int R, int C, int axis, int H,
+                                                       int m_h, int m_hp, bool vec) {
+  const int c = (blockIdx.x * 256 + threadIdx.x) * 8;
+  if (c >= C) return;
+  const int n = C - c < 8 ? C - c : 8;
+  for (int r = blockIdx.y; r < R; r += gridDim.y) {
+    T v[8];
+    if (axis == 0) {
+      // the whole row comes from one source row, or is zero
+      const int head = r / m_hp, j = r - head * m_hp;
+      const T* srow = src + ((size_t)head * m_h + (j < m_h ? j : 0)) * C;
+      if (vec && n == 8 && j < m_h) {
+        *reinterpret_cast<uint4*>(dst + (size_t)r * C + c) = *reinterpret_cast<const uint4*>(srow + c);
+        if (sizeof(T) == 4)
+          *reinterpret_cast<uint4*>(dst + (size_t)r * C + c + 4) = *reinterpret_cast<const uint4*>(srow + c + 4);
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = (e < n && j < m_h) ? srow[c + e] : T(0.f);
+    } else {
+      const T* srow = src + (size_t)r * ((size_t)H * m_h);
+      int head = c / m_hp, j = c - head * m_hp;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[e] = (e < n && j < m_h) ? srow[head * m_h + j] : T(0.f);
+        if (++j == m_hp) {
+          j = 0;
+          ++head;
+        }
+      }
+    }
+    store8(dst + (size_t)r * C + c, v, n, vec);
   }
 }
 
@@ -464,15 +505,19 @@ cudaError_t launch_embed(tg_dtype dt, const int* ids, const void* E, void* h, lo
 
 cudaError_t launch_pad_gate(tg_dtype dt, const void* src, void* dst, long long R, long long C, int axis, int H,
                             int m_h, int m_hp, cudaStream_t s) {
-  const long long n = R * C;
-  const long long want = (n + 255) / 256;
-  const unsigned blocks = (unsigned)(want < 4096 ? (want > 0 ? want : 1) : 4096);
+  if (R * C == 0) return cudaSuccess;
+  if (R > 0x7fffffffLL || C > 0x7fffffffLL - 2048) return cudaErrorInvalidValue;
+  const size_t es = dt == TG_F32 ? 4 : 2;
+  const bool vec = ((size_t)C * es) % 16 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  const dim3 grid((unsigned)((C + 2047) / 2048), (unsigned)(R < 65535 ? R : 65535));  // 2048 elements per block
   if (dt == TG_F32)
-    pad_gate_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(src), static_cast<float*>(dst), R, C,
-                                                  axis, H, m_h, m_hp);
+    pad_gate_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(src), static_cast<float*>(dst), (int)R,
+                                                (int)C, axis, H, m_h, m_hp, vec);
   else
-    pad_gate_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
-                                                          static_cast<__nv_bfloat16*>(dst), R, C, axis, H, m_h, m_hp);
+    pad_gate_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
+                                                        static_cast<__nv_bfloat16*>(dst), (int)R, (int)C, axis, H,
+                                                        m_h, m_hp, vec);
   return cudaGetLastError();
 }
 
