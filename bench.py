@@ -63,6 +63,19 @@ def dist_env():
     return rank, world, local
 
 
+def job_rate(local_ms: float, units_per_rank: float, world: int, device) -> tuple:
+    """The job's step time and rate: every rank does `units_per_rank` per step and the job
+    is as slow as its slowest rank, so the step time is the maximum over ranks (one
+    all-reduce when world > 1) and the rate counts every rank's units."""
+    import torch
+    t = torch.tensor([local_ms], device=device, dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * units_per_rank / (ms_max * 1e-3)
+
+
 def measured_traffic(kernel: str, source: str, B_: int, T_: int):
     """DRAM bytes per launch of `kernel` at (B_, T_) from the committed ncu summary
     profiles/traffic.json, or None when there is none or the kernel's source has
@@ -271,11 +284,7 @@ def main():
         barrier()
     ms = e0.elapsed_time(e1) / args.steps
     clocks = clk.summary()
-    t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * B * T / (ms_max * 1e-3)
+    ms_max, value = job_rate(ms, B * T, world, dev)
     st, word = tg.tg_check_device_error(stream)
     if st != tg.TG_OK:
         raise RuntimeError(f"device error in timed region: {tg.status_string(st)} ({word:#x})")
@@ -369,10 +378,7 @@ def main():
     barrier()
     if not torch.equal(o_host[(args.steps - 1) % 2].to(dev), out):
         raise RuntimeError("pipelined e2e result differs from the plain step")
-    t = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e = {"value": world * B * T / (float(t.item()) * 1e-3), "unit": "tokens/s",
+    e2e = {"value": job_rate(e2e_ms, B * T, world, dev)[1], "unit": "tokens/s",
            "h2d_bytes_per_step": h_host.numel() * 2, "d2h_bytes_per_step": o_host[0].numel() * 2,
            "copies": "second stream, double-buffered, overlapping the neighbouring steps"}
 
