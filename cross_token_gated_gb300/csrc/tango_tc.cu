@@ -17,16 +17,19 @@
 //                their own so that score loads never wait behind the G ring.
 //   warps 1, 2   MMA issue, one thread each on two SM sub-partitions (J counts source
 //                blocks over all tiles of the CTA):
-//                  warp 2: S_J = Qhat Khat_J^T (M=128, N=128, K=d_h) -> TMEM slot J % 2,
-//                          once the P.G of block J - 2 has completed;
-//                  warp 1: O += P_J G_J (M=128, N=256, K=64 x 2), A = P_J from TMEM;
-//                          warp 1 also allocates TMEM.
+//                  warp 2: S_J = Qhat Khat_J^T (M=128, N=128, K=d_h) -> the TMEM score
+//                          slot, once the softmax warps have read S_{J-1} out of it;
+//                  warp 1: O += P_J G_J (M=128, N=256, K=64 x 2), A = P_J from TMEM P
+//                          slot J % 2; warp 1 also allocates TMEM.
 //                Both keep descriptors in registers and avoid compiler memory barriers.
 //   warps 4-11   softmax: warpgroup w takes columns [64w, 64w+64) of every score block;
 //                one row per thread from TMEM, exp2(tau log2e (s - 1)) with the causal
 //                mask on the diagonal block, rounded to bf16; the ROUNDED weights are
-//                summed into the row's denominator; P (bf16) is written back over S
-//                once both warpgroups have read their scores.
+//                summed into the row's denominator.  Once both warpgroups have read
+//                S_J the score slot is released for S_{J+1}, and P_J (bf16) goes to P
+//                slot J % 2 once the P.G of block J - 2 has completed.  Scores and P
+//                thus have slots of their own, so S_{J+1} enters the tensor pipe ahead
+//                of P.G(J) instead of behind P.G(J+1).
 //   warps 12-15  epilogue: O / den from TMEM in bf16 pairs, times v from shared memory
 //                (a bf16x2 product); u is written over v in shared memory, 64 columns at
 //                a time, and each row half (two warps) stores its box by TMA as soon as
@@ -34,7 +37,8 @@
 //                stage is freed by its own half.  The softmax warps meanwhile work on the
 //                next tile.  (A 64-column box that straddles the end of a head's gate
 //                columns is written directly instead.)
-// TMEM: O in columns [0, 256), S[0] in [256, 384), S[1] in [384, 512).
+// TMEM: O in columns [0, 256), the score slot in [256, 384), P slots (bf16 pairs, 64
+// columns each) in [384, 448) and [448, 512).
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
 #include "tg_tc.h"
@@ -56,15 +60,15 @@ constexpr int kSoftWarp0 = 4, kEpiWarp0 = 12;
 constexpr uint32_t kQKMax = kBlk * 64 * 2;     // 16 KB at d_h = 64
 constexpr uint32_t kGBox = kHalf * 64 * 2;     // 8 KB: 64 rows x 64 columns
 constexpr uint32_t kGStage = 4 * kGBox;        // 32 KB
-constexpr uint32_t kColO = 0, kColS0 = 256;
+constexpr uint32_t kColO = 0, kColS0 = 256, kColP0 = 384;
 
 struct __align__(8) Bars {
   uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t g_full[kGStages], g_empty[kGStages];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full, s_free, p_full[2];
   uint64_t o_full, o_empty, den_full, den_empty;
-  uint64_t slot_free[2];                         // the P.G of a slot's block has completed
+  uint64_t p_free[2];                            // the P.G of a P slot's block has completed
   uint64_t drain[2], never;
   uint32_t tmem_base;
   int abort;
@@ -207,16 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b.g_full[s], 1);
       mbar_init(&b.g_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], 8);
-    }
+    mbar_init(&b.s_full, 1);
+    mbar_init(&b.s_free, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&b.p_full[i], 8);
     mbar_init(&b.o_full, 1);
     mbar_init(&b.o_empty, 4);
     mbar_init(&b.den_full, 8);
     mbar_init(&b.den_empty, 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&b.slot_free[i], 1);
+      mbar_init(&b.p_free[i], 1);
       mbar_init(&b.drain[i], 1);
     }
     mbar_init(&b.never, 1);
@@ -297,8 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kmask & (1u << s)) mbar_wait(&b.k_full[s], kph[s], a.timeout_ns);
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------------------ MMA issue: scores
-    // S_J = Qhat Khat_J^T into slot J % 2 once the P.G of block J - 2 (the slot's
-    // previous user) has completed.
+    // S_J = Qhat Khat_J^T into the score slot once the softmax warps have read S_{J-1}.
     const uint32_t idesc_s = idesc_bf16_f32(kBlk, kBlk, false, false);
     const uint32_t lay = qk_layout(a.d_h);
     const uint32_t sbo = 8u * a.d_h * 2u;
@@ -318,15 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd = qdesc0 + (uint64_t)((qb * kQKMax) >> 4);
       const int nj = seq.t.ib + 1;
       for (int j = 0; j < nj; ++j, ++J) {
-        if (J >= 2 && !(ok = wait_bar(&b.slot_free[J & 1], ((J - 2) >> 1) & 1, b, a))) break;
+        if (J >= 1 && !(ok = wait_bar(&b.s_free, (J - 1) & 1, b, a))) break;
         if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
         tc_fence_after_nc();
         const uint64_t kd = kdesc0 + (uint64_t)((kr.stage * kQKMax) >> 4);
-        const uint32_t stm = tmem + kColS0 + (J & 1) * 128;
+        const uint32_t stm = tmem + kColS0;
         for (int kk = 0; kk < ksteps; ++kk)
           mma_bf16_ss_nc(stm, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), idesc_s, kk != 0);
         mma_commit_nc(&b.k_empty[kr.stage]);
-        mma_commit_nc(&b.s_full[J & 1]);
+        mma_commit_nc(&b.s_full);
         kr.next(kKStages);
         if (j == nj - 1) mma_commit_nc(&b.q_empty[qb]);
       }
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar(&b.o_empty, ophase ^ 1, b, a))) break;
           ophase ^= 1;
         }
-        const uint32_t ptm = tmem + kColS0 + buf * 128;
+        const uint32_t ptm = tmem + kColP0 + buf * 64;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (!(ok = wait_bar(&b.g_full[gr.stage], gr.phase, b, a))) break;
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           gr.next(kGStages);
         }
         if (!ok) break;
-        mma_commit_nc(&b.slot_free[buf]);
+        mma_commit_nc(&b.p_free[buf]);
       }
       if (!ok) break;
       mma_commit_nc(&b.o_full);
@@ -395,22 +397,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nj = t.ib + 1;
       for (int j = 0; j < nj; ++j, ++J) {
         const uint32_t buf = J & 1;
-        const uint32_t stm = tmem + kColS0 + buf * 128 + lane_off;
+        const uint32_t stm = tmem + kColS0 + lane_off;
+        const uint32_t pw = tmem + kColP0 + buf * 64 + lane_off;
         uint32_t r[2][32];
-        if (ok) ok = wait_bar(&b.s_full[buf], (J >> 1) & 1, b, a);
+        if (ok) ok = wait_bar(&b.s_full, J & 1, b, a);
         if (ok) {
           tc_fence_after();
           tmem_ld32(stm + wg * 64, r[0]);
           tmem_ld32(stm + wg * 64 + 32, r[1]);
           tmem_ld_wait();
         }
-        // P overwrites the first half of the buffer: both warpgroups must have read
-        // their scores first.  The barrier also ANDs their status.
+        // this block's P slot is free once the P.G of block J - 2 has completed
+        if (ok && J >= 2) ok = wait_bar(&b.p_free[buf], ((J - 2) >> 1) & 1, b, a);
+        tc_fence_before();
+        // both warpgroups have read their scores: the S slot takes the next block's.
+        // The barrier also ANDs their status.
         ok = named_bar_and(1, 256, ok);
         if (!ok) break;
+        if (warp == kSoftWarp0 && lane == 0) mbar_arrive(&b.s_free);
+        tc_fence_after();
         const int src0 = (j - t.ib) * kBlk + wg * 64;  // relative to the destination block
-        if (src0 + 63 > 0) softmax64<true>(r, stm + wg * 32, c, row, src0, dsum2);
-        else softmax64<false>(r, stm + wg * 32, c, row, src0, dsum2);
+        if (src0 + 63 > 0) softmax64<true>(r, pw + wg * 32, c, row, src0, dsum2);
+        else softmax64<false>(r, pw + wg * 32, c, row, src0, dsum2);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
