@@ -148,7 +148,7 @@ __device__ __forceinline__ uint32_t qk_layout(int d_h) {
 
 // 64 scores of one row (columns [64w, 64w+64) of a block): weights exp2(c (s - 1)),
 // with sources after the destination zeroed on the diagonal block, rounded to bf16
-// and written as P at TMEM columns [32w, 32w+32) of the score buffer; the rounded
+// and written as P at TMEM columns [32w, 32w+32) of the block's P slot; the rounded
 // weights are added to two partial denominators, each a pair of f32.  The exponent
 // argument and the sums use packed f32x2 arithmetic (two values per instruction).
 template <bool kDiag>
