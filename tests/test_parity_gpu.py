@@ -193,6 +193,20 @@ def test_block_output_gemm_many_tiles(mode):
     assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_block_160m_tier_widths(mode):
+    """The 160M tier's widths (d=768, F=52,176; H=2 heads of 64, m_h=26,088, W=256), one
+    sequence of 300 tokens compared in full: K = 768 in the projection, three 256-column
+    tiles in the output GEMM, 102 gate tiles per head in the aggregation."""
+    B, T, d, dqk, m, H, W = 1, 300, 768, 128, 52176, 2, 256
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=13, dtype="bf16")
+    out = run_block(h, w, H, mode, W)
+    ref = ref_block(h, w, H, mode, W)
+    h64 = h.double().numpy()
+    assert rel_err(out, ref) <= TOL["bf16"]
+    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+
+
 def test_block_70m_shape_sampled_sequences():
     """The benchmarked configuration (B=8, T=2048, d=512, m=28480, q/k width 128, TANGO,
     bf16): sequences 0 and 7 compared in full against the oracle."""
