@@ -16,6 +16,22 @@ def test_exports_every_declared_function(lib):
         assert hasattr(raw, n), f"library does not export {n}"
 
 
+def test_exports_no_undeclared_c_function(lib):
+    """The C ABI is exactly the header: every exported function with C linkage (an
+    unmangled name) is declared in include/tango.h; internal helpers stay internal."""
+    import shutil
+    import subprocess
+
+    from cross_token_gated_gb300 import build
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm is not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True).stdout
+    c_funcs = {parts[2] for parts in (line.split() for line in out.splitlines())
+               if len(parts) == 3 and parts[1] == "T" and not parts[2].startswith("_Z")}
+    assert c_funcs == set(tg.declared_functions())
+
+
 def test_status_strings(lib):
     for st in range(7):
         assert tg.status_string(st)
