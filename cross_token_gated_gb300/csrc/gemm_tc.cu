@@ -7,12 +7,14 @@
 //
 // C[M, N] = A[M, K] * B[N, K]^T with both operands K-major bf16, fp32 accumulation
 // in tensor memory.  Persistent kernel, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer (4-stage ring of 128x64 A and 256x64 B tiles, 128B swizzle)
+//   warp 0      TMA producer (4-stage ring of 128x64 A and 256x64 B tiles, 128B swizzle);
+//               in the output GEMM it also asks u's box 8 k-blocks ahead into L2
 //   warp 1      TMEM allocator and MMA issuer (128x256x16 tcgen05.mma, one thread)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, fused elementwise, bf16 out:
 //               g and v through shared memory and TMA stores (64-column chunks,
 //               L2 evict-first),
-//               q/k and the residual output by direct stores
+//               q/k (RoPE angles in fp32 with an exact turn reduction) and the
+//               residual output by direct stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile overlap the
 // main loop of the next.  Every wait is bounded; on expiry the kernel records a
 // timeout in the error word and all roles leave their loops.
