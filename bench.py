@@ -50,6 +50,9 @@ def parse():
                     help="only run one aggregation kernel (for profiler captures)")
     ap.add_argument("--block-only", action="store_true",
                     help="only run the block forward at batch --agg-B (for profiler captures)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only run WANGO decode steps (W=256) for --agg-B sequences: W + --agg-iters "
+                         "steps (for profiler captures)")
     ap.add_argument("--agg-B", type=int, default=2)
     ap.add_argument("--agg-T", type=int, default=2048)
     ap.add_argument("--agg-iters", type=int, default=3)
@@ -236,6 +239,9 @@ def main():
         return
     if args.block_only:
         run_block_only(args)
+        return
+    if args.decode_only:
+        run_decode_only(args)
         return
     import torch
     import torch.distributed as dist
@@ -487,6 +493,33 @@ def run_agg_only(args):
     dt = (time.perf_counter() - t0) / args.agg_iters
     print(json.dumps({"agg_only": args.agg_only, "B": b, "T": t_len, "status": st, "word": word,
                       "wall_ms_per_launch": dt * 1e3}))
+    if st != tg.TG_OK:
+        sys.exit(1)
+
+
+def run_decode_only(args):
+    """W + --agg-iters WANGO decode steps (W = 256) for --agg-B sequences, so that the last
+    steps run at steady state; prints one timing line for those last steps."""
+    import torch
+
+    import cross_token_gated_gb300 as tg
+    from cross_token_gated_gb300 import synth
+    dev = torch.device("cuda", 0)
+    b, W = args.agg_B, 256
+    q, k, g, v = (x[:, 0].contiguous().to(dev) for x in synth.agg_inputs(b, 1, DQK, M, seed=0, dtype="bf16"))
+    out = torch.empty_like(g)
+    st_buf = tg.decode_state(b, H, DQK, M, window=W, dtype=tg.TG_BF16, device=dev)
+    for pos in range(W):
+        tg.wango_decode_step(q, k, g, v, out, st_buf, pos, H=H, window=W)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for pos in range(W, W + args.agg_iters):
+        tg.wango_decode_step(q, k, g, v, out, st_buf, pos, H=H, window=W)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.agg_iters
+    st, word = tg.tg_check_device_error()
+    print(json.dumps({"decode_only": True, "B": b, "W": W, "status": st, "word": word,
+                      "wall_us_per_step": dt * 1e6}))
     if st != tg.TG_OK:
         sys.exit(1)
 
