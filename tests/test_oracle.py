@@ -155,6 +155,71 @@ def test_wango_zero_scale_closed_form(phi_mode, W):
         assert rel(fn(q, k, g, None, H=H, tau=0.0, window=W, phi_mode=phi_mode), expect) < 1e-13
 
 
+def _axis_heads(B, T, H, d_h, axis, sign):
+    """Every token's head vector is sign * e_axis (already a unit vector)."""
+    x = np.zeros((B, T, H, d_h))
+    x[..., axis] = sign
+    return x.reshape(B, T, H * d_h)
+
+
+@pytest.mark.parametrize("phi_mode", [0, 1])
+@pytest.mark.parametrize("W", [1, 2, 5])
+def test_wango_phi_at_positive_scale_closed_form(phi_mode, W):
+    """tau > 0 with q_hat = -e_0 and k_hat = e_1 in every head and token: every cosine is
+    0, so each window weight is exp(0) = 1, and every older weight is the feature-map dot
+    product of eqs. 8-9 at u = sqrt(tau) q_hat and w = sqrt(tau) k_hat, expanded here by
+    hand (u_0 = -sqrt(tau) takes ELU's negative branch e^u - 1, w_1 = +sqrt(tau) the
+    identity branch, every other coordinate is 0):
+      eq. 8:  [(e^-r + eps)(1 + eps) + (1 + eps)(r + 1 + eps) + (d_h - 2)(1 + eps)^2] / d_h
+      elu+1:   e^-r + (r + 1) + (d_h - 2)
+    with r = sqrt(tau).  Two heads with different tau fix the per-head sqrt(tau); a
+    scaled q/k fixes the unit normalisation in front of it."""
+    B, T, H, d_h, m = 1, 7, 2, 4, 6
+    eps = 1e-4
+    taus = [10.0, 2.25]
+    q = _axis_heads(B, T, H, d_h, 0, -3.0)     # normalised to -e_0 inside the oracle
+    k = _axis_heads(B, T, H, d_h, 1, 0.5)      # normalised to +e_1
+    g = rnd((B, T, m), 31)
+    m_h = m // H
+    expect = np.empty_like(g)
+    for a, tau in enumerate(taus):
+        r = np.sqrt(tau)
+        if phi_mode == 0:
+            c = ((np.exp(-r) + eps) * (1 + eps) + (1 + eps) * (r + 1 + eps)
+                 + (d_h - 2) * (1 + eps) ** 2) / d_h
+        else:
+            c = np.exp(-r) + (r + 1) + (d_h - 2)
+        ga = g[..., a * m_h:(a + 1) * m_h]
+        for i in range(T):
+            lo = max(0, i - W + 1)
+            num = ga[:, lo:i + 1].sum(axis=1) + c * ga[:, :lo].sum(axis=1)
+            expect[:, i, a * m_h:(a + 1) * m_h] = num / ((i + 1 - lo) + c * lo)
+    for fn in (oracle.wango_direct, oracle.wango_scan):
+        got = fn(q, k, g, None, H=H, tau=taus, window=W, phi_mode=phi_mode)
+        assert rel(got, expect) < 1e-13
+    # the older weight differs from both the window weight and the tau = 0 weight, so
+    # the case really exercises it
+    assert W < T
+
+
+def test_wango_phi_negative_branch_pin():
+    """One more hand value for ELU's negative branch: q_hat = -e_0, k_hat = -e_0 (cosine
+    1, so the window weight is e^tau), tau = 4, d_h = 4, eq. 8.  The older weight is
+    [(e^-2 + eps)^2 + 3 (1 + eps)^2] / 4 (both vectors on the negative branch)."""
+    B, T, H, d_h, m = 1, 3, 1, 4, 2
+    eps, tau = 1e-4, 4.0
+    q = _axis_heads(B, T, H, d_h, 0, -1.0)
+    k = _axis_heads(B, T, H, d_h, 0, -1.0)
+    g = rnd((B, T, m), 32)
+    c = ((np.exp(-2.0) + eps) ** 2 + 3 * (1 + eps) ** 2) / 4
+    wwin = np.exp(tau)
+    # W = 1: row 2 has source 2 in the window and sources 0, 1 older
+    expect2 = (wwin * g[0, 2] + c * (g[0, 0] + g[0, 1])) / (wwin + 2 * c)
+    for fn in (oracle.wango_direct, oracle.wango_scan):
+        got = fn(q, k, g, None, H=H, tau=tau, window=1, phi_mode=0)
+        assert rel(got[0, 2], expect2) < 1e-13
+
+
 def test_phi_mode_readings_differ():
     """Guard: the eq. 8 feature map and the literal elu + 1 are different rules."""
     B, T, H, dqk, m = 1, 10, 2, 8, 4
