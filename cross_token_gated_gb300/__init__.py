@@ -234,21 +234,22 @@ TG_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def block_params(B, T, d, H, d_qk, m, *, dtype, mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None,
-                 window=1, phi_mode=0, rms_eps=1e-6, rope_base=10000.0) -> tg_block_params:
+                 window=1, phi_mode=0, rms_eps=1e-6, rope_base=10000.0, flags=0) -> tg_block_params:
     return tg_block_params(agg_params(B, T, H, d_qk, m, dtype=dtype, s=s, tau=tau, null_bias=null_bias,
-                                      window=window, phi_mode=phi_mode), int(d), int(mode), float(rms_eps),
-                           float(rope_base))
+                                      window=window, phi_mode=phi_mode, flags=flags), int(d), int(mode),
+                           float(rms_eps), float(rope_base))
 
 
 def tango_block_forward(h, weights, h_out, *, H, mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None,
-                        window=1, phi_mode=0, rms_eps=1e-6, rope_base=10000.0, ws=None, stream=None):
+                        window=1, phi_mode=0, rms_eps=1e-6, rope_base=10000.0, flags=0, ws=None, stream=None):
     """One block application (eqs. 2-10).  h, h_out [B, T, d]; weights: dict with gamma,
-    Wq, Wk, Wg, Wv, Wo device tensors of h's dtype.  h_out may be h."""
+    Wq, Wk, Wg, Wv, Wo device tensors of h's dtype.  h_out may be h.  flags: 0, or
+    TG_FLAG_DEBUG_TIMEOUT (the projection GEMM's test hook)."""
     B, T, d = h.shape
     d_qk, m = weights["Wq"].shape[0], weights["Wg"].shape[0]
     p = block_params(B, T, d, H, d_qk, m, dtype=_dtype_code(h), mode=mode, s=s, tau=tau,
                      null_bias=null_bias, window=window, phi_mode=phi_mode, rms_eps=rms_eps,
-                     rope_base=rope_base)
+                     rope_base=rope_base, flags=flags)
     w = tg_block_weights(*[_ptr(weights[n]) for n in ("gamma", "Wq", "Wk", "Wg", "Wv", "Wo")])
     need = load().tg_workspace_size(TG_WS_BLOCK, ctypes.byref(p))
     wbuf = _workspace(need, h.device, ws)

@@ -119,7 +119,7 @@ tg_status validate_block(const tg_block_params* p) {
   const tg_agg_params a = block_agg(p);
   tg_status st = validate_agg(&a, p->mode == TG_MODE_WANGO);
   if (st != TG_OK) return st;
-  if (p->agg.flags != 0) return TG_ERR_INVALID_ARG;
+  if (p->agg.flags & ~TG_FLAG_DEBUG_TIMEOUT) return TG_ERR_INVALID_ARG;
   if (p->d < 1 || !(p->rms_eps > 0.f) || !(p->rope_base >= 0.f)) return TG_ERR_INVALID_ARG;
   if (p->mode != TG_MODE_TANGO && p->mode != TG_MODE_WANGO) return TG_ERR_INVALID_ARG;
   if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
@@ -341,6 +341,7 @@ static tg_status block_forward(const tg_block_params* p, const tg_block_weights*
   pa.q = qb; pa.k = kb; pa.g = gb; pa.v = vb;
   pa.M = M; pa.d = d; pa.T = ap.T; pa.H = ap.H; pa.dqk = ap.d_qk; pa.m = ap.m;
   pa.rope_base = p->rope_base; pa.err = a.err;
+  pa.debug_timeout = (p->agg.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
   e = launch_proj_tc(pa, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
   e = p->mode == TG_MODE_WANGO ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream);

@@ -17,7 +17,9 @@
 //               residual output by direct stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile overlap the
 // main loop of the next.  Every wait is bounded; on expiry the kernel records a
-// timeout in the error word and all roles leave their loops.
+// timeout in the error word and all roles leave their loops.  A test hook
+// (debug_timeout) makes the MMA issuer wait first on a barrier that nothing signals,
+// with a 1 ms bound, to exercise that path.
 #include <math.h>
 
 #include "tg_common.cuh"
@@ -54,10 +56,12 @@ struct GemmArgs {
   const __nv_bfloat16* h;
   __nv_bfloat16* h_out;
   unsigned* err;
+  uint64_t timeout_ns;  // bound of every wait
+  int debug_timeout;    // test hook: the MMA issuer first waits on a barrier nothing signals
 };
 
 struct __align__(8) Bars {
-  uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
+  uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -93,11 +97,11 @@ __device__ __forceinline__ Tile tile_of(const GemmArgs& a, int t) {
   return r;
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, unsigned* err) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars& b, const GemmArgs& a) {
   if (*(volatile int*)&b.abort) return false;
-  if (mbar_wait(bar, parity, kTimeoutNs)) return true;
+  if (mbar_wait(bar, parity, a.timeout_ns)) return true;
   *(volatile int*)&b.abort = 1;
-  record_error(err, kErrTimeout | kKernGemm);
+  record_error(a.err, kErrTimeout | kKernGemm);
   return false;
 }
 
@@ -172,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b.acc_empty[i], 4);
     }
     mbar_init(&b.drain, 1);
+    mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(a, t);
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!wait_bar(&b.empty[stage], phase ^ 1, b, a.err)) goto producer_done;
+        if (!wait_bar(&b.empty[stage], phase ^ 1, b, a)) goto producer_done;
         uint8_t* dA = sA + stage * kABytes;
         uint8_t* dB = sB + stage * kBBytes;
         const int k0 = kb * BK;
@@ -229,16 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const bool hooked = a.debug_timeout && !wait_bar(&b.never, 0, b, a);  // nothing ever arrives there
+    for (int t = blockIdx.x; !hooked && t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(a, t);
       const int N = (tl.seg == kSegQK && a.nb_qk == 1) ? 2 * a.dqk : BN;
       const uint32_t idesc = idesc_bf16_f32(BM, N, false, false);
-      if (!wait_bar(&b.acc_empty[acc], acc_phase ^ 1, b, a.err)) break;
+      if (!wait_bar(&b.acc_empty[acc], acc_phase ^ 1, b, a)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BN;
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!wait_bar(&b.full[stage], phase, b, a.err)) { ok = false; break; }
+        if (!wait_bar(&b.full[stage], phase, b, a)) { ok = false; break; }
         tc_fence_after();
         const uint32_t aaddr = smem_u32(sA + stage * kABytes), baddr = smem_u32(sB + stage * kBBytes);
 #pragma unroll
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(a, t);
-      bool ok = wait_bar(&b.acc_full[acc], acc_phase, b, a.err);
+      bool ok = wait_bar(&b.acc_full[acc], acc_phase, b, a);
       // the four epilogue warps agree (they meet at named barriers below)
       if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
@@ -421,6 +427,8 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   a.g = static_cast<__nv_bfloat16*>(p.g);
   a.v = static_cast<__nv_bfloat16*>(p.v);
   a.err = p.err;
+  a.debug_timeout = p.debug_timeout;
+  a.timeout_ns = p.debug_timeout ? 1000000ull : kTimeoutNs;
   return launch(mA, mq, mk, mg, mv, mog, mov, a, s);
 }
 
@@ -440,6 +448,7 @@ cudaError_t launch_matmul_tc(const void* A, const void* B, void* C, int M, int N
   a.T = 1; a.H = 1; a.m = N; a.d = 0;
   a.v = static_cast<__nv_bfloat16*>(C);
   a.err = err;
+  a.timeout_ns = kTimeoutNs;
   return launch(mA, mB, mB, mB, mB, mC, mC, a, s);
 }
 
@@ -458,6 +467,7 @@ cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_
   a.h = static_cast<const __nv_bfloat16*>(h);
   a.h_out = static_cast<__nv_bfloat16*>(h_out);
   a.err = err;
+  a.timeout_ns = kTimeoutNs;
   return launch(mA, mo, mo, mo, mo, mo, mo, a, s);
 }
 

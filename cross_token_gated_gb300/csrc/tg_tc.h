@@ -14,6 +14,7 @@ struct ProjArgs {
   int M, d, T, H, dqk, m;
   float rope_base;
   unsigned* err;
+  int debug_timeout;  // test hook: the GEMM times out on purpose (1 ms bound)
 };
 
 cudaError_t launch_proj_tc(const ProjArgs& a, cudaStream_t s);

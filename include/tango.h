@@ -30,6 +30,10 @@
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   - Calls are thread-safe with respect to each other; concurrent calls that share
  *     a workspace race.
+ *   - The library runs in each device's primary context (the CUDA runtime's); the
+ *     device address of the error word is looked up once per device and kept, so
+ *     cudaDeviceReset, or a non-primary context made current through the driver API,
+ *     is not supported.
  */
 #ifndef TANGO_GB300_H
 #define TANGO_GB300_H
@@ -56,9 +60,12 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 
 /* tg_agg_params.flags */
 #define TG_FLAG_QK_NORMALIZED 0x1u  /* q and k are already unit vectors per head */
-#define TG_FLAG_DEBUG_TIMEOUT 0x100u /* test hook: bf16 kernels wait on a barrier that is
-                                        never signalled, with a ~1 ms limit, and return
-                                        TG_ERR_TIMEOUT through tg_check_device_error() */
+#define TG_FLAG_DEBUG_TIMEOUT 0x100u /* test hook: a bf16 kernel waits on a barrier that is
+                                        never signalled, with a ~1 ms limit, and returns
+                                        TG_ERR_TIMEOUT through tg_check_device_error().
+                                        tango_aggregate: the TANGO kernel; wango_aggregate:
+                                        the gate-strip kernel; tango_block_forward (the
+                                        only flag a block accepts): the projection GEMM */
 
 /* tango_block_forward mode */
 #define TG_MODE_TANGO 0
@@ -164,7 +171,7 @@ typedef struct {
 
 /*
  * Block parameters: agg gives B, T, H, d_qk, m, s/tau, null_bias, window, phi_mode,
- * dtype (agg.flags must be 0).  d: residual width.  mode: TG_MODE_TANGO or
+ * dtype (agg.flags must be 0 or TG_FLAG_DEBUG_TIMEOUT).  d: residual width.  mode: TG_MODE_TANGO or
  * TG_MODE_WANGO.  rms_eps: RMSNorm epsilon (> 0).  rope_base: RoPE base (0 = no
  * RoPE); rotate-half pairing (c, c + d_h/2), positions 0..T-1 per sequence.
  */
@@ -259,7 +266,9 @@ tg_status tango_model_forward(const tg_model_params *p, const tg_model_weights *
  *     nothing; for bf16 that is B*T*d_qk > 4,194,304.
  *   - The first call on each device looks up the array's device address with that
  *     device current (cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *     capture.  The address is kept for the life of the process and belongs to the
+ *     device's primary context (the one the CUDA runtime uses): cudaDeviceReset, or a
+ *     non-primary context made current through the driver API, is not supported.
  *   - Every call on a device shares the one array and keeps the last call's contents;
  *     each call overwrites the part it reads before reading it, so nothing has to be
  *     cleared between calls.  Calls whose kernels overlap on the GPU (different

@@ -1,10 +1,30 @@
 """Parity of the CUDA path with the fp64 oracle, element by element, on seeded inputs.
 
-Tolerances (stated for the path): max |gpu - oracle| / max |oracle| per output tensor
-must be <= 1e-4 for fp32 storage (CUDA-core fp32 arithmetic) and <= 2e-2 for bf16
-storage (bf16 tensor-core operands, fp32 accumulation).  The oracle reads exactly the
-values the GPU reads (bf16 inputs are widened, not re-rounded).
+Bounds, checked by `check` on every output tensor (the oracle reads exactly the values
+the GPU reads: bf16 inputs are widened, not re-rounded):
+- normwise: max |gpu - oracle| / max |oracle| <= TOL, i.e. 1e-4 for fp32 storage (CUDA
+  core fp32 arithmetic) and 2e-2 for bf16 storage (bf16 tensor-core operands, fp32
+  accumulation);
+- per row and head (the gate columns of one head in one output row): the same ratio
+  within each, <= 2 TOL.  A row holds far fewer elements than the tensor, so its
+  largest value sits closer to its typical ones; this keeps an error confined to rows
+  or heads of small magnitude from hiding behind the tensor's largest values;
+- element-wise, for aggregation outputs: |gpu - oracle| / scale <= COND_TOL, where
+  scale = sum_j alpha_ij |g_j| |v_i| is the oracle's own aggregation of |g| and |v|
+  (the weights alpha do not depend on g).  A weighted average computed with relative
+  weight errors e_j is off by sum_j alpha_j e_j (g_j - gbar), at most 2 max|e| times
+  that scale, so this bound holds element by element, even where the output is near
+  zero through cancellation.  In bf16 the weights carry the rounding of qhat, khat (a
+  logit error of up to tau 2^-8) and of P (2^-9).
+The element-wise ratio of the survey's tolerance note, |gpu - oracle| / (|oracle| +
+1e-3 rms(oracle)), is computed and reported (TG_PARITY_REPORT) but not bounded: an
+output element that cancels to near zero keeps the absolute error of the weights, and
+the ratio then measures the cancellation, not the kernel.  With TG_PARITY_REPORT=<path>
+every check appends its figures as one JSON line to that file.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,12 +36,50 @@ from cross_token_gated_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+COND_TOL = {"f32": 1e-4, "bf16": 4e-2}
+
+
+def as_f64(gpu: torch.Tensor, shape) -> np.ndarray:
+    g = gpu.detach().double().cpu().numpy().reshape(shape)
+    assert np.all(np.isfinite(g)), "non-finite values in the GPU output"
+    return g
 
 
 def rel_err(gpu: torch.Tensor, ref: np.ndarray) -> float:
-    g = gpu.detach().double().cpu().numpy().reshape(ref.shape)
-    assert np.all(np.isfinite(g)), "non-finite values in the GPU output"
+    """Normwise relative error max |gpu - ref| / max |ref| over the whole tensor."""
+    g = as_f64(gpu, ref.shape)
     return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def errors(gpu: torch.Tensor, ref: np.ndarray, H: int = 1, scale=None) -> dict:
+    """Normwise, worst per-(row, head), survey element-wise and (with `scale`)
+    condition-normalised element-wise errors.  Rows are the last axis; H splits it into
+    heads of equal width."""
+    g = as_f64(gpu, ref.shape)
+    d = np.abs(g - ref)
+    a = np.abs(ref)
+    n = ref.shape[-1]
+    H = H if n % H == 0 else 1
+    dr, ar = d.reshape(-1, H, n // H), a.reshape(-1, H, n // H)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    out = {"norm": float(d.max() / max(a.max(), 1e-30)),
+           "row_head": float(np.max(dr.max(-1) / np.maximum(ar.max(-1), 1e-30))),
+           "elem_rms": float(np.max(d / (a + 1e-3 * rms)))}
+    if scale is not None:
+        out["elem_cond"] = float(np.max(d / np.maximum(np.asarray(scale).reshape(ref.shape), 1e-30)))
+    return out
+
+
+def check(gpu: torch.Tensor, ref: np.ndarray, dtype: str, H: int = 1, scale=None):
+    e = errors(gpu, ref, H, scale)
+    path = os.environ.get("TG_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(test=os.environ.get("PYTEST_CURRENT_TEST", ""), dtype=dtype, **e)) + "\n")
+    assert e["norm"] <= TOL[dtype], ("normwise", e)
+    assert e["row_head"] <= 2 * TOL[dtype], ("per row and head", e)
+    if scale is not None:
+        assert e["elem_cond"] <= COND_TOL[dtype], ("element-wise", e)
 
 
 def run_agg(kind, q, k, g, v, H, W=16, **kw):
@@ -42,6 +100,18 @@ def ref_agg(kind, q, k, g, v, H, W=16, s=10.0, rows=None, **kw):
     if kind == "tango":
         return oracle.tango(*args, H=H, tau=s, rows=rows, **kw)
     return oracle.wango_direct(*args, H=H, tau=s, window=W, rows=rows, **kw)
+
+
+def abs_inputs(g, v):
+    """|g| and |v| (exact in either storage type): the oracle's aggregation of them is the
+    element-wise error scale sum_j alpha_ij |g_j| |v_i|."""
+    return g.abs(), (v.abs() if v is not None else None)
+
+
+def ref_agg_scaled(kind, q, k, g, v, H, W=16, **kw):
+    """(oracle output, element-wise error scale) for one aggregation."""
+    ga, va = abs_inputs(g, v)
+    return ref_agg(kind, q, k, g, v, H, W, **kw), ref_agg(kind, q, k, ga, va, H, W, **kw)
 
 
 # (B, T, H, d_qk, m, W): tiny oracle config, ragged T, ragged gate tiles, several W
@@ -67,8 +137,22 @@ def test_agg_parity_small(kind, dtype, case):
     B, T, H, dqk, m, W = case
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=T + m, dtype=dtype)
     out = run_agg(kind, q, k, g, v, H, W)
-    ref = ref_agg(kind, q, k, g, v, H, W)
-    assert rel_err(out, ref) <= TOL[dtype]
+    ref, scale = ref_agg_scaled(kind, q, k, g, v, H, W)
+    check(out, ref, dtype, H, scale)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}T{c[1]}H{c[2]}dqk{c[3]}m{c[4]}W{c[5]}" for c in SMALL])
+def test_wango_plain_elu_feature_map(dtype, case):
+    """phi_mode = 1, the literal phi(u) = elu(u) + 1 of the benchmark configurations
+    (no epsilon, no 1/sqrt(d_h)), through the same kernels: the feature-map pre-pass
+    computes Fq and Fk with it, and every older-prefix weight and the state read-out use
+    them."""
+    B, T, H, dqk, m, W = case
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=T + m + 1, dtype=dtype)
+    out = run_agg("wango", q, k, g, v, H, W, phi_mode=1)
+    ref, scale = ref_agg_scaled("wango", q, k, g, v, H, W, phi_mode=1)
+    check(out, ref, dtype, H, scale)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -81,16 +165,17 @@ def test_agg_null_gate_tau_array_and_gbar_output(kind, dtype):
     tau = torch.tensor([10.0, 4.0], device="cuda")
     nb = torch.tensor([-1.0, 0.5], device="cuda")
     out = run_agg(kind, q, k, g, None, H, W, tau=tau, null_bias=nb)
-    ref = ref_agg(kind, q, k, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5])
-    assert rel_err(out, ref) <= TOL[dtype]
+    ref, scale = ref_agg_scaled(kind, q, k, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5])
+    check(out, ref, dtype, H, scale)
     # unit vectors in, no normalisation inside
     qn = q.double().reshape(B, T, H, -1)
     qn = (qn / qn.norm(dim=-1, keepdim=True)).reshape(B, T, dqk).to(q.dtype)
     kn = k.double().reshape(B, T, H, -1)
     kn = (kn / kn.norm(dim=-1, keepdim=True)).reshape(B, T, dqk).to(k.dtype)
     out2 = run_agg(kind, qn, kn, g, None, H, W, tau=tau, null_bias=nb, flags=tg.TG_FLAG_QK_NORMALIZED)
-    ref2 = ref_agg(kind, qn, kn, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5], qk_normalized=True)
-    assert rel_err(out2, ref2) <= TOL[dtype]
+    ref2, scale2 = ref_agg_scaled(kind, qn, kn, g, None, H, W, s=[10.0, 4.0], null_bias=[-1.0, 0.5],
+                                  qk_normalized=True)
+    check(out2, ref2, dtype, H, scale2)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -116,9 +201,22 @@ def test_agg_parity_70m_shape_sampled(kind):
     out = run_agg(kind, q, k, g, v, H, W)
     extra = [0, 1, 127, 128, 255, 256, 257, 383, 384, 2047, 7 * T + 2047, 3 * T + 1000]
     rows = synth.random_rows(B, T, 40, seed=1, extra=extra)
-    ref = ref_agg(kind, q, k, g, v, H, W, rows=rows)
+    ref, scale = ref_agg_scaled(kind, q, k, g, v, H, W, rows=rows)
     got = out.reshape(B * T, m)[torch.from_numpy(rows).cuda()]
-    assert rel_err(got, ref) <= TOL["bf16"]
+    check(got, ref, "bf16", H, scale)
+
+
+def test_wango_70m_shape_plain_elu_sampled():
+    """The WANGO benchmark configuration as written (phi = elu + 1 on the 64 feature
+    dimensions of each head): B=8, T=2048, m=28480, W=256, bf16, sampled rows."""
+    B, T, H, dqk, m, W = 8, 2048, 2, 128, 28480, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=4, dtype="bf16")
+    out = run_agg("wango", q, k, g, v, H, W, phi_mode=1)
+    extra = [0, 255, 256, 257, 383, 384, 1000, 2047, 5 * T + 300, 7 * T + 2047]
+    rows = synth.random_rows(B, T, 30, seed=5, extra=extra)
+    ref, scale = ref_agg_scaled("wango", q, k, g, v, H, W, rows=rows, phi_mode=1)
+    got = out.reshape(B * T, m)[torch.from_numpy(rows).cuda()]
+    check(got, ref, "bf16", H, scale)
 
 
 @pytest.mark.parametrize("kind", ["tango", "wango"])
@@ -132,9 +230,9 @@ def test_agg_parity_long_context_sampled(kind):
     out = run_agg(kind, q, k, g, v, H, W)
     extra = [0, 255, 256, 4095, 4096, 4097, 4223, 4224, 4351, 4352, 8191]
     rows = synth.random_rows(B, T, 24, seed=2, extra=extra)
-    ref = ref_agg(kind, q, k, g, v, H, W, rows=rows)
+    ref, scale = ref_agg_scaled(kind, q, k, g, v, H, W, rows=rows)
     got = out.reshape(B * T, m)[torch.from_numpy(rows).cuda()]
-    assert rel_err(got, ref) <= TOL["bf16"]
+    check(got, ref, "bf16", H, scale)
 
 
 # ------------------------------------------------------------------ block forward
@@ -149,9 +247,9 @@ def run_block(h, w, H, mode, W, **kw):
     return out
 
 
-def ref_block(h, w, H, mode, W, batches=None, s=10.0):
+def ref_block(h, w, H, mode, W, batches=None, s=10.0, phi_mode=0):
     wv = {n: synth.oracle_view(t) for n, t in w.items()}
-    return oracle.block_forward(synth.oracle_view(h), wv, H=H, tau=s, mode=mode, window=W,
+    return oracle.block_forward(synth.oracle_view(h), wv, H=H, tau=s, mode=mode, window=W, phi_mode=phi_mode,
                                 batches=batches, rope_base=10000.0, rms_eps=1e-6)
 
 
@@ -163,8 +261,8 @@ def test_block_tiny_fp32(mode):
     out = run_block(h, w, H, mode, W)
     ref = ref_block(h, w, H, mode, W)
     h64 = h.double().numpy()
-    assert rel_err(out, ref) <= 1e-4
-    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= 1e-4
+    check(out, ref, "f32")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "f32")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -175,8 +273,22 @@ def test_block_bf16_small(mode, shape):
     out = run_block(h, w, H, mode, W)
     ref = ref_block(h, w, H, mode, W)
     h64 = h.double().numpy()
-    assert rel_err(out, ref) <= TOL["bf16"]
-    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+    check(out, ref, "bf16")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
+
+
+@pytest.mark.parametrize("shape", [(2, 100, 128, 64, 512, 2, 32), (1, 600, 512, 128, 28480, 2, 256)])
+def test_block_wango_plain_elu(shape):
+    """The WANGO block with phi = elu + 1 (the benchmark configuration's feature map):
+    a small shape, and one 600-token sequence at the 70M-tier widths with W=256, every
+    output compared."""
+    B, T, d, dqk, m, H, W = shape
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=6, dtype="bf16")
+    out = run_block(h, w, H, 1, W, phi_mode=1)
+    ref = ref_block(h, w, H, 1, W, phi_mode=1)
+    h64 = h.double().numpy()
+    check(out, ref, "bf16")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -189,8 +301,8 @@ def test_block_output_gemm_many_tiles(mode):
     out = run_block(h, w, H, mode, W)
     ref = ref_block(h, w, H, mode, W)
     h64 = h.double().numpy()
-    assert rel_err(out, ref) <= TOL["bf16"]
-    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+    check(out, ref, "bf16")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -203,8 +315,8 @@ def test_block_160m_tier_widths(mode):
     out = run_block(h, w, H, mode, W)
     ref = ref_block(h, w, H, mode, W)
     h64 = h.double().numpy()
-    assert rel_err(out, ref) <= TOL["bf16"]
-    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+    check(out, ref, "bf16")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
 def test_block_70m_shape_sampled_sequences():
@@ -216,8 +328,8 @@ def test_block_70m_shape_sampled_sequences():
     ref = ref_block(h, w, H, 0, 1, batches=[0, 7])
     got = out[[0, 7]]
     h64 = h[[0, 7]].double().numpy()
-    assert rel_err(got, ref) <= TOL["bf16"]
-    assert rel_err(got.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+    check(got, ref, "bf16")
+    check(got.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
 def test_bounded_wait_timeout_reports_status():
@@ -234,19 +346,52 @@ def test_bounded_wait_timeout_reports_status():
     assert word & 1 and (word >> 8) & 0xFF == 1
     assert tg.tg_check_device_error() == (tg.TG_OK, 0)      # the word was cleared
     out = run_agg("tango", q, k, g, v, H)
-    assert rel_err(out, ref_agg("tango", q, k, g, v, H)) <= TOL["bf16"]
+    ref, scale = ref_agg_scaled("tango", q, k, g, v, H)
+    check(out, ref, "bf16", H, scale)
+
+
+@pytest.mark.parametrize("T,m", [(700, 1040), (1024, 20480)])
+def test_bounded_wait_timeout_reports_status_wango(T, m):
+    """The same hook in the WANGO gate-strip kernel: its MMA issuer waits on a barrier
+    that nothing signals, runs out (1 ms), records a timeout and every role leaves its
+    loops.  The second shape splits the strips into segments, so later segments also
+    give up (bounded) on the state their aborted predecessors never hand over.  The
+    context stays usable: the next call is correct."""
+    B, H, dqk, W = 1, 2, 128, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=8, dtype="bf16")
+    qd, kd, gd, vd = q.cuda(), k.cuda(), g.cuda(), v.cuda()
+    out = torch.empty_like(gd)
+    tg.wango_aggregate(qd, kd, gd, vd, out, H=H, window=W, flags=tg.TG_FLAG_DEBUG_TIMEOUT)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_ERR_TIMEOUT
+    assert word & 1 and (word >> 8) & 0xFF == 2
+    assert tg.tg_check_device_error() == (tg.TG_OK, 0)
+    out = run_agg("wango", q, k, g, v, H, W)
+    rows = synth.random_rows(B, T, 12, seed=9, extra=[0, 255, 256, T - 1])
+    ref, scale = ref_agg_scaled("wango", q, k, g, v, H, W, rows=rows)
+    check(out.reshape(B * T, m)[torch.from_numpy(rows).cuda()], ref, "bf16", H, scale)
+
+
+def test_bounded_wait_timeout_reports_status_gemm():
+    """In tango_block_forward the flag arms the hook of the projection GEMM only: its
+    MMA issuer waits on a barrier that nothing signals, runs out (1 ms), and the GEMM
+    records its timeout (kernel code 3).  The rest of the block then runs on whatever
+    the workspace held, without faults; the next block call is correct."""
+    B, T, d, dqk, m, H = 1, 256, 512, 128, 1024, 2
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=12, dtype="bf16")
+    hd = h.cuda()
+    wd = {n: t.cuda() for n, t in w.items()}
+    out = torch.empty_like(hd)
+    tg.tango_block_forward(hd, wd, out, H=H, flags=tg.TG_FLAG_DEBUG_TIMEOUT)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_ERR_TIMEOUT
+    assert word & 1 and (word >> 8) & 0xFF == 3
+    assert tg.tg_check_device_error() == (tg.TG_OK, 0)
+    out = run_block(h, w, H, 0, 1)
+    check(out, ref_block(h, w, H, 0, 1), "bf16")
 
 
 # ------------------------------------------------------------------ model forward
-
-def model_tol(dtype, n_apps=4):
-    """Tolerance of the model's logits: the per-operation bound times sqrt(n_apps).  Each
-    application adds its own storage roundings (h, x, q, k, g, v, u) and the residual
-    path carries earlier errors forward, so independent per-application errors add in
-    quadrature.  Measured on GB300 (bf16, d=128): max relative error 0.4-0.85 % after one
-    application and 1.1-2.4 % after four; RMS 0.55 % -> 1.2 %, the sqrt(4) growth."""
-    return TOL[dtype] * float(np.sqrt(n_apps))
-
 
 def model_setup(B, T, d, dqk, m, vocab, n_sets, seed, dtype):
     """Token ids, the tied embedding N(0, 0.02^2), unit final gain and n_sets weight sets
@@ -276,35 +421,44 @@ def ref_model(ids, E, gam_f, sets, H, mode, W, n_apps=4):
                                 rms_eps=1e-6, final_rms_eps=1e-6)
 
 
+# The model's logits are held to the same bounds as one operation.  In bf16 they are met
+# at the benchmark's widths: four applications at d = 512 and m >= 4,096.  At smaller
+# widths (d = 128, or m in the hundreds) bf16 storage of the GEMM operands alone, x and u,
+# gives 1.5-2.7 % after four applications, whether the residual stream is bf16 or fp32:
+# the output projection's sum over m averages fewer independent roundings.
+
 @pytest.mark.parametrize("mode", [0, 1])
 def test_model_tiny_fp32(mode):
     """Four applications of the tiny block (d=64, m=256, q/k width 32, W=16) with a
     1,000-entry tied embedding, fp32, every logit compared."""
     ids, E, gam_f, sets = model_setup(1, 64, 64, 32, 256, 1000, 1, seed=40, dtype="f32")
     out = run_model(ids, E, gam_f, sets, 2, mode, 16)
-    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 16)) <= model_tol("f32")
+    check(out, ref_model(ids, E, gam_f, sets, 2, mode, 16), "f32")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
 def test_model_bf16_small(mode):
-    ids, E, gam_f, sets = model_setup(2, 100, 128, 64, 512, 1000, 1, seed=41, dtype="bf16")
+    """Four applications at d=512, m=4,096 (two heads of 2,048 gates), T=100, every
+    logit compared; one application alone too."""
+    ids, E, gam_f, sets = model_setup(2, 100, 512, 128, 4096, 1000, 1, seed=41, dtype="bf16")
     out = run_model(ids, E, gam_f, sets, 2, mode, 32)
-    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 32)) <= model_tol("bf16")
-    # one application alone meets the per-operation bound
+    check(out, ref_model(ids, E, gam_f, sets, 2, mode, 32), "bf16")
     one = run_model(ids, E, gam_f, sets, 2, mode, 32, n_apps=1)
-    assert rel_err(one, ref_model(ids, E, gam_f, sets, 2, mode, 32, n_apps=1)) <= TOL["bf16"]
+    check(one, ref_model(ids, E, gam_f, sets, 2, mode, 32, n_apps=1), "bf16")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
 def test_model_three_sets_unaligned_gate_width(mode):
-    """Three gated-projection sets (first / middle / last applications) with a head gate
-    width of 47, which the bf16 block pads to 48 internally."""
-    ids, E, gam_f, sets = model_setup(2, 150, 128, 64, 94, 1000, 3, seed=42, dtype="bf16")
+    """Three gated-projection sets (first / middle / last applications) of m=9,494, i.e.
+    a head gate width of 4,747, which the bf16 block pads to 4,752 internally; T=150,
+    every logit compared."""
+    ids, E, gam_f, sets = model_setup(2, 150, 512, 128, 9494, 1000, 3, seed=42, dtype="bf16")
     out = run_model(ids, E, gam_f, sets, 2, mode, 64)
-    assert rel_err(out, ref_model(ids, E, gam_f, sets, 2, mode, 64)) <= model_tol("bf16")
+    ref = ref_model(ids, E, gam_f, sets, 2, mode, 64)
+    check(out, ref, "bf16")
     # the assignment matters: swapping the first and last sets changes the logits
     swapped = run_model(ids, E, gam_f, [sets[2], sets[1], sets[0]], 2, mode, 64)
-    assert rel_err(swapped, ref_model(ids, E, gam_f, sets, 2, mode, 64)) > 3 * model_tol("bf16")
+    assert rel_err(swapped, ref) > 3 * TOL["bf16"]
 
 
 @pytest.mark.parametrize("m,n_sets", [(28480, 1), (9494, 3)])
@@ -318,7 +472,7 @@ def test_model_shared_block_config_sampled(m, n_sets):
     out = run_model(ids, E, gam_f, sets, 2, 0, 1)
     got = out[[0, 15], :Tp]
     ref = ref_model(ids[[0, 15], :Tp], E, gam_f, sets, 2, 0, 1)
-    assert rel_err(got, ref) <= model_tol("bf16")
+    check(got, ref, "bf16")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -331,8 +485,8 @@ def test_block_paper_head_geometry(mode):
     out = run_block(h, w, H, mode, W)
     ref = ref_block(h, w, H, mode, W)
     h64 = h.double().numpy()
-    assert rel_err(out, ref) <= TOL["bf16"]
-    assert rel_err(out.cpu().double() - torch.from_numpy(h64), ref - h64) <= TOL["bf16"]
+    check(out, ref, "bf16")
+    check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
 # ------------------------------------------------------------------ WANGO decode step
@@ -375,7 +529,9 @@ def test_decode_steps_match_the_whole_sequence(dtype, case):
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=21, dtype=dtype)
     out = run_decode(q, k, g, v, H, W)
     ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g, v)], H=H, tau=10.0, window=W)
-    assert rel_err(out, ref) <= TOL[dtype]
+    scale = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, *abs_inputs(g, v))], H=H, tau=10.0,
+                              window=W)
+    check(out, ref, dtype, H, scale)
 
 
 def test_decode_null_gate_tau_array_and_gbar():
@@ -384,9 +540,10 @@ def test_decode_null_gate_tau_array_and_gbar():
     tau = torch.tensor([3.0, 12.0], dtype=torch.float32)
     nb = torch.tensor([-1.0, 0.5], dtype=torch.float32)
     out = run_decode(q, k, g, None, H, W, tau=tau.cuda(), null_bias=nb.cuda(), phi_mode=1)
-    ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g)], None, H=H, tau=tau.numpy(), window=W,
-                            null_bias=nb.numpy(), phi_mode=1)
-    assert rel_err(out, ref) <= TOL["bf16"]
+    kw = dict(H=H, tau=tau.numpy(), window=W, null_bias=nb.numpy(), phi_mode=1)
+    ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g)], None, **kw)
+    scale = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g.abs())], None, **kw)
+    check(out, ref, "bf16", H, scale)
 
 
 def test_wango_segments_hand_over_the_state():
@@ -398,4 +555,6 @@ def test_wango_segments_hand_over_the_state():
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=31, dtype="bf16")
     out = run_agg("wango", q, k, g, v, H, W)
     ref = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, g, v)], H=H, tau=10.0, window=W)
-    assert rel_err(out, ref) <= TOL["bf16"]
+    scale = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, *abs_inputs(g, v))], H=H, tau=10.0,
+                              window=W)
+    check(out, ref, "bf16", H, scale)

@@ -9,15 +9,11 @@ other tests.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import cross_token_gated_gb300 as tg
 from cross_token_gated_gb300 import synth
-
-TOL = {"f32": 1e-4, "bf16": 2e-2}
-
 
 def rel(a, b):
     a, b = a.double().cpu(), b.double().cpu()
@@ -36,7 +32,10 @@ def test_noalloc_rejects_oversized_problem_on_host(lib):
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_noalloc_matches_tango_aggregate_twice(dtype):
-    """Two calls in a row on different inputs: each equals tango_aggregate's output."""
+    """Two calls in a row on different inputs, the second smaller than the first so that
+    a stale part of the scratch left by the first would show: each equals
+    tango_aggregate's output bit for bit (the same kernels run on the same inputs, and
+    their summation order does not depend on where the scratch lives)."""
     H = 2
     for call, (B, T, dqk, m, seed) in enumerate([(2, 300, 128, 1040, 21), (1, 700, 64, 512, 22)]):
         q, k, g, v = (t.cuda() for t in synth.agg_inputs(B, T, dqk, m, seed=seed, dtype=dtype))
@@ -47,4 +46,4 @@ def test_noalloc_matches_tango_aggregate_twice(dtype):
         st, word = tg.tg_check_device_error()
         assert st == tg.TG_OK, (call, st, hex(word))
         assert torch.isfinite(got.float()).all(), call
-        assert rel(got, ref) <= TOL[dtype], call
+        assert torch.equal(got, ref), (call, rel(got, ref))
