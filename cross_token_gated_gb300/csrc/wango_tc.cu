@@ -657,6 +657,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (has_leaving(it.ib0, W) && !(ok = load_fk(jlo_of(it.ib0, W)))) break;
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib) {
         const int jlo = jlo_of(ib, W), ppos = prefetch_pos(ib, W);
+        // the next block's v into L2 ahead of its load: the epilogue loads it only once
+        // this block's u has left the staging tile, and would otherwise wait out the HBM
+        // latency there.  (The same prefetch of the G tile two blocks ahead was slower:
+        // that tile's load already overlaps two blocks of MMAs.)
+        if (a.v && ib + 1 < it.ib1) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&tmV, gx + 64 * c, (ib + 1) * kBlk + 64 * h, sp.b);
+        }
         for (int jb = jlo; ok && jb <= ib; ++jb) {
           if ((!reuse || ib == it.ib0) && !(ok = load_g(jb))) break;
           for (int hh = 0; hh < 2; ++hh) {
@@ -1075,10 +1085,36 @@ cudaError_t launch_p(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   return cudaGetLastError();
 }
 
+// The segmented kernel waits (bounded) for states that other CTAs of the same launch
+// hand over, so all its CTAs must be resident at once: it is launched cooperatively,
+// which the driver either schedules with every CTA resident or refuses.  When it is
+// refused (fewer SMs available than the grid, e.g. under SM partitioning), the strips
+// run unsegmented, which has no waits between CTAs.
 template <int DH>
 cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtensorMap& mfq, const CUtensorMap& mfk,
-                     const CUtensorMap& mv, const CUtensorMap& mu, const GArgs& a, cudaStream_t s) {
-  auto kern = a.nseg > 1 ? wango_g_kernel<DH, true> : wango_g_kernel<DH, false>;
+                     const CUtensorMap& mv, const CUtensorMap& mu, GArgs a, cudaStream_t s) {
+  if (a.nseg > 1) {
+    auto kern = wango_g_kernel<DH, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.n_items < num_sms() ? a.n_items : num_sms()));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kGSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mp, mg, mfq, mfk, mv, mu, a);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();  // not sticky: clear it and run the strips whole
+    a.nseg = 1;
+    a.seg_len = a.n_iblk;
+    a.n_items = a.n_strips;
+  }
+  auto kern = wango_g_kernel<DH, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
