@@ -417,18 +417,78 @@ def main():
         dist.destroy_process_group()
 
 
-def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
-    """Aggregation-only timings: TANGO at B=8/T=2048 and B=1/T=8192, WANGO (W=256) at
-    both; unit-normalised q/k and N(0,1) g, v generated on the device."""
+def event_ms(f, dev, stream, reps=5, warm=3):
+    """Mean device time of f() over `reps` calls, CUDA events on `stream`, after `warm`
+    untimed calls."""
     import torch
+    for _ in range(warm):
+        f()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        f()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+def kernel_breakdown(f, dev):
+    """Per-kernel device time of one call of f(), from the CUDA profiler's activity
+    records (CUPTI): {kernel: {"launches", "ms", "share"}}.  Shares of one call; the
+    call's own time is taken separately, without the profiler."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize(dev)
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            f()
+            torch.cuda.synchronize(dev)
+        rows = {}
+        for ev in prof.key_averages():
+            us = getattr(ev, "self_device_time_total", None)
+            if us is None:
+                us = getattr(ev, "self_cuda_time_total", 0.0)
+            if not us or ev.key.startswith(("cudaLaunch", "cuda", "Memcpy", "Memset")):
+                continue
+            name = ev.key.replace("(anonymous namespace)::", "").replace("void ", "").replace("tg::", "")
+            name = name.split("(")[0].split("<")[0].strip()
+            r = rows.setdefault(name, {"launches": 0, "ms": 0.0})
+            r["launches"] += int(ev.count)
+            r["ms"] += us / 1e3
+        total = sum(r["ms"] for r in rows.values()) or 1.0
+        for r in rows.values():
+            r["share"] = r["ms"] / total
+        return dict(sorted(rows.items(), key=lambda kv: -kv[1]["ms"]))
+    except Exception as exc:  # the profiler is context only
+        return {"unavailable": str(exc)[:200]}
+
+
+def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
+    """Context measurements beside the headline step, each event-timed on the device:
+    - aggregation only (TANGO, and WANGO with W=256) at B=8 T=2048 and at B=1 over
+      T = 1k, 2k, 4k, 8k, with each time's ratio to the T/2 point (the full prefix grows
+      quadratically in T, the window linearly); unit-normalised q/k and N(0,1) g, v
+      generated on the device;
+    - the WANGO block step at B=8 T=2048 (W=256);
+    - the shared-block model forward at B=16 T=1024 (4 TANGO applications, 32,768-entry
+      tied embedding): one set of m=28,480 and three sets of m=9,494, with per-kernel
+      device times;
+    - WANGO decode steps (W=256) at B=1 and B=8, timed as one CUDA-graph replay of 64
+      consecutive steps."""
+    import torch
+    from cross_token_gated_gb300 import synth  # noqa: F401  (the recipe the weights follow)
     res = {}
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    for (b, t_len) in ((8, 2048), (1, 8192)):
-        q = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
-        q = (q / q.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
-        k = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
-        k = (k / k.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+
+    def unit(b, t_len):
+        x = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+        return (x / x.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+
+    prev = {}
+    for (b, t_len) in ((8, 2048), (1, 1024), (1, 2048), (1, 4096), (1, 8192)):
+        q, k = unit(b, t_len), unit(b, t_len)
         g = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
         v = torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16()
         o = torch.empty_like(g)
@@ -440,27 +500,95 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
                 f = lambda: tg.wango_aggregate(q, k, g, v, o, H=H, window=256, flags=tg.TG_FLAG_QK_NORMALIZED,
                                                stream=stream)
                 fl = acc.wango_agg_flops(b, t_len, DQK, M, H, 256)
-            for _ in range(3):
-                f()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 5
-            e0.record(stream)
-            for _ in range(reps):
-                f()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            ms = e0.elapsed_time(e1) / reps
+            ms = event_ms(f, dev, stream)
             by = acc.agg_bytes(b, t_len, DQK, M)
-            res[f"{kind}_B{b}_T{t_len}"] = {
-                "ms": ms, "tokens_per_s": b * t_len / (ms * 1e-3),
-                "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf,
-                "gbs": by / (ms * 1e-3) / 1e9, "frac_hbm_peak": by / (ms * 1e-3) / 1e9 / peak_gbs}
+            rec = {"ms": ms, "tokens_per_s": b * t_len / (ms * 1e-3),
+                   "tflops": fl / (ms * 1e-3) / 1e12, "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf,
+                   "gbs": by / (ms * 1e-3) / 1e9, "frac_hbm_peak": by / (ms * 1e-3) / 1e9 / peak_gbs}
+            if b == 1 and (kind, t_len // 2) in prev:
+                rec["ratio_to_half_T"] = ms / prev[(kind, t_len // 2)]
+            if b == 1:
+                prev[(kind, t_len)] = ms
+            res[f"{kind}_B{b}_T{t_len}"] = rec
         del q, k, g, v, o
         torch.cuda.empty_cache()
+    res["t_sweep_B1"] = {kind: {str(t): prev[(kind, t)] for t in (1024, 2048, 4096, 8192)}
+                         for kind in ("tango", "wango")}
+    res["t_sweep_B1"]["unit"] = "ms"
+
+    # ---- the WANGO block step (B=8, T=2048, W=256)
+    def block_weights(d, m, n_sets=1):
+        n = lambda r, c: (torch.randn(r, c, device=dev, generator=gen) * c ** -0.5).bfloat16()
+        base = {"gamma": torch.ones(d, device=dev).bfloat16(), "Wq": n(DQK, d), "Wk": n(DQK, d)}
+        return [dict(base, Wg=n(m, d), Wv=n(m, d), Wo=n(d, m)) for _ in range(n_sets)]
+
+    w = block_weights(D, M)[0]
+    h = torch.randn(B, T, D, device=dev, generator=gen).bfloat16()
+    out = torch.empty_like(h)
+    wsb = tg.block_workspace(B, T, D, H, DQK, M, dtype=tg.TG_BF16, mode=tg.TG_MODE_WANGO, window=256, device=dev)
+    f = lambda: tg.tango_block_forward(h, w, out, H=H, mode=tg.TG_MODE_WANGO, window=256, ws=wsb, stream=stream)
+    ms = event_ms(f, dev, stream, reps=10)
+    fl = acc.block_flops(B, T, D, DQK, M, mode=1, H=H, W=256)
+    res[f"wango_block_B{B}_T{T}"] = {"ms": ms, "tokens_per_s": B * T / (ms * 1e-3),
+                                     "tflops": fl / (ms * 1e-3) / 1e12, "kernels": kernel_breakdown(f, dev)}
+    del w, h, out, wsb
+    torch.cuda.empty_cache()
+
+    # ---- the shared-block model forward (B=16, T=1024, 4 applications, vocab 32,768)
+    Bm, Tm, V = 16, 1024, 32768
+    E = (torch.randn(V, D, device=dev, generator=gen) * 0.02).bfloat16()
+    gam_f = torch.ones(D, device=dev).bfloat16()
+    ids = torch.randint(0, V, (Bm, Tm), device=dev, generator=gen, dtype=torch.int32)
+    logits = torch.empty(Bm, Tm, V, device=dev, dtype=torch.bfloat16)
+    for m_set, n_sets in ((M, 1), (9494, 3)):
+        sets = block_weights(D, m_set, n_sets)
+        mp = tg.model_params(Bm, Tm, D, H, DQK, m_set, V, dtype=tg.TG_BF16, n_apps=4, n_sets=n_sets)
+        wsm = torch.empty(tg.tg_workspace_size(tg.TG_WS_MODEL, mp) + 256, dtype=torch.uint8, device=dev)
+        f = lambda: tg.tango_model_forward(ids, E, gam_f, sets, logits, H=H, n_apps=4, ws=wsm, stream=stream)
+        ms = event_ms(f, dev, stream, reps=5)
+        fl = acc.model_flops(Bm, Tm, D, DQK, m_set, V, 4)
+        res[f"model_B{Bm}_T{Tm}_sets{n_sets}_m{m_set}"] = {
+            "ms": ms, "tokens_per_s": Bm * Tm / (ms * 1e-3), "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf, "algorithmic_tflop": fl / 1e12,
+            "kernels": kernel_breakdown(f, dev)}
+        del sets, wsm
+        torch.cuda.empty_cache()
+    del E, ids, logits
+
+    # ---- WANGO decode steps (W=256), steady state, one graph replay of 64 steps
+    for b in (1, 8):
+        Wd, n = 256, 64
+        q, k = unit(b, 1)[:, 0].contiguous(), unit(b, 1)[:, 0].contiguous()
+        g = torch.randn(b, M, device=dev, generator=gen).bfloat16()
+        v = torch.randn(b, M, device=dev, generator=gen).bfloat16()
+        o = torch.empty_like(g)
+        st = tg.decode_state(b, H, DQK, M, window=Wd, dtype=tg.TG_BF16, device=dev)
+        for pos in range(Wd + 8):
+            tg.wango_decode_step(q, k, g, v, o, st, pos, H=H, window=Wd, flags=tg.TG_FLAG_QK_NORMALIZED,
+                                 stream=stream)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            for pos in range(Wd + 8, Wd + 8 + n):
+                tg.wango_decode_step(q, k, g, v, o, st, pos, H=H, window=Wd, flags=tg.TG_FLAG_QK_NORMALIZED,
+                                     stream=cap)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) / n * 1e3
+        by = acc.decode_bytes(b, DQK, M, H, Wd)
+        res[f"decode_B{b}_W{Wd}"] = {"us_per_step": us, "tokens_per_s": b / (us * 1e-6),
+                                     "gbs": by / (us * 1e-6) / 1e9, "frac_hbm_peak": by / (us * 1e-6) / 1e9 / peak_gbs,
+                                     "timing": f"one CUDA-graph replay of {n} consecutive steps"}
+        del graph, q, k, g, v, o, st
+        torch.cuda.empty_cache()
+
     st, word = tg.tg_check_device_error(stream)
     if st != tg.TG_OK:
-        raise RuntimeError(f"device error in aggregation timings ({word:#x})")
+        raise RuntimeError(f"device error in the context measurements ({word:#x})")
     return res
 
 

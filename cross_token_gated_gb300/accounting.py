@@ -85,3 +85,23 @@ def block_flops(B: int, T: int, d: int, dqk: int, m: int, mode: int = 0, H: int 
                 W: int = 1) -> int:
     agg = tango_agg_flops(B, T, dqk, m) if mode == 0 else wango_agg_flops(B, T, dqk, m, H, W)
     return proj_flops(B, T, d, dqk, m) + agg + out_flops(B, T, d, m)
+
+
+def logits_flops(B: int, T: int, d: int, vocab: int) -> int:
+    """The tied-embedding logits x E^T of the language model (sec. 2.3)."""
+    return 2 * B * T * d * vocab
+
+
+def model_flops(B: int, T: int, d: int, dqk: int, m: int, vocab: int, n_apps: int, mode: int = 0,
+                H: int = 2, W: int = 1) -> int:
+    """n_apps block applications (eq. 11) and the logits; the embedding lookup and the
+    RMSNorms are not counted."""
+    return n_apps * block_flops(B, T, d, dqk, m, mode, H, W) + logits_flops(B, T, d, vocab)
+
+
+def decode_bytes(B: int, dqk: int, m: int, H: int, W: int, elem: int = 2) -> int:
+    """One WANGO decode step: the ring of W gate vectors read, the f32 state S read and
+    written, and this token's g, v read and u written (sec. 2.2 eq. 10 taken one token
+    at a time); the q/k-sized terms are negligible and not counted."""
+    d_h = dqk // H
+    return B * (W * m * elem + 2 * d_h * m * 4 + 3 * m * elem)
