@@ -61,11 +61,14 @@ def _load():
             lib.oracle_wango_scan.argtypes = agg + [i, i] + [vp, i, vp, i, vp, i, vp, i, vp, vp, i, vp]
             lib.oracle_block_forward.argtypes = ([i] * 9 + [d, d] + [vp] * 6 + [i] + [vp, i, vp, vp]
                                                  + [vp, i, vp] + [vp] * 5)
+            bwd = [vp, i, vp, i, vp, i, vp, i, vp, i, vp, vp, i, vp, vp, vp, vp]
+            lib.oracle_tango_backward.argtypes = agg + bwd
+            lib.oracle_wango_backward.argtypes = agg + [i, i] + bwd
             lib.oracle_embed.argtypes = [ll, vp, i, i, vp, i, vp]
             lib.oracle_final_logits.argtypes = [ll, i, i, vp, vp, i, d, vp, i, vp]
             for name in ("oracle_tango", "oracle_wango_direct", "oracle_wango_scan",
                          "oracle_block_forward", "oracle_embed", "oracle_final_logits",
-                         "oracle_num_threads"):
+                         "oracle_tango_backward", "oracle_wango_backward", "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -151,6 +154,35 @@ def wango_direct(q, k, g, v, *, H, tau, window, phi_mode=0, null_bias=None,
                                      out.ctypes.data)
     _check(rc, "oracle_wango_direct")
     return out if rows is not None else out.reshape(B, T, m)
+
+
+def _backward(fn, extra, q, k, g, v, dout, H, tau, null_bias, qk_normalized):
+    B, T, dqk = q.shape
+    m = g.shape[-1]
+    qp, qd, qa = _arr(q); kp, kd, ka = _arr(k); gp, gd, ga = _arr(g); vp_, vd, va = _arr(v)
+    op, od, oa = _arr(dout)
+    tp, ta = _f64(_tau_vec(tau, H), H)
+    bp, ba = _f64(null_bias, H)
+    dq = np.empty((B, T, dqk)); dk = np.empty((B, T, dqk))
+    dg = np.empty((B, T, m)); dv = np.zeros((B, T, m))
+    rc = getattr(_load(), fn)(B, T, H, dqk, m, *extra, qp, qd, kp, kd, gp, gd, vp_, vd, op, od, tp, bp,
+                              int(bool(qk_normalized)), dq.ctypes.data, dk.ctypes.data, dg.ctypes.data,
+                              dv.ctypes.data)
+    _check(rc, fn)
+    return {"dq": dq, "dk": dk, "dg": dg, "dv": dv if v is not None else None}
+
+
+def tango_backward(q, k, g, v, dout, *, H, tau, null_bias=None, qk_normalized=False):
+    """Gradients of L = sum(dout * u) for the TANGO aggregation u (eqs. 5-6) with respect
+    to q, k, g and v (dv is None when v is None, i.e. u = gbar).  Returns a dict of fp64
+    arrays dq, dk [B, T, dqk] and dg, dv [B, T, m]."""
+    return _backward("oracle_tango_backward", (), q, k, g, v, dout, H, tau, null_bias, qk_normalized)
+
+
+def wango_backward(q, k, g, v, dout, *, H, tau, window, phi_mode=0, null_bias=None, qk_normalized=False):
+    """Gradients of L = sum(dout * u) for the WANGO aggregation (eqs. 5-9), pair by pair."""
+    return _backward("oracle_wango_backward", (int(window), int(phi_mode)), q, k, g, v, dout, H, tau,
+                     null_bias, qk_normalized)
 
 
 def wango_scan(q, k, g, v, *, H, tau, window, phi_mode=0, null_bias=None, qk_normalized=False):

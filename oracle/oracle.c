@@ -19,6 +19,7 @@
  *   - feature map phi and older-source weight              (sec. 2.2, eqs. 8-9)
  *   - running sums S, z                                    (sec. 2.2, eq. 10)
  *   - residual update h+ = h + W_o(gbar * v)               (sec. 2.1, eq. 3)
+ *   - gradients of eq. 5 with respect to q, k, g and v     (derivative of eqs. 4-9)
  *
  * Inputs may be fp64, fp32 or bf16 (raw 16-bit patterns); they are widened
  * exactly to fp64 before any arithmetic, so input quantisation is never an
@@ -488,6 +489,188 @@ int oracle_final_logits(long long n, int d, int vocab, const double *h, const vo
         free(x);
     }
     return fail ? OR_ENOMEM : OR_OK;
+}
+
+/* ------------------------------------------------------------ gradients */
+
+/* Derivative of the feature map with respect to its argument: ELU'(u) = 1 for
+ * u > 0 and e^u otherwise, divided by sqrt(d_h) for eq. 8 (mode 0).  The
+ * max(., eps) of eq. 8 never binds, since ELU(u) + 1 > 0. */
+static double phi_deriv(double u, int d_h, int mode) {
+    double e = u > 0.0 ? 1.0 : exp(u);
+    return mode == 1 ? e : e / sqrt((double)d_h);
+}
+
+/*
+ * Gradients of the scalar L = sum_{i,c} dout_ic u_ic, where u = gbar * v (or
+ * u = gbar when v == NULL) is the aggregation of eq. 5 with TANGO (mode 0, eq. 6)
+ * or WANGO (mode 1, eqs. 7-9) weights, with respect to q, k, g and v.  Each pair
+ * is taken directly from the derivative of eq. 5, per batch and head:
+ *   alpha_ij = w_ij / den_i,  gbar_i = sum_{j<=i} alpha_ij g_j
+ *   dgbar_i = dout_i * v_i (dout_i without v),  dv_i = dout_i * gbar_i
+ *   dg_j = sum_{i>=j} alpha_ij dgbar_i
+ *   dL/dw_ij = (g_j . dgbar_i - gbar_i . dgbar_i) / den_i   (the null term carries no
+ *                                                            value, only weight)
+ *   window pair, w = exp(tau qhat_i . khat_j):
+ *       dqhat_i += tau w dL/dw khat_j,   dkhat_j += tau w dL/dw qhat_i
+ *   older pair, w = phi(x_i) . phi(y_j) with x = sqrt(tau) qhat, y = sqrt(tau) khat:
+ *       dqhat_i += sqrt(tau) dL/dw phi'(x_i) * phi(y_j)
+ *       dkhat_j += sqrt(tau) dL/dw phi(x_i) * phi'(y_j)
+ *   unit normalisation qhat = q / max(|q|, 1e-12) (sec. 2.1):
+ *       dq = (dqhat - qhat (qhat . dqhat)) / |q|, or dqhat / 1e-12 where the clamp holds
+ * Outputs (fp64): dq, dk [B*T, dqk]; dg [B*T, m]; dv [B*T, m] (untouched when v == NULL).
+ */
+static int agg_backward(int mode, int B, int T, int H, int dqk, int m, int W, int phi_mode,
+                        const void *q, int qdt, const void *k, int kdt,
+                        const void *g, int gdt, const void *v, int vdt, const void *dout, int odt,
+                        const double *tau, const double *null_b, int qk_normalized,
+                        double *dq, double *dk, double *dg, double *dv) {
+    if (!check_dims(B, T, H, dqk, m) || (mode == 1 && W < 1)) return OR_EINVAL;
+    int d_h = dqk / H, m_h = m / H;
+    long long BT = (long long)B * T;
+    double *qn = prep_unit(q, qdt, BT, H, dqk, qk_normalized);
+    double *kn = prep_unit(k, kdt, BT, H, dqk, qk_normalized);
+    double *fq = NULL, *fk = NULL;
+    if (mode == 1 && qn && kn) {
+        fq = prep_phi(qn, BT, H, dqk, tau, phi_mode);
+        fk = prep_phi(kn, BT, H, dqk, tau, phi_mode);
+    }
+    if (!qn || !kn || (mode == 1 && (!fq || !fk))) {
+        free(qn); free(kn); free(fq); free(fk);
+        return OR_ENOMEM;
+    }
+    memset(dq, 0, sizeof(double) * (size_t)BT * dqk);
+    memset(dk, 0, sizeof(double) * (size_t)BT * dqk);
+    memset(dg, 0, sizeof(double) * (size_t)BT * m);
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long u = 0; u < (long long)B * H; ++u) {
+        int a = (int)(u % H);
+        size_t row0 = (size_t)(u / H) * T;
+        double *gbar = (double *)malloc(sizeof(double) * (size_t)T * m_h);
+        double *dgb = (double *)malloc(sizeof(double) * (size_t)T * m_h);
+        double *den = (double *)malloc(sizeof(double) * (size_t)T);
+        double *delta = (double *)malloc(sizeof(double) * (size_t)T);
+        double *gj = (double *)malloc(sizeof(double) * (size_t)m_h);
+        double *dqh = (double *)calloc((size_t)T * d_h, sizeof(double));
+        double *dkh = (double *)calloc((size_t)T * d_h, sizeof(double));
+        if (!gbar || !dgb || !den || !delta || !gj || !dqh || !dkh) {
+            fail = 1;
+            free(gbar); free(dgb); free(den); free(delta); free(gj); free(dqh); free(dkh);
+            continue;
+        }
+        const double st = sqrt(tau[a]);
+        /* weight of pair (i, j), j <= i: eq. 6 inside the window, eq. 9 older */
+#define PAIR_W(i, j) ((mode == 0 || (j) >= (i) - W + 1)                                          \
+        ? exp(tau[a] * dot(qn + (row0 + (i)) * dqk + (size_t)a * d_h,                            \
+                           kn + (row0 + (j)) * dqk + (size_t)a * d_h, d_h))                      \
+        : dot(fq + (row0 + (i)) * dqk + (size_t)a * d_h, fk + (row0 + (j)) * dqk + (size_t)a * d_h, d_h))
+        /* the forward pass: den_i and gbar_i */
+        for (int i = 0; i < T; ++i) {
+            double *gb = gbar + (size_t)i * m_h;
+            for (int n = 0; n < m_h; ++n) gb[n] = 0.0;
+            double dsum = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                double w = PAIR_W(i, j);
+                dsum += w;
+                axpy_from(gb, w, g, gdt, (row0 + j) * (size_t)m + (size_t)a * m_h, m_h);
+            }
+            if (null_b) dsum += (double)(i + 1) * exp(null_b[a]);
+            den[i] = dsum;
+            for (int n = 0; n < m_h; ++n) gb[n] /= dsum;
+        }
+        /* dgbar, dv and delta_i = gbar_i . dgbar_i */
+        for (int i = 0; i < T; ++i) {
+            size_t off = (row0 + i) * (size_t)m + (size_t)a * m_h;
+            double dl = 0.0;
+            for (int n = 0; n < m_h; ++n) {
+                double o = ld(dout, odt, off + n);
+                double x = v ? o * ld(v, vdt, off + n) : o;
+                dgb[(size_t)i * m_h + n] = x;
+                dl += gbar[(size_t)i * m_h + n] * x;
+                if (v) dv[off + n] = o * gbar[(size_t)i * m_h + n];
+            }
+            delta[i] = dl;
+        }
+        /* every pair j <= i */
+        for (int j = 0; j < T; ++j) {
+            widen_row(gj, g, gdt, (row0 + j) * (size_t)m + (size_t)a * m_h, m_h);
+            double *dgj = dg + (row0 + j) * (size_t)m + (size_t)a * m_h;
+            for (int i = j; i < T; ++i) {
+                double w = PAIR_W(i, j);
+                const double *dgi = dgb + (size_t)i * m_h;
+                double alpha = w / den[i];
+                for (int n = 0; n < m_h; ++n) dgj[n] += alpha * dgi[n];
+                double dw = (dot(gj, dgi, m_h) - delta[i]) / den[i];
+                const double *qi = qn + (row0 + i) * dqk + (size_t)a * d_h;
+                const double *kj = kn + (row0 + j) * dqk + (size_t)a * d_h;
+                double *dqi = dqh + (size_t)i * d_h, *dkj = dkh + (size_t)j * d_h;
+                if (mode == 0 || j >= i - W + 1) {
+                    for (int c = 0; c < d_h; ++c) {
+                        dqi[c] += tau[a] * w * dw * kj[c];
+                        dkj[c] += tau[a] * w * dw * qi[c];
+                    }
+                } else {
+                    const double *fqi = fq + (row0 + i) * dqk + (size_t)a * d_h;
+                    const double *fkj = fk + (row0 + j) * dqk + (size_t)a * d_h;
+                    for (int c = 0; c < d_h; ++c) {
+                        dqi[c] += st * dw * phi_deriv(st * qi[c], d_h, phi_mode) * fkj[c];
+                        dkj[c] += st * dw * fqi[c] * phi_deriv(st * kj[c], d_h, phi_mode);
+                    }
+                }
+            }
+        }
+#undef PAIR_W
+        /* through the unit normalisation */
+        for (int i = 0; i < T; ++i) {
+            for (int side = 0; side < 2; ++side) {
+                const void *raw = side ? k : q;
+                int rdt = side ? kdt : qdt;
+                const double *unit = (side ? kn : qn) + (row0 + i) * dqk + (size_t)a * d_h;
+                const double *dh = (side ? dkh : dqh) + (size_t)i * d_h;
+                double *dst = (side ? dk : dq) + (row0 + i) * dqk + (size_t)a * d_h;
+                if (qk_normalized) {
+                    for (int c = 0; c < d_h; ++c) dst[c] = dh[c];
+                    continue;
+                }
+                double nrm = 0.0;
+                for (int c = 0; c < d_h; ++c) {
+                    double x = ld(raw, rdt, (row0 + i) * dqk + (size_t)a * d_h + c);
+                    nrm += x * x;
+                }
+                nrm = sqrt(nrm);
+                if (nrm < 1e-12) {
+                    for (int c = 0; c < d_h; ++c) dst[c] = dh[c] / 1e-12;
+                } else {
+                    double pr = dot(unit, dh, d_h);
+                    for (int c = 0; c < d_h; ++c) dst[c] = (dh[c] - unit[c] * pr) / nrm;
+                }
+            }
+        }
+        free(gbar); free(dgb); free(den); free(delta); free(gj); free(dqh); free(dkh);
+    }
+    free(qn); free(kn); free(fq); free(fk);
+    return fail ? OR_ENOMEM : OR_OK;
+}
+
+/* Gradients of TANGO (eqs. 5-6); see agg_backward. */
+int oracle_tango_backward(int B, int T, int H, int dqk, int m,
+                          const void *q, int qdt, const void *k, int kdt,
+                          const void *g, int gdt, const void *v, int vdt, const void *dout, int odt,
+                          const double *tau, const double *null_b, int qk_normalized,
+                          double *dq, double *dk, double *dg, double *dv) {
+    return agg_backward(0, B, T, H, dqk, m, 1, 0, q, qdt, k, kdt, g, gdt, v, vdt, dout, odt,
+                        tau, null_b, qk_normalized, dq, dk, dg, dv);
+}
+
+/* Gradients of WANGO (eqs. 5-9), pair by pair; see agg_backward. */
+int oracle_wango_backward(int B, int T, int H, int dqk, int m, int W, int phi_mode,
+                          const void *q, int qdt, const void *k, int kdt,
+                          const void *g, int gdt, const void *v, int vdt, const void *dout, int odt,
+                          const double *tau, const double *null_b, int qk_normalized,
+                          double *dq, double *dk, double *dg, double *dv) {
+    return agg_backward(1, B, T, H, dqk, m, W, phi_mode, q, qdt, k, kdt, g, gdt, v, vdt, dout, odt,
+                        tau, null_b, qk_normalized, dq, dk, dg, dv);
 }
 
 /* Number of OpenMP threads the oracle runs on. */
