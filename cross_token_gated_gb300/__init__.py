@@ -6,9 +6,9 @@ kernels.  PyTorch supplies device memory and streams.  There is no fallback: if
 the library cannot be loaded, every call raises.
 
 Functions (same names as the C ABI):
-  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, wango_decode_step,
-  tango_block_forward, tango_model_forward, tg_workspace_size, tg_status_string,
-  tg_check_device_error, tg_version
+  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_aggregate_backward,
+  wango_aggregate_backward, wango_decode_step, tango_block_forward, tango_model_forward,
+  tg_workspace_size, tg_status_string, tg_check_device_error, tg_version
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ TG_F32, TG_BF16 = 0, 1
 TG_FLAG_QK_NORMALIZED = 0x1
 TG_FLAG_DEBUG_TIMEOUT = 0x100
 TG_MODE_TANGO, TG_MODE_WANGO = 0, 1
-TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL, TG_WS_DECODE = 0, 1, 2, 3, 4
+TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL, TG_WS_DECODE, TG_WS_TANGO_BWD, TG_WS_WANGO_BWD = range(7)
 
 HEADER = os.path.join(_build.INCLUDE, "tango.h")
 
@@ -93,6 +93,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("tango_aggregate", "wango_aggregate"):
             f = getattr(lib, name)
             f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, sz, vp]
+            f.restype = ctypes.c_int
+        for name in ("tango_aggregate_backward", "wango_aggregate_backward"):
+            f = getattr(lib, name)
+            f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             f.restype = ctypes.c_int
         lib.tango_aggregate_noalloc.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp]
         lib.tango_aggregate_noalloc.restype = ctypes.c_int
@@ -213,6 +217,40 @@ def wango_aggregate(q, k, g, v, out, *, H, window, s=10.0, tau=None, null_bias=N
     """Windowed aggregation (eqs. 7-10); arguments as for tango_aggregate."""
     return _aggregate("wango_aggregate", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias,
                       window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream)
+
+
+def _aggregate_backward(fn_name, q, k, g, v, dout, dq, dk, dg, dv, *, H, s, tau, null_bias, window, phi_mode,
+                        flags, ws, stream):
+    B, T, d_qk = q.shape
+    m = g.shape[-1]
+    p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias,
+                   window=window, phi_mode=phi_mode, flags=flags)
+    which = TG_WS_TANGO_BWD if fn_name == "tango_aggregate_backward" else TG_WS_WANGO_BWD
+    need = load().tg_workspace_size(which, ctypes.byref(p))
+    wbuf = _workspace(need, g.device, ws)
+    wp, wn = _ws_ptr(wbuf)
+    st = getattr(load(), fn_name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(dout), _ptr(dq),
+                                  _ptr(dk), _ptr(dg), _ptr(dv), wp, wn, _stream(stream))
+    if st != TG_OK:
+        raise TgError(st, fn_name)
+    return dq, dk, dg, dv
+
+
+def tango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, s=10.0, tau=None, null_bias=None, flags=0,
+                             ws=None, stream=None):
+    """Gradients of sum(dout * tango_aggregate(q, k, g, v)) with respect to q, k, g, v
+    (bf16).  dq, dk [B, T, d_qk] and dg, dv [B, T, m] are written; v and dv may be None."""
+    return _aggregate_backward("tango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
+                               null_bias=null_bias, window=1, phi_mode=0, flags=flags, ws=ws, stream=stream)
+
+
+def wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, window, s=10.0, tau=None, null_bias=None,
+                             phi_mode=0, flags=0, ws=None, stream=None):
+    """Gradients of sum(dout * wango_aggregate(q, k, g, v)); arguments as for
+    tango_aggregate_backward."""
+    return _aggregate_backward("wango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
+                               null_bias=null_bias, window=window, phi_mode=phi_mode, flags=flags, ws=ws,
+                               stream=stream)
 
 
 def tango_aggregate_noalloc(q, k, g, v, out, *, H, s=10.0, tau=None, null_bias=None, flags=0,

@@ -251,6 +251,156 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
   return cuda_status(wango ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream));
 }
 
+// ---- aggregation backward (bf16, tensor cores)
+tg_status validate_bwd(const tg_agg_params* p, bool wango) {
+  tg_status st = validate_agg(p, wango);
+  if (st != TG_OK) return st;
+  if (p->flags & ~TG_FLAG_QK_NORMALIZED) return TG_ERR_INVALID_ARG;
+  if (p->dtype != TG_BF16) return TG_ERR_UNSUPPORTED;
+  return TG_OK;
+}
+
+struct BwdWs {
+  size_t qn, kn, gbar, den, dp, E, X, aux, erev, qrev, krev, total;
+  int T_pad;
+};
+BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
+  const size_t B = p->B, T = p->T, H = p->H, m = p->m, dqk = p->d_qk;
+  BwdWs L;
+  L.T_pad = bwd_tpad(p->T);
+  const size_t Tp = L.T_pad;
+  const bool norm = !(p->flags & TG_FLAG_QK_NORMALIZED);
+  L.qn = 0;
+  L.kn = L.qn + (norm ? align256(B * T * dqk * 2) : 0);
+  L.gbar = L.kn + (norm ? align256(B * T * dqk * 2) : 0);
+  // gbar is dead once E is formed; WANGO's reversed gate gradient reuses its space
+  L.den = L.gbar + align256(B * (wango ? Tp : T) * m * 2);
+  L.dp = L.den + (wango ? 0 : align256(B * H * Tp * 4));
+  L.E = L.dp + align256(B * H * Tp * 4);
+  L.X = L.E + align256(B * T * m * 2);
+  L.aux = L.X + align256(B * H * Tp * Tp * 2);
+  size_t aux = 0;
+  if (wango) {
+    aux = wango_aux_bytes(p->B, p->T, p->H, p->d_qk, p->m, p->window);
+    const size_t aux_rev = wango_aux_bytes(p->B, L.T_pad, p->H, p->d_qk, p->m, p->window);
+    if (aux_rev > aux) aux = aux_rev;
+  }
+  L.erev = L.aux + align256(aux);
+  L.qrev = L.erev + (wango ? align256(B * Tp * m * 2) : 0);
+  L.krev = L.qrev + (wango ? align256(B * Tp * dqk * 2) : 0);
+  L.total = L.krev + (wango ? align256(B * Tp * dqk * 2) : 0);
+  return L;
+}
+
+// Gradients of L = sum(dout * u) for u = aggregate(q, k, g, v), as laid out in
+// tango.h.  The forward is recomputed (gbar and the denominators), then:
+//   E = dout * v / den, D = E . gbar, dv = dout * gbar                       (prep)
+//   dg_j = sum_{i >= j} w_ij E_i: the forward numerator with the roles of destinations
+//     and sources exchanged (TANGO: the tensor-core kernel in reverse mode; WANGO: the
+//     windowed kernel on the time-reversed sequence, whose older-pair weights
+//     e^-tau phi(k~_j) . phi(q~_i) are the same products)
+//   X = pair-weight gradients (tensor cores), then dq, dk from X (CUDA cores).
+tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
+                             const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  tg_status st = validate_bwd(p, wango);
+  if (st != TG_OK) return st;
+  if (!q || !k || !g || !dout || !dq || !dk || !dg || (dv && !v)) return TG_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, g, dout, dq, dk, dg};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return TG_ERR_UNSUPPORTED;
+  if ((v && !aligned16(v)) || (dv && !aligned16(dv))) return TG_ERR_UNSUPPORTED;
+  const BwdWs L = bwd_ws_layout(p, wango);
+  st = check_ws(ws, ws_bytes, L.total);
+  if (st != TG_OK) return st;
+  char* base = static_cast<char*>(ws);
+  unsigned* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return TG_ERR_CUDA;
+  const long long rows = (long long)p->B * p->T;
+  const bool norm = !(p->flags & TG_FLAG_QK_NORMALIZED);
+  const void* qh = q;
+  const void* kh = k;
+  cudaError_t e = cudaSuccess;
+  if (norm) {
+    e = launch_qk_prep(p->dtype, q, base + L.qn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
+    if (e == cudaSuccess) e = launch_qk_prep(p->dtype, k, base + L.kn, rows, p->T, p->H, p->d_qk, 0.f, true, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    qh = base + L.qn;
+    kh = base + L.kn;
+  }
+  void* gbar = base + L.gbar;
+  float* dp = reinterpret_cast<float*>(base + L.dp);
+  void* E = base + L.E;
+  void* aux = base + L.aux;
+
+  // the forward again: gbar and every row's denominator
+  AggArgs a;
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = p->m;
+  a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
+  a.window = p->window; a.phi_mode = p->phi_mode; a.flags = 0; a.dtype = p->dtype;
+  a.q = qh; a.k = kh; a.g = g; a.v = nullptr; a.out = gbar; a.err = err; a.aux = aux;
+  const float* den = nullptr;
+  if (wango) {
+    e = launch_wango_tc(a, stream);
+    den = wango_den_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window);
+  } else {
+    a.den_out = reinterpret_cast<float*>(base + L.den);
+    e = launch_tango_tc(a, stream);
+    den = a.den_out;
+  }
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  e = launch_bwd_prep(dout, v, gbar, den, E, dv, dp, wango ? base + L.erev : nullptr, p->B, p->T, L.T_pad, p->H,
+                      p->m, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+
+  // dg: the numerator of the aggregation with destinations and sources exchanged
+  AggArgs r = a;
+  r.null_bias = nullptr;
+  r.no_norm = 1;
+  r.den_out = nullptr;
+  if (wango) {
+    void* grev = gbar;  // gbar has been read by the prep kernel
+    e = launch_reverse_rows(qh, base + L.qrev, p->B, p->T, L.T_pad, p->d_qk, true, stream);
+    if (e == cudaSuccess) e = launch_reverse_rows(kh, base + L.krev, p->B, p->T, L.T_pad, p->d_qk, true, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    r.T = L.T_pad;
+    r.q = base + L.krev;
+    r.k = base + L.qrev;
+    r.g = base + L.erev;
+    r.out = grev;
+    e = launch_wango_tc(r, stream);
+    if (e == cudaSuccess) e = launch_reverse_rows(grev, dg, p->B, p->T, L.T_pad, p->m, false, stream);
+  } else {
+    r.rev = 1;
+    r.q = kh;
+    r.k = qh;
+    r.g = E;
+    r.out = dg;
+    e = launch_tango_tc(r, stream);
+  }
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+
+  // pair-weight gradients, then dq and dk
+  BwdPairsArgs pa;
+  pa.B = p->B; pa.T = p->T; pa.H = p->H; pa.dqk = p->d_qk; pa.m = p->m;
+  pa.wango = wango ? 1 : 0; pa.window = p->window;
+  pa.s = p->s; pa.tau = p->tau;
+  pa.E = E; pa.g = g; pa.qhat = qh; pa.khat = kh; pa.dp = dp;
+  pa.X = base + L.X;
+  pa.err = err;
+  e = launch_bwd_pairs_tc(pa, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  BwdQKArgs qa;
+  qa.B = p->B; qa.T = p->T; qa.H = p->H; qa.dqk = p->d_qk; qa.T_pad = L.T_pad;
+  qa.wango = wango ? 1 : 0; qa.window = p->window; qa.phi_mode = p->phi_mode;
+  qa.s = p->s; qa.tau = p->tau;
+  qa.X = base + L.X; qa.qhat = qh; qa.khat = kh;
+  qa.raw_q = norm ? q : nullptr;
+  qa.raw_k = norm ? k : nullptr;
+  qa.dq = dq; qa.dk = dk; qa.err = err;
+  return cuda_status(launch_bwd_qk(qa, stream));
+}
+
 }  // namespace
 }  // namespace tg
 
@@ -266,6 +416,20 @@ tg_status tango_aggregate(const tg_agg_params* p, const void* q, const void* k, 
 tg_status wango_aggregate(const tg_agg_params* p, const void* q, const void* k, const void* g, const void* v,
                           void* out, void* ws, size_t ws_bytes, tg_stream_t stream) {
   return aggregate(true, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tango_aggregate_backward(const tg_agg_params* p, const void* q, const void* k, const void* g,
+                                   const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
+                                   size_t ws_bytes, tg_stream_t stream) {
+  return aggregate_backward(false, p, q, k, g, v, dout, dq, dk, dg, dv, ws, ws_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status wango_aggregate_backward(const tg_agg_params* p, const void* q, const void* k, const void* g,
+                                   const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
+                                   size_t ws_bytes, tg_stream_t stream) {
+  return aggregate_backward(true, p, q, k, g, v, dout, dq, dk, dg, dv, ws, ws_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 // The block forward; with pad_weights false the workspace already holds this weight
@@ -437,6 +601,12 @@ size_t tg_workspace_size(int which, const void* params) {
     const tg_agg_params* p = static_cast<const tg_agg_params*>(params);
     if (validate_decode(p) != TG_OK) return 0;
     return decode_ws_layout(p).total;
+  }
+  if (which == TG_WS_TANGO_BWD || which == TG_WS_WANGO_BWD) {
+    const tg_agg_params* p = static_cast<const tg_agg_params*>(params);
+    const bool wango = which == TG_WS_WANGO_BWD;
+    if (validate_bwd(p, wango) != TG_OK) return 0;
+    return bwd_ws_layout(p, wango).total;
   }
   if (which == TG_WS_MODEL) {
     const tg_model_params* p = static_cast<const tg_model_params*>(params);

@@ -85,6 +85,10 @@ struct Args {
   const float* tau;
   const float* null_bias;
   int has_v;
+  int rev;       // sources after the destination (j >= i) instead of before it
+  int no_norm;   // the numerator alone: no division by the denominator
+  int T_pad;
+  float* den_out;  // if set: every row's denominator, [B * H, T_pad]
   __nv_bfloat16* out;
   unsigned* err;
   uint64_t timeout_ns;
@@ -94,6 +98,11 @@ struct Args {
 struct Tile {
   int b, head, ib, n0;
 };
+
+// Source blocks of a tile, and the index of its jj-th one: blocks 0 .. ib (sources up
+// to the destination), or ib .. n_iblk - 1 in reverse mode (sources from it on).
+__device__ __forceinline__ int n_src(const Args& a, int ib) { return a.rev ? a.n_iblk - ib : ib + 1; }
+__device__ __forceinline__ int src_blk(const Args& a, int ib, int jj) { return a.rev ? ib + jj : jj; }
 
 // Walks this CTA's tiles: units u = blockIdx.x, blockIdx.x + gridDim.x, ...; a unit
 // is the pair of destination blocks (nI-1-p, p) of one (batch, head, gate tile), the
@@ -151,7 +160,7 @@ __device__ __forceinline__ uint32_t qk_layout(int d_h) {
 // and written as P at TMEM columns [32w, 32w+32) of the block's P slot; the rounded
 // weights are added to two partial denominators, each a pair of f32.  The exponent
 // argument and the sums use packed f32x2 arithmetic (two values per instruction).
-template <bool kDiag>
+template <int kDiag>  // 0: no mask; 1: sources after the row masked; 2: sources before it
 __device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p_tm, float c, int row,
                                           int src0, uint64_t (&dsum2)[2]) {
   const uint64_t cc = f32x2_pack(c, c), nc = f32x2_pack(-c, -c);
@@ -164,9 +173,12 @@ __device__ __forceinline__ void softmax64(const uint32_t (&r)[2][32], uint32_t p
       f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), cc, nc), x0, x1);
       float w0 = ex2_approx(x0);
       float w1 = ex2_approx(x1);
-      if (kDiag) {
+      if (kDiag == 1) {
         if (src0 + q * 32 + e > row) w0 = 0.f;
         if (src0 + q * 32 + e + 1 > row) w1 = 0.f;
+      } else if (kDiag == 2) {
+        if (src0 + q * 32 + e < row) w0 = 0.f;
+        if (src0 + q * 32 + e + 1 < row) w1 = 0.f;
       }
       const uint32_t pk = pack_bf16x2(w0, w1);
       dsum2[(e >> 1) & 1] = add_f32x2(dsum2[(e >> 1) & 1], bf16x2_widen(pk));
@@ -260,8 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile& t = seq.t;
       const int i0 = t.ib * kBlk;
       const int gx = t.head * a.m_h + t.n0;
-      for (int j = 0; ok && j <= t.ib; ++j)
-        for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, j * kBlk + h * kHalf, t.b);
+      const int nj = n_src(a, t.ib);
+      for (int jj = 0; ok && jj < nj; ++jj)
+        for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, src_blk(a, t.ib, jj) * kBlk + h * kHalf, t.b);
       // the tile's v, rows [i0, i0+64) and [i0+64, i0+128), for the epilogue
       for (int h = 0; ok && h < 2; ++h) ok = ring_load(a.has_v ? &tmV : nullptr, gx, i0 + h * kHalf, t.b);
     }
@@ -285,10 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sQ + qb * kQKMax, &tmQ, &b.q_full[qb], t.head * a.d_h, i0, t.b);
       qmask |= 1u << qb;
       qph[qb] = qp;
-      for (int j = 0; ok && j <= t.ib; ++j) {
+      const int nj = n_src(a, t.ib);
+      for (int jj = 0; ok && jj < nj; ++jj) {
         if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
         mbar_arrive_expect_tx(&b.k_full[kr.stage], qk_bytes);
-        tma_load_3d(sK + kr.stage * kQKMax, &tmK, &b.k_full[kr.stage], t.head * a.d_h, j * kBlk, t.b);
+        tma_load_3d(sK + kr.stage * kQKMax, &tmK, &b.k_full[kr.stage], t.head * a.d_h,
+                    src_blk(a, t.ib, jj) * kBlk, t.b);
         kmask |= 1u << kr.stage;
         kph[kr.stage] = kr.phase;
         kr.next(kKStages);
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = tc & 1;
       if (!(ok = wait_bar(&b.q_full[qb], (tc >> 1) & 1, b, a))) break;
       const uint64_t qd = qdesc0 + (uint64_t)((qb * kQKMax) >> 4);
-      const int nj = seq.t.ib + 1;
+      const int nj = n_src(a, seq.t.ib);
       for (int j = 0; j < nj; ++j, ++J) {
         if (J >= 1 && !(ok = wait_bar(&b.s_free, (J - 1) & 1, b, a))) break;
         if (!(ok = wait_bar(&b.k_full[kr.stage], kr.phase, b, a))) break;
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t J = 0;  // source blocks of this CTA
     TileSeq seq;
     for (bool have = ok && seq.first(a); ok && have; have = seq.next(a)) {
-      const int nj = seq.t.ib + 1;
+      const int nj = n_src(a, seq.t.ib);
       for (int j = 0; j < nj; ++j, ++J) {
         // O += P_J G_J (two half blocks); the tile's first block overwrites O once the
         // epilogue has read the previous tile's accumulator out of TMEM.
@@ -394,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       const float c = tau * kLog2e;
       uint64_t dsum2[2] = {0, 0};  // independent partial sums, pairs of f32
-      const int nj = t.ib + 1;
+      const int nj = n_src(a, t.ib);
       for (int j = 0; j < nj; ++j, ++J) {
         const uint32_t buf = J & 1;
         const uint32_t stm = tmem + kColS0 + lane_off;
@@ -416,9 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (warp == kSoftWarp0 && lane == 0) mbar_arrive(&b.s_free);
         tc_fence_after();
-        const int src0 = (j - t.ib) * kBlk + wg * 64;  // relative to the destination block
-        if (src0 + 63 > 0) softmax64<true>(r, pw + wg * 32, c, row, src0, dsum2);
-        else softmax64<false>(r, pw + wg * 32, c, row, src0, dsum2);
+        // sources relative to the destination block; the diagonal block is masked
+        const int sb = src_blk(a, t.ib, j);
+        const int src0 = (sb - t.ib) * kBlk + wg * 64;
+        if (sb != t.ib) softmax64<0>(r, pw + wg * 32, c, row, src0, dsum2);
+        else if (a.rev) softmax64<2>(r, pw + wg * 32, c, row, src0, dsum2);
+        else softmax64<1>(r, pw + wg * 32, c, row, src0, dsum2);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -452,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (bool have = seq.first(a); ok && have; have = seq.next(a), ++tc) {
       const Tile t = seq.t;
       const int i = t.ib * kBlk + row;
-      gpos += 2 * (t.ib + 1);
+      gpos += 2 * n_src(a, t.ib);
       const int sa = gpos % kGStages, sb = (gpos + 1) % kGStages;
       const uint32_t pa = (gpos / kGStages) & 1, pb = ((gpos + 1) / kGStages) & 1;
       gpos += 2;
@@ -471,10 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ophase ^= 1;
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
-      const float inv = 1.f / den;
+      const bool row_ok = i < a.T;
+      if (a.den_out && t.n0 == 0 && row_ok) a.den_out[(size_t)(t.b * a.H + t.head) * a.T_pad + i] = den;
+      const float inv = a.no_norm ? 1.f : 1.f / den;
       const uint64_t inv2 = f32x2_pack(inv, inv), zero2 = f32x2_pack(0.f, 0.f);
       tc_fence_after();
-      const bool row_ok = i < a.T;
       const int rr = row & 63;
       const uint32_t vrow = smem_u32(sG + (row < 64 ? sa : sb) * kGStage) + rr * 128;
       const size_t grow = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_h;
@@ -566,6 +585,10 @@ cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
   a.n_units = (int)units;
   a.s = p.s; a.tau = p.tau; a.null_bias = p.null_bias;
   a.has_v = p.v != nullptr;
+  a.rev = p.rev;
+  a.no_norm = p.no_norm;
+  a.T_pad = a.n_iblk * kBlk;
+  a.den_out = p.den_out;
   a.out = static_cast<__nv_bfloat16*>(p.out);
   a.err = p.err;
   a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;

@@ -15,6 +15,7 @@ constexpr unsigned kKernTango = 1u << 8;
 constexpr unsigned kKernWango = 2u << 8;
 constexpr unsigned kKernGemm = 3u << 8;
 constexpr unsigned kKernModel = 4u << 8;  // embedding lookup
+constexpr unsigned kKernBackward = 5u << 8;
 
 // Kernels receive the address of the per-device error word (owned by api.cu) as an
 // argument, so that translation units need no relocatable device code.

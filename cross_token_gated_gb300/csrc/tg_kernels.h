@@ -26,6 +26,10 @@ struct AggArgs {
   void* out;
   unsigned* err;  // device error word
   void* aux;      // WANGO, tensor-core path: feature-map scratch (wango_aux_bytes)
+  // Backward helpers (tensor-core kernels):
+  int rev = 0;              // TANGO: sources j >= i instead of j <= i
+  int no_norm = 0;          // TANGO and WANGO: the numerator alone, no division by the denominator
+  float* den_out = nullptr; // TANGO: every row's denominator, [B * H, ceil(T / 128) * 128]
 };
 
 enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
@@ -69,6 +73,37 @@ cudaError_t launch_embed(tg_dtype dt, const int* ids, const void* E, void* h, lo
 cudaError_t launch_pad_gate(tg_dtype dt, const void* src, void* dst, long long R, long long C, int axis, int H,
                             int m_h, int m_hp, cudaStream_t s);
 cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
+
+// ---- backward helpers (backward_simt.cu), bf16 storage --------------------
+// Per (row, head): E = dout * v / den (v == NULL: dout / den) in bf16, dv = dout * gbar
+// (if dv), and D = sum_c E_c gbar_c over the head's columns into dp [B * H, T_pad];
+// e_rev (if set) receives E with the rows of every sequence reversed, row t at
+// T_pad - 1 - t, and zero rows before them.
+cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
+                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, cudaStream_t s);
+// Rows of every sequence reversed: dst[b, T_pad - 1 - t] = src[b, t] for t < T and zero
+// rows dst[b, 0 .. T_pad - T) (to_padded), or back: dst[b, t] = src[b, T_pad - 1 - t].
+cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,
+                                cudaStream_t s);
+// dq (side 0) or dk (side 1) from the pair gradients X (backward_tc.cu): window pairs
+// through the unit keys / queries, older pairs (WANGO) through the feature maps, then
+// through the unit normalisation of the raw q / k (raw == NULL: the inputs were unit
+// vectors and the gradient stops at them).
+struct BwdQKArgs {
+  int B, T, H, dqk, T_pad;
+  int wango, window, phi_mode;
+  float s;
+  const float* tau;
+  const void* X;      // [B * H, T_pad, T_pad] bf16
+  const void* qhat;   // unit q, k used by the forward
+  const void* khat;
+  const void* raw_q;  // the caller's q, k (NULL when they were unit vectors)
+  const void* raw_k;
+  void* dq;
+  void* dk;
+  unsigned* err;
+};
+cudaError_t launch_bwd_qk(const BwdQKArgs& a, cudaStream_t s);
 cudaError_t launch_wango_simt(const AggArgs& a, cudaStream_t s);
 
 }  // namespace tg

@@ -26,6 +26,28 @@ cudaError_t launch_out_tc(const void* u, const void* Wo, const void* h, void* h_
 cudaError_t launch_matmul_tc(const void* A, const void* B, void* C, int M, int N, int K, unsigned* err,
                              cudaStream_t s);
 cudaError_t launch_tango_tc(const AggArgs& a, cudaStream_t s);
+// Pair-weight gradients of the aggregation backward (backward_tc.cu): for every pair
+// j <= i of each (batch, head), X_ij = tau w_ij (E_i . g_j - D_i) for window pairs
+// (all pairs in TANGO) and E_i . g_j - D_i for older pairs (WANGO), in bf16.
+struct BwdPairsArgs {
+  int B, T, H, dqk, m;
+  int wango, window;
+  float s;
+  const float* tau;
+  const void* E;     // [B, T, m] bf16
+  const void* g;     // [B, T, m] bf16
+  const void* qhat;  // [B, T, dqk] bf16 unit
+  const void* khat;
+  const float* dp;   // [B * H, T_pad]
+  void* X;           // [B * H, T_pad, T_pad] bf16
+  unsigned* err;
+};
+cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& a, cudaStream_t s);
+// Destination rows padded to whole 128-row blocks.
+int bwd_tpad(int T);
+// Address of the per-row WANGO denominators [B * H, T_pad] inside the scratch of the
+// tensor-core path, as the last launch_wango_tc with this scratch left them.
+const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
 // Scratch bytes the tensor-core WANGO path needs in AggArgs::aux (256-byte aligned):
 // e^-tau phi(q~) and phi(k~) in bf16, per-block sums of phi(k~), the older-prefix

@@ -36,7 +36,7 @@ cudaError_t encode(CUtensorMap* map, const void* base, cuuint32_t rank, const cu
                    const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn enc = encoder();
   if (!enc) return cudaErrorNotSupported;
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box[0] * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -59,6 +59,14 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, uint64_t batch, uin
   cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
   cuuint32_t box[3] = {box_cols, box_rows, 1};
   return encode(map, base, 3, dims, strides, box);
+}
+
+cudaError_t make_tmap_4d_heads(CUtensorMap* map, const void* base, uint64_t batch, uint64_t rows, uint64_t heads,
+                               uint64_t head_cols, uint32_t box_rows, uint32_t box_cols) {
+  cuuint64_t dims[4] = {head_cols, heads, rows, batch};
+  cuuint64_t strides[3] = {head_cols * 2, heads * head_cols * 2, rows * heads * head_cols * 2};
+  cuuint32_t box[4] = {box_cols, 1, box_rows, 1};
+  return encode(map, base, 4, dims, strides, box);
 }
 
 }  // namespace tg

@@ -430,6 +430,7 @@ struct GArgs {
   unsigned* err;
   uint64_t timeout_ns;
   int debug_timeout;
+  int no_norm;                 // the numerator alone: no division by the denominator
 };
 
 struct Strip {
@@ -873,7 +874,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!ok) break;
         if (a.v) ++v_n;
         tc_fence_after();
-        const float inv = 1.f / den;
+        const float inv = a.no_norm ? 1.f : 1.f / den;
         // gbar = O / den, rounded to bf16, in registers; the accumulator is released as
         // soon as it has been read
         uint32_t gb[kNg / 2];
@@ -1126,6 +1127,10 @@ cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtenso
 
 size_t wango_aux_bytes(int B, int T, int H, int dqk, int m, int W) { return aux_layout(B, T, H, dqk, m, W).total; }
 
+const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
+  return reinterpret_cast<const float*>(static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).den);
+}
+
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   const int d_h = p.dqk / p.H, m_h = p.m / p.H;
   const int n_iblk = ceil_div(p.T, kBlk);
@@ -1188,6 +1193,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.err = p.err;
   a.debug_timeout = debug ? 1 : 0;
   a.timeout_ns = timeout_ns;
+  a.no_norm = p.no_norm;
   if (a.nseg > 1) {  // no segment's state is ready yet
     e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;

@@ -11,7 +11,9 @@ Recipe (fixed, so every caller sees the same values for the same seed):
   * aggregation-only inputs: q, k, g, v ~ N(0, 1), each [B, T, width];
   * block inputs: h ~ N(0, 1) [B, T, d], then W_q, W_k [dqk, d], W_g, W_v [m, d],
     W_o [d, m] ~ N(0, 1/fan_in), RMSNorm gain = 1;
-  * model inputs: token ids uniform over [0, vocab), tied embedding N(0, 0.02^2).
+  * model inputs: token ids uniform over [0, vocab), tied embedding N(0, 0.02^2);
+  * backward inputs: the upstream gradient dout ~ N(0, 1) [B, T, m], from its own
+    generator default_rng(seed).
 """
 from __future__ import annotations
 
@@ -50,6 +52,12 @@ def agg_inputs(B: int, T: int, dqk: int, m: int, seed: int = 0, dtype: str = "bf
     g = cast(_normal(rng, (B, T, m), g_scale), dtype)
     v = cast(_normal(rng, (B, T, m)), dtype)
     return q, k, g, v
+
+
+def upstream_grad(B: int, T: int, m: int, seed: int = 0, dtype: str = "bf16"):
+    """dout ~ N(0, 1) [B, T, m]: the gradient of a loss with respect to an aggregation output."""
+    rng = np.random.default_rng(seed)
+    return cast(_normal(rng, (B, T, m)), dtype)
 
 
 def block_inputs(B: int, T: int, d: int, dqk: int, m: int, seed: int = 0, dtype: str = "bf16"):

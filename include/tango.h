@@ -11,6 +11,9 @@
  *   - tango_model_forward  the language model of sec. 2.3: token embedding, the shared block
  *                          applied n times (eq. 11), final RMSNorm and tied logits; with
  *                          one weight set, or with the revision's gated-projection sets
+ *   - tango_aggregate_backward, wango_aggregate_backward
+ *                          gradients of the two aggregations (eq. 5 differentiated with
+ *                          respect to q, k, g and v), for training (sec. 3)
  *
  * Conventions shared by every call:
  *   - Every pointer argument named as "device" is a CUDA device pointer owned by the
@@ -77,6 +80,8 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 #define TG_WS_BLOCK 2 /* params: const tg_block_params* */
 #define TG_WS_MODEL 3 /* params: const tg_model_params* */
 #define TG_WS_DECODE 4 /* params: const tg_agg_params*: bytes of the wango_decode_step state */
+#define TG_WS_TANGO_BWD 5 /* params: const tg_agg_params*: tango_aggregate_backward */
+#define TG_WS_WANGO_BWD 6 /* params: const tg_agg_params*: wango_aggregate_backward */
 
 #define TG_MAX_HEADS 64
 
@@ -135,6 +140,50 @@ tg_status tango_aggregate(const tg_agg_params *p, const void *q, const void *k, 
 tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, const void *g,
                           const void *v, void *out, void *ws, size_t ws_bytes,
                           tg_stream_t stream);
+
+/*
+ * Backward of tango_aggregate (sec. 2.1 eq. 5 with the weights of sec. 2.2 eq. 6):
+ * given dout = dL/d(out) for the output out = gbar * v (out = gbar when v == NULL),
+ * writes the gradients of L with respect to the call's inputs:
+ *   dv_i = dout_i * gbar_i,   dg_j = sum_{i>=j} alpha_ij (dout_i * v_i),
+ *   dq, dk through the weights alpha_ij = w_ij / den_i: with
+ *   dL/dw_ij = (dout_i * v_i) . (g_j - gbar_i) / den_i, the score gradient
+ *   tau w_ij dL/dw_ij goes to qhat_i (times khat_j) and khat_j (times qhat_i), and from
+ *   there through the unit normalisation qhat = q / max(|q|, 1e-12) of sec. 2.1 (with
+ *   TG_FLAG_QK_NORMALIZED the gradients are those of the given unit vectors).
+ * The null gate, if any, enters through the denominator; tau and null_bias receive no
+ * gradient.
+ *   p, q, k, g, v   as for the forward call (bf16 only: TG_F32 returns TG_ERR_UNSUPPORTED;
+ *                   flags may hold TG_FLAG_QK_NORMALIZED only)
+ *   dout            device [B, T, m], read only
+ *   dq, dk          device [B, T, d_qk], written
+ *   dg              device [B, T, m], written
+ *   dv              device [B, T, m], written, or NULL (must be NULL when v is NULL)
+ *   ws              device scratch of tg_workspace_size(TG_WS_TANGO_BWD, p) bytes,
+ *                   256-byte aligned.  It holds the recomputed forward (gbar and the
+ *                   denominators), E = dout * v / den, and the pair-weight gradients of
+ *                   every causal pair in bf16, B * H * T_pad^2 * 2 bytes with
+ *                   T_pad = T rounded up to a multiple of 128.
+ * Outputs must not overlap inputs or each other.  Arithmetic: bf16 operands and fp32
+ * accumulation on the tensor cores for the two T^2 m contractions; fp32 on the CUDA
+ * cores elsewhere.
+ */
+tg_status tango_aggregate_backward(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                                   const void *v, const void *dout, void *dq, void *dk, void *dg,
+                                   void *dv, void *ws, size_t ws_bytes, tg_stream_t stream);
+
+/*
+ * Backward of wango_aggregate (sec. 2.2 eqs. 7-10 in sec. 2.1 eq. 5).  Arguments,
+ * outputs and requirements as for tango_aggregate_backward; the workspace is sized by
+ * tg_workspace_size(TG_WS_WANGO_BWD, p).  Window pairs contribute as in TANGO; an older
+ * pair's weight phi(sqrt(tau) qhat_i) . phi(sqrt(tau) khat_j) passes its gradient
+ * through phi' (ELU's derivative, over sqrt(d_h) for eq. 8) and sqrt(tau).  dg is the
+ * forward numerator of the time-reversed sequence (linear in T); the weight gradients
+ * of the older pairs are formed pair by pair, so that part costs T^2 m like TANGO's.
+ */
+tg_status wango_aggregate_backward(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                                   const void *v, const void *dout, void *dq, void *dk, void *dg,
+                                   void *dv, void *ws, size_t ws_bytes, tg_stream_t stream);
 
 /*
  * One autoregressive step of the windowed aggregation (sec. 2.2 eqs. 7-10) for B
@@ -291,7 +340,8 @@ const char *tg_status_string(tg_status s);
  * Returns TG_OK, TG_ERR_TIMEOUT or TG_ERR_DEVICE (the first kind recorded), or
  * TG_ERR_CUDA if the synchronisation itself failed.  If `detail` is not NULL it
  * receives the raw word (bit 0: timeout, bit 1: value out of range; bits 8..15:
- * the kernel that recorded it, 1 = TANGO, 2 = WANGO, 3 = GEMM, 4 = embedding lookup).
+ * the kernel that recorded it, 1 = TANGO, 2 = WANGO, 3 = GEMM, 4 = embedding lookup,
+ * 5 = the aggregation backward).
  */
 tg_status tg_check_device_error(tg_stream_t stream, unsigned *detail);
 

@@ -213,3 +213,28 @@ def test_decode_state_size_and_validation(lib):
         tg.TG_ERR_INVALID_ARG
     assert raw.wango_decode_step(ctypes.byref(p), 0, 256, 256, 256, None, 256, None, 0, None) == \
         tg.TG_ERR_WORKSPACE
+
+
+def test_backward_validation_and_workspace(lib):
+    """The backward entry points validate on the host: bf16 only, only the unit-input
+    flag, v needed for dv, aligned pointers, a workspace that holds the recomputed
+    forward, E and the bf16 pair gradients of B * H * T_pad^2 entries."""
+    raw = tg.load()
+    p = _agg(B=2, T=300, H=2, d_qk=128, m=512)
+    for which in (tg.TG_WS_TANGO_BWD, tg.TG_WS_WANGO_BWD):
+        need = tg.tg_workspace_size(which, p)
+        assert need >= 2 * 2 * 384 * 384 * 2 + 2 * 300 * 512 * 2 * 2
+    assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, p) > tg.tg_workspace_size(tg.TG_WS_TANGO_BWD, p)
+    assert tg.tg_workspace_size(tg.TG_WS_TANGO_BWD, _agg(dtype=tg.TG_F32)) == 0
+    a = [256] * 9
+    for fn in (raw.tango_aggregate_backward, raw.wango_aggregate_backward):
+        assert fn(ctypes.byref(_agg(dtype=tg.TG_F32)), *a, None, 0, None) == tg.TG_ERR_UNSUPPORTED
+        assert fn(ctypes.byref(_agg(flags=tg.TG_FLAG_DEBUG_TIMEOUT)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
+        assert fn(ctypes.byref(_agg(B=0)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
+        # dv without v
+        assert fn(ctypes.byref(p), 256, 256, 256, None, 256, 256, 256, 256, 256, None, 0, None) == \
+            tg.TG_ERR_INVALID_ARG
+        # misaligned dout
+        assert fn(ctypes.byref(p), 256, 256, 256, 256, 264, 256, 256, 256, 256, None, 0, None) == \
+            tg.TG_ERR_UNSUPPORTED
+        assert fn(ctypes.byref(p), *a, None, 0, None) == tg.TG_ERR_WORKSPACE
