@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--decode-only", action="store_true",
                     help="only run WANGO decode steps (W=256) for --agg-B sequences: W + --agg-iters "
                          "steps (for profiler captures)")
+    ap.add_argument("--bwd-only", choices=["tango", "wango"],
+                    help="only run one aggregation backward at --agg-B, --agg-T (for profiler captures)")
     ap.add_argument("--agg-B", type=int, default=2)
     ap.add_argument("--agg-T", type=int, default=2048)
     ap.add_argument("--agg-iters", type=int, default=3)
@@ -236,6 +238,9 @@ def main():
         return
     if args.agg_only:
         run_agg_only(args)
+        return
+    if args.bwd_only:
+        run_bwd_only(args)
         return
     if args.block_only:
         run_block_only(args)
@@ -475,7 +480,8 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
       tied embedding): one set of m=28,480 and three sets of m=9,494, with per-kernel
       device times;
     - WANGO decode steps (W=256) at B=1 and B=8, timed as one CUDA-graph replay of 64
-      consecutive steps."""
+      consecutive steps;
+    - the backward of both aggregations at B=8 T=2048, with per-kernel device times."""
     import torch
     from cross_token_gated_gb300 import synth  # noqa: F401  (the recipe the weights follow)
     res = {}
@@ -515,6 +521,35 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     res["t_sweep_B1"] = {kind: {str(t): prev[(kind, t)] for t in (1024, 2048, 4096, 8192)}
                          for kind in ("tango", "wango")}
     res["t_sweep_B1"]["unit"] = "ms"
+
+    # ---- the aggregation backward (B=8, T=2048; WANGO with W=256)
+    q, k = unit(B, T), unit(B, T)
+    g = torch.randn(B, T, M, device=dev, generator=gen).bfloat16()
+    v = torch.randn(B, T, M, device=dev, generator=gen).bfloat16()
+    dout = torch.randn(B, T, M, device=dev, generator=gen).bfloat16()
+    dq, dk, dg, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(g), torch.empty_like(g)
+    for kind in ("tango", "wango"):
+        which = tg.TG_WS_TANGO_BWD if kind == "tango" else tg.TG_WS_WANGO_BWD
+        p = tg.agg_params(B, T, H, DQK, M, dtype=tg.TG_BF16, window=256, flags=tg.TG_FLAG_QK_NORMALIZED)
+        wsb = torch.empty(tg.tg_workspace_size(which, p) + 256, dtype=torch.uint8, device=dev)
+        if kind == "tango":
+            f = lambda: tg.tango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H,
+                                                    flags=tg.TG_FLAG_QK_NORMALIZED, ws=wsb, stream=stream)
+            fl = acc.tango_bwd_flops(B, T, DQK, M)
+        else:
+            f = lambda: tg.wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H, window=256,
+                                                    flags=tg.TG_FLAG_QK_NORMALIZED, ws=wsb, stream=stream)
+            fl = acc.wango_bwd_flops(B, T, DQK, M, H, 256)
+        ms = event_ms(f, dev, stream, reps=5)
+        by = acc.agg_bwd_bytes(B, T, DQK, M)
+        res[f"{kind}_backward_B{B}_T{T}"] = {
+            "ms": ms, "tokens_per_s": B * T / (ms * 1e-3), "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf, "gbs": by / (ms * 1e-3) / 1e9,
+            "algorithmic_tflop": fl / 1e12, "kernels": kernel_breakdown(f, dev)}
+        del wsb
+        torch.cuda.empty_cache()
+    del q, k, g, v, dout, dq, dk, dg, dv
+    torch.cuda.empty_cache()
 
     # ---- the WANGO block step (B=8, T=2048, W=256)
     def block_weights(d, m, n_sets=1):
@@ -621,6 +656,37 @@ def run_agg_only(args):
     dt = (time.perf_counter() - t0) / args.agg_iters
     print(json.dumps({"agg_only": args.agg_only, "B": b, "T": t_len, "status": st, "word": word,
                       "wall_ms_per_launch": dt * 1e3}))
+    if st != tg.TG_OK:
+        sys.exit(1)
+
+
+def run_bwd_only(args):
+    """A few backward calls of one aggregation (W = 256 for WANGO) at --agg-B, --agg-T,
+    for profiler captures; prints one timing line."""
+    import torch
+
+    import cross_token_gated_gb300 as tg
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    b, t_len = args.agg_B, args.agg_T
+
+    def unit():
+        x = torch.randn(b, t_len, H, DQK // H, device=dev, generator=gen)
+        return (x / x.norm(dim=-1, keepdim=True)).reshape(b, t_len, DQK).bfloat16()
+    q, k = unit(), unit()
+    g, v, dout = (torch.randn(b, t_len, M, device=dev, generator=gen).bfloat16() for _ in range(3))
+    dq, dk, dg, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(g), torch.empty_like(g)
+    fn = tg.tango_aggregate_backward if args.bwd_only == "tango" else tg.wango_aggregate_backward
+    kw = {} if args.bwd_only == "tango" else {"window": 256}
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.agg_iters):
+        fn(q, k, g, v, dout, dq, dk, dg, dv, H=H, flags=tg.TG_FLAG_QK_NORMALIZED, **kw)
+    st, word = tg.tg_check_device_error()
+    dt = (time.perf_counter() - t0) / args.agg_iters
+    print(json.dumps({"bwd_only": args.bwd_only, "B": b, "T": t_len, "status": st, "word": word,
+                      "wall_ms_per_call": dt * 1e3}))
     if st != tg.TG_OK:
         sys.exit(1)
 

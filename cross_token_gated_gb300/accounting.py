@@ -99,6 +99,29 @@ def model_flops(B: int, T: int, d: int, dqk: int, m: int, vocab: int, n_apps: in
     return n_apps * block_flops(B, T, d, dqk, m, mode, H, W) + logits_flops(B, T, d, vocab)
 
 
+def tango_bwd_flops(B: int, T: int, dqk: int, m: int) -> int:
+    """Gradients of the TANGO aggregation per causal pair: the gate gradient
+    sum_i alpha_ij dgbar_i and the weight gradient dgbar_i . g_j (m MACs each), the score
+    and its two gradients into qhat and khat (dqk MACs each).  The recomputed forward is
+    not counted (a training step may keep gbar and the denominators instead)."""
+    return 2 * B * causal_pairs(T) * (2 * m + 3 * dqk)
+
+
+def wango_bwd_flops(B: int, T: int, dqk: int, m: int, H: int, W: int) -> int:
+    """Gradients of the WANGO aggregation at its linear cost: window pairs as in TANGO,
+    and per token with an older prefix five d_h x m contractions against the running
+    sums (the gate gradient through the reverse sum of phi(q~) dgbar^T and its update,
+    the feature-map gradients S dgbar and R g, and the forward sum's update)."""
+    d_h = dqk // H
+    n_old = max(0, T - W)
+    return 2 * B * (window_pairs(T, W) * (2 * m + 3 * dqk) + 5 * n_old * (d_h * m + dqk))
+
+
+def agg_bwd_bytes(B: int, T: int, dqk: int, m: int, elem: int = 2) -> int:
+    """q, k, g, v and dout read once; dq, dk, dg and dv written once."""
+    return B * T * (4 * dqk + 5 * m) * elem
+
+
 def decode_bytes(B: int, dqk: int, m: int, H: int, W: int, elem: int = 2) -> int:
     """One WANGO decode step: the ring of W gate vectors read, the f32 state S read and
     written, and this token's g, v read and u written (sec. 2.2 eq. 10 taken one token

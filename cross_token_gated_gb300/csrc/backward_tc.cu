@@ -26,8 +26,9 @@
 //               tile's products
 //   warps 2-9   epilogue, two warps per TMEM lane quarter (columns [0, 128) and
 //               [128, 256)): the score qhat_i . khat_j on the CUDA cores from the keys in
-//               shared memory, the weight, X in bf16, staged in 64-column boxes and
-//               written by TMA stores
+//               shared memory, the weight, and X in bf16, each thread storing 64-byte
+//               pieces of its own row (no staging: the shared memory goes to a fourth
+//               operand stage)
 // Every wait is bounded; on expiry the kernel records a timeout and all roles leave.
 #include "tg_common.cuh"
 #include "tg_ptx.cuh"
@@ -40,11 +41,10 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kABytes = BM * BK * 2;      // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;      // 32 KB
 constexpr uint32_t kKeyBytes = BN * 64 * 2;    // 32 KB: 256 unit keys at d_h <= 64
-constexpr uint32_t kOutBytes = BM * 64 * 2;    // 16 KB: one 128 x 64 box of X per column half
 constexpr int kThreads = 320;
 constexpr int kEpiWarp0 = 2;
 
@@ -55,7 +55,7 @@ struct __align__(8) Bars {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kKeyBytes + 2 * kOutBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kKeyBytes + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
@@ -67,6 +67,7 @@ struct Args {
   const __nv_bfloat16* qhat;  // [B, T, H * d_h], unit per head
   int dqk;
   const float* dp;            // D_i: [B * H, T_pad]
+  __nv_bfloat16* X;           // [B * H, T_pad, T_pad]
   unsigned* err;
   uint64_t timeout_ns;
 };
@@ -115,15 +116,13 @@ __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t row_bytes) {
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     agg_bwd_pairs_kernel(const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmG,
-                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmX,
-                         const Args a) {
+                         const __grid_constant__ CUtensorMap tmK, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = sA + kStages * kABytes;
   uint8_t* sKey = sB + kStages * kBBytes;
-  uint8_t* sOut = sKey + kKeyBytes;
-  Bars& b = *reinterpret_cast<Bars*>(sOut + 2 * kOutBytes);
+  Bars& b = *reinterpret_cast<Bars*>(sKey + kKeyBytes);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr uint32_t kRowBytes = DH * 2;
   constexpr uint32_t kKeyHalf = 128 * kRowBytes;  // one TMA box of 128 keys
@@ -216,8 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                // TMEM lanes 32 quarter .. + 31
     const int half = (warp - kEpiWarp0) >> 2;    // columns [128 half, 128 half + 128)
     const int lrow = quarter * 32 + lane;
-    const bool issuer = lane == 0 && (warp - kEpiWarp0) % 4 == 0;
-    const uint32_t stg = smem_u32(sOut + half * kOutBytes);
     const uint32_t key = smem_u32(sKey);
     int acc = 0, tc = 0;
     uint32_t acc_phase = 0;
@@ -249,18 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t trow = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16) + half * 128;
       const int jbase = tl.jt * BN + half * 128;
+      __nv_bfloat16* xrow = a.X + ((size_t)(tl.b * a.H + tl.head) * a.T_pad + i) * a.T_pad;
+      {
 #pragma unroll 1
-      for (int box = 0; box < 2; ++box) {
-        // this half's staging box is free once its previous store has read it
-        if (issuer) bulk_wait_group_read0();
-        named_bar_sync(2 + half, 128);
-#pragma unroll 1
-        for (int sub = 0; sub < 2; ++sub) {
-          const int cbase = box * 64 + sub * 32;
+        for (int cbase = 0; cbase < 128; cbase += 32) {
           uint32_t r[32];
           tmem_ld32(trow + cbase, r);
           tmem_ld_wait();
-          if (box == 1 && sub == 1) {  // the accumulator is free for the tile after next
+          if (cbase == 96) {  // the accumulator is free for the tile after next
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&b.acc_empty[acc]);
@@ -303,17 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[e / 2] = pack_bf16x2(x2[0], x2[1]);
           }
+          if (jbase + cbase < a.T_pad) {  // 32 whole columns inside the padded matrix
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            st_shared_v4(stg + (uint32_t)lrow * 128 + (uint32_t)(((sub * 4 + k) ^ (lrow & 7)) << 4),
-                         make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]));
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2 + half, 128);
-        if (issuer) {
-          const int x0 = jbase + box * 64;
-          if (x0 < a.T_pad) tma_store_3d(&tmX, sOut + half * kOutBytes, x0, tl.ib * BM, tl.b * a.H + tl.head);
-          bulk_commit_group();
+            for (int k = 0; k < 4; ++k)
+              st_global_v4(xrow + jbase + cbase + 8 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
       }
       // both halves have read the keys
@@ -321,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&b.key_empty);
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
-    if (issuer) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -339,13 +325,13 @@ int num_sms() {
 }
 
 template <int DH>
-cudaError_t launch_dh(const CUtensorMap& mE, const CUtensorMap& mG, const CUtensorMap& mK, const CUtensorMap& mX,
-                      const Args& a, cudaStream_t s) {
+cudaError_t launch_dh(const CUtensorMap& mE, const CUtensorMap& mG, const CUtensorMap& mK, const Args& a,
+                      cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(agg_bwd_pairs_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_tiles < num_sms() ? a.n_tiles : num_sms();
-  agg_bwd_pairs_kernel<DH><<<grid, kThreads, kSmemBytes, s>>>(mE, mG, mK, mX, a);
+  agg_bwd_pairs_kernel<DH><<<grid, kThreads, kSmemBytes, s>>>(mE, mG, mK, a);
   return cudaGetLastError();
 }
 
@@ -372,17 +358,17 @@ cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& p, cudaStream_t s) {
   a.tau = p.tau;
   a.qhat = static_cast<const __nv_bfloat16*>(p.qhat);
   a.dp = p.dp;
+  a.X = static_cast<__nv_bfloat16*>(p.X);
   a.err = p.err;
   a.timeout_ns = 2000000000ull;
-  CUtensorMap mE, mG, mK, mX;
+  CUtensorMap mE, mG, mK;
   cudaError_t e = make_tmap_4d_heads(&mE, p.E, p.B, p.T, p.H, m_h, BM, BK);
   if (e == cudaSuccess) e = make_tmap_4d_heads(&mG, p.g, p.B, p.T, p.H, m_h, BN, BK);
   if (e == cudaSuccess) e = make_tmap_3d(&mK, p.khat, p.B, p.T, p.dqk, 128, a.d_h);
-  if (e == cudaSuccess) e = make_tmap_3d(&mX, p.X, (uint64_t)p.B * p.H, a.T_pad, a.T_pad, BM, 64);
   if (e != cudaSuccess) return e;
-  if (a.d_h == 64) return launch_dh<64>(mE, mG, mK, mX, a, s);
-  if (a.d_h == 32) return launch_dh<32>(mE, mG, mK, mX, a, s);
-  if (a.d_h == 16) return launch_dh<16>(mE, mG, mK, mX, a, s);
+  if (a.d_h == 64) return launch_dh<64>(mE, mG, mK, a, s);
+  if (a.d_h == 32) return launch_dh<32>(mE, mG, mK, a, s);
+  if (a.d_h == 16) return launch_dh<16>(mE, mG, mK, a, s);
   return cudaErrorInvalidValue;
 }
 

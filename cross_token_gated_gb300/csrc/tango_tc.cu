@@ -263,7 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         gmask |= 1u << gr.stage;
         gph[gr.stage] = gr.phase;
       } else {
+        // no copy: the stage's phase completes here, and a final wait on the parity of an
+        // earlier copy into it would no longer see that copy's phase
         mbar_arrive(&b.g_full[gr.stage]);
+        gmask &= ~(1u << gr.stage);
       }
       gr.next(kGStages);
       return true;
