@@ -261,7 +261,7 @@ tg_status validate_bwd(const tg_agg_params* p, bool wango) {
 }
 
 struct BwdWs {
-  size_t qn, kn, gbar, den, dp, E, X, aux, erev, qrev, krev, total;
+  size_t qn, kn, gbar, den, dp, E, X, Xo, aux, erev, qrev, krev, total;
   int T_pad;
 };
 BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
@@ -278,7 +278,8 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
   L.dp = L.den + (wango ? 0 : align256(B * H * Tp * 4));
   L.E = L.dp + align256(B * H * Tp * 4);
   L.X = L.E + align256(B * T * m * 2);
-  L.aux = L.X + align256(B * H * Tp * Tp * 2);
+  L.Xo = L.X + align256(B * H * Tp * Tp * 2);
+  L.aux = L.Xo + (wango ? align256(B * H * Tp * Tp * 2) : 0);
   size_t aux = 0;
   if (wango) {
     aux = wango_aux_bytes(p->B, p->T, p->H, p->d_qk, p->m, p->window);
@@ -295,11 +296,13 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
 // Gradients of L = sum(dout * u) for u = aggregate(q, k, g, v), as laid out in
 // tango.h.  The forward is recomputed (gbar and the denominators), then:
 //   E = dout * v / den, D = E . gbar, dv = dout * gbar                       (prep)
+//   X, X_old = pair-weight gradients of window and older pairs, then dq, dk from them
+//     (tensor cores; WANGO's older pairs through the forward's feature maps, which are
+//     still in the scratch at that point)
 //   dg_j = sum_{i >= j} w_ij E_i: the forward numerator with the roles of destinations
 //     and sources exchanged (TANGO: the tensor-core kernel in reverse mode; WANGO: the
 //     windowed kernel on the time-reversed sequence, whose older-pair weights
-//     e^-tau phi(k~_j) . phi(q~_i) are the same products)
-//   X = pair-weight gradients (tensor cores), then dq, dk from X (CUDA cores).
+//     e^-tau phi(k~_j) . phi(q~_i) are the same products).
 tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
                              const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
                              size_t ws_bytes, cudaStream_t stream) {
@@ -353,6 +356,30 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
                       p->m, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
+  // pair-weight gradients, then dq and dk
+  BwdPairsArgs pa;
+  pa.B = p->B; pa.T = p->T; pa.H = p->H; pa.dqk = p->d_qk; pa.m = p->m;
+  pa.wango = wango ? 1 : 0; pa.window = p->window;
+  pa.s = p->s; pa.tau = p->tau;
+  pa.E = E; pa.g = g; pa.qhat = qh; pa.khat = kh; pa.dp = dp;
+  pa.X = base + L.X;
+  pa.X_old = wango ? base + L.Xo : nullptr;
+  pa.err = err;
+  e = launch_bwd_pairs_tc(pa, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+  BwdQKTcArgs qa;
+  qa.B = p->B; qa.T = p->T; qa.H = p->H; qa.dqk = p->d_qk;
+  qa.wango = wango ? 1 : 0; qa.window = p->window; qa.phi_mode = p->phi_mode;
+  qa.s = p->s; qa.tau = p->tau;
+  qa.X = pa.X; qa.X_old = pa.X_old; qa.qhat = qh; qa.khat = kh;
+  qa.fq = wango ? wango_fq_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window) : nullptr;
+  qa.fk = wango ? wango_fk_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window) : nullptr;
+  qa.raw_q = norm ? q : nullptr;
+  qa.raw_k = norm ? k : nullptr;
+  qa.dq = dq; qa.dk = dk; qa.err = err;
+  e = launch_bwd_qk_tc(qa, stream);
+  if (e != cudaSuccess) return TG_ERR_CUDA;
+
   // dg: the numerator of the aggregation with destinations and sources exchanged
   AggArgs r = a;
   r.null_bias = nullptr;
@@ -380,25 +407,7 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   }
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
-  // pair-weight gradients, then dq and dk
-  BwdPairsArgs pa;
-  pa.B = p->B; pa.T = p->T; pa.H = p->H; pa.dqk = p->d_qk; pa.m = p->m;
-  pa.wango = wango ? 1 : 0; pa.window = p->window;
-  pa.s = p->s; pa.tau = p->tau;
-  pa.E = E; pa.g = g; pa.qhat = qh; pa.khat = kh; pa.dp = dp;
-  pa.X = base + L.X;
-  pa.err = err;
-  e = launch_bwd_pairs_tc(pa, stream);
-  if (e != cudaSuccess) return TG_ERR_CUDA;
-  BwdQKArgs qa;
-  qa.B = p->B; qa.T = p->T; qa.H = p->H; qa.dqk = p->d_qk; qa.T_pad = L.T_pad;
-  qa.wango = wango ? 1 : 0; qa.window = p->window; qa.phi_mode = p->phi_mode;
-  qa.s = p->s; qa.tau = p->tau;
-  qa.X = base + L.X; qa.qhat = qh; qa.khat = kh;
-  qa.raw_q = norm ? q : nullptr;
-  qa.raw_k = norm ? k : nullptr;
-  qa.dq = dq; qa.dk = dk; qa.err = err;
-  return cuda_status(launch_bwd_qk(qa, stream));
+  return TG_OK;
 }
 
 }  // namespace

@@ -3,14 +3,7 @@
 //   bwd_prep_kernel   E = dU * v / den, dv = dU * gbar, D = E . gbar per (row, head)
 //   reverse_rows_kernel  a sequence's rows in reverse order (the WANGO gate gradient is
 //                     the forward numerator of the time-reversed problem)
-//   bwd_qk_kernel     dqhat = sum_j X_ij khat_j and dkhat = sum_i X_ij qhat_i over the
-//                     window pairs; over the older pairs (WANGO) the feature-map
-//                     gradients sum_j X_ij phi(k~_j) and sum_i X_ij e^-tau phi(q~_i),
-//                     taken through phi' and sqrt(tau); then through the unit
-//                     normalisation q^ = q / max(|q|, 1e-12) of sec. 2.1
 // All arithmetic is f32; tensors are bf16.
-#include <math.h>
-
 #include "tg_common.cuh"
 #include "tg_kernels.h"
 #include "tg_ptx.cuh"
@@ -99,175 +92,6 @@ __global__ void reverse_rows_kernel(const __nv_bfloat16* __restrict__ src, __nv_
   for (int c = threadIdx.x; c < nvec; c += blockDim.x) d[c] = s ? s[c] : make_uint4(0, 0, 0, 0);
 }
 
-// ---------------------------------------------------------------- dq / dk
-constexpr int kQKThreads = 256;
-constexpr int kRB = 64;  // own rows per CTA, partner rows per step
-
-// phi (eq. 8 with mode 0, plain ELU + 1 with mode 1) and its derivative
-__device__ __forceinline__ float phi_f(float u, int mode, float inv_sqrt_dh) {
-  const float e = u > 0.f ? u + 1.f : expf(u);
-  return mode == 0 ? fmaxf(e + 1e-4f, 1e-4f) * inv_sqrt_dh : e;
-}
-__device__ __forceinline__ float dphi_f(float u, int mode, float inv_sqrt_dh) {
-  const float d = u > 0.f ? 1.f : expf(u);
-  return mode == 0 ? d * inv_sqrt_dh : d;
-}
-
-template <int DH>
-__global__ void __launch_bounds__(kQKThreads) bwd_qk_kernel(BwdQKArgs a) {
-  extern __shared__ float sm[];
-  float* xs = sm;                    // [kRB][kRB + 1]: X of (own, partner)
-  float* pv = xs + kRB * (kRB + 1);  // [kRB][DH] partner unit vectors
-  float* fv = pv + kRB * DH;         // [kRB][DH] partner feature maps (WANGO)
-  constexpr int DG = DH / 4;         // 4-dim groups
-  constexpr int R = DH / 16;         // own rows per thread (64 rows / (256 / DG) groups)
-  const int side = blockIdx.z;       // 0: dq (own = destinations), 1: dk (own = sources)
-  const int bh = blockIdx.y, b = bh / a.H, head = bh % a.H;
-  const int own0 = blockIdx.x * kRB;
-  const int tid = threadIdx.x, dg = tid % DG, rg = tid / DG;
-  const float tau = head_tau(a.tau, a.s, head, a.err, kKernBackward);
-  const float st = sqrtf(tau), inv_sqrt_dh = rsqrtf((float)DH), etau = expf(-tau);
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.X) + (size_t)bh * a.T_pad * a.T_pad;
-  const __nv_bfloat16* partner = static_cast<const __nv_bfloat16*>(side == 0 ? a.khat : a.qhat);
-  const int nblk = (a.T + kRB - 1) / kRB;
-  const int p_lo = side == 0 ? 0 : blockIdx.x, p_hi = side == 0 ? blockIdx.x : nblk - 1;
-
-  float accA[R][4], accB[R][4];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int d = 0; d < 4; ++d) accA[r][d] = accB[r][d] = 0.f;
-
-  for (int pb = p_lo; pb <= p_hi; ++pb) {
-    const int p0 = pb * kRB;
-    __syncthreads();
-    // X tile: rows of destinations, columns of sources; stored as xs[own][partner]
-    for (int e = tid; e < kRB * kRB / 8; e += blockDim.x) {
-      const int rr = e / (kRB / 8), c8 = (e % (kRB / 8)) * 8;
-      const int i = side == 0 ? own0 + rr : p0 + rr;   // destination row of X
-      const int j0 = side == 0 ? p0 + c8 : own0 + c8;  // first source column
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (i < a.T) x = *reinterpret_cast<const uint4*>(X + (size_t)i * a.T_pad + j0);
-      const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float f = (k & 1) ? bf16hi(xv[k / 2]) : bf16lo(xv[k / 2]);
-        if (side == 0) xs[rr * (kRB + 1) + c8 + k] = f;
-        else xs[(c8 + k) * (kRB + 1) + rr] = f;
-      }
-    }
-    // partner unit vectors (and their feature maps)
-    for (int e = tid; e < kRB * DH; e += blockDim.x) {
-      const int rr = e / DH, c = e % DH, t = p0 + rr;
-      const float u = t < a.T ? __bfloat162float(partner[((size_t)b * a.T + t) * a.dqk + head * DH + c]) : 0.f;
-      pv[e] = u;
-      if (a.wango) {
-        const float f = phi_f(st * u, a.phi_mode, inv_sqrt_dh);
-        fv[e] = t < a.T ? (side == 0 ? f : etau * f) : 0.f;
-      }
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int p = 0; p < kRB; ++p) {
-      const float4 pvv = *reinterpret_cast<const float4*>(pv + p * DH + 4 * dg);
-      if (!a.wango) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float x = xs[(rg * R + r) * (kRB + 1) + p];
-          accA[r][0] = fmaf(x, pvv.x, accA[r][0]);
-          accA[r][1] = fmaf(x, pvv.y, accA[r][1]);
-          accA[r][2] = fmaf(x, pvv.z, accA[r][2]);
-          accA[r][3] = fmaf(x, pvv.w, accA[r][3]);
-        }
-      } else {
-        const float4 fvv = *reinterpret_cast<const float4*>(fv + p * DH + 4 * dg);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float x = xs[(rg * R + r) * (kRB + 1) + p];
-          const int own = own0 + rg * R + r, par = p0 + p;
-          const int dist = side == 0 ? own - par : par - own;  // i - j
-          const float xw = dist < a.window ? x : 0.f, xo = x - xw;
-          accA[r][0] = fmaf(xw, pvv.x, accA[r][0]);
-          accA[r][1] = fmaf(xw, pvv.y, accA[r][1]);
-          accA[r][2] = fmaf(xw, pvv.z, accA[r][2]);
-          accA[r][3] = fmaf(xw, pvv.w, accA[r][3]);
-          accB[r][0] = fmaf(xo, fvv.x, accB[r][0]);
-          accB[r][1] = fmaf(xo, fvv.y, accB[r][1]);
-          accB[r][2] = fmaf(xo, fvv.z, accB[r][2]);
-          accB[r][3] = fmaf(xo, fvv.w, accB[r][3]);
-        }
-      }
-    }
-  }
-  // gather the own rows' sums: sA [kRB][DH], sB [kRB][DH]
-  __syncthreads();
-  float* sA = sm;
-  float* sB = sm + kRB * DH;
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int d = 0; d < 4; ++d) {
-      sA[(rg * R + r) * DH + 4 * dg + d] = accA[r][d];
-      sB[(rg * R + r) * DH + 4 * dg + d] = accB[r][d];
-    }
-  __syncthreads();
-  // per own row (four threads, DH / 4 dims each): feature-map chain rule, then the
-  // unit normalisation
-  const int row = tid / 4, part = tid % 4;
-  const int t = own0 + row;
-  const bool ok = t < a.T;
-  const __nv_bfloat16* unit = static_cast<const __nv_bfloat16*>(side == 0 ? a.qhat : a.khat);
-  const __nv_bfloat16* raw = static_cast<const __nv_bfloat16*>(side == 0 ? a.raw_q : a.raw_k);
-  const size_t roff = ((size_t)b * a.T + (ok ? t : 0)) * a.dqk + head * DH;
-  constexpr int PD = DH / 4;
-  float u[PD], dh[PD];
-  float n2 = 0.f;
-#pragma unroll
-  for (int c = 0; c < PD; ++c) {
-    const int col = part * PD + c;
-    u[c] = ok ? __bfloat162float((raw ? raw : unit)[roff + col]) : 0.f;
-    n2 = fmaf(u[c], u[c], n2);
-  }
-  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
-  n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
-  const float nrm = sqrtf(n2);
-  const float inv_n = 1.f / fmaxf(nrm, 1e-12f);
-  float pr = 0.f;
-#pragma unroll
-  for (int c = 0; c < PD; ++c) {
-    const int col = part * PD + c;
-    const float uh = raw ? u[c] * inv_n : u[c];  // the unit vector
-    float g = sA[row * DH + col];
-    if (a.wango) {
-      const float fac = side == 0 ? st * etau : st;
-      g = fmaf(fac * dphi_f(st * uh, a.phi_mode, inv_sqrt_dh), sB[row * DH + col], g);
-    }
-    dh[c] = g;
-    u[c] = uh;
-    pr = fmaf(uh, g, pr);
-  }
-  pr += __shfl_xor_sync(0xffffffffu, pr, 1);
-  pr += __shfl_xor_sync(0xffffffffu, pr, 2);
-  if (!ok) return;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(side == 0 ? a.dq : a.dk) + roff;
-#pragma unroll
-  for (int c = 0; c < PD; ++c) {
-    float y = dh[c];
-    if (raw) y = nrm < 1e-12f ? y * 1e12f : (y - u[c] * pr) * inv_n;
-    out[part * PD + c] = __float2bfloat16_rn(y);
-  }
-}
-
-template <int DH>
-cudaError_t launch_qk_dh(const BwdQKArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (kRB * (kRB + 1) + 2 * kRB * DH);
-  cudaError_t e = cudaFuncSetAttribute(bwd_qk_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((a.T + kRB - 1) / kRB, a.B * a.H, 2);
-  bwd_qk_kernel<DH><<<grid, kQKThreads, smem, s>>>(a);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
@@ -290,14 +114,6 @@ cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_
                                                      static_cast<__nv_bfloat16*>(dst), T, T_pad, width,
                                                      to_padded ? 1 : 0);
   return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_qk(const BwdQKArgs& a, cudaStream_t s) {
-  const int d_h = a.dqk / a.H;
-  if (d_h == 64) return launch_qk_dh<64>(a, s);
-  if (d_h == 32) return launch_qk_dh<32>(a, s);
-  if (d_h == 16) return launch_qk_dh<16>(a, s);
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace tg

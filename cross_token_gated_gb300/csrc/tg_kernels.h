@@ -85,25 +85,7 @@ cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, c
 // rows dst[b, 0 .. T_pad - T) (to_padded), or back: dst[b, t] = src[b, T_pad - 1 - t].
 cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,
                                 cudaStream_t s);
-// dq (side 0) or dk (side 1) from the pair gradients X (backward_tc.cu): window pairs
-// through the unit keys / queries, older pairs (WANGO) through the feature maps, then
-// through the unit normalisation of the raw q / k (raw == NULL: the inputs were unit
-// vectors and the gradient stops at them).
-struct BwdQKArgs {
-  int B, T, H, dqk, T_pad;
-  int wango, window, phi_mode;
-  float s;
-  const float* tau;
-  const void* X;      // [B * H, T_pad, T_pad] bf16
-  const void* qhat;   // unit q, k used by the forward
-  const void* khat;
-  const void* raw_q;  // the caller's q, k (NULL when they were unit vectors)
-  const void* raw_k;
-  void* dq;
-  void* dk;
-  unsigned* err;
-};
-cudaError_t launch_bwd_qk(const BwdQKArgs& a, cudaStream_t s);
+
 cudaError_t launch_wango_simt(const AggArgs& a, cudaStream_t s);
 
 }  // namespace tg

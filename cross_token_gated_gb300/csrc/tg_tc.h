@@ -39,15 +39,42 @@ struct BwdPairsArgs {
   const void* qhat;  // [B, T, dqk] bf16 unit
   const void* khat;
   const float* dp;   // [B * H, T_pad]
-  void* X;           // [B * H, T_pad, T_pad] bf16
+  void* X;           // [B * H, T_pad, T_pad] bf16: window pairs
+  void* X_old;       // the same for older pairs (WANGO), else NULL
   unsigned* err;
 };
 cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& a, cudaStream_t s);
+// dq and dk from X and X_old on the tensor cores (backward_tc.cu): window pairs through
+// the unit vectors, older pairs through the forward's bf16 feature maps fq =
+// e^-tau phi(sqrt(tau) qhat) and fk = phi(sqrt(tau) khat) and phi', then the unit
+// normalisation of the raw q, k (raw == NULL: the gradient stops at the unit inputs).
+struct BwdQKTcArgs {
+  int B, T, H, dqk;
+  int wango, window, phi_mode;
+  float s;
+  const float* tau;
+  const void* X;
+  const void* X_old;
+  const void* qhat;
+  const void* khat;
+  const void* fq;     // WANGO only, [B, T, dqk] bf16
+  const void* fk;
+  const void* raw_q;
+  const void* raw_k;
+  void* dq;
+  void* dk;
+  unsigned* err;
+};
+cudaError_t launch_bwd_qk_tc(const BwdQKTcArgs& a, cudaStream_t s);
 // Destination rows padded to whole 128-row blocks.
 int bwd_tpad(int T);
 // Address of the per-row WANGO denominators [B * H, T_pad] inside the scratch of the
 // tensor-core path, as the last launch_wango_tc with this scratch left them.
 const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
+// The forward's bf16 feature maps e^-tau phi(sqrt(tau) qhat) and phi(sqrt(tau) khat),
+// [B, T, dqk], in the same scratch.
+const void* wango_fq_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
+const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
 // Scratch bytes the tensor-core WANGO path needs in AggArgs::aux (256-byte aligned):
 // e^-tau phi(q~) and phi(k~) in bf16, per-block sums of phi(k~), the older-prefix

@@ -1130,6 +1130,12 @@ size_t wango_aux_bytes(int B, int T, int H, int dqk, int m, int W) { return aux_
 const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
   return reinterpret_cast<const float*>(static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).den);
 }
+const void* wango_fq_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
+  return static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).fq;
+}
+const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
+  return static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).fk;
+}
 
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   const int d_h = p.dqk / p.H, m_h = p.m / p.H;
