@@ -475,7 +475,8 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
       T = 1k, 2k, 4k, 8k, with each time's ratio to the T/2 point (the full prefix grows
       quadratically in T, the window linearly); unit-normalised q/k and N(0,1) g, v
       generated on the device;
-    - the WANGO block step at B=8 T=2048 (W=256);
+    - the WANGO block step at B=8 T=2048 (W=256), with v from the projection GEMM and
+      with v formed inside the aggregation (TG_FLAG_FUSED_V);
     - the shared-block model forward at B=16 T=1024 (4 TANGO applications, 32,768-entry
       tied embedding): one set of m=28,480 and three sets of m=9,494, with per-kernel
       device times;
@@ -566,6 +567,12 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     fl = acc.block_flops(B, T, D, DQK, M, mode=1, H=H, W=256)
     res[f"wango_block_B{B}_T{T}"] = {"ms": ms, "tokens_per_s": B * T / (ms * 1e-3),
                                      "tflops": fl / (ms * 1e-3) / 1e12, "kernels": kernel_breakdown(f, dev)}
+    # the same step with v = W_v x formed inside the aggregation kernel (TG_FLAG_FUSED_V)
+    f = lambda: tg.tango_block_forward(h, w, out, H=H, mode=tg.TG_MODE_WANGO, window=256, flags=tg.TG_FLAG_FUSED_V,
+                                       ws=wsb, stream=stream)
+    ms = event_ms(f, dev, stream, reps=10)
+    res[f"wango_block_fused_v_B{B}_T{T}"] = {"ms": ms, "tokens_per_s": B * T / (ms * 1e-3),
+                                             "tflops": fl / (ms * 1e-3) / 1e12, "kernels": kernel_breakdown(f, dev)}
     del w, h, out, wsb
     torch.cuda.empty_cache()
 

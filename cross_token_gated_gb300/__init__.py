@@ -26,6 +26,7 @@ TG_OK, TG_ERR_INVALID_ARG, TG_ERR_UNSUPPORTED, TG_ERR_WORKSPACE, TG_ERR_CUDA, TG
 TG_F32, TG_BF16 = 0, 1
 TG_FLAG_QK_NORMALIZED = 0x1
 TG_FLAG_DEBUG_TIMEOUT = 0x100
+TG_FLAG_FUSED_V = 0x200
 TG_MODE_TANGO, TG_MODE_WANGO = 0, 1
 TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL, TG_WS_DECODE, TG_WS_TANGO_BWD, TG_WS_WANGO_BWD = range(7)
 
@@ -281,8 +282,9 @@ def block_params(B, T, d, H, d_qk, m, *, dtype, mode=TG_MODE_TANGO, s=10.0, tau=
 def tango_block_forward(h, weights, h_out, *, H, mode=TG_MODE_TANGO, s=10.0, tau=None, null_bias=None,
                         window=1, phi_mode=0, rms_eps=1e-6, rope_base=10000.0, flags=0, ws=None, stream=None):
     """One block application (eqs. 2-10).  h, h_out [B, T, d]; weights: dict with gamma,
-    Wq, Wk, Wg, Wv, Wo device tensors of h's dtype.  h_out may be h.  flags: 0, or
-    TG_FLAG_DEBUG_TIMEOUT (the projection GEMM's test hook)."""
+    Wq, Wk, Wg, Wv, Wo device tensors of h's dtype.  h_out may be h.  flags: 0,
+    TG_FLAG_DEBUG_TIMEOUT (the projection GEMM's test hook) and/or TG_FLAG_FUSED_V
+    (WANGO: v formed inside the aggregation instead of by the projection GEMM)."""
     B, T, d = h.shape
     d_qk, m = weights["Wq"].shape[0], weights["Wg"].shape[0]
     p = block_params(B, T, d, H, d_qk, m, dtype=_dtype_code(h), mode=mode, s=s, tau=tau,

@@ -116,10 +116,11 @@ BlockWs block_ws_layout(const tg_block_params* p) {
 tg_status validate_block(const tg_block_params* p) {
   if (!p) return TG_ERR_INVALID_ARG;
   if (p->agg.H < 1 || p->agg.m < 1 || p->agg.m % p->agg.H != 0) return TG_ERR_INVALID_ARG;
-  const tg_agg_params a = block_agg(p);
+  tg_agg_params a = block_agg(p);
+  a.flags &= ~TG_FLAG_FUSED_V;  // a block flag, checked below
   tg_status st = validate_agg(&a, p->mode == TG_MODE_WANGO);
   if (st != TG_OK) return st;
-  if (p->agg.flags & ~TG_FLAG_DEBUG_TIMEOUT) return TG_ERR_INVALID_ARG;
+  if (p->agg.flags & ~(TG_FLAG_DEBUG_TIMEOUT | TG_FLAG_FUSED_V)) return TG_ERR_INVALID_ARG;
   if (p->d < 1 || !(p->rms_eps > 0.f) || !(p->rope_base >= 0.f)) return TG_ERR_INVALID_ARG;
   if (p->mode != TG_MODE_TANGO && p->mode != TG_MODE_WANGO) return TG_ERR_INVALID_ARG;
   if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
@@ -509,8 +510,17 @@ static tg_status block_forward(const tg_block_params* p, const tg_block_weights*
     Wv = base + L.wv;
     Wo = base + L.wo;
   }
+  // on request, WANGO forms v = x W_v^T inside the aggregation (no v tensor in memory)
+  const bool fuse_v = p->mode == TG_MODE_WANGO && (p->agg.flags & TG_FLAG_FUSED_V);
+  if (fuse_v) {
+    a.v = nullptr;  // u goes to the v buffer; v itself is never stored
+    a.fuse_x = x;
+    a.fuse_wv = Wv;
+    a.fuse_d = d;
+  }
   ProjArgs pa;
   pa.x = x; pa.Wq = w->Wq; pa.Wk = w->Wk; pa.Wg = Wg; pa.Wv = Wv;
+  pa.skip_v = fuse_v ? 1 : 0;
   pa.q = qb; pa.k = kb; pa.g = gb; pa.v = vb;
   pa.M = M; pa.d = d; pa.T = ap.T; pa.H = ap.H; pa.dqk = ap.d_qk; pa.m = ap.m;
   pa.rope_base = p->rope_base; pa.err = a.err;

@@ -412,7 +412,7 @@ cudaError_t launch_proj_tc(const ProjArgs& p, cudaStream_t s) {
   a.M = p.M; a.K = p.d;
   a.n_mblk = ceil_div(p.M, BM);
   a.nb_qk = 2 * p.dqk <= BN ? 1 : 2 * p.dqk / BN;
-  a.nb_g = ceil_div(p.m, BN); a.nb_v = a.nb_g; a.nb_out = 0;
+  a.nb_g = ceil_div(p.m, BN); a.nb_v = p.skip_v ? 0 : a.nb_g; a.nb_out = 0;
   a.m_major = 0;
   a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m; a.d = p.d;
   const int d_h = p.dqk / p.H;

@@ -30,6 +30,10 @@ struct AggArgs {
   int rev = 0;              // TANGO: sources j >= i instead of j <= i
   int no_norm = 0;          // TANGO and WANGO: the numerator alone, no division by the denominator
   float* den_out = nullptr; // TANGO: every row's denominator, [B * H, ceil(T / 128) * 128]
+  // WANGO with v fused: v = x W_v^T is formed inside the aggregation (then v == NULL)
+  const void* fuse_x = nullptr;   // [B, T, fuse_d] bf16, the block's normalised input
+  const void* fuse_wv = nullptr;  // [m, fuse_d] bf16
+  int fuse_d = 0;                 // a multiple of 64
 };
 
 enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };

@@ -15,6 +15,7 @@ struct ProjArgs {
   float rope_base;
   unsigned* err;
   int debug_timeout;  // test hook: the GEMM times out on purpose (1 ms bound)
+  int skip_v = 0;     // no v segment (the WANGO aggregation forms v itself)
 };
 
 cudaError_t launch_proj_tc(const ProjArgs& a, cudaStream_t s);

@@ -397,17 +397,20 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kPStages = 3;                 // P ring: 128 destinations x 64 sources per stage
 constexpr uint32_t kPBox = kBlk * 64 * 2;   // 16 KB
 constexpr int kGSlots = 3;                  // G tiles (128 sources x 128 columns) kept in place
+constexpr int kGSlotsMax = kGSlots + 1;     // with v fused: the v staging tile is a fourth slot
 constexpr uint32_t kColO = 0, kColSt = 256; // O double buffer [0, 256); S^T
+constexpr uint32_t kColV = 384;             // fused v: the v tile x W_v^T, [384, 512)
 
 struct __align__(8) GBars {
   uint64_t pfull[kPStages], pempty[kPStages];
-  uint64_t gfull[kGSlots], gempty[kGSlots];
+  uint64_t gfull[kGSlotsMax], gempty[kGSlotsMax];
   uint64_t fk_full, fk_empty;  // Fk of the block's leaving source block
   uint64_t fq_full, fq_empty;  // Fq of the destination block (the read-out)
   uint64_t o_full[2], o_empty[2];
   uint64_t st_full;            // the block's read-out and state update are complete
   uint64_t sb_full;            // bf16 state copy in place for the next read-out
   uint64_t v_full;             // the destination block's v in the staging tile
+  uint64_t vacc_full, vacc_empty;  // fused v: the v tile in TMEM / read out of it
   uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
@@ -431,6 +434,8 @@ struct GArgs {
   uint64_t timeout_ns;
   int debug_timeout;
   int no_norm;                 // the numerator alone: no division by the denominator
+  int fuse;                    // v = x W_v^T computed here (v == NULL, reuse == 0)
+  int nkc;                     // fused v: 64-column chunks of the residual width d
 };
 
 struct Strip {
@@ -558,7 +563,8 @@ template <int DH, bool kSeg>
 __global__ void __launch_bounds__(kGThreads, 1)
     wango_g_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmFQ, const __grid_constant__ CUtensorMap tmFK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmU, const GArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmU,
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWv, const GArgs a) {
   constexpr int RB = DH * 2;
   constexpr uint32_t lay = DH == 64 ? kSwizzle128B : DH == 32 ? kSwizzle64B : kSwizzle32B;
   constexpr uint32_t sbo = 8u * RB;
@@ -575,16 +581,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int W = a.W;
   const bool reuse = a.reuse != 0;
+  const bool fuse = a.fuse != 0;
+  // G slots: three in place; with v fused, the v staging tile (unused then) is a fourth
+  const int nslots = fuse ? kGSlotsMax : kGSlots;
+  auto slot_ptr = [&](int s) -> uint8_t* { return s < kGSlots ? sG + s * kGStage : sU; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPStages; ++s) {
       mbar_init(&b.pfull[s], 1);
       mbar_init(&b.pempty[s], 1);
     }
-    for (int s = 0; s < kGSlots; ++s) {
+    for (int s = 0; s < kGSlotsMax; ++s) {
       mbar_init(&b.gfull[s], 1);
       mbar_init(&b.gempty[s], 1);
     }
+    mbar_init(&b.vacc_full, 1);
+    mbar_init(&b.vacc_empty, 4);
     mbar_init(&b.fk_full, 1);
     mbar_init(&b.fk_empty, 1);
     mbar_init(&b.fq_full, 1);
@@ -615,22 +627,34 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // ------------------------------------------------------------ TMA producer
     Ring pr;
     bool ok = true;
-    uint32_t gload[kGSlots] = {}, fq_n = 0, fk_n = 0;  // loads issued (slot phases)
+    uint32_t gload[kGSlotsMax] = {}, fq_n = 0, fk_n = 0;  // loads issued (slot phases)
     uint32_t pmask = 0, pph[kPStages] = {};
     int gseq = 0;  // slot counter when tiles are not kept
     Strip sp = {};
     int gx = 0, pz = 0;
     auto load_g = [&](int jb) -> bool {
-      const int s = reuse ? jb % kGSlots : (gseq++ % kGSlots);
+      const int s = reuse ? jb % kGSlots : (gseq++ % nslots);
       if (!wait_bar(&b.gempty[s], (gload[s] & 1) ^ 1, b, a)) return false;
       ++gload[s];
-      uint8_t* dst = sG + s * kGStage;
+      uint8_t* dst = slot_ptr(s);
       mbar_arrive_expect_tx(&b.gfull[s], kGStage);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
           tma_load_3d(dst + h * 2 * kGBox + c * kGBox, &tmG, &b.gfull[s], gx + 64 * c, jb * kBlk + 64 * h, sp.b);
+      return true;
+    };
+    // fused v: chunk kc of the block's x rows (128 x 64) and of the strip's W_v rows
+    // (128 gate columns x 64), together in the next slot
+    auto load_xw = [&](int ib, int kc) -> bool {
+      const int s = gseq++ % nslots;
+      if (!wait_bar(&b.gempty[s], (gload[s] & 1) ^ 1, b, a)) return false;
+      ++gload[s];
+      uint8_t* dst = slot_ptr(s);
+      mbar_arrive_expect_tx(&b.gfull[s], kGStage);
+      tma_load_3d(dst, &tmX, &b.gfull[s], kc * 64, ib * kBlk, sp.b);
+      tma_load_2d(dst + 2 * kGBox, &tmWv, &b.gfull[s], kc * 64, gx);
       return true;
     };
     auto load_fq = [&](int ib) -> bool {
@@ -687,12 +711,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
           // would hold up the P loads queued after it)
           if (ok && jb == ib && reuse && ib + 1 < it.ib1 && !(ok = load_g(ib + 1))) break;
         }
+        for (int kc = 0; ok && fuse && kc < a.nkc; ++kc) ok = load_xw(ib, kc);
       }
     }
     // no copy may be in flight when the CTA exits
     if (fq_n) mbar_wait(&b.fq_full, (fq_n - 1) & 1, a.timeout_ns);
     if (fk_n) mbar_wait(&b.fk_full, (fk_n - 1) & 1, a.timeout_ns);
-    for (int s = 0; s < kGSlots; ++s)
+    for (int s = 0; s < nslots; ++s)
       if (gload[s]) mbar_wait(&b.gfull[s], (gload[s] - 1) & 1, a.timeout_ns);
     for (int s = 0; s < kPStages; ++s)
       if (pmask & (1u << s)) mbar_wait(&b.pfull[s], pph[s], a.timeout_ns);
@@ -707,7 +732,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     bool ok = true;
     if (a.debug_timeout) ok = wait_bar(&b.never, 0, b, a);  // nothing ever arrives here
     Ring pr;
-    uint32_t guse[kGSlots] = {}, sbph = 0, fkph = 0, fqph = 0;
+    constexpr uint32_t idesc_v = idesc_bf16_f32(kBlk, kNg, false, false);  // V = X W_v^T
+    uint32_t guse[kGSlotsMax] = {}, sbph = 0, fkph = 0, fqph = 0;
     int gseq = 0, dc = 0;
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
@@ -735,7 +761,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         auto tile = [&](int jb) -> int {
           if (jb == cur_jb) return cur_slot;
           const bool loaded_now = !reuse || ib == it.ib0 || jb == ib;
-          const int s = reuse ? jb % kGSlots : (gseq++ % kGSlots);
+          const int s = reuse ? jb % kGSlots : (gseq++ % nslots);
           if (loaded_now) {
             if (!(ok = wait_bar(&b.gfull[s], guse[s] & 1, b, a))) return -1;
             ++guse[s];
@@ -752,7 +778,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (!(ok = wait_bar(&b.fk_full, fkph, b, a))) break;
           fkph ^= 1;
           tc_fence_after_nc();
-          const uint32_t gaddr = smem_u32(sG + s * kGStage);
+          const uint32_t gaddr = smem_u32(slot_ptr(s));
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const uint64_t gd = smem_desc(gaddr + hh * 2 * kGBox, kGBox, 1024, kSwizzle128B);
@@ -770,7 +796,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         for (int jb = jlo; ok && jb <= ib; ++jb) {
           const int s = tile(jb);
           if (s < 0) break;
-          const uint32_t gaddr = smem_u32(sG + s * kGStage);
+          const uint32_t gaddr = smem_u32(slot_ptr(s));
           for (int hh = 0; hh < 2; ++hh) {
             if (!(ok = wait_bar(&b.pfull[pr.stage], pr.phase, b, a))) break;
             tc_fence_after_nc();
@@ -787,6 +813,25 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (!reuse || ib + 1 == it.ib1 || jb < jlo_of(ib + 1, W)) mma_commit_nc(&b.gempty[s]);
         }
         if (!ok) break;
+        // fused v: V = X W_v^T over the residual width (after this block's P G, so that
+        // the wait for the epilogue to read the previous block's V overlaps those MMAs)
+        if (ok && fuse) {
+          if (!(ok = wait_bar(&b.vacc_empty, (dc & 1) ^ 1, b, a))) break;
+          for (int kc = 0; ok && kc < a.nkc; ++kc) {
+            const int s = gseq++ % nslots;
+            if (!(ok = wait_bar(&b.gfull[s], guse[s] & 1, b, a))) break;
+            ++guse[s];
+            tc_fence_after_nc();
+            const uint32_t xa = smem_u32(slot_ptr(s)), wa = xa + 2 * kGBox;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss_nc(tmem + kColV, smem_desc(xa + kk * 32, 16, 1024, kSwizzle128B),
+                             smem_desc(wa + kk * 32, 16, 1024, kSwizzle128B), idesc_v, (kc | kk) != 0 ? 1u : 0u);
+            mma_commit_nc(&b.gempty[s]);
+          }
+          if (!ok) break;
+          mma_commit_nc(&b.vacc_full);
+        }
         mma_commit_nc(&b.o_full[ob]);
       }
     }
@@ -844,7 +889,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const Item it = item_of<kSeg>(a, w);
       if (it.ib0 >= it.ib1) continue;
       const Strip sp = strip_of(a, it.st);
-      if (issuer && a.v) load_v(sp, it.ib0);
+      if (issuer && a.v && !fuse) load_v(sp, it.ib0);
       // the state before the first destination block: empty, or the previous
       // segment's (into TMEM for the updates, bf16 into shared memory for the read-out)
       if (kSeg && it.seg > 0 && jlo_of(it.ib0, W) > 0) {
@@ -870,6 +915,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (ib + 1 < it.ib1) copy_state(jlo_of(ib + 1, W) == 0);
         if (ok) ok = wait_bar(&b.o_full[ob], (gib >> 1) & 1, b, a);
         if (ok && a.v) ok = wait_bar(&b.v_full, v_n & 1, b, a);
+        if (ok && fuse) ok = wait_bar(&b.vacc_full, gib & 1, b, a);
         ok = named_bar_and(2, 128, ok);
         if (!ok) break;
         if (a.v) ++v_n;
@@ -890,6 +936,32 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&b.o_empty[ob]);
+        if (fuse) {
+          // v of this row in bf16 (as a separate projection would have stored it), u = gbar
+          // * v, and the row written straight from registers (the staging tile is a G slot)
+#pragma unroll
+          for (int c0 = 0; c0 < kNg; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + kColV + lane_off + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              gb[(c0 + e) / 2] = mul_bf16x2(gb[(c0 + e) / 2],
+                                            pack_bf16x2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b.vacc_empty);
+          if (row_ok) {
+#pragma unroll
+            for (int k = 0; k < kNg / 8; ++k) {
+              const int col = sp.n0 + 8 * k;
+              if (col < a.m_h)
+                st_global_v4(a.out + grow + col, gb[4 * k], gb[4 * k + 1], gb[4 * k + 2], gb[4 * k + 3]);
+            }
+          }
+          continue;
+        }
         if (!a.v) {  // without v the tile is written from scratch: the previous store must have read it
           if (issuer) bulk_wait_group_read0();
           named_bar_sync(2, 128);
@@ -1093,7 +1165,8 @@ cudaError_t launch_p(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 // run unsegmented, which has no waits between CTAs.
 template <int DH>
 cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtensorMap& mfq, const CUtensorMap& mfk,
-                     const CUtensorMap& mv, const CUtensorMap& mu, GArgs a, cudaStream_t s) {
+                     const CUtensorMap& mv, const CUtensorMap& mu, const CUtensorMap& mx, const CUtensorMap& mw, GArgs a,
+                     cudaStream_t s) {
   if (a.nseg > 1) {
     auto kern = wango_g_kernel<DH, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
@@ -1108,7 +1181,7 @@ cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtenso
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mp, mg, mfq, mfk, mv, mu, a);
+    e = cudaLaunchKernelEx(&cfg, kern, mp, mg, mfq, mfk, mv, mu, mx, mw, a);
     if (e != cudaErrorCooperativeLaunchTooLarge) return e;
     (void)cudaGetLastError();  // not sticky: clear it and run the strips whole
     a.nseg = 1;
@@ -1119,7 +1192,7 @@ cudaError_t launch_g(const CUtensorMap& mp, const CUtensorMap& mg, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_items < num_sms() ? a.n_items : num_sms();
-  kern<<<grid, kGThreads, kGSmemBytes, s>>>(mp, mg, mfq, mfk, mv, mu, a);
+  kern<<<grid, kGThreads, kGSmemBytes, s>>>(mp, mg, mfq, mfk, mv, mu, mx, mw, a);
   return cudaGetLastError();
 }
 
@@ -1157,7 +1230,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mk, mfq, mfk, mp, mg, mv, mu;
+  CUtensorMap mq, mk, mfq, mfk, mp, mg, mv, mu, mx, mw;
   e = make_tmap_3d(&mq, p.q, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mk, p.k, p.B, p.T, p.dqk, kBlk, d_h);
   if (e == cudaSuccess) e = make_tmap_3d(&mfq, fq, p.B, p.T, p.dqk, kBlk, d_h);
@@ -1166,6 +1239,10 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   if (e == cudaSuccess) e = make_tmap_3d(&mg, p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mv, p.v ? p.v : p.g, p.B, p.T, p.m, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d(&mu, p.out, p.B, p.T, p.m, 64, 64);
+  // fused v: x [B, T, d] and W_v [m, d] in 128-row x 64-column boxes
+  const bool fuse = p.fuse_x != nullptr;
+  if (e == cudaSuccess) e = fuse ? make_tmap_3d(&mx, p.fuse_x, p.B, p.T, p.fuse_d, kBlk, 64) : make_tmap_3d(&mx, p.g, p.B, p.T, p.m, 64, 64);
+  if (e == cudaSuccess) e = fuse ? make_tmap_2d(&mw, p.fuse_wv, p.m, p.fuse_d, p.fuse_d, kBlk, 64) : make_tmap_3d(&mw, p.g, p.B, p.T, p.m, 64, 64);
   if (e != cudaSuccess) return e;
 
   // weights P and the denominators, once per destination block
@@ -1190,7 +1267,9 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.nseg = L.nseg;
   a.seg_len = ceil_div(n_iblk, a.nseg);
   a.n_items = a.n_strips * a.nseg;
-  a.reuse = L.ldp / kBlk <= kGSlots ? 1 : 0;
+  a.reuse = (L.ldp / kBlk <= kGSlots && !fuse) ? 1 : 0;
+  a.fuse = fuse ? 1 : 0;
+  a.nkc = fuse ? p.fuse_d / 64 : 0;
   a.seg_state = reinterpret_cast<float*>(aux + L.seg);
   a.seg_flag = reinterpret_cast<int*>(aux + L.flag);
   a.den = den;
@@ -1204,9 +1283,9 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
     e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  return d_h == 64 ? launch_g<64>(mp, mg, mfq, mfk, mv, mu, a, s)
-                   : d_h == 32 ? launch_g<32>(mp, mg, mfq, mfk, mv, mu, a, s)
-                               : launch_g<16>(mp, mg, mfq, mfk, mv, mu, a, s);
+  return d_h == 64 ? launch_g<64>(mp, mg, mfq, mfk, mv, mu, mx, mw, a, s)
+                   : d_h == 32 ? launch_g<32>(mp, mg, mfq, mfk, mv, mu, mx, mw, a, s)
+                               : launch_g<16>(mp, mg, mfq, mfk, mv, mu, mx, mw, a, s);
 }
 
 }  // namespace tg

@@ -67,8 +67,12 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
                                         never signalled, with a ~1 ms limit, and returns
                                         TG_ERR_TIMEOUT through tg_check_device_error().
                                         tango_aggregate: the TANGO kernel; wango_aggregate:
-                                        the gate-strip kernel; tango_block_forward (the
-                                        only flag a block accepts): the projection GEMM */
+                                        the gate-strip kernel; tango_block_forward: the
+                                        projection GEMM */
+#define TG_FLAG_FUSED_V 0x200u       /* tango_block_forward, WANGO mode, bf16: v = W_v x is
+                                        formed inside the aggregation kernel instead of by
+                                        the projection GEMM (v is then never stored); see
+                                        tango_block_forward */
 
 /* tango_block_forward mode */
 #define TG_MODE_TANGO 0
@@ -220,7 +224,7 @@ typedef struct {
 
 /*
  * Block parameters: agg gives B, T, H, d_qk, m, s/tau, null_bias, window, phi_mode,
- * dtype (agg.flags must be 0 or TG_FLAG_DEBUG_TIMEOUT).  d: residual width.  mode: TG_MODE_TANGO or
+ * dtype (agg.flags: 0, TG_FLAG_DEBUG_TIMEOUT and/or TG_FLAG_FUSED_V).  d: residual width.  mode: TG_MODE_TANGO or
  * TG_MODE_WANGO.  rms_eps: RMSNorm epsilon (> 0).  rope_base: RoPE base (0 = no
  * RoPE); rotate-half pairing (c, c + d_h/2), positions 0..T-1 per sequence.
  */
@@ -240,7 +244,14 @@ typedef struct {
  * ws: device scratch of at least tg_workspace_size(TG_WS_BLOCK, p) bytes, 256-byte
  * aligned.  On return it holds, in this order, each region starting on a 256-byte
  * boundary: x [B*T, d], unit q [B*T, d_qk], unit k [B*T, d_qk], g [B*T, m'] and
- * u = gbar * v [B*T, m'] (v is overwritten in place).
+ * u = gbar * v [B*T, m'] (v is overwritten in place).  With TG_FLAG_FUSED_V (bf16 WANGO
+ * mode), v = W_v x is formed tile by tile inside the aggregation kernel (a 128-row x
+ * 128-column tile on the tensor cores, rounded to bf16 as a stored v would be) and never
+ * written to memory; the region then holds u only.  Both forms give the same v.  The
+ * fused form saves the v write and read in HBM (2 m 2 bytes per token) but streams x and
+ * a 128-row strip of W_v (256 KB at d = 512) through shared memory for every 128 x 128
+ * output tile; on GB300 it is the slower of the two (2.31 against 1.72 ms per WANGO block
+ * at B=8, T=2048, d=512, m=28,480), so it is not the default.
  * Gate width: the aggregate calls need m_h % 8 == 0 in bf16; the block does not.  In
  * bf16 it keeps each head's gates at a pitch of m_hp = m_h rounded up to a multiple
  * of 8, m' = H * m_hp: it copies W_g, W_v (rows) and W_o (columns) into the end of ws

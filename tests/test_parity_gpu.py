@@ -291,6 +291,28 @@ def test_block_wango_plain_elu(shape):
     check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
 
 
+@pytest.mark.parametrize("shape", [(2, 100, 128, 64, 512, 2, 32), (1, 2048, 512, 128, 4096, 2, 256),
+                                   (1, 300, 768, 128, 2 * 4747, 2, 64)])
+def test_block_wango_fused_v_and_separate_v(shape):
+    """With TG_FLAG_FUSED_V the WANGO block forms v = W_v x inside the aggregation kernel
+    (v never stored); by default v comes from the projection GEMM.  Both are compared with
+    the oracle in full, on shapes that cover 2 and 12 chunks of the residual width, strips
+    split into segments (few strips, long sequence), and the padded per-head gate pitch
+    (m_h = 4,747); the two paths compute v with the same chunks in the same order, so
+    their outputs agree to within a bf16 rounding of the residual."""
+    B, T, d, dqk, m, H, W = shape
+    h, w = synth.block_inputs(B, T, d, dqk, m, seed=17, dtype="bf16")
+    fused = run_block(h, w, H, 1, W, flags=tg.TG_FLAG_FUSED_V)
+    separate = run_block(h, w, H, 1, W)
+    ref = ref_block(h, w, H, 1, W)
+    h64 = h.double().numpy()
+    for out in (fused, separate):
+        check(out, ref, "bf16")
+        check(out.cpu().double() - torch.from_numpy(h64), ref - h64, "bf16")
+    diff = (fused.double() - separate.double()).abs().max().item()
+    assert diff <= 2 * 2.0 ** -8 * h.double().abs().max().item(), diff
+
+
 @pytest.mark.parametrize("mode", [0, 1])
 def test_block_output_gemm_many_tiles(mode):
     """d=1024 and B*T=5000 rows give 40 row blocks of 4 output tiles, 160 tiles for 152
