@@ -43,7 +43,7 @@ class tg_agg_params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("d_qk", ctypes.c_int),
                 ("m", ctypes.c_int), ("s", ctypes.c_float), ("tau", ctypes.c_void_p),
                 ("null_bias", ctypes.c_void_p), ("window", ctypes.c_int), ("phi_mode", ctypes.c_int),
-                ("flags", ctypes.c_uint), ("dtype", ctypes.c_int)]
+                ("flags", ctypes.c_uint), ("dtype", ctypes.c_int), ("m_pitch", ctypes.c_int)]
 
 
 class tg_block_weights(ctypes.Structure):
@@ -146,9 +146,20 @@ def _stream(stream):
 
 
 def agg_params(B, T, H, d_qk, m, *, dtype, s=10.0, tau=None, null_bias=None, window=1, phi_mode=0,
-               flags=0) -> tg_agg_params:
+               flags=0, m_pitch=0) -> tg_agg_params:
     return tg_agg_params(B, T, H, d_qk, m, float(s), _ptr(tau), _ptr(null_bias), int(window),
-                         int(phi_mode), int(flags), int(dtype))
+                         int(phi_mode), int(flags), int(dtype), int(m_pitch))
+
+
+def _gate_width(g, H, m_h):
+    """(m, m_pitch) for a gate tensor of last dimension H * pitch: the logical total width
+    H * m_h and the per-head pitch (0 when dense)."""
+    width = g.shape[-1]
+    if m_h is None:
+        return width, 0
+    if width % H != 0:
+        raise ValueError("gate tensor width must be H * m_pitch")
+    return H * int(m_h), width // H
 
 
 def status_string(status: int) -> str:
@@ -189,11 +200,11 @@ def _ws_ptr(ws):
     return aligned, ws.numel() - (aligned - p)
 
 
-def _aggregate(fn_name, q, k, g, v, out, *, H, s, tau, null_bias, window, phi_mode, flags, ws, stream):
+def _aggregate(fn_name, q, k, g, v, out, *, H, s, tau, null_bias, window, phi_mode, flags, ws, stream, m_h=None):
     B, T, d_qk = q.shape
-    m = g.shape[-1]
+    m, pitch = _gate_width(g, H, m_h)
     p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias,
-                   window=window, phi_mode=phi_mode, flags=flags)
+                   window=window, phi_mode=phi_mode, flags=flags, m_pitch=pitch)
     which = TG_WS_TANGO if fn_name == "tango_aggregate" else TG_WS_WANGO
     need = load().tg_workspace_size(which, ctypes.byref(p))
     wbuf = _workspace(need, g.device, ws)
@@ -206,26 +217,28 @@ def _aggregate(fn_name, q, k, g, v, out, *, H, s, tau, null_bias, window, phi_mo
 
 
 def tango_aggregate(q, k, g, v, out, *, H, s=10.0, tau=None, null_bias=None, flags=0, ws=None,
-                    stream=None):
+                    stream=None, m_h=None):
     """Full-prefix aggregation (eqs. 5-6).  q, k [B, T, d_qk]; g, v, out [B, T, m] on the
-    device, one storage dtype.  v may be None (then out = gbar)."""
+    device, one storage dtype.  v may be None (then out = gbar).  With m_h given, the gate
+    tensors are [B, T, H * pitch] and each head's m_h gates sit at a pitch of
+    g.shape[-1] / H columns (m_pitch in tango.h)."""
     return _aggregate("tango_aggregate", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias,
-                      window=1, phi_mode=0, flags=flags, ws=ws, stream=stream)
+                      window=1, phi_mode=0, flags=flags, ws=ws, stream=stream, m_h=m_h)
 
 
 def wango_aggregate(q, k, g, v, out, *, H, window, s=10.0, tau=None, null_bias=None, phi_mode=0,
-                    flags=0, ws=None, stream=None):
+                    flags=0, ws=None, stream=None, m_h=None):
     """Windowed aggregation (eqs. 7-10); arguments as for tango_aggregate."""
     return _aggregate("wango_aggregate", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias,
-                      window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream)
+                      window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream, m_h=m_h)
 
 
 def _aggregate_backward(fn_name, q, k, g, v, dout, dq, dk, dg, dv, *, H, s, tau, null_bias, window, phi_mode,
-                        flags, ws, stream):
+                        flags, ws, stream, m_h=None):
     B, T, d_qk = q.shape
-    m = g.shape[-1]
+    m, pitch = _gate_width(g, H, m_h)
     p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias,
-                   window=window, phi_mode=phi_mode, flags=flags)
+                   window=window, phi_mode=phi_mode, flags=flags, m_pitch=pitch)
     which = TG_WS_TANGO_BWD if fn_name == "tango_aggregate_backward" else TG_WS_WANGO_BWD
     need = load().tg_workspace_size(which, ctypes.byref(p))
     wbuf = _workspace(need, g.device, ws)
@@ -238,20 +251,21 @@ def _aggregate_backward(fn_name, q, k, g, v, dout, dq, dk, dg, dv, *, H, s, tau,
 
 
 def tango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, s=10.0, tau=None, null_bias=None, flags=0,
-                             ws=None, stream=None):
+                             ws=None, stream=None, m_h=None):
     """Gradients of sum(dout * tango_aggregate(q, k, g, v)) with respect to q, k, g, v
     (bf16).  dq, dk [B, T, d_qk] and dg, dv [B, T, m] are written; v and dv may be None."""
     return _aggregate_backward("tango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
-                               null_bias=null_bias, window=1, phi_mode=0, flags=flags, ws=ws, stream=stream)
+                               null_bias=null_bias, window=1, phi_mode=0, flags=flags, ws=ws, stream=stream,
+                               m_h=m_h)
 
 
 def wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, window, s=10.0, tau=None, null_bias=None,
-                             phi_mode=0, flags=0, ws=None, stream=None):
+                             phi_mode=0, flags=0, ws=None, stream=None, m_h=None):
     """Gradients of sum(dout * wango_aggregate(q, k, g, v)); arguments as for
     tango_aggregate_backward."""
     return _aggregate_backward("wango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
                                null_bias=null_bias, window=window, phi_mode=phi_mode, flags=flags, ws=ws,
-                               stream=stream)
+                               stream=stream, m_h=m_h)
 
 
 def tango_aggregate_noalloc(q, k, g, v, out, *, H, s=10.0, tau=None, null_bias=None, flags=0,

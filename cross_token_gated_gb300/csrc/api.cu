@@ -52,15 +52,20 @@ tg_status validate_agg(const tg_agg_params* p, bool wango) {
   if (wango && p->window < 1) return TG_ERR_INVALID_ARG;
   if (wango && p->phi_mode != 0 && p->phi_mode != 1) return TG_ERR_INVALID_ARG;
   if (p->flags & ~(TG_FLAG_QK_NORMALIZED | TG_FLAG_DEBUG_TIMEOUT)) return TG_ERR_INVALID_ARG;
+  if (p->m_pitch != 0 && p->m_pitch < p->m / p->H) return TG_ERR_INVALID_ARG;
   const int d_h = p->d_qk / p->H;
   if (d_h > 128) return TG_ERR_UNSUPPORTED;
   if ((long long)p->B * p->T > (1LL << 31) - 1) return TG_ERR_UNSUPPORTED;
+  if ((long long)p->H * (p->m_pitch ? p->m_pitch : p->m / p->H) > (1LL << 30)) return TG_ERR_UNSUPPORTED;
   if (p->dtype == TG_BF16) {
     if (d_h != 16 && d_h != 32 && d_h != 64) return TG_ERR_UNSUPPORTED;
-    if ((p->m / p->H) % 8 != 0) return TG_ERR_UNSUPPORTED;
+    if ((p->m_pitch ? p->m_pitch : p->m / p->H) % 8 != 0) return TG_ERR_UNSUPPORTED;
   }
   return TG_OK;
 }
+
+// Gate columns of a row in memory: H times the per-head pitch.
+int mem_width(const tg_agg_params* p) { return p->H * (p->m_pitch ? p->m_pitch : p->m / p->H); }
 
 // Normalised q/k copies (unless the caller passes unit vectors).
 size_t agg_qk_bytes(const tg_agg_params* p) {
@@ -121,6 +126,7 @@ tg_status validate_block(const tg_block_params* p) {
   tg_status st = validate_agg(&a, p->mode == TG_MODE_WANGO);
   if (st != TG_OK) return st;
   if (p->agg.flags & ~(TG_FLAG_DEBUG_TIMEOUT | TG_FLAG_FUSED_V)) return TG_ERR_INVALID_ARG;
+  if (p->agg.m_pitch != 0) return TG_ERR_INVALID_ARG;  // the block lays out its own gates
   if (p->d < 1 || !(p->rms_eps > 0.f) || !(p->rope_base >= 0.f)) return TG_ERR_INVALID_ARG;
   if (p->mode != TG_MODE_TANGO && p->mode != TG_MODE_WANGO) return TG_ERR_INVALID_ARG;
   if (p->rope_base > 0.f && (p->agg.d_qk / p->agg.H) % 2 != 0) return TG_ERR_INVALID_ARG;
@@ -182,6 +188,7 @@ tg_status validate_decode(const tg_agg_params* p) {
   if (!p->tau && !(p->s >= 0.f && p->s <= 20.f)) return TG_ERR_INVALID_ARG;
   if (p->window < 1 || (p->phi_mode != 0 && p->phi_mode != 1)) return TG_ERR_INVALID_ARG;
   if (p->flags & ~TG_FLAG_QK_NORMALIZED) return TG_ERR_INVALID_ARG;
+  if (p->m_pitch != 0 && p->m_pitch != p->m / p->H) return TG_ERR_UNSUPPORTED;  // dense tensors only
   if (p->d_qk / p->H > 128) return TG_ERR_UNSUPPORTED;
   return TG_OK;
 }
@@ -227,7 +234,7 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
   if (st != TG_OK) return st;
 
   AggArgs a;
-  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = p->m;
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = mem_width(p); a.m_h = p->m / p->H;
   a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
   a.window = p->window; a.phi_mode = p->phi_mode; a.flags = p->flags; a.dtype = p->dtype;
   a.g = g; a.v = v; a.out = out;
@@ -266,7 +273,7 @@ struct BwdWs {
   int T_pad;
 };
 BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
-  const size_t B = p->B, T = p->T, H = p->H, m = p->m, dqk = p->d_qk;
+  const size_t B = p->B, T = p->T, H = p->H, m = mem_width(p), dqk = p->d_qk;
   BwdWs L;
   L.T_pad = bwd_tpad(p->T);
   const size_t Tp = L.T_pad;
@@ -339,7 +346,7 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
 
   // the forward again: gbar and every row's denominator
   AggArgs a;
-  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = p->m;
+  a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = mem_width(p); a.m_h = p->m / p->H;
   a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
   a.window = p->window; a.phi_mode = p->phi_mode; a.flags = 0; a.dtype = p->dtype;
   a.q = qh; a.k = kh; a.g = g; a.v = nullptr; a.out = gbar; a.err = err; a.aux = aux;
@@ -354,12 +361,12 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   }
   if (e != cudaSuccess) return TG_ERR_CUDA;
   e = launch_bwd_prep(dout, v, gbar, den, E, dv, dp, wango ? base + L.erev : nullptr, p->B, p->T, L.T_pad, p->H,
-                      p->m, stream);
+                      mem_width(p), p->m / p->H, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
   // pair-weight gradients, then dq and dk
   BwdPairsArgs pa;
-  pa.B = p->B; pa.T = p->T; pa.H = p->H; pa.dqk = p->d_qk; pa.m = p->m;
+  pa.B = p->B; pa.T = p->T; pa.H = p->H; pa.dqk = p->d_qk; pa.m = mem_width(p); pa.m_h = p->m / p->H;
   pa.wango = wango ? 1 : 0; pa.window = p->window;
   pa.s = p->s; pa.tau = p->tau;
   pa.E = E; pa.g = g; pa.qhat = qh; pa.khat = kh; pa.dp = dp;
@@ -397,7 +404,7 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
     r.g = base + L.erev;
     r.out = grev;
     e = launch_wango_tc(r, stream);
-    if (e == cudaSuccess) e = launch_reverse_rows(grev, dg, p->B, p->T, L.T_pad, p->m, false, stream);
+    if (e == cudaSuccess) e = launch_reverse_rows(grev, dg, p->B, p->T, L.T_pad, mem_width(p), false, stream);
   } else {
     r.rev = 1;
     r.q = kh;

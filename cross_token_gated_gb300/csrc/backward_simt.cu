@@ -28,49 +28,66 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
 }
 
 // One CTA per row (b, t) of `rows` per sequence (T, or T_pad with a reversed copy, whose
-// rows t >= T only clear their slot of it).  den and dp have a row pitch of T_pad.
+// rows t >= T only clear their slot of it).  Rows are m wide in memory, H heads at a
+// pitch of m / H of which the first m_h columns are gates.  den and dp have a row pitch
+// of T_pad.
+__device__ __forceinline__ void prep8(const uint4 du, const uint4 gb, const uint4 vv, float inv, uint4& eo, uint4& dvo,
+                                      float& acc) {
+  const uint32_t dus[4] = {du.x, du.y, du.z, du.w}, gbs[4] = {gb.x, gb.y, gb.z, gb.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
+  uint32_t es[4], dvs[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float d0 = bf16lo(dus[k]), d1 = bf16hi(dus[k]);
+    const float g0 = bf16lo(gbs[k]), g1 = bf16hi(gbs[k]);
+    es[k] = pack_bf16x2(d0 * bf16lo(vs[k]) * inv, d1 * bf16hi(vs[k]) * inv);
+    acc = fmaf(bf16lo(es[k]), g0, acc);
+    acc = fmaf(bf16hi(es[k]), g1, acc);
+    dvs[k] = pack_bf16x2(d0 * g0, d1 * g1);
+  }
+  eo = make_uint4(es[0], es[1], es[2], es[3]);
+  dvo = make_uint4(dvs[0], dvs[1], dvs[2], dvs[3]);
+}
+
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ gbar,
     const float* __restrict__ den, __nv_bfloat16* __restrict__ E, __nv_bfloat16* __restrict__ dv, float* __restrict__ dp,
-    __nv_bfloat16* __restrict__ e_rev, int T, int T_pad, int rows, int H, int m) {
+    __nv_bfloat16* __restrict__ e_rev, int T, int T_pad, int rows, int H, int m, int m_h) {
   __shared__ float red[kPrepThreads / 32];
   const int b = blockIdx.x / rows, t = blockIdx.x % rows;
-  const int nvec = m / 8, m_h = m / H;
-  uint4* rev_row = e_rev ? reinterpret_cast<uint4*>(e_rev + ((size_t)b * T_pad + (T_pad - 1 - t)) * m) : nullptr;
+  const int nvec = m / 8, m_hp = m / H;
+  __nv_bfloat16* rev_row = e_rev ? e_rev + ((size_t)b * T_pad + (T_pad - 1 - t)) * m : nullptr;
   if (t >= T) {
-    for (int c = threadIdx.x; c < nvec; c += blockDim.x) rev_row[c] = make_uint4(0, 0, 0, 0);
+    for (int c = threadIdx.x; c < nvec; c += blockDim.x) reinterpret_cast<uint4*>(rev_row)[c] = make_uint4(0, 0, 0, 0);
     return;
   }
   const size_t off = ((size_t)b * T + t) * m;
-  const uint4* du4 = reinterpret_cast<const uint4*>(dout + off);
-  const uint4* v4 = v ? reinterpret_cast<const uint4*>(v + off) : nullptr;
-  const uint4* gb4 = reinterpret_cast<const uint4*>(gbar + off);
-  uint4* e4 = reinterpret_cast<uint4*>(E + off);
-  uint4* dv4 = dv ? reinterpret_cast<uint4*>(dv + off) : nullptr;
+  const bool vec = m_h % 8 == 0;
   for (int a = 0; a < H; ++a) {
     const float inv = 1.f / den[(size_t)(b * H + a) * T_pad + t];
     float acc = 0.f;
-    const int c0 = a * (m_h / 8), c1 = (a + 1) * (m_h / 8);
-    for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
-      const uint4 du = du4[c];
-      const uint4 gb = gb4[c];
-      const uint4 vv = v4 ? v4[c] : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);  // 1.0
-      const uint32_t dus[4] = {du.x, du.y, du.z, du.w}, gbs[4] = {gb.x, gb.y, gb.z, gb.w},
-                     vs[4] = {vv.x, vv.y, vv.z, vv.w};
-      uint32_t es[4], dvs[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float d0 = bf16lo(dus[k]), d1 = bf16hi(dus[k]);
-        const float g0 = bf16lo(gbs[k]), g1 = bf16hi(gbs[k]);
-        es[k] = pack_bf16x2(d0 * bf16lo(vs[k]) * inv, d1 * bf16hi(vs[k]) * inv);
-        acc = fmaf(bf16lo(es[k]), g0, acc);
-        acc = fmaf(bf16hi(es[k]), g1, acc);
-        dvs[k] = pack_bf16x2(d0 * g0, d1 * g1);
+    const size_t h0 = off + (size_t)a * m_hp;
+    if (vec) {
+      for (int c = threadIdx.x; c < m_h / 8; c += blockDim.x) {
+        const size_t o = h0 + 8 * (size_t)c;
+        const uint4 vv = v ? *reinterpret_cast<const uint4*>(v + o)
+                           : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);  // 1.0
+        uint4 eo, dvo;
+        prep8(*reinterpret_cast<const uint4*>(dout + o), *reinterpret_cast<const uint4*>(gbar + o), vv, inv, eo, dvo,
+              acc);
+        *reinterpret_cast<uint4*>(E + o) = eo;
+        if (rev_row) *reinterpret_cast<uint4*>(rev_row + (o - off)) = eo;
+        if (dv) *reinterpret_cast<uint4*>(dv + o) = dvo;
       }
-      const uint4 eo = make_uint4(es[0], es[1], es[2], es[3]);
-      e4[c] = eo;
-      if (rev_row) rev_row[c] = eo;
-      if (dv4) dv4[c] = make_uint4(dvs[0], dvs[1], dvs[2], dvs[3]);
+    } else {  // a head width that is not a multiple of 8: one column at a time
+      for (int c = threadIdx.x; c < m_h; c += blockDim.x) {
+        const size_t o = h0 + c;
+        const float d = __bfloat162float(dout[o]), gb = __bfloat162float(gbar[o]);
+        const __nv_bfloat16 e = __float2bfloat16_rn(d * (v ? __bfloat162float(v[o]) : 1.f) * inv);
+        acc = fmaf(__bfloat162float(e), gb, acc);
+        E[o] = e;
+        if (rev_row) rev_row[o - off] = e;
+        if (dv) dv[o] = __float2bfloat16_rn(d * gb);
+      }
     }
     const float tot = block_sum(acc, red);
     if (threadIdx.x == 0) dp[(size_t)(b * H + a) * T_pad + t] = tot;
@@ -95,14 +112,14 @@ __global__ void reverse_rows_kernel(const __nv_bfloat16* __restrict__ src, __nv_
 }  // namespace
 
 cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
-                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, cudaStream_t s) {
+                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h, cudaStream_t s) {
   const int rows = e_rev ? T_pad : T;
   const long long n = (long long)B * rows;
   if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
   bwd_prep_kernel<<<(unsigned)n, kPrepThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(v),
       static_cast<const __nv_bfloat16*>(gbar), den, static_cast<__nv_bfloat16*>(E), static_cast<__nv_bfloat16*>(dv),
-      dp, static_cast<__nv_bfloat16*>(e_rev), T, T_pad, rows, H, m);
+      dp, static_cast<__nv_bfloat16*>(e_rev), T, T_pad, rows, H, m, m_h);
   return cudaGetLastError();
 }
 

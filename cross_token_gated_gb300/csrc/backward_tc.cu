@@ -649,7 +649,7 @@ cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& p, cudaStream_t s) {
   Args a = {};
   a.B = p.B; a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.d_h = p.dqk / p.H;
   a.T_pad = bwd_tpad(p.T);
-  const int m_h = p.m / p.H;
+  const int m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int n_iblk = a.T_pad / BM;
   int per = 0;
   for (int ib = 0; ib < n_iblk; ++ib) per += ib / 2 + 1;
@@ -669,8 +669,8 @@ cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& p, cudaStream_t s) {
   a.err = p.err;
   a.timeout_ns = 2000000000ull;
   CUtensorMap mE, mG, mK;
-  cudaError_t e = make_tmap_4d_heads(&mE, p.E, p.B, p.T, p.H, m_h, BM, BK);
-  if (e == cudaSuccess) e = make_tmap_4d_heads(&mG, p.g, p.B, p.T, p.H, m_h, BN, BK);
+  cudaError_t e = make_tmap_4d_heads(&mE, p.E, p.B, p.T, p.H, m_h, m_hp, BM, BK);
+  if (e == cudaSuccess) e = make_tmap_4d_heads(&mG, p.g, p.B, p.T, p.H, m_h, m_hp, BN, BK);
   if (e == cudaSuccess) e = make_tmap_3d(&mK, p.khat, p.B, p.T, p.dqk, 128, a.d_h);
   if (e != cudaSuccess) return e;
   if (a.d_h == 64) return launch_dh<64>(mE, mG, mK, a, s);

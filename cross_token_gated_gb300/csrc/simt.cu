@@ -169,7 +169,7 @@ __device__ void finish_rows(const AggArgs& p, const TileThread& tt, const float*
   if (i >= p.T) return;
   if (p.null_bias) den += (float)(i + 1) * expf(p.null_bias[a] - tau);
   const float inv = 1.f / den;
-  const long long rowoff = ((long long)b * p.T + i) * p.m + (long long)a * m_h + n0;
+  const long long rowoff = ((long long)b * p.T + i) * p.m + (long long)a * (p.m / p.H) + n0;
   const T* v = static_cast<const T*>(p.v);
   T* out = static_cast<T*>(p.out);
 #pragma unroll
@@ -186,7 +186,7 @@ __device__ void finish_rows(const AggArgs& p, const TileThread& tt, const float*
 template <typename T>
 __global__ void __launch_bounds__(kThreads) tango_simt_kernel(AggArgs p) {
   extern __shared__ float sm[];
-  const int d_h = p.dqk / p.H, m_h = p.m / p.H;
+  const int d_h = p.dqk / p.H, m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int ntile = (m_h + kCols - 1) / kCols;
   const int a = blockIdx.x / ntile, n0 = (blockIdx.x % ntile) * kCols;
   const int i0 = blockIdx.y * kRows, b = blockIdx.z;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) tango_simt_kernel(AggArgs p) {
     __syncthreads();
     const int src_valid = min(kSrc, p.T - j0);
     load_rows<T>(Ks, k, seq + j0, src_valid, d_h, p.dqk, a * d_h, d_h);
-    load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_h + n0, m_h - n0);
+    load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_hp + n0, m_h - n0);
     __syncthreads();
     float part = 0.f;
 #pragma unroll
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) tango_simt_kernel(AggArgs p) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) wango_simt_kernel(AggArgs p) {
   extern __shared__ float sm[];
-  const int d_h = p.dqk / p.H, m_h = p.m / p.H;
+  const int d_h = p.dqk / p.H, m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int ntile = (m_h + kCols - 1) / kCols;
   const int a = blockIdx.x / ntile, n0 = (blockIdx.x % ntile) * kCols;
   const int b = blockIdx.z;
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) wango_simt_kernel(AggArgs p) {
       __syncthreads();
       const int src_valid = min(kSrc, p.T - j0);
       load_rows<T>(Ks, k, seq + j0, src_valid, d_h, p.dqk, a * d_h, d_h);
-      load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_h + n0, m_h - n0);
+      load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_hp + n0, m_h - n0);
       __syncthreads();
       for (int e = threadIdx.x; e < kSrc * d_h; e += kThreads) FK[e] = phi_f32(sq * Ks[e], inv_sqrt_dh, p.phi_mode);
       __syncthreads();
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) wango_simt_kernel(AggArgs p) {
       __syncthreads();
       const int src_valid = min(kSrc, new_lo - j0);
       load_rows<T>(Ks, k, seq + j0, src_valid, d_h, p.dqk, a * d_h, d_h);
-      load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_h + n0, m_h - n0);
+      load_rows<T>(Gs, g, seq + j0, src_valid, kCols, p.m, a * m_hp + n0, m_h - n0);
       __syncthreads();
       for (int e = threadIdx.x; e < kSrc * d_h; e += kThreads) {
         const int jj = e / d_h;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads) wango_simt_kernel(AggArgs p) {
 
 template <typename T>
 cudaError_t launch_agg(const AggArgs& p, cudaStream_t s, bool wango) {
-  const int d_h = p.dqk / p.H, m_h = p.m / p.H;
+  const int d_h = p.dqk / p.H, m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int ntile = (m_h + kCols - 1) / kCols;
   if (!wango) {
     const size_t smem = sizeof(float) * (size_t)(kRows * d_h + kSrc * d_h + kSrc * kCols + kRows * 33);

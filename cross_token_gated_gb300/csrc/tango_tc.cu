@@ -79,7 +79,7 @@ constexpr size_t kSmemBytes = 1024 + kQKMax * (kQBufs + kKStages) + kGStage * kG
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Args {
-  int B, T, H, dqk, m, d_h, m_h;
+  int B, T, H, dqk, m, d_h, m_h, m_hp;  // m: row width in memory, m_hp: per-head pitch
   int n_iblk, n_ntile, n_pair, n_units;
   float s;
   const float* tau;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (bool have = seq.first(a); ok && have; have = seq.next(a)) {
       const Tile& t = seq.t;
       const int i0 = t.ib * kBlk;
-      const int gx = t.head * a.m_h + t.n0;
+      const int gx = t.head * a.m_hp + t.n0;
       const int nj = n_src(a, t.ib);
       for (int jj = 0; ok && jj < nj; ++jj)
         for (int h = 0; ok && h < 2; ++h) ok = ring_load(&tmG, gx, src_blk(a, t.ib, jj) * kBlk + h * kHalf, t.b);
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int rr = row & 63;
       const uint32_t vrow = smem_u32(sG + (row < 64 ? sa : sb) * kGStage) + rr * 128;
-      const size_t grow = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_h;
+      const size_t grow = ((size_t)t.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)t.head * a.m_hp;
 #pragma unroll 1
       for (int cq = 0; cq < 4; ++cq) {
         uint32_t o[2][32];
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (hissuer) {
           const int y = t.ib * kBlk + hh * kHalf;
           if (y < a.T && !straddle && col0 + 64 <= a.m_h)
-            tma_store_3d(&tmU, sG + (hh == 0 ? sa : sb) * kGStage + cq * kGBox, t.head * a.m_h + col0, y, t.b);
+            tma_store_3d(&tmU, sG + (hh == 0 ? sa : sb) * kGStage + cq * kGBox, t.head * a.m_hp + col0, y, t.b);
           bulk_commit_group();
         }
       }
@@ -579,7 +579,7 @@ int num_sms() {
 cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
   Args a = {};
   a.B = p.B; a.T = p.T; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
-  a.d_h = p.dqk / p.H; a.m_h = p.m / p.H;
+  a.d_h = p.dqk / p.H; a.m_hp = p.m / p.H; a.m_h = p.m_h ? p.m_h : a.m_hp;
   a.n_iblk = ceil_div(p.T, kBlk);
   a.n_ntile = ceil_div(a.m_h, kNg);
   a.n_pair = (a.n_iblk + 1) / 2;

@@ -26,6 +26,9 @@ struct AggArgs {
   void* out;
   unsigned* err;  // device error word
   void* aux;      // WANGO, tensor-core path: feature-map scratch (wango_aux_bytes)
+  // m is the row width in memory, H gate blocks of m / H columns (the per-head pitch);
+  // m_h the gates of a head that are read and written (0: m / H)
+  int m_h = 0;
   // Backward helpers (tensor-core kernels):
   int rev = 0;              // TANGO: sources j >= i instead of j <= i
   int no_norm = 0;          // TANGO and WANGO: the numerator alone, no division by the denominator
@@ -84,7 +87,7 @@ cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
 // e_rev (if set) receives E with the rows of every sequence reversed, row t at
 // T_pad - 1 - t, and zero rows before them.
 cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
-                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, cudaStream_t s);
+                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h, cudaStream_t s);
 // Rows of every sequence reversed: dst[b, T_pad - 1 - t] = src[b, t] for t < T and zero
 // rows dst[b, 0 .. T_pad - T) (to_padded), or back: dst[b, t] = src[b, T_pad - 1 - t].
 cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,

@@ -31,7 +31,8 @@ cudaError_t launch_tango_tc(const AggArgs& a, cudaStream_t s);
 // j <= i of each (batch, head), X_ij = tau w_ij (E_i . g_j - D_i) for window pairs
 // (all pairs in TANGO) and E_i . g_j - D_i for older pairs (WANGO), in bf16.
 struct BwdPairsArgs {
-  int B, T, H, dqk, m;
+  int B, T, H, dqk, m;  // m: row width in memory (H x per-head pitch)
+  int m_h;              // gates per head
   int wango, window;
   float s;
   const float* tau;

@@ -19,11 +19,11 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, uint64_t batch, uint64_t rows, uint64_t cols,
                          uint32_t box_rows, uint32_t box_cols);
 
-// Over a [batch, rows, heads, head_cols] tensor (one head's columns contiguous, row
-// pitch heads * head_cols), box [1, box_rows, 1, box_cols]: columns past the end of a
-// head read as zero instead of running into the next head.  head_cols * 2 must be a
-// multiple of 16.
+// Over a [batch, rows, heads, head_pitch] tensor of which the first head_cols columns of
+// each head are read (row pitch heads * head_pitch), box [1, box_rows, 1, box_cols]:
+// columns past a head's head_cols read as zero instead of running into the padding or
+// the next head.  head_pitch * 2 must be a multiple of 16.
 cudaError_t make_tmap_4d_heads(CUtensorMap* map, const void* base, uint64_t batch, uint64_t rows, uint64_t heads,
-                               uint64_t head_cols, uint32_t box_rows, uint32_t box_cols);
+                               uint64_t head_cols, uint64_t head_pitch, uint32_t box_rows, uint32_t box_cols);
 
 }  // namespace tg

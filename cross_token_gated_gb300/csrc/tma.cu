@@ -62,9 +62,9 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, uint64_t batch, uin
 }
 
 cudaError_t make_tmap_4d_heads(CUtensorMap* map, const void* base, uint64_t batch, uint64_t rows, uint64_t heads,
-                               uint64_t head_cols, uint32_t box_rows, uint32_t box_cols) {
+                               uint64_t head_cols, uint64_t head_pitch, uint32_t box_rows, uint32_t box_cols) {
   cuuint64_t dims[4] = {head_cols, heads, rows, batch};
-  cuuint64_t strides[3] = {head_cols * 2, heads * head_cols * 2, rows * heads * head_cols * 2};
+  cuuint64_t strides[3] = {head_pitch * 2, heads * head_pitch * 2, rows * heads * head_pitch * 2};
   cuuint32_t box[4] = {box_cols, 1, box_rows, 1};
   return encode(map, base, 4, dims, strides, box);
 }

@@ -421,7 +421,8 @@ constexpr size_t kGSmemBytes =
 static_assert(kGSmemBytes <= 232448, "shared memory budget");
 
 struct GArgs {
-  int B, T, T_pad, H, dqk, m, d_h, m_h, W;
+  int B, T, T_pad, H, dqk, m, d_h, m_h, W;  // m: row width in memory, m_h: gates per head
+  int m_hp;                                 // per-head pitch (m / H)
   int n_iblk, n_ntile, n_strips;
   int nseg, seg_len, n_items;  // each strip's destination blocks in nseg segments
   int reuse;                   // every destination block has at most kGSlots source blocks
@@ -675,7 +676,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const Item it = item_of<kSeg>(a, w);
       if (it.ib0 >= it.ib1) continue;
       sp = strip_of(a, it.st);
-      gx = sp.head * a.m_h + sp.n0;
+      gx = sp.head * a.m_hp + sp.n0;
       pz = sp.b * a.H + sp.head;
       // the first block's read-out and update operands
       if (!(ok = load_fq(it.ib0))) break;
@@ -882,7 +883,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sU + h * 2 * kGBox + c * kGBox, &tmV, &b.v_full, sp.head * a.m_h + sp.n0 + 64 * c,
+          tma_load_3d(sU + h * 2 * kGBox + c * kGBox, &tmV, &b.v_full, sp.head * a.m_hp + sp.n0 + 64 * c,
                       ib * kBlk + 64 * h, sp.b);
     };
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
@@ -904,7 +905,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int i = ib * kBlk + row;
         const bool row_ok = i < a.T;
         const float den = a.den[(size_t)(sp.b * a.H + sp.head) * a.T_pad + i];
-        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_h;
+        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_hp;
         // the state after this block's update, for the next block's read-out (this
         // block's read-out and update are complete; the next block changes it only after
         // its own read-out)
@@ -1001,7 +1002,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int cq = 0; cq < 2; ++cq) {
               const int c = sp.n0 + cq * 64;
               if (c + 64 > a.m_h) continue;
-              tma_store_3d(&tmU, sU + h * 2 * kGBox + cq * kGBox, sp.head * a.m_h + c, y, sp.b);
+              tma_store_3d(&tmU, sU + h * 2 * kGBox + cq * kGBox, sp.head * a.m_hp + c, y, sp.b);
             }
           }
           bulk_commit_group();
@@ -1211,9 +1212,10 @@ const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m
 }
 
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
-  const int d_h = p.dqk / p.H, m_h = p.m / p.H;
+  const int d_h = p.dqk / p.H, m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int n_iblk = ceil_div(p.T, kBlk);
-  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk, p.m, p.window);
+  // the scratch is laid out for the logical gate width (as wango_aux_bytes is asked)
+  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk, p.H * m_h, p.window);
   const bool debug = (p.flags & TG_FLAG_DEBUG_TIMEOUT) != 0;
   const uint64_t timeout_ns = debug ? 1000000ull : 2000000000ull;
   char* aux = static_cast<char*>(p.aux);
@@ -1258,7 +1260,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   // the gate strips
   GArgs a = {};
   a.B = p.B; a.T = p.T; a.T_pad = L.T_pad; a.H = p.H; a.dqk = p.dqk; a.m = p.m;
-  a.d_h = d_h; a.m_h = m_h; a.W = p.window;
+  a.d_h = d_h; a.m_h = m_h; a.m_hp = m_hp; a.W = p.window;
   a.n_iblk = n_iblk;
   a.n_ntile = ceil_div(m_h, kNg);
   const long long strips = (long long)p.B * p.H * a.n_ntile;

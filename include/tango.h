@@ -107,8 +107,16 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
  *              1 = plain ELU(u) + 1
  *   flags      TG_FLAG_*
  *   dtype      storage type of q, k, g, v, out
- * bf16 requirements: d_h in {16, 32, 64}, m_h % 8 == 0, all tensor base
- * addresses 16-byte aligned (else TG_ERR_UNSUPPORTED).
+ *   m_pitch    gate columns per head in memory: 0 means m_h = m / H (dense).  Otherwise
+ *              >= m_h, and the gate-indexed tensors (g, v, out, and the backward's dout,
+ *              dg, dv) are [B, T, H * m_pitch] with head a's m_h gates in columns
+ *              [a*m_pitch, a*m_pitch + m_h); the other columns are not read, and in
+ *              the outputs their contents are unspecified.  This lets a head width that is not a multiple of 8 (e.g. the
+ *              revision's three-set width m = 9,494, m_h = 4,747) run in bf16 at a padded
+ *              pitch.  wango_decode_step takes dense tensors only (0 or m_h), and a
+ *              block's agg.m_pitch must be 0 (the block pads its own gates).
+ * bf16 requirements: d_h in {16, 32, 64}, the per-head pitch (m_pitch, else m_h) a
+ * multiple of 8, all tensor base addresses 16-byte aligned (else TG_ERR_UNSUPPORTED).
  */
 typedef struct {
     int B, T, H, d_qk, m;
@@ -119,6 +127,7 @@ typedef struct {
     int phi_mode;
     unsigned flags;
     tg_dtype dtype;
+    int m_pitch;
 } tg_agg_params;
 
 /*

@@ -238,3 +238,27 @@ def test_backward_validation_and_workspace(lib):
         assert fn(ctypes.byref(p), 256, 256, 256, 256, 264, 256, 256, 256, 256, None, 0, None) == \
             tg.TG_ERR_UNSUPPORTED
         assert fn(ctypes.byref(p), *a, None, 0, None) == tg.TG_ERR_WORKSPACE
+
+
+def test_gate_pitch_validation(lib):
+    """A per-head gate pitch: at least m_h, a multiple of 8 in bf16; it lets the
+    revision's three-set width (m_h = 4,747) run in bf16; blocks and decode steps take
+    none."""
+    raw = tg.load()
+    a = [256] * 5
+    dense = _agg(m=2 * 4747)
+    assert raw.tango_aggregate(ctypes.byref(dense), *a, None, 0, None) == tg.TG_ERR_UNSUPPORTED
+    for fn in (raw.tango_aggregate, raw.wango_aggregate):
+        ok = _agg(m=2 * 4747, m_pitch=4752)
+        assert fn(ctypes.byref(ok), *a, None, 0, None) == tg.TG_ERR_WORKSPACE   # valid: only the workspace is missing
+        assert fn(ctypes.byref(_agg(m=2 * 4747, m_pitch=4740)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
+        assert fn(ctypes.byref(_agg(m=2 * 4747, m_pitch=4750)), *a, None, 0, None) == tg.TG_ERR_UNSUPPORTED
+        assert fn(ctypes.byref(_agg(m=2 * 4747, m_pitch=4750, dtype=tg.TG_F32)), *a, None, 0, None) == \
+            tg.TG_ERR_WORKSPACE
+    for which in (tg.TG_WS_TANGO_BWD, tg.TG_WS_WANGO_BWD):
+        assert tg.tg_workspace_size(which, _agg(m=2 * 4747, m_pitch=4752)) > 0
+    bp = tg.block_params(1, 64, 128, 2, 128, 512, dtype=tg.TG_BF16)
+    bp.agg.m_pitch = 264
+    assert tg.tg_workspace_size(tg.TG_WS_BLOCK, bp) == 0
+    dp = _agg(m=512, m_pitch=264)
+    assert tg.tg_workspace_size(tg.TG_WS_DECODE, dp) == 0

@@ -213,3 +213,38 @@ def test_backward_full_size_properties(kind):
         dot = (dd * xx).sum(-1)
         bound = dd.norm(dim=-1) * xx.norm(dim=-1)
         assert float((dot.abs() / bound.clamp_min(1e-30)).max()) < 2e-2
+
+
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_backward_gate_pitch(kind):
+    """The backward at the three-set head width m_h = 4,747 with a per-head pitch of
+    4,752: NaN in the padding columns of g, v and dout must reach no gradient."""
+    B, T, H, dqk, m_h, pitch, W = 1, 260, 2, 128, 4747, 4752, 100
+    q, k, g, v = synth.agg_inputs(B, T, dqk, H * m_h, seed=51, dtype="bf16")
+    dout = synth.upstream_grad(B, T, H * m_h, seed=52)
+
+    def pad(t):
+        out = torch.full((B, T, H, pitch), float("nan"), dtype=t.dtype)
+        out[..., :m_h] = t.view(B, T, H, m_h)
+        return out.view(B, T, H * pitch).cuda()
+
+    gp, vp, dp_ = pad(g), pad(v), pad(dout)
+    qd, kd = q.cuda(), k.cuda()
+    dq, dk, dg, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(gp), torch.empty_like(gp)
+    if kind == "tango":
+        tg.tango_aggregate_backward(qd, kd, gp, vp, dp_, dq, dk, dg, dv, H=H, m_h=m_h)
+    else:
+        tg.wango_aggregate_backward(qd, kd, gp, vp, dp_, dq, dk, dg, dv, H=H, window=W, m_h=m_h)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    view = [synth.oracle_view(t) for t in (q, k, g, v, dout)]
+    if kind == "tango":
+        ref = oracle.tango_backward(*view, H=H, tau=10.0)
+    else:
+        ref = oracle.wango_backward(*view, H=H, tau=10.0, window=W)
+    sq, sk = grad_scales(kind, view, H, 10.0, W, 0, None, False)
+    logical = lambda t: t.view(B, T, H, pitch)[..., :m_h].reshape(B, T, H * m_h)
+    for name, t, scale in (("dq", dq, sq), ("dk", dk, sk), ("dg", logical(dg), None), ("dv", logical(dv), None)):
+        e = errs(t, ref[name], H, scale)
+        assert e["norm"] <= TOL, (name, e)
+        assert e.get("row_head", 0.0) <= 2 * TOL and e.get("row_head_cond", 0.0) <= TOL, (name, e)

@@ -580,3 +580,37 @@ def test_wango_segments_hand_over_the_state():
     scale = oracle.wango_scan(*[synth.oracle_view(t) for t in (q, k, *abs_inputs(g, v))], H=H, tau=10.0,
                               window=W)
     check(out, ref, "bf16", H, scale)
+
+
+def pitched(t, H, pitch, fill):
+    """[B, T, H*m_h] -> [B, T, H*pitch] with each head's gates first and `fill` after them."""
+    B, T, m = t.shape
+    m_h = m // H
+    out = torch.full((B, T, H, pitch), fill, dtype=t.dtype)
+    out[..., :m_h] = t.view(B, T, H, m_h)
+    return out.view(B, T, H * pitch)
+
+
+@pytest.mark.parametrize("kind,W", [("tango", 1), ("wango", 16), ("wango", 300)])
+@pytest.mark.parametrize("dtype,pitch", [("bf16", 4752), ("f32", 4750)])
+def test_agg_gate_pitch(kind, W, dtype, pitch):
+    """The revision's three-set head width m_h = 4,747 through the aggregate calls at a
+    padded per-head pitch (m_pitch): the padding columns of g and v hold NaN, which must
+    reach no gate column (the padding columns of the output are unspecified)."""
+    B, T, H, dqk, m_h = 1, 300, 2, 128, 4747
+    q, k, g, v = synth.agg_inputs(B, T, dqk, H * m_h, seed=41, dtype=dtype)
+    gp, vp = (pitched(t, H, pitch, float("nan")).cuda() for t in (g, v))
+    out = torch.full_like(gp, 7.0)
+    kw = dict(H=H, m_h=m_h)
+    if kind == "tango":
+        tg.tango_aggregate(q.cuda(), k.cuda(), gp, vp, out, **kw)
+    else:
+        tg.wango_aggregate(q.cuda(), k.cuda(), gp, vp, out, window=W, **kw)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    o4 = out.view(B, T, H, pitch)
+    got = o4[..., :m_h].reshape(B, T, H * m_h)
+    ref, scale = ref_agg_scaled(kind, q, k, g, v, H, W)
+    check(got, ref, dtype, H=H, scale=scale)
+    if dtype == "f32":  # bf16 stores 16-byte vectors, which may run into the padding
+        assert bool((o4[..., m_h:] == 7.0).all())
