@@ -194,20 +194,21 @@ tg_status validate_decode(const tg_agg_params* p) {
 }
 
 struct DecodeWs {
-  size_t S, z, ring_k, ring_g, w, fq, fk, inv, total;
+  size_t S, z, ring_k, ring_g, w, fq, fk, wpart, older, total;
 };
 DecodeWs decode_ws_layout(const tg_agg_params* p) {
   const size_t B = p->B, H = p->H, W = p->window, d_h = p->d_qk / p->H;
   DecodeWs L;
   L.S = 0;
   L.z = L.S + align256(B * d_h * p->m * 4);
-  L.ring_k = L.z + align256(B * H * d_h * 4);
+  L.ring_k = L.z + align256(2 * B * H * d_h * 4);
   L.ring_g = L.ring_k + align256(B * H * W * d_h * elem_size(p->dtype));
   L.w = L.ring_g + align256(B * W * p->m * elem_size(p->dtype));
   L.fq = L.w + align256(B * H * W * 4);
   L.fk = L.fq + align256(B * H * d_h * 4);
-  L.inv = L.fk + align256(B * H * d_h * 4);
-  L.total = L.inv + align256(B * H * 4);
+  L.wpart = L.fk + align256(B * H * d_h * 4);
+  L.older = L.wpart + align256(B * H * 8 * 4);
+  L.total = L.older + align256(B * H * 4);
   return L;
 }
 
@@ -603,7 +604,8 @@ tg_status wango_decode_step(const tg_agg_params* p, long long pos, const void* q
   ds.w = reinterpret_cast<float*>(base + L.w);
   ds.fq = reinterpret_cast<float*>(base + L.fq);
   ds.fk_leave = reinterpret_cast<float*>(base + L.fk);
-  ds.inv_den = reinterpret_cast<float*>(base + L.inv);
+  ds.wpart = reinterpret_cast<float*>(base + L.wpart);
+  ds.older = reinterpret_cast<float*>(base + L.older);
   unsigned* err = nullptr;
   if (error_word(&err) != cudaSuccess) return TG_ERR_CUDA;
   return cuda_status(launch_wango_decode(p->dtype, p->B, p->H, p->d_qk, p->m, p->window, pos, p->s, p->tau,

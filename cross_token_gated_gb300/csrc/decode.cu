@@ -7,11 +7,17 @@
 // the ring of the last W tokens.  One call per token; the state is constant-size in T.
 //
 // Two kernels per step:
-//   wango_decode_scores_kernel  per (head, batch): unit q and k, the window weights, the
-//       feature maps, the denominator, z's update and the ring's khat slot.
-//   wango_decode_gate_kernel    per 128 gate columns and batch (HBM-bound): the window
-//       sum over the ring of g, the older-prefix read-out from S, u = gbar * v, the
-//       leaving token's rank-1 update of S and the ring's g slot.
+//   wango_decode_scores_kernel  per (head, batch, part of the ring): unit q and k, the
+//       window weights of its ring slots and their partial sum; the first part also the
+//       feature maps, the older-prefix term, z's update and the ring's khat slot.  At
+//       one or two sequences the ring is split over 8 CTAs per head, so that the chain
+//       of dependent steps in one CTA is short.
+//   wango_decode_gate_kernel    per 128 gate columns and batch (HBM-bound): the
+//       denominator from the partial sums, the window sum over the ring of g, the
+//       older-prefix read-out from S, u = gbar * v, the leaving token's rank-1 update of
+//       S and the ring's g slot.  At one or two sequences it is launched as a
+//       programmatic dependent of the score kernel: it asks its rows of the ring and of
+//       S into L2 while the score kernel runs, and waits for the scores only then.
 #include <math.h>
 
 #include "tg_common.cuh"
@@ -21,6 +27,20 @@ namespace tg {
 namespace {
 
 constexpr int kMaxDh = 128;
+constexpr int kMaxParts = 8;  // ring parts of the score kernel (the partial sums' stride)
+
+// Programmatic dependent launch: the score kernel lets the gate kernel of the same step
+// start early; the gate kernel waits for the score kernel's results (and memory) only
+// where it first needs them.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+__device__ __forceinline__ uint32_t smem_u32_of(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
 template <typename T>
 struct DecodeArgs {
@@ -54,15 +74,18 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// grid (H, B), 256 threads.
+// grid (H, B, parts), 256 threads; part p takes ring slots [p * ceil(W / parts), ...).
 template <typename T>
 __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeArgs<T> a) {
   __shared__ float qh[kMaxDh], kh[kMaxDh], red[8];
   __shared__ __align__(16) unsigned char kstage[32768];  // a chunk of the ring's keys
-  const int head = blockIdx.x, bb = blockIdx.y, t = threadIdx.x;
+  const int head = blockIdx.x, bb = blockIdx.y, part = blockIdx.z, t = threadIdx.x;
   const int d_h = a.d_h, W = a.W;
   const long long i = a.pos;
   const int bh = bb * a.H + head;
+  const int per = (W + gridDim.z - 1) / gridDim.z;
+  const int s_lo = min(W, part * per), s_hi = min(W, s_lo + per);
+  griddep_launch_dependents();  // the gate kernel may start fetching its rows now
   const float tau = head_tau(a.tau, a.s, head, a.err, kKernWango);
   const float sq = sqrtf(tau), shift = expf(-tau), inv_sqrt_dh = rsqrtf((float)d_h);
   // unit q and k of this head (sec. 2.1)
@@ -73,7 +96,10 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   const float kn = a.qk_normalized ? 1.f : fmaxf(sqrtf(block_sum(kv * kv, red)), 1e-12f);
   if (t < d_h) {
     qh[t] = qv / qn;
-    kh[t] = kv / kn;
+    // as the ring stores it (the storage type): the current slot's weight uses this value
+    T kr1;
+    io<T>::st(&kr1, kv / kn);
+    kh[t] = io<T>::ld(&kr1);
   }
   __syncthreads();
   // the current token's khat into its ring slot (slot i mod W held source i - W, which is
@@ -82,25 +108,27 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   const int cur = (int)(i % W);
   const long long jl = i - W + 1;  // the source that leaves the window after this step
   const int lslot = jl >= 0 ? (int)(jl % W) : -1;
-  // feature map of the leaving source, read before its slot could be overwritten
+  // part 0: feature map of the leaving source (its slot is not rewritten this step), and
+  // the current key into its slot.  No part reads slot cur from the ring: its weight
+  // comes from kh.
   float* fkl = a.st.fk_leave + (size_t)bh * d_h;
-  if (t < d_h && lslot >= 0) {
-    const float kl = lslot == cur ? kh[t] : io<T>::ld(ring_k + (size_t)lslot * d_h + t);
-    fkl[t] = phi_of(sq * kl, inv_sqrt_dh, a.phi_mode);
+  if (part == 0 && t < d_h) {
+    if (lslot >= 0) {
+      const float kl = lslot == cur ? kh[t] : io<T>::ld(ring_k + (size_t)lslot * d_h + t);
+      fkl[t] = phi_of(sq * kl, inv_sqrt_dh, a.phi_mode);
+    }
+    io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
   }
-  __syncthreads();
-  if (t < d_h) io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
-  __syncthreads();
   // window weights: the ring's keys pass through shared memory in chunks (one coalesced
   // copy each), then one ring slot per thread; slot s holds source j = the largest
   // j <= i with j = s (mod W).  The dot product starts at column s (mod d_h), so the
   // threads of a warp read different banks.
   float* wv = a.st.w + (size_t)bh * W;
   T* ks = reinterpret_cast<T*>(kstage);
-  const int per = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
+  const int chunk = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
   float wsum = 0.f;
-  for (int s0 = 0; s0 < W; s0 += per) {
-    const int n = min(per, W - s0);
+  for (int s0 = s_lo; s0 < s_hi; s0 += chunk) {
+    const int n = min(chunk, s_hi - s0);
     const T* src = ring_k + (size_t)s0 * d_h;
     const size_t bytes = (size_t)n * d_h * sizeof(T);
     __syncthreads();  // the previous chunk has been read
@@ -118,8 +146,12 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
       if (j >= 0) {
         const T* kr = ks + (size_t)sl * d_h;
         float dot = 0.f;
-        for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1)
-          dot = fmaf(qh[c], io<T>::ld(kr + c), dot);
+        if (s == cur) {
+          for (int c = 0; c < d_h; ++c) dot = fmaf(qh[c], kh[c], dot);
+        } else {
+          for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1)
+            dot = fmaf(qh[c], io<T>::ld(kr + c), dot);
+        }
         w = expf(tau * (dot - 1.f));
       }
       wv[s] = w;
@@ -127,19 +159,21 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
     }
   }
   wsum = block_sum(wsum, red);
-  // older prefix: e^-tau phi(q~) . z, then z += phi(k~_leave)
-  float* z = a.st.z + (size_t)bh * d_h;
+  if (t == 0) a.st.wpart[(size_t)bh * kMaxParts + part] = wsum;
+  if (part != 0) return;
+  // part 0: older prefix e^-tau phi(q~) . z, then z' = z + phi(k~_leave) into the other
+  // buffer (the sums alternate between two buffers by step parity)
+  const float* z = a.st.z + ((size_t)(i & 1) * a.B * a.H + bh) * d_h;
+  float* z_next = a.st.z + ((size_t)((i + 1) & 1) * a.B * a.H + bh) * d_h;
   float* fq = a.st.fq + (size_t)bh * d_h;
   const float fqv = t < d_h ? shift * phi_of(sq * qh[t], inv_sqrt_dh, a.phi_mode) : 0.f;
+  __syncthreads();  // fkl written above by this CTA
   const float older = block_sum(t < d_h ? fqv * z[t] : 0.f, red);
   if (t < d_h) {
     fq[t] = fqv;
-    if (lslot >= 0) z[t] += fkl[t];
+    z_next[t] = lslot >= 0 ? z[t] + fkl[t] : z[t];
   }
-  if (t == 0) {
-    const float null_w = a.null_bias ? expf(a.null_bias[head] - tau) : 0.f;
-    a.st.inv_den[bh] = 1.f / (wsum + older + (float)(i + 1) * null_w);
-  }
+  if (t == 0) a.st.older[bh] = older;
 }
 
 // Gate kernel layout: a CTA takes 128 gate columns of one sequence as 16 groups of 8
@@ -196,8 +230,9 @@ __device__ __forceinline__ void st_f32x8(float* p, int c0, int lim, const float*
 
 // grid (ceil(m / 128), B), 256 threads.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a) {
+__global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a, int parts) {
   __shared__ float red[kSlices][kGateCols + 4];
+  __shared__ float inv_den[TG_MAX_HEADS];
   const int bb = blockIdx.y, grp = threadIdx.x % kSlices, sl = threadIdx.x / kSlices;
   const int col0 = blockIdx.x * kGateCols, d_h = a.d_h, W = a.W, m = a.m;
   const int c0 = col0 + grp * kGroup;  // first of this thread's 8 columns
@@ -207,6 +242,25 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
   const int lslot = jl >= 0 ? (int)(jl % W) : -1;
   const T* gin = a.g + (size_t)bb * m;
   const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * W * m;
+  // while the score kernel runs: this thread's ring and state rows into L2 (the previous
+  // step's gate kernel, which wrote them, has completed before the score kernel began)
+  if (parts > 1 && c0 < m) {  // launched early (one or two sequences)
+    for (int s = sl; s < W; s += kSlices)
+      if (s != cur) prefetch_l2(ring_g + (size_t)s * m + c0);
+    const int hd = c0 / a.m_h;
+    for (int d = sl; d < d_h; d += kSlices)
+      prefetch_l2(a.st.S + (((size_t)bb * a.H + hd) * d_h + d) * a.m_h + (c0 - hd * a.m_h));
+  }
+  griddep_wait();  // the window weights, feature maps and partial sums of this step
+  if (threadIdx.x < a.H) {  // this sequence's denominators
+    const int hd = threadIdx.x, bh = bb * a.H + hd;
+    float wsum = 0.f;
+    for (int p = 0; p < parts; ++p) wsum += a.st.wpart[(size_t)bh * kMaxParts + p];
+    const float tau = head_tau(a.tau, a.s, hd, a.err, kKernWango);
+    const float null_w = a.null_bias ? expf(a.null_bias[hd] - tau) : 0.f;
+    inv_den[hd] = 1.f / (wsum + a.st.older[bh] + (float)(i + 1) * null_w);
+  }
+  __syncthreads();
   float acc[kGroup];
 #pragma unroll
   for (int e = 0; e < kGroup; ++e) acc[e] = 0.f;
@@ -215,10 +269,36 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
     // otherwise each column takes its own head below
     const int head0 = c0 / a.m_h;
     const int lim = m;
-    // window: ring slots sl, sl + 16, ...; the current token's slot from the input
+    // window: ring slots sl, sl + 16, ...; the current token's slot from the input.  With
+    // bf16 vectors and one or two sequences, eight slots' loads are issued before their
+    // products, so that one thread keeps eight loads in flight (a single sequence has
+    // few threads to hide HBM latency with)
     float x[kGroup];
+    int s_begin = sl;
+    if constexpr (VEC && sizeof(T) == 2) if (parts > 1) {
+      const float* wrow = a.st.w + (size_t)(bb * a.H + head0) * W;
+      for (; s_begin + 7 * kSlices < W; s_begin += 8 * kSlices) {
+        uint4 r[8];
+        float wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int s = s_begin + u * kSlices;
+          r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
+          wv[u] = wrow[s];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t gw[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = fmaf(wv[u], __uint_as_float(gw[e] << 16), acc[2 * e]);
+            acc[2 * e + 1] = fmaf(wv[u], __uint_as_float(gw[e] & 0xFFFF0000u), acc[2 * e + 1]);
+          }
+        }
+      }
+    }
 #pragma unroll 2
-    for (int s = sl; s < W; s += kSlices) {
+    for (int s = s_begin; s < W; s += kSlices) {
       Cols8<T, VEC>::ld(s == cur ? gin : ring_g + (size_t)s * m, c0, lim, x);
       if (VEC) {
         const float w = a.st.w[(size_t)(bb * a.H + head0) * W + s];
@@ -280,7 +360,7 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
 #pragma unroll
       for (int r = 0; r < kSlices; ++r) num += red[r][threadIdx.x];
       const int hd = c / a.m_h;
-      const float gbar = num * a.st.inv_den[bb * a.H + hd];
+      const float gbar = num * inv_den[hd];
       const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * m + c) : gbar;
       io<T>::st(a.out + (size_t)bb * m + c, u);
       io<T>::st(const_cast<T*>(ring_g) + (size_t)cur * m + c, io<T>::ld(gin + c));
@@ -292,15 +372,32 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 template <typename T>
 cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
-  wango_decode_scores_kernel<T><<<dim3(a.H, a.B), 256, 0, s>>>(a);
+  // one or two sequences: the ring split over 8 CTAs per head (a short dependent chain
+  // per CTA) and the gate kernel launched early
+  const bool few = a.B <= 2;
+  const int parts = few ? min(kMaxParts, (a.W + 31) / 32) : 1;
+  wango_decode_scores_kernel<T><<<dim3(a.H, a.B, parts), 256, 0, s>>>(a);
   // 8-column vectors when every row of g, the ring and S starts 16-byte aligned and no
   // 8-column group straddles a head
   const bool vec = (a.m * sizeof(T)) % 16 == 0 && a.m_h % kGroup == 0 && aligned16(a.g) &&
                    aligned16(a.st.ring_g) && aligned16(a.st.S);
   const dim3 grid((a.m + kGateCols - 1) / kGateCols, a.B);
-  if (vec) wango_decode_gate_kernel<T, true><<<grid, 256, 0, s>>>(a);
-  else wango_decode_gate_kernel<T, false><<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  if (!few) {  // enough CTAs to hide latency: a plain launch
+    if (vec) wango_decode_gate_kernel<T, true><<<grid, 256, 0, s>>>(a, parts);
+    else wango_decode_gate_kernel<T, false><<<grid, 256, 0, s>>>(a, parts);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true>, a, parts)
+             : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false>, a, parts);
 }
 
 }  // namespace

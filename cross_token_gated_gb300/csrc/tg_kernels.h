@@ -42,10 +42,11 @@ struct AggArgs {
 enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
 
 // WANGO decode state (one buffer, regions 256-byte aligned): the running sums S
-// [B, H, d_h, m_h] and z [B, H, d_h] in f32, the ring of the last W tokens' unit k
+// [B, H, d_h, m_h] and z [2, B, H, d_h] in f32 (z alternates between its two buffers by
+// step parity: a step reads buffer pos % 2 and writes the other), the ring of the last W tokens' unit k
 // [B, H, W, d_h] and g [B, W, m] (both in the storage type), and per-step scratch: the window
-// weights by ring slot [B, H, W], e^-tau phi(q~) and phi(k~_leave) [B, H, d_h], and
-// 1 / denominator [B, H].
+// weights by ring slot [B, H, W], e^-tau phi(q~) and phi(k~_leave) [B, H, d_h], the
+// window weights' partial sums [B, H, 8] and the older-prefix term [B, H].
 struct DecodeState {
   float* S;
   float* z;
@@ -54,7 +55,8 @@ struct DecodeState {
   float* w;
   float* fq;
   float* fk_leave;
-  float* inv_den;
+  float* wpart;
+  float* older;
 };
 cudaError_t launch_wango_decode(tg_dtype dt, int B, int H, int dqk, int m, int W, long long pos, float s,
                                 const float* tau, const float* null_bias, int phi_mode, int qk_normalized,
