@@ -482,7 +482,9 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
       device times;
     - WANGO decode steps (W=256) at B=1 and B=8, timed as one CUDA-graph replay of 64
       consecutive steps;
-    - the backward of both aggregations at B=8 T=2048, with per-kernel device times."""
+    - the backward of both aggregations at B=8 T=2048, with per-kernel device times,
+      and with the gbar and denominators a saving forward keeps (a training step's
+      aggregation: the saving forward plus that backward)."""
     import torch
     from cross_token_gated_gb300 import synth  # noqa: F401  (the recipe the weights follow)
     res = {}
@@ -529,27 +531,37 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     v = torch.randn(B, T, M, device=dev, generator=gen).bfloat16()
     dout = torch.randn(B, T, M, device=dev, generator=gen).bfloat16()
     dq, dk, dg, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(g), torch.empty_like(g)
+    u, gbar = torch.empty_like(g), torch.empty_like(g)
+    den = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    nf = tg.TG_FLAG_QK_NORMALIZED
     for kind in ("tango", "wango"):
         which = tg.TG_WS_TANGO_BWD if kind == "tango" else tg.TG_WS_WANGO_BWD
-        p = tg.agg_params(B, T, H, DQK, M, dtype=tg.TG_BF16, window=256, flags=tg.TG_FLAG_QK_NORMALIZED)
+        p = tg.agg_params(B, T, H, DQK, M, dtype=tg.TG_BF16, window=256, flags=nf)
         wsb = torch.empty(tg.tg_workspace_size(which, p) + 256, dtype=torch.uint8, device=dev)
-        if kind == "tango":
-            f = lambda: tg.tango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H,
-                                                    flags=tg.TG_FLAG_QK_NORMALIZED, ws=wsb, stream=stream)
-            fl = acc.tango_bwd_flops(B, T, DQK, M)
-        else:
-            f = lambda: tg.wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H, window=256,
-                                                    flags=tg.TG_FLAG_QK_NORMALIZED, ws=wsb, stream=stream)
-            fl = acc.wango_bwd_flops(B, T, DQK, M, H, 256)
+        kw = {} if kind == "tango" else {"window": 256}
+        bwd = tg.tango_aggregate_backward if kind == "tango" else tg.wango_aggregate_backward
+        save = tg.tango_aggregate_save if kind == "tango" else tg.wango_aggregate_save
+        f = lambda: bwd(q, k, g, v, dout, dq, dk, dg, dv, H=H, flags=nf, ws=wsb, stream=stream, **kw)
+        fl = acc.tango_bwd_flops(B, T, DQK, M) if kind == "tango" else acc.wango_bwd_flops(B, T, DQK, M, H, 256)
         ms = event_ms(f, dev, stream, reps=5)
         by = acc.agg_bwd_bytes(B, T, DQK, M)
+        # a training step's aggregation: the forward that keeps gbar and the denominators,
+        # then the backward that uses them (no recomputation)
+        ms_save = event_ms(lambda: save(q, k, g, v, u, gbar, den, H=H, flags=nf, stream=stream, **kw), dev, stream,
+                           reps=5)
+        f_saved = lambda: bwd(q, k, g, v, dout, dq, dk, dg, dv, H=H, flags=nf, ws=wsb, stream=stream, gbar=gbar,
+                              den=den, **kw)
+        ms_saved = event_ms(f_saved, dev, stream, reps=5)
         res[f"{kind}_backward_B{B}_T{T}"] = {
             "ms": ms, "tokens_per_s": B * T / (ms * 1e-3), "tflops": fl / (ms * 1e-3) / 1e12,
             "frac_bf16_peak": fl / (ms * 1e-3) / 1e12 / peak_tf, "gbs": by / (ms * 1e-3) / 1e9,
-            "algorithmic_tflop": fl / 1e12, "kernels": kernel_breakdown(f, dev)}
+            "algorithmic_tflop": fl / 1e12, "kernels": kernel_breakdown(f, dev),
+            "ms_with_saved_forward": ms_saved,
+            "frac_bf16_peak_with_saved_forward": fl / (ms_saved * 1e-3) / 1e12 / peak_tf,
+            "forward_save_ms": ms_save, "training_step_ms": ms_save + ms_saved}
         del wsb
         torch.cuda.empty_cache()
-    del q, k, g, v, dout, dq, dk, dg, dv
+    del q, k, g, v, dout, dq, dk, dg, dv, u, gbar, den
     torch.cuda.empty_cache()
 
     # ---- the WANGO block step (B=8, T=2048, W=256)

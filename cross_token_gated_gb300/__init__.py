@@ -6,8 +6,8 @@ kernels.  PyTorch supplies device memory and streams.  There is no fallback: if
 the library cannot be loaded, every call raises.
 
 Functions (same names as the C ABI):
-  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_aggregate_backward,
-  wango_aggregate_backward, wango_decode_step, tango_block_forward, tango_model_forward,
+  tango_aggregate, tango_aggregate_noalloc, wango_aggregate, tango_aggregate_save,
+  wango_aggregate_save, tango_aggregate_backward, wango_aggregate_backward, wango_decode_step, tango_block_forward, tango_model_forward,
   tg_workspace_size, tg_status_string, tg_check_device_error, tg_version
 """
 from __future__ import annotations
@@ -97,7 +97,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             f.restype = ctypes.c_int
         for name in ("tango_aggregate_backward", "wango_aggregate_backward"):
             f = getattr(lib, name)
-            f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            f.restype = ctypes.c_int
+        for name in ("tango_aggregate_save", "wango_aggregate_save"):
+            f = getattr(lib, name)
+            f.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             f.restype = ctypes.c_int
         lib.tango_aggregate_noalloc.argtypes = [P(tg_agg_params), vp, vp, vp, vp, vp, vp]
         lib.tango_aggregate_noalloc.restype = ctypes.c_int
@@ -200,16 +204,18 @@ def _ws_ptr(ws):
     return aligned, ws.numel() - (aligned - p)
 
 
-def _aggregate(fn_name, q, k, g, v, out, *, H, s, tau, null_bias, window, phi_mode, flags, ws, stream, m_h=None):
+def _aggregate(fn_name, q, k, g, v, out, *, H, s, tau, null_bias, window, phi_mode, flags, ws, stream, m_h=None,
+               saved=None):
     B, T, d_qk = q.shape
     m, pitch = _gate_width(g, H, m_h)
     p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias,
                    window=window, phi_mode=phi_mode, flags=flags, m_pitch=pitch)
-    which = TG_WS_TANGO if fn_name == "tango_aggregate" else TG_WS_WANGO
+    which = TG_WS_TANGO if fn_name.startswith("tango") else TG_WS_WANGO
     need = load().tg_workspace_size(which, ctypes.byref(p))
     wbuf = _workspace(need, g.device, ws)
     wp, wn = _ws_ptr(wbuf)
-    st = getattr(load(), fn_name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(out), wp, wn,
+    extra = () if saved is None else (_ptr(saved[0]), _ptr(saved[1]))
+    st = getattr(load(), fn_name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(out), *extra, wp, wn,
                                   _stream(stream))
     if st != TG_OK:
         raise TgError(st, fn_name)
@@ -233,8 +239,24 @@ def wango_aggregate(q, k, g, v, out, *, H, window, s=10.0, tau=None, null_bias=N
                       window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream, m_h=m_h)
 
 
+def tango_aggregate_save(q, k, g, v, out, gbar, den, *, H, s=10.0, tau=None, null_bias=None, flags=0, ws=None,
+                         stream=None, m_h=None):
+    """tango_aggregate that also writes gbar (laid out as out) and den (float32 [B, H, T])
+    for the backward (bf16)."""
+    return _aggregate("tango_aggregate_save", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias, window=1,
+                      phi_mode=0, flags=flags, ws=ws, stream=stream, m_h=m_h, saved=(gbar, den))
+
+
+def wango_aggregate_save(q, k, g, v, out, gbar, den, *, H, window, s=10.0, tau=None, null_bias=None, phi_mode=0,
+                         flags=0, ws=None, stream=None, m_h=None):
+    """wango_aggregate that also writes gbar and den for the backward (bf16)."""
+    return _aggregate("wango_aggregate_save", q, k, g, v, out, H=H, s=s, tau=tau, null_bias=null_bias,
+                      window=window, phi_mode=phi_mode, flags=flags, ws=ws, stream=stream, m_h=m_h,
+                      saved=(gbar, den))
+
+
 def _aggregate_backward(fn_name, q, k, g, v, dout, dq, dk, dg, dv, *, H, s, tau, null_bias, window, phi_mode,
-                        flags, ws, stream, m_h=None):
+                        flags, ws, stream, m_h=None, gbar=None, den=None):
     B, T, d_qk = q.shape
     m, pitch = _gate_width(g, H, m_h)
     p = agg_params(B, T, H, d_qk, m, dtype=_dtype_code(g), s=s, tau=tau, null_bias=null_bias,
@@ -243,29 +265,29 @@ def _aggregate_backward(fn_name, q, k, g, v, dout, dq, dk, dg, dv, *, H, s, tau,
     need = load().tg_workspace_size(which, ctypes.byref(p))
     wbuf = _workspace(need, g.device, ws)
     wp, wn = _ws_ptr(wbuf)
-    st = getattr(load(), fn_name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(dout), _ptr(dq),
-                                  _ptr(dk), _ptr(dg), _ptr(dv), wp, wn, _stream(stream))
+    st = getattr(load(), fn_name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g), _ptr(v), _ptr(dout), _ptr(gbar),
+                                  _ptr(den), _ptr(dq), _ptr(dk), _ptr(dg), _ptr(dv), wp, wn, _stream(stream))
     if st != TG_OK:
         raise TgError(st, fn_name)
     return dq, dk, dg, dv
 
 
 def tango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, s=10.0, tau=None, null_bias=None, flags=0,
-                             ws=None, stream=None, m_h=None):
+                             ws=None, stream=None, m_h=None, gbar=None, den=None):
     """Gradients of sum(dout * tango_aggregate(q, k, g, v)) with respect to q, k, g, v
     (bf16).  dq, dk [B, T, d_qk] and dg, dv [B, T, m] are written; v and dv may be None."""
     return _aggregate_backward("tango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
                                null_bias=null_bias, window=1, phi_mode=0, flags=flags, ws=ws, stream=stream,
-                               m_h=m_h)
+                               m_h=m_h, gbar=gbar, den=den)
 
 
 def wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, *, H, window, s=10.0, tau=None, null_bias=None,
-                             phi_mode=0, flags=0, ws=None, stream=None, m_h=None):
+                             phi_mode=0, flags=0, ws=None, stream=None, m_h=None, gbar=None, den=None):
     """Gradients of sum(dout * wango_aggregate(q, k, g, v)); arguments as for
     tango_aggregate_backward."""
     return _aggregate_backward("wango_aggregate_backward", q, k, g, v, dout, dq, dk, dg, dv, H=H, s=s, tau=tau,
                                null_bias=null_bias, window=window, phi_mode=phi_mode, flags=flags, ws=ws,
-                               stream=stream, m_h=m_h)
+                               stream=stream, m_h=m_h, gbar=gbar, den=den)
 
 
 def tango_aggregate_noalloc(q, k, g, v, out, *, H, s=10.0, tau=None, null_bias=None, flags=0,

@@ -221,12 +221,19 @@ tg_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 
 tg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TG_OK : TG_ERR_CUDA; }
 
-// Shared body of tango_aggregate / wango_aggregate.
+// Shared body of tango_aggregate / wango_aggregate (and, with gbar and den, of the
+// _save variants).
 tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
-                    const void* v, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                    const void* v, void* out, void* ws, size_t ws_bytes, cudaStream_t stream, void* gbar = nullptr,
+                    float* den = nullptr) {
   tg_status st = validate_agg(p, wango);
   if (st != TG_OK) return st;
   if (!q || !k || !g || !out) return TG_ERR_INVALID_ARG;
+  if (gbar || den) {
+    if (!gbar || !den) return TG_ERR_INVALID_ARG;
+    if (p->dtype != TG_BF16) return TG_ERR_UNSUPPORTED;
+    if (!aligned16(gbar) || !aligned16(den)) return TG_ERR_UNSUPPORTED;
+  }
   if (p->dtype == TG_BF16 && !(aligned16(q) && aligned16(k) && aligned16(g) && aligned16(out) &&
                                (!v || aligned16(v))))
     return TG_ERR_UNSUPPORTED;
@@ -257,7 +264,18 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
     a.k = kn;
   }
   if (p->dtype == TG_F32) return cuda_status(wango ? launch_wango_simt(a, stream) : launch_tango_simt(a, stream));
-  return cuda_status(wango ? launch_wango_tc(a, stream) : launch_tango_tc(a, stream));
+  a.gbar_out = gbar;
+  if (!wango) {
+    a.den_out = den;
+    a.den_pitch = p->T;
+    return cuda_status(launch_tango_tc(a, stream));
+  }
+  e = launch_wango_tc(a, stream);
+  if (e == cudaSuccess && den)  // the denominators as the weights kernel left them, at a pitch of T
+    e = cudaMemcpy2DAsync(den, (size_t)p->T * 4, wango_den_in_aux(a.aux, p->B, p->T, p->H, p->d_qk, p->m, p->window),
+                          (size_t)bwd_tpad(p->T) * 4, (size_t)p->T * 4, (size_t)p->B * p->H, cudaMemcpyDeviceToDevice,
+                          stream);
+  return cuda_status(e);
 }
 
 // ---- aggregation backward (bf16, tensor cores)
@@ -313,11 +331,13 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
 //     windowed kernel on the time-reversed sequence, whose older-pair weights
 //     e^-tau phi(k~_j) . phi(q~_i) are the same products).
 tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
-                             const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
-                             size_t ws_bytes, cudaStream_t stream) {
+                             const void* v, const void* dout, const void* saved_gbar, const float* saved_den,
+                             void* dq, void* dk, void* dg, void* dv, void* ws, size_t ws_bytes, cudaStream_t stream) {
   tg_status st = validate_bwd(p, wango);
   if (st != TG_OK) return st;
   if (!q || !k || !g || !dout || !dq || !dk || !dg || (dv && !v)) return TG_ERR_INVALID_ARG;
+  if (!saved_gbar != !saved_den) return TG_ERR_INVALID_ARG;
+  if (saved_gbar && !(aligned16(saved_gbar) && aligned16(saved_den))) return TG_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k, g, dout, dq, dk, dg};
   for (const void* x : ptrs)
     if (!aligned16(x)) return TG_ERR_UNSUPPORTED;
@@ -345,14 +365,22 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   void* E = base + L.E;
   void* aux = base + L.aux;
 
-  // the forward again: gbar and every row's denominator
+  // the forward again for gbar and every row's denominator, unless the caller kept them
+  // from the forward (the _save calls)
   AggArgs a;
   a.B = p->B; a.T = p->T; a.H = p->H; a.dqk = p->d_qk; a.m = mem_width(p); a.m_h = p->m / p->H;
   a.s = p->s; a.tau = p->tau; a.null_bias = p->null_bias;
   a.window = p->window; a.phi_mode = p->phi_mode; a.flags = 0; a.dtype = p->dtype;
   a.q = qh; a.k = kh; a.g = g; a.v = nullptr; a.out = gbar; a.err = err; a.aux = aux;
   const float* den = nullptr;
-  if (wango) {
+  int den_pitch = L.T_pad;
+  const void* gb = gbar;
+  if (saved_gbar) {
+    den = saved_den;
+    den_pitch = p->T;
+    gb = saved_gbar;
+    if (wango) e = launch_wango_prepass(a, stream);  // the feature maps for dq and dk
+  } else if (wango) {
     e = launch_wango_tc(a, stream);
     den = wango_den_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window);
   } else {
@@ -361,8 +389,8 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
     den = a.den_out;
   }
   if (e != cudaSuccess) return TG_ERR_CUDA;
-  e = launch_bwd_prep(dout, v, gbar, den, E, dv, dp, wango ? base + L.erev : nullptr, p->B, p->T, L.T_pad, p->H,
-                      mem_width(p), p->m / p->H, stream);
+  e = launch_bwd_prep(dout, v, gb, den, den_pitch, E, dv, dp, wango ? base + L.erev : nullptr, p->B, p->T, L.T_pad,
+                      p->H, mem_width(p), p->m / p->H, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
   // pair-weight gradients, then dq and dk
@@ -436,17 +464,29 @@ tg_status wango_aggregate(const tg_agg_params* p, const void* q, const void* k, 
   return aggregate(true, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tg_status tango_aggregate_save(const tg_agg_params* p, const void* q, const void* k, const void* g, const void* v,
+                               void* out, void* gbar, float* den, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  if (!gbar || !den) return TG_ERR_INVALID_ARG;
+  return aggregate(false, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), gbar, den);
+}
+
+tg_status wango_aggregate_save(const tg_agg_params* p, const void* q, const void* k, const void* g, const void* v,
+                               void* out, void* gbar, float* den, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  if (!gbar || !den) return TG_ERR_INVALID_ARG;
+  return aggregate(true, p, q, k, g, v, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), gbar, den);
+}
+
 tg_status tango_aggregate_backward(const tg_agg_params* p, const void* q, const void* k, const void* g,
-                                   const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
-                                   size_t ws_bytes, tg_stream_t stream) {
-  return aggregate_backward(false, p, q, k, g, v, dout, dq, dk, dg, dv, ws, ws_bytes,
+                                   const void* v, const void* dout, const void* gbar, const float* den, void* dq,
+                                   void* dk, void* dg, void* dv, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  return aggregate_backward(false, p, q, k, g, v, dout, gbar, den, dq, dk, dg, dv, ws, ws_bytes,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 tg_status wango_aggregate_backward(const tg_agg_params* p, const void* q, const void* k, const void* g,
-                                   const void* v, const void* dout, void* dq, void* dk, void* dg, void* dv, void* ws,
-                                   size_t ws_bytes, tg_stream_t stream) {
-  return aggregate_backward(true, p, q, k, g, v, dout, dq, dk, dg, dv, ws, ws_bytes,
+                                   const void* v, const void* dout, const void* gbar, const float* den, void* dq,
+                                   void* dk, void* dg, void* dv, void* ws, size_t ws_bytes, tg_stream_t stream) {
+  return aggregate_backward(true, p, q, k, g, v, dout, gbar, den, dq, dk, dg, dv, ws, ws_bytes,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -30,7 +30,7 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
 // One CTA per row (b, t) of `rows` per sequence (T, or T_pad with a reversed copy, whose
 // rows t >= T only clear their slot of it).  Rows are m wide in memory, H heads at a
 // pitch of m / H of which the first m_h columns are gates.  den and dp have a row pitch
-// of T_pad.
+// of T_pad (dp) and den_pitch (den).
 __device__ __forceinline__ void prep8(const uint4 du, const uint4 gb, const uint4 vv, float inv, uint4& eo, uint4& dvo,
                                       float& acc) {
   const uint32_t dus[4] = {du.x, du.y, du.z, du.w}, gbs[4] = {gb.x, gb.y, gb.z, gb.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
@@ -51,7 +51,7 @@ __device__ __forceinline__ void prep8(const uint4 du, const uint4 gb, const uint
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ gbar,
     const float* __restrict__ den, __nv_bfloat16* __restrict__ E, __nv_bfloat16* __restrict__ dv, float* __restrict__ dp,
-    __nv_bfloat16* __restrict__ e_rev, int T, int T_pad, int rows, int H, int m, int m_h) {
+    __nv_bfloat16* __restrict__ e_rev, int T, int T_pad, int rows, int H, int m, int m_h, int den_pitch) {
   __shared__ float red[kPrepThreads / 32];
   const int b = blockIdx.x / rows, t = blockIdx.x % rows;
   const int nvec = m / 8, m_hp = m / H;
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
   const size_t off = ((size_t)b * T + t) * m;
   const bool vec = m_h % 8 == 0;
   for (int a = 0; a < H; ++a) {
-    const float inv = 1.f / den[(size_t)(b * H + a) * T_pad + t];
+    const float inv = 1.f / den[(size_t)(b * H + a) * den_pitch + t];
     float acc = 0.f;
     const size_t h0 = off + (size_t)a * m_hp;
     if (vec) {
@@ -111,15 +111,16 @@ __global__ void reverse_rows_kernel(const __nv_bfloat16* __restrict__ src, __nv_
 
 }  // namespace
 
-cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
-                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h, cudaStream_t s) {
+cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, int den_pitch,
+                            void* E, void* dv, float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h,
+                            cudaStream_t s) {
   const int rows = e_rev ? T_pad : T;
   const long long n = (long long)B * rows;
   if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
   bwd_prep_kernel<<<(unsigned)n, kPrepThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(v),
       static_cast<const __nv_bfloat16*>(gbar), den, static_cast<__nv_bfloat16*>(E), static_cast<__nv_bfloat16*>(dv),
-      dp, static_cast<__nv_bfloat16*>(e_rev), T, T_pad, rows, H, m, m_h);
+      dp, static_cast<__nv_bfloat16*>(e_rev), T, T_pad, rows, H, m, m_h, den_pitch);
   return cudaGetLastError();
 }
 

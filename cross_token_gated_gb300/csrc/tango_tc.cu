@@ -88,7 +88,9 @@ struct Args {
   int rev;       // sources after the destination (j >= i) instead of before it
   int no_norm;   // the numerator alone: no division by the denominator
   int T_pad;
-  float* den_out;  // if set: every row's denominator, [B * H, T_pad]
+  float* den_out;  // if set: every row's denominator, [B * H, den_pitch]
+  int den_pitch;
+  __nv_bfloat16* gbar_out;  // if set: gbar (bf16), laid out as out
   __nv_bfloat16* out;
   unsigned* err;
   uint64_t timeout_ns;
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tau = head_tau(a.tau, a.s, t.head, a.err, kKernTango);
       if (a.null_bias) den += (float)(i + 1) * exp2f((a.null_bias[t.head] - tau) * kLog2e);
       const bool row_ok = i < a.T;
-      if (a.den_out && t.n0 == 0 && row_ok) a.den_out[(size_t)(t.b * a.H + t.head) * a.T_pad + i] = den;
+      if (a.den_out && t.n0 == 0 && row_ok) a.den_out[(size_t)(t.b * a.H + t.head) * a.den_pitch + i] = den;
       const float inv = a.no_norm ? 1.f : 1.f / den;
       const uint64_t inv2 = f32x2_pack(inv, inv), zero2 = f32x2_pack(0.f, 0.f);
       tc_fence_after();
@@ -530,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          y0, y1);
             gq[e] = pack_bf16x2(y0, y1);
           }
+          if (a.gbar_out && row_ok && col0 + 8 * k < a.m_h)
+            st_global_v4(a.gbar_out + grow + col0 + 8 * k, gq[0], gq[1], gq[2], gq[3]);
           uint4 uu;
           uu.x = a.has_v ? ptx::mul_bf16x2(gq[0], vv.x) : gq[0];
           uu.y = a.has_v ? ptx::mul_bf16x2(gq[1], vv.y) : gq[1];
@@ -592,6 +596,8 @@ cudaError_t launch_tango_tc(const AggArgs& p, cudaStream_t s) {
   a.no_norm = p.no_norm;
   a.T_pad = a.n_iblk * kBlk;
   a.den_out = p.den_out;
+  a.den_pitch = p.den_pitch ? p.den_pitch : a.T_pad;
+  a.gbar_out = static_cast<__nv_bfloat16*>(p.gbar_out);
   a.out = static_cast<__nv_bfloat16*>(p.out);
   a.err = p.err;
   a.debug_timeout = (p.flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;

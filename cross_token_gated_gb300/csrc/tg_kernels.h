@@ -32,7 +32,9 @@ struct AggArgs {
   // Backward helpers (tensor-core kernels):
   int rev = 0;              // TANGO: sources j >= i instead of j <= i
   int no_norm = 0;          // TANGO and WANGO: the numerator alone, no division by the denominator
-  float* den_out = nullptr; // TANGO: every row's denominator, [B * H, ceil(T / 128) * 128]
+  float* den_out = nullptr; // TANGO: every row's denominator, [B * H, den_pitch]
+  int den_pitch = 0;        // 0: ceil(T / 128) * 128
+  void* gbar_out = nullptr; // TANGO and WANGO (tensor cores): gbar in the storage type, laid out as out
   // WANGO with v fused: v = x W_v^T is formed inside the aggregation (then v == NULL)
   const void* fuse_x = nullptr;   // [B, T, fuse_d] bf16, the block's normalised input
   const void* fuse_wv = nullptr;  // [m, fuse_d] bf16
@@ -88,8 +90,9 @@ cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
 // (if dv), and D = sum_c E_c gbar_c over the head's columns into dp [B * H, T_pad];
 // e_rev (if set) receives E with the rows of every sequence reversed, row t at
 // T_pad - 1 - t, and zero rows before them.
-cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, void* E, void* dv,
-                            float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h, cudaStream_t s);
+cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, int den_pitch,
+                            void* E, void* dv, float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h,
+                            cudaStream_t s);
 // Rows of every sequence reversed: dst[b, T_pad - 1 - t] = src[b, t] for t < T and zero
 // rows dst[b, 0 .. T_pad - T) (to_padded), or back: dst[b, t] = src[b, T_pad - 1 - t].
 cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,

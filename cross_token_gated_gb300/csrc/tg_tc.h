@@ -77,6 +77,8 @@ const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int
 // [B, T, dqk], in the same scratch.
 const void* wango_fq_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
 const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
+// The WANGO feature-map pre-pass alone (fq, fk and the block sums of fk into a.aux).
+cudaError_t launch_wango_prepass(const AggArgs& a, cudaStream_t s);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);
 // Scratch bytes the tensor-core WANGO path needs in AggArgs::aux (256-byte aligned):
 // e^-tau phi(q~) and phi(k~) in bf16, per-block sums of phi(k~), the older-prefix

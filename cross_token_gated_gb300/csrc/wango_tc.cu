@@ -436,6 +436,7 @@ struct GArgs {
   int debug_timeout;
   int no_norm;                 // the numerator alone: no division by the denominator
   int fuse;                    // v = x W_v^T computed here (v == NULL, reuse == 0)
+  __nv_bfloat16* gbar_out;     // if set: gbar (bf16), laid out as out
   int nkc;                     // fused v: 64-column chunks of the residual width d
 };
 
@@ -937,6 +938,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&b.o_empty[ob]);
+        if (a.gbar_out && row_ok) {
+#pragma unroll
+          for (int k = 0; k < kNg / 8; ++k)
+            if (sp.n0 + 8 * k < a.m_h)
+              st_global_v4(a.gbar_out + grow + sp.n0 + 8 * k, gb[4 * k], gb[4 * k + 1], gb[4 * k + 2], gb[4 * k + 3]);
+        }
         if (fuse) {
           // v of this row in bf16 (as a separate projection would have stored it), u = gbar
           // * v, and the row written straight from registers (the staging tile is a G slot)
@@ -1211,6 +1218,18 @@ const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m
   return static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).fk;
 }
 
+cudaError_t launch_wango_prepass(const AggArgs& p, cudaStream_t s) {
+  const int m_h = p.m_h ? p.m_h : p.m / p.H;
+  const int n_iblk = ceil_div(p.T, kBlk);
+  const AuxLayout L = aux_layout(p.B, p.T, p.H, p.dqk, p.H * m_h, p.window);
+  char* aux = static_cast<char*>(p.aux);
+  wango_phi_kernel<<<dim3(n_iblk, p.H, p.B), kBlk, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
+      reinterpret_cast<__nv_bfloat16*>(aux + L.fq), reinterpret_cast<__nv_bfloat16*>(aux + L.fk),
+      reinterpret_cast<float*>(aux + L.zb), p.T, p.H, p.dqk, n_iblk, p.s, p.tau, p.phi_mode, p.err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   const int d_h = p.dqk / p.H, m_hp = p.m / p.H, m_h = p.m_h ? p.m_h : m_hp;
   const int n_iblk = ceil_div(p.T, kBlk);
@@ -1281,6 +1300,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.debug_timeout = debug ? 1 : 0;
   a.timeout_ns = timeout_ns;
   a.no_norm = p.no_norm;
+  a.gbar_out = static_cast<__nv_bfloat16*>(p.gbar_out);
   if (a.nseg > 1) {  // no segment's state is ready yet
     e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;

@@ -13,7 +13,9 @@
  *                          one weight set, or with the revision's gated-projection sets
  *   - tango_aggregate_backward, wango_aggregate_backward
  *                          gradients of the two aggregations (eq. 5 differentiated with
- *                          respect to q, k, g and v), for training (sec. 3)
+ *                          respect to q, k, g and v), for training (sec. 3); the
+ *                          tango_aggregate_save / wango_aggregate_save forwards keep what
+ *                          they need
  *
  * Conventions shared by every call:
  *   - Every pointer argument named as "device" is a CUDA device pointer owned by the
@@ -155,6 +157,24 @@ tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, 
                           tg_stream_t stream);
 
 /*
+ * tango_aggregate / wango_aggregate that also keep what their backward needs, as a
+ * training forward does (bf16 only; TG_F32 returns TG_ERR_UNSUPPORTED):
+ *   gbar  device, laid out as out: gbar = out / v (the aggregated gate before the
+ *         product with v), in the storage type; written
+ *   den   device float [B, H, T]: every row's denominator as the kernels form it
+ *         (sum of the weights e^{tau (qhat.khat - 1)} as applied, plus the null term,
+ *         all shifted by e^-tau); written.  An opaque statistic for the backward.
+ * Passing both to the backward skips its recomputation of the forward.  Other arguments
+ * as for tango_aggregate / wango_aggregate.
+ */
+tg_status tango_aggregate_save(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                               const void *v, void *out, void *gbar, float *den, void *ws,
+                               size_t ws_bytes, tg_stream_t stream);
+tg_status wango_aggregate_save(const tg_agg_params *p, const void *q, const void *k, const void *g,
+                               const void *v, void *out, void *gbar, float *den, void *ws,
+                               size_t ws_bytes, tg_stream_t stream);
+
+/*
  * Backward of tango_aggregate (sec. 2.1 eq. 5 with the weights of sec. 2.2 eq. 6):
  * given dout = dL/d(out) for the output out = gbar * v (out = gbar when v == NULL),
  * writes the gradients of L with respect to the call's inputs:
@@ -169,6 +189,8 @@ tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, 
  *   p, q, k, g, v   as for the forward call (bf16 only: TG_F32 returns TG_ERR_UNSUPPORTED;
  *                   flags may hold TG_FLAG_QK_NORMALIZED only)
  *   dout            device [B, T, m], read only
+ *   gbar, den       the forward's gbar and den from tango_aggregate_save with the same
+ *                   arguments, or both NULL: the backward then recomputes them
  *   dq, dk          device [B, T, d_qk], written
  *   dg              device [B, T, m], written
  *   dv              device [B, T, m], written, or NULL (must be NULL when v is NULL)
@@ -182,21 +204,24 @@ tg_status wango_aggregate(const tg_agg_params *p, const void *q, const void *k, 
  * cores elsewhere.
  */
 tg_status tango_aggregate_backward(const tg_agg_params *p, const void *q, const void *k, const void *g,
-                                   const void *v, const void *dout, void *dq, void *dk, void *dg,
-                                   void *dv, void *ws, size_t ws_bytes, tg_stream_t stream);
+                                   const void *v, const void *dout, const void *gbar, const float *den,
+                                   void *dq, void *dk, void *dg, void *dv, void *ws, size_t ws_bytes,
+                                   tg_stream_t stream);
 
 /*
  * Backward of wango_aggregate (sec. 2.2 eqs. 7-10 in sec. 2.1 eq. 5).  Arguments,
  * outputs and requirements as for tango_aggregate_backward; the workspace is sized by
- * tg_workspace_size(TG_WS_WANGO_BWD, p).  Window pairs contribute as in TANGO; an older
+ * tg_workspace_size(TG_WS_WANGO_BWD, p); gbar and den come from wango_aggregate_save.
+ * Window pairs contribute as in TANGO; an older
  * pair's weight phi(sqrt(tau) qhat_i) . phi(sqrt(tau) khat_j) passes its gradient
  * through phi' (ELU's derivative, over sqrt(d_h) for eq. 8) and sqrt(tau).  dg is the
  * forward numerator of the time-reversed sequence (linear in T); the weight gradients
  * of the older pairs are formed pair by pair, so that part costs T^2 m like TANGO's.
  */
 tg_status wango_aggregate_backward(const tg_agg_params *p, const void *q, const void *k, const void *g,
-                                   const void *v, const void *dout, void *dq, void *dk, void *dg,
-                                   void *dv, void *ws, size_t ws_bytes, tg_stream_t stream);
+                                   const void *v, const void *dout, const void *gbar, const float *den,
+                                   void *dq, void *dk, void *dg, void *dv, void *ws, size_t ws_bytes,
+                                   tg_stream_t stream);
 
 /*
  * One autoregressive step of the windowed aggregation (sec. 2.2 eqs. 7-10) for B

@@ -228,18 +228,26 @@ def test_backward_validation_and_workspace(lib):
         assert need >= 2 * 2 * 384 * 384 * 2 + 2 * 300 * 512 * 2 * 2
     assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, p) > tg.tg_workspace_size(tg.TG_WS_TANGO_BWD, p)
     assert tg.tg_workspace_size(tg.TG_WS_TANGO_BWD, _agg(dtype=tg.TG_F32)) == 0
-    a = [256] * 9
+    a = [256] * 5 + [None, None] + [256] * 4   # q k g v dout, no saved gbar/den, dq dk dg dv
     for fn in (raw.tango_aggregate_backward, raw.wango_aggregate_backward):
         assert fn(ctypes.byref(_agg(dtype=tg.TG_F32)), *a, None, 0, None) == tg.TG_ERR_UNSUPPORTED
         assert fn(ctypes.byref(_agg(flags=tg.TG_FLAG_DEBUG_TIMEOUT)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
         assert fn(ctypes.byref(_agg(B=0)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
         # dv without v
-        assert fn(ctypes.byref(p), 256, 256, 256, None, 256, 256, 256, 256, 256, None, 0, None) == \
+        assert fn(ctypes.byref(p), 256, 256, 256, None, 256, None, None, 256, 256, 256, 256, None, 0, None) == \
             tg.TG_ERR_INVALID_ARG
         # misaligned dout
-        assert fn(ctypes.byref(p), 256, 256, 256, 256, 264, 256, 256, 256, 256, None, 0, None) == \
+        assert fn(ctypes.byref(p), 256, 256, 256, 256, 264, None, None, 256, 256, 256, 256, None, 0, None) == \
             tg.TG_ERR_UNSUPPORTED
+        # a saved gbar without its denominators
+        assert fn(ctypes.byref(p), 256, 256, 256, 256, 256, 256, None, 256, 256, 256, 256, None, 0, None) == \
+            tg.TG_ERR_INVALID_ARG
         assert fn(ctypes.byref(p), *a, None, 0, None) == tg.TG_ERR_WORKSPACE
+    for fn in (raw.tango_aggregate_save, raw.wango_aggregate_save):
+        assert fn(ctypes.byref(p), 256, 256, 256, 256, 256, None, 256, None, 0, None) == tg.TG_ERR_INVALID_ARG
+        assert fn(ctypes.byref(_agg(dtype=tg.TG_F32)), 256, 256, 256, 256, 256, 256, 256, None, 0, None) == \
+            tg.TG_ERR_UNSUPPORTED
+        assert fn(ctypes.byref(p), 256, 256, 256, 256, 256, 256, 256, None, 0, None) == tg.TG_ERR_WORKSPACE
 
 
 def test_gate_pitch_validation(lib):

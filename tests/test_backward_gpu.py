@@ -248,3 +248,32 @@ def test_backward_gate_pitch(kind):
         e = errs(t, ref[name], H, scale)
         assert e["norm"] <= TOL, (name, e)
         assert e.get("row_head", 0.0) <= 2 * TOL and e.get("row_head_cond", 0.0) <= TOL, (name, e)
+
+
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_saved_forward_feeds_the_backward(kind):
+    """tango/wango_aggregate_save write u as the plain call does, plus gbar and the row
+    denominators; the backward given them (no recomputation of the forward) returns
+    exactly the gradients it computes without them.  gbar equals the forward with v = NULL."""
+    B, T, H, dqk, m, W = 2, 300, 2, 128, 1040, 100
+    q, k, g, v = (t.cuda() for t in synth.agg_inputs(B, T, dqk, m, seed=61, dtype="bf16"))
+    dout = synth.upstream_grad(B, T, m, seed=62).cuda()
+    u, u_ref, gbar, gbar_ref = (torch.empty_like(g) for _ in range(4))
+    den = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
+    kw = {} if kind == "tango" else {"window": W}
+    fwd = tg.tango_aggregate if kind == "tango" else tg.wango_aggregate
+    save = tg.tango_aggregate_save if kind == "tango" else tg.wango_aggregate_save
+    bwd = tg.tango_aggregate_backward if kind == "tango" else tg.wango_aggregate_backward
+    save(q, k, g, v, u, gbar, den, H=H, **kw)
+    fwd(q, k, g, v, u_ref, H=H, **kw)
+    fwd(q, k, g, None, gbar_ref, H=H, **kw)
+    assert torch.equal(u, u_ref)
+    assert torch.equal(gbar, gbar_ref)
+    assert bool(torch.isfinite(den).all()) and bool((den > 0).all())
+    grads = [[torch.empty_like(x) for x in (q, k, g, g)] for _ in range(2)]
+    bwd(q, k, g, v, dout, *grads[0], H=H, **kw)
+    bwd(q, k, g, v, dout, *grads[1], H=H, gbar=gbar, den=den, **kw)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    for a, b in zip(*grads):
+        assert torch.equal(a, b)
