@@ -64,11 +64,14 @@ def _load():
             bwd = [vp, i, vp, i, vp, i, vp, i, vp, i, vp, vp, i, vp, vp, vp, vp]
             lib.oracle_tango_backward.argtypes = agg + bwd
             lib.oracle_wango_backward.argtypes = agg + [i, i] + bwd
+            lib.oracle_agg_backward_rows.argtypes = ([i] * 8 + [vp, i, vp, i, vp, i, vp, i, vp, i, vp, vp, i]
+                                                     + [vp, i, vp, i, vp, vp, vp, vp])
             lib.oracle_embed.argtypes = [ll, vp, i, i, vp, i, vp]
             lib.oracle_final_logits.argtypes = [ll, i, i, vp, vp, i, d, vp, i, vp]
             for name in ("oracle_tango", "oracle_wango_direct", "oracle_wango_scan",
                          "oracle_block_forward", "oracle_embed", "oracle_final_logits",
-                         "oracle_tango_backward", "oracle_wango_backward", "oracle_num_threads"):
+                         "oracle_tango_backward", "oracle_wango_backward", "oracle_agg_backward_rows",
+                         "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -183,6 +186,30 @@ def wango_backward(q, k, g, v, dout, *, H, tau, window, phi_mode=0, null_bias=No
     """Gradients of L = sum(dout * u) for the WANGO aggregation (eqs. 5-9), pair by pair."""
     return _backward("oracle_wango_backward", (int(window), int(phi_mode)), q, k, g, v, dout, H, tau,
                      null_bias, qk_normalized)
+
+
+def backward_rows(kind, q, k, g, v, dout, *, H, tau, rows_q, rows_k, window=1, phi_mode=0, null_bias=None,
+                  qk_normalized=False):
+    """The gradients of tango_backward / wango_backward (kind "tango" or "wango") at
+    selected rows only: dq, dv [len(rows_q), .] for destination rows and dk, dg
+    [len(rows_k), .] for source rows (row = b * T + t).  dk of a source needs every later
+    destination's gbar, so early sources cost about as much as the full backward."""
+    B, T, dqk = q.shape
+    m = g.shape[-1]
+    qp, qd, qa = _arr(q); kp, kd, ka = _arr(k); gp, gd, ga = _arr(g); vp_, vd, va = _arr(v)
+    op, od, oa = _arr(dout)
+    tp, ta = _f64(_tau_vec(tau, H), H)
+    bp, ba = _f64(null_bias, H)
+    rq = np.ascontiguousarray(np.asarray(rows_q, dtype=np.int64))
+    rk = np.ascontiguousarray(np.asarray(rows_k, dtype=np.int64))
+    dq = np.empty((len(rq), dqk)); dv = np.zeros((len(rq), m))
+    dk = np.empty((len(rk), dqk)); dg = np.empty((len(rk), m))
+    rc = _load().oracle_agg_backward_rows(0 if kind == "tango" else 1, B, T, H, dqk, m, int(window), int(phi_mode),
+                                          qp, qd, kp, kd, gp, gd, vp_, vd, op, od, tp, bp, int(bool(qk_normalized)),
+                                          rq.ctypes.data, len(rq), rk.ctypes.data, len(rk), dq.ctypes.data,
+                                          dv.ctypes.data, dk.ctypes.data, dg.ctypes.data)
+    _check(rc, "oracle_agg_backward_rows")
+    return {"dq": dq, "dk": dk, "dg": dg, "dv": dv if v is not None else None}
 
 
 def wango_scan(q, k, g, v, *, H, tau, window, phi_mode=0, null_bias=None, qk_normalized=False):

@@ -673,6 +673,190 @@ int oracle_wango_backward(int B, int T, int H, int dqk, int m, int W, int phi_mo
                         tau, null_b, qk_normalized, dq, dk, dg, dv);
 }
 
+/*
+ * The gradients of agg_backward for selected rows only, so that long sequences can be
+ * checked without the full O(T^2 m) evaluation: dq and dv of the destination rows
+ * rows_q[0..nq) and dk and dg of the source rows rows_k[0..nk) (a row is b*T + t).
+ * The per-pair terms are those of agg_backward.  Per (batch, head) with a selected row it
+ * takes every row's denominator (O(T^2 d_h)), gbar_i and delta_i = gbar_i . dgbar_i for
+ * the destinations that the selected rows need (each selected destination; every
+ * destination at or after a selected source, for dk), and dgbar_i = dout_i * v_i.
+ * dk of an early source therefore costs about as much as the full backward.
+ * Outputs (fp64): dq [nq, dqk], dv [nq, m] (untouched when v == NULL), dk [nk, dqk],
+ * dg [nk, m].
+ */
+int oracle_agg_backward_rows(int mode, int B, int T, int H, int dqk, int m, int W, int phi_mode,
+                             const void *q, int qdt, const void *k, int kdt,
+                             const void *g, int gdt, const void *v, int vdt, const void *dout, int odt,
+                             const double *tau, const double *null_b, int qk_normalized,
+                             const long long *rows_q, int nq, const long long *rows_k, int nk,
+                             double *dq, double *dv, double *dk, double *dg) {
+    if (!check_dims(B, T, H, dqk, m) || (mode == 1 && W < 1) || nq < 0 || nk < 0) return OR_EINVAL;
+    if (dqk / H > 128) return OR_EINVAL;
+    for (int r = 0; r < nq; ++r) if (rows_q[r] < 0 || rows_q[r] >= (long long)B * T) return OR_EINVAL;
+    for (int r = 0; r < nk; ++r) if (rows_k[r] < 0 || rows_k[r] >= (long long)B * T) return OR_EINVAL;
+    int d_h = dqk / H, m_h = m / H;
+    long long BT = (long long)B * T;
+    double *qn = prep_unit(q, qdt, BT, H, dqk, qk_normalized);
+    double *kn = prep_unit(k, kdt, BT, H, dqk, qk_normalized);
+    double *fq = NULL, *fk = NULL;
+    if (mode == 1 && qn && kn) {
+        fq = prep_phi(qn, BT, H, dqk, tau, phi_mode);
+        fk = prep_phi(kn, BT, H, dqk, tau, phi_mode);
+    }
+    if (!qn || !kn || (mode == 1 && (!fq || !fk))) {
+        free(qn); free(kn); free(fq); free(fk);
+        return OR_ENOMEM;
+    }
+    memset(dq, 0, sizeof(double) * (size_t)nq * dqk);
+    memset(dk, 0, sizeof(double) * (size_t)nk * dqk);
+    memset(dg, 0, sizeof(double) * (size_t)nk * m);
+    int fail = 0;
+    for (long long u = 0; u < (long long)B * H && !fail; ++u) {
+        int b = (int)(u / H), a = (int)(u % H);
+        size_t row0 = (size_t)b * T;
+        /* which destinations need gbar and delta */
+        int any = 0, jmin_k = T;
+        for (int r = 0; r < nq; ++r) if (rows_q[r] / T == b) any = 1;
+        for (int r = 0; r < nk; ++r)
+            if (rows_k[r] / T == b) { any = 1; if ((int)(rows_k[r] % T) < jmin_k) jmin_k = (int)(rows_k[r] % T); }
+        if (!any) continue;
+        char *need = (char *)calloc((size_t)T, 1);
+        double *den = (double *)malloc(sizeof(double) * (size_t)T);
+        double *delta = (double *)calloc((size_t)T, sizeof(double));
+        double **gbar = (double **)calloc((size_t)T, sizeof(double *));
+        if (!need || !den || !delta || !gbar) { fail = 1; free(need); free(den); free(delta); free(gbar); break; }
+        for (int r = 0; r < nq; ++r) if (rows_q[r] / T == b) need[rows_q[r] % T] = 1;
+        for (int i = jmin_k; i < T; ++i) need[i] = 1;
+        const double st = sqrt(tau[a]);
+#define PW(i, j) ((mode == 0 || (j) >= (i) - W + 1)                                             \
+        ? exp(tau[a] * dot(qn + (row0 + (i)) * dqk + (size_t)a * d_h,                            \
+                           kn + (row0 + (j)) * dqk + (size_t)a * d_h, d_h))                      \
+        : dot(fq + (row0 + (i)) * dqk + (size_t)a * d_h, fk + (row0 + (j)) * dqk + (size_t)a * d_h, d_h))
+        /* every row's denominator */
+#pragma omp parallel for schedule(dynamic, 16)
+        for (int i = 0; i < T; ++i) {
+            double s = 0.0;
+            for (int j = 0; j <= i; ++j) s += PW(i, j);
+            if (null_b) s += (double)(i + 1) * exp(null_b[a]);
+            den[i] = s;
+        }
+        /* gbar_i and delta_i where needed */
+        int nofail = 1;
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int i = 0; i < T; ++i) {
+            if (!need[i]) continue;
+            double *gb = (double *)calloc((size_t)m_h, sizeof(double));
+            if (!gb) { nofail = 0; continue; }
+            for (int j = 0; j <= i; ++j)
+                axpy_from(gb, PW(i, j) / den[i], g, gdt, (row0 + j) * (size_t)m + (size_t)a * m_h, m_h);
+            size_t off = (row0 + i) * (size_t)m + (size_t)a * m_h;
+            double dl = 0.0;
+            for (int n = 0; n < m_h; ++n) {
+                double o = ld(dout, odt, off + n);
+                dl += gb[n] * (v ? o * ld(v, vdt, off + n) : o);
+            }
+            delta[i] = dl;
+            gbar[i] = gb;
+        }
+        if (!nofail) fail = 1;
+        /* destinations: dq (through the normalisation) and dv */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int r = 0; r < nq; ++r) {
+            if (rows_q[r] / T != b || fail) continue;
+            int i = (int)(rows_q[r] % T);
+            size_t offi = (row0 + i) * (size_t)m + (size_t)a * m_h;
+            double *dgi = (double *)malloc(sizeof(double) * (size_t)m_h);
+            double *gj = (double *)malloc(sizeof(double) * (size_t)m_h);
+            double dh[128];
+            if (!dgi || !gj) { free(dgi); free(gj); continue; }
+            for (int n = 0; n < m_h; ++n) {
+                double o = ld(dout, odt, offi + n);
+                dgi[n] = v ? o * ld(v, vdt, offi + n) : o;
+                if (v && dv) dv[(size_t)r * m + (size_t)a * m_h + n] = o * gbar[i][n];
+            }
+            for (int c = 0; c < d_h; ++c) dh[c] = 0.0;
+            const double *qi = qn + (row0 + i) * dqk + (size_t)a * d_h;
+            for (int j = 0; j <= i; ++j) {
+                widen_row(gj, g, gdt, (row0 + j) * (size_t)m + (size_t)a * m_h, m_h);
+                double w = PW(i, j);
+                double dw = (dot(gj, dgi, m_h) - delta[i]) / den[i];
+                const double *kj = kn + (row0 + j) * dqk + (size_t)a * d_h;
+                if (mode == 0 || j >= i - W + 1) {
+                    for (int c = 0; c < d_h; ++c) dh[c] += tau[a] * w * dw * kj[c];
+                } else {
+                    const double *fkj = fk + (row0 + j) * dqk + (size_t)a * d_h;
+                    for (int c = 0; c < d_h; ++c) dh[c] += st * dw * phi_deriv(st * qi[c], d_h, phi_mode) * fkj[c];
+                }
+            }
+            double *dst = dq + (size_t)r * dqk + (size_t)a * d_h;
+            if (qk_normalized) {
+                for (int c = 0; c < d_h; ++c) dst[c] = dh[c];
+            } else {
+                double nrm = 0.0;
+                for (int c = 0; c < d_h; ++c) {
+                    double x = ld(q, qdt, (row0 + i) * dqk + (size_t)a * d_h + c);
+                    nrm += x * x;
+                }
+                nrm = sqrt(nrm);
+                double pr = dot(qi, dh, d_h);
+                for (int c = 0; c < d_h; ++c) dst[c] = nrm < 1e-12 ? dh[c] / 1e-12 : (dh[c] - qi[c] * pr) / nrm;
+            }
+            free(dgi); free(gj);
+        }
+        /* sources: dg and dk (through the normalisation) */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int r = 0; r < nk; ++r) {
+            if (rows_k[r] / T != b || fail) continue;
+            int j = (int)(rows_k[r] % T);
+            double *gj = (double *)malloc(sizeof(double) * (size_t)m_h);
+            double *dgi = (double *)malloc(sizeof(double) * (size_t)m_h);
+            double dh[128];
+            if (!gj || !dgi) { free(gj); free(dgi); continue; }
+            widen_row(gj, g, gdt, (row0 + j) * (size_t)m + (size_t)a * m_h, m_h);
+            double *dgj = dg + (size_t)r * m + (size_t)a * m_h;
+            for (int c = 0; c < d_h; ++c) dh[c] = 0.0;
+            const double *kj = kn + (row0 + j) * dqk + (size_t)a * d_h;
+            for (int i = j; i < T; ++i) {
+                size_t offi = (row0 + i) * (size_t)m + (size_t)a * m_h;
+                for (int n = 0; n < m_h; ++n) {
+                    double o = ld(dout, odt, offi + n);
+                    dgi[n] = v ? o * ld(v, vdt, offi + n) : o;
+                }
+                double w = PW(i, j);
+                for (int n = 0; n < m_h; ++n) dgj[n] += w / den[i] * dgi[n];
+                double dw = (dot(gj, dgi, m_h) - delta[i]) / den[i];
+                const double *qi = qn + (row0 + i) * dqk + (size_t)a * d_h;
+                if (mode == 0 || j >= i - W + 1) {
+                    for (int c = 0; c < d_h; ++c) dh[c] += tau[a] * w * dw * qi[c];
+                } else {
+                    const double *fqi = fq + (row0 + i) * dqk + (size_t)a * d_h;
+                    for (int c = 0; c < d_h; ++c) dh[c] += st * dw * fqi[c] * phi_deriv(st * kj[c], d_h, phi_mode);
+                }
+            }
+            double *dst = dk + (size_t)r * dqk + (size_t)a * d_h;
+            if (qk_normalized) {
+                for (int c = 0; c < d_h; ++c) dst[c] = dh[c];
+            } else {
+                double nrm = 0.0;
+                for (int c = 0; c < d_h; ++c) {
+                    double x = ld(k, kdt, (row0 + j) * dqk + (size_t)a * d_h + c);
+                    nrm += x * x;
+                }
+                nrm = sqrt(nrm);
+                double pr = dot(kj, dh, d_h);
+                for (int c = 0; c < d_h; ++c) dst[c] = nrm < 1e-12 ? dh[c] / 1e-12 : (dh[c] - kj[c] * pr) / nrm;
+            }
+            free(gj); free(dgi);
+        }
+#undef PW
+        for (int i = 0; i < T; ++i) free(gbar[i]);
+        free(need); free(den); free(delta); free(gbar);
+    }
+    free(qn); free(kn); free(fq); free(fk);
+    return fail ? OR_ENOMEM : OR_OK;
+}
+
 /* Number of OpenMP threads the oracle runs on. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -277,3 +277,38 @@ def test_saved_forward_feeds_the_backward(kind):
     assert st == tg.TG_OK, (st, hex(word))
     for a, b in zip(*grads):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kind", ["tango", "wango"])
+def test_backward_full_size_sampled_rows(kind):
+    """B = 8, T = 2,048, m = 28,480 (the benchmark shape, W = 256 for WANGO): dq and dv at
+    sampled destinations (first, window and block edges, last, random) and dk, dg at the
+    last sources of two sequences, against the oracle's gradients at those rows alone.
+    Bounds: normwise over the sample, and per (row, head) for dg and dv."""
+    B, T, H, dqk, m, W = 8, 2048, 2, 128, 28480, 256
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=71, dtype="bf16")
+    dout = synth.upstream_grad(B, T, m, seed=72)
+    dev = [t.cuda() for t in (q, k, g, v, dout)]
+    dq, dk, dg, dv = (torch.empty_like(x) for x in (dev[0], dev[1], dev[2], dev[2]))
+    if kind == "tango":
+        tg.tango_aggregate_backward(*dev, dq, dk, dg, dv, H=H)
+    else:
+        tg.wango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, window=W)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_OK, (st, hex(word))
+    rng = np.random.default_rng(73)
+    rows_q = []
+    for b in (0, 5, 7):
+        ts = [0, 1, 2, 127, 128, 255, 256, 257, 1024, 2045, 2046, 2047] + list(rng.integers(0, T, 6))
+        rows_q += [b * T + int(t) for t in ts]
+    rows_k = [b * T + t for b in (2, 7) for t in (T - 1, T - 2, T - 5, T - 9, T - 14)]
+    view = [synth.oracle_view(t) for t in (q, k, g, v, dout)]
+    kw = {} if kind == "tango" else {"window": W}
+    ref = oracle.backward_rows(kind, *view, H=H, tau=10.0, rows_q=rows_q, rows_k=rows_k, **kw)
+    got = {"dq": dq.view(B * T, -1)[rows_q], "dv": dv.view(B * T, -1)[rows_q],
+           "dk": dk.view(B * T, -1)[rows_k], "dg": dg.view(B * T, -1)[rows_k]}
+    for name, t in got.items():
+        e = errs(t, ref[name], H)
+        assert e["norm"] <= TOL, (name, e)
+        if name in ("dg", "dv"):
+            assert e["row_head"] <= 2 * TOL, (name, e)

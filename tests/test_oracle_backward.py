@@ -146,3 +146,30 @@ def test_causality_of_gradients():
         d = backward(kind, q, k, g, v, dout, dict(kw, H=H, tau=10.0))
         for n in ("dq", "dk", "dg", "dv"):
             assert np.all(d[n][:, t:] == 0.0), (kind, n)
+
+
+@pytest.mark.parametrize("kind,kw", [("tango", {}), ("wango", dict(window=5, phi_mode=0)),
+                                     ("wango", dict(window=9, phi_mode=1, null_bias=np.array([-1.0, 0.5])))])
+def test_rows_variant_equals_the_full_backward(kind, kw):
+    """The sampled-row gradients (for long sequences on the GPU side) are the full
+    backward's rows, including early sources, the first and last rows, and with unit
+    inputs."""
+    B, T, H, dqk, m = 2, 23, 2, 8, 6
+    rng = np.random.default_rng(5)
+    q, k, g, v, dout = (rng.standard_normal(s) for s in [(B, T, dqk)] * 2 + [(B, T, m)] * 3)
+    full_fn = oracle.tango_backward if kind == "tango" else oracle.wango_backward
+    rows_q = [0, 1, 7, T - 1, T, T + 13, 2 * T - 1]
+    rows_k = [0, 3, T - 2, T - 1, T + 2, 2 * T - 1]
+    for qn in (False, True):
+        unit = lambda x: (x.reshape(B, T, H, -1) / np.linalg.norm(x.reshape(B, T, H, -1), axis=-1,
+                                                                   keepdims=True)).reshape(B, T, dqk)
+        qq, kk = (unit(q), unit(k)) if qn else (q, k)
+        full = full_fn(qq, kk, g, v, dout, H=H, tau=4.0, qk_normalized=qn, **kw)
+        part = oracle.backward_rows(kind, qq, kk, g, v, dout, H=H, tau=4.0, rows_q=rows_q, rows_k=rows_k,
+                                    qk_normalized=qn, **kw)
+        fq, fk = (x.reshape(B * T, -1) for x in (full["dq"], full["dk"]))
+        fg, fv = (x.reshape(B * T, -1) for x in (full["dg"], full["dv"]))
+        np.testing.assert_allclose(part["dq"], fq[rows_q], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(part["dv"], fv[rows_q], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(part["dk"], fk[rows_k], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(part["dg"], fg[rows_k], rtol=1e-12, atol=1e-12)
