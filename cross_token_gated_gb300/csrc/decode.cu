@@ -229,12 +229,14 @@ __device__ __forceinline__ void st_f32x8(float* p, int c0, int lim, const float*
 }
 
 // grid (ceil(m / 128), B), 256 threads.
-template <typename T, bool VEC>
+template <typename T, bool VEC, int C>
 __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a, int parts) {
-  __shared__ float red[kSlices][kGateCols + 4];
+  constexpr int kG = C / kGroup;  // 8-column groups
+  constexpr int kSl = 256 / kG;   // slices per group
+  __shared__ float red[kSl][C + 4];
   __shared__ float inv_den[TG_MAX_HEADS];
-  const int bb = blockIdx.y, grp = threadIdx.x % kSlices, sl = threadIdx.x / kSlices;
-  const int col0 = blockIdx.x * kGateCols, d_h = a.d_h, W = a.W, m = a.m;
+  const int bb = blockIdx.y, grp = threadIdx.x % kG, sl = threadIdx.x / kG;
+  const int col0 = blockIdx.x * C, d_h = a.d_h, W = a.W, m = a.m;
   const int c0 = col0 + grp * kGroup;  // first of this thread's 8 columns
   const long long i = a.pos;
   const int cur = (int)(i % W);
@@ -245,10 +247,10 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
   // while the score kernel runs: this thread's ring and state rows into L2 (the previous
   // step's gate kernel, which wrote them, has completed before the score kernel began)
   if (parts > 1 && c0 < m) {  // launched early (one or two sequences)
-    for (int s = sl; s < W; s += kSlices)
+    for (int s = sl; s < W; s += kSl)
       if (s != cur) prefetch_l2(ring_g + (size_t)s * m + c0);
     const int hd = c0 / a.m_h;
-    for (int d = sl; d < d_h; d += kSlices)
+    for (int d = sl; d < d_h; d += kSl)
       prefetch_l2(a.st.S + (((size_t)bb * a.H + hd) * d_h + d) * a.m_h + (c0 - hd * a.m_h));
   }
   griddep_wait();  // the window weights, feature maps and partial sums of this step
@@ -277,12 +279,12 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
     int s_begin = sl;
     if constexpr (VEC && sizeof(T) == 2) if (parts > 1) {
       const float* wrow = a.st.w + (size_t)(bb * a.H + head0) * W;
-      for (; s_begin + 7 * kSlices < W; s_begin += 8 * kSlices) {
+      for (; s_begin + 7 * kSl < W; s_begin += 8 * kSl) {
         uint4 r[8];
         float wv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int s = s_begin + u * kSlices;
+          const int s = s_begin + u * kSl;
           r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
           wv[u] = wrow[s];
         }
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
       }
     }
 #pragma unroll 2
-    for (int s = s_begin; s < W; s += kSlices) {
+    for (int s = s_begin; s < W; s += kSl) {
       Cols8<T, VEC>::ld(s == cur ? gin : ring_g + (size_t)s * m, c0, lim, x);
       if (VEC) {
         const float w = a.st.w[(size_t)(bb * a.H + head0) * W + s];
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
     float gl[kGroup];
     if (lslot >= 0) Cols8<T, VEC>::ld(lslot == cur ? gin : ring_g + (size_t)lslot * m, c0, lim, gl);
 #pragma unroll 1
-    for (int d = sl; d < d_h; d += kSlices) {
+    for (int d = sl; d < d_h; d += kSl) {
       if (VEC) {
         const size_t bh = (size_t)bb * a.H + head0;
         float* Srow = a.st.S + (bh * d_h + d) * a.m_h;
@@ -353,12 +355,12 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
   __syncthreads();
   // one column per thread: the slices' sums, the denominator, u = gbar * v, and the
   // current token's g into its ring slot
-  if (threadIdx.x < kGateCols) {
+  if (threadIdx.x < C) {
     const int c = col0 + threadIdx.x;
     if (c < m) {
       float num = 0.f;
 #pragma unroll
-      for (int r = 0; r < kSlices; ++r) num += red[r][threadIdx.x];
+      for (int r = 0; r < kSl; ++r) num += red[r][threadIdx.x];
       const int hd = c / a.m_h;
       const float gbar = num * inv_den[hd];
       const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * m + c) : gbar;
@@ -372,8 +374,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 template <typename T>
 cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
-  // one or two sequences: the ring split over 8 CTAs per head (a short dependent chain
-  // per CTA) and the gate kernel launched early
+  // one or two sequences: the ring split over up to 8 CTAs per head (a short dependent
+  // chain per CTA) and the gate kernel launched early
   const bool few = a.B <= 2;
   const int parts = few ? min(kMaxParts, (a.W + 31) / 32) : 1;
   wango_decode_scores_kernel<T><<<dim3(a.H, a.B, parts), 256, 0, s>>>(a);
@@ -381,14 +383,17 @@ cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
   // 8-column group straddles a head
   const bool vec = (a.m * sizeof(T)) % 16 == 0 && a.m_h % kGroup == 0 && aligned16(a.g) &&
                    aligned16(a.st.ring_g) && aligned16(a.st.S);
-  const dim3 grid((a.m + kGateCols - 1) / kGateCols, a.B);
-  if (!few) {  // enough CTAs to hide latency: a plain launch
-    if (vec) wango_decode_gate_kernel<T, true><<<grid, 256, 0, s>>>(a, parts);
-    else wango_decode_gate_kernel<T, false><<<grid, 256, 0, s>>>(a, parts);
+  if (!few) {  // enough CTAs to hide latency: 128-column blocks and a plain launch
+    const dim3 grid((a.m + kGateCols - 1) / kGateCols, a.B);
+    if (vec) wango_decode_gate_kernel<T, true, kGateCols><<<grid, 256, 0, s>>>(a, parts);
+    else wango_decode_gate_kernel<T, false, kGateCols><<<grid, 256, 0, s>>>(a, parts);
     return cudaGetLastError();
   }
+  // one or two sequences: launched as a programmatic dependent of the score kernel; for
+  // one sequence in 64-column blocks (twice the CTAs, spread more evenly over the SMs)
+  const int cols = a.B == 1 ? 64 : kGateCols;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3((a.m + cols - 1) / cols, a.B);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -396,8 +401,11 @@ cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true>, a, parts)
-             : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false>, a, parts);
+  if (cols == 64)
+    return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, 64>, a, parts)
+               : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, 64>, a, parts);
+  return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, kGateCols>, a, parts)
+             : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, kGateCols>, a, parts);
 }
 
 }  // namespace
