@@ -27,6 +27,8 @@ TG_F32, TG_BF16 = 0, 1
 TG_FLAG_QK_NORMALIZED = 0x1
 TG_FLAG_DEBUG_TIMEOUT = 0x100
 TG_FLAG_FUSED_V = 0x200
+TG_FLAG_BWD_FAR_SCAN = 0x400
+TG_FLAG_BWD_FAR_PAIRS = 0x800
 TG_MODE_TANGO, TG_MODE_WANGO = 0, 1
 TG_WS_TANGO, TG_WS_WANGO, TG_WS_BLOCK, TG_WS_MODEL, TG_WS_DECODE, TG_WS_TANGO_BWD, TG_WS_WANGO_BWD = range(7)
 

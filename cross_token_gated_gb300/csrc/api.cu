@@ -280,16 +280,21 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
 
 // ---- aggregation backward (bf16, tensor cores)
 tg_status validate_bwd(const tg_agg_params* p, bool wango) {
-  tg_status st = validate_agg(p, wango);
+  const unsigned far_flags = TG_FLAG_BWD_FAR_SCAN | TG_FLAG_BWD_FAR_PAIRS;
+  if (p->flags & ~(TG_FLAG_QK_NORMALIZED | (wango ? far_flags : 0u))) return TG_ERR_INVALID_ARG;
+  tg_agg_params shape = *p;  // the forward's checks, without the backward-only flags
+  shape.flags &= ~far_flags;
+  tg_status st = validate_agg(&shape, wango);
   if (st != TG_OK) return st;
-  if (p->flags & ~TG_FLAG_QK_NORMALIZED) return TG_ERR_INVALID_ARG;
+  if ((p->flags & far_flags) == far_flags) return TG_ERR_INVALID_ARG;
   if (p->dtype != TG_BF16) return TG_ERR_UNSUPPORTED;
   return TG_OK;
 }
 
 struct BwdWs {
-  size_t qn, kn, gbar, den, dp, E, X, Xo, aux, erev, qrev, krev, total;
+  size_t qn, kn, gbar, den, dp, E, X, Xo, aux, erev, qrev, krev, part, rb, total;
   int T_pad;
+  bool scan;  // WANGO: far older pairs through the running sums
 };
 BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
   const size_t B = p->B, T = p->T, H = p->H, m = mem_width(p), dqk = p->d_qk;
@@ -316,7 +321,16 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
   L.erev = L.aux + align256(aux);
   L.qrev = L.erev + (wango ? align256(B * Tp * m * 2) : 0);
   L.krev = L.qrev + (wango ? align256(B * Tp * dqk * 2) : 0);
-  L.total = L.krev + (wango ? align256(B * Tp * dqk * 2) : 0);
+  L.part = L.krev + (wango ? align256(B * Tp * dqk * 2) : 0);
+  // WANGO with blocks wholly beyond the window's band: the scans' per-strip sums (two
+  // directions) and the block sums for rho
+  const int band = bwd_band(p->window), nblk = L.T_pad / 128;
+  L.scan = wango && nblk - band - 1 > 0 && !(p->flags & TG_FLAG_BWD_FAR_PAIRS) &&
+           ((p->flags & TG_FLAG_BWD_FAR_SCAN) || bwd_scan_pays(p->B, p->T, p->H, p->d_qk, p->m / p->H, p->window));
+  const size_t strips = L.scan ? (size_t)bwd_scan_strips(p->B, p->H, p->m / p->H) : 0;
+  L.rb = L.part + (L.scan ? align256(2 * strips * B * T * dqk * 4) : 0);
+  // rb, then the two plain far sums
+  L.total = L.rb + (L.scan ? align256(3 * B * H * nblk * (dqk / H) * 4) : 0);
   return L;
 }
 
@@ -402,6 +416,26 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   pa.X = base + L.X;
   pa.X_old = wango ? base + L.Xo : nullptr;
   pa.err = err;
+  const size_t part_half = L.scan ? (size_t)bwd_scan_strips(p->B, p->H, p->m / p->H) * p->B * p->T * p->d_qk : 0;
+  float* part = reinterpret_cast<float*>(base + L.part);
+  if (L.scan) {  // the far older pairs through the running sums; the pair kernel keeps the band
+    pa.band = bwd_band(p->window);
+    BwdScanArgs sa;
+    sa.B = p->B; sa.T = p->T; sa.H = p->H; sa.dqk = p->d_qk; sa.m = mem_width(p); sa.m_h = p->m / p->H;
+    sa.window = p->window;
+    sa.E = E; sa.g = g;
+    sa.fq = wango_fq_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window);
+    sa.fk = wango_fk_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window);
+    sa.zb = wango_zb_in_aux(aux, p->B, p->T, p->H, p->d_qk, p->m, p->window);
+    sa.dp = dp;
+    sa.part[0] = part;
+    sa.part[1] = part + part_half;
+    sa.rb = reinterpret_cast<float*>(base + L.rb);
+    sa.fb = sa.rb + (size_t)p->B * p->H * (L.T_pad / 128) * (p->d_qk / p->H);
+    sa.err = err;
+    e = launch_bwd_scan(sa, stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+  }
   e = launch_bwd_pairs_tc(pa, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
   BwdQKTcArgs qa;
@@ -414,6 +448,11 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   qa.raw_q = norm ? q : nullptr;
   qa.raw_k = norm ? k : nullptr;
   qa.dq = dq; qa.dk = dk; qa.err = err;
+  if (L.scan) {
+    qa.band = bwd_band(p->window);
+    qa.far[0] = part;
+    qa.far[1] = part + part_half;
+  }
   e = launch_bwd_qk_tc(qa, stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 

@@ -43,9 +43,39 @@ struct BwdPairsArgs {
   const float* dp;   // [B * H, T_pad]
   void* X;           // [B * H, T_pad, T_pad] bf16: window pairs
   void* X_old;       // the same for older pairs (WANGO), else NULL
+  int band = -1;     // WANGO with the far older pairs left to the scans: only source blocks
+                     // jb >= ib - band of destination block ib (band = ceil((W - 1) / 128))
   unsigned* err;
 };
 cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& a, cudaStream_t s);
+// WANGO: the far older pairs' feature-map gradients through running sums (backward_tc.cu).
+// The scans write per-strip sums (strips of 256-512 gate columns) into part[0] [strips, B*T,
+// H, d_h] for dFq (sum_far (E_i . g_j) Fk_j) and part[1] for dFk (sum_far (E_i . g_j)
+// Fq_i); a reduction then leaves in strip 0 of each, for every row of a far block, the
+// whole far term: sum_far (E_i . g_j - D_i) Fk_j (part[0]) and sum_far (E_i . g_j - D_i)
+// Fq_i (part[1]).  rb [B, H, nblk, d_h] holds the block sums of D_i Fq_i and fb [2, B,
+// H, nblk, d_h] the plain far sums of Fk (per destination block) and of D_i Fq_i (per
+// source block).
+struct BwdScanArgs {
+  int B, T, H, dqk, m, m_h, window;
+  const void* E;
+  const void* g;
+  const void* fq;
+  const void* fk;
+  const float* zb;  // [B, H, nblk, d_h] block sums of Fk (the forward's)
+  const float* dp;  // [B * H, T_pad]
+  float* part[2];
+  float* rb;
+  float* fb;
+  unsigned* err;
+};
+// Strips of the scans (of bwd_scan_ns columns each) for B * H sequence-heads of m_h gates.
+int bwd_scan_strips(int B, int H, int m_h);
+int bwd_scan_ns(int B, int H, int m_h);
+int bwd_band(int window);
+// Whether the scans are estimated to beat forming the far older pairs one by one.
+bool bwd_scan_pays(int B, int T, int H, int dqk, int m_h, int window);
+cudaError_t launch_bwd_scan(const BwdScanArgs& a, cudaStream_t s);
 // dq and dk from X and X_old on the tensor cores (backward_tc.cu): window pairs through
 // the unit vectors, older pairs through the forward's bf16 feature maps fq =
 // e^-tau phi(sqrt(tau) qhat) and fk = phi(sqrt(tau) khat) and phi', then the unit
@@ -65,6 +95,10 @@ struct BwdQKTcArgs {
   const void* raw_k;
   void* dq;
   void* dk;
+  // far older pairs from the scans (band >= 0): partner blocks beyond the band are skipped
+  // and far[side] [B*T, H, d_h] (f32, rows of far blocks only) is added instead
+  int band = -1;
+  const float* far[2] = {nullptr, nullptr};
   unsigned* err;
 };
 cudaError_t launch_bwd_qk_tc(const BwdQKTcArgs& a, cudaStream_t s);
@@ -77,6 +111,7 @@ const float* wango_den_in_aux(const void* aux, int B, int T, int H, int dqk, int
 // [B, T, dqk], in the same scratch.
 const void* wango_fq_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
 const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
+const float* wango_zb_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W);
 // The WANGO feature-map pre-pass alone (fq, fk and the block sums of fk into a.aux).
 cudaError_t launch_wango_prepass(const AggArgs& a, cudaStream_t s);
 cudaError_t launch_wango_tc(const AggArgs& a, cudaStream_t s);

@@ -1217,6 +1217,9 @@ const void* wango_fq_in_aux(const void* aux, int B, int T, int H, int dqk, int m
 const void* wango_fk_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
   return static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).fk;
 }
+const float* wango_zb_in_aux(const void* aux, int B, int T, int H, int dqk, int m, int W) {
+  return reinterpret_cast<const float*>(static_cast<const char*>(aux) + aux_layout(B, T, H, dqk, m, W).zb);
+}
 
 cudaError_t launch_wango_prepass(const AggArgs& p, cudaStream_t s) {
   const int m_h = p.m_h ? p.m_h : p.m / p.H;

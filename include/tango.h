@@ -75,6 +75,14 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
                                         formed inside the aggregation kernel instead of by
                                         the projection GEMM (v is then never stored); see
                                         tango_block_forward */
+#define TG_FLAG_BWD_FAR_SCAN 0x400u  /* wango_aggregate_backward: the older pairs beyond the
+                                        window's band of 128-row blocks always go through
+                                        running-sum scans (linear in T) */
+#define TG_FLAG_BWD_FAR_PAIRS 0x800u /* wango_aggregate_backward: every older pair is formed
+                                        pair by pair (T^2 m).  With neither flag the call
+                                        picks by an estimate of the two costs (scans from
+                                        about T = 4,096 at B = 8, m = 28,480); both flags:
+                                        TG_ERR_INVALID_ARG */
 
 /* tango_block_forward mode */
 #define TG_MODE_TANGO 0
@@ -215,8 +223,15 @@ tg_status tango_aggregate_backward(const tg_agg_params *p, const void *q, const 
  * Window pairs contribute as in TANGO; an older
  * pair's weight phi(sqrt(tau) qhat_i) . phi(sqrt(tau) khat_j) passes its gradient
  * through phi' (ELU's derivative, over sqrt(d_h) for eq. 8) and sqrt(tau).  dg is the
- * forward numerator of the time-reversed sequence (linear in T); the weight gradients
- * of the older pairs are formed pair by pair, so that part costs T^2 m like TANGO's.
+ * forward numerator of the time-reversed sequence (linear in T).  The older pairs next
+ * to the window (128-row blocks within ceil((W-1)/128) of the destination's) are formed
+ * pair by pair; the rest either pair by pair too (T^2 m) or through running sums of
+ * phi(k~_j) g_j^T and of phi(q~_i) E_i^T, eq. 10 taken backwards (linear in T): flags may
+ * add TG_FLAG_BWD_FAR_SCAN or TG_FLAG_BWD_FAR_PAIRS to force one, else the call picks
+ * by a cost estimate that depends on the current device's SM count (query the workspace
+ * with the same device current).  The scans add 2 * ceil(m_h / n_s) * B * T * d_qk * 4
+ * bytes of workspace (strips of n_s = 256, 384 or 512 gate columns, also picked by the SM
+ * count).
  */
 tg_status wango_aggregate_backward(const tg_agg_params *p, const void *q, const void *k, const void *g,
                                    const void *v, const void *dout, const void *gbar, const float *den,

@@ -243,6 +243,12 @@ def test_backward_validation_and_workspace(lib):
         assert fn(ctypes.byref(p), 256, 256, 256, 256, 256, 256, None, 256, 256, 256, 256, None, 0, None) == \
             tg.TG_ERR_INVALID_ARG
         assert fn(ctypes.byref(p), *a, None, 0, None) == tg.TG_ERR_WORKSPACE
+    # the far-pair choice: WANGO only, not both at once
+    both = tg.TG_FLAG_BWD_FAR_SCAN | tg.TG_FLAG_BWD_FAR_PAIRS
+    assert raw.wango_aggregate_backward(ctypes.byref(_agg(flags=both)), *a, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert raw.tango_aggregate_backward(ctypes.byref(_agg(flags=tg.TG_FLAG_BWD_FAR_SCAN)), *a, None, 0, None) == \
+        tg.TG_ERR_INVALID_ARG
+    assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=both)) == 0
     for fn in (raw.tango_aggregate_save, raw.wango_aggregate_save):
         assert fn(ctypes.byref(p), 256, 256, 256, 256, 256, None, 256, None, 0, None) == tg.TG_ERR_INVALID_ARG
         assert fn(ctypes.byref(_agg(dtype=tg.TG_F32)), 256, 256, 256, 256, 256, 256, 256, None, 0, None) == \
@@ -272,3 +278,23 @@ def test_gate_pitch_validation(lib):
     assert tg.tg_workspace_size(tg.TG_WS_BLOCK, bp) == 0
     dp = _agg(m=512, m_pitch=264)
     assert tg.tg_workspace_size(tg.TG_WS_DECODE, dp) == 0
+
+
+def test_backward_far_scan_workspace(lib):
+    """WANGO's far older pairs through the scans need their per-strip sums, 2 directions x
+    ceil(m_h / n_s) strips (n_s in 512, 384, 256) x B * T * d_qk floats, plus 3 x B * H * nblk * d_h floats of
+    block sums; the pair path needs neither.  With no block beyond the window's band
+    (T = 300, W = 200: 3 blocks, band 2) the two are the same."""
+    kw = dict(B=2, T=1500, H=2, d_qk=128, m=4096, window=64)
+    scan = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_SCAN, **kw))
+    pairs = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_PAIRS, **kw))
+    nblk = -(-1500 // 128)
+    fits = [s for s in (-(-2048 // ns) for ns in (512, 384, 256))
+            if 0 <= scan - pairs - (2 * s * 2 * 1500 * 128 * 4 + 3 * 2 * 2 * nblk * 64 * 4) <= 512]
+    assert fits, scan - pairs
+    # the library's own choice is one of the two
+    auto = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(**kw))
+    assert auto in (scan, pairs)
+    kw = dict(B=2, T=300, H=2, d_qk=128, m=512, window=200)
+    assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_SCAN, **kw)) == \
+        tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_PAIRS, **kw))

@@ -85,7 +85,13 @@ def grad_scales(kind, view, H, s, W, phi_mode, nbo, normalized):
     return sq, sk
 
 
-def run(kind, B, T, H, dqk, m, *, W=16, phi_mode=0, null=False, has_v=True, normalized=False, seed=0, s=10.0):
+FAR_FLAGS = {None: 0, "scan": tg.TG_FLAG_BWD_FAR_SCAN, "pairs": tg.TG_FLAG_BWD_FAR_PAIRS}
+
+
+def run(kind, B, T, H, dqk, m, *, W=16, phi_mode=0, null=False, has_v=True, normalized=False, seed=0, s=10.0,
+        far=None):
+    """far: how WANGO forms the older pairs beyond the window's band of blocks ("scan":
+    running sums, "pairs": pair by pair, None: the library's choice)."""
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=seed, dtype="bf16")
     if normalized:  # unit vectors per head, rounded to bf16
         qf, kf = q.float().view(B, T, H, -1), k.float().view(B, T, H, -1)
@@ -105,7 +111,7 @@ def run(kind, B, T, H, dqk, m, *, W=16, phi_mode=0, null=False, has_v=True, norm
         tg.tango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, s=s, null_bias=nbd, flags=flags)
     else:
         tg.wango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, window=W, s=s, null_bias=nbd, phi_mode=phi_mode,
-                                    flags=flags)
+                                    flags=flags | FAR_FLAGS[far])
     st, word = tg.tg_check_device_error()
     assert st == tg.TG_OK, (st, hex(word))
     view = [synth.oracle_view(t) if t is not None else None for t in (q, k, g, v, dout)]
@@ -164,22 +170,56 @@ def test_backward_t1():
 
 @pytest.mark.parametrize("W", [1, 16, 200, 1000])
 @pytest.mark.parametrize("phi_mode", [0, 1])
-def test_wango_backward_small(W, phi_mode):
-    run("wango", 1, 300, 2, 128, 512, W=W, phi_mode=phi_mode, seed=W + phi_mode)
+@pytest.mark.parametrize("far", ["scan", "pairs"])
+def test_wango_backward_small(W, phi_mode, far):
+    """T = 300 (3 blocks): W = 1 and 16 leave blocks beyond the band (the scans' far
+    pairs, 2 and 1 steps), W = 200 and 1000 none."""
+    run("wango", 1, 300, 2, 128, 512, W=W, phi_mode=phi_mode, seed=W + phi_mode, far=far)
 
 
-def test_wango_backward_shapes():
-    run("wango", 2, 129, 2, 64, 256, W=40, seed=11)
-    run("wango", 1, 520, 2, 128, 1040, W=256, seed=12)
-    run("wango", 1, 300, 2, 128, 512, W=64, null=True, has_v=False, seed=13)
-    run("wango", 3, 64, 4, 128, 384, W=8, normalized=True, seed=14)
+@pytest.mark.parametrize("far", ["scan", "pairs"])
+def test_wango_backward_shapes(far):
+    run("wango", 2, 129, 2, 64, 256, W=40, seed=11, far=far)
+    run("wango", 1, 520, 2, 128, 1040, W=256, seed=12, far=far)
+    run("wango", 1, 300, 2, 128, 512, W=64, null=True, has_v=False, seed=13, far=far)
+    run("wango", 3, 64, 4, 128, 384, W=8, normalized=True, seed=14, far=far)
+    # d_h = 16 and 32 through the scans, 5 and 7 blocks, a strip's partial last chunk
+    run("wango", 2, 600, 4, 64, 1120, W=100, seed=15, far=far)
+    run("wango", 1, 900, 4, 128, 2592, W=130, normalized=True, seed=16, far=far)
 
 
-@pytest.mark.parametrize("kind", ["tango", "wango"])
-def test_backward_full_width(kind):
-    """The 70M-tier gate width (m = 28,480 as two heads of 14,240), one 640-token
-    sequence compared in full."""
-    run(kind, 1, 640, 2, 128, 28480, W=256, seed=21)
+@pytest.mark.parametrize("kind,far", [("tango", None), ("wango", "scan"), ("wango", "pairs")])
+def test_backward_full_width(kind, far):
+    """The 70M-tier gate width (m = 28,480 as two heads of 14,240, i.e. 38 strips of 384
+    for the scans at B = 1), one 640-token sequence compared in full."""
+    run(kind, 1, 640, 2, 128, 28480, W=256, seed=21, far=far)
+
+
+@pytest.mark.parametrize("B,T,H,dqk,m,W", [(2, 1500, 2, 128, 4096, 64), (8, 2048, 2, 128, 28480, 256)])
+def test_wango_backward_far_paths_agree(B, T, H, dqk, m, W):
+    """The scans and the pair path give the same dq and dk within bf16 rounding (the
+    pair path rounds X_ij to bf16, the scans their running sums), and dg, dv bit for bit
+    (neither depends on the choice): B = 2, T = 1,500, W = 64 (11 blocks beyond the band
+    of 1), and the benchmark shape, where the side-1 far rows (the first 13 blocks) are
+    beyond the oracle's reach at this size."""
+    q, k, g, v = (t.cuda() for t in synth.agg_inputs(B, T, dqk, m, seed=41, dtype="bf16"))
+    dout = synth.upstream_grad(B, T, m, seed=42).cuda()
+    res = {}
+    for far in ("scan", "pairs"):
+        dq, dk, dg, dv = (torch.empty_like(x) for x in (q, k, g, g))
+        tg.wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H, window=W, flags=FAR_FLAGS[far])
+        st, word = tg.tg_check_device_error()
+        assert st == tg.TG_OK, (st, hex(word))
+        res[far] = (dq, dk, dg, dv)
+    for name, a, b in zip(("dq", "dk"), res["scan"][:2], res["pairs"][:2]):
+        e = float((a.float() - b.float()).abs().max() / b.float().abs().max())
+        assert e <= TOL, (name, e)
+        # per (row, head), against the row's own scale
+        d = (a.float() - b.float()).view(B * T, H, -1).abs().amax(-1)
+        r = b.float().view(B * T, H, -1).abs().amax(-1)
+        assert float((d / (r + 1e-2 * float(r.max()))).max()) <= 4 * TOL, name
+    assert torch.equal(res["scan"][2], res["pairs"][2])
+    assert torch.equal(res["scan"][3], res["pairs"][3])
 
 
 @pytest.mark.parametrize("kind", ["tango", "wango"])
@@ -279,8 +319,8 @@ def test_saved_forward_feeds_the_backward(kind):
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("kind", ["tango", "wango"])
-def test_backward_full_size_sampled_rows(kind):
+@pytest.mark.parametrize("kind,far", [("tango", None), ("wango", "pairs"), ("wango", "scan")])
+def test_backward_full_size_sampled_rows(kind, far):
     """B = 8, T = 2,048, m = 28,480 (the benchmark shape, W = 256 for WANGO): dq and dv at
     sampled destinations (first, window and block edges, last, random) and dk, dg at the
     last sources of two sequences, against the oracle's gradients at those rows alone.
@@ -293,7 +333,7 @@ def test_backward_full_size_sampled_rows(kind):
     if kind == "tango":
         tg.tango_aggregate_backward(*dev, dq, dk, dg, dv, H=H)
     else:
-        tg.wango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, window=W)
+        tg.wango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, window=W, flags=FAR_FLAGS[far])
     st, word = tg.tg_check_device_error()
     assert st == tg.TG_OK, (st, hex(word))
     rng = np.random.default_rng(73)
