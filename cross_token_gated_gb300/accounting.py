@@ -122,9 +122,10 @@ def agg_bwd_bytes(B: int, T: int, dqk: int, m: int, elem: int = 2) -> int:
     return B * T * (4 * dqk + 5 * m) * elem
 
 
-def decode_bytes(B: int, dqk: int, m: int, H: int, W: int, elem: int = 2) -> int:
-    """One WANGO decode step: the ring of W gate vectors read, the f32 state S read and
-    written, and this token's g, v read and u written (sec. 2.2 eq. 10 taken one token
-    at a time); the q/k-sized terms are negligible and not counted."""
+def decode_bytes(B: int, dqk: int, m: int, H: int, W: int, elem: int = 2, fold: int = 8) -> float:
+    """One WANGO decode step, on average: the ring of W gate vectors read, the f32 state
+    S read, S written once per `fold` steps (sources enter S in groups of `fold`), and
+    this token's g, v read and u written (sec. 2.2 eq. 10 taken one token at a time); the
+    q/k-sized terms are negligible and not counted."""
     d_h = dqk // H
-    return B * (W * m * elem + 2 * d_h * m * 4 + 3 * m * elem)
+    return B * (W * m * elem + d_h * m * 4 * (1 + 1 / fold) + 3 * m * elem)

@@ -187,6 +187,7 @@ tg_status validate_decode(const tg_agg_params* p) {
   if (p->dtype != TG_F32 && p->dtype != TG_BF16) return TG_ERR_INVALID_ARG;
   if (!p->tau && !(p->s >= 0.f && p->s <= 20.f)) return TG_ERR_INVALID_ARG;
   if (p->window < 1 || (p->phi_mode != 0 && p->phi_mode != 1)) return TG_ERR_INVALID_ARG;
+  if (p->window > (1 << 30)) return TG_ERR_UNSUPPORTED;  // the ring's slot count stays an int
   if (p->flags & ~TG_FLAG_QK_NORMALIZED) return TG_ERR_INVALID_ARG;
   if (p->m_pitch != 0 && p->m_pitch != p->m / p->H) return TG_ERR_UNSUPPORTED;  // dense tensors only
   if (p->d_qk / p->H > 128) return TG_ERR_UNSUPPORTED;
@@ -197,16 +198,16 @@ struct DecodeWs {
   size_t S, z, ring_k, ring_g, w, fq, fk, wpart, older, total;
 };
 DecodeWs decode_ws_layout(const tg_agg_params* p) {
-  const size_t B = p->B, H = p->H, W = p->window, d_h = p->d_qk / p->H;
+  const size_t B = p->B, H = p->H, R = (size_t)p->window + kDecodeFold, d_h = p->d_qk / p->H;
   DecodeWs L;
   L.S = 0;
   L.z = L.S + align256(B * d_h * p->m * 4);
   L.ring_k = L.z + align256(2 * B * H * d_h * 4);
-  L.ring_g = L.ring_k + align256(B * H * W * d_h * elem_size(p->dtype));
-  L.w = L.ring_g + align256(B * W * p->m * elem_size(p->dtype));
-  L.fq = L.w + align256(B * H * W * 4);
+  L.ring_g = L.ring_k + align256(B * H * R * d_h * elem_size(p->dtype));
+  L.w = L.ring_g + align256(B * R * p->m * elem_size(p->dtype));
+  L.fq = L.w + align256(B * H * R * 4);
   L.fk = L.fq + align256(B * H * d_h * 4);
-  L.wpart = L.fk + align256(B * H * d_h * 4);
+  L.wpart = L.fk + align256(B * H * kDecodeFold * d_h * 4);
   L.older = L.wpart + align256(B * H * 8 * 4);
   L.total = L.older + align256(B * H * 4);
   return L;
@@ -682,7 +683,7 @@ tg_status wango_decode_step(const tg_agg_params* p, long long pos, const void* q
   ds.ring_g = base + L.ring_g;
   ds.w = reinterpret_cast<float*>(base + L.w);
   ds.fq = reinterpret_cast<float*>(base + L.fq);
-  ds.fk_leave = reinterpret_cast<float*>(base + L.fk);
+  ds.fk_fold = reinterpret_cast<float*>(base + L.fk);
   ds.wpart = reinterpret_cast<float*>(base + L.wpart);
   ds.older = reinterpret_cast<float*>(base + L.older);
   unsigned* err = nullptr;

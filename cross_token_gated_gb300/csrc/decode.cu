@@ -1,21 +1,28 @@
 // WANGO autoregressive decode step, "TANGO: Token-Aggregated Nonlinear Gating
 // Operators ...", sec. 2.2 eqs. 7-10: destination i = pos takes exp(tau (qhat.khat_j - 1))
-// weights over its window j = i-W+1 .. i and, for every older source, the running sums
-//   S = sum_{j <= i-W} phi(k~_j) g_j^T   (d_h x m_h per head),   z = sum phi(k~_j),
-// read out as e^-tau phi(q~_i)^T S and e^-tau phi(q~_i)^T z (eq. 10).  After the
-// output, source i-W+1 leaves the window and enters S and z, and the current token joins
-// the ring of the last W tokens.  One call per token; the state is constant-size in T.
+// weights over its window j = i-W+1 .. i and, for every older source, the feature-map
+// weight e^-tau phi(q~_i) . phi(k~_j), summed through the running sums
+//   S = sum_j phi(k~_j) g_j^T   (d_h x m_h per head),   z = sum_j phi(k~_j)
+// and read out as e^-tau phi(q~_i)^T S and e^-tau phi(q~_i)^T z (eq. 10).  One call per
+// token; the state is constant-size in T.
+//
+// Sources enter S and z in groups of kDecodeFold: a source that leaves the window stays
+// in the ring (W + kDecodeFold slots) with its feature-map weight computed directly until
+// its group is complete, and the step that completes a group adds the whole group to S
+// and z.  S is therefore rewritten on one step in kDecodeFold instead of on every step
+// (S is about a quarter of a step's bytes at W = 256, d_h = 64); the sums are the same.
 //
 // Two kernels per step:
 //   wango_decode_scores_kernel  per (head, batch, part of the ring): unit q and k, the
-//       window weights of its ring slots and their partial sum; the first part also the
-//       feature maps, the older-prefix term, z's update and the ring's khat slot.  At
-//       one or two sequences the ring is split over 8 CTAs per head, so that the chain
-//       of dependent steps in one CTA is short.
-//   wango_decode_gate_kernel    per 128 gate columns and batch (HBM-bound): the
-//       denominator from the partial sums, the window sum over the ring of g, the
-//       older-prefix read-out from S, u = gbar * v, the leaving token's rank-1 update of
-//       S and the ring's g slot.  At one or two sequences it is launched as a
+//       weights of its ring slots (window, or left the window and not yet folded) and
+//       their partial sum; the first part also the feature maps, the older-prefix term
+//       Fq . z, the current key into its ring slot, and on a fold step the group's feature
+//       maps and z's update.  At one or two sequences the ring is split over 8 CTAs per
+//       head, so that the chain of dependent steps in one CTA is short.
+//   wango_decode_gate_kernel    per 128 (or 64) gate columns and batch (HBM-bound): the
+//       denominator from the partial sums, the weighted sum over the ring of g, the
+//       read-out Fq^T S, u = gbar * v, on a fold step S's update by the group, and the
+//       current token's g into its ring slot.  At one or two sequences it is launched as a
 //       programmatic dependent of the score kernel: it asks its rows of the ring and of
 //       S into L2 while the score kernel runs, and waits for the scores only then.
 #include <math.h>
@@ -38,13 +45,10 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
-__device__ __forceinline__ uint32_t smem_u32_of(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
 template <typename T>
 struct DecodeArgs {
   int B, H, dqk, m, d_h, m_h, W;
+  int R;  // ring slots, W + kDecodeFold
   long long pos;
   float s;
   const float* tau;
@@ -74,17 +78,30 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// grid (H, B, parts), 256 threads; part p takes ring slots [p * ceil(W / parts), ...).
+// Which sources a step sees where (i = pos): the window i-W+1 .. i; the sources from
+// `first` (the oldest not yet in S, a multiple of kDecodeFold) to i-W through the ring with
+// their feature-map weight; everything older through S and z.  The step folds when the
+// source that leaves after it, i-W+1, completes a group.
+__device__ __forceinline__ long long first_unfolded(long long i, int W) {
+  const long long lo = i - W + 1;
+  return lo > 0 ? (long long)kDecodeFold * (lo / kDecodeFold) : 0;
+}
+__host__ __device__ __forceinline__ bool fold_step(long long i, int W) {
+  const long long lo = i - W + 1;
+  return lo >= 0 && (lo + 1) % kDecodeFold == 0;
+}
+
+// grid (H, B, parts), 256 threads; part p takes ring slots [p * ceil(R / parts), ...).
 template <typename T>
 __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeArgs<T> a) {
-  __shared__ float qh[kMaxDh], kh[kMaxDh], red[8];
-  __shared__ __align__(16) unsigned char kstage[32768];  // a chunk of the ring's keys
+  __shared__ float qh[kMaxDh], kh[kMaxDh], fqs[kMaxDh], red[8];
+  __shared__ __align__(16) unsigned char kstage[40960];  // a chunk of the ring's keys
   const int head = blockIdx.x, bb = blockIdx.y, part = blockIdx.z, t = threadIdx.x;
-  const int d_h = a.d_h, W = a.W;
+  const int d_h = a.d_h, W = a.W, R = a.R;
   const long long i = a.pos;
   const int bh = bb * a.H + head;
-  const int per = (W + gridDim.z - 1) / gridDim.z;
-  const int s_lo = min(W, part * per), s_hi = min(W, s_lo + per);
+  const int per = (R + gridDim.z - 1) / gridDim.z;
+  const int s_lo = min(R, part * per), s_hi = min(R, s_lo + per);
   griddep_launch_dependents();  // the gate kernel may start fetching its rows now
   const float tau = head_tau(a.tau, a.s, head, a.err, kKernWango);
   const float sq = sqrtf(tau), shift = expf(-tau), inv_sqrt_dh = rsqrtf((float)d_h);
@@ -100,30 +117,20 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
     T kr1;
     io<T>::st(&kr1, kv / kn);
     kh[t] = io<T>::ld(&kr1);
+    fqs[t] = shift * phi_of(sq * qh[t], inv_sqrt_dh, a.phi_mode);  // e^-tau phi(q~)
   }
   __syncthreads();
-  // the current token's khat into its ring slot (slot i mod W held source i - W, which is
-  // already in the state and outside the window)
-  T* ring_k = static_cast<T*>(a.st.ring_k) + (size_t)bh * W * d_h;
-  const int cur = (int)(i % W);
-  const long long jl = i - W + 1;  // the source that leaves the window after this step
-  const int lslot = jl >= 0 ? (int)(jl % W) : -1;
-  // part 0: feature map of the leaving source (its slot is not rewritten this step), and
-  // the current key into its slot.  No part reads slot cur from the ring: its weight
-  // comes from kh.
-  float* fkl = a.st.fk_leave + (size_t)bh * d_h;
-  if (part == 0 && t < d_h) {
-    if (lslot >= 0) {
-      const float kl = lslot == cur ? kh[t] : io<T>::ld(ring_k + (size_t)lslot * d_h + t);
-      fkl[t] = phi_of(sq * kl, inv_sqrt_dh, a.phi_mode);
-    }
-    io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
-  }
-  // window weights: the ring's keys pass through shared memory in chunks (one coalesced
-  // copy each), then one ring slot per thread; slot s holds source j = the largest
-  // j <= i with j = s (mod W).  The dot product starts at column s (mod d_h), so the
-  // threads of a warp read different banks.
-  float* wv = a.st.w + (size_t)bh * W;
+  // the current token's khat into its ring slot (slot i mod R held source i - R, which is
+  // already in the state)
+  T* ring_k = static_cast<T*>(a.st.ring_k) + (size_t)bh * R * d_h;
+  const int cur = (int)(i % R);
+  const long long lo_win = i - W + 1, first = first_unfolded(i, W);
+  if (part == 0 && t < d_h) io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
+  // weights: the ring's keys pass through shared memory in chunks (one coalesced copy
+  // each), then one ring slot per thread; slot s holds source j = the largest j <= i with
+  // j = s (mod R).  No part reads slot cur from the ring: its weight comes from kh.  The
+  // dot products start at column s (mod d_h), so the threads of a warp read different banks.
+  float* wv = a.st.w + (size_t)bh * R;
   T* ks = reinterpret_cast<T*>(kstage);
   const int chunk = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
   float wsum = 0.f;
@@ -141,18 +148,23 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
     __syncthreads();
     for (int sl = t; sl < n; sl += blockDim.x) {
       const int s = s0 + sl;
-      const long long j = i - (long long)((cur - s + W) % W);
+      const long long j = i - (long long)((cur - s + R) % R);
       float w = 0.f;
-      if (j >= 0) {
+      if (j >= 0 && j >= first) {
         const T* kr = ks + (size_t)sl * d_h;
-        float dot = 0.f;
-        if (s == cur) {
-          for (int c = 0; c < d_h; ++c) dot = fmaf(qh[c], kh[c], dot);
-        } else {
-          for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1)
-            dot = fmaf(qh[c], io<T>::ld(kr + c), dot);
+        if (j >= lo_win) {  // in the window
+          float dot = 0.f;
+          if (s == cur) {
+            for (int c = 0; c < d_h; ++c) dot = fmaf(qh[c], kh[c], dot);
+          } else {
+            for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1)
+              dot = fmaf(qh[c], io<T>::ld(kr + c), dot);
+          }
+          w = expf(tau * (dot - 1.f));
+        } else {  // left the window, not yet in S: e^-tau phi(q~) . phi(k~_j)
+          const float* fk = a.st.fk_fold + ((size_t)bh * kDecodeFold + (int)(j % kDecodeFold)) * d_h;
+          for (int cc = 0, c = s % d_h; cc < d_h; ++cc, c = c + 1 == d_h ? 0 : c + 1) w = fmaf(fqs[c], fk[c], w);
         }
-        w = expf(tau * (dot - 1.f));
       }
       wv[s] = w;
       wsum += w;
@@ -161,28 +173,37 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   wsum = block_sum(wsum, red);
   if (t == 0) a.st.wpart[(size_t)bh * kMaxParts + part] = wsum;
   if (part != 0) return;
-  // part 0: older prefix e^-tau phi(q~) . z, then z' = z + phi(k~_leave) into the other
-  // buffer (the sums alternate between two buffers by step parity)
+  // part 0: the older prefix Fq . z; the feature map of the source that leaves the window
+  // after this step (i - W + 1) into its slot of the feature-map ring (slot j mod
+  // kDecodeFold, which no pending source holds now); z' into the other buffer (the sums
+  // alternate between two buffers by step parity): z plus, on a fold step, the group's
+  // feature maps, which the gate kernel also takes for S
   const float* z = a.st.z + ((size_t)(i & 1) * a.B * a.H + bh) * d_h;
   float* z_next = a.st.z + ((size_t)((i + 1) & 1) * a.B * a.H + bh) * d_h;
-  float* fq = a.st.fq + (size_t)bh * d_h;
-  const float fqv = t < d_h ? shift * phi_of(sq * qh[t], inv_sqrt_dh, a.phi_mode) : 0.f;
-  __syncthreads();  // fkl written above by this CTA
-  const float older = block_sum(t < d_h ? fqv * z[t] : 0.f, red);
+  const float older = block_sum(t < d_h ? fqs[t] * z[t] : 0.f, red);
   if (t < d_h) {
-    fq[t] = fqv;
-    z_next[t] = lslot >= 0 ? z[t] + fkl[t] : z[t];
+    float* fkf = a.st.fk_fold + (size_t)bh * kDecodeFold * d_h;
+    if (lo_win >= 0) {
+      const float kj = lo_win == i ? kh[t] : io<T>::ld(ring_k + (size_t)(lo_win % R) * d_h + t);
+      fkf[(int)(lo_win % kDecodeFold) * d_h + t] = phi_of(sq * kj, inv_sqrt_dh, a.phi_mode);
+    }
+    float zs = z[t];
+    if (fold_step(i, W))
+      for (int u = 0; u < kDecodeFold; ++u) zs += fkf[u * d_h + t];
+    a.st.fq[(size_t)bh * d_h + t] = fqs[t];
+    z_next[t] = zs;
   }
   if (t == 0) a.st.older[bh] = older;
 }
 
-// Gate kernel layout: a CTA takes 128 gate columns of one sequence as 16 groups of 8
-// columns, and its 256 threads split each group's work 16 ways ("slices"): slice r sums
-// the ring slots r, r + 16, ... and the state rows r, r + 16, ...  The slices' partial
+// Gate kernel layout: a CTA takes C (128 or 64) gate columns of one sequence as C / 8
+// groups of 8 columns, and its 256 threads split each group's work kSl = 2048 / C ways
+// ("slices"): slice r sums the ring slots r, r + kSl, ... and the state rows r, r + kSl,
+// ...  The slices' partial
 // sums meet in shared memory.  A thread moves 8 columns at a time (16-byte loads of
 // bf16, two of f32) when every row pitch and base allows it and no group straddles a
 // head; otherwise it takes its 8 columns one by one.
-constexpr int kGateCols = 128, kGroup = 8, kSlices = 16;
+constexpr int kGateCols = 128, kGroup = 8;
 
 template <typename T, bool VEC>
 struct Cols8 {
@@ -228,68 +249,110 @@ __device__ __forceinline__ void st_f32x8(float* p, int c0, int lim, const float*
   }
 }
 
-// grid (ceil(m / 128), B), 256 threads.
-template <typename T, bool VEC, int C>
-__global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs<T> a, int parts) {
+// The 8 columns of a fold group's g rows, kept in the storage type (bf16: one 16-byte
+// vector a row) until they are used.
+template <typename T, bool VEC, int N>
+struct FoldRows {
+  float x[N][kGroup];
+  __device__ __forceinline__ void ld(int u, const T* p, int c0, int lim) { Cols8<T, VEC>::ld(p, c0, lim, x[u]); }
+  __device__ __forceinline__ float get(int u, int e) const { return x[u][e]; }
+};
+template <int N>
+struct FoldRows<__nv_bfloat16, true, N> {
+  uint4 r[N];
+  __device__ __forceinline__ void ld(int u, const __nv_bfloat16* p, int c0, int) {
+    r[u] = *reinterpret_cast<const uint4*>(p + c0);
+  }
+  __device__ __forceinline__ float get(int u, int e) const {
+    const uint32_t w = (e >> 1) == 0 ? r[u].x : (e >> 1) == 1 ? r[u].y : (e >> 1) == 2 ? r[u].z : r[u].w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+
+// grid (ceil(m / C), B), 256 threads.  FOLD: this step completes a group (fold_step).
+// FEW: one or two sequences (launched early, the ring read in batches of 9 slots, three
+// CTAs an SM so that one sequence's 64-column blocks fit in one wave).  Each is a
+// separate instance so that the other launches keep a lean register budget.
+template <typename T, bool VEC, int C, bool FOLD, bool FEW>
+__global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
+    wango_decode_gate_kernel(const DecodeArgs<T> a, int parts) {
   constexpr int kG = C / kGroup;  // 8-column groups
   constexpr int kSl = 256 / kG;   // slices per group
+  // bf16 vectors: the ring is read kB slots a thread at a time, and for one or two
+  // sequences the first kB are loaded into registers before the scores are waited for
+  // (the ring rows and the inputs do not depend on them)
+  constexpr bool kPre = VEC && sizeof(T) == 2;
+  constexpr int kB = 9;  // W + 8 slots of W = 256 are 9 a thread at 64 columns
   __shared__ float red[kSl][C + 4];
   __shared__ float inv_den[TG_MAX_HEADS];
   const int bb = blockIdx.y, grp = threadIdx.x % kG, sl = threadIdx.x / kG;
-  const int col0 = blockIdx.x * C, d_h = a.d_h, W = a.W, m = a.m;
+  const int col0 = blockIdx.x * C, d_h = a.d_h, W = a.W, R = a.R, m = a.m;
   const int c0 = col0 + grp * kGroup;  // first of this thread's 8 columns
+  const bool col_ok = c0 < m;
   const long long i = a.pos;
-  const int cur = (int)(i % W);
-  const long long jl = i - W + 1;
-  const int lslot = jl >= 0 ? (int)(jl % W) : -1;
+  const int cur = (int)(i % R);
+  const long long j0 = i - W + 1 - (kDecodeFold - 1);  // a fold step's first source
   const T* gin = a.g + (size_t)bb * m;
-  const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * W * m;
-  // while the score kernel runs: this thread's ring and state rows into L2 (the previous
-  // step's gate kernel, which wrote them, has completed before the score kernel began)
-  if (parts > 1 && c0 < m) {  // launched early (one or two sequences)
-    for (int s = sl; s < W; s += kSl)
+  const T* ring_g = static_cast<const T*>(a.st.ring_g) + (size_t)bb * R * m;
+  // ---- before the scores: what the previous steps (completed before the score kernel
+  // began) and the inputs fix
+  uint4 r[kPre ? kB : 1];
+  if constexpr (kPre) {
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int s = sl + u * kSl;
+      r[u] = make_uint4(0, 0, 0, 0);
+      if (col_ok && s < R) r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
+    }
+  }
+  if (FEW && col_ok) {  // this thread's state rows (and any further ring rows) into L2
+    for (int s = sl + (kPre ? kB * kSl : 0); s < R; s += kSl)
       if (s != cur) prefetch_l2(ring_g + (size_t)s * m + c0);
     const int hd = c0 / a.m_h;
     for (int d = sl; d < d_h; d += kSl)
       prefetch_l2(a.st.S + (((size_t)bb * a.H + hd) * d_h + d) * a.m_h + (c0 - hd * a.m_h));
   }
-  griddep_wait();  // the window weights, feature maps and partial sums of this step
-  if (threadIdx.x < a.H) {  // this sequence's denominators
-    const int hd = threadIdx.x, bh = bb * a.H + hd;
-    float wsum = 0.f;
-    for (int p = 0; p < parts; ++p) wsum += a.st.wpart[(size_t)bh * kMaxParts + p];
-    const float tau = head_tau(a.tau, a.s, hd, a.err, kKernWango);
-    const float null_w = a.null_bias ? expf(a.null_bias[hd] - tau) : 0.f;
-    inv_den[hd] = 1.f / (wsum + a.st.older[bh] + (float)(i + 1) * null_w);
+  const int oc = col0 + (int)threadIdx.x;  // the output stage's column
+  const bool o_ok = (int)threadIdx.x < C && oc < m;
+  float v_o = 1.f, g_o = 0.f;
+  if (o_ok) {
+    if (a.v) v_o = io<T>::ld(a.v + (size_t)bb * m + oc);
+    g_o = io<T>::ld(gin + oc);
   }
-  __syncthreads();
+  griddep_wait();  // the weights, feature maps and partial sums of this step
+  // ---- after: this sequence's denominators (loaded now, used at the end)
+  float wsum = 0.f, older = 0.f;
+  if ((int)threadIdx.x < a.H) {
+    const int bh = bb * a.H + (int)threadIdx.x;
+    for (int p = 0; p < parts; ++p) wsum += a.st.wpart[(size_t)bh * kMaxParts + p];
+    older = a.st.older[bh];
+  }
   float acc[kGroup];
 #pragma unroll
   for (int e = 0; e < kGroup; ++e) acc[e] = 0.f;
-  if (c0 < m) {
+  if (col_ok) {
     // the head of the group's first column; with VEC the whole group shares it, and
     // otherwise each column takes its own head below
     const int head0 = c0 / a.m_h;
     const int lim = m;
-    // window: ring slots sl, sl + 16, ...; the current token's slot from the input.  With
-    // bf16 vectors and one or two sequences, eight slots' loads are issued before their
-    // products, so that one thread keeps eight loads in flight (a single sequence has
-    // few threads to hide HBM latency with)
-    float x[kGroup];
+    // the ring: slots sl, sl + kSl, ... with the score kernel's weights (0 for a slot whose
+    // source is already in S); the current token's slot from the input
     int s_begin = sl;
-    if constexpr (VEC && sizeof(T) == 2) if (parts > 1) {
-      const float* wrow = a.st.w + (size_t)(bb * a.H + head0) * W;
-      for (; s_begin + 7 * kSl < W; s_begin += 8 * kSl) {
-        uint4 r[8];
-        float wv[8];
+    if constexpr (kPre) {
+      const float* wrow = a.st.w + (size_t)(bb * a.H + head0) * R;
+      for (int batch = 0;; ++batch) {
+        float wv[kB];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kB; ++u) {
           const int s = s_begin + u * kSl;
-          r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
-          wv[u] = wrow[s];
+          wv[u] = s < R ? wrow[s] : 0.f;
+          if (batch > 0) {
+            r[u] = make_uint4(0, 0, 0, 0);
+            if (s < R) r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kB; ++u) {
           const uint32_t gw[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -297,29 +360,40 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
             acc[2 * e + 1] = fmaf(wv[u], __uint_as_float(gw[e] & 0xFFFF0000u), acc[2 * e + 1]);
           }
         }
+        s_begin += kB * kSl;
+        if (s_begin >= R) break;
       }
     }
+    float x[kGroup];
 #pragma unroll 2
-    for (int s = s_begin; s < W; s += kSl) {
+    for (int s = s_begin; s < R; s += kSl) {
       Cols8<T, VEC>::ld(s == cur ? gin : ring_g + (size_t)s * m, c0, lim, x);
       if (VEC) {
-        const float w = a.st.w[(size_t)(bb * a.H + head0) * W + s];
+        const float w = a.st.w[(size_t)(bb * a.H + head0) * R + s];
 #pragma unroll
         for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(w, x[e], acc[e]);
       } else {
 #pragma unroll
         for (int e = 0; e < kGroup; ++e) {
           const int hd = min(c0 + e, m - 1) / a.m_h;
-          acc[e] = fmaf(a.st.w[(size_t)(bb * a.H + hd) * W + s], x[e], acc[e]);
+          acc[e] = fmaf(a.st.w[(size_t)(bb * a.H + hd) * R + s], x[e], acc[e]);
         }
       }
     }
-    // older prefix: rows sl, sl + 16, ... of S, read out and then updated by the source
-    // that leaves the window
-    float gl[kGroup];
-    if (lslot >= 0) Cols8<T, VEC>::ld(lslot == cur ? gin : ring_g + (size_t)lslot * m, c0, lim, gl);
+    // older prefix: rows sl, sl + kSl, ... of S read out, and on a fold step updated by the
+    // group of kDecodeFold sources that completes now
 #pragma unroll 1
     for (int d = sl; d < d_h; d += kSl) {
+      // a fold step's group of g rows (8 columns each), read again for every state row
+      // (from L2): holding them across the loop would cost the other steps' occupancy
+      FoldRows<T, VEC, FOLD ? kDecodeFold : 1> gf;
+      if constexpr (FOLD) {
+#pragma unroll
+        for (int u = 0; u < kDecodeFold; ++u) {
+          const long long j = j0 + u;
+          gf.ld(u, j == i ? gin : ring_g + (size_t)(j % R) * m, c0, lim);
+        }
+      }
       if (VEC) {
         const size_t bh = (size_t)bb * a.H + head0;
         float* Srow = a.st.S + (bh * d_h + d) * a.m_h;
@@ -329,10 +403,14 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
         const float fq = a.st.fq[bh * d_h + d];
 #pragma unroll
         for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(fq, sv[e], acc[e]);
-        if (lslot >= 0) {
-          const float fk = a.st.fk_leave[bh * d_h + d];
+        if constexpr (FOLD) {
+          const float* fkf = a.st.fk_fold + bh * kDecodeFold * d_h + d;
 #pragma unroll
-          for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, gl[e], sv[e]);
+          for (int u = 0; u < kDecodeFold; ++u) {
+            const float fk = fkf[u * d_h];
+#pragma unroll
+            for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, gf.get(u, e), sv[e]);
+          }
           st_f32x8<true>(Srow, cl, a.m_h, sv);
         }
       } else {
@@ -343,50 +421,49 @@ __global__ void __launch_bounds__(256) wango_decode_gate_kernel(const DecodeArgs
           const int hd = c / a.m_h;
           const size_t bh = (size_t)bb * a.H + hd;
           float* sp = a.st.S + (bh * d_h + d) * a.m_h + (c - hd * a.m_h);
-          const float sv = *sp;
+          float sv = *sp;
           acc[e] = fmaf(a.st.fq[bh * d_h + d], sv, acc[e]);
-          if (lslot >= 0) *sp = fmaf(a.st.fk_leave[bh * d_h + d], gl[e], sv);
+          if constexpr (FOLD) {
+#pragma unroll
+            for (int u = 0; u < kDecodeFold; ++u)
+              sv = fmaf(a.st.fk_fold[(bh * kDecodeFold + u) * d_h + d], gf.get(u, e), sv);
+            *sp = sv;
+          }
         }
       }
     }
+  }
+  if ((int)threadIdx.x < a.H) {
+    const int hd = (int)threadIdx.x;
+    const float tau = head_tau(a.tau, a.s, hd, a.err, kKernWango);
+    const float null_w = a.null_bias ? expf(a.null_bias[hd] - tau) : 0.f;
+    inv_den[hd] = 1.f / (wsum + older + (float)(i + 1) * null_w);
   }
 #pragma unroll
   for (int e = 0; e < kGroup; ++e) red[sl][grp * kGroup + e] = acc[e];
   __syncthreads();
   // one column per thread: the slices' sums, the denominator, u = gbar * v, and the
   // current token's g into its ring slot
-  if (threadIdx.x < C) {
-    const int c = col0 + threadIdx.x;
-    if (c < m) {
-      float num = 0.f;
+  if (o_ok) {
+    float num = 0.f;
 #pragma unroll
-      for (int r = 0; r < kSl; ++r) num += red[r][threadIdx.x];
-      const int hd = c / a.m_h;
-      const float gbar = num * inv_den[hd];
-      const float u = a.v ? gbar * io<T>::ld(a.v + (size_t)bb * m + c) : gbar;
-      io<T>::st(a.out + (size_t)bb * m + c, u);
-      io<T>::st(const_cast<T*>(ring_g) + (size_t)cur * m + c, io<T>::ld(gin + c));
-    }
+    for (int q = 0; q < kSl; ++q) num += red[q][threadIdx.x];
+    const float gbar = num * inv_den[oc / a.m_h];
+    io<T>::st(a.out + (size_t)bb * m + oc, a.v ? gbar * v_o : gbar);
+    T gs;
+    io<T>::st(&gs, g_o);
+    const_cast<T*>(ring_g)[(size_t)cur * m + oc] = gs;
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <typename T>
-cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
-  // one or two sequences: the ring split over up to 8 CTAs per head (a short dependent
-  // chain per CTA) and the gate kernel launched early
-  const bool few = a.B <= 2;
-  const int parts = few ? min(kMaxParts, (a.W + 31) / 32) : 1;
-  wango_decode_scores_kernel<T><<<dim3(a.H, a.B, parts), 256, 0, s>>>(a);
-  // 8-column vectors when every row of g, the ring and S starts 16-byte aligned and no
-  // 8-column group straddles a head
-  const bool vec = (a.m * sizeof(T)) % 16 == 0 && a.m_h % kGroup == 0 && aligned16(a.g) &&
-                   aligned16(a.st.ring_g) && aligned16(a.st.S);
+template <typename T, bool FOLD>
+cudaError_t launch_gate(const DecodeArgs<T>& a, int parts, bool few, bool vec, cudaStream_t s) {
   if (!few) {  // enough CTAs to hide latency: 128-column blocks and a plain launch
     const dim3 grid((a.m + kGateCols - 1) / kGateCols, a.B);
-    if (vec) wango_decode_gate_kernel<T, true, kGateCols><<<grid, 256, 0, s>>>(a, parts);
-    else wango_decode_gate_kernel<T, false, kGateCols><<<grid, 256, 0, s>>>(a, parts);
+    if (vec) wango_decode_gate_kernel<T, true, kGateCols, FOLD, false><<<grid, 256, 0, s>>>(a, parts);
+    else wango_decode_gate_kernel<T, false, kGateCols, FOLD, false><<<grid, 256, 0, s>>>(a, parts);
     return cudaGetLastError();
   }
   // one or two sequences: launched as a programmatic dependent of the score kernel; for
@@ -402,10 +479,25 @@ cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cols == 64)
-    return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, 64>, a, parts)
-               : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, 64>, a, parts);
-  return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, kGateCols>, a, parts)
-             : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, kGateCols>, a, parts);
+    return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, 64, FOLD, true>, a, parts)
+               : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, 64, FOLD, true>, a, parts);
+  return vec ? cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, true, kGateCols, FOLD, true>, a, parts)
+             : cudaLaunchKernelEx(&cfg, wango_decode_gate_kernel<T, false, kGateCols, FOLD, true>, a, parts);
+}
+
+template <typename T>
+cudaError_t launch(const DecodeArgs<T>& a, cudaStream_t s) {
+  // one or two sequences: the ring split over up to 8 CTAs per head (a short dependent
+  // chain per CTA) and the gate kernel launched early
+  const bool few = a.B <= 2;
+  const int parts = few ? min(kMaxParts, (a.R + 31) / 32) : min(kMaxParts, (a.R + 127) / 128);
+  wango_decode_scores_kernel<T><<<dim3(a.H, a.B, parts), 256, 0, s>>>(a);
+  // 8-column vectors when every row of g, the ring and S starts 16-byte aligned and no
+  // 8-column group straddles a head
+  const bool vec = (a.m * sizeof(T)) % 16 == 0 && a.m_h % kGroup == 0 && aligned16(a.g) &&
+                   aligned16(a.st.ring_g) && aligned16(a.st.S);
+  return fold_step(a.pos, a.W) ? launch_gate<T, true>(a, parts, few, vec, s)
+                               : launch_gate<T, false>(a, parts, few, vec, s);
 }
 
 }  // namespace
@@ -415,13 +507,13 @@ cudaError_t launch_wango_decode(tg_dtype dt, int B, int H, int dqk, int m, int W
                                 const void* q, const void* k, const void* g, const void* v, void* out,
                                 const DecodeState& st, unsigned* err, cudaStream_t stream) {
   if (dt == TG_F32) {
-    DecodeArgs<float> a{B, H, dqk, m, dqk / H, m / H, W, pos, s, tau, null_bias, phi_mode, qk_normalized,
-                        static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(g),
+    DecodeArgs<float> a{B, H, dqk, m, dqk / H, m / H, W, W + kDecodeFold, pos, s, tau, null_bias, phi_mode,
+                        qk_normalized, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(g),
                         static_cast<const float*>(v), static_cast<float*>(out), st, err};
     return launch(a, stream);
   }
-  DecodeArgs<__nv_bfloat16> a{B, H, dqk, m, dqk / H, m / H, W, pos, s, tau, null_bias, phi_mode, qk_normalized,
-                              static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+  DecodeArgs<__nv_bfloat16> a{B, H, dqk, m, dqk / H, m / H, W, W + kDecodeFold, pos, s, tau, null_bias, phi_mode,
+                              qk_normalized, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                               static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(v),
                               static_cast<__nv_bfloat16*>(out), st, err};
   return launch(a, stream);

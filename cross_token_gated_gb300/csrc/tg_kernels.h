@@ -49,14 +49,17 @@ enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
 // [B, H, W, d_h] and g [B, W, m] (both in the storage type), and per-step scratch: the window
 // weights by ring slot [B, H, W], e^-tau phi(q~) and phi(k~_leave) [B, H, d_h], the
 // window weights' partial sums [B, H, 8] and the older-prefix term [B, H].
+// Sources that leave the window are folded into S and z in groups of this many; until
+// then they stay in the ring (of W + kDecodeFold slots) with their feature-map weight.
+constexpr int kDecodeFold = 8;
 struct DecodeState {
   float* S;
   float* z;
-  void* ring_k;
-  void* ring_g;
-  float* w;
+  void* ring_k;   // [B * H, W + kDecodeFold, d_h]
+  void* ring_g;   // [B, W + kDecodeFold, m]
+  float* w;       // [B * H, W + kDecodeFold]
   float* fq;
-  float* fk_leave;
+  float* fk_fold; // [B * H, kDecodeFold, d_h]: phi(k~_j) of pending source j in slot j mod kDecodeFold
   float* wpart;
   float* older;
 };

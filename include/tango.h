@@ -251,11 +251,15 @@ tg_status wango_aggregate_backward(const tg_agg_params *p, const void *q, const 
  *   out       device [B, m], written
  *   state     device buffer of tg_workspace_size(TG_WS_DECODE, p) bytes, 256-byte aligned,
  *             owned by the caller and kept between steps: S and z in f32, a ring of the
- *             last W tokens' unit k and g (storage type), and per-step scratch.  The call with pos == 0
- *             clears it; steps must then come in order pos = 0, 1, 2, ...
- * Requirements: d_h <= 128.  Arithmetic is fp32 for either storage type; the weights
- * are not rounded to bf16.  The step reads the ring (W g vectors) and S, and rewrites
- * S: it is bound by HBM bandwidth.
+ *             last W + 8 tokens' unit k and g (storage type), and per-step scratch.  The
+ *             call with pos == 0 clears it; steps must then come in order pos = 0, 1, 2, ...
+ * Sources enter S and z in groups of 8: one that has left the window waits in the ring,
+ * weighted by e^-tau phi(q~_i) . phi(k~_j) directly, until the step that completes its
+ * group adds the group to S and z (the same sums, formed later).
+ * Requirements: d_h <= 128, W <= 2^30.  Arithmetic is fp32 for either storage type; the
+ * weights are not rounded to bf16.  The step reads the ring (W + 8 g vectors) and S, and
+ * rewrites S on one step in 8: it is bound by HBM bandwidth and, for one sequence, by
+ * latency.
  */
 tg_status wango_decode_step(const tg_agg_params *p, long long pos, const void *q, const void *k,
                             const void *g, const void *v, void *out, void *state,

@@ -194,17 +194,20 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
 
 def test_decode_state_size_and_validation(lib):
     """The decode state: S [B, d_h, m] and z (two buffers, by step parity) in f32, the
-    ring of W unit keys and gates (storage type), and per-step scratch (window weights,
-    feature maps, 8 partial window sums and the older-prefix term per head), each region
-    256-byte aligned."""
+    ring of R = W + 8 unit keys and gates (storage type: the window plus the sources that
+    left it and wait to be folded into S in a group of 8), and per-step scratch (ring
+    weights, q's feature map, the group's key feature maps, 8 partial sums and the
+    older-prefix term per head), each region 256-byte aligned."""
     raw = tg.load()
     B, H, dqk, m, W = 2, 2, 128, 512, 16
+    R = W + 8
     p = tg.agg_params(B, 1, H, dqk, m, dtype=tg.TG_BF16, window=W)
     def a256(x):
         return (x + 255) // 256 * 256
     d_h = dqk // H
-    want = (a256(B * d_h * m * 4) + a256(2 * B * H * d_h * 4) + a256(B * H * W * d_h * 2) + a256(B * W * m * 2)
-            + a256(B * H * W * 4) + 2 * a256(B * H * d_h * 4) + a256(B * H * 8 * 4) + a256(B * H * 4))
+    want = (a256(B * d_h * m * 4) + a256(2 * B * H * d_h * 4) + a256(B * H * R * d_h * 2) + a256(B * R * m * 2)
+            + a256(B * H * R * 4) + a256(B * H * d_h * 4) + a256(B * H * 8 * d_h * 4) + a256(B * H * 8 * 4)
+            + a256(B * H * 4))
     assert tg.tg_workspace_size(tg.TG_WS_DECODE, p) == want
     for bad in (dict(window=0), dict(phi_mode=3), dict(flags=tg.TG_FLAG_DEBUG_TIMEOUT)):
         q = tg.agg_params(B, 1, H, dqk, m, dtype=tg.TG_BF16, **dict(dict(window=W), **bad))

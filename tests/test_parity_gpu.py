@@ -543,16 +543,18 @@ def run_decode(q, k, g, v, H, W, **kw):
     ("bf16", (2, 90, 2, 64, 3560, 40)),
     ("bf16", (1, 50, 2, 32, 206, 12)),
     ("f32", (1, 60, 2, 32, 150, 9)),
-    # the one-kernel step (bf16, B <= 2, W <= 512, m_h >= 64 and a multiple of 8) with
-    # 64-column blocks that straddle two heads, and a window too wide for it (the
-    # two-kernel step)
+    # one sequence: 64-column blocks that straddle two heads, and a window wider than the
+    # 9-slot register batch of the ring (W + 8 = 608 slots: several batches)
     ("bf16", (1, 120, 2, 64, 272, 24)),
     ("bf16", (1, 700, 2, 64, 512, 600)),
-    ("bf16", (4, 60, 2, 64, 512, 16)),     # four sequences: the two-kernel step
+    ("bf16", (4, 60, 2, 64, 512, 16)),     # four sequences: the plain launch
+    ("bf16", (3, 50, 2, 64, 256, 41)),     # the last group of 8 still waiting at the end
 ])
 def test_decode_steps_match_the_whole_sequence(dtype, case):
     """T decode steps reproduce every row of WANGO over the whole sequence (the oracle's
-    running-sum evaluation of eq. 10)."""
+    running-sum evaluation of eq. 10).  Sources that left the window enter S in groups of
+    8, so every case with T > W + 8 crosses several group boundaries, and W = 1 folds
+    the current token's own group."""
     B, T, H, dqk, m, W = case
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=21, dtype=dtype)
     out = run_decode(q, k, g, v, H, W)
