@@ -480,11 +480,13 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     - the shared-block model forward at B=16 T=1024 (4 TANGO applications, 32,768-entry
       tied embedding): one set of m=28,480 and three sets of m=9,494, with per-kernel
       device times;
-    - WANGO decode steps (W=256) at B=1 and B=8, timed as one CUDA-graph replay of 64
+    - WANGO decode steps (W=256) at B=1, 8 and 32, timed as one CUDA-graph replay of 64
       consecutive steps;
     - the backward of both aggregations at B=8 T=2048, with per-kernel device times,
       and with the gbar and denominators a saving forward keeps (a training step's
-      aggregation: the saving forward plus that backward)."""
+      aggregation: the saving forward plus that backward);
+    - the WANGO backward at B=1 T=8192 with the saved forward, on the library's path
+      (the running-sum scans for the far older pairs) and on the pair-by-pair path."""
     import torch
     from cross_token_gated_gb300 import synth  # noqa: F401  (the recipe the weights follow)
     res = {}
@@ -564,6 +566,36 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     del q, k, g, v, dout, dq, dk, dg, dv, u, gbar, den
     torch.cuda.empty_cache()
 
+    # ---- the WANGO backward at long context (B=1, T=8192, W=256): the older pairs beyond
+    # the window's band go through the running-sum scans there (the library's choice),
+    # timed beside the pair-by-pair path
+    b1, t1 = 1, 8192
+    q, k = unit(b1, t1), unit(b1, t1)
+    g, v, dout = (torch.randn(b1, t1, M, device=dev, generator=gen).bfloat16() for _ in range(3))
+    dq, dk, dg, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(g), torch.empty_like(g)
+    u, gbar = torch.empty_like(g), torch.empty_like(g)
+    den = torch.empty(b1, H, t1, dtype=torch.float32, device=dev)
+    ms_save = event_ms(lambda: tg.wango_aggregate_save(q, k, g, v, u, gbar, den, H=H, window=256, flags=nf,
+                                                       stream=stream), dev, stream, reps=5)
+    rec = {"forward_save_ms": ms_save, "algorithmic_tflop": acc.wango_bwd_flops(b1, t1, DQK, M, H, 256) / 1e12}
+    sizes = {}
+    for name, ff in (("library", 0), ("scans", tg.TG_FLAG_BWD_FAR_SCAN), ("pairs", tg.TG_FLAG_BWD_FAR_PAIRS)):
+        p = tg.agg_params(b1, t1, H, DQK, M, dtype=tg.TG_BF16, window=256, flags=nf | ff)
+        sizes[name] = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, p)
+        wsb = torch.empty(sizes[name] + 256, dtype=torch.uint8, device=dev)
+        f_saved = lambda: tg.wango_aggregate_backward(q, k, g, v, dout, dq, dk, dg, dv, H=H, window=256,
+                                                      flags=nf | ff, ws=wsb, stream=stream, gbar=gbar, den=den)
+        rec[f"ms_with_saved_forward_{name}"] = event_ms(f_saved, dev, stream, reps=5)
+        if name == "library":
+            rec["kernels"] = kernel_breakdown(f_saved, dev)
+        del wsb
+        torch.cuda.empty_cache()
+    rec["library_path"] = "scans" if sizes["library"] == sizes["scans"] else "pairs"
+    rec["training_step_ms"] = ms_save + rec["ms_with_saved_forward_library"]
+    res[f"wango_backward_B{b1}_T{t1}"] = rec
+    del q, k, g, v, dout, dq, dk, dg, dv, u, gbar, den
+    torch.cuda.empty_cache()
+
     # ---- the WANGO block step (B=8, T=2048, W=256)
     def block_weights(d, m, n_sets=1):
         n = lambda r, c: (torch.randn(r, c, device=dev, generator=gen) * c ** -0.5).bfloat16()
@@ -610,7 +642,7 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
     del E, ids, logits
 
     # ---- WANGO decode steps (W=256), steady state, one graph replay of 64 steps
-    for b in (1, 8):
+    for b in (1, 8, 32):
         Wd, n = 256, 64
         q, k = unit(b, 1)[:, 0].contiguous(), unit(b, 1)[:, 0].contiguous()
         g = torch.randn(b, M, device=dev, generator=gen).bfloat16()
@@ -627,6 +659,8 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
             for pos in range(Wd + 8, Wd + 8 + n):
                 tg.wango_decode_step(q, k, g, v, o, st, pos, H=H, window=Wd, flags=tg.TG_FLAG_QK_NORMALIZED,
                                      stream=cap)
+        graph.replay()  # a first replay warms the graph (its upload and the caches)
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         graph.replay()
@@ -636,7 +670,7 @@ def other_configs(tg, acc, dev, stream, peak_tf, peak_gbs):
         by = acc.decode_bytes(b, DQK, M, H, Wd)
         res[f"decode_B{b}_W{Wd}"] = {"us_per_step": us, "tokens_per_s": b / (us * 1e-6),
                                      "gbs": by / (us * 1e-6) / 1e9, "frac_hbm_peak": by / (us * 1e-6) / 1e9 / peak_gbs,
-                                     "timing": f"one CUDA-graph replay of {n} consecutive steps"}
+                                     "timing": f"one CUDA-graph replay of {n} consecutive steps, after a warm-up replay"}
         del graph, q, k, g, v, o, st
         torch.cuda.empty_cache()
 
