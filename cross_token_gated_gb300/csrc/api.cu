@@ -293,7 +293,7 @@ tg_status validate_bwd(const tg_agg_params* p, bool wango) {
 }
 
 struct BwdWs {
-  size_t qn, kn, gbar, den, dp, E, X, Xo, aux, erev, qrev, krev, part, rb, total;
+  size_t qn, kn, gbar, den, dp, E, X, Xo, aux, part, rb, total;
   int T_pad;
   bool scan;  // WANGO: far older pairs through the running sums
 };
@@ -306,23 +306,14 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
   L.qn = 0;
   L.kn = L.qn + (norm ? align256(B * T * dqk * 2) : 0);
   L.gbar = L.kn + (norm ? align256(B * T * dqk * 2) : 0);
-  // gbar is dead once E is formed; WANGO's reversed gate gradient reuses its space
-  L.den = L.gbar + align256(B * (wango ? Tp : T) * m * 2);
+  L.den = L.gbar + align256(B * T * m * 2);
   L.dp = L.den + (wango ? 0 : align256(B * H * Tp * 4));
   L.E = L.dp + align256(B * H * Tp * 4);
   L.X = L.E + align256(B * T * m * 2);
   L.Xo = L.X + align256(B * H * Tp * Tp * 2);
   L.aux = L.Xo + (wango ? align256(B * H * Tp * Tp * 2) : 0);
-  size_t aux = 0;
-  if (wango) {
-    aux = wango_aux_bytes(p->B, p->T, p->H, p->d_qk, p->m, p->window);
-    const size_t aux_rev = wango_aux_bytes(p->B, L.T_pad, p->H, p->d_qk, p->m, p->window);
-    if (aux_rev > aux) aux = aux_rev;
-  }
-  L.erev = L.aux + align256(aux);
-  L.qrev = L.erev + (wango ? align256(B * Tp * m * 2) : 0);
-  L.krev = L.qrev + (wango ? align256(B * Tp * dqk * 2) : 0);
-  L.part = L.krev + (wango ? align256(B * Tp * dqk * 2) : 0);
+  const size_t aux = wango ? wango_aux_bytes(p->B, p->T, p->H, p->d_qk, p->m, p->window) : 0;
+  L.part = L.aux + align256(aux);
   // WANGO with blocks wholly beyond the window's band: the scans' per-strip sums (two
   // directions) and the block sums for rho
   const int band = bwd_band(p->window), nblk = L.T_pad / 128;
@@ -404,8 +395,8 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
     den = a.den_out;
   }
   if (e != cudaSuccess) return TG_ERR_CUDA;
-  e = launch_bwd_prep(dout, v, gb, den, den_pitch, E, dv, dp, wango ? base + L.erev : nullptr, p->B, p->T, L.T_pad,
-                      p->H, mem_width(p), p->m / p->H, stream);
+  e = launch_bwd_prep(dout, v, gb, den, den_pitch, E, dv, dp, p->B, p->T, L.T_pad, p->H, mem_width(p), p->m / p->H,
+                      stream);
   if (e != cudaSuccess) return TG_ERR_CUDA;
 
   // pair-weight gradients, then dq and dk
@@ -463,17 +454,14 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   r.no_norm = 1;
   r.den_out = nullptr;
   if (wango) {
-    void* grev = gbar;  // gbar has been read by the prep kernel
-    e = launch_reverse_rows(qh, base + L.qrev, p->B, p->T, L.T_pad, p->d_qk, true, stream);
-    if (e == cudaSuccess) e = launch_reverse_rows(kh, base + L.krev, p->B, p->T, L.T_pad, p->d_qk, true, stream);
-    if (e != cudaSuccess) return TG_ERR_CUDA;
-    r.T = L.T_pad;
-    r.q = base + L.krev;
-    r.k = base + L.qrev;
-    r.g = base + L.erev;
-    r.out = grev;
+    // the windowed kernels on the time-reversed sequence, read and written in place
+    // (mirrored: blocks in reverse order, rows reversed within each)
+    r.mirror = 1;
+    r.q = kh;
+    r.k = qh;
+    r.g = E;
+    r.out = dg;
     e = launch_wango_tc(r, stream);
-    if (e == cudaSuccess) e = launch_reverse_rows(grev, dg, p->B, p->T, L.T_pad, mem_width(p), false, stream);
   } else {
     r.rev = 1;
     r.q = kh;

@@ -1,8 +1,6 @@
 // CUDA-core kernels of the aggregation backward, "TANGO: Token-Aggregated Nonlinear
 // Gating Operators ...", sec. 2.1 eq. 5 with the weights of sec. 2.2 eqs. 6-9:
 //   bwd_prep_kernel   E = dU * v / den, dv = dU * gbar, D = E . gbar per (row, head)
-//   reverse_rows_kernel  a sequence's rows in reverse order (the WANGO gate gradient is
-//                     the forward numerator of the time-reversed problem)
 // All arithmetic is f32; tensors are bf16.
 #include "tg_common.cuh"
 #include "tg_kernels.h"
@@ -27,10 +25,9 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
   return s;
 }
 
-// One CTA per row (b, t) of `rows` per sequence (T, or T_pad with a reversed copy, whose
-// rows t >= T only clear their slot of it).  Rows are m wide in memory, H heads at a
-// pitch of m / H of which the first m_h columns are gates.  den and dp have a row pitch
-// of T_pad (dp) and den_pitch (den).
+// One CTA per row (b, t).  Rows are m wide in memory, H heads at a pitch of m / H of
+// which the first m_h columns are gates.  den and dp have a row pitch of T_pad (dp) and
+// den_pitch (den).
 __device__ __forceinline__ void prep8(const uint4 du, const uint4 gb, const uint4 vv, float inv, uint4& eo, uint4& dvo,
                                       float& acc) {
   const uint32_t dus[4] = {du.x, du.y, du.z, du.w}, gbs[4] = {gb.x, gb.y, gb.z, gb.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
@@ -51,15 +48,10 @@ __device__ __forceinline__ void prep8(const uint4 du, const uint4 gb, const uint
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
     const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ gbar,
     const float* __restrict__ den, __nv_bfloat16* __restrict__ E, __nv_bfloat16* __restrict__ dv, float* __restrict__ dp,
-    __nv_bfloat16* __restrict__ e_rev, int T, int T_pad, int rows, int H, int m, int m_h, int den_pitch) {
+    int T, int T_pad, int H, int m, int m_h, int den_pitch) {
   __shared__ float red[kPrepThreads / 32];
-  const int b = blockIdx.x / rows, t = blockIdx.x % rows;
-  const int nvec = m / 8, m_hp = m / H;
-  __nv_bfloat16* rev_row = e_rev ? e_rev + ((size_t)b * T_pad + (T_pad - 1 - t)) * m : nullptr;
-  if (t >= T) {
-    for (int c = threadIdx.x; c < nvec; c += blockDim.x) reinterpret_cast<uint4*>(rev_row)[c] = make_uint4(0, 0, 0, 0);
-    return;
-  }
+  const int b = blockIdx.x / T, t = blockIdx.x % T;
+  const int m_hp = m / H;
   const size_t off = ((size_t)b * T + t) * m;
   const bool vec = m_h % 8 == 0;
   for (int a = 0; a < H; ++a) {
@@ -75,7 +67,6 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
         prep8(*reinterpret_cast<const uint4*>(dout + o), *reinterpret_cast<const uint4*>(gbar + o), vv, inv, eo, dvo,
               acc);
         *reinterpret_cast<uint4*>(E + o) = eo;
-        if (rev_row) *reinterpret_cast<uint4*>(rev_row + (o - off)) = eo;
         if (dv) *reinterpret_cast<uint4*>(dv + o) = dvo;
       }
     } else {  // a head width that is not a multiple of 8: one column at a time
@@ -85,7 +76,6 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
         const __nv_bfloat16 e = __float2bfloat16_rn(d * (v ? __bfloat162float(v[o]) : 1.f) * inv);
         acc = fmaf(__bfloat162float(e), gb, acc);
         E[o] = e;
-        if (rev_row) rev_row[o - off] = e;
         if (dv) dv[o] = __float2bfloat16_rn(d * gb);
       }
     }
@@ -94,43 +84,17 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(
   }
 }
 
-// One CTA per destination row; 16-byte vectors (width % 8 == 0).
-__global__ void reverse_rows_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, int T,
-                                    int T_pad, int width, int to_padded) {
-  const int rows_dst = to_padded ? T_pad : T;
-  const int b = blockIdx.x / rows_dst, t = blockIdx.x % rows_dst;
-  const int nvec = width / 8;
-  uint4* d = reinterpret_cast<uint4*>(dst + ((size_t)b * rows_dst + t) * width);
-  int ts;  // source row, or -1 for a zero row
-  if (to_padded) ts = (t >= T_pad - T) ? T_pad - 1 - t : -1;
-  else ts = T_pad - 1 - t;
-  const int rows_src = to_padded ? T : T_pad;
-  const uint4* s = ts >= 0 ? reinterpret_cast<const uint4*>(src + ((size_t)b * rows_src + ts) * width) : nullptr;
-  for (int c = threadIdx.x; c < nvec; c += blockDim.x) d[c] = s ? s[c] : make_uint4(0, 0, 0, 0);
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, int den_pitch,
-                            void* E, void* dv, float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h,
+                            void* E, void* dv, float* dp, int B, int T, int T_pad, int H, int m, int m_h,
                             cudaStream_t s) {
-  const int rows = e_rev ? T_pad : T;
-  const long long n = (long long)B * rows;
+  const long long n = (long long)B * T;
   if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
   bwd_prep_kernel<<<(unsigned)n, kPrepThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(v),
       static_cast<const __nv_bfloat16*>(gbar), den, static_cast<__nv_bfloat16*>(E), static_cast<__nv_bfloat16*>(dv),
-      dp, static_cast<__nv_bfloat16*>(e_rev), T, T_pad, rows, H, m, m_h, den_pitch);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,
-                                cudaStream_t s) {
-  const long long rows = (long long)B * (to_padded ? T_pad : T);
-  if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
-  reverse_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src),
-                                                     static_cast<__nv_bfloat16*>(dst), T, T_pad, width,
-                                                     to_padded ? 1 : 0);
+      dp, T, T_pad, H, m, m_h, den_pitch);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,8 @@ struct AggArgs {
   int m_h = 0;
   // Backward helpers (tensor-core kernels):
   int rev = 0;              // TANGO: sources j >= i instead of j <= i
+  int mirror = 0;           // WANGO: the time-reversed problem on the tensors as they lie
+                            // (see launch_wango_tc); needs no_norm, v and null_bias NULL
   int no_norm = 0;          // TANGO and WANGO: the numerator alone, no division by the denominator
   float* den_out = nullptr; // TANGO: every row's denominator, [B * H, den_pitch]
   int den_pitch = 0;        // 0: ceil(T / 128) * 128
@@ -45,10 +47,11 @@ enum Epi : int { kEpiStore = 0, kEpiSilu = 1, kEpiResidual = 2 };
 
 // WANGO decode state (one buffer, regions 256-byte aligned): the running sums S
 // [B, H, d_h, m_h] and z [2, B, H, d_h] in f32 (z alternates between its two buffers by
-// step parity: a step reads buffer pos % 2 and writes the other), the ring of the last W tokens' unit k
-// [B, H, W, d_h] and g [B, W, m] (both in the storage type), and per-step scratch: the window
-// weights by ring slot [B, H, W], e^-tau phi(q~) and phi(k~_leave) [B, H, d_h], the
-// window weights' partial sums [B, H, 8] and the older-prefix term [B, H].
+// step parity: a step reads buffer pos % 2 and writes the other), the ring of the last
+// W + kDecodeFold tokens' unit k [B, H, R, d_h] and g [B, R, m] (both in the storage
+// type), and per-step scratch: the ring weights [B, H, R], e^-tau phi(q~) [B, H, d_h],
+// the feature maps of the sources waiting to be folded [B, H, kDecodeFold, d_h], the
+// weights' partial sums [B, H, 8] and the older-prefix term [B, H].
 // Sources that leave the window are folded into S and z in groups of this many; until
 // then they stay in the ring (of W + kDecodeFold slots) with their feature-map weight.
 constexpr int kDecodeFold = 8;
@@ -90,16 +93,10 @@ cudaError_t launch_tango_simt(const AggArgs& a, cudaStream_t s);
 
 // ---- backward helpers (backward_simt.cu), bf16 storage --------------------
 // Per (row, head): E = dout * v / den (v == NULL: dout / den) in bf16, dv = dout * gbar
-// (if dv), and D = sum_c E_c gbar_c over the head's columns into dp [B * H, T_pad];
-// e_rev (if set) receives E with the rows of every sequence reversed, row t at
-// T_pad - 1 - t, and zero rows before them.
+// (if dv), and D = sum_c E_c gbar_c over the head's columns into dp [B * H, T_pad].
 cudaError_t launch_bwd_prep(const void* dout, const void* v, const void* gbar, const float* den, int den_pitch,
-                            void* E, void* dv, float* dp, void* e_rev, int B, int T, int T_pad, int H, int m, int m_h,
+                            void* E, void* dv, float* dp, int B, int T, int T_pad, int H, int m, int m_h,
                             cudaStream_t s);
-// Rows of every sequence reversed: dst[b, T_pad - 1 - t] = src[b, t] for t < T and zero
-// rows dst[b, 0 .. T_pad - T) (to_padded), or back: dst[b, t] = src[b, T_pad - 1 - t].
-cudaError_t launch_reverse_rows(const void* src, void* dst, int B, int T, int T_pad, int width, bool to_padded,
-                                cudaStream_t s);
 
 cudaError_t launch_wango_simt(const AggArgs& a, cudaStream_t s);
 

@@ -55,6 +55,13 @@ __host__ __device__ __forceinline__ int jlo_of(int ib, int W) {
   return lo > 0 ? lo / kBlk : 0;
 }
 __device__ __forceinline__ bool is_mixed(int jb, int ib, int W) { return jb * kBlk <= ib * kBlk + kBlk - 1 - W; }
+// The memory row of block blk's first row.  Mirrored, the kernels solve the time-reversed
+// problem on the tensors as they lie: block blk of the reversed sequence is memory block
+// n_iblk - 1 - blk, whose rows come in reverse order (row r is position kBlk - 1 - r of
+// the block); rows past T read as zero and are not written.
+__host__ __device__ __forceinline__ int mem_row(int blk, int n_iblk, int mirror) {
+  return (mirror ? n_iblk - 1 - blk : blk) * kBlk;
+}
 
 struct Ring {
   int stage = 0;
@@ -93,9 +100,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 //   kMode 0: every source is in the window: exp2(c (s - 1)).
 //   kMode 2: general: 0 after i, exp2(c (s - 1)) in the window (j >= jw), else the
 //            feature-map score f (older source).
-// dsum2 accumulates the row sum of the weights as rounded to bf16 (the denominator
-// as applied), two f32 lanes per packed instruction.
-template <int kMode>
+// Source e sits at position j0 + e (kRev: j0 - e, a mirrored block).  dsum2 accumulates
+// the row sum of the weights as rounded to bf16 (the denominator as applied), two f32
+// lanes per packed instruction.
+template <int kMode, bool kRev = false>
 __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, float c, int j0, int i, int jw,
                                           uint32_t (&p)[16], uint64_t (&dsum2)[2]) {
   const uint64_t cc = f32x2_pack(c, c), nc = f32x2_pack(-c, -c);
@@ -106,10 +114,11 @@ __device__ __forceinline__ void weights32(const uint32_t* r, const uint32_t* f, 
     float w0 = ex2_approx(x0);
     float w1 = ex2_approx(x1);
     if (kMode == 2) {
-      if (j0 + e < jw) w0 = __uint_as_float(f[e]);
-      if (j0 + e + 1 < jw) w1 = __uint_as_float(f[e + 1]);
-      if (j0 + e > i) w0 = 0.f;
-      if (j0 + e + 1 > i) w1 = 0.f;
+      const int ja = kRev ? j0 - e : j0 + e, jn = kRev ? j0 - e - 1 : j0 + e + 1;
+      if (ja < jw) w0 = __uint_as_float(f[e]);
+      if (jn < jw) w1 = __uint_as_float(f[e + 1]);
+      if (ja > i) w0 = 0.f;
+      if (jn > i) w1 = 0.f;
     }
     const uint32_t pk = pack_bf16x2(w0, w1);
     dsum2[(e >> 1) & 1] = add_f32x2(dsum2[(e >> 1) & 1], bf16x2_widen(pk));
@@ -140,6 +149,7 @@ constexpr size_t kPSmemBytes = 1024 + kTile * 5 + sizeof(PBars);
 
 struct PArgs {
   int B, T, T_pad, H, dqk, d_h, W, n_iblk, ldp;
+  int mirror;                      // the time-reversed problem (mem_row)
   float s;
   const float* tau;
   const float* null_bias;
@@ -209,25 +219,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     bool ok = true;
+    const int irow = mem_row(ib, a.n_iblk, a.mirror);
     mbar_arrive_expect_tx(&b.qh_full, tile_bytes);
-    tma_load_3d(sQ, &tmQ, &b.qh_full, head * DH, ib * kBlk, bb);
+    tma_load_3d(sQ, &tmQ, &b.qh_full, head * DH, irow, bb);
     if (any_mixed) {
       mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
-      tma_load_3d(sFQ, &tmFQ, &b.fq_full, head * DH, ib * kBlk, bb);
+      tma_load_3d(sFQ, &tmFQ, &b.fq_full, head * DH, irow, bb);
     }
     Ring kr;
     uint32_t kmask = 0, kph[2] = {}, fkph = 0, fk_n = 0;
     for (int jb = ib; ok && jb >= jlo; --jb) {
       if (!(ok = wait_bar(&b.k_empty[kr.stage], kr.phase ^ 1, b, a))) break;
       mbar_arrive_expect_tx(&b.k_full[kr.stage], tile_bytes);
-      tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], head * DH, jb * kBlk, bb);
+      tma_load_3d(sK + kr.stage * kTile, &tmK, &b.k_full[kr.stage], head * DH, mem_row(jb, a.n_iblk, a.mirror), bb);
       kmask |= 1u << kr.stage;
       kph[kr.stage] = kr.phase;
       kr.next(2);
       if (is_mixed(jb, ib, W)) {
         if (!(ok = wait_bar(&b.fk_empty, fkph ^ 1, b, a))) break;
         mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
-        tma_load_3d(sFK, &tmFK, &b.fk_full, head * DH, jb * kBlk, bb);
+        tma_load_3d(sFK, &tmFK, &b.fk_full, head * DH, mem_row(jb, a.n_iblk, a.mirror), bb);
         fkph ^= 1;
         ++fk_n;
       }
@@ -293,11 +304,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int i = ib * kBlk + row;
-    const int i0 = ib * kBlk + quarter * 32;
+    const int pi = ib * kBlk + row;                                 // this row of P and den
+    const int i = ib * kBlk + (a.mirror ? kBlk - 1 - row : row);    // its position
+    const int mi = mem_row(ib, a.n_iblk, a.mirror) + row;           // its row in memory
+    const int i0 = ib * kBlk + (a.mirror ? kBlk - 32 - quarter * 32 : quarter * 32);  // the warp's first position
     const float tau = head_tau(a.tau, a.s, head, a.err, kKernWango);
     const float c = tau * kLog2e;
-    __nv_bfloat16* prow = a.P + ((size_t)(bb * a.H + head) * a.T_pad + i) * a.ldp;
+    __nv_bfloat16* prow = a.P + ((size_t)(bb * a.H + head) * a.T_pad + pi) * a.ldp;
     uint64_t dsum2[2] = {0, 0};
     // z = the column sums of Fk over the blocks below the window (jb < jlo), for the
     // older-prefix denominator Fq_i . z
@@ -329,7 +342,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int q = 0; q < nq; ++q) {
           const int off = h < 0 ? wg * 64 + q * 32 : h * 64 + wg * 32;  // first source in the block
           const uint32_t cs = sl + (uint32_t)(h < 0 ? off : wg * 32);     // its cos score column
-          const int js = jb * kBlk + off;
+          // the chunk's positions: j0 that of its first column, js the lowest
+          const int j0 = jb * kBlk + (a.mirror ? kBlk - 1 - off : off);
+          const int js = a.mirror ? j0 - 31 : j0;
           uint32_t p[16];
           if (js > i0 + 31) {
 #pragma unroll
@@ -344,7 +359,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_ld32(cs, r[0]);
             tmem_ld32(h < 0 ? cs : cs + 64, r[1]);
             tmem_ld_wait();
-            weights32<2>(r[0], r[1], c, js, i, h < 0 ? -0x7fffffff - 1 : i - W + 1, p, dsum2);
+            const int jw = h < 0 ? -0x7fffffff - 1 : i - W + 1;
+            if (a.mirror) weights32<2, true>(r[0], r[1], c, j0, i, jw, p, dsum2);
+            else weights32<2>(r[0], r[1], c, j0, i, jw, p, dsum2);
           }
           __nv_bfloat16* dst = prow + (ib - jb) * kBlk + off;
 #pragma unroll
@@ -364,9 +381,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) mbar_arrive(&b.rs_full);
     if (ok && wg == 0 && (ok = wait_bar(&b.rs_full, 0, b, a))) {
       float den = 1.f;  // rows past T: any finite value
-      if (i < a.T) {
+      if (mi < a.T) {
         const float null_w = a.null_bias ? exp2f((a.null_bias[head] - tau) * kLog2e) : 0.f;
-        const __nv_bfloat16* f = a.fq + ((size_t)bb * a.T + i) * a.dqk + (size_t)head * a.d_h;
+        const __nv_bfloat16* f = a.fq + ((size_t)bb * a.T + mi) * a.dqk + (size_t)head * a.d_h;
         float older = 0.f;
         for (int c = 0; c < a.d_h; c += 8) {
           const uint4 w = *reinterpret_cast<const uint4*>(f + c);
@@ -379,7 +396,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         den = b.rowsum[0][row] + b.rowsum[1][row] + older + (float)(i + 1) * null_w;
       }
-      a.den[(size_t)(bb * a.H + head) * a.T_pad + i] = den;
+      a.den[(size_t)(bb * a.H + head) * a.T_pad + pi] = den;
     }
   }
   tc_fence_before();
@@ -435,6 +452,7 @@ struct GArgs {
   uint64_t timeout_ns;
   int debug_timeout;
   int no_norm;                 // the numerator alone: no division by the denominator
+  int mirror;                  // the time-reversed problem (mem_row)
   int fuse;                    // v = x W_v^T computed here (v == NULL, reuse == 0)
   __nv_bfloat16* gbar_out;     // if set: gbar (bf16), laid out as out
   int nkc;                     // fused v: 64-column chunks of the residual width d
@@ -644,7 +662,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(dst + h * 2 * kGBox + c * kGBox, &tmG, &b.gfull[s], gx + 64 * c, jb * kBlk + 64 * h, sp.b);
+          tma_load_3d(dst + h * 2 * kGBox + c * kGBox, &tmG, &b.gfull[s], gx + 64 * c,
+                      mem_row(jb, a.n_iblk, a.mirror) + 64 * h, sp.b);
       return true;
     };
     // fused v: chunk kc of the block's x rows (128 x 64) and of the strip's W_v rows
@@ -655,7 +674,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       ++gload[s];
       uint8_t* dst = slot_ptr(s);
       mbar_arrive_expect_tx(&b.gfull[s], kGStage);
-      tma_load_3d(dst, &tmX, &b.gfull[s], kc * 64, ib * kBlk, sp.b);
+      tma_load_3d(dst, &tmX, &b.gfull[s], kc * 64, mem_row(ib, a.n_iblk, a.mirror), sp.b);
       tma_load_2d(dst + 2 * kGBox, &tmWv, &b.gfull[s], kc * 64, gx);
       return true;
     };
@@ -663,14 +682,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (!wait_bar(&b.fq_empty, (fq_n & 1) ^ 1, b, a)) return false;
       ++fq_n;
       mbar_arrive_expect_tx(&b.fq_full, tile_bytes);
-      tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, ib * kBlk, sp.b);
+      tma_load_3d(sFQ, &tmFQ, &b.fq_full, sp.head * DH, mem_row(ib, a.n_iblk, a.mirror), sp.b);
       return true;
     };
     auto load_fk = [&](int jb) -> bool {
       if (!wait_bar(&b.fk_empty, (fk_n & 1) ^ 1, b, a)) return false;
       ++fk_n;
       mbar_arrive_expect_tx(&b.fk_full, tile_bytes);
-      tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, jb * kBlk, sp.b);
+      tma_load_3d(sFK, &tmFK, &b.fk_full, sp.head * DH, mem_row(jb, a.n_iblk, a.mirror), sp.b);
       return true;
     };
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
@@ -692,7 +711,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&tmV, gx + 64 * c, (ib + 1) * kBlk + 64 * h, sp.b);
+            for (int c = 0; c < 2; ++c)
+              tma_prefetch_l2_3d(&tmV, gx + 64 * c, mem_row(ib + 1, a.n_iblk, a.mirror) + 64 * h, sp.b);
         }
         for (int jb = jlo; ok && jb <= ib; ++jb) {
           if ((!reuse || ib == it.ib0) && !(ok = load_g(jb))) break;
@@ -885,7 +905,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
           tma_load_3d(sU + h * 2 * kGBox + c * kGBox, &tmV, &b.v_full, sp.head * a.m_hp + sp.n0 + 64 * c,
-                      ib * kBlk + 64 * h, sp.b);
+                      mem_row(ib, a.n_iblk, a.mirror) + 64 * h, sp.b);
     };
     for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
       const Item it = item_of<kSeg>(a, w);
@@ -903,10 +923,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       for (int ib = it.ib0; ok && ib < it.ib1; ++ib, ++gib) {
         const int ob = gib & 1;
-        const int i = ib * kBlk + row;
-        const bool row_ok = i < a.T;
+        const int i = ib * kBlk + row;                          // this row of den
+        const int mi = mem_row(ib, a.n_iblk, a.mirror) + row;   // its row in memory
+        const bool row_ok = mi < a.T;
         const float den = a.den[(size_t)(sp.b * a.H + sp.head) * a.T_pad + i];
-        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? i : 0)) * a.m + (size_t)sp.head * a.m_hp;
+        const size_t grow = ((size_t)sp.b * a.T + (row_ok ? mi : 0)) * a.m + (size_t)sp.head * a.m_hp;
         // the state after this block's update, for the next block's read-out (this
         // block's read-out and update are complete; the next block changes it only after
         // its own read-out)
@@ -1004,7 +1025,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         named_bar_sync(2, 128);
         if (issuer) {
           for (int h = 0; h < 2; ++h) {
-            const int y = ib * kBlk + 64 * h;
+            const int y = mem_row(ib, a.n_iblk, a.mirror) + 64 * h;
             if (y >= a.T) continue;
             for (int cq = 0; cq < 2; ++cq) {
               const int c = sp.n0 + cq * 64;
@@ -1047,7 +1068,7 @@ __device__ __forceinline__ float phi_fast(float u, float inv_sqrt_dh, int mode) 
 __global__ void __launch_bounds__(kBlk) wango_phi_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                                         __nv_bfloat16* fq, __nv_bfloat16* fk, float* zb, int T,
                                                         int H, int dqk, int n_iblk, float s, const float* tau,
-                                                        int phi_mode, unsigned* err) {
+                                                        int phi_mode, unsigned* err, int mirror) {
   __shared__ float part[kBlk / 32][64];
   const int jb = blockIdx.x, a = blockIdx.y, bb = blockIdx.z;
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
@@ -1090,7 +1111,8 @@ __global__ void __launch_bounds__(kBlk) wango_phi_kernel(const __nv_bfloat16* q,
   }
   __syncthreads();
   if (t < d_h)
-    zb[(((size_t)bb * H + a) * n_iblk + jb) * d_h + t] = (part[0][t] + part[1][t]) + (part[2][t] + part[3][t]);
+    zb[(((size_t)bb * H + a) * n_iblk + (mirror ? n_iblk - 1 - jb : jb)) * d_h + t] =
+        (part[0][t] + part[1][t]) + (part[2][t] + part[3][t]);
 }
 
 int num_sms() {
@@ -1229,7 +1251,7 @@ cudaError_t launch_wango_prepass(const AggArgs& p, cudaStream_t s) {
   wango_phi_kernel<<<dim3(n_iblk, p.H, p.B), kBlk, 0, s>>>(
       static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
       reinterpret_cast<__nv_bfloat16*>(aux + L.fq), reinterpret_cast<__nv_bfloat16*>(aux + L.fk),
-      reinterpret_cast<float*>(aux + L.zb), p.T, p.H, p.dqk, n_iblk, p.s, p.tau, p.phi_mode, p.err);
+      reinterpret_cast<float*>(aux + L.zb), p.T, p.H, p.dqk, n_iblk, p.s, p.tau, p.phi_mode, p.err, 0);
   return cudaGetLastError();
 }
 
@@ -1246,11 +1268,15 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   float* zb = reinterpret_cast<float*>(aux + L.zb);
   __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(aux + L.P);
   float* den = reinterpret_cast<float*>(aux + L.den);
+  // mirrored (the time-reversed problem, for the backward's gate gradient): the numerator
+  // alone, whose positions past T (the reversed sequence's leading padding) have zero
+  // g rows and so add nothing; the denominator terms that count positions are not formed
+  if (p.mirror && (!p.no_norm || p.v || p.null_bias || p.fuse_x)) return cudaErrorInvalidValue;
 
   // pre-pass: feature maps and their per-block column sums
   wango_phi_kernel<<<dim3(n_iblk, p.H, p.B), kBlk, 0, s>>>(
       static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k), fq, fk, zb, p.T, p.H, p.dqk,
-      n_iblk, p.s, p.tau, p.phi_mode, p.err);
+      n_iblk, p.s, p.tau, p.phi_mode, p.err, p.mirror);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1272,7 +1298,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   // weights P and the denominators, once per destination block
   PArgs pa = {};
   pa.B = p.B; pa.T = p.T; pa.T_pad = L.T_pad; pa.H = p.H; pa.dqk = p.dqk; pa.d_h = d_h; pa.W = p.window;
-  pa.n_iblk = n_iblk; pa.ldp = L.ldp;
+  pa.n_iblk = n_iblk; pa.ldp = L.ldp; pa.mirror = p.mirror;
   pa.s = p.s; pa.tau = p.tau; pa.null_bias = p.null_bias; pa.zb = zb; pa.fq = fq;
   pa.P = P; pa.den = den; pa.err = p.err; pa.timeout_ns = timeout_ns;
   e = d_h == 64 ? launch_p<64>(mq, mk, mfq, mfk, pa, s)
@@ -1303,6 +1329,7 @@ cudaError_t launch_wango_tc(const AggArgs& p, cudaStream_t s) {
   a.debug_timeout = debug ? 1 : 0;
   a.timeout_ns = timeout_ns;
   a.no_norm = p.no_norm;
+  a.mirror = p.mirror;
   a.gbar_out = static_cast<__nv_bfloat16*>(p.gbar_out);
   if (a.nseg > 1) {  // no segment's state is ready yet
     e = cudaMemsetAsync(a.seg_flag, 0, (size_t)a.n_strips * (a.nseg - 1) * sizeof(int), s);
