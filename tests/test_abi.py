@@ -301,3 +301,26 @@ def test_backward_far_scan_workspace(lib):
     kw = dict(B=2, T=300, H=2, d_qk=128, m=512, window=200)
     assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_SCAN, **kw)) == \
         tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_PAIRS, **kw))
+
+
+def test_backward_far_path_choice(lib):
+    """The library's own choice for WANGO's far older pairs (W = 256, the 70M-tier gate
+    width): pair by pair where the band covers most of the sequence (B = 8, T = 2,048:
+    42 far tiles per head against a scan chain of 13 steps on 6 waves), the running-sum
+    scans at long context (T >= 4,096), which is linear in T.  Read from the workspace
+    size, which carries the scans' per-strip sums only when they run."""
+    def path(B, T):
+        kw = dict(B=B, T=T, H=2, d_qk=128, m=28480, window=256)
+        auto = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(**kw))
+        scan = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_SCAN, **kw))
+        pairs = tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_PAIRS, **kw))
+        assert scan > pairs
+        return "scan" if auto == scan else "pairs" if auto == pairs else None
+    assert path(8, 2048) == "pairs"
+    assert path(1, 2048) == "pairs"
+    for B, T in ((1, 4096), (8, 4096), (1, 8192), (1, 16384)):
+        assert path(B, T) == "scan", (B, T)
+    # a window that leaves no block beyond its band: both are the pair path
+    kw = dict(B=1, T=512, H=2, d_qk=128, m=2048, window=512)
+    assert tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(flags=tg.TG_FLAG_BWD_FAR_SCAN, **kw)) == \
+        tg.tg_workspace_size(tg.TG_WS_WANGO_BWD, _agg(**kw))
