@@ -44,6 +44,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+// 16 bytes global -> shared without a register round trip (completes at cp_async_wait)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <typename T>
 struct DecodeArgs {
@@ -65,6 +73,27 @@ __device__ __forceinline__ float phi_of(float u, float inv_sqrt_dh, int mode) {
   const float e1 = u > 0.f ? u + 1.f : expf(u);  // ELU(u) + 1
   if (mode == 1) return e1;
   return fmaxf(e1 + 1e-4f, 1e-4f) * inv_sqrt_dh;
+}
+
+// Two block-wide sums in one pass (red: 16 floats).
+__device__ __forceinline__ void block_sum2(float& x, float& y, float* red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) {
+    red[2 * w] = x;
+    red[2 * w + 1] = y;
+  }
+  __syncthreads();
+  x = 0.f;
+  y = 0.f;
+  for (int k = 0; k < (int)(blockDim.x >> 5); ++k) {
+    x += red[2 * k];
+    y += red[2 * k + 1];
+  }
 }
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -94,7 +123,7 @@ __host__ __device__ __forceinline__ bool fold_step(long long i, int W) {
 // grid (H, B, parts), 256 threads; part p takes ring slots [p * ceil(R / parts), ...).
 template <typename T>
 __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeArgs<T> a) {
-  __shared__ float qh[kMaxDh], kh[kMaxDh], fqs[kMaxDh], red[8];
+  __shared__ float qh[kMaxDh], kh[kMaxDh], fqs[kMaxDh], red[16];
   __shared__ __align__(16) unsigned char kstage[40960];  // a chunk of the ring's keys
   const int head = blockIdx.x, bb = blockIdx.y, part = blockIdx.z, t = threadIdx.x;
   const int d_h = a.d_h, W = a.W, R = a.R;
@@ -103,6 +132,22 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   const int per = (R + gridDim.z - 1) / gridDim.z;
   const int s_lo = min(R, part * per), s_hi = min(R, s_lo + per);
   griddep_launch_dependents();  // the gate kernel may start fetching its rows now
+  // the ring's keys (written by earlier steps) start on their way to shared memory at
+  // once: the first chunk by asynchronous copies when it is 16-byte aligned
+  T* ring_k = static_cast<T*>(a.st.ring_k) + (size_t)bh * R * d_h;
+  T* ks = reinterpret_cast<T*>(kstage);
+  const int chunk = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
+  bool first_async = false;
+  if (s_lo < s_hi) {
+    const T* src = ring_k + (size_t)s_lo * d_h;
+    const size_t bytes = (size_t)min(chunk, s_hi - s_lo) * d_h * sizeof(T);
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && bytes % 16 == 0) {
+      for (size_t x = t; x < bytes / 16; x += blockDim.x)
+        cp_async16(kstage + 16 * x, reinterpret_cast<const uint8_t*>(src) + 16 * x);
+      cp_async_commit();
+      first_async = true;
+    }
+  }
   const float tau = head_tau(a.tau, a.s, head, a.err, kKernWango);
   const float sq = sqrtf(tau), shift = expf(-tau), inv_sqrt_dh = rsqrtf((float)d_h);
   // unit q and k of this head (sec. 2.1)
@@ -121,8 +166,7 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   }
   __syncthreads();
   // the current token's khat into its ring slot (slot i mod R held source i - R, which is
-  // already in the state)
-  T* ring_k = static_cast<T*>(a.st.ring_k) + (size_t)bh * R * d_h;
+  // already in the state; no part uses what its copy reads there)
   const int cur = (int)(i % R);
   const long long lo_win = i - W + 1, first = first_unfolded(i, W);
   if (part == 0 && t < d_h) io<T>::st(ring_k + (size_t)cur * d_h + t, kh[t]);
@@ -131,18 +175,19 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
   // j = s (mod R).  No part reads slot cur from the ring: its weight comes from kh.  The
   // dot products start at column s (mod d_h), so the threads of a warp read different banks.
   float* wv = a.st.w + (size_t)bh * R;
-  T* ks = reinterpret_cast<T*>(kstage);
-  const int chunk = (int)(sizeof(kstage) / ((size_t)d_h * sizeof(T)));  // slots per chunk
   float wsum = 0.f;
   for (int s0 = s_lo; s0 < s_hi; s0 += chunk) {
     const int n = min(chunk, s_hi - s0);
     const T* src = ring_k + (size_t)s0 * d_h;
     const size_t bytes = (size_t)n * d_h * sizeof(T);
-    __syncthreads();  // the previous chunk has been read
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && bytes % 16 == 0) {
+    if (s0 == s_lo && first_async) {
+      cp_async_wait();
+    } else if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && bytes % 16 == 0) {
+      __syncthreads();  // the previous chunk has been read
       for (size_t x = t; x < bytes / 16; x += blockDim.x)
         reinterpret_cast<uint4*>(kstage)[x] = reinterpret_cast<const uint4*>(src)[x];
     } else {
+      __syncthreads();
       for (int x = t; x < n * d_h; x += blockDim.x) ks[x] = src[x];
     }
     __syncthreads();
@@ -170,17 +215,18 @@ __global__ void __launch_bounds__(256) wango_decode_scores_kernel(const DecodeAr
       wsum += w;
     }
   }
-  wsum = block_sum(wsum, red);
-  if (t == 0) a.st.wpart[(size_t)bh * kMaxParts + part] = wsum;
-  if (part != 0) return;
-  // part 0: the older prefix Fq . z; the feature map of the source that leaves the window
-  // after this step (i - W + 1) into its slot of the feature-map ring (slot j mod
-  // kDecodeFold, which no pending source holds now); z' into the other buffer (the sums
-  // alternate between two buffers by step parity): z plus, on a fold step, the group's
-  // feature maps, which the gate kernel also takes for S
+  // the partial sum of the weights, and in part 0 the older prefix Fq . z, in one pass
   const float* z = a.st.z + ((size_t)(i & 1) * a.B * a.H + bh) * d_h;
   float* z_next = a.st.z + ((size_t)((i + 1) & 1) * a.B * a.H + bh) * d_h;
-  const float older = block_sum(t < d_h ? fqs[t] * z[t] : 0.f, red);
+  float older = part == 0 && t < d_h ? fqs[t] * z[t] : 0.f;
+  block_sum2(wsum, older, red);
+  if (t == 0) a.st.wpart[(size_t)bh * kMaxParts + part] = wsum;
+  if (part != 0) return;
+  // part 0: the feature map of the source that leaves the window after this step
+  // (i - W + 1) into its slot of the feature-map ring (slot j mod kDecodeFold, which no
+  // pending source holds now); z' into the other buffer (the sums alternate between two
+  // buffers by step parity): z plus, on a fold step, the group's feature maps, which the
+  // gate kernel also takes for S
   if (t < d_h) {
     float* fkf = a.st.fk_fold + (size_t)bh * kDecodeFold * d_h;
     if (lo_win >= 0) {
