@@ -106,6 +106,14 @@ def peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+def sustained_peak():
+    """The bf16 GEMM rate measured back to back under the power cap, or None."""
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -339,6 +347,10 @@ def main():
                 "kernel": "tango_tc_kernel", "kernel_ms": agg_ms,
                 "algorithmic_flops_per_launch": agg_flops,
                 "peak_source": f"{peak_src} bf16 dense (burst)"}
+    sus = sustained_peak()
+    if sus:  # context: the step runs at the power cap, where the GEMM itself sustains less
+        roofline["sustained_peak"] = sus
+        roofline["frac_of_sustained"] = achieved / sus
 
     # ------------------------------------------------------------------ e2e
     # Every step uploads its input from pinned host memory and reads its result back.
