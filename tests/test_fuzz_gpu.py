@@ -1,0 +1,93 @@
+"""Seeded random configurations against the oracle: the aggregations (both storage types),
+their backward (both far-pair paths of WANGO) and the decode step, over shapes that the
+fixed cases do not pick: 1-4 heads, head widths 16/32/64, gate widths per head from 16 to
+792 (multiples of 8), ragged lengths up to 400 tokens, windows from 1 to past T, score
+scales from 1 to 20, with and without the null gate and v.  The configurations are drawn
+once from a fixed seed, so every run checks the same ones; the bounds are those of the
+fixed-case tests (test_parity_gpu.check, test_backward_gpu.run).  The backward draws run
+up to 700 tokens, so that WANGO's far-pair scans (blocks wholly beyond the window's band)
+take part."""
+import numpy as np
+import pytest
+import torch
+
+import cross_token_gated_gb300 as tg
+import oracle
+from cross_token_gated_gb300 import synth
+from test_backward_gpu import run as run_backward
+from test_parity_gpu import abs_inputs, check, ref_agg_scaled, run_agg, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw(n, seed, backward=False, decode=False):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        H = int(rng.choice([1, 2, 4]))
+        d_h = int(rng.choice([16, 32, 64]))
+        m_h = 8 * int(rng.integers(2, 100 if not backward else 40))
+        B = int(rng.integers(1, 4))
+        T = int(rng.integers(1, 120 if decode else (700 if backward else 400)))
+        if backward:  # mostly WANGO, with windows that leave blocks beyond the band
+            kind = "wango" if rng.random() < 0.7 else "tango"
+            W = int(rng.integers(1, min(T, 200) + 1))
+        else:
+            kind = "wango" if decode else str(rng.choice(["tango", "wango"]))
+            W = int(rng.integers(1, T + 64))
+        out.append(dict(
+            kind=kind, dtype="bf16" if backward else str(rng.choice(["bf16", "f32"])),
+            B=B, T=T, H=H, dqk=H * d_h, m=H * m_h, W=W,
+            s=float(rng.choice([1.0, 4.0, 10.0, 20.0])),
+            null=bool(rng.random() < 0.3) and not decode, has_v=bool(rng.random() < 0.7),
+            phi_mode=int(rng.integers(0, 2)), normalized=bool(rng.random() < 0.3),
+            far=str(rng.choice(["scan", "pairs"])), seed=int(rng.integers(0, 1 << 30))))
+    return out
+
+
+def _id(c):
+    s = "{kind}-{dtype}-B{B}T{T}H{H}dqk{dqk}m{m}".format(**c)
+    if c["kind"] == "wango":
+        s += "W{W}-phi{phi_mode}".format(**c)
+    return s + "-s{s:g}".format(**c) + ("-null" if c["null"] else "") + ("" if c["has_v"] else "-nov")
+
+
+FWD = _draw(16, 20261202)
+BWD = _draw(12, 20261203, backward=True)
+DEC = _draw(6, 20261204, decode=True)
+
+
+@pytest.mark.parametrize("c", FWD, ids=[_id(c) for c in FWD])
+def test_fuzz_aggregation(c):
+    q, k, g, v = synth.agg_inputs(c["B"], c["T"], c["dqk"], c["m"], seed=c["seed"], dtype=c["dtype"])
+    if not c["has_v"]:
+        v = None
+    nb = torch.linspace(-1.5, 0.5, c["H"], dtype=torch.float32) if c["null"] else None
+    kw = dict(s=c["s"])
+    if c["kind"] == "wango":
+        kw["phi_mode"] = c["phi_mode"]
+    gpu_kw = dict(kw, null_bias=nb.cuda() if nb is not None else None)
+    out = run_agg(c["kind"], q, k, g, v, c["H"], c["W"], **gpu_kw)
+    ref_kw = dict(kw, null_bias=nb.double().numpy() if nb is not None else None)
+    ref, scale = ref_agg_scaled(c["kind"], q, k, g, v, c["H"], c["W"], **ref_kw)
+    check(out, ref, c["dtype"], c["H"], scale)
+
+
+@pytest.mark.parametrize("c", BWD, ids=[_id(c) + (f"-{c['far']}" if c["kind"] == "wango" else "") for c in BWD])
+def test_fuzz_backward(c):
+    run_backward(c["kind"], c["B"], c["T"], c["H"], c["dqk"], c["m"], W=c["W"], phi_mode=c["phi_mode"],
+                 null=c["null"], has_v=c["has_v"], normalized=c["normalized"], seed=c["seed"], s=c["s"],
+                 far=c["far"] if c["kind"] == "wango" else None)
+
+
+@pytest.mark.parametrize("c", DEC, ids=[_id(c) for c in DEC])
+def test_fuzz_decode(c):
+    q, k, g, v = synth.agg_inputs(c["B"], c["T"], c["dqk"], c["m"], seed=c["seed"], dtype=c["dtype"])
+    if not c["has_v"]:
+        v = None
+    out = run_decode(q, k, g, v, c["H"], c["W"], s=c["s"], phi_mode=c["phi_mode"])
+    kw = dict(H=c["H"], tau=c["s"], window=c["W"], phi_mode=c["phi_mode"])
+    ref = oracle.wango_scan(*[synth.oracle_view(t) if t is not None else None for t in (q, k, g, v)], **kw)
+    ga, va = abs_inputs(g, v)
+    scale = oracle.wango_scan(*[synth.oracle_view(t) if t is not None else None for t in (q, k, ga, va)], **kw)
+    check(out, ref, c["dtype"], c["H"], scale)
