@@ -6,7 +6,11 @@ scales from 1 to 20, with and without the null gate and v.  The configurations a
 once from a fixed seed, so every run checks the same ones; the bounds are those of the
 fixed-case tests (test_parity_gpu.check, test_backward_gpu.run).  The backward draws run
 up to 700 tokens, so that WANGO's far-pair scans (blocks wholly beyond the window's band)
-take part."""
+take part.  The backward draws keep tau <= 10: at tau = 20 the bf16 rounding of qhat and
+khat moves a logit by up to about tau 2^-8, and an fp64 emulation of the GPU's roundings
+(bf16 qhat, khat, P and E, exact products) of one such draw (B = 2, T = 584, 24 gate
+columns per head, null gate) is itself 2.05 % off normwise and 9.1 % per (row, head) in
+dg, which is where the GPU lands too (2.03 %, 9.3 %)."""
 import numpy as np
 import pytest
 import torch
@@ -38,7 +42,7 @@ def _draw(n, seed, backward=False, decode=False):
         out.append(dict(
             kind=kind, dtype="bf16" if backward else str(rng.choice(["bf16", "f32"])),
             B=B, T=T, H=H, dqk=H * d_h, m=H * m_h, W=W,
-            s=float(rng.choice([1.0, 4.0, 10.0, 20.0])),
+            s=float(rng.choice([1.0, 4.0, 10.0] if backward else [1.0, 4.0, 10.0, 20.0])),
             null=bool(rng.random() < 0.3) and not decode, has_v=bool(rng.random() < 0.7),
             phi_mode=int(rng.integers(0, 2)), normalized=bool(rng.random() < 0.3),
             far=str(rng.choice(["scan", "pairs"])), seed=int(rng.integers(0, 1 << 30))))
