@@ -6,11 +6,13 @@ scales from 1 to 20, with and without the null gate and v.  The configurations a
 once from a fixed seed, so every run checks the same ones; the bounds are those of the
 fixed-case tests (test_parity_gpu.check, test_backward_gpu.run).  The backward draws run
 up to 700 tokens, so that WANGO's far-pair scans (blocks wholly beyond the window's band)
-take part.  The backward draws keep tau <= 10: at tau = 20 the bf16 rounding of qhat and
-khat moves a logit by up to about tau 2^-8, and an fp64 emulation of the GPU's roundings
-(bf16 qhat, khat, P and E, exact products) of one such draw (B = 2, T = 584, 24 gate
-columns per head, null gate) is itself 2.05 % off normwise and 9.1 % per (row, head) in
-dg, which is where the GPU lands too (2.03 %, 9.3 %)."""
+take part.  bf16 draws keep tau <= 10 (fp32 draws go to 20): at tau = 20 the bf16
+rounding of qhat and khat moves a logit by up to about tau 2^-8, and fp64 emulations of
+the GPU's roundings (bf16 qhat, khat, P and E, exact products) land where the GPU does:
+a forward draw (B = 2, T = 143, 4 heads of 290 gates) 1.33 % normwise and 4.46 % per
+(row, head), the same figures to four digits; a backward draw (B = 2, T = 584, 24 gate
+columns per head, null gate) 2.05 % and 9.1 % in dg, against the GPU's 2.03 % and
+9.3 %."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +21,7 @@ import cross_token_gated_gb300 as tg
 import oracle
 from cross_token_gated_gb300 import synth
 from test_backward_gpu import run as run_backward
-from test_parity_gpu import abs_inputs, check, ref_agg_scaled, run_agg, run_decode
+from test_parity_gpu import abs_inputs, check, pitched, ref_agg_scaled, run_agg, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +33,11 @@ def _draw(n, seed, backward=False, decode=False):
         H = int(rng.choice([1, 2, 4]))
         d_h = int(rng.choice([16, 32, 64]))
         m_h = 8 * int(rng.integers(2, 100 if not backward else 40))
+        if not backward and not decode and rng.random() < 0.2:
+            m_h += int(rng.integers(1, 8))  # a head width that is no multiple of 8
+        pad = 0
+        if m_h % 8 or (not backward and not decode and rng.random() < 0.2):
+            pad = (-m_h) % 8 + 8 * int(rng.integers(0, 3))  # a padded per-head pitch
         B = int(rng.integers(1, 4))
         T = int(rng.integers(1, 120 if decode else (700 if backward else 400)))
         if backward:  # mostly WANGO, with windows that leave blocks beyond the band
@@ -39,13 +46,13 @@ def _draw(n, seed, backward=False, decode=False):
         else:
             kind = "wango" if decode else str(rng.choice(["tango", "wango"]))
             W = int(rng.integers(1, T + 64))
+        dtype = "bf16" if backward else str(rng.choice(["bf16", "f32"]))
         out.append(dict(
-            kind=kind, dtype="bf16" if backward else str(rng.choice(["bf16", "f32"])),
-            B=B, T=T, H=H, dqk=H * d_h, m=H * m_h, W=W,
-            s=float(rng.choice([1.0, 4.0, 10.0] if backward else [1.0, 4.0, 10.0, 20.0])),
+            kind=kind, dtype=dtype, B=B, T=T, H=H, dqk=H * d_h, m=H * m_h, W=W,
+            s=float(rng.choice([1.0, 4.0, 10.0] if dtype == "bf16" else [1.0, 4.0, 10.0, 20.0])),
             null=bool(rng.random() < 0.3) and not decode, has_v=bool(rng.random() < 0.7),
             phi_mode=int(rng.integers(0, 2)), normalized=bool(rng.random() < 0.3),
-            far=str(rng.choice(["scan", "pairs"])), seed=int(rng.integers(0, 1 << 30))))
+            far=str(rng.choice(["scan", "pairs"])), pad=pad, seed=int(rng.integers(0, 1 << 30))))
     return out
 
 
@@ -53,28 +60,51 @@ def _id(c):
     s = "{kind}-{dtype}-B{B}T{T}H{H}dqk{dqk}m{m}".format(**c)
     if c["kind"] == "wango":
         s += "W{W}-phi{phi_mode}".format(**c)
-    return s + "-s{s:g}".format(**c) + ("-null" if c["null"] else "") + ("" if c["has_v"] else "-nov")
+    return s + "-s{s:g}".format(**c) + ("-null" if c["null"] else "") + ("" if c["has_v"] else "-nov") + \
+        (f"-pitch{c['m'] // c['H'] + c['pad']}" if c["pad"] else "") + ("-unit" if c["normalized"] else "")
 
 
-FWD = _draw(16, 20261202)
-BWD = _draw(12, 20261203, backward=True)
-DEC = _draw(6, 20261204, decode=True)
+FWD = _draw(40, 20261202)
+BWD = _draw(20, 20261203, backward=True)
+DEC = _draw(12, 20261204, decode=True)
 
 
 @pytest.mark.parametrize("c", FWD, ids=[_id(c) for c in FWD])
 def test_fuzz_aggregation(c):
-    q, k, g, v = synth.agg_inputs(c["B"], c["T"], c["dqk"], c["m"], seed=c["seed"], dtype=c["dtype"])
+    B, T, H, m = c["B"], c["T"], c["H"], c["m"]
+    q, k, g, v = synth.agg_inputs(B, T, c["dqk"], m, seed=c["seed"], dtype=c["dtype"])
+    if c["normalized"]:  # unit vectors per head, rounded to the storage type
+        qf, kf = q.double().view(B, T, H, -1), k.double().view(B, T, H, -1)
+        q = (qf / qf.norm(dim=-1, keepdim=True)).view(B, T, -1).to(q.dtype)
+        k = (kf / kf.norm(dim=-1, keepdim=True)).view(B, T, -1).to(k.dtype)
     if not c["has_v"]:
         v = None
-    nb = torch.linspace(-1.5, 0.5, c["H"], dtype=torch.float32) if c["null"] else None
+    nb = torch.linspace(-1.5, 0.5, H, dtype=torch.float32) if c["null"] else None
     kw = dict(s=c["s"])
     if c["kind"] == "wango":
         kw["phi_mode"] = c["phi_mode"]
-    gpu_kw = dict(kw, null_bias=nb.cuda() if nb is not None else None)
-    out = run_agg(c["kind"], q, k, g, v, c["H"], c["W"], **gpu_kw)
-    ref_kw = dict(kw, null_bias=nb.double().numpy() if nb is not None else None)
-    ref, scale = ref_agg_scaled(c["kind"], q, k, g, v, c["H"], c["W"], **ref_kw)
-    check(out, ref, c["dtype"], c["H"], scale)
+    flags = tg.TG_FLAG_QK_NORMALIZED if c["normalized"] else 0
+    if c["pad"]:  # gates at a padded per-head pitch whose padding holds NaN
+        m_h = m // H
+        pitch = m_h + c["pad"]
+        gp = pitched(g, H, pitch, float("nan")).cuda()
+        vp = pitched(v, H, pitch, float("nan")).cuda() if v is not None else None
+        out = torch.empty_like(gp)
+        nbd = nb.cuda() if nb is not None else None
+        if c["kind"] == "tango":
+            tg.tango_aggregate(q.cuda(), k.cuda(), gp, vp, out, H=H, m_h=m_h, null_bias=nbd, flags=flags, **kw)
+        else:
+            tg.wango_aggregate(q.cuda(), k.cuda(), gp, vp, out, H=H, window=c["W"], m_h=m_h, null_bias=nbd,
+                               flags=flags, **kw)
+        st, word = tg.tg_check_device_error()
+        assert st == tg.TG_OK, (st, hex(word))
+        out = out.view(B, T, H, pitch)[..., :m_h].reshape(B, T, m)
+    else:
+        out = run_agg(c["kind"], q, k, g, v, H, c["W"], flags=flags,
+                      null_bias=nb.cuda() if nb is not None else None, **kw)
+    ref_kw = dict(kw, null_bias=nb.double().numpy() if nb is not None else None, qk_normalized=c["normalized"])
+    ref, scale = ref_agg_scaled(c["kind"], q, k, g, v, H, c["W"], **ref_kw)
+    check(out, ref, c["dtype"], H, scale)
 
 
 @pytest.mark.parametrize("c", BWD, ids=[_id(c) + (f"-{c['far']}" if c["kind"] == "wango" else "") for c in BWD])
