@@ -458,9 +458,10 @@ def kernel_breakdown(f, dev):
     try:
         from torch.profiler import ProfilerActivity, profile
         torch.cuda.synchronize(dev)
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            f()
-            torch.cuda.synchronize(dev)
+        for _ in range(2):  # the first session of a process can come back empty: it warms up
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                f()
+                torch.cuda.synchronize(dev)
         rows = {}
         for ev in prof.key_averages():
             us = getattr(ev, "self_device_time_total", None)
