@@ -327,15 +327,18 @@ BwdWs bwd_ws_layout(const tg_agg_params* p, bool wango) {
 }
 
 // Gradients of L = sum(dout * u) for u = aggregate(q, k, g, v), as laid out in
-// tango.h.  The forward is recomputed (gbar and the denominators), then:
+// tango.h.  The forward is recomputed (gbar and the denominators) unless the caller
+// kept them from a _save call, then:
 //   E = dout * v / den, D = E . gbar, dv = dout * gbar                       (prep)
-//   X, X_old = pair-weight gradients of window and older pairs, then dq, dk from them
-//     (tensor cores; WANGO's older pairs through the forward's feature maps, which are
-//     still in the scratch at that point)
+//   WANGO, when it pays: the older pairs beyond the window's band of blocks through
+//     running-sum scans, reduced over the gate strips (linear in T)
+//   X, X_old = pair-weight gradients of window and older pairs (with the scans, the band
+//     only), then dq, dk from them (tensor cores; WANGO's older pairs through the
+//     forward's feature maps, which are still in the scratch at that point)
 //   dg_j = sum_{i >= j} w_ij E_i: the forward numerator with the roles of destinations
 //     and sources exchanged (TANGO: the tensor-core kernel in reverse mode; WANGO: the
-//     windowed kernel on the time-reversed sequence, whose older-pair weights
-//     e^-tau phi(k~_j) . phi(q~_i) are the same products).
+//     windowed kernels on the time-reversed sequence, read and written mirrored in place,
+//     whose older-pair weights e^-tau phi(k~_j) . phi(q~_i) are the same products).
 tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, const void* k, const void* g,
                              const void* v, const void* dout, const void* saved_gbar, const float* saved_den,
                              void* dq, void* dk, void* dg, void* dv, void* ws, size_t ws_bytes, cudaStream_t stream) {
