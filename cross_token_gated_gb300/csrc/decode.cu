@@ -295,26 +295,6 @@ __device__ __forceinline__ void st_f32x8(float* p, int c0, int lim, const float*
   }
 }
 
-// The 8 columns of a fold group's g rows, kept in the storage type (bf16: one 16-byte
-// vector a row) until they are used.
-template <typename T, bool VEC, int N>
-struct FoldRows {
-  float x[N][kGroup];
-  __device__ __forceinline__ void ld(int u, const T* p, int c0, int lim) { Cols8<T, VEC>::ld(p, c0, lim, x[u]); }
-  __device__ __forceinline__ float get(int u, int e) const { return x[u][e]; }
-};
-template <int N>
-struct FoldRows<__nv_bfloat16, true, N> {
-  uint4 r[N];
-  __device__ __forceinline__ void ld(int u, const __nv_bfloat16* p, int c0, int) {
-    r[u] = *reinterpret_cast<const uint4*>(p + c0);
-  }
-  __device__ __forceinline__ float get(int u, int e) const {
-    const uint32_t w = (e >> 1) == 0 ? r[u].x : (e >> 1) == 1 ? r[u].y : (e >> 1) == 2 ? r[u].z : r[u].w;
-    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
-  }
-};
-
 // grid (ceil(m / C), B), 256 threads.  FOLD: this step completes a group (fold_step).
 // FEW: one or two sequences (launched early, the ring read in batches of 9 slots, three
 // CTAs an SM so that one sequence's 64-column blocks fit in one wave).  Each is a
@@ -331,6 +311,9 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
   constexpr int kB = 9;  // W + 8 slots of W = 256 are 9 a thread at 64 columns
   __shared__ float red[kSl][C + 4];
   __shared__ float inv_den[TG_MAX_HEADS];
+  // a fold step's group of kDecodeFold g rows over this block's columns, staged once and
+  // read by every state row's update
+  __shared__ __align__(16) T fold_g[FOLD ? kDecodeFold : 1][FOLD ? C : kGroup];
   const int bb = blockIdx.y, grp = threadIdx.x % kG, sl = threadIdx.x / kG;
   const int col0 = blockIdx.x * C, d_h = a.d_h, W = a.W, R = a.R, m = a.m;
   const int c0 = col0 + grp * kGroup;  // first of this thread's 8 columns
@@ -350,6 +333,21 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
       r[u] = make_uint4(0, 0, 0, 0);
       if (col_ok && s < R) r[u] = *reinterpret_cast<const uint4*>((s == cur ? gin : ring_g + (size_t)s * m) + c0);
     }
+  }
+  if constexpr (FOLD) {  // the group's rows (written by earlier steps, or this step's input)
+    constexpr int kPer = 16 / (int)sizeof(T);  // elements of a 16-byte chunk
+    for (int e = threadIdx.x; e < kDecodeFold * (C / kPer); e += blockDim.x) {
+      const int u = e / (C / kPer), x = (e % (C / kPer)) * kPer;
+      const long long j = j0 + u;
+      const T* row = j == i ? gin : ring_g + (size_t)(j % R) * m;
+      if (VEC && col0 + x < m) {
+        cp_async16(&fold_g[u][x], row + col0 + x);
+      } else {
+#pragma unroll
+        for (int y = 0; y < kPer; ++y) io<T>::st(&fold_g[u][x + y], col0 + x + y < m ? io<T>::ld(row + col0 + x + y) : 0.f);
+      }
+    }
+    cp_async_commit();
   }
   if (FEW && col_ok) {  // this thread's state rows (and any further ring rows) into L2
     for (int s = sl + (kPre ? kB * kSl : 0); s < R; s += kSl)
@@ -372,6 +370,10 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
     const int bh = bb * a.H + (int)threadIdx.x;
     for (int p = 0; p < parts; ++p) wsum += a.st.wpart[(size_t)bh * kMaxParts + p];
     older = a.st.older[bh];
+  }
+  if constexpr (FOLD) {
+    cp_async_wait();
+    __syncthreads();
   }
   float acc[kGroup];
 #pragma unroll
@@ -427,19 +429,9 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
       }
     }
     // older prefix: rows sl, sl + kSl, ... of S read out, and on a fold step updated by the
-    // group of kDecodeFold sources that completes now
+    // group of kDecodeFold sources that completes now (its g rows from shared memory)
 #pragma unroll 1
     for (int d = sl; d < d_h; d += kSl) {
-      // a fold step's group of g rows (8 columns each), read again for every state row
-      // (from L2): holding them across the loop would cost the other steps' occupancy
-      FoldRows<T, VEC, FOLD ? kDecodeFold : 1> gf;
-      if constexpr (FOLD) {
-#pragma unroll
-        for (int u = 0; u < kDecodeFold; ++u) {
-          const long long j = j0 + u;
-          gf.ld(u, j == i ? gin : ring_g + (size_t)(j % R) * m, c0, lim);
-        }
-      }
       if (VEC) {
         const size_t bh = (size_t)bb * a.H + head0;
         float* Srow = a.st.S + (bh * d_h + d) * a.m_h;
@@ -451,11 +443,13 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
         for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(fq, sv[e], acc[e]);
         if constexpr (FOLD) {
           const float* fkf = a.st.fk_fold + bh * kDecodeFold * d_h + d;
-#pragma unroll
+#pragma unroll 2
           for (int u = 0; u < kDecodeFold; ++u) {
             const float fk = fkf[u * d_h];
+            float x[kGroup];
+            Cols8<T, true>::ld(&fold_g[u][0], grp * kGroup, C, x);
 #pragma unroll
-            for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, gf.get(u, e), sv[e]);
+            for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, x[e], sv[e]);
           }
           st_f32x8<true>(Srow, cl, a.m_h, sv);
         }
@@ -472,7 +466,7 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
           if constexpr (FOLD) {
 #pragma unroll
             for (int u = 0; u < kDecodeFold; ++u)
-              sv = fmaf(a.st.fk_fold[(bh * kDecodeFold + u) * d_h + d], gf.get(u, e), sv);
+              sv = fmaf(a.st.fk_fold[(bh * kDecodeFold + u) * d_h + d], io<T>::ld(&fold_g[u][grp * kGroup + e]), sv);
             *sp = sv;
           }
         }
