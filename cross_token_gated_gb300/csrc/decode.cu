@@ -429,31 +429,55 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
       }
     }
     // older prefix: rows sl, sl + kSl, ... of S read out, and on a fold step updated by the
-    // group of kDecodeFold sources that completes now (its g rows from shared memory)
+    // group of kDecodeFold sources that completes now (its g rows from shared memory).
+    // With 16-byte vectors a thread has kSB of its state rows in flight at once (all loads
+    // first, then the read-out, the update and the stores): 4 in the plain launches that
+    // leave registers for them, 2 in the early launches for one or two sequences (whose
+    // rows are already on their way to L2, and whose chain after the wait is the step's).
+    if (VEC) {
+      constexpr int kSB = FEW ? 2 : (kPre ? 4 : 1);
+      const size_t bh = (size_t)bb * a.H + head0;
+      const int cl = c0 - head0 * a.m_h;
 #pragma unroll 1
-    for (int d = sl; d < d_h; d += kSl) {
-      if (VEC) {
-        const size_t bh = (size_t)bb * a.H + head0;
-        float* Srow = a.st.S + (bh * d_h + d) * a.m_h;
-        const int cl = c0 - head0 * a.m_h;
-        float sv[kGroup];
-        ld_f32x8<true>(Srow, cl, a.m_h, sv);
-        const float fq = a.st.fq[bh * d_h + d];
+      for (int d0 = sl; d0 < d_h; d0 += kSB * kSl) {
+        float sv[kSB][kGroup], fq[kSB];
 #pragma unroll
-        for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(fq, sv[e], acc[e]);
-        if constexpr (FOLD) {
-          const float* fkf = a.st.fk_fold + bh * kDecodeFold * d_h + d;
-#pragma unroll 2
-          for (int u = 0; u < kDecodeFold; ++u) {
-            const float fk = fkf[u * d_h];
-            float x[kGroup];
-            Cols8<T, true>::ld(&fold_g[u][0], grp * kGroup, C, x);
+        for (int b = 0; b < kSB; ++b) {
+          const int d = d0 + b * kSl;
+          fq[b] = 0.f;
+          if (d < d_h) {
+            ld_f32x8<true>(a.st.S + (bh * d_h + d) * a.m_h, cl, a.m_h, sv[b]);
+            fq[b] = a.st.fq[bh * d_h + d];
+          } else {
 #pragma unroll
-            for (int e = 0; e < kGroup; ++e) sv[e] = fmaf(fk, x[e], sv[e]);
+            for (int e = 0; e < kGroup; ++e) sv[b][e] = 0.f;
           }
-          st_f32x8<true>(Srow, cl, a.m_h, sv);
         }
-      } else {
+#pragma unroll
+        for (int b = 0; b < kSB; ++b)
+#pragma unroll
+          for (int e = 0; e < kGroup; ++e) acc[e] = fmaf(fq[b], sv[b][e], acc[e]);
+        if constexpr (FOLD) {
+#pragma unroll
+          for (int b = 0; b < kSB; ++b) {
+            const int d = d0 + b * kSl;
+            if (d >= d_h) break;
+            const float* fkf = a.st.fk_fold + bh * kDecodeFold * d_h + d;
+#pragma unroll 2
+            for (int u = 0; u < kDecodeFold; ++u) {
+              const float fk = fkf[u * d_h];
+              float x[kGroup];
+              Cols8<T, true>::ld(&fold_g[u][0], grp * kGroup, C, x);
+#pragma unroll
+              for (int e = 0; e < kGroup; ++e) sv[b][e] = fmaf(fk, x[e], sv[b][e]);
+            }
+            st_f32x8<true>(a.st.S + (bh * d_h + d) * a.m_h, cl, a.m_h, sv[b]);
+          }
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int d = sl; d < d_h; d += kSl) {
 #pragma unroll
         for (int e = 0; e < kGroup; ++e) {
           const int c = c0 + e;

@@ -549,6 +549,8 @@ def run_decode(q, k, g, v, H, W, **kw):
     ("bf16", (1, 700, 2, 64, 512, 600)),
     ("bf16", (4, 60, 2, 64, 512, 16)),     # four sequences: the plain launch
     ("bf16", (3, 50, 2, 64, 256, 41)),     # the last group of 8 still waiting at the end
+    ("f32", (3, 60, 2, 64, 256, 20)),      # three sequences in fp32: the plain launch's vectors
+    ("bf16", (4, 80, 1, 128, 512, 30)),    # one head of 128: two batches of 4 state rows a thread
 ])
 def test_decode_steps_match_the_whole_sequence(dtype, case):
     """T decode steps reproduce every row of WANGO over the whole sequence (the oracle's
