@@ -676,21 +676,24 @@ def test_tango_matches_its_rounding_points(case):
     assert stats["differ"] <= 5e-3 and stats["norm"] <= 2.0 ** -9, stats
 
 
-@pytest.mark.parametrize("case", [(1, 300, 2, 128, 1040, 16), (1, 300, 2, 128, 1040, 100),
-                                  (2, 520, 2, 64, 272, 256), (1, 700, 2, 128, 272, 200)])
-def test_wango_matches_its_rounding_points(case):
+@pytest.mark.parametrize("case,null", [((1, 300, 2, 128, 1040, 16), False), ((1, 300, 2, 128, 1040, 100), False),
+                                       ((2, 520, 2, 64, 272, 256), False), ((1, 700, 2, 128, 272, 200), False),
+                                       ((1, 600, 4, 64, 128, 300), True)])  # d_h = 16, null gate
+def test_wango_matches_its_rounding_points(case, null):
     """The bf16 WANGO path against an fp64 emulation of the rounding points its kernels
     document: Fq = bf16(e^-tau phi(sqrt(tau) qhat)) and Fk = bf16(phi(sqrt(tau) khat))
     from bf16 unit vectors; for destination block ib the source blocks jlo(ib)..ib give
     bf16 weights (window pairs exp(tau (qhat.khat - 1)), older pairs Fq.Fk, zero after
     the row), every older block through the state S = sum Fk g^T read out as Fq .
     bf16(S); the denominator sums the rounded weights, Fq . z (z the sums of the rounded
-    Fk below the window) and nothing else; gbar and u rounded to bf16.  Compared in bf16
-    steps of the output, like the TANGO case."""
+    Fk below the window) and, with the null gate, (i + 1) e^(b - tau); gbar and u rounded
+    to bf16.  Compared in bf16 steps of the output, like the TANGO case."""
     B, T, H, dqk, m, W = case
     s = 10.0
     q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=B * T + m + W, dtype="bf16")
-    out = run_agg("wango", q, k, g, v, H, W, s=s)
+    nb = np.linspace(-1.0, 0.5, H) if null else np.full(H, -np.inf)
+    out = run_agg("wango", q, k, g, v, H, W, s=s,
+                  null_bias=torch.tensor(nb, dtype=torch.float32).cuda() if null else None)
     qv, kv, gv, vv = (_widen(synth.oracle_view(t)) for t in (q, k, g, v))
     d_h, m_h = dqk // H, m // H
     nblk = -(-T // 128)
@@ -720,7 +723,7 @@ def test_wango_matches_its_rounding_points(case):
                 S = _bf16(fk[:j0].T @ ga[:j0])           # the state before the block, as read out
                 z = zb[:jlo].sum(0)
                 num = P @ ga[j0:i1] + fq[i0:i1] @ S
-                den = P.sum(1) + fq[i0:i1] @ z
+                den = P.sum(1) + fq[i0:i1] @ z + (np.arange(i0, i1) + 1.0) * np.exp(nb[a] - s)
                 emu[b, i0:i1, a * m_h:(a + 1) * m_h] = _bf16(_bf16(num / den[:, None]) * va[i0:i1])
 
     def key(t):
