@@ -16,8 +16,8 @@ the GPU reads: bf16 inputs are widened, not re-rounded):
   that scale, so this bound holds element by element, even where the output is near
   zero through cancellation.  In bf16 the weights carry the rounding of qhat, khat (a
   logit error of up to tau 2^-8) and of P (2^-9).
-The element-wise ratio of the survey's tolerance note, |gpu - oracle| / (|oracle| +
-1e-3 rms(oracle)), is computed and reported (TG_PARITY_REPORT) but not bounded: an
+The plain element-wise ratio |gpu - oracle| / (|oracle| + 1e-3 rms(oracle)) is
+computed and reported (TG_PARITY_REPORT) but not bounded: an
 output element that cancels to near zero keeps the absolute error of the weights, and
 the ratio then measures the cancellation, not the kernel.  With TG_PARITY_REPORT=<path>
 every check appends its figures as one JSON line to that file.
@@ -52,7 +52,7 @@ def rel_err(gpu: torch.Tensor, ref: np.ndarray) -> float:
 
 
 def errors(gpu: torch.Tensor, ref: np.ndarray, H: int = 1, scale=None) -> dict:
-    """Normwise, worst per-(row, head), survey element-wise and (with `scale`)
+    """Normwise, worst per-(row, head), plain element-wise and (with `scale`)
     condition-normalised element-wise errors.  Rows are the last axis; H splits it into
     heads of equal width."""
     g = as_f64(gpu, ref.shape)
