@@ -432,10 +432,11 @@ __global__ void __launch_bounds__(256, (VEC && sizeof(T) == 2) || FEW ? 3 : 6)
     // group of kDecodeFold sources that completes now (its g rows from shared memory).
     // With 16-byte vectors a thread has kSB of its state rows in flight at once (all loads
     // first, then the read-out, the update and the stores): 4 in the plain launches that
-    // leave registers for them, 2 in the early launches for one or two sequences (whose
-    // rows are already on their way to L2, and whose chain after the wait is the step's).
+    // leave registers for them, 2 on their fold steps (which also store the rows) and in
+    // the early launches for one or two sequences (whose rows are already on their way to
+    // L2, and whose chain after the wait is the step's).
     if (VEC) {
-      constexpr int kSB = FEW ? 2 : (kPre ? 4 : 1);
+      constexpr int kSB = FEW ? 2 : (kPre ? (FOLD ? 2 : 4) : 1);
       const size_t bh = (size_t)bb * a.H + head0;
       const int cl = c0 - head0 * a.m_h;
 #pragma unroll 1
