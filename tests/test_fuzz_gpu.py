@@ -12,7 +12,9 @@ the GPU's roundings (bf16 qhat, khat, P and E, exact products) land where the GP
 a forward draw (B = 2, T = 143, 4 heads of 290 gates) 1.33 % normwise and 4.46 % per
 (row, head), the same figures to four digits; a backward draw (B = 2, T = 584, 24 gate
 columns per head, null gate) 2.05 % and 9.1 % in dg, against the GPU's 2.03 % and
-9.3 %."""
+9.3 %.  Ten longer backward draws (700-2,500 tokens, windows up to 600; the library's
+choice of far-pair path, or one of the two forced) put many blocks beyond the window's
+band."""
 import numpy as np
 import pytest
 import torch
@@ -64,8 +66,28 @@ def _id(c):
         (f"-pitch{c['m'] // c['H'] + c['pad']}" if c["pad"] else "") + ("-unit" if c["normalized"] else "")
 
 
+def _draw_long(n, seed):
+    """Backward draws over 700-2,500 tokens: WANGO's older pairs then reach far beyond the
+    window's band of blocks."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        H = int(rng.choice([1, 2, 4]))
+        d_h = int(rng.choice([16, 32, 64]))
+        m_h = 8 * int(rng.integers(2, 48))
+        B = int(rng.integers(1, 3))
+        T = int(rng.integers(700, 2500))
+        W = int(rng.integers(1, 600))
+        out.append(dict(kind="wango" if rng.random() < 0.8 else "tango", dtype="bf16", B=B, T=T, H=H,
+                        dqk=H * d_h, m=H * m_h, W=W, s=float(rng.choice([1.0, 4.0, 10.0])),
+                        null=bool(rng.random() < 0.3), has_v=bool(rng.random() < 0.7),
+                        phi_mode=int(rng.integers(0, 2)), normalized=bool(rng.random() < 0.3),
+                        far=str(rng.choice(["scan", "pairs", "auto"])), pad=0, seed=int(rng.integers(0, 1 << 30))))
+    return out
+
+
 FWD = _draw(40, 20261202)
-BWD = _draw(20, 20261203, backward=True)
+BWD = _draw(20, 20261203, backward=True) + _draw_long(10, 888004)
 DEC = _draw(12, 20261204, decode=True)
 
 
@@ -109,9 +131,10 @@ def test_fuzz_aggregation(c):
 
 @pytest.mark.parametrize("c", BWD, ids=[_id(c) + (f"-{c['far']}" if c["kind"] == "wango" else "") for c in BWD])
 def test_fuzz_backward(c):
+    far = c["far"] if c["kind"] == "wango" and c["far"] != "auto" else None
     run_backward(c["kind"], c["B"], c["T"], c["H"], c["dqk"], c["m"], W=c["W"], phi_mode=c["phi_mode"],
                  null=c["null"], has_v=c["has_v"], normalized=c["normalized"], seed=c["seed"], s=c["s"],
-                 far=c["far"] if c["kind"] == "wango" else None)
+                 far=far)
 
 
 @pytest.mark.parametrize("c", DEC, ids=[_id(c) for c in DEC])
