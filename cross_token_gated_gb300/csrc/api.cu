@@ -282,7 +282,8 @@ tg_status aggregate(bool wango, const tg_agg_params* p, const void* q, const voi
 // ---- aggregation backward (bf16, tensor cores)
 tg_status validate_bwd(const tg_agg_params* p, bool wango) {
   const unsigned far_flags = TG_FLAG_BWD_FAR_SCAN | TG_FLAG_BWD_FAR_PAIRS;
-  if (p->flags & ~(TG_FLAG_QK_NORMALIZED | (wango ? far_flags : 0u))) return TG_ERR_INVALID_ARG;
+  if (p->flags & ~(TG_FLAG_QK_NORMALIZED | TG_FLAG_DEBUG_TIMEOUT | (wango ? far_flags : 0u)))
+    return TG_ERR_INVALID_ARG;
   tg_agg_params shape = *p;  // the forward's checks, without the backward-only flags
   shape.flags &= ~far_flags;
   tg_status st = validate_agg(&shape, wango);
@@ -411,6 +412,10 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   pa.X = base + L.X;
   pa.X_old = wango ? base + L.Xo : nullptr;
   pa.err = err;
+  // TG_FLAG_DEBUG_TIMEOUT arms the test hook of the backward's own tensor-core kernels
+  // (pairs, scans, dq/dk) only; the forward kernels it also runs get no flags
+  const int hook = (p->flags & TG_FLAG_DEBUG_TIMEOUT) ? 1 : 0;
+  pa.debug_timeout = hook;
   const size_t part_half = L.scan ? (size_t)bwd_scan_strips(p->B, p->H, p->m / p->H) * p->B * p->T * p->d_qk : 0;
   float* part = reinterpret_cast<float*>(base + L.part);
   if (L.scan) {  // the far older pairs through the running sums; the pair kernel keeps the band
@@ -428,6 +433,7 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
     sa.rb = reinterpret_cast<float*>(base + L.rb);
     sa.fb = sa.rb + (size_t)p->B * p->H * (L.T_pad / 128) * (p->d_qk / p->H);
     sa.err = err;
+    sa.debug_timeout = hook;
     e = launch_bwd_scan(sa, stream);
     if (e != cudaSuccess) return TG_ERR_CUDA;
   }
@@ -443,6 +449,7 @@ tg_status aggregate_backward(bool wango, const tg_agg_params* p, const void* q, 
   qa.raw_q = norm ? q : nullptr;
   qa.raw_k = norm ? k : nullptr;
   qa.dq = dq; qa.dk = dk; qa.err = err;
+  qa.debug_timeout = hook;
   if (L.scan) {
     qa.band = bwd_band(p->window);
     qa.far[0] = part;

@@ -52,7 +52,7 @@ constexpr int kEpiWarp0 = 2;
 
 struct __align__(8) Bars {
   uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
-  uint64_t key_full, key_empty, drain;
+  uint64_t key_full, key_empty, drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -74,6 +74,7 @@ struct Args {
   int band;                   // >= 0: only source blocks jb >= ib - band
   unsigned* err;
   uint64_t timeout_ns;
+  int debug_timeout;          // test hook: the MMA issuer first waits on a barrier nothing signals
 };
 
 struct Tile {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&b.key_full, 1);
     mbar_init(&b.key_empty, 8);
     mbar_init(&b.drain, 1);
+    mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
-    bool ok = true;
+    bool ok = !a.debug_timeout || wait_bar(&b.never, 0, b, a);  // nothing ever arrives there
     for (int t = blockIdx.x; ok && t < a.n_tiles; t += gridDim.x) {
       if (!(ok = wait_bar(&b.acc_empty[acc], acc_phase ^ 1, b, a))) break;
       tc_fence_after();
@@ -364,7 +366,7 @@ constexpr uint32_t kXBytes = 2 * kXBox;        // 32 KB: a 128 x 128 block
 constexpr uint32_t kVBytes = 128 * 64 * 2;     // 16 KB: 128 vectors, 64 columns
 constexpr uint32_t kStageBytes = 2 * kXBytes + 2 * kVBytes;  // X, X_old, unit vectors, feature maps
 struct __align__(8) Bars {
-  uint64_t full[kStages], empty[kStages], acc_full, drain;
+  uint64_t full[kStages], empty[kStages], acc_full, drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -382,6 +384,7 @@ struct Args {
   const float* far[2];
   unsigned* err;
   uint64_t timeout_ns;
+  int debug_timeout;          // test hook: the MMA issuer first waits on a barrier nothing signals
 };
 
 __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
@@ -459,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.drain, 1);
+    mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
@@ -509,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc = idesc_bf16_f32(128, 64, tr, true);
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true, first_w = true, first_o = true;
+    bool ok = !a.debug_timeout || wait_bar(&b.never, 0, b, a), first_w = true, first_o = true;
     for (int p = 0; ok && p < it.n_steps; ++p) {
       int ib, jb;
       bool hw, ho;
@@ -677,7 +681,7 @@ struct __align__(8) Bars {
   uint64_t st_full;                        // the update's MMAs are done
   uint64_t sb_full, sb_empty;              // the bf16 state copy / its last reader is done
   uint64_t y_full, y_empty;
-  uint64_t drain;
+  uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -690,6 +694,7 @@ struct Args {
   float* part[2];   // [n_strips, B * T, H, d_h] per direction
   unsigned* err;
   uint64_t timeout_ns;
+  int debug_timeout;  // test hook: the MMA issuer first waits on a barrier nothing signals
 };
 
 __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, Bars& b, const Args& a) {
@@ -749,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&b.y_full, 1);
     mbar_init(&b.y_empty, 4);
     mbar_init(&b.drain, 1);
+    mbar_init(&b.never, 1);
     b.abort = 0;
     fence_mbar_init();
   }
@@ -770,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int mask = 0;
     uint32_t sph[kStages] = {0, 0, 0, 0};
+    int vlast = -1;  // the step of the last vector tile issued
     bool ok = true;
     for (int s = 0; ok && s < a.n_act; ++s) {
       int ub, cb;
@@ -778,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bar(&b.vec_empty, (s & 1) ^ 1, b, a))) break;
       mbar_arrive_expect_tx(&b.vec_full, kBox);
       tma_load_3d(sVec, vec_map, &b.vec_full, head * a.d_h, ub * 128, bb);
+      vlast = s;
       for (int q = 0; ok && q < nchunk; ++q) {
         if (!(ok = wait_bar(&b.empty[stage], phase ^ 1, b, a))) break;
         mbar_arrive_expect_tx(&b.full[stage], kStage);
@@ -800,16 +808,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
     }
+    // copies still in flight land before the CTA exits (also when the loop was cut short)
     for (int s = 0; s < kStages; ++s)
       if (mask & (1 << s)) mbar_wait(&b.full[s], sph[s], a.timeout_ns);
-    if (a.n_act > 0) mbar_wait(&b.vec_full, (a.n_act - 1) & 1, a.timeout_ns);
+    if (vlast >= 0) mbar_wait(&b.vec_full, vlast & 1, a.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issue
     const uint32_t idesc_u = idesc_bf16_f32(128, 64, true, true);    // S^T (+)= A^T V
     const uint32_t idesc_c = idesc_bf16_f32(128, 64, false, true);   // Y = A S
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
+    bool ok = !a.debug_timeout || wait_bar(&b.never, 0, b, a);  // nothing ever arrives there
     for (int s = 0; ok && s < a.n_act; ++s) {
       // the update: S^T[c, d] += sum_t A[t, c] V[t, d], chunk q of 128 columns; the previous
       // state copy has been read out (sb_full of step s - 1 was waited for below)
@@ -1090,7 +1099,8 @@ cudaError_t launch_bwd_scan(const BwdScanArgs& p, cudaStream_t s) {
   a.part[0] = p.part[0];
   a.part[1] = p.part[1];
   a.err = p.err;
-  a.timeout_ns = 2000000000ull;
+  a.debug_timeout = p.debug_timeout;
+  a.timeout_ns = p.debug_timeout ? 1000000ull : 2000000000ull;
   if (a.n_act <= 0) return cudaSuccess;  // no block is wholly beyond the band
   // the block sums of D_i Fq_i for rho
   bwd_rho_kernel<<<dim3(a.nblk, p.H, p.B), 128, 0, s>>>(static_cast<const __nv_bfloat16*>(p.fq), p.dp, p.rb, p.T,
@@ -1143,7 +1153,8 @@ cudaError_t launch_bwd_qk_tc(const BwdQKTcArgs& p, cudaStream_t s) {
   a.far[0] = p.far[0];
   a.far[1] = p.far[1];
   a.err = p.err;
-  a.timeout_ns = 2000000000ull;
+  a.debug_timeout = p.debug_timeout;
+  a.timeout_ns = p.debug_timeout ? 1000000ull : 2000000000ull;
   const long long items = 2LL * a.n_bh * a.nblk;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   CUtensorMap mX, mXo, mQ, mK, mFq, mFk;
@@ -1185,7 +1196,8 @@ cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& p, cudaStream_t s) {
   a.X = static_cast<__nv_bfloat16*>(p.X);
   a.X_old = static_cast<__nv_bfloat16*>(p.X_old);
   a.err = p.err;
-  a.timeout_ns = 2000000000ull;
+  a.debug_timeout = p.debug_timeout;
+  a.timeout_ns = p.debug_timeout ? 1000000ull : 2000000000ull;
   CUtensorMap mE, mG, mK;
   cudaError_t e = make_tmap_4d_heads(&mE, p.E, p.B, p.T, p.H, m_h, m_hp, BM, BK);
   if (e == cudaSuccess) e = make_tmap_4d_heads(&mG, p.g, p.B, p.T, p.H, m_h, m_hp, BN, BK);

@@ -46,6 +46,7 @@ struct BwdPairsArgs {
   int band = -1;     // WANGO with the far older pairs left to the scans: only source blocks
                      // jb >= ib - band of destination block ib (band = ceil((W - 1) / 128))
   unsigned* err;
+  int debug_timeout = 0;  // test hook: the MMA issuer waits on a barrier nothing signals (1 ms)
 };
 cudaError_t launch_bwd_pairs_tc(const BwdPairsArgs& a, cudaStream_t s);
 // WANGO: the far older pairs' feature-map gradients through running sums (backward_tc.cu).
@@ -68,6 +69,7 @@ struct BwdScanArgs {
   float* rb;
   float* fb;
   unsigned* err;
+  int debug_timeout = 0;  // test hook: the MMA issuer waits on a barrier nothing signals (1 ms)
 };
 // Strips of the scans (of bwd_scan_ns columns each) for B * H sequence-heads of m_h gates.
 int bwd_scan_strips(int B, int H, int m_h);
@@ -100,6 +102,7 @@ struct BwdQKTcArgs {
   int band = -1;
   const float* far[2] = {nullptr, nullptr};
   unsigned* err;
+  int debug_timeout = 0;  // test hook: the MMA issuer waits on a barrier nothing signals (1 ms)
 };
 cudaError_t launch_bwd_qk_tc(const BwdQKTcArgs& a, cudaStream_t s);
 // Destination rows padded to whole 128-row blocks.

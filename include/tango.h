@@ -70,7 +70,9 @@ typedef enum { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
                                         TG_ERR_TIMEOUT through tg_check_device_error().
                                         tango_aggregate: the TANGO kernel; wango_aggregate:
                                         the gate-strip kernel; tango_block_forward: the
-                                        projection GEMM */
+                                        projection GEMM; tango/wango_aggregate_backward:
+                                        the pair-gradient, dq/dk and running-sum scan
+                                        kernels (the outputs are then undefined) */
 #define TG_FLAG_FUSED_V 0x200u       /* tango_block_forward, WANGO mode, bf16: v = W_v x is
                                         formed inside the aggregation kernel instead of by
                                         the projection GEMM (v is then never stored); see

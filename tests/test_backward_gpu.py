@@ -352,3 +352,27 @@ def test_backward_full_size_sampled_rows(kind, far):
         assert e["norm"] <= TOL, (name, e)
         if name in ("dg", "dv"):
             assert e["row_head"] <= 2 * TOL, (name, e)
+
+
+@pytest.mark.parametrize("kind,far", [("tango", None), ("wango", "scan"), ("wango", "pairs")])
+def test_backward_bounded_wait_timeout_reports_status(kind, far):
+    """TG_FLAG_DEBUG_TIMEOUT arms the hook of the backward's own tensor-core kernels (the
+    pair gradients, dq/dk and, on the scan path, the running-sum scans): each MMA issuer
+    first waits on a barrier that nothing signals, runs out (1 ms), records a timeout
+    (kernel code 5) and every role leaves its loops.  The forward kernels that the call
+    also runs get no flag.  The context stays usable: the next call is correct."""
+    B, T, H, dqk, m, W = 1, 700, 2, 128, 512, 16  # W = 16: blocks beyond the band, so scans
+    q, k, g, v = synth.agg_inputs(B, T, dqk, m, seed=31, dtype="bf16")
+    dout = synth.upstream_grad(B, T, m, seed=131)
+    dev = [t.cuda() for t in (q, k, g, v, dout)]
+    dq, dk, dg, dv = (torch.empty_like(dev[i]) for i in (0, 1, 2, 2))
+    flags = tg.TG_FLAG_DEBUG_TIMEOUT | FAR_FLAGS[far]
+    if kind == "tango":
+        tg.tango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, flags=flags)
+    else:
+        tg.wango_aggregate_backward(*dev, dq, dk, dg, dv, H=H, window=W, flags=flags)
+    st, word = tg.tg_check_device_error()
+    assert st == tg.TG_ERR_TIMEOUT
+    assert word & 1 and (word >> 8) & 0xFF == 5, hex(word)
+    assert tg.tg_check_device_error() == (tg.TG_OK, 0)
+    run(kind, B, T, H, dqk, m, W=W, seed=31, far=far)
